@@ -1,0 +1,105 @@
+"""Seeded synthetic inputs for the GMA forward pass, shared by the tests, the benchmark and the
+smoke check.  This module only draws random numbers and names workloads; it holds none of the
+method's arithmetic, and it serves the CUDA library and the oracle alike.
+
+Recipe (the page's own workloads are WikiText-103 language modelling and Long-Range Arena
+classification; their datasets are not used -- tensors of the same shapes stand in for them):
+
+* one ``torch.Generator('cpu')`` seeded per workload;
+* draw order, all fp32: Q_X, K_X, V, mu, raw variance, prior logits;
+* Q_X, K_X ~ N(0, 1); V ~ N(0, 1) or U(-1, 1); mu ~ N(0, mu_std); raw ~ N(0, raw_std);
+  prior logits ~ N(0, 1)  (N(0, s) names the standard deviation s);
+* activations are then rounded to bf16 (round-to-nearest-even) for bf16 workloads; the GMM
+  parameters stay fp32.
+"""
+from dataclasses import dataclass, field, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    causal: bool
+    B: int
+    H: int
+    N: int
+    d_r: int
+    K: int
+    d_v: int
+    dtype: str = "bf16"          # "bf16" or "f32": the activation / output type
+    seed: int = 0
+    v_dist: str = "normal"       # "normal": N(0,1); "uniform": U(-1,1)
+    mu_std: float = 1.0
+    raw_std: float = 0.5
+    logit_std: float = 1.0
+    eps: float = 1e-6
+    var_floor: float = 1e-3
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.N
+
+    @property
+    def token_heads(self) -> int:
+        return self.B * self.H * self.N
+
+
+def _ws(name, causal, B, H, N, d_r, K, d_v, **kw):
+    return Workload(name, causal, B, H, N, d_r, K, d_v, **kw)
+
+
+# The five benchmark workloads.  Names say what they are; sizes are in the names and fields.
+TINY_BIDIR_F32 = _ws("bidir_f32_b1h1_n256_dr16_k8_dv32", False, 1, 1, 256, 16, 8, 32,
+                     dtype="f32", seed=0)
+LM_CAUSAL = _ws("causal_bf16_b4h8_n2048_dr64_k64_dv64", True, 4, 8, 2048, 64, 64, 64, seed=1)
+LRA_BIDIR = _ws("bidir_bf16_b32h8_n4096_dr32_k32_dv64", False, 32, 8, 4096, 32, 32, 64, seed=2,
+                v_dist="uniform", mu_std=1.5)
+LONG_CAUSAL = _ws("causal_bf16_b1h16_n65536_dr64_k128_dv128", True, 1, 16, 65536, 64, 128, 128,
+                  seed=3)
+K_SWEEP = tuple(_ws(f"causal_bf16_b2h16_n16384_dr64_k{k}_dv128", True, 2, 16, 16384, 64, k, 128,
+                    seed=4) for k in (16, 64, 256, 1024))
+N_SWEEP = tuple(_ws(f"causal_bf16_b2h16_n{n}_dr64_k64_dv128", True, 2, 16, n, 64, 64, 128,
+                    seed=4) for n in (4096, 8192, 16384, 32768, 65536, 131072))
+
+ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP
+
+
+def by_name(name: str) -> Workload:
+    for w in ALL_WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def scaled(w: Workload, **changes) -> Workload:
+    """The same recipe with some sizes changed (smaller parity cases)."""
+    return replace(w, name=w.name + "_scaled", **changes)
+
+
+def make_inputs(w: Workload):
+    """Draw one workload's inputs on the CPU.
+
+    Returns a dict of CPU tensors: QX, KX [B,H,N,d_r], V [B,H,N,d_v] (bf16 or fp32),
+    mu, raw [H,K,d_r] fp32, logits [H,K] fp32.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed))
+    B, H, N, d_r, K, d_v = w.B, w.H, w.N, w.d_r, w.K, w.d_v
+    QX = torch.randn(B, H, N, d_r, generator=g, dtype=torch.float32)
+    KX = torch.randn(B, H, N, d_r, generator=g, dtype=torch.float32)
+    if w.v_dist == "uniform":
+        V = torch.rand(B, H, N, d_v, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    else:
+        V = torch.randn(B, H, N, d_v, generator=g, dtype=torch.float32)
+    mu = torch.randn(H, K, d_r, generator=g, dtype=torch.float32) * w.mu_std
+    raw = torch.randn(H, K, d_r, generator=g, dtype=torch.float32) * w.raw_std
+    logits = torch.randn(H, K, generator=g, dtype=torch.float32) * w.logit_std
+    if w.dtype == "bf16":
+        QX, KX, V = QX.to(torch.bfloat16), KX.to(torch.bfloat16), V.to(torch.bfloat16)
+    return {"QX": QX, "KX": KX, "V": V, "mu": mu, "raw": raw, "logits": logits}
+
+
+def to_numpy(inputs):
+    """fp32 numpy views of an input dict (bf16 widens to fp32 exactly)."""
+    return {k: v.float().numpy() for k, v in inputs.items()}

@@ -1,0 +1,100 @@
+"""fp64 CPU oracle for the Gaussian Mixture Attention (GMA) forward pass.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()`` and by the CPU
+baseline leg of ``bench.py``.  The CUDA library never imports, links or calls anything here, and
+this package imports nothing from the CUDA library.
+
+Two independent formulations of the same definition
+(page "Attention par Mélange Gaussien (GMA)", gist.science/fr/paper/2606.18283, Méthodologie):
+
+* ``forward`` / ``responsibilities`` / ``params`` -- the linear (latent-memory) form in plain C,
+  fp64, one token at a time (``gma_oracle.c``);
+* ``oracle.bruteforce`` -- the explicit N x N affinity form in numpy fp64, for tiny inputs.
+
+Inputs are numpy arrays (any float dtype; they are widened to float64 exactly).
+"""
+import ctypes
+import numpy as np
+
+from .build import build_oracle
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build_oracle())
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.gmao_params.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp, ctypes.c_double, dp, dp]
+        lib.gmao_params.restype = None
+        lib.gmao_responsibilities.argtypes = [ctypes.c_int] * 3 + [dp] * 4 + [ctypes.c_double, dp]
+        lib.gmao_responsibilities.restype = None
+        lib.gmao_forward.argtypes = ([ctypes.c_int] * 7 + [dp] * 6
+                                     + [ctypes.c_double, ctypes.c_double, dp, ctypes.c_int])
+        lib.gmao_forward.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def params(raw, logits, var_floor):
+    """sigma^2 = softplus(raw) + var_floor and log pi = log softmax(logits), for one head.
+
+    raw: [K, d_r]; logits: [K].  Returns (var [K, d_r], logpi [K]) as float64.
+    """
+    raw = _f64(raw)
+    logits = _f64(logits)
+    K, d_r = raw.shape
+    var = np.empty((K, d_r))
+    logpi = np.empty(K)
+    _load().gmao_params(K, d_r, _p(raw), _p(logits), float(var_floor), _p(var), _p(logpi))
+    return var, logpi
+
+
+def responsibilities(X, mu, raw, logits, var_floor):
+    """GMM posterior responsibilities p(z = k | x) of the rows of X for one head.
+
+    X: [N, d_r]; mu, raw: [K, d_r]; logits: [K].  Returns gamma [N, K] float64.
+    """
+    X = _f64(X)
+    mu = _f64(mu)
+    raw = _f64(raw)
+    logits = _f64(logits)
+    N, d_r = X.shape
+    K = mu.shape[0]
+    g = np.empty((N, K))
+    _load().gmao_responsibilities(N, d_r, K, _p(X), _p(mu), _p(raw), _p(logits),
+                                  float(var_floor), _p(g))
+    return g
+
+
+def forward(causal, QX, KX, V, mu, raw, logits, var_floor, eps, nthreads=0, return_threads=False):
+    """GMA forward output O [B, H, N, d_v] (float64) for all slices.
+
+    QX, KX: [B, H, N, d_r]; V: [B, H, N, d_v]; mu, raw: [H, K, d_r]; logits: [H, K].
+    ``causal`` selects the prefix-sum variant.  ``nthreads`` caps the OpenMP threads (0 = all).
+    """
+    QX = _f64(QX)
+    KX = _f64(KX)
+    V = _f64(V)
+    mu = _f64(mu)
+    raw = _f64(raw)
+    logits = _f64(logits)
+    B, H, N, d_r = QX.shape
+    d_v = V.shape[-1]
+    K = mu.shape[1]
+    assert KX.shape == QX.shape and V.shape[:3] == QX.shape[:3]
+    assert mu.shape == (H, K, d_r) and raw.shape == (H, K, d_r) and logits.shape == (H, K)
+    O = np.empty((B, H, N, d_v))
+    used = _load().gmao_forward(int(bool(causal)), B, H, N, d_r, K, d_v, _p(QX), _p(KX), _p(V),
+                                _p(mu), _p(raw), _p(logits), float(var_floor), float(eps), _p(O),
+                                int(nthreads))
+    return (O, used) if return_threads else O
