@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of the GMA forward pass on GB300: tokens/s and fraction of roofline.
+
+One step = one full forward pass (responsibilities of queries and keys, write phase, read
+phase) over the workload's synthetic inputs, which are resident in HBM before timing starts.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gma|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own independent
+replica on its own heads (the (batch, head) slices do not interact), so per-GPU work is fixed
+and ``scaling`` is "weak"; the only collectives are the timing barrier and the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same workload (the
+only reference this method has: the page publishes no implementation).
+"""
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_latent_routing_gb300 import inputs as W  # noqa: E402
+
+METRIC = "GMA causal fwd tokens/s at N=65536,K=128 on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = W.LONG_CAUSAL.name
+L2_BYTES = 129 * 2 ** 20
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- work model
+def path_bytes(w):
+    """Algorithmic bytes of one step: Q_X, K_X, V read once and O written once."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return w.token_heads * esz * (2 * w.d_r + 2 * w.d_v)
+
+
+def path_flops(w):
+    """Algorithmic flops of one step: the two [x^2, x] contractions (8 d_r K) plus the write and
+    read contractions including the normaliser (4 K (d_v + 1)), per token-head."""
+    return w.token_heads * (8 * w.d_r * w.K + 4 * w.K * (w.d_v + 1))
+
+
+def kernel_work(w, name):
+    """(bound, amount, unit) of one launch of the named kernel.  Tensor-core kernels count
+    algorithmic bytes or flops of the steps they fuse; CUDA-core kernels count their fp32
+    arithmetic (bound "alu")."""
+    th = w.token_heads
+    esz = 2 if w.dtype == "bf16" else 4
+    if name == "tc_causal_chunked":
+        return "hbm", th * esz * (2 * w.d_r + 2 * w.d_v), "GB/s"
+    if name == "tc_causal_segment_memory":
+        return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
+    if name == "tc_bidir_write":
+        return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
+    if name == "tc_bidir_read":
+        return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
+    if name == "tc_responsibilities":
+        return "hbm", th * (esz * w.d_r + esz * w.K), "GB/s"
+    if name == "simt_responsibilities":      # one launch covers one side (queries or keys)
+        return "alu", th * 2 * w.K * w.d_r * 3, "TFLOP/s"
+    if name == "simt_read":
+        f = 2 * w.K * (w.d_v + 1)
+        if w.causal:
+            f += 2 * 64 * w.K + 64 * (w.d_v + 1)
+        return "alu", th * f, "TFLOP/s"
+    if name == "simt_segment_memory":
+        return "alu", th * 2 * w.K * (w.d_v + 1), "TFLOP/s"
+    return "hbm", 0, "GB/s"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.target = None
+        try:
+            self.target = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.target = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.target:
+            cmd += ["-i", self.target]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, budget_s, threads=0):
+    """Time the fp64 oracle on the first n tokens of every head of batch row 0 (n sized to take
+    about budget_s; exact work of the causal variant on those tokens).  Returns
+    (tokens/s, cores used, description)."""
+    import oracle
+    host = W.to_numpy(W.make_inputs(W.scaled(w, B=1)))
+
+    def run(n):
+        sl = slice(0, n)
+        t0 = time.perf_counter()
+        _, used = oracle.forward(w.causal, host["QX"][:, :, sl], host["KX"][:, :, sl],
+                                 host["V"][:, :, sl], host["mu"], host["raw"], host["logits"],
+                                 w.var_floor, w.eps, nthreads=threads, return_threads=True)
+        return time.perf_counter() - t0, used
+
+    n = min(64, w.N)
+    t, used = run(n)
+    while t < budget_s / 8 and n < w.N:
+        n = min(w.N, n * 4)
+        t, used = run(n)
+    if t < budget_s / 2 and n < w.N:
+        n = min(w.N, max(n, int(n * budget_s / max(t, 1e-3))))
+        t, used = run(n)
+    desc = (f"oracle (fp64 C, OpenMP over heads) on tokens 0..{n - 1} of all {w.H} heads of one "
+            f"sequence of {w.name}; {'causal prefix: exact work for those tokens' if w.causal else 'bidirectional over the truncated sequence'}")
+    return n / t, used, desc, n
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_gma(args, ws, rank, local):
+    from linear_latent_routing_gb300 import gma
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w0 = W.by_name(args.workload)
+    w = W.Workload(**{**w0.__dict__, "seed": w0.seed + 1000 * rank})
+    host = W.make_inputs(w)
+    dev = {k: v.to(device) for k, v in host.items()}
+    shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v,
+                           gma.GMA_BF16 if w.dtype == "bf16" else gma.GMA_F32, w.eps, w.var_floor)
+    variant = gma.GMA_VARIANT_CAUSAL if w.causal else gma.GMA_VARIANT_BIDIRECTIONAL
+    ws_n = gma.gma_workspace_size(shape, variant)
+    workspace = torch.empty(ws_n, dtype=torch.uint8, device=device)
+    O = torch.empty(w.B, w.H, w.N, w.d_v, dtype=dev["V"].dtype, device=device)
+    stream = torch.cuda.Stream(device)
+    sh = stream.cuda_stream
+    fn = gma.gma_forward_causal if w.causal else gma.gma_forward_bidirectional
+    ptrs = [dev[k].data_ptr() for k in ("QX", "KX", "V", "mu", "raw", "logits")]
+
+    def step():
+        r = fn(shape, *ptrs, O.data_ptr(), workspace.data_ptr(), ws_n, sh)
+        if r != 0:
+            raise gma.GmaError(r, fn.__name__)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    st = gma.gma_check_workspace(workspace.data_ptr(), sh)
+    if st != 0:
+        raise gma.GmaError(st, "warm-up")
+
+    steps = args.steps
+    if steps <= 0:   # auto: about 3 s of timed work, at least 20 steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(5):
+                step()
+            e1.record(stream)
+        stream.synchronize()
+        per = max(e0.elapsed_time(e1) / 5.0, 1e-3)
+        steps = int(min(20000, max(20, 3000.0 / per)))
+
+    gma.gma_timing_enable(steps * 8 + 64)
+    clocks = ClockSampler(device)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    total_ms = e0.elapsed_time(e1)
+    launches = gma.gma_timing_read(steps * 8 + 64)
+    gma.gma_timing_enable(0)
+    st = gma.gma_check_workspace(workspace.data_ptr(), sh)
+    if st != 0:
+        raise gma.GmaError(st, "timed region")
+
+    total_ms_max = max_over_ranks(total_ms, ws, device)
+    tokens_all = w.tokens * ws * steps
+    value = tokens_all / (total_ms_max / 1e3)
+
+    # dominant kernel and its roofline
+    per_kernel = {}
+    for name, ms in launches:
+        per_kernel.setdefault(name, []).append(ms)
+    dom = max(per_kernel, key=lambda k: sum(per_kernel[k]))
+    avg_ms = sum(per_kernel[dom]) / len(per_kernel[dom])
+    bound, amount, unit = kernel_work(w, dom)
+    pk = peaks()
+    if bound == "hbm":
+        achieved = amount / (avg_ms / 1e3) / 1e9
+        peak = pk["hbm_gbs"]
+        peak_src = f"hbm_gbs of {pk['source']}"
+    elif bound == "tensor":
+        achieved = amount / (avg_ms / 1e3) / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        peak_src = f"bf16_tflops_sustained of {pk['source']}"
+    else:
+        achieved = amount / (avg_ms / 1e3) / 1e12
+        peak = SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+        peak_src = "fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock"
+    roofline = {"bound": bound, "kernel": dom, "achieved": round(achieved, 3),
+                "peak": round(peak, 3), "unit": unit, "frac": round(achieved / peak, 4),
+                "traffic": None, "avg_launch_us": round(avg_ms * 1e3, 3),
+                "launches": len(per_kernel[dom]), "peak_source": peak_src}
+    step_bytes = path_bytes(w)
+    step_flops = path_flops(w)
+    step_s = total_ms_max / steps / 1e3
+    roof_s = max(step_bytes / (pk["hbm_gbs"] * 1e9), step_flops / (pk["bf16_tflops"] * 1e12))
+    path_roofline = {"roofline_step_us": round(roof_s * 1e6, 3),
+                     "measured_step_us": round(step_s * 1e6, 3),
+                     "frac": round(roof_s / step_s, 4),
+                     "alg_bytes": step_bytes, "alg_flops": step_flops}
+
+    # end to end through the C ABI with pinned host buffers
+    e2e_steps = max(3, min(steps, 10))
+    pin = {k: host[k].pin_memory() for k in ("QX", "KX", "V", "mu", "raw", "logits")}
+    O_host = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in pin)
+    d2h = O_host.numel() * O_host.element_size()
+
+    def e2e_step():
+        for k in pin:
+            dev[k].copy_(pin[k], non_blocking=True)
+        step()
+        O_host.copy_(O, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    stream.synchronize()
+    barrier(ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(a.elapsed_time(b), ws, device)
+    e2e = {"value": w.tokens * ws * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    if rank != 0:
+        return None
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_sample(W.by_name(args.workload), args.cpu_budget)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    fam = gma.gma_kernel_family(shape, variant)
+    launches_per_step = len(launches) / steps
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": total_ms_max / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded N(0,1) routing vectors and values)",
+        "config": {"workload": w0.name, "variant": "causal" if w.causal else "bidirectional",
+                   "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r, "K": w.K, "d_v": w.d_v,
+                   "eps": w.eps, "var_floor": w.var_floor,
+                   "kernel_family": "tcgen05" if fam == 1 else "fp32 cuda-core",
+                   "l2": ("inputs larger than L2 (%.0f MB > 129 MB), no flush"
+                          % (path_bytes(w) / 1e6)) if path_bytes(w) > L2_BYTES else
+                         "inputs smaller than L2: not flushed",
+                   "parallelism": f"replicas x{ws} (independent heads per rank)"},
+        "roofline": roofline, "path_roofline": path_roofline,
+        "kernels": {k: {"launches": len(v), "total_ms": round(sum(v), 4)}
+                    for k, v in per_kernel.items()},
+        "gpu_launches": len(launches), "launches_per_step": launches_per_step,
+        "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+    }
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    w = W.by_name(args.workload)
+    steps = args.steps if args.steps > 0 else 5
+    warm = max(args.warmup, 3)
+    per_step_budget = min(5.0, 150.0 / (steps + warm))
+    rate, cores, desc, n = oracle_sample(w, per_step_budget)
+    import oracle
+    host = W.to_numpy(W.make_inputs(W.scaled(w, B=1)))
+    sl = slice(0, n)
+
+    def one():
+        oracle.forward(w.causal, host["QX"][:, :, sl], host["KX"][:, :, sl], host["V"][:, :, sl],
+                       host["mu"], host["raw"], host["logits"], w.var_floor, w.eps)
+
+    for _ in range(warm):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    value = n * steps / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded), truncated sample",
+        "config": {"workload": w.name, "variant": "causal" if w.causal else "bidirectional",
+                   "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r, "K": w.K, "d_v": w.d_v},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 3 s of work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[x.name for x in W.ALL_WORKLOADS])
+    ap.add_argument("--impl", default="gma", choices=["gma", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of CPU work for the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    if args.impl == "reference":
+        ws, rank, _ = dist_setup("gloo") if int(os.environ.get("WORLD_SIZE", "1")) > 1 else (1, 0, 0)
+        out = run_reference(args, ws, rank)
+    else:
+        from linear_latent_routing_gb300 import build
+        build.build()
+        ws, rank, local = dist_setup("nccl")
+        out = run_gma(args, ws, rank, local)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,144 @@
+/*
+ * gma.h -- C ABI of libgma.so: the forward pass of Gaussian Mixture Attention (GMA) on an
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (page "Attention par Mélange Gaussien (GMA)", gist.science/fr/paper/2606.18283):
+ *
+ *   Méthodologie §1 "Routage Latent Probabiliste": each routing vector x (a row of Q_X or K_X)
+ *     is mapped to its GMM posterior responsibilities gamma_k = p(z = k | x) over K learned
+ *     diagonal Gaussians with means mu_k, variances Sigma_k and priors pi_k.
+ *   Méthodologie §3 "Variantes et Entraînement": variances through softplus, priors through
+ *     softmax.  Here  sigma^2 = softplus(raw_var) + var_floor  and  pi = softmax(prior_logits).
+ *   Méthodologie §2 "Routage de Mémoire Latente": keys write a K-slot memory
+ *     V~ = Gamma_K^T V and a normaliser Z = Gamma_K^T 1; queries read it through the page's
+ *     displayed equation  O = Gamma_Q V~ / (Gamma_Q Z + eps).
+ *   Méthodologie §3: the causal variant replaces V~ and Z by prefix sums, so that row i of O
+ *     depends only on keys j <= i (inclusive).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense, row-major and contiguous, in DEVICE memory of the current CUDA
+ *     device, 16-byte aligned:
+ *       Q_X, K_X      [B][H][N][d_r]    dtype (bf16 or fp32)
+ *       V             [B][H][N][d_v]    dtype
+ *       O             [B][H][N][d_v]    dtype (fp32 if GMA_FLAG_OUT_F32)
+ *       gamma         [B][H][N][K]      dtype (fp32 if GMA_FLAG_OUT_F32)
+ *       mu, raw_var   [H][K][d_r]       fp32   (one GMM per head, shared by queries, keys and
+ *                                               the whole batch)
+ *       prior_logits  [H][K]            fp32
+ *   - The caller owns and allocates every buffer, including the workspace (size from
+ *     gma_workspace_size).  The library never allocates, frees or synchronises inside these
+ *     calls: all work is enqueued on `stream` (NULL = the legacy default stream) and the call
+ *     returns without waiting for it.
+ *   - The workspace needs no initialisation: the library clears what it must on `stream`.
+ *     Calls that share one workspace must be ordered on the GPU (same stream, or events).
+ *   - Argument and shape errors return before anything is enqueued.  A failed kernel launch
+ *     returns GMA_ERR_CUDA.  Conditions found on the device (parameters outside the range the
+ *     tensor-core path can represent, a bounded wait that timed out) are recorded in the
+ *     workspace's error word and reported by gma_check_workspace; the library never traps.
+ *   - Supported sizes: B, H, N >= 1; d_r, d_v in {16, 32, 64, 128}; 1 <= K <= 1024;
+ *     B*H*N*max(d_r, d_v, K) < 2^31.  Inputs must be finite and |x| < 256 for bf16 inputs.
+ */
+#ifndef GMA_H
+#define GMA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t. */
+typedef struct CUstream_st *gma_stream_t;
+
+typedef enum {
+    GMA_OK = 0,
+    GMA_ERR_INVALID_ARG = 1,       /* null or misaligned pointer, non-positive size, bad eps  */
+    GMA_ERR_UNSUPPORTED_SHAPE = 2, /* d_r, d_v or K outside the supported set               */
+    GMA_ERR_RANGE = 3,             /* device: a reparametrised parameter exceeds fp16 range  */
+    GMA_ERR_WORKSPACE = 4,         /* workspace null, misaligned or smaller than required    */
+    GMA_ERR_CUDA = 5,              /* a CUDA runtime call or kernel launch failed            */
+    GMA_ERR_TIMEOUT = 6,           /* device: a bounded wait gave up                         */
+    GMA_ERR_NO_DEVICE = 7          /* no usable sm_103 device is current                     */
+} gma_status_t;
+
+typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype_t;
+
+/* Bits of gma_shape_t.flags. */
+#define GMA_FLAG_SIMT 0x1u     /* force the fp32 CUDA-core kernels (the path fp32 inputs take) */
+#define GMA_FLAG_OUT_F32 0x2u  /* write O (or gamma) as fp32 even for bf16 inputs              */
+
+typedef struct {
+    int B, H, N;     /* batch, heads, sequence length                                       */
+    int d_r;         /* routing dimension (columns of Q_X and K_X)                          */
+    int K;           /* number of Gaussian components                                       */
+    int d_v;         /* value dimension                                                     */
+    int dtype;       /* gma_dtype_t of Q_X, K_X, V and the output                           */
+    float eps;       /* added to every query row's normaliser Gamma_Q Z; eps >= 0           */
+    float var_floor; /* sigma^2 = softplus(raw_var) + var_floor; var_floor >= 0             */
+    unsigned flags;  /* GMA_FLAG_* bits                                                     */
+} gma_shape_t;
+
+/* Variants for gma_workspace_size. */
+#define GMA_VARIANT_RESPONSIBILITIES 0
+#define GMA_VARIANT_BIDIRECTIONAL 1
+#define GMA_VARIANT_CAUSAL 2
+
+/* Bytes of device workspace one call of `variant` with `shape` needs (0 for an invalid shape).
+ * The workspace must be 256-byte aligned.  Its first 256 bytes hold the error word that
+ * gma_check_workspace reads. */
+size_t gma_workspace_size(const gma_shape_t *shape, int variant);
+
+/* Posterior responsibilities (Méthodologie §1):
+ *   gamma[b][h][i][k] = p(z = k | X[b][h][i]) under head h's GMM.
+ * X [B][H][N][d_r] dtype; gamma [B][H][N][K] dtype (fp32 with GMA_FLAG_OUT_F32).
+ * shape->d_v and shape->eps are ignored. */
+gma_status_t gma_responsibilities(const gma_shape_t *shape, const void *X, const float *mu,
+                                  const float *raw_var, const float *prior_logits, void *gamma,
+                                  void *workspace, size_t workspace_bytes, gma_stream_t stream);
+
+/* Bidirectional GMA (Méthodologie §2):
+ *   V~ = Gamma_K^T V,  Z = Gamma_K^T 1,  O = Gamma_Q V~ / (Gamma_Q Z + eps)
+ * per (b, h) slice, over the whole sequence. */
+gma_status_t gma_forward_bidirectional(const gma_shape_t *shape, const void *QX, const void *KX,
+                                       const void *V, const float *mu, const float *raw_var,
+                                       const float *prior_logits, void *O, void *workspace,
+                                       size_t workspace_bytes, gma_stream_t stream);
+
+/* Causal GMA (Méthodologie §3): as above with V~ and Z replaced by inclusive prefix sums,
+ *   O_i = gamma_Q,i (sum_{j<=i} gamma_K,j^T v_j) / (gamma_Q,i . sum_{j<=i} gamma_K,j + eps). */
+gma_status_t gma_forward_causal(const gma_shape_t *shape, const void *QX, const void *KX,
+                                const void *V, const float *mu, const float *raw_var,
+                                const float *prior_logits, void *O, void *workspace,
+                                size_t workspace_bytes, gma_stream_t stream);
+
+/* Waits for `stream`, then returns the condition the device recorded in `workspace` during the
+ * last call that used it (GMA_OK if none), or GMA_ERR_CUDA if the stream reported an error. */
+gma_status_t gma_check_workspace(const void *workspace, gma_stream_t stream);
+
+/* Which kernel family a call with this shape and variant runs: 0 = fp32 CUDA-core kernels,
+ * 1 = tcgen05 tensor-core kernels, -1 = the shape is invalid. */
+int gma_kernel_family(const gma_shape_t *shape, int variant);
+
+/* Static description of a status code. */
+const char *gma_status_string(gma_status_t status);
+
+/* Launch timing, for benchmarks.  gma_timing_enable(capacity > 0) creates `capacity` pairs of
+ * CUDA events (call it outside stream capture); from then on every kernel launch of the library
+ * is bracketed by an event pair recorded on its stream.  gma_timing_enable(0) turns it off.
+ * gma_timing_read waits for the recorded launches and copies up to `cap` (kernel id, ms) pairs,
+ * oldest first, into caller-owned host arrays, then clears the record; it returns the number
+ * copied, or -1 on a CUDA error.  Launches beyond `capacity` are not recorded.
+ * gma_kernel_name maps a kernel id to a static string. */
+gma_status_t gma_timing_enable(int capacity);
+int gma_timing_read(int *kernel_ids, float *ms, int cap);
+const char *gma_kernel_name(int kernel_id);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int gma_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMA_H */

@@ -1,0 +1,92 @@
+// gma_internal.cuh -- definitions shared by the CUDA translation units of libgma.so.
+//
+// Nothing here is part of the public ABI (that is include/gma.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gma.h"
+
+namespace gma {
+
+// ------------------------------------------------------------------ workspace header
+// The first 256 bytes of every workspace.  `error` holds the first device-side condition that a
+// kernel recorded (a gma_status_t), `detail` a kernel-specific code for diagnostics.
+struct WsHeader {
+    unsigned error;
+    unsigned detail;
+    unsigned reserved[62];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+__device__ __forceinline__ void record_error(WsHeader *hdr, unsigned code, unsigned detail)
+{
+    if (atomicCAS(&hdr->error, 0u, code) == 0u) hdr->detail = detail;
+}
+
+// ------------------------------------------------------------------ element access
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v)
+{
+    return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v)
+{
+    return __float2bfloat16_rn(v);
+}
+
+// ------------------------------------------------------------------ host-side helpers
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// A linear allocator over a caller-provided workspace: offsets only, no allocation.
+struct Carve {
+    size_t off = sizeof(WsHeader);
+    size_t take(size_t bytes)
+    {
+        size_t at = align_up(off, 256);
+        off = at + bytes;
+        return at;
+    }
+    size_t total() const { return align_up(off, 256); }
+};
+
+inline bool valid_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// ------------------------------------------------------------------ optional launch timing
+// When enabled through gma_timing_enable, every kernel launch of the library is bracketed by a
+// pair of CUDA events recorded on the launching stream; gma_timing_read returns the durations.
+// Kernel ids name the launch sites (kernel_name gives the string).
+enum KernelId {
+    KID_SIMT_PARAMS = 1, KID_SIMT_RESP, KID_SIMT_STATE, KID_SIMT_SCAN, KID_SIMT_OUT,
+    KID_TC_PARAMS = 16, KID_TC_RESP, KID_TC_BIDIR_WRITE, KID_TC_BIDIR_READ, KID_TC_CAUSAL_AGG,
+    KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_COUNT
+};
+const char *kernel_name(int id);
+void timing_begin(cudaStream_t st, int kernel_id);
+void timing_end(cudaStream_t st);
+
+// --------------------------------------------------------------- fp32 CUDA-core kernel family
+size_t simt_workspace_size(const gma_shape_t &s, int variant);
+gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
+                                   const float *raw, const float *logits, void *gamma, void *ws,
+                                   cudaStream_t st);
+gma_status_t simt_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+                          const void *V, const float *mu, const float *raw, const float *logits,
+                          void *O, void *ws, cudaStream_t st);
+
+}  // namespace gma
+
+// Launch helper: timing brackets plus the launch-error check.
+#define GMA_LAUNCH(kid, st, ...)                                                              \
+    do {                                                                                      \
+        ::gma::timing_begin((st), (kid));                                                     \
+        __VA_ARGS__;                                                                          \
+        ::gma::timing_end((st));                                                              \
+        if (cudaPeekAtLastError() != cudaSuccess) return GMA_ERR_CUDA;                        \
+    } while (0)

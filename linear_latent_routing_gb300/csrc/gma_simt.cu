@@ -1,0 +1,339 @@
+// gma_simt.cu -- the fp32 CUDA-core kernel family of libgma.so.
+//
+// Every step in fp32 on the CUDA cores, with the Gaussian log-density in its direct form
+// (x - mu)^2 / sigma^2.  This is the path fp32 inputs take (tensor cores cannot hold fp32's
+// precision), the path GMA_FLAG_SIMT selects, and the correctness anchor for the tcgen05 family.
+//
+// Method (page "Attention par Mélange Gaussien (GMA)", gist.science/fr/paper/2606.18283,
+// Méthodologie §1-§3): responsibilities by the GMM posterior; write phase
+// V~ = Gamma_K^T V, Z = Gamma_K^T 1; read phase O = Gamma_Q V~ / (Gamma_Q Z + eps); causal
+// variant by inclusive prefix sums.
+//
+// Structure: Gamma_Q and Gamma_K are materialised in the workspace (fp32); keys are cut into
+// segments of SEG tokens whose partial memories [V~ | Z] are summed (bidirectional) or
+// exclusive-prefix-scanned (causal); each query segment then reads its memory and, for the
+// causal variant, adds the masked in-segment affinity (Gamma_Q Gamma_K^T restricted to j <= i).
+#include "gma_internal.cuh"
+
+namespace gma {
+namespace {
+
+constexpr int SEG = 64;        // tokens per segment
+constexpr int KT = 32;         // component tile for the staged dot products
+constexpr int THREADS = 256;
+
+// ---------------------------------------------------------------- reparametrisation
+// Per head h: inv_var[h][k][d] = 1 / (softplus(raw) + floor);
+//             cst[h][k]        = log pi_k - 1/2 sum_d log sigma^2_kd,  log pi = log softmax.
+__global__ void simt_params_kernel(const float *__restrict__ raw, const float *__restrict__ logits,
+                                   float *__restrict__ inv_var, float *__restrict__ cst, int K,
+                                   int d_r, float floor_)
+{
+    const int h = blockIdx.x;
+    const float *rh = raw + (size_t)h * K * d_r;
+    const float *lh = logits + (size_t)h * K;
+    __shared__ float red[THREADS];
+    float m = -INFINITY;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) m = fmaxf(m, lh[k]);
+    red[threadIdx.x] = m;
+    __syncthreads();
+    for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + o]);
+        __syncthreads();
+    }
+    m = red[0];
+    __syncthreads();
+    float s = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) s += expf(lh[k] - m);
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+        __syncthreads();
+    }
+    const float lse = m + logf(red[0]);
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        float logdet = 0.f;
+        for (int d = 0; d < d_r; ++d) {
+            const float r = rh[(size_t)k * d_r + d];
+            const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
+            inv_var[((size_t)h * K + k) * d_r + d] = 1.0f / var;
+            logdet += logf(var);
+        }
+        cst[(size_t)h * K + k] = (lh[k] - lse) - 0.5f * logdet;
+    }
+}
+
+// ---------------------------------------------------------------- responsibilities
+template <int DR>
+__device__ __forceinline__ float logit_direct(const float (&x)[DR], const float *__restrict__ mu_k,
+                                              const float *__restrict__ iv_k, float c_k)
+{
+    float q = 0.f;
+#pragma unroll
+    for (int d = 0; d < DR; ++d) {
+        const float t = x[d] - __ldg(mu_k + d);
+        q = fmaf(t * t, __ldg(iv_k + d), q);
+    }
+    return fmaf(-0.5f, q, c_k);
+}
+
+// One thread per routing vector: online max/sum over K, then a second pass writes
+// gamma_k = exp(L_k - max) / sum.
+template <int DR, typename Tin, typename Tout>
+__global__ void simt_resp_kernel(const Tin *__restrict__ X, const float *__restrict__ mu,
+                                 const float *__restrict__ inv_var, const float *__restrict__ cst,
+                                 Tout *__restrict__ gamma, int H, int N, int K, long long rows)
+{
+    const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    const int h = (int)((r / N) % H);
+    float x[DR];
+#pragma unroll
+    for (int d = 0; d < DR; ++d) x[d] = to_f32(X[r * DR + d]);
+    const float *muh = mu + (size_t)h * K * DR;
+    const float *ivh = inv_var + (size_t)h * K * DR;
+    const float *ch = cst + (size_t)h * K;
+    float m = -INFINITY, s = 0.f;
+    for (int k = 0; k < K; ++k) {
+        const float L = logit_direct<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k));
+        if (L > m) {
+            s = s * expf(m - L) + 1.f;
+            m = L;
+        } else {
+            s += expf(L - m);
+        }
+    }
+    const float inv = 1.f / s;
+    Tout *g = gamma + r * K;
+    for (int k = 0; k < K; ++k) {
+        const float L = logit_direct<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k));
+        g[k] = from_f32<Tout>(expf(L - m) * inv);
+    }
+}
+
+// ---------------------------------------------------------------- write phase, per segment
+// agg[bh][seg][k][c] = sum_{j in seg} gamma_K[j][k] * [v_j | 1][c],  c in [0, d_v].
+template <typename Tin>
+__global__ void simt_state_kernel(const float *__restrict__ gk, const Tin *__restrict__ V,
+                                  float *__restrict__ agg, int N, int K, int d_v, int nseg)
+{
+    const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
+    const int k0 = blockIdx.y * KT;
+    const int j0 = seg * SEG, jn = min(SEG, N - j0);
+    const int kn = min(KT, K - k0);
+    const int DV1 = d_v + 1;
+    __shared__ float sg[SEG][KT + 1];
+    __shared__ float sv[SEG][129];
+    for (int e = threadIdx.x; e < SEG * KT; e += blockDim.x) {
+        const int j = e / KT, kk = e % KT;
+        sg[j][kk] = (j < jn && kk < kn) ? gk[((size_t)bh * N + j0 + j) * K + k0 + kk] : 0.f;
+    }
+    for (int e = threadIdx.x; e < SEG * d_v; e += blockDim.x) {
+        const int j = e / d_v, c = e % d_v;
+        sv[j][c] = j < jn ? to_f32(V[((size_t)bh * N + j0 + j) * d_v + c]) : 0.f;
+    }
+    __syncthreads();
+    float *out = agg + ((size_t)bh * nseg + seg) * K * DV1;
+    for (int e = threadIdx.x; e < kn * DV1; e += blockDim.x) {
+        const int kk = e / DV1, c = e % DV1;
+        float acc = 0.f;
+        if (c < d_v) {
+            for (int j = 0; j < jn; ++j) acc = fmaf(sg[j][kk], sv[j][c], acc);
+        } else {
+            for (int j = 0; j < jn; ++j) acc += sg[j][kk];
+        }
+        out[(size_t)(k0 + kk) * DV1 + c] = acc;
+    }
+}
+
+// Causal: replace each segment's partial by the exclusive prefix over earlier segments.
+// Bidirectional: write the total over all segments into segment 0's slot.
+__global__ void simt_scan_kernel(float *__restrict__ agg, long long total, int nseg, int KD,
+                                 int causal)
+{
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const long long bh = idx / KD, e = idx % KD;
+    float *base = agg + bh * nseg * KD + e;
+    float run = 0.f;
+    for (int s = 0; s < nseg; ++s) {
+        const float a = base[(size_t)s * KD];
+        if (causal) base[(size_t)s * KD] = run;
+        run += a;
+    }
+    if (!causal) base[0] = run;
+}
+
+// ---------------------------------------------------------------- read phase, per segment
+// O_i = (gamma_Q,i S + sum_{j<=i in seg} P_ij v_j) / (gamma_Q,i Z + sum_{j<=i in seg} P_ij + eps)
+// with P = Gamma_Q Gamma_K^T on the segment (causal only) and [S | Z] the segment's memory.
+template <typename Tin, typename Tout>
+__global__ void simt_out_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
+                                const Tin *__restrict__ V, const float *__restrict__ agg,
+                                Tout *__restrict__ O, int N, int K, int d_v, int nseg, float eps,
+                                int causal)
+{
+    const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
+    const int i0 = seg * SEG, in = min(SEG, N - i0);
+    const int DV1 = d_v + 1;
+    const float *S = agg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * DV1;
+    const float *gqs = gq + ((size_t)bh * N + i0) * K;
+    const float *gks = gk + ((size_t)bh * N + i0) * K;
+    __shared__ float P[SEG][SEG + 1];
+    __shared__ float sq[SEG][KT + 1];
+    __shared__ float sk[SEG][KT + 1];
+    __shared__ float den[SEG];
+
+    if (causal) {
+        float acc[SEG * SEG / THREADS];
+#pragma unroll
+        for (int r = 0; r < SEG * SEG / THREADS; ++r) acc[r] = 0.f;
+        for (int k0 = 0; k0 < K; k0 += KT) {
+            const int kn = min(KT, K - k0);
+            for (int e = threadIdx.x; e < SEG * KT; e += blockDim.x) {
+                const int i = e / KT, kk = e % KT;
+                const bool ok = i < in && kk < kn;
+                sq[i][kk] = ok ? gqs[(size_t)i * K + k0 + kk] : 0.f;
+                sk[i][kk] = ok ? gks[(size_t)i * K + k0 + kk] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < SEG * SEG / THREADS; ++r) {
+                const int e = threadIdx.x + r * THREADS;
+                const int i = e / SEG, j = e % SEG;
+                float a = acc[r];
+                for (int kk = 0; kk < KT; ++kk) a = fmaf(sq[i][kk], sk[j][kk], a);
+                acc[r] = a;
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int r = 0; r < SEG * SEG / THREADS; ++r) {
+            const int e = threadIdx.x + r * THREADS;
+            const int i = e / SEG, j = e % SEG;
+            P[i][j] = (j <= i && i < in) ? acc[r] : 0.f;
+        }
+        __syncthreads();
+    }
+    // denominators first (column d_v of the memory), then numerators
+    for (int i = threadIdx.x; i < in; i += blockDim.x) {
+        float d = 0.f;
+        for (int k = 0; k < K; ++k) d = fmaf(gqs[(size_t)i * K + k], S[(size_t)k * DV1 + d_v], d);
+        if (causal)
+            for (int j = 0; j <= i; ++j) d += P[i][j];
+        den[i] = d + eps;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < in * d_v; e += blockDim.x) {
+        const int i = e / d_v, c = e % d_v;
+        float n = 0.f;
+        for (int k = 0; k < K; ++k) n = fmaf(gqs[(size_t)i * K + k], S[(size_t)k * DV1 + c], n);
+        if (causal)
+            for (int j = 0; j <= i; ++j)
+                n = fmaf(P[i][j], to_f32(V[((size_t)bh * N + i0 + j) * d_v + c]), n);
+        O[((size_t)bh * N + i0 + i) * d_v + c] = from_f32<Tout>(n / den[i]);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+struct SimtLayout {
+    size_t inv_var, cst, gq, gk, agg, total;
+    int nseg;
+};
+
+SimtLayout simt_layout(const gma_shape_t &s, int variant)
+{
+    SimtLayout L{};
+    Carve c;
+    const size_t rows = (size_t)s.B * s.H * s.N;
+    L.inv_var = c.take(sizeof(float) * (size_t)s.H * s.K * s.d_r);
+    L.cst = c.take(sizeof(float) * (size_t)s.H * s.K);
+    L.nseg = (s.N + SEG - 1) / SEG;
+    if (variant != GMA_VARIANT_RESPONSIBILITIES) {
+        L.gq = c.take(sizeof(float) * rows * s.K);
+        L.gk = c.take(sizeof(float) * rows * s.K);
+        L.agg = c.take(sizeof(float) * (size_t)s.B * s.H * L.nseg * s.K * (s.d_v + 1));
+    }
+    L.total = c.total();
+    return L;
+}
+
+template <typename Tin, typename Tout>
+gma_status_t launch_resp(int d_r, const Tin *X, const float *mu, const float *iv, const float *cst,
+                         Tout *g, int H, int N, int K, long long rows, cudaStream_t st)
+{
+    const unsigned blocks = (unsigned)((rows + 127) / 128);
+    switch (d_r) {
+    case 16: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<16, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
+    case 32: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<32, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
+    case 64: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<64, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
+    case 128: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<128, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
+    default: return GMA_ERR_UNSUPPORTED_SHAPE;
+    }
+    return GMA_OK;
+}
+
+template <typename Tin, typename Tout>
+gma_status_t forward_typed(const gma_shape_t &s, bool causal, const Tin *QX, const Tin *KX,
+                           const Tin *V, const float *mu, const float *raw, const float *logits,
+                           Tout *O, char *ws, cudaStream_t st)
+{
+    const SimtLayout L = simt_layout(s, causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL);
+    float *iv = (float *)(ws + L.inv_var), *cst = (float *)(ws + L.cst);
+    float *gq = (float *)(ws + L.gq), *gk = (float *)(ws + L.gk), *agg = (float *)(ws + L.agg);
+    const long long rows = (long long)s.B * s.H * s.N;
+    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<s.H, THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
+    gma_status_t r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
+    if (r != GMA_OK) return r;
+    r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, s.N, s.K, rows, st);
+    if (r != GMA_OK) return r;
+    const int BH = s.B * s.H;
+    dim3 gs((unsigned)(BH * L.nseg), (unsigned)((s.K + KT - 1) / KT));
+    GMA_LAUNCH(KID_SIMT_STATE, st, (simt_state_kernel<Tin><<<gs, THREADS, 0, st>>>(gk, V, agg, s.N, s.K, s.d_v, L.nseg)));
+    const int KD = s.K * (s.d_v + 1);
+    const long long tot = (long long)BH * KD;
+    GMA_LAUNCH(KID_SIMT_SCAN, st, (simt_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(agg, tot, L.nseg, KD, causal ? 1 : 0)));
+    GMA_LAUNCH(KID_SIMT_OUT, st, (simt_out_kernel<Tin, Tout><<<(unsigned)(BH * L.nseg), THREADS, 0, st>>>(
+        gq, gk, V, agg, O, s.N, s.K, s.d_v, L.nseg, s.eps, causal ? 1 : 0)));
+    return GMA_OK;
+}
+
+}  // namespace
+
+size_t simt_workspace_size(const gma_shape_t &s, int variant) { return simt_layout(s, variant).total; }
+
+gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
+                                   const float *raw, const float *logits, void *gamma, void *ws,
+                                   cudaStream_t st)
+{
+    const SimtLayout L = simt_layout(s, GMA_VARIANT_RESPONSIBILITIES);
+    char *w = (char *)ws;
+    float *iv = (float *)(w + L.inv_var), *cst = (float *)(w + L.cst);
+    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<s.H, THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
+    const long long rows = (long long)s.B * s.H * s.N;
+    const bool out32 = (s.flags & GMA_FLAG_OUT_F32) || s.dtype == GMA_F32;
+    if (s.dtype == GMA_F32)
+        return launch_resp<float, float>(s.d_r, (const float *)X, mu, iv, cst, (float *)gamma, s.H, s.N, s.K, rows, st);
+    if (out32)
+        return launch_resp<__nv_bfloat16, float>(s.d_r, (const __nv_bfloat16 *)X, mu, iv, cst, (float *)gamma, s.H, s.N, s.K, rows, st);
+    return launch_resp<__nv_bfloat16, __nv_bfloat16>(s.d_r, (const __nv_bfloat16 *)X, mu, iv, cst, (__nv_bfloat16 *)gamma, s.H, s.N, s.K, rows, st);
+}
+
+gma_status_t simt_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+                          const void *V, const float *mu, const float *raw, const float *logits,
+                          void *O, void *ws, cudaStream_t st)
+{
+    char *w = (char *)ws;
+    if (s.dtype == GMA_F32)
+        return forward_typed<float, float>(s, causal, (const float *)QX, (const float *)KX,
+                                           (const float *)V, mu, raw, logits, (float *)O, w, st);
+    typedef __nv_bfloat16 bf;
+    if (s.flags & GMA_FLAG_OUT_F32)
+        return forward_typed<bf, float>(s, causal, (const bf *)QX, (const bf *)KX, (const bf *)V,
+                                        mu, raw, logits, (float *)O, w, st);
+    return forward_typed<bf, bf>(s, causal, (const bf *)QX, (const bf *)KX, (const bf *)V, mu,
+                                 raw, logits, (bf *)O, w, st);
+}
+
+}  // namespace gma

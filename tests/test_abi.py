@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and exports every
+function include/gma.h declares; validation and workspace sizing behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def g():
+    from linear_latent_routing_gb300 import build
+    build.build()
+    from linear_latent_routing_gb300 import gma
+    return gma
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(gma_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("gma_responsibilities", "gma_forward_bidirectional", "gma_forward_causal",
+              "gma_workspace_size", "gma_check_workspace", "gma_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(g):
+    lib = ctypes.CDLL(g.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(g):
+    for code in range(8):
+        s = g.gma_status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert g.gma_status_string(99) == "unknown status"
+    assert g.gma_version() >= 100
+
+
+def _shape(g, **kw):
+    d = dict(B=2, H=3, N=100, d_r=64, K=64, d_v=64, dtype=g.GMA_BF16)
+    d.update(kw)
+    return g.make_shape(**d)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_workspace_size_valid_shapes(g, variant):
+    s = _shape(g)
+    n = g.gma_workspace_size(s, variant)
+    assert n > 256 and n % 256 == 0
+    assert g.gma_kernel_family(s, variant) in (0, 1)
+
+
+@pytest.mark.parametrize("bad", [dict(B=0), dict(N=-1), dict(K=0), dict(K=1025), dict(d_r=48),
+                                 dict(d_v=8), dict(dtype=7), dict(eps=-1.0),
+                                 dict(var_floor=float("nan")), dict(flags=0x80)])
+def test_invalid_shapes_have_no_workspace(g, bad):
+    s = _shape(g, **bad)
+    assert g.gma_workspace_size(s, g.GMA_VARIANT_CAUSAL) == 0
+    assert g.gma_kernel_family(s, g.GMA_VARIANT_CAUSAL) == -1
+
+
+def test_responsibilities_ignore_value_dimension(g):
+    s = _shape(g, d_v=7)
+    assert g.gma_workspace_size(s, g.GMA_VARIANT_RESPONSIBILITIES) > 0
+    assert g.gma_workspace_size(s, g.GMA_VARIANT_CAUSAL) == 0
+
+
+def test_workspace_grows_linearly_in_sequence_length(g):
+    # the page's profiling claim: activation memory O(N K) at fixed K
+    sizes = [g.gma_workspace_size(_shape(g, N=n), g.GMA_VARIANT_CAUSAL) for n in (4096, 8192, 16384)]
+    d1, d2 = sizes[1] - sizes[0], sizes[2] - sizes[1]
+    assert abs(d2 - 2 * d1) <= 4096
+
+
+def test_bad_arguments_rejected_before_any_device_work(g):
+    s = _shape(g)
+    ws_n = g.gma_workspace_size(s, g.GMA_VARIANT_CAUSAL)
+    fake = 1 << 20   # never dereferenced: validation fails first
+    args = [fake] * 7
+    # null pointer
+    r = g.gma_forward_causal(s, None, *args[1:], fake, ws_n, None)
+    assert r == 1
+    # misaligned pointer
+    r = g.gma_forward_causal(s, fake + 8, *args[1:], fake, ws_n, None)
+    assert r == 1
+    # workspace too small / misaligned
+    r = g.gma_forward_causal(s, *args, fake, ws_n - 1, None)
+    assert r == 4
+    r = g.gma_forward_causal(s, *args, fake + 16, ws_n, None)
+    assert r == 4
+    # unsupported shape
+    r = g.gma_forward_bidirectional(_shape(g, d_v=24), *args, fake, ws_n, None)
+    assert r == 2
+    r = g.gma_responsibilities(_shape(g, K=2000), *args[:5], fake, ws_n, None)
+    assert r == 2
+
+
+def test_no_device_is_reported_without_a_gpu(g):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    s = _shape(g)
+    ws_n = g.gma_workspace_size(s, g.GMA_VARIANT_CAUSAL)
+    fake = 1 << 20
+    r = g.gma_forward_causal(s, *([fake] * 7), fake, ws_n, None)
+    assert r == 7

@@ -1,0 +1,167 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on the same seeded
+inputs.  Tolerances: max relative error 1e-5 for fp32 inputs, 2e-2 for bf16 inputs with fp32
+accumulation (normwise per slice, see tests/parity.py)."""
+import numpy as np
+import pytest
+import torch
+
+from linear_latent_routing_gb300 import inputs as W
+from parity import (TOL, gpu_forward, normwise_error, oracle_forward, rowwise_error, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from linear_latent_routing_gb300 import build
+    build.build()
+
+
+def _gma():
+    from linear_latent_routing_gb300 import gma
+    return gma
+
+
+def _run(w, flags=0):
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    O = gpu_forward(w, dev, flags=flags).float().cpu().numpy()
+    ref = oracle_forward(w, host)
+    return O, ref
+
+
+# ------------------------------------------------------------- small cases, whole output
+
+SMALL = [
+    W.TINY_BIDIR_F32,
+    W.scaled(W.TINY_BIDIR_F32, causal=True),
+    W.scaled(W.LM_CAUSAL, B=1, H=2, N=1000),
+    W.scaled(W.LM_CAUSAL, B=2, H=1, N=1000, causal=False),
+    W.scaled(W.LRA_BIDIR, B=2, H=2, N=777),
+    W.scaled(W.LONG_CAUSAL, B=1, H=2, N=1500),
+    W.scaled(W.LONG_CAUSAL, B=1, H=1, N=700, causal=False),
+    W.scaled(W.LM_CAUSAL, B=1, H=1, N=1, K=16),
+    W.scaled(W.LM_CAUSAL, B=1, H=1, N=129, K=1),
+    W.scaled(W.LRA_BIDIR, B=1, H=1, N=130, K=1),
+    W.scaled(W.LM_CAUSAL, B=1, H=1, N=300, d_r=16, K=8, d_v=16),
+    W.scaled(W.LM_CAUSAL, B=1, H=1, N=300, d_r=128, K=24, d_v=128),
+    W.scaled(W.LRA_BIDIR, B=1, H=1, N=257, d_r=128, K=40, d_v=32),
+    W.scaled(W.K_SWEEP[2], B=1, H=1, N=400),
+    W.scaled(W.K_SWEEP[3], B=1, H=1, N=300),
+    W.scaled(W.K_SWEEP[3], B=1, H=1, N=300, causal=False),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: f"{'c' if w.causal else 'b'}_{w.dtype}_"
+                         f"B{w.B}H{w.H}N{w.N}r{w.d_r}K{w.K}v{w.d_v}")
+@pytest.mark.parametrize("flags", [0, 1], ids=["default", "simt"])
+def test_small_cases_match_oracle(w, flags):
+    O, ref = _run(w, flags=flags)
+    err = normwise_error(O, ref)
+    assert np.isfinite(O).all()
+    assert err <= TOL[w.dtype], (err, rowwise_error(O, ref))
+
+
+def test_fp32_output_flag():
+    w = W.scaled(W.LM_CAUSAL, B=1, H=2, N=500)
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    O = gpu_forward(w, dev, flags=_gma().GMA_FLAG_OUT_F32)
+    assert O.dtype == torch.float32
+    assert normwise_error(O.cpu().numpy(), oracle_forward(w, host)) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------- responsibilities
+
+@pytest.mark.parametrize("w,tol", [(W.TINY_BIDIR_F32, 1e-5),
+                                   (W.scaled(W.LONG_CAUSAL, B=1, H=2, N=600), 2e-2),
+                                   (W.scaled(W.K_SWEEP[3], B=1, H=1, N=200), 2e-2),
+                                   (W.scaled(W.LM_CAUSAL, B=1, H=1, N=77, K=1), 2e-2)])
+def test_responsibilities_match_oracle(w, tol):
+    import oracle
+    gma = _gma()
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    g = gma.responsibilities(dev["QX"], dev["mu"], dev["raw"], dev["logits"],
+                             var_floor=w.var_floor, check=True).float().cpu().numpy()
+    a = W.to_numpy(host)
+    for b in range(w.B):
+        for h in range(w.H):
+            ref = oracle.responsibilities(a["QX"][b, h], a["mu"][h], a["raw"][h], a["logits"][h],
+                                          w.var_floor)
+            assert np.abs(g[b, h] - ref).max() <= tol
+    assert (g >= 0).all()
+    np.testing.assert_allclose(g.sum(-1), 1.0, atol=3e-2 if w.dtype == "bf16" else 1e-5)
+
+
+# ------------------------------------------------------------- the benchmark workloads, full size
+
+FULL = [W.LM_CAUSAL, W.LRA_BIDIR, W.LONG_CAUSAL]
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_full_size_sampled_slices(w):
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    O = gpu_forward(w, dev)
+    torch.cuda.synchronize()
+    picks = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]
+    n = w.N if w.N * w.K <= 65536 * 128 else 16384
+    for b, h in picks:
+        ref = oracle_forward(w, host, b=b, h=h, n=n if w.causal else None)
+        got = O[b:b + 1, h:h + 1, :ref.shape[2]].float().cpu().numpy()
+        assert normwise_error(got, ref) <= TOL[w.dtype]
+    assert torch.isfinite(O).all()
+
+
+@pytest.mark.parametrize("w", [W.K_SWEEP[0], W.K_SWEEP[3], W.N_SWEEP[-1]], ids=lambda w: w.name)
+def test_sweep_points_sampled_prefix(w):
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    O = gpu_forward(w, dev)
+    torch.cuda.synchronize()
+    n = 2048
+    ref = oracle_forward(w, host, b=w.B - 1, h=w.H - 1, n=n)
+    got = O[w.B - 1:w.B, w.H - 1:w.H, :n].float().cpu().numpy()
+    assert normwise_error(got, ref) <= TOL[w.dtype]
+    assert torch.isfinite(O).all()
+
+
+# ------------------------------------------------------------- buffers, streams, status
+
+def test_guard_bands_untouched_and_status_ok():
+    gma = _gma()
+    w = W.scaled(W.LM_CAUSAL, B=1, H=2, N=333)
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor)
+    n_out = w.B * w.H * w.N * w.d_v
+    pad = 4096
+    big = torch.full((n_out + 2 * pad,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    O = big[pad:pad + n_out]
+    ws_n = gma.gma_workspace_size(shape, gma.GMA_VARIANT_CAUSAL)
+    wsbig = torch.full((ws_n + 2 * 65536,), 0x7F, dtype=torch.uint8, device="cuda")
+    ws = wsbig[65536:65536 + ws_n]
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        r = gma.gma_forward_causal(shape, dev["QX"].data_ptr(), dev["KX"].data_ptr(),
+                                   dev["V"].data_ptr(), dev["mu"].data_ptr(),
+                                   dev["raw"].data_ptr(), dev["logits"].data_ptr(),
+                                   O.data_ptr(), ws.data_ptr(), ws_n, st.cuda_stream)
+    assert r == 0
+    assert gma.gma_check_workspace(ws.data_ptr(), st.cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert torch.isnan(big[:pad].float()).all() and torch.isnan(big[pad + n_out:].float()).all()
+    assert (wsbig[:65536] == 0x7F).all() and (wsbig[65536 + ws_n:] == 0x7F).all()
+    ref = oracle_forward(w, host)
+    assert normwise_error(O.view(w.B, w.H, w.N, w.d_v).float().cpu().numpy(), ref) <= TOL["bf16"]
+
+
+def test_repeat_calls_are_deterministic_and_reuse_workspace():
+    w = W.scaled(W.LONG_CAUSAL, B=1, H=2, N=1200)
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    a = gpu_forward(w, dev)
+    b = gpu_forward(w, dev)
+    assert torch.equal(a, b)
