@@ -28,13 +28,8 @@ gma_status_t validate_shape(const gma_shape_t *s, int variant)
     return GMA_OK;
 }
 
-int family_of(const gma_shape_t &s, int /*variant*/)
-{
-    // The tcgen05 family is added alongside; until it covers a shape, the fp32 CUDA-core
-    // kernels run it.
-    (void)s;
-    return 0;
-}
+// 1 = tcgen05 tensor-core family (bf16 inputs it covers), 0 = fp32 CUDA-core family.
+int family_of(const gma_shape_t &s, int variant) { return tc_supported(s, variant) ? 1 : 0; }
 
 gma_status_t check_device()
 {
@@ -73,6 +68,8 @@ gma_status_t forward_common(bool causal, const gma_shape_t *s, const void *QX, c
     cudaStream_t st = (cudaStream_t)stream;
     r = begin_call(s, variant, ws, ws_bytes, st);
     if (r != GMA_OK) return r;
+    if (family_of(*s, variant) == 1)
+        return tc_forward(*s, causal, QX, KX, V, mu, raw, logits, O, ws, st);
     return simt_forward(*s, causal, QX, KX, V, mu, raw, logits, O, ws, st);
 }
 
@@ -84,7 +81,8 @@ size_t gma_workspace_size(const gma_shape_t *s, int variant)
 {
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return 0;
     if (validate_shape(s, variant) != GMA_OK) return 0;
-    return simt_workspace_size(*s, variant);
+    return family_of(*s, variant) == 1 ? tc_workspace_size(*s, variant)
+                                       : simt_workspace_size(*s, variant);
 }
 
 int gma_kernel_family(const gma_shape_t *s, int variant)
@@ -106,6 +104,8 @@ gma_status_t gma_responsibilities(const gma_shape_t *s, const void *X, const flo
     cudaStream_t st = (cudaStream_t)stream;
     r = begin_call(s, GMA_VARIANT_RESPONSIBILITIES, ws, ws_bytes, st);
     if (r != GMA_OK) return r;
+    if (family_of(*s, GMA_VARIANT_RESPONSIBILITIES) == 1)
+        return tc_responsibilities(*s, X, mu, raw, logits, gamma, ws, st);
     return simt_responsibilities(*s, X, mu, raw, logits, gamma, ws, st);
 }
 

@@ -80,6 +80,16 @@ gma_status_t simt_forward(const gma_shape_t &s, bool causal, const void *QX, con
                           const void *V, const float *mu, const float *raw, const float *logits,
                           void *O, void *ws, cudaStream_t st);
 
+// --------------------------------------------------------------- tcgen05 kernel family
+bool tc_supported(const gma_shape_t &s, int variant);
+size_t tc_workspace_size(const gma_shape_t &s, int variant);
+gma_status_t tc_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
+                                 const float *raw, const float *logits, void *gamma, void *ws,
+                                 cudaStream_t st);
+gma_status_t tc_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+                        const void *V, const float *mu, const float *raw, const float *logits,
+                        void *O, void *ws, cudaStream_t st);
+
 }  // namespace gma
 
 // Launch helper: timing brackets plus the launch-error check.

@@ -1,0 +1,1078 @@
+// gma_tc.cu -- the tcgen05 tensor-core kernel family of libgma.so (bf16 inputs, sm_103a).
+//
+// Method: page "Attention par Mélange Gaussien (GMA)" (gist.science/fr/paper/2606.18283),
+// Méthodologie §1 (posterior responsibilities), §2 (write phase V~ = Gamma_K^T V, Z = Gamma_K^T 1;
+// read phase O = Gamma_Q V~ / (Gamma_Q Z + eps)), §3 (causal variant by prefix sums; softplus
+// variances and softmax priors).
+//
+// GB300 design.
+//  * The diagonal-Gaussian log-density is expanded into one dense contraction per token:
+//      log2e * L_k = [x^2 , x] . [-w_k/2 ; mu_k w_k] * log2e + c_k,   w = 1/sigma^2,
+//    an M=128 x N=K x K=2 d_r tcgen05.mma (fp16 operands, fp32 accumulators in TMEM).  The
+//    softmax over K runs on the CUDA cores straight out of TMEM (one thread per token row).
+//  * Gamma stays on chip (shared memory, bf16).  Write, read and the causal chunk products are
+//    tcgen05.mma with bf16 operands and fp32 accumulation.  The normaliser rides along as an
+//    extra block of ones next to V (16 extra MMA columns), so Z and Gamma_Q Z come out of the
+//    same MMAs as V~ and Gamma_Q V~.
+//  * Causal: the sequence is cut into chunks of C = 128 tokens.  Per chunk
+//      O_c = (Gamma_Q,c S_{c-1} + tril(Gamma_Q,c Gamma_K,c^T) [V_c, 1])  (numerator | normaliser)
+//      S_c = S_{c-1} + Gamma_K,c^T [V_c, 1]
+//    with the running memory S (K x (d_v+16), fp32) in TMEM.  Chunks are grouped into segments
+//    handled by different CTAs; a first kernel writes each segment's memory, a scan turns them
+//    into exclusive prefixes, and the chunked kernel starts each segment from its prefix.
+//  * Gamma_Q is kept unnormalised (row maximum 1); with row sum s_i the read is
+//      O_i = num_i / (den_i + eps * s_i),
+//    which equals the page's O_i exactly.
+//
+// Shared-memory operand layouts (all written either by TMA or by the CUDA cores with the same
+// address swizzle the tensor cores read):
+//  * K-major, 128-byte swizzle: rows of 64 two-byte elements (128 B), 8-row groups of 1 KB,
+//    64-element column blocks ("atoms") stacked after each other; chunk q of row r lives at
+//    16 * ((q % 8) ^ (r % 8)).  Used for [x^2, x], the Gaussian table, Gamma_Q, Gamma_K, P.
+//  * MN-major, 32-byte swizzle: blocks of 16 columns x rows, 32 B per row; the two 16-byte
+//    halves of row r are swapped when bit 2 of r is set.  Used for [V | 1] and the memory S.
+#include <cuda.h>
+#include <mutex>
+
+#include "gma_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace gma {
+namespace tck {
+
+using namespace tc;
+
+constexpr int C = 128;          // tokens per chunk (the MMA M dimension)
+constexpr int THREADS = 128;    // one thread per TMEM lane / token row / component row
+constexpr int KMAX = 128;       // components handled by this family
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float NEG_BIG = -1.0e30f;
+
+typedef __nv_bfloat16 bf16;
+
+struct Args {
+    const bf16 *QX, *KX;
+    void *O;                 // output (bf16 or fp32)
+    void *gamma;             // responsibilities output (bf16 or fp32)
+    const uint8_t *bimg;     // per-head Gaussian table image [H][bimg_bytes]
+    const float *cst;        // per-head log2-domain constants [H][kn16]
+    float *agg;              // segment memories [BH][nseg][KMAX][ne] fp32
+    WsHeader *hdr;
+    int H, N, K, kn16, d_v, ne;
+    int nseg, cps;           // segments per slice, chunks per segment
+    int bimg_bytes;
+    float eps;
+    int out_f32;
+};
+
+// ------------------------------------------------------------------ layout helpers
+__device__ __forceinline__ uint32_t sw128(int row, int q, int rows)
+{
+    return (uint32_t)((q >> 3) * rows * 128 + row * 128 + (((q & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t sw32(int row, int blk, int half, int rows)
+{
+    return (uint32_t)(blk * rows * 32 + row * 32 + ((half ^ ((row >> 2) & 1)) << 4));
+}
+
+// K-major SW128 operand, k-step s (16 elements)
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int s, int rows)
+{
+    return smem_desc(base + (uint32_t)((s >> 2) * rows * 128 + (s & 3) * 32), 16, 1024, SW_128B);
+}
+
+// MN-major SW128 operand whose K dimension runs along rows (128 B each), k-step s.
+__device__ __forceinline__ uint64_t mn128desc(uint32_t base, int s, int rows)
+{
+    return smem_desc(base + (uint32_t)(s * 16 * 128), (uint32_t)(rows * 128), 1024, SW_128B);
+}
+
+// MN-major SW32 operand (blocks of 16 MN elements), k-step s.
+__device__ __forceinline__ uint64_t mn32desc(uint32_t base, int s, int rows)
+{
+    return smem_desc(base + (uint32_t)(s * 16 * 32), (uint32_t)(rows * 32), 256, SW_32B);
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float a, float b)
+{
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Shared-memory plan of one CTA.  Regions are 1 KB aligned.
+struct Smem {
+    uint32_t bimg, abuf, gk, gq, ve, sp, cst, bars, tslot, total;
+    __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    __host__ __device__ Smem(int DR, int kn16, int d_v, bool need_k, bool need_q, bool need_sp)
+    {
+        const int ka = DR * 2 < 64 ? 64 : DR * 2;
+        const uint32_t tile_bytes = (uint32_t)(ka / 64) * 128u;   // per row of a K-major tile
+        uint32_t o = 0;
+        bimg = o; o = al(o + tile_bytes * (uint32_t)kn16);
+        abuf = o; o = al(o + tile_bytes * (uint32_t)C);
+        gk = o; if (need_k) o = al(o + 2u * C * 128u);
+        gq = o; if (need_q) o = al(o + 2u * C * 128u);
+        ve = o; if (need_k) o = al(o + (uint32_t)(d_v + 16) * C * 2u);
+        sp = o; if (need_sp) o = al(o + (uint32_t)(d_v + 16) * KMAX * 2u);
+        cst = o; o += KMAX * 4;
+        bars = o; o += 8 * 8;
+        tslot = o; o += 16;
+        total = o;
+    }
+};
+
+struct Bars {
+    uint64_t *bimg, *v, *mma, *mma2;
+};
+
+// Builds [x^2, x] (fp16, K-major SW128, ka columns) for token row `row` from its bf16 vector.
+template <int DR>
+__device__ __forceinline__ void build_a(uint8_t *abuf, int row, const uint4 (&x)[DR / 8])
+{
+    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
+#pragma unroll
+    for (int q = 0; q < KA / 8; ++q) {
+        uint4 v;
+        if (q < DR / 8) {
+            const bf16 *e = reinterpret_cast<const bf16 *>(&x[q]);
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+            v.x = pack_f16(f[0] * f[0], f[1] * f[1]);
+            v.y = pack_f16(f[2] * f[2], f[3] * f[3]);
+            v.z = pack_f16(f[4] * f[4], f[5] * f[5]);
+            v.w = pack_f16(f[6] * f[6], f[7] * f[7]);
+        } else if (q < DR / 4) {
+            const bf16 *e = reinterpret_cast<const bf16 *>(&x[q - DR / 8]);
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+            v.x = pack_f16(f[0], f[1]);
+            v.y = pack_f16(f[2], f[3]);
+            v.z = pack_f16(f[4], f[5]);
+            v.w = pack_f16(f[6], f[7]);
+        } else {
+            v = make_uint4(0, 0, 0, 0);
+        }
+        *reinterpret_cast<uint4 *>(abuf + sw128(row, q, C)) = v;
+    }
+}
+
+template <int DR>
+__device__ __forceinline__ void load_x(const bf16 *X, long long row, bool valid, uint4 (&x)[DR / 8])
+{
+#pragma unroll
+    for (int q = 0; q < DR / 8; ++q)
+        x[q] = valid ? __ldg(reinterpret_cast<const uint4 *>(X + row * DR) + q) : make_uint4(0, 0, 0, 0);
+}
+
+// Issues the logits MMA  L[tmem d] = A[abuf] * B[bimg]^T  (M = 128 tokens, N = kn16, K = ka).
+template <int DR>
+__device__ __forceinline__ void issue_logits(uint32_t d, uint32_t abuf, uint32_t bimg, int kn16)
+{
+    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
+    const uint32_t id = idesc_f16(128, (uint32_t)kn16, 0, 0, 0, 0);
+#pragma unroll
+    for (int s = 0; s < KA / 16; ++s) mma_f16(d, kdesc(abuf, s, C), kdesc(bimg, s, kn16), id, s > 0);
+}
+
+// Softmax over the K logits of this thread's TMEM row (log2 domain), in two passes over TMEM:
+// the row maximum first, then exp2(L - max) packed straight to bf16 pairs.  Writes the values
+// (unnormalised, or divided by their sum when `normalize`) into row `row` of the K-major SW128
+// tile `g`; invalid rows get zeros.  Returns the row sum of the unnormalised fp32 values.
+__device__ __noinline__ float softmax_row(uint32_t taddr, const float *cst_, int K, int row,
+                                             bool valid, bool normalize, uint8_t *g)
+{
+    // re-read the constants from shared memory in each pass instead of holding 128 registers
+    const volatile float *cst = cst_;
+    const int kc = (K + 31) >> 5;
+    float m = NEG_BIG;
+#pragma unroll
+    for (int c = 0; c < KMAX / 32; ++c) {
+        if (c < kc) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int k = c * 32 + j;
+                if (k < K) m = fmaxf(m, __uint_as_float(r[j]) + cst[k]);
+            }
+        }
+    }
+    float s = 0.f;
+    uint32_t pk[KMAX / 2];
+#pragma unroll
+    for (int c = 0; c < KMAX / 32; ++c) {
+        if (c < kc) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const int k = c * 32 + j;
+                const float e0 = k < K ? ex2(__uint_as_float(r[j]) + cst[k] - m) : 0.f;
+                const float e1 = k + 1 < K ? ex2(__uint_as_float(r[j + 1]) + cst[k + 1] - m) : 0.f;
+                s += e0 + e1;
+                pk[k / 2] = pack_bf16(e0, e1);
+            }
+        }
+    }
+    const bool rescale = normalize || !valid;
+    const float sc = valid ? 1.0f / s : 0.f;
+#pragma unroll
+    for (int c = 0; c < KMAX / 32; ++c) {
+        if (c < kc) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint32_t v = pk[c * 16 + q * 4 + u];
+                    if (rescale) {
+                        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&v);
+                        const float2 f = __bfloat1622float2(b);
+                        v = pack_bf16(f.x * sc, f.y * sc);
+                    }
+                    w[u] = v;
+                }
+                *reinterpret_cast<uint4 *>(g + sw128(row, c * 4 + q, C)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+    return s;
+}
+
+__device__ __forceinline__ void zero_region(uint8_t *p, uint32_t bytes)
+{
+    for (uint32_t o = threadIdx.x * 16; o < bytes; o += THREADS * 16)
+        *reinterpret_cast<uint4 *>(p + o) = make_uint4(0, 0, 0, 0);
+}
+
+// [V | 1]: fills the block of ones after the d_v/16 value blocks (all 16 columns are ones, so
+// every one of the 16 extra accumulator columns receives the normaliser).
+__device__ __forceinline__ void fill_ones(uint8_t *ve, int d_v)
+{
+    const uint32_t o0 = (uint32_t)(d_v / 16) * C * 32;
+    const uint32_t one2 = 0x3F803F80u;
+    for (uint32_t o = threadIdx.x * 16; o < (uint32_t)C * 32; o += THREADS * 16)
+        *reinterpret_cast<uint4 *>(ve + o0 + o) = make_uint4(one2, one2, one2, one2);
+}
+
+// TMA of V rows [tok, tok + 128) of slice bh into the MN-major SW32 blocks of `ve`.
+__device__ __forceinline__ void load_v_chunk(uint8_t *ve, const CUtensorMap *vmap, uint64_t *bar,
+                                             int d_v, int tok, int bh)
+{
+    mbar_arrive_expect_tx(bar, (uint32_t)(C * d_v * 2));
+    for (int b = 0; b < d_v / 16; ++b) {
+        // 3-D map {d_v, N, BH}, box {16, 128, 1}
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(ve + b * C * 32)),
+            "l"((uint64_t)vmap), "r"(smem_u32(bar)), "r"(b * 16), "r"(tok), "r"(bh)
+            : "memory");
+    }
+}
+
+// Reads this thread's row (component k) of the memory S from TMEM: ne fp32 columns, writes them
+// as bf16 into the MN-major SW32 B-operand tile `sp` (KMAX rows), and optionally to `out`.
+__device__ __forceinline__ void readout_state(uint32_t taddr, int ne, int k, uint8_t *sp, float *out)
+{
+    for (int b = 0; b < ne / 16; ++b) {
+        uint32_t r[16];
+        tmem_ld16(taddr + b * 16, r);
+        tmem_ld_wait();
+        if (sp) {
+            uint4 lo, hi;
+            lo.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
+            lo.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
+            lo.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
+            lo.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
+            hi.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
+            hi.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
+            hi.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
+            hi.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
+            *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
+            *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
+        }
+        if (out) {
+            float4 *o4 = reinterpret_cast<float4 *>(out + b * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                o4[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+    }
+}
+
+// Loads an fp32 memory row (ne columns) from global into TMEM (this thread's lane) and, as
+// bf16, into the SW32 tile `sp`.
+__device__ __forceinline__ void load_state(const float *src, uint32_t taddr, int ne, int k, uint8_t *sp)
+{
+    for (int b = 0; b < ne / 16; ++b) {
+        uint32_t r[16];
+        const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 f = s4[q];
+            r[4 * q] = __float_as_uint(f.x);
+            r[4 * q + 1] = __float_as_uint(f.y);
+            r[4 * q + 2] = __float_as_uint(f.z);
+            r[4 * q + 3] = __float_as_uint(f.w);
+        }
+        if (taddr != 0xFFFFFFFFu) tmem_st16(taddr + b * 16, r);
+        uint4 lo, hi;
+        lo.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
+        lo.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
+        lo.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
+        lo.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
+        hi.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
+        hi.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
+        hi.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
+        hi.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
+        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
+        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
+    }
+    if (taddr != 0xFFFFFFFFu) tmem_st_wait();
+}
+
+// Epilogue: O_i = num_i / (den_i + eps * s_i) from this thread's TMEM row (d_v numerator
+// columns, the normaliser in column d_v), stored to global row `orow` when valid.
+__device__ __forceinline__ void write_out(uint32_t taddr, int d_v, float eps_s, bool valid,
+                                          void *O, long long orow, int out_f32)
+{
+    uint32_t dr[16];
+    tmem_ld16(taddr + d_v, dr);
+    tmem_ld_wait();
+    const float inv = 1.0f / (__uint_as_float(dr[0]) + eps_s);
+    for (int b = 0; b < d_v / 16; ++b) {
+        uint32_t r[16];
+        tmem_ld16(taddr + b * 16, r);
+        tmem_ld_wait();
+        if (!valid) continue;
+        if (out_f32) {
+            float4 *o4 = reinterpret_cast<float4 *>((float *)O + orow * d_v + b * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                o4[q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                    __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+        } else {
+            uint4 lo, hi;
+            lo.x = pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+            lo.y = pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+            lo.z = pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+            lo.w = pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+            hi.x = pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
+            hi.y = pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
+            hi.z = pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
+            hi.w = pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
+            uint4 *o4 = reinterpret_cast<uint4 *>((bf16 *)O + orow * d_v + b * 16);
+            o4[0] = lo;
+            o4[1] = hi;
+        }
+    }
+}
+
+// Masked affinity row i: P_ij for j <= i (else 0), as bf16 into the K-major SW128 tile `ps`.
+__device__ __forceinline__ void mask_row(uint32_t taddr, int i, uint8_t *ps)
+{
+#pragma unroll
+    for (int c = 0; c < C / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int col = c * 32 + q * 8 + j;
+                f[j] = col <= i ? __uint_as_float(r[q * 8 + j]) : 0.f;
+            }
+            uint4 w;
+            w.x = pack_bf16(f[0], f[1]);
+            w.y = pack_bf16(f[2], f[3]);
+            w.z = pack_bf16(f[4], f[5]);
+            w.w = pack_bf16(f[6], f[7]);
+            *reinterpret_cast<uint4 *>(ps + sw128(i, c * 4 + q, C)) = w;
+        }
+    }
+}
+
+__device__ __forceinline__ void sync_tc()
+{
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// Everything written to shared memory by the CUDA cores becomes visible to the tensor cores.
+__device__ __forceinline__ void publish_smem()
+{
+    fence_proxy_async_smem();
+    sync_tc();
+}
+
+// Common CTA prologue: barriers, TMEM, Gaussian table and constants.
+__device__ __forceinline__ void cta_setup(uint8_t *smem, const Smem &L, Bars &bars, uint32_t ncols,
+                                          const Args &a, int h, uint32_t &tmem)
+{
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + L.bars);
+    bars.bimg = b;
+    bars.v = b + 1;
+    bars.mma = b + 2;
+    bars.mma2 = b + 3;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.tslot);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(b + i, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 32) tmem_alloc(tslot, ncols);
+    float *cst = reinterpret_cast<float *>(smem + L.cst);
+    for (int k = threadIdx.x; k < KMAX; k += THREADS) cst[k] = k < a.kn16 ? a.cst[(size_t)h * a.kn16 + k] : NEG_BIG;
+    sync_tc();
+    tmem = *tslot;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bars.bimg, (uint32_t)a.bimg_bytes);
+        bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars.bimg);
+    }
+}
+
+__device__ __forceinline__ void cta_teardown(uint32_t tmem, uint32_t ncols)
+{
+    sync_tc();
+    if (threadIdx.x < 32) tmem_dealloc(tmem, ncols);
+}
+
+// All threads wait; returns false on every thread if any of them timed out.
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase, WsHeader *hdr, unsigned where)
+{
+    const bool ok = mbar_wait(bar, phase, hdr, where);
+    phase ^= 1u;
+    return !__syncthreads_or(!ok);
+}
+
+// After a timed-out wait: give copies and MMAs still in flight a bounded chance to finish
+// before the CTA releases its tensor memory and exits.  (The phases passed are the ones the
+// abandoned waits were for; wait_all already flipped them, so flip back.)
+__device__ __forceinline__ void drain(const Bars &bars, bool v_pending, uint32_t ph_v,
+                                      bool mma_pending, uint32_t ph_m, WsHeader *hdr)
+{
+    if (v_pending) mbar_wait(bars.v, ph_v ^ 1u, hdr, 90);
+    if (mma_pending) mbar_wait(bars.mma, ph_m ^ 1u, hdr, 91);
+}
+
+// ================================================================== kernels
+
+// Per head: the Gaussian table B = log2e * [-w/2 ; mu w] (fp16, K-major SW128 image of kn16
+// rows) and c_k = log2e * (log pi_k - 1/2 sum_d (mu^2 w + log sigma^2)), padded components with
+// B = 0 and c = -1e30.  w = 1 / (softplus(raw) + floor), log pi = log softmax(logits).
+__global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restrict__ mu,
+                                                            const float *__restrict__ raw,
+                                                            const float *__restrict__ logits,
+                                                            uint8_t *__restrict__ bimg,
+                                                            float *__restrict__ cst, int K, int kn16,
+                                                            int d_r, int bimg_bytes, float floor_,
+                                                            WsHeader *hdr)
+{
+    const int h = blockIdx.x;
+    const int ka = d_r * 2 < 64 ? 64 : d_r * 2;
+    const float *lh = logits + (size_t)h * K;
+    __shared__ float red[THREADS];
+    float m = -INFINITY;
+    for (int k = threadIdx.x; k < K; k += THREADS) m = fmaxf(m, lh[k]);
+    red[threadIdx.x] = m;
+    __syncthreads();
+    for (int o = THREADS / 2; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + o]);
+        __syncthreads();
+    }
+    m = red[0];
+    __syncthreads();
+    float s = 0.f;
+    for (int k = threadIdx.x; k < K; k += THREADS) s += expf(lh[k] - m);
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = THREADS / 2; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+        __syncthreads();
+    }
+    const float lse = m + logf(red[0]);
+    uint8_t *img = bimg + (size_t)h * bimg_bytes;
+    for (int n = threadIdx.x; n < kn16; n += THREADS) {
+        const bool real = n < K;
+        float acc = 0.f;
+        bool range_ok = true;
+        for (int q = 0; q < ka / 8; ++q) {
+            uint16_t hv[8];
+            for (int j = 0; j < 8; ++j) {
+                const int f = q * 8 + j;
+                float val = 0.f;
+                if (real && f < 2 * d_r) {
+                    const int d = f < d_r ? f : f - d_r;
+                    const float r = raw[((size_t)h * K + n) * d_r + d];
+                    const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
+                    const float w = 1.0f / var;
+                    const float mv = mu[((size_t)h * K + n) * d_r + d];
+                    if (f < d_r) {
+                        val = -0.5f * w * LOG2E;
+                        acc += mv * mv * w + logf(var);
+                    } else {
+                        val = mv * w * LOG2E;
+                    }
+                    if (!(fabsf(val) < 65504.f)) range_ok = false;
+                }
+                __half hh = __float2half_rn(val);
+                hv[j] = *reinterpret_cast<uint16_t *>(&hh);
+            }
+            uint4 v;
+            v.x = hv[0] | ((uint32_t)hv[1] << 16);
+            v.y = hv[2] | ((uint32_t)hv[3] << 16);
+            v.z = hv[4] | ((uint32_t)hv[5] << 16);
+            v.w = hv[6] | ((uint32_t)hv[7] << 16);
+            const uint32_t off = (uint32_t)((q >> 3) * kn16 * 128 + n * 128 + (((q & 7) ^ (n & 7)) << 4));
+            *reinterpret_cast<uint4 *>(img + off) = v;
+        }
+        if (!range_ok) record_error(hdr, GMA_ERR_RANGE, 1u);
+        cst[(size_t)h * kn16 + n] = real ? ((lh[n] - lse) - 0.5f * acc) * LOG2E : NEG_BIG;
+    }
+}
+
+// Segment memories: agg[bh][seg] = sum over the segment's tokens of gamma_K^T [v, 1]
+// (KMAX x ne, fp32).  Used by both variants (the bidirectional one sums all segments).
+template <int DR>
+__global__ void __launch_bounds__(THREADS, 1) tc_segment_memory_kernel(const Args a,
+                                                                       const __grid_constant__ CUtensorMap vmap)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Smem L(DR, a.kn16, a.d_v, true, false, false);
+    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int tok0 = seg * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    const uint32_t R_L = 0, R_S = 128;
+    Bars bars;
+    uint32_t tmem;
+    uint32_t ph_b = 0, ph_v = 0, ph_m = 0;
+    zero_region(smem + L.gk, 2u * C * 128u);
+    fill_ones(smem + L.ve, a.d_v);
+    cta_setup(smem, L, bars, 512, a, h, tmem);
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t idesc_s = idesc_f16(128, (uint32_t)a.ne, 1, 1, 1, 1);
+    bool ok = wait_all(bars.bimg, ph_b, a.hdr, 10);
+    float *cst = reinterpret_cast<float *>(smem + L.cst);
+    uint4 x[DR / 8];
+    if (ok) load_x<DR>(a.KX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, x);
+    int nchunk = 0;
+    bool v_pending = false, mma_pending = false;
+    for (int base = tok0; ok && base < tok_end; base += C, ++nchunk) {
+        if (t == 0) load_v_chunk(smem + L.ve, &vmap, bars.v, a.d_v, base, bh);
+        v_pending = true;
+        build_a<DR>(smem + L.abuf, t, x);
+        publish_smem();
+        if (t == 0) {
+            issue_logits<DR>(tmem + R_L, sb + L.abuf, sb + L.bimg, a.kn16);
+            mma_commit(bars.mma);
+        }
+        mma_pending = true;
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 11))) break;
+        mma_pending = false;
+        softmax_row(tmem + lane_off + R_L, cst, a.K, t, base + t < tok_end, true, smem + L.gk);
+        const int nb = base + C;
+        load_x<DR>(a.KX, (long long)bh * a.N + nb + t, nb + t < tok_end, x);
+        publish_smem();
+        if (!(ok = wait_all(bars.v, ph_v, a.hdr, 12))) break;
+        v_pending = false;
+        if (t == 0) {
+            for (int s = 0; s < C / 16; ++s)
+                mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(sb + L.ve, s, C), idesc_s,
+                        (nchunk > 0 || s > 0) ? 1u : 0u);
+            mma_commit(bars.mma);
+        }
+        mma_pending = true;
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 13))) break;
+        mma_pending = false;
+    }
+    drain(bars, v_pending, ph_v, mma_pending, ph_m, a.hdr);
+    if (ok) {
+        float *dst = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + t) * a.ne;
+        if (nchunk == 0) {
+            for (int c = 0; c < a.ne; ++c) dst[c] = 0.f;
+        } else {
+            readout_state(tmem + lane_off + R_S, a.ne, t, nullptr, dst);
+        }
+    }
+    cta_teardown(tmem, 512);
+}
+
+// Causal: exclusive prefix of the segment memories within each slice (in place).
+// Bidirectional: the total over all segments, written to segment 0.
+__global__ void tc_scan_kernel(float *__restrict__ agg, long long total, int nseg, int KD, int causal)
+{
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const long long bh = idx / KD, e = idx % KD;
+    float *base = agg + bh * nseg * KD + e;
+    float run = 0.f;
+    for (int s = 0; s < nseg; ++s) {
+        const float v = base[(size_t)s * KD];
+        if (causal) base[(size_t)s * KD] = run;
+        run += v;
+    }
+    if (!causal) base[0] = run;
+}
+
+// Chunked causal forward for one segment, starting from the exclusive prefix memory.
+template <int DR>
+__global__ void __launch_bounds__(THREADS, 1) tc_causal_chunked_kernel(const Args a,
+                                                                       const __grid_constant__ CUtensorMap vmap)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Smem L(DR, a.kn16, a.d_v, true, true, true);
+    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int tok0 = seg * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    const uint32_t R_L = 0, R_O = 128, R_S = 288;    // L_K then P | L_Q then O | S
+    Bars bars;
+    uint32_t tmem;
+    uint32_t ph_b = 0, ph_v = 0, ph_m = 0, ph_m2 = 0;
+    zero_region(smem + L.gk, 2u * C * 128u);
+    fill_ones(smem + L.ve, a.d_v);
+    cta_setup(smem, L, bars, 512, a, h, tmem);
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t id_p = idesc_f16(128, 128, 1, 1, 0, 0);
+    const uint32_t id_o = idesc_f16(128, (uint32_t)a.ne, 1, 1, 0, 1);
+    const uint32_t id_s = idesc_f16(128, (uint32_t)a.ne, 1, 1, 1, 1);
+    float *cst = reinterpret_cast<float *>(smem + L.cst);
+    // the segment's starting memory: TMEM (fp32, accumulated further) and bf16 operand copy
+    load_state(a.agg + (((size_t)bh * a.nseg + seg) * KMAX + t) * a.ne, tmem + lane_off + R_S, a.ne,
+               t, smem + L.sp);
+    bool ok = wait_all(bars.bimg, ph_b, a.hdr, 20);
+    uint4 xk[DR / 8], xq[DR / 8];
+    if (ok) {
+        load_x<DR>(a.KX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, xk);
+        load_x<DR>(a.QX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, xq);
+    }
+    bool v_pending = false, mma_pending = false;
+    for (int base = tok0; ok && base < tok_end; base += C) {
+        const bool valid = base + t < tok_end;
+        if (t == 0) load_v_chunk(smem + L.ve, &vmap, bars.v, a.d_v, base, bh);
+        v_pending = true;
+        // keys: logits -> Gamma_K
+        build_a<DR>(smem + L.abuf, t, xk);
+        publish_smem();
+        if (t == 0) {
+            issue_logits<DR>(tmem + R_L, sb + L.abuf, sb + L.bimg, a.kn16);
+            mma_commit(bars.mma);
+        }
+        mma_pending = true;
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 21))) break;
+        mma_pending = false;
+        // queries: logits (tensor cores) while the CUDA cores turn the key logits into Gamma_K
+        build_a<DR>(smem + L.abuf, t, xq);
+        publish_smem();
+        if (t == 0) {
+            issue_logits<DR>(tmem + R_O, sb + L.abuf, sb + L.bimg, a.kn16);
+            mma_commit(bars.mma2);
+        }
+        softmax_row(tmem + lane_off + R_L, cst, a.K, t, valid, true, smem + L.gk);
+        if (!(ok = wait_all(bars.mma2, ph_m2, a.hdr, 22))) {
+            mbar_wait(bars.mma2, ph_m2 ^ 1u, a.hdr, 92);   // bounded drain of the query logits
+            break;
+        }
+        const float srow = softmax_row(tmem + lane_off + R_O, cst, a.K, t, valid, false, smem + L.gq);
+        const int nb = base + C;   // next chunk's routing vectors, in flight behind the MMAs
+        load_x<DR>(a.KX, (long long)bh * a.N + nb + t, nb + t < tok_end, xk);
+        load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, xq);
+        publish_smem();
+        if (!(ok = wait_all(bars.v, ph_v, a.hdr, 23))) break;
+        v_pending = false;
+        if (t == 0) {
+            const uint32_t gq = sb + L.gq, gk = sb + L.gk, ve = sb + L.ve, sp = sb + L.sp;
+            for (int s = 0; s < a.kn16 / 16; ++s)   // P = Gamma_Q Gamma_K^T
+                mma_f16(tmem + R_L, kdesc(gq, s, C), kdesc(gk, s, C), id_p, s > 0);
+            for (int s = 0; s < a.kn16 / 16; ++s)   // O = Gamma_Q [S | Z]_{c-1}
+                mma_f16(tmem + R_O, kdesc(gq, s, C), mn32desc(sp, s, KMAX), id_o, s > 0);
+            for (int s = 0; s < C / 16; ++s)         // S += Gamma_K^T [V | 1]
+                mma_f16(tmem + R_S, mn128desc(gk, s, C), mn32desc(ve, s, C), id_s, 1u);
+            mma_commit(bars.mma);
+        }
+        mma_pending = true;
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 24))) break;
+        mma_pending = false;
+        mask_row(tmem + lane_off + R_L, t, smem + L.gq);                     // P -> bf16, j <= i
+        readout_state(tmem + lane_off + R_S, a.ne, t, smem + L.sp, nullptr);  // S_c for the next chunk
+        publish_smem();
+        if (t == 0) {
+            for (int s = 0; s < C / 16; ++s)         // O += tril(P) [V | 1]
+                mma_f16(tmem + R_O, kdesc(sb + L.gq, s, C), mn32desc(sb + L.ve, s, C), id_o, 1u);
+            mma_commit(bars.mma);
+        }
+        mma_pending = true;
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 25))) break;
+        mma_pending = false;
+        write_out(tmem + lane_off + R_O, a.d_v, a.eps * srow, valid, a.O, (long long)bh * a.N + base + t,
+                  a.out_f32);
+        sync_tc();
+    }
+    drain(bars, v_pending, ph_v, mma_pending, ph_m, a.hdr);
+    cta_teardown(tmem, 512);
+}
+
+// Bidirectional read: O = Gamma_Q [V~ | Z] / (.. + eps) for `cps` chunks of one slice.
+template <int DR>
+__global__ void __launch_bounds__(THREADS, 1) tc_bidir_read_kernel(const Args a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Smem L(DR, a.kn16, a.d_v, false, true, true);
+    const int ntile = a.nseg;   // tile groups per slice
+    const int bh = blockIdx.x / ntile, grp = blockIdx.x % ntile, h = bh % a.H;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int tok0 = grp * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    const uint32_t R_O = 0;
+    Bars bars;
+    uint32_t tmem;
+    uint32_t ph_b = 0, ph_m = 0;
+    cta_setup(smem, L, bars, 256, a, h, tmem);
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t id_o = idesc_f16(128, (uint32_t)a.ne, 1, 1, 0, 1);
+    float *cst = reinterpret_cast<float *>(smem + L.cst);
+    // the slice's total memory (segment 0 after the scan), bf16 operand only
+    load_state(a.agg + ((size_t)bh * a.nseg * KMAX + t) * a.ne, 0xFFFFFFFFu, a.ne, t, smem + L.sp);
+    bool ok = wait_all(bars.bimg, ph_b, a.hdr, 30);
+    uint4 xq[DR / 8];
+    if (ok) load_x<DR>(a.QX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, xq);
+    for (int base = tok0; ok && base < tok_end; base += C) {
+        const bool valid = base + t < tok_end;
+        build_a<DR>(smem + L.abuf, t, xq);
+        publish_smem();
+        if (t == 0) {
+            issue_logits<DR>(tmem + R_O, sb + L.abuf, sb + L.bimg, a.kn16);
+            mma_commit(bars.mma);
+        }
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 31))) break;
+        const float srow = softmax_row(tmem + lane_off + R_O, cst, a.K, t, valid, false, smem + L.gq);
+        const int nb = base + C;
+        load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, xq);
+        publish_smem();
+        if (t == 0) {
+            for (int s = 0; s < a.kn16 / 16; ++s)
+                mma_f16(tmem + R_O, kdesc(sb + L.gq, s, C), mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
+            mma_commit(bars.mma);
+        }
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 32))) break;
+        write_out(tmem + lane_off + R_O, a.d_v, a.eps * srow, valid, a.O, (long long)bh * a.N + base + t,
+                  a.out_f32);
+        sync_tc();
+    }
+    cta_teardown(tmem, 256);
+}
+
+// Responsibilities only: gamma rows (normalised) straight from registers to global memory.
+template <int DR>
+__global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Smem L(DR, a.kn16, 16, false, true, false);
+    const int ntile = a.nseg;
+    const int bh = blockIdx.x / ntile, grp = blockIdx.x % ntile, h = bh % a.H;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int tok0 = grp * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    Bars bars;
+    uint32_t tmem;
+    uint32_t ph_b = 0, ph_m = 0;
+    cta_setup(smem, L, bars, 128, a, h, tmem);
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t sb = smem_u32(smem);
+    float *cst = reinterpret_cast<float *>(smem + L.cst);
+    bool ok = wait_all(bars.bimg, ph_b, a.hdr, 40);
+    uint4 x[DR / 8];
+    if (ok) load_x<DR>(a.QX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, x);
+    const int kc = (a.K + 31) >> 5;
+    for (int base = tok0; ok && base < tok_end; base += C) {
+        const bool valid = base + t < tok_end;
+        build_a<DR>(smem + L.abuf, t, x);
+        publish_smem();
+        if (t == 0) {
+            issue_logits<DR>(tmem, sb + L.abuf, sb + L.bimg, a.kn16);
+            mma_commit(bars.mma);
+        }
+        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 41))) break;
+        const int nb = base + C;
+        load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, x);
+        // softmax in registers, then store K values of this row
+        float v[KMAX];
+        float m = NEG_BIG;
+#pragma unroll
+        for (int c = 0; c < KMAX / 32; ++c) {
+            if (c < kc) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + c * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int k = c * 32 + j;
+                    v[k] = k < a.K ? __uint_as_float(r[j]) + cst[k] : NEG_BIG;
+                    m = fmaxf(m, v[k]);
+                }
+            }
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            if ((k >> 5) < kc) {
+                v[k] = k < a.K ? ex2(v[k] - m) : 0.f;
+                s += v[k];
+            }
+        }
+        const float inv = 1.0f / s;
+        if (valid) {
+            const long long row = (long long)bh * a.N + base + t;
+            if (a.out_f32) {
+                float *g = (float *)a.gamma + row * a.K;
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k)
+                    if (k < a.K) g[k] = v[k] * inv;
+            } else {
+                bf16 *g = (bf16 *)a.gamma + row * a.K;
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k)
+                    if (k < a.K) g[k] = __float2bfloat16_rn(v[k] * inv);
+            }
+        }
+        sync_tc();
+    }
+    cta_teardown(tmem, 128);
+}
+
+// ================================================================== host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    });
+    return fn;
+}
+
+// 3-D map over V [BH][N][d_v] bf16: dims {d_v, N, BH}, box {16, 128, 1}, 32-byte swizzle.
+bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d_v, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d_v * 2, (cuuint64_t)N * d_v * 2};
+    cuuint32_t box[3] = {16, (cuuint32_t)C, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(V), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int kn16, ne, ka, bimg_bytes;
+    int nseg, cps;              // forward: segments per slice and chunks per segment
+    size_t off_bimg, off_cst, off_agg, total;
+};
+
+constexpr int kTargetCtas = 152 * 4;
+
+Plan make_plan(const gma_shape_t &s, int variant)
+{
+    Plan p{};
+    p.kn16 = (s.K + 15) / 16 * 16;
+    p.ne = s.d_v + 16;
+    p.ka = s.d_r * 2 < 64 ? 64 : s.d_r * 2;
+    p.bimg_bytes = p.ka / 64 * 128 * p.kn16;
+    const int BH = s.B * s.H;
+    const int nchunks = (s.N + C - 1) / C;
+    int nseg = (kTargetCtas + BH - 1) / BH;
+    if (nseg > nchunks) nseg = nchunks;
+    if (nseg < 1) nseg = 1;
+    p.cps = (nchunks + nseg - 1) / nseg;
+    p.nseg = (nchunks + p.cps - 1) / p.cps;
+    Carve c;
+    p.off_bimg = c.take((size_t)s.H * p.bimg_bytes);
+    p.off_cst = c.take(sizeof(float) * (size_t)s.H * p.kn16);
+    if (variant != GMA_VARIANT_RESPONSIBILITIES)
+        p.off_agg = c.take(sizeof(float) * (size_t)BH * p.nseg * KMAX * p.ne);
+    p.total = c.total();
+    return p;
+}
+
+Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
+{
+    Args a{};
+    a.bimg = (const uint8_t *)(ws + p.off_bimg);
+    a.cst = (const float *)(ws + p.off_cst);
+    a.agg = p.off_agg ? (float *)(ws + p.off_agg) : nullptr;
+    a.hdr = (WsHeader *)ws;
+    a.H = s.H;
+    a.N = s.N;
+    a.K = s.K;
+    a.kn16 = p.kn16;
+    a.d_v = s.d_v;
+    a.ne = p.ne;
+    a.nseg = p.nseg;
+    a.cps = p.cps;
+    a.bimg_bytes = p.bimg_bytes;
+    a.eps = s.eps;
+    a.out_f32 = (s.flags & GMA_FLAG_OUT_F32) ? 1 : 0;
+    return a;
+}
+
+// Dynamic shared memory for a kernel that allocates `tmem_cols` TMEM columns: at least enough
+// that no more CTAs fit on one SM (228 KB of shared memory) than its 512 columns can serve,
+// so no CTA ever waits inside tcgen05.alloc for a co-resident CTA.
+uint32_t smem_for(uint32_t need, uint32_t tmem_cols)
+{
+    const uint32_t per_sm = 228u * 1024u;
+    const uint32_t ctas = 512u / tmem_cols;              // CTAs the TMEM can hold at once
+    const uint32_t floor_ = per_sm / (ctas + 1) + 1024u; // one more would not fit
+    return need > floor_ ? need : floor_;
+}
+
+template <typename KernelT>
+bool set_smem(KernelT kernel, uint32_t bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
+}
+
+gma_status_t launch_params(const gma_shape_t &s, const Plan &p, char *ws, const float *mu,
+                           const float *raw, const float *logits, cudaStream_t st)
+{
+    GMA_LAUNCH(KID_TC_PARAMS, st,
+               (tc_params_kernel<<<s.H, THREADS, 0, st>>>(mu, raw, logits, (uint8_t *)(ws + p.off_bimg),
+                                                          (float *)(ws + p.off_cst), s.K, p.kn16, s.d_r,
+                                                          p.bimg_bytes, s.var_floor, (WsHeader *)ws)));
+    return GMA_OK;
+}
+
+template <int DR>
+gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+                        const void *V, void *O, char *ws, const Plan &p, cudaStream_t st)
+{
+    Args a = make_args(s, p, ws);
+    a.QX = (const bf16 *)QX;
+    a.KX = (const bf16 *)KX;
+    a.O = O;
+    const int BH = s.B * s.H;
+    CUtensorMap vmap;
+    if (!make_vmap(&vmap, V, BH, s.N, s.d_v)) return GMA_ERR_CUDA;
+    const uint32_t sm_seg = smem_for(Smem(DR, p.kn16, s.d_v, true, false, false).total + 1024, 512);
+    if (!set_smem(tc_segment_memory_kernel<DR>, sm_seg)) return GMA_ERR_CUDA;
+    GMA_LAUNCH(KID_TC_CAUSAL_AGG, st,
+               (tc_segment_memory_kernel<DR><<<BH * p.nseg, THREADS, sm_seg, st>>>(a, vmap)));
+    const int KD = KMAX * p.ne;
+    const long long tot = (long long)BH * KD;
+    GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st,
+               (tc_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(a.agg, tot, p.nseg, KD,
+                                                                               causal ? 1 : 0)));
+    if (causal) {
+        const uint32_t sm = smem_for(Smem(DR, p.kn16, s.d_v, true, true, true).total + 1024, 512);
+        if (!set_smem(tc_causal_chunked_kernel<DR>, sm)) return GMA_ERR_CUDA;
+        GMA_LAUNCH(KID_TC_CAUSAL_OUT, st,
+                   (tc_causal_chunked_kernel<DR><<<BH * p.nseg, THREADS, sm, st>>>(a, vmap)));
+    } else {
+        const uint32_t sm = smem_for(Smem(DR, p.kn16, s.d_v, false, true, true).total + 1024, 256);
+        if (!set_smem(tc_bidir_read_kernel<DR>, sm)) return GMA_ERR_CUDA;
+        GMA_LAUNCH(KID_TC_BIDIR_READ, st, (tc_bidir_read_kernel<DR><<<BH * p.nseg, THREADS, sm, st>>>(a)));
+    }
+    return GMA_OK;
+}
+
+template <int DR>
+gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws, const Plan &p,
+                     cudaStream_t st)
+{
+    Args a = make_args(s, p, ws);
+    a.QX = (const bf16 *)X;
+    a.gamma = gamma;
+    const uint32_t sm = smem_for(Smem(DR, p.kn16, 16, false, true, false).total + 1024, 128);
+    if (!set_smem(tc_resp_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    GMA_LAUNCH(KID_TC_RESP, st, (tc_resp_kernel<DR><<<s.B * s.H * p.nseg, THREADS, sm, st>>>(a)));
+    return GMA_OK;
+}
+
+}  // namespace tck
+
+// ------------------------------------------------------------------ family entry points
+bool tc_supported(const gma_shape_t &s, int variant)
+{
+    if (s.dtype != GMA_BF16 || (s.flags & GMA_FLAG_SIMT)) return false;
+    if (!(s.d_r == 16 || s.d_r == 32 || s.d_r == 64)) return false;
+    if (s.K > tck::KMAX) return false;
+    (void)variant;
+    return tck::encode_fn() != nullptr;
+}
+
+size_t tc_workspace_size(const gma_shape_t &s, int variant) { return tck::make_plan(s, variant).total; }
+
+gma_status_t tc_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
+                                 const float *raw, const float *logits, void *gamma, void *ws,
+                                 cudaStream_t st)
+{
+    const tck::Plan p = tck::make_plan(s, GMA_VARIANT_RESPONSIBILITIES);
+    char *w = (char *)ws;
+    gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
+    if (r != GMA_OK) return r;
+    switch (s.d_r) {
+    case 16: return tck::resp_dr<16>(s, X, gamma, w, p, st);
+    case 32: return tck::resp_dr<32>(s, X, gamma, w, p, st);
+    case 64: return tck::resp_dr<64>(s, X, gamma, w, p, st);
+    }
+    return GMA_ERR_UNSUPPORTED_SHAPE;
+}
+
+gma_status_t tc_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+                        const void *V, const float *mu, const float *raw, const float *logits,
+                        void *O, void *ws, cudaStream_t st)
+{
+    const tck::Plan p = tck::make_plan(s, causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL);
+    char *w = (char *)ws;
+    gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
+    if (r != GMA_OK) return r;
+    switch (s.d_r) {
+    case 16: return tck::forward_dr<16>(s, causal, QX, KX, V, O, w, p, st);
+    case 32: return tck::forward_dr<32>(s, causal, QX, KX, V, O, w, p, st);
+    case 64: return tck::forward_dr<64>(s, causal, QX, KX, V, O, w, p, st);
+    }
+    return GMA_ERR_UNSUPPORTED_SHAPE;
+}
+
+}  // namespace gma
