@@ -112,6 +112,28 @@ gma_status_t gma_forward_causal(const gma_shape_t *shape, const void *QX, const 
                                 const float *prior_logits, void *O, void *workspace,
                                 size_t workspace_bytes, gma_stream_t stream);
 
+/* Causal GMA for callers that cannot allocate device memory.  The page has no counterpart to
+ * this entry point: it exists for callers such as allocator or memory-pool callbacks, plugins
+ * whose host application owns every device allocation, or loops that must not call cudaMalloc
+ * after start-up, which can pass inputs and outputs but no workspace.
+ *   - Computes exactly what gma_forward_causal computes, with the same arguments minus the
+ *     workspace, which comes from a fixed array of GMA_NOALLOC_SCRATCH_BYTES inside the library's
+ *     device image.  Every GPU that loads libgma.so holds that array until the process exits.
+ *   - A shape whose gma_workspace_size(shape, GMA_VARIANT_CAUSAL) exceeds
+ *     GMA_NOALLOC_SCRATCH_BYTES returns GMA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device (with that device current) looks up the array's device
+ *     address once; make that first call before any stream capture.  No call allocates or frees
+ *     memory (no cudaMalloc, cudaFree or allocating library routine).
+ *   - All calls on a device share the one array, which keeps the last call's contents; the call
+ *     clears what must start at zero.  Calls that overlap on the GPU (other streams, other host
+ *     threads) race on the array: order them on one stream or with events.
+ *   - Device-side conditions are recorded in the array's header, which this entry point does not
+ *     report; argument, shape and launch errors are returned as usual. */
+#define GMA_NOALLOC_SCRATCH_BYTES (32u << 20)
+gma_status_t gma_forward_causal_noalloc(const gma_shape_t *shape, const void *QX, const void *KX,
+                                        const void *V, const float *mu, const float *raw_var,
+                                        const float *prior_logits, void *O, gma_stream_t stream);
+
 /* Waits for `stream`, then returns the condition the device recorded in `workspace` during the
  * last call that used it (GMA_OK if none), or GMA_ERR_CUDA if the stream reported an error. */
 gma_status_t gma_check_workspace(const void *workspace, gma_stream_t stream);

@@ -1,0 +1,64 @@
+// gma_noalloc.cu -- gma_forward_causal_noalloc: the causal forward pass for callers that cannot
+// allocate device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocator) at the point where they run GMA: code
+// inside a custom allocator or memory-pool callback, a plugin whose host application owns every
+// device allocation, or a real-time loop that must not touch the allocator after start-up.  They
+// can still pass their inputs and outputs, but not a workspace.  This entry point supplies the
+// workspace itself from a fixed-size array that lives in the library's device image.
+//
+// The array is a file-scope __device__ variable: every GPU that loads this library holds
+// GMA_NOALLOC_SCRATCH_BYTES of it until the process exits.  Host code cannot use the array's
+// name as a device address (in host code the name is only a host-side stand-in), so the first
+// call on each device, with that device current, asks the runtime for the array's device
+// address with cudaGetSymbolAddress and caches it.
+#include <mutex>
+
+#include "gma_internal.cuh"
+
+namespace {
+
+constexpr size_t kScratchBytes = (size_t)GMA_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+std::mutex g_setup_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of this device's copy of the scratch array, looked up once per device.
+gma_status_t scratch_for_current_device(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_NO_DEVICE;
+    if (dev < 0 || dev >= kMaxDevices) return GMA_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return GMA_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return GMA_OK;
+}
+
+}  // namespace
+
+extern "C" gma_status_t gma_forward_causal_noalloc(const gma_shape_t *shape, const void *QX,
+                                                   const void *KX, const void *V,
+                                                   const float *mu, const float *raw_var,
+                                                   const float *prior_logits, void *O,
+                                                   gma_stream_t stream)
+{
+    const size_t need = gma_workspace_size(shape, GMA_VARIANT_CAUSAL);
+    if (need == 0)   // invalid shape: the regular entry point names the error, enqueuing nothing
+        return gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, nullptr, 0,
+                                  stream);
+    if (need > kScratchBytes) return GMA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    const gma_status_t r = scratch_for_current_device(&scratch);
+    if (r != GMA_OK) return r;
+    return gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, scratch,
+                              kScratchBytes, stream);
+}

@@ -50,6 +50,8 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         fn.restype = ctypes.c_int
+    lib.gma_forward_causal_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.gma_forward_causal_noalloc.restype = ctypes.c_int
     lib.gma_check_workspace.argtypes = [vp, vp]
     lib.gma_check_workspace.restype = ctypes.c_int
     lib.gma_kernel_family.argtypes = [sp, ctypes.c_int]
@@ -104,6 +106,14 @@ def gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, workspace
                        workspace_bytes, stream):
     return int(_lib.gma_forward_causal(ctypes.byref(shape), QX, KX, V, mu, raw_var,
                                        prior_logits, O, workspace, int(workspace_bytes), stream))
+
+
+GMA_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def gma_forward_causal_noalloc(shape, QX, KX, V, mu, raw_var, prior_logits, O, stream):
+    return int(_lib.gma_forward_causal_noalloc(ctypes.byref(shape), QX, KX, V, mu, raw_var,
+                                               prior_logits, O, stream))
 
 
 def gma_check_workspace(workspace, stream):
