@@ -91,6 +91,26 @@ def kernel_work(w, name):
     return "hbm", 0, "GB/s"
 
 
+def traffic_per_launch(kernel, w):
+    """DRAM bytes (read + write) of one launch of `kernel` on workload `w`, from the committed
+    ncu summary profiles/dram_traffic.json (captured per token-head on a smaller case of the same
+    kernel, scaled by the units one launch processes); None when no capture exists or the
+    kernel's source changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+        return None
+    if rec.get("workload_shape") != [w.d_r, w.K, w.d_v, w.dtype, w.causal]:
+        return None
+    return rec["dram_bytes_per_token_head"] * w.token_heads
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -205,7 +225,10 @@ def run_gma(args, ws, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     w0 = W.by_name(args.workload)
-    w = W.Workload(**{**w0.__dict__, "seed": w0.seed + 1000 * rank})
+    over = {"seed": w0.seed + 1000 * rank}
+    if args.heads:
+        over["H"] = args.heads
+    w = W.Workload(**{**w0.__dict__, **over})
     host = W.make_inputs(w)
     dev = {k: v.to(device) for k, v in host.items()}
     shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v,
@@ -303,6 +326,9 @@ def run_gma(args, ws, rank, local):
                      "frac": round(roof_s / step_s, 4),
                      "alg_bytes": step_bytes, "alg_flops": step_flops}
 
+    traffic = traffic_per_launch(dom, w)
+    roofline["traffic"] = traffic
+
     # end to end through the C ABI with pinned host buffers
     e2e_steps = max(3, min(steps, 10))
     pin = {k: host[k].pin_memory() for k in ("QX", "KX", "V", "mu", "raw", "logits")}
@@ -316,21 +342,23 @@ def run_gma(args, ws, rank, local):
         step()
         O_host.copy_(O, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        e2e_step()
-    stream.synchronize()
-    barrier(ws)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        for _ in range(e2e_steps):
+    e2e = None
+    if not args.no_e2e:
+        with torch.cuda.stream(stream):
             e2e_step()
-        b.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
-    e2e_ms = max_over_ranks(a.elapsed_time(b), ws, device)
-    e2e = {"value": w.tokens * ws * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+        stream.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), ws, device)
+        e2e = {"value": w.tokens * ws * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
     if rank != 0:
         return None
@@ -409,6 +437,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="profiling only: run the workload with this many heads instead")
     args = ap.parse_args()
 
     if args.impl == "reference":
