@@ -34,84 +34,12 @@
 #include <cuda.h>
 #include <mutex>
 
-#include "gma_internal.cuh"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace gma {
 namespace tck {
 
 using namespace tc;
-
-constexpr int C = 128;          // tokens per chunk (the MMA M dimension)
-constexpr int THREADS = 128;    // one thread per TMEM lane / token row / component row
-constexpr int KMAX = 128;       // components handled by this family
-constexpr float LOG2E = 1.4426950408889634f;
-constexpr float NEG_BIG = -1.0e30f;
-
-typedef __nv_bfloat16 bf16;
-
-struct Args {
-    const bf16 *QX, *KX;
-    void *O;                 // output (bf16 or fp32)
-    void *gamma;             // responsibilities output (bf16 or fp32)
-    const uint8_t *bimg;     // per-head Gaussian table image [H][bimg_bytes]
-    const float *cst;        // per-head log2-domain constants [H][kn16]
-    float *agg;              // segment memories [BH][nseg][KMAX][ne] fp32
-    WsHeader *hdr;
-    int H, N, K, kn16, d_v, ne;
-    int nseg, cps;           // segments per slice, chunks per segment
-    int bimg_bytes;
-    float eps;
-    int out_f32;
-};
-
-// ------------------------------------------------------------------ layout helpers
-__device__ __forceinline__ uint32_t sw128(int row, int q, int rows)
-{
-    return (uint32_t)((q >> 3) * rows * 128 + row * 128 + (((q & 7) ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ uint32_t sw32(int row, int blk, int half, int rows)
-{
-    return (uint32_t)(blk * rows * 32 + row * 32 + ((half ^ ((row >> 2) & 1)) << 4));
-}
-
-// K-major SW128 operand, k-step s (16 elements)
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int s, int rows)
-{
-    return smem_desc(base + (uint32_t)((s >> 2) * rows * 128 + (s & 3) * 32), 16, 1024, SW_128B);
-}
-
-// MN-major SW128 operand whose K dimension runs along rows (128 B each), k-step s.
-__device__ __forceinline__ uint64_t mn128desc(uint32_t base, int s, int rows)
-{
-    return smem_desc(base + (uint32_t)(s * 16 * 128), (uint32_t)(rows * 128), 1024, SW_128B);
-}
-
-// MN-major SW32 operand (blocks of 16 MN elements), k-step s.
-__device__ __forceinline__ uint64_t mn32desc(uint32_t base, int s, int rows)
-{
-    return smem_desc(base + (uint32_t)(s * 16 * 32), (uint32_t)(rows * 32), 256, SW_32B);
-}
-
-__device__ __forceinline__ float ex2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
-{
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float a, float b)
-{
-    __half2 v = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
 
 // Shared-memory plan of one CTA.  Regions are 1 KB aligned.
 struct Smem {
@@ -122,7 +50,7 @@ struct Smem {
         const int ka = DR * 2 < 64 ? 64 : DR * 2;
         const uint32_t tile_bytes = (uint32_t)(ka / 64) * 128u;   // per row of a K-major tile
         uint32_t o = 0;
-        bimg = o; o = al(o + tile_bytes * (uint32_t)kn16);
+        bimg = o; o = al(o + tile_bytes * (uint32_t)kn16 + 32u * (uint32_t)kn16);
         abuf = o; o = al(o + tile_bytes * (uint32_t)C);
         gk = o; if (need_k) o = al(o + 2u * C * 128u);
         gq = o; if (need_q) o = al(o + 2u * C * 128u);
@@ -138,47 +66,6 @@ struct Smem {
 struct Bars {
     uint64_t *bimg, *v, *mma, *mma2;
 };
-
-// Builds [x^2, x] (fp16, K-major SW128, ka columns) for token row `row` from its bf16 vector.
-template <int DR>
-__device__ __forceinline__ void build_a(uint8_t *abuf, int row, const uint4 (&x)[DR / 8])
-{
-    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
-#pragma unroll
-    for (int q = 0; q < KA / 8; ++q) {
-        uint4 v;
-        if (q < DR / 8) {
-            const bf16 *e = reinterpret_cast<const bf16 *>(&x[q]);
-            float f[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
-            v.x = pack_f16(f[0] * f[0], f[1] * f[1]);
-            v.y = pack_f16(f[2] * f[2], f[3] * f[3]);
-            v.z = pack_f16(f[4] * f[4], f[5] * f[5]);
-            v.w = pack_f16(f[6] * f[6], f[7] * f[7]);
-        } else if (q < DR / 4) {
-            const bf16 *e = reinterpret_cast<const bf16 *>(&x[q - DR / 8]);
-            float f[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
-            v.x = pack_f16(f[0], f[1]);
-            v.y = pack_f16(f[2], f[3]);
-            v.z = pack_f16(f[4], f[5]);
-            v.w = pack_f16(f[6], f[7]);
-        } else {
-            v = make_uint4(0, 0, 0, 0);
-        }
-        *reinterpret_cast<uint4 *>(abuf + sw128(row, q, C)) = v;
-    }
-}
-
-template <int DR>
-__device__ __forceinline__ void load_x(const bf16 *X, long long row, bool valid, uint4 (&x)[DR / 8])
-{
-#pragma unroll
-    for (int q = 0; q < DR / 8; ++q)
-        x[q] = valid ? __ldg(reinterpret_cast<const uint4 *>(X + row * DR) + q) : make_uint4(0, 0, 0, 0);
-}
 
 // Issues the logits MMA  L[tmem d] = A[abuf] * B[bimg]^T  (M = 128 tokens, N = kn16, K = ka).
 template <int DR>
@@ -271,21 +158,6 @@ __device__ __forceinline__ void fill_ones(uint8_t *ve, int d_v)
     const uint32_t one2 = 0x3F803F80u;
     for (uint32_t o = threadIdx.x * 16; o < (uint32_t)C * 32; o += THREADS * 16)
         *reinterpret_cast<uint4 *>(ve + o0 + o) = make_uint4(one2, one2, one2, one2);
-}
-
-// TMA of V rows [tok, tok + 128) of slice bh into the MN-major SW32 blocks of `ve`.
-__device__ __forceinline__ void load_v_chunk(uint8_t *ve, const CUtensorMap *vmap, uint64_t *bar,
-                                             int d_v, int tok, int bh)
-{
-    mbar_arrive_expect_tx(bar, (uint32_t)(C * d_v * 2));
-    for (int b = 0; b < d_v / 16; ++b) {
-        // 3-D map {d_v, N, BH}, box {16, 128, 1}
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(ve + b * C * 32)),
-            "l"((uint64_t)vmap), "r"(smem_u32(bar)), "r"(b * 16), "r"(tok), "r"(bh)
-            : "memory");
-    }
 }
 
 // Reads this thread's row (component k) of the memory S from TMEM: ne fp32 columns, writes them
@@ -478,16 +350,20 @@ __device__ __forceinline__ void drain(const Bars &bars, bool v_pending, uint32_t
 
 // ================================================================== kernels
 
-// Per head: the Gaussian table B = log2e * [-w/2 ; mu w] (fp16, K-major SW128 image of kn16
-// rows) and c_k = log2e * (log pi_k - 1/2 sum_d (mu^2 w + log sigma^2)), padded components with
-// B = 0 and c = -1e30.  w = 1 / (softplus(raw) + floor), log pi = log softmax(logits).
+// Per head h (grid.x) and group of 16 components (grid.y): the Gaussian table (main part
+// log2e * [-w/2 ; mu w] as fp16, K-major SW128, kn16 rows; const part (c_hi, c_lo) with
+// c_hi + c_lo = c_k = log2e * (log pi_k - 1/2 sum_d (mu^2 w + log sigma^2)), K-major SW32) and
+// the fp32 constants cst[h][k] = c_k.  w = 1 / (softplus(raw) + floor), log pi = log softmax.
+// Padded components (k >= K) get zero rows.  Values beyond fp16 range are reported as
+// GMA_ERR_RANGE.  Each component is handled by 8 consecutive threads, one 16-byte feature chunk
+// at a time; their partial sums meet through warp shuffles.
 __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restrict__ mu,
                                                             const float *__restrict__ raw,
                                                             const float *__restrict__ logits,
                                                             uint8_t *__restrict__ bimg,
                                                             float *__restrict__ cst, int K, int kn16,
-                                                            int d_r, int bimg_bytes, float floor_,
-                                                            WsHeader *hdr)
+                                                            int d_r, int bimg_bytes, int main_bytes,
+                                                            float floor_, WsHeader *hdr)
 {
     const int h = blockIdx.x;
     const int ka = d_r * 2 < 64 ? 64 : d_r * 2;
@@ -503,9 +379,9 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
     }
     m = red[0];
     __syncthreads();
-    float s = 0.f;
-    for (int k = threadIdx.x; k < K; k += THREADS) s += expf(lh[k] - m);
-    red[threadIdx.x] = s;
+    float sum = 0.f;
+    for (int k = threadIdx.x; k < K; k += THREADS) sum += expf(lh[k] - m);
+    red[threadIdx.x] = sum;
     __syncthreads();
     for (int o = THREADS / 2; o > 0; o >>= 1) {
         if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
@@ -513,11 +389,14 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
     }
     const float lse = m + logf(red[0]);
     uint8_t *img = bimg + (size_t)h * bimg_bytes;
-    for (int n = threadIdx.x; n < kn16; n += THREADS) {
-        const bool real = n < K;
-        float acc = 0.f;
-        bool range_ok = true;
-        for (int q = 0; q < ka / 8; ++q) {
+    const int n = blockIdx.y * 16 + (threadIdx.x >> 3);   // component
+    const int sub = threadIdx.x & 7;
+    const bool in_table = n < kn16;
+    const bool real = n < K;
+    float acc = 0.f;
+    bool range_ok = true;
+    if (in_table) {
+        for (int q = sub; q < ka / 8; q += 8) {
             uint16_t hv[8];
             for (int j = 0; j < 8; ++j) {
                 const int f = q * 8 + j;
@@ -544,12 +423,28 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
             v.y = hv[2] | ((uint32_t)hv[3] << 16);
             v.z = hv[4] | ((uint32_t)hv[5] << 16);
             v.w = hv[6] | ((uint32_t)hv[7] << 16);
-            const uint32_t off = (uint32_t)((q >> 3) * kn16 * 128 + n * 128 + (((q & 7) ^ (n & 7)) << 4));
-            *reinterpret_cast<uint4 *>(img + off) = v;
+            *reinterpret_cast<uint4 *>(img + sw128(n, q, kn16)) = v;
         }
-        if (!range_ok) record_error(hdr, GMA_ERR_RANGE, 1u);
-        cst[(size_t)h * kn16 + n] = real ? ((lh[n] - lse) - 0.5f * acc) * LOG2E : NEG_BIG;
     }
+    // sum the 8 partial sums of this component (lanes 8g .. 8g+7 of the warp)
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (in_table && sub == 0) {
+        const float c = real ? ((lh[n] - lse) - 0.5f * acc) * LOG2E : 0.f;
+        if (!(fabsf(c) < 65504.f)) range_ok = false;
+        const __half hi = __float2half_rn(c);
+        const __half lo = __float2half_rn(c - __half2float(hi));
+        uint4 half0 = make_uint4(0, 0, 0, 0);
+        half0.x = (uint32_t)(*reinterpret_cast<const uint16_t *>(&hi)) |
+                  ((uint32_t)(*reinterpret_cast<const uint16_t *>(&lo)) << 16);
+        uint8_t *row = img + main_bytes + n * 32;
+        const int flip = (n >> 2) & 1;
+        *reinterpret_cast<uint4 *>(row + (flip << 4)) = half0;
+        *reinterpret_cast<uint4 *>(row + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
+        cst[(size_t)h * kn16 + n] = real ? c : NEG_BIG;
+    }
+    if (!range_ok) record_error(hdr, GMA_ERR_RANGE, 1u);
 }
 
 // Segment memories: agg[bh][seg] = sum over the segment's tokens of gamma_K^T [v, 1]
@@ -623,17 +518,31 @@ __global__ void __launch_bounds__(THREADS, 1) tc_segment_memory_kernel(const Arg
 
 // Causal: exclusive prefix of the segment memories within each slice (in place).
 // Bidirectional: the total over all segments, written to segment 0.
-__global__ void tc_scan_kernel(float *__restrict__ agg, long long total, int nseg, int KD, int causal)
+// One thread per 4 consecutive floats of one slice; segments are read 8 at a time so that the
+// loads are in flight together.
+__global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, long long total4,
+                                                      int nseg, int KD4, int causal)
 {
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= total) return;
-    const long long bh = idx / KD, e = idx % KD;
-    float *base = agg + bh * nseg * KD + e;
-    float run = 0.f;
-    for (int s = 0; s < nseg; ++s) {
-        const float v = base[(size_t)s * KD];
-        if (causal) base[(size_t)s * KD] = run;
-        run += v;
+    if (idx >= total4) return;
+    const long long bh = idx / KD4, e = idx % KD4;
+    float4 *base = reinterpret_cast<float4 *>(agg) + bh * nseg * KD4 + e;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nseg; s0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (s0 + u < nseg) v[u] = base[(size_t)(s0 + u) * KD4];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (s0 + u < nseg) {
+                if (causal) base[(size_t)(s0 + u) * KD4] = run;
+                run.x += v[u].x;
+                run.y += v[u].y;
+                run.z += v[u].z;
+                run.w += v[u].w;
+            }
+        }
     }
     if (!causal) base[0] = run;
 }
@@ -905,7 +814,7 @@ bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v)
 }
 
 struct Plan {
-    int kn16, ne, ka, bimg_bytes;
+    int kn16, ne, ka, bimg_bytes, bimg_main_bytes;
     int nseg, cps;              // forward: segments per slice and chunks per segment
     size_t off_bimg, off_cst, off_agg, total;
 };
@@ -918,7 +827,8 @@ Plan make_plan(const gma_shape_t &s, int variant)
     p.kn16 = (s.K + 15) / 16 * 16;
     p.ne = s.d_v + 16;
     p.ka = s.d_r * 2 < 64 ? 64 : s.d_r * 2;
-    p.bimg_bytes = p.ka / 64 * 128 * p.kn16;
+    p.bimg_main_bytes = p.ka / 64 * 128 * p.kn16;
+    p.bimg_bytes = p.bimg_main_bytes + 32 * p.kn16;
     const int BH = s.B * s.H;
     const int nchunks = (s.N + C - 1) / C;
     int nseg = (kTargetCtas + BH - 1) / BH;
@@ -951,6 +861,7 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
     a.nseg = p.nseg;
     a.cps = p.cps;
     a.bimg_bytes = p.bimg_bytes;
+    a.bimg_main_bytes = p.bimg_main_bytes;
     a.eps = s.eps;
     a.out_f32 = (s.flags & GMA_FLAG_OUT_F32) ? 1 : 0;
     return a;
@@ -959,6 +870,8 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
 // Dynamic shared memory for a kernel that allocates `tmem_cols` TMEM columns: at least enough
 // that no more CTAs fit on one SM (228 KB of shared memory) than its 512 columns can serve,
 // so no CTA ever waits inside tcgen05.alloc for a co-resident CTA.
+bool encode_available() { return encode_fn() != nullptr; }
+
 uint32_t smem_for(uint32_t need, uint32_t tmem_cols)
 {
     const uint32_t per_sm = 228u * 1024u;
@@ -967,19 +880,14 @@ uint32_t smem_for(uint32_t need, uint32_t tmem_cols)
     return need > floor_ ? need : floor_;
 }
 
-template <typename KernelT>
-bool set_smem(KernelT kernel, uint32_t bytes)
-{
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
-}
 
 gma_status_t launch_params(const gma_shape_t &s, const Plan &p, char *ws, const float *mu,
                            const float *raw, const float *logits, cudaStream_t st)
 {
     GMA_LAUNCH(KID_TC_PARAMS, st,
-               (tc_params_kernel<<<s.H, THREADS, 0, st>>>(mu, raw, logits, (uint8_t *)(ws + p.off_bimg),
+               (tc_params_kernel<<<dim3(s.H, (p.kn16 + 15) / 16), THREADS, 0, st>>>(mu, raw, logits, (uint8_t *)(ws + p.off_bimg),
                                                           (float *)(ws + p.off_cst), s.K, p.kn16, s.d_r,
-                                                          p.bimg_bytes, s.var_floor, (WsHeader *)ws)));
+                                                          p.bimg_bytes, p.bimg_main_bytes, s.var_floor, (WsHeader *)ws)));
     return GMA_OK;
 }
 
@@ -998,16 +906,14 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     if (!set_smem(tc_segment_memory_kernel<DR>, sm_seg)) return GMA_ERR_CUDA;
     GMA_LAUNCH(KID_TC_CAUSAL_AGG, st,
                (tc_segment_memory_kernel<DR><<<BH * p.nseg, THREADS, sm_seg, st>>>(a, vmap)));
-    const int KD = KMAX * p.ne;
-    const long long tot = (long long)BH * KD;
+    const int KD4 = KMAX * p.ne / 4;
+    const long long tot4 = (long long)BH * KD4;
     GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st,
-               (tc_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(a.agg, tot, p.nseg, KD,
-                                                                               causal ? 1 : 0)));
+               (tc_scan_kernel<<<(unsigned)((tot4 + 255) / 256), 256, 0, st>>>(a.agg, tot4, p.nseg, KD4,
+                                                                                causal ? 1 : 0)));
     if (causal) {
-        const uint32_t sm = smem_for(Smem(DR, p.kn16, s.d_v, true, true, true).total + 1024, 512);
-        if (!set_smem(tc_causal_chunked_kernel<DR>, sm)) return GMA_ERR_CUDA;
-        GMA_LAUNCH(KID_TC_CAUSAL_OUT, st,
-                   (tc_causal_chunked_kernel<DR><<<BH * p.nseg, THREADS, sm, st>>>(a, vmap)));
+        const gma_status_t r = launch_causal_pipelined<DR>(a, vmap, BH * p.nseg, st);
+        if (r != GMA_OK) return r;
     } else {
         const uint32_t sm = smem_for(Smem(DR, p.kn16, s.d_v, false, true, true).total + 1024, 256);
         if (!set_smem(tc_bidir_read_kernel<DR>, sm)) return GMA_ERR_CUDA;

@@ -1,0 +1,589 @@
+// gma_tc_causal.cu -- the chunked causal GMA kernel (tcgen05, sm_103a), warp-specialised.
+//
+// Method: page "Attention par Mélange Gaussien (GMA)" (gist.science/fr/paper/2606.18283),
+// Méthodologie §3 (causal variant: the latent memory and its normaliser become prefix sums, so
+// row i of O sees keys j <= i) on top of §1 (posterior responsibilities) and §2 (write phase,
+// read phase O = Gamma_Q V~ / (Gamma_Q Z + eps)).
+//
+// One CTA handles one segment of one (batch, head) slice, starting from the segment's exclusive
+// prefix memory S_start (V~ part and Z part), in chunks of C = 128 tokens:
+//   Gamma_K, Gamma_Q       responsibilities of the chunk's keys and queries
+//   P      = Gamma_Q Gamma_K^T                       (tensor cores, fp32 in TMEM)
+//   O_num  = Gamma_Q S_{c-1} + tril(P) V_c           (tensor cores)
+//   den    = Gamma_Q . Z_{c-1} + rowsum(tril(P))     (CUDA cores, fp32)
+//   O      = O_num / (den + eps * s)                 (s: row sum of the unnormalised Gamma_Q)
+//   S_c    = S_{c-1} + Gamma_K^T V_c                 (tensor cores, fp32 in TMEM)
+//   Z_c    = Z_{c-1} + column sums of Gamma_K        (CUDA cores, fp32)
+//
+// Warp roles (288 threads):
+//   warps 0-3  key side:   [x^2, x] of the keys, softmax -> Gamma_K (shared memory), column sums
+//                          (Z), readout of S_c into the bf16 operand copy used by the next chunk;
+//   warps 4-7  query side: [x^2, x] of the queries, softmax -> Gamma_Q (bf16, back into TMEM as the
+//                          A operand), normaliser, causal mask of P (bf16, back into TMEM), output;
+//   warp 8     control:    TMA of the value tiles (double-buffered) and every tcgen05.mma, issued
+//                          as soon as its operands are ready (mbarrier handshakes).
+// Tensor memory (512 columns): [0,128) key logits, then P; [128,256) query logits, then Gamma_Q;
+// [256,384) output numerator; [384,512) the running memory S.
+// Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all roles leave their loops.
+#include "tc_common.cuh"
+
+namespace gma {
+namespace tck {
+
+namespace {
+
+constexpr int CTHREADS = 288;
+enum BarId { B_BIMG, B_V0, B_V1, B_AK, B_AQ, B_GK, B_GQ, B_PS, B_SP, B_OF, B_LK, B_LQ, B_S, B_PQ, B_PV, NBAR };
+constexpr uint32_t R_LK = 0, R_LQ = 128, R_O = 256, R_S = 384;
+
+struct CausalSmem {
+    uint32_t bimg, ax, abuf, gk, sp, ve0, ve1, zbuf, bars, misc, total;
+    __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    __host__ __device__ CausalSmem(int DR, int kn16, int d_v)
+    {
+        const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
+        const uint32_t tile = ka / 64u * 128u;
+        uint32_t o = 0;
+        bimg = o; o = al(o + tile * (uint32_t)kn16 + 32u * (uint32_t)kn16);
+        ax = o; o = al(o + (uint32_t)C * 32u);
+        abuf = o; o = al(o + tile * (uint32_t)C);
+        gk = o; o = al(o + 2u * C * 128u);
+        sp = o; o = al(o + (uint32_t)d_v * KMAX * 2u);
+        ve0 = o; o = al(o + (uint32_t)d_v * C * 2u);
+        ve1 = o; o = al(o + (uint32_t)d_v * C * 2u);
+        zbuf = o; o += 2u * KMAX * 4u;
+        bars = o; o += NBAR * 8u;
+        misc = o; o += 16u;
+        total = o;
+    }
+};
+
+// Row maximum over the first K fp32 columns of this thread's TMEM lane (kc = ceil(K/32) chunks
+// of 32 columns, read two chunks per wait).
+__device__ __forceinline__ float row_max(uint32_t taddr, int K, int kc)
+{
+    float m = NEG_BIG;
+#pragma unroll
+    for (int c0 = 0; c0 < 4; c0 += 2) {
+        if (c0 < kc) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32(taddr + 32 * c0, ra);
+            if (c0 + 1 < kc) tmem_ld32(taddr + 32 * (c0 + 1), rb);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if ((c0 + 1) * 32 <= K || 32 * c0 + j < K) m = fmaxf(m, __uint_as_float(ra[j]));
+            if (c0 + 1 < kc) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if ((c0 + 2) * 32 <= K || 32 * (c0 + 1) + j < K) m = fmaxf(m, __uint_as_float(rb[j]));
+            }
+        }
+    }
+    return m;
+}
+
+// exp2(L - m) of one chunk of 32 columns (0 beyond K), accumulating the sum.
+__device__ __forceinline__ void chunk_exp(uint32_t (&r)[32], int c, int K, float m, float &s)
+{
+    const bool full = (c + 1) * 32 <= K;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float e = (full || 32 * c + j < K) ? ex2(__uint_as_float(r[j]) - m) : 0.f;
+        r[j] = __float_as_uint(e);
+        s += e;
+    }
+}
+
+__device__ __forceinline__ uint32_t pk2(uint32_t a, uint32_t b, float sc)
+{
+    return pack_bf16(__uint_as_float(a) * sc, __uint_as_float(b) * sc);
+}
+
+// Key side: Gamma_K row `row` = softmax of the TMEM logits at tl, normalised (zeros when not
+// valid), as bf16 into the K-major SW128 tile gk.
+__device__ __noinline__ void key_softmax(uint32_t tl, int K, int kc, bool valid, uint8_t *gk, int k)
+{
+    const float m = row_max(tl, K, kc);
+    float sum = 0.f;
+    // exp2(L - m) as bf16 pairs straight into the row of the tile ...
+#pragma unroll
+    for (int c0 = 0; c0 < 4; c0 += 2) {
+        if (c0 < kc) {
+            uint32_t r2[2][32];
+            tmem_ld32(tl + 32 * c0, r2[0]);
+            if (c0 + 1 < kc) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int c2 = c0 + h2;
+                if (c2 < kc) {
+                    chunk_exp(r2[h2], c2, K, m, sum);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int e = 8 * q;
+                        *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c2 + q, C)) =
+                            make_uint4(pk2(r2[h2][e], r2[h2][e + 1], 1.f), pk2(r2[h2][e + 2], r2[h2][e + 3], 1.f),
+                                       pk2(r2[h2][e + 4], r2[h2][e + 5], 1.f), pk2(r2[h2][e + 6], r2[h2][e + 7], 1.f));
+                    }
+                }
+            }
+        }
+    }
+    // ... then divided by the row sum in place (zeros for rows beyond the sequence)
+    const float scf = valid ? 1.0f / sum : 0.f;
+    const __nv_bfloat162 sc2 = __floats2bfloat162_rn(scf, scf);
+    for (int q = 0; q < 4 * kc; ++q) {
+        uint4 *p4 = reinterpret_cast<uint4 *>(gk + sw128(k, q, C));
+        uint4 v = *p4;
+        __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&v);
+        b2[0] = __hmul2(b2[0], sc2);
+        b2[1] = __hmul2(b2[1], sc2);
+        b2[2] = __hmul2(b2[2], sc2);
+        b2[3] = __hmul2(b2[3], sc2);
+        *p4 = v;
+    }
+}
+
+// Key side: row k of the running memory S (d_v fp32 columns of TMEM at tl) as bf16 into the
+// MN-major SW32 operand tile sp.
+__device__ __noinline__ void state_readout(uint32_t tl, int d_v, uint8_t *sp, int k)
+{
+            for (int b0 = 0; b0 < d_v / 16; b0 += 4) {   // 64 columns per wait
+                uint32_t ra[32], rb[32];
+                if (d_v == 16) {
+                    uint32_t r16[16];
+                    tmem_ld16(tl, r16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) ra[j] = r16[j];
+                } else {
+                    tmem_ld32(tl + 16 * b0, ra);
+                    if (b0 + 2 < d_v / 16) tmem_ld32(tl + 16 * b0 + 32, rb);
+                    tmem_ld_wait();
+                }
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int b = b0 + bb;
+                    if (b < d_v / 16) {
+                        uint32_t r[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) r[j] = bb < 2 ? ra[16 * bb + j] : rb[16 * (bb - 2) + j];
+                        const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f),
+                                                    pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
+                        const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f),
+                                                    pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
+                        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
+                        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
+                    }
+                }
+            }
+}
+
+// Query side: unnormalised Gamma_Q of this row (zeros when not valid) back into TMEM at tl as
+// bf16 pairs; returns (row sum of the fp32 values, Gamma_Q . Z) with Z the fp32 normaliser z.
+__device__ __noinline__ float2 query_softmax(uint32_t tl, int K, int kc, bool valid, const float *z)
+{
+                const float m = row_max(tl, K, kc);
+                const float sc = valid ? 1.f : 0.f;
+                const float4 *z4 = reinterpret_cast<const float4 *>(z);
+                float srow = 0.f, den = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < 4; c0 += 2) {
+                    if (c0 < kc) {
+                        uint32_t r2[2][32];
+                        tmem_ld32(tl + 32 * c0, r2[0]);
+                        if (c0 + 1 < kc) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int c2 = c0 + h2;
+                            if (c2 < kc) {
+                                chunk_exp(r2[h2], c2, K, m, srow);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const float4 z = z4[8 * c2 + q];
+                                    den = fmaf(__uint_as_float(r2[h2][4 * q]), z.x, den);
+                                    den = fmaf(__uint_as_float(r2[h2][4 * q + 1]), z.y, den);
+                                    den = fmaf(__uint_as_float(r2[h2][4 * q + 2]), z.z, den);
+                                    den = fmaf(__uint_as_float(r2[h2][4 * q + 3]), z.w, den);
+                                }
+                                uint32_t w[16];
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) w[j] = pk2(r2[h2][2 * j], r2[h2][2 * j + 1], sc);
+                                tmem_st16(tl + 16 * c2, w);   // Gamma_Q (bf16 pairs), in place
+                            }
+                        }
+                    }
+                }
+                tmem_st_wait();
+                return make_float2(srow, den);
+}
+
+// Query side: row i of P (fp32 in TMEM at tl) masked to columns j <= i, written back as bf16
+// pairs in place; returns the sum of the kept fp32 values.
+__device__ __noinline__ float causal_mask(uint32_t tl, int i)
+{
+    float den = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < 4; c0 += 2) {
+                uint32_t r2[2][32];
+                tmem_ld32(tl + 32 * c0, r2[0]);
+                tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c2 = c0 + h2;
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = 32 * c2 + 2 * j;
+                        const float p0 = col <= i ? __uint_as_float(r2[h2][2 * j]) : 0.f;
+                        const float p1 = col + 1 <= i ? __uint_as_float(r2[h2][2 * j + 1]) : 0.f;
+                        den += p0 + p1;
+                        w[j] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(tl + 16 * c2, w);
+                }
+            }
+            tmem_st_wait();
+    return den;
+}
+
+// Query side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.
+__device__ __noinline__ void write_output(uint32_t tl, int d_v, float inv, bool valid, void *O,
+                                          long long orow, int out_f32)
+{
+                for (int c0 = 0; c0 < (d_v + 31) / 32; c0 += 2) {   // 64 columns per wait
+                    uint32_t r2[2][32];
+                    if (d_v == 16) {
+                        uint32_t r16[16];
+                        tmem_ld16(tl, r16);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) r2[0][j] = r16[j];
+                    } else {
+                        tmem_ld32(tl + 32 * c0, r2[0]);
+                        if (32 * (c0 + 1) < d_v) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
+                        tmem_ld_wait();
+                    }
+                    if (!valid) continue;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int col0 = 32 * (c0 + h2);
+                        if (col0 >= d_v) continue;
+                        const int ncol = d_v - col0 < 32 ? d_v - col0 : 32;
+                        if (out_f32) {
+                            float4 *o4 = reinterpret_cast<float4 *>((float *)O + orow * d_v + col0);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                if (4 * q < ncol)
+                                    o4[q] = make_float4(__uint_as_float(r2[h2][4 * q]) * inv,
+                                                        __uint_as_float(r2[h2][4 * q + 1]) * inv,
+                                                        __uint_as_float(r2[h2][4 * q + 2]) * inv,
+                                                        __uint_as_float(r2[h2][4 * q + 3]) * inv);
+                        } else {
+                            uint4 *o4 = reinterpret_cast<uint4 *>((bf16 *)O + orow * d_v + col0);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (8 * q < ncol)
+                                    o4[q] = make_uint4(pk2(r2[h2][8 * q], r2[h2][8 * q + 1], inv),
+                                                       pk2(r2[h2][8 * q + 2], r2[h2][8 * q + 3], inv),
+                                                       pk2(r2[h2][8 * q + 4], r2[h2][8 * q + 5], inv),
+                                                       pk2(r2[h2][8 * q + 6], r2[h2][8 * q + 7], inv));
+                        }
+                    }
+                }
+            }
+
+template <int DR>
+__device__ __forceinline__ void issue_logits_c(uint32_t d, uint32_t abuf, uint32_t bimg, uint32_t bconst,
+                                               uint32_t ax, int kn16)
+{
+    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
+    const uint32_t id = idesc_f16(128, (uint32_t)kn16, 0, 0, 0, 0);
+#pragma unroll
+    for (int s = 0; s < KA / 16; ++s) mma_f16(d, kdesc(abuf, s, C), kdesc(bimg, s, kn16), id, s > 0);
+    mma_f16(d, kdesc32(ax), kdesc32(bconst), id, 1u);   // + per-component constant
+}
+
+}  // namespace
+
+template <int DR>
+__global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const Args a,
+                                                                          const __grid_constant__ CUtensorMap vmap)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const CausalSmem L(DR, a.kn16, a.d_v);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 4);
+    float *zbuf = reinterpret_cast<float *>(smem + L.zbuf);
+    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int tok0 = seg * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    const int nch = (tok_end - tok0 + C - 1) / C;
+    const int d_v = a.d_v;
+    const int kc = (a.K + 31) >> 5;
+
+    // ---------------------------------------------------------------- set-up (all threads)
+    if (warp == 8) {
+        if (t == 256) {
+            static const uint32_t counts[NBAR] = {1, 1, 1, 128, 128, 128, 128, 128, 128, 128, 1, 1, 1, 1, 1};
+            for (int i = 0; i < NBAR; ++i) mbar_init(bars + i, counts[i]);
+            *abort = 0;
+            fence_mbar_init();
+        }
+        __syncwarp();
+        tmem_alloc(tslot, 512);
+    } else if (warp < 4) {
+        // Gamma_K tile: components the softmax never writes must read as zero
+        for (uint32_t o = t * 16; o < 2u * C * 128u; o += 128 * 16)
+            *reinterpret_cast<uint4 *>(smem + L.gk + o) = make_uint4(0, 0, 0, 0);
+    } else {
+        // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
+        const int i = t - 128;
+        const uint32_t one2 = 0x3C003C00u;   // fp16 pair (1, 1)
+        const int flip = (i >> 2) & 1;
+        *reinterpret_cast<uint4 *>(smem + L.ax + i * 32 + (flip << 4)) = make_uint4(one2, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(smem + L.ax + i * 32 + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t sb = smem_u32(smem);
+
+    if (warp == 8) {
+        // ============================================================ control warp
+        if (t == 256) {
+            // value-tile ring of two buffers, selected by chunk parity (no runtime-indexed arrays)
+            auto ve = [&](int c) { return (c & 1) ? sb + L.ve1 : sb + L.ve0; };
+            auto vep = [&](int c) { return (c & 1) ? smem + L.ve1 : smem + L.ve0; };
+            const uint32_t id_p = idesc_f16(128, 128, 1, 1, 0, 0);
+            const uint32_t id_o = idesc_f16(128, (uint32_t)d_v, 1, 1, 0, 1);
+            const uint32_t id_s = idesc_f16(128, (uint32_t)d_v, 1, 1, 1, 1);
+            const int ksteps = a.kn16 / 16;
+            bool vpend0 = false, vpend1 = false;   // a value-tile load in flight per buffer
+            int last_pv = -1;
+            bool ok = true;
+            mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + B_BIMG);
+            if (nch > 0) {
+                load_v_chunk(vep(0), &vmap, bars + B_V0, d_v, tok0, bh);
+                vpend0 = true;
+            }
+            ok = mbar_wait_abortable(bars + B_BIMG, 0, a.hdr, 50, abort);
+            const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
+            for (int c = 0; ok && c < nch; ++c) {
+                const uint32_t ph = c & 1;
+                if (c > 0 && !(ok = mbar_wait_abortable(bars + B_PV, (c - 1) & 1, a.hdr, 51, abort))) break;
+                if (c + 1 < nch) {
+                    load_v_chunk(vep(c + 1), &vmap, bars + B_V0 + ((c + 1) & 1), d_v, tok0 + (c + 1) * C, bh);
+                    if ((c + 1) & 1) vpend1 = true; else vpend0 = true;
+                }
+                // key logits
+                if (!(ok = mbar_wait_abortable(bars + B_AK, ph, a.hdr, 52, abort))) break;
+                tc_fence_after();
+                issue_logits_c<DR>(tmem + R_LK, sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
+                mma_commit(bars + B_LK);
+                // query logits (query-side softmax of the previous chunk is done with R_LQ)
+                if (!(ok = mbar_wait_abortable(bars + B_AQ, ph, a.hdr, 53, abort))) break;
+                if (c > 0 && !(ok = mbar_wait_abortable(bars + B_PQ, (c - 1) & 1, a.hdr, 54, abort))) break;
+                tc_fence_after();
+                issue_logits_c<DR>(tmem + R_LQ, sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
+                mma_commit(bars + B_LQ);
+                // S update and the P / inter-chunk read, whichever has its operands first
+                bool s_done = false, pq_done = false;
+                const long long t0 = clock64();
+                while (!(s_done && pq_done)) {
+                    const bool gk = mbar_try_wait(bars + B_GK, ph);
+                    const bool spr = mbar_try_wait(bars + B_SP, ph);
+                    if (!s_done && gk && spr && mbar_try_wait(bars + B_V0 + (c & 1), (c >> 1) & 1)) {
+                        if (c & 1) vpend1 = false; else vpend0 = false;
+                        tc_fence_after();
+                        for (int s = 0; s < C / 16; ++s)   // S += Gamma_K^T V
+                            mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(ve(c), s, C), id_s, 1u);
+                        mma_commit(bars + B_S);
+                        s_done = true;
+                    }
+                    if (!pq_done && gk && spr && mbar_try_wait(bars + B_GQ, ph) &&
+                        (c == 0 || mbar_try_wait(bars + B_OF, (c - 1) & 1))) {
+                        tc_fence_after();
+                        for (int s = 0; s < ksteps; ++s)   // P = Gamma_Q Gamma_K^T
+                            mma_f16_tmem_a(tmem + R_LK, tmem + R_LQ + 8 * s, kdesc(sb + L.gk, s, C), id_p, s > 0);
+                        for (int s = 0; s < ksteps; ++s)   // O = Gamma_Q S_{c-1}
+                            mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + 8 * s, mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
+                        mma_commit(bars + B_PQ);
+                        pq_done = true;
+                    }
+                    if (*abort) { ok = false; break; }
+                    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+                        record_error(a.hdr, GMA_ERR_TIMEOUT, 55);
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok) break;
+                // intra-chunk: O += tril(P) V
+                if (!(ok = mbar_wait_abortable(bars + B_PS, ph, a.hdr, 56, abort))) break;
+                tc_fence_after();
+                for (int s = 0; s < C / 16; ++s)
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_LK + 8 * s, mn32desc(ve(c), s, C), id_o, 1u);
+                mma_commit(bars + B_PV);
+                last_pv = c;
+            }
+            // drain: MMAs complete in issue order, so the last commit covers them all
+            if (last_pv >= 0) mbar_wait(bars + B_PV, last_pv & 1, a.hdr, 57);
+            // a value-tile load that was issued but never consumed (only after a timeout): the most
+            // recent chunk of that buffer's parity
+            if (vpend0 || vpend1) {
+                for (int c = nch - 1; c >= 0 && c >= nch - 2; --c) {
+                    if ((c & 1) ? vpend1 : vpend0) mbar_wait(bars + B_V0 + (c & 1), (c >> 1) & 1, a.hdr, 58);
+                }
+            }
+        }
+    } else if (warp < 4) {
+        // ============================================================ key side
+        const int k = t;   // TMEM lane, token row of the chunk, and component row of S
+        const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+        // starting memory: V~ part to TMEM and as the bf16 operand, Z part to the running sum
+        const float *src = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + k) * a.ne;
+        for (int b = 0; b < d_v / 16; ++b) {
+            uint32_t r[16];
+            const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = s4[q];
+                r[4 * q] = __float_as_uint(f.x);
+                r[4 * q + 1] = __float_as_uint(f.y);
+                r[4 * q + 2] = __float_as_uint(f.z);
+                r[4 * q + 3] = __float_as_uint(f.w);
+            }
+            tmem_st16(lane + R_S + 16 * b, r);
+            uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
+            uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
+            *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 0, KMAX)) = lo;
+            *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 1, KMAX)) = hi;
+        }
+        float zrun = src[d_v];
+        zbuf[k] = zrun;
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bars + B_SP);   // phase 0: S_start ready
+        uint4 x[DR / 8];
+        load_x<DR>(a.KX, (long long)bh * a.N + tok0 + k, tok0 + k < tok_end, x);
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            const int base = tok0 + c * C;
+            if (c > 0 && !mbar_wait_abortable(bars + B_LQ, (c - 1) & 1, a.hdr, 60, abort)) break;
+            build_a<DR>(smem + L.abuf, k, x);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + B_AK);
+            if (!mbar_wait_abortable(bars + B_LK, ph, a.hdr, 61, abort)) break;
+            if (c > 0 && !mbar_wait_abortable(bars + B_S, (c - 1) & 1, a.hdr, 62, abort)) break;
+            if (c > 0 && !mbar_wait_abortable(bars + B_PQ, (c - 1) & 1, a.hdr, 63, abort)) break;
+            tc_fence_after();
+            key_softmax(lane + R_LK, a.K, kc, base + k < tok_end, smem + L.gk, k);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars + B_GK);
+            // Z_c = Z_{c-1} + column k of Gamma_K (the bf16 values the tensor cores use), once all
+            // 128 rows are in (the same barrier the control warp waits on)
+            if (!mbar_wait_abortable(bars + B_GK, ph, a.hdr, 66, abort)) break;
+            {
+                const int q = k >> 3;
+                const uint32_t col = (uint32_t)(k & 7) * 2;
+                float zs = 0.f;
+                for (int j = 0; j < C; ++j)
+                    zs += __bfloat162float(*reinterpret_cast<const bf16 *>(smem + L.gk + sw128(j, q, C) + col));
+                zrun += zs;
+            }
+            // readout of S_c (after the update and the read of S_{c-1} that it overwrites)
+            if (!mbar_wait_abortable(bars + B_S, ph, a.hdr, 64, abort)) break;
+            if (!mbar_wait_abortable(bars + B_PQ, ph, a.hdr, 65, abort)) break;
+            tc_fence_after();
+            state_readout(lane + R_S, d_v, smem + L.sp, k);
+            zbuf[((c + 1) & 1) * KMAX + k] = zrun;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars + B_SP);
+            // next chunk's keys: in flight while the control warp waits for this chunk's output
+            load_x<DR>(a.KX, (long long)bh * a.N + base + C + k, base + C + k < tok_end, x);
+        }
+    } else {
+        // ============================================================ query side
+        const int i = t - 128;
+        const uint32_t lane = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        uint4 x[DR / 8];
+        load_x<DR>(a.QX, (long long)bh * a.N + tok0 + i, tok0 + i < tok_end, x);
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            const int base = tok0 + c * C;
+            const bool valid = base + i < tok_end;
+            if (!mbar_wait_abortable(bars + B_LK, ph, a.hdr, 70, abort)) break;
+            build_a<DR>(smem + L.abuf, i, x);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + B_AQ);
+            if (!mbar_wait_abortable(bars + B_LQ, ph, a.hdr, 71, abort)) break;
+            if (!mbar_wait_abortable(bars + B_SP, ph, a.hdr, 72, abort)) break;
+            tc_fence_after();
+            float srow, den;
+            {
+                const float2 r = query_softmax(lane + R_LQ, a.K, kc, valid, zbuf + ph * KMAX);
+                srow = r.x;
+                den = r.y;
+            }
+            tc_fence_before();
+            mbar_arrive(bars + B_GQ);
+            // causal mask of P; P (bf16 pairs) back into TMEM as the A operand of tril(P) V
+            if (!mbar_wait_abortable(bars + B_PQ, ph, a.hdr, 73, abort)) break;
+            tc_fence_after();
+            den += causal_mask(lane + R_LK, i);
+            tc_fence_before();
+            mbar_arrive(bars + B_PS);
+            // output
+            if (!mbar_wait_abortable(bars + B_PV, ph, a.hdr, 74, abort)) break;
+            tc_fence_after();
+            write_output(lane + R_O, d_v, 1.0f / (den + a.eps * srow), valid, a.O,
+                         (long long)bh * a.N + base + i, a.out_f32);
+            tc_fence_before();
+            mbar_arrive(bars + B_OF);
+            // next chunk's queries: in flight while the next key logits are computed
+            load_x<DR>(a.QX, (long long)bh * a.N + base + C + i, base + C + i < tok_end, x);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 8) tmem_dealloc(tmem, 512);
+}
+
+// Shared memory the pipelined causal kernel needs (0 if the shape does not fit).
+uint32_t causal_pipelined_smem(int d_r, int kn16, int d_v)
+{
+    const uint32_t need = CausalSmem(d_r, kn16, d_v).total + 1024;
+    return need <= 227u * 1024u ? smem_for(need, 512) : 0;
+}
+
+template <int DR>
+gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st)
+{
+    const uint32_t sm = causal_pipelined_smem(DR, a.kn16, a.d_v);
+    if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!set_smem(tc_causal_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st, (tc_causal_pipelined_kernel<DR><<<nblocks, CTHREADS, sm, st>>>(a, vmap)));
+    return GMA_OK;
+}
+
+template gma_status_t launch_causal_pipelined<16>(const Args &, const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_pipelined<32>(const Args &, const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_pipelined<64>(const Args &, const CUtensorMap &, int, cudaStream_t);
+
+}  // namespace tck
+}  // namespace gma

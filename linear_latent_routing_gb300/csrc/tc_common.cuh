@@ -1,0 +1,179 @@
+// tc_common.cuh -- definitions shared by the tcgen05 translation units of libgma.so: constants,
+// kernel arguments, shared-memory operand layouts and their descriptors, the [x^2, x] builder and
+// the TMA of value tiles.
+//
+// The Gaussian table of a head (written by tc_params_kernel) has two parts:
+//   main:  kn16 rows (components) x ka columns, fp16, K-major 128-byte swizzle, holding
+//          log2e * [-w/2 ; mu w] (w = 1/sigma^2), so that [x^2, x] . row = the x-dependent part of
+//          log2e * log N(x; mu, sigma^2);
+//   const: kn16 rows x 16 columns, fp16, K-major 32-byte swizzle, holding (c_hi, c_lo, 0, ...)
+//          with c_hi + c_lo = log2e * (log pi - 1/2 sum_d (mu^2 w + log sigma^2)).
+// Multiplied by a constant operand whose rows are (1, 1, 0, ...), the const part adds the
+// per-component constant inside the same MMA, so the accumulator holds complete log2 logits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "gma_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace gma {
+namespace tck {
+
+using namespace tc;
+
+constexpr int C = 128;          // tokens per chunk (the MMA M dimension)
+constexpr int THREADS = 128;    // one thread per TMEM lane / token row / component row
+constexpr int KMAX = 128;       // components handled by this family
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float NEG_BIG = -1.0e30f;
+
+typedef __nv_bfloat16 bf16;
+
+struct Args {
+    const bf16 *QX, *KX;
+    void *O;                 // output (bf16 or fp32)
+    void *gamma;             // responsibilities output (bf16 or fp32)
+    const uint8_t *bimg;     // per-head Gaussian table image [H][bimg_bytes]: the [x^2, x] part
+                             // (bimg_main_bytes), then the constant part (kn16 rows x 32 B)
+    const float *cst;        // per-head log2-domain constants [H][kn16]
+    float *agg;              // segment memories [BH][nseg][KMAX][ne] fp32
+    WsHeader *hdr;
+    int H, N, K, kn16, d_v, ne;
+    int nseg, cps;           // segments per slice, chunks per segment
+    int bimg_bytes, bimg_main_bytes;
+    float eps;
+    int out_f32;
+};
+
+// ------------------------------------------------------------------ layout helpers
+__device__ __forceinline__ uint32_t sw128(int row, int q, int rows)
+{
+    return (uint32_t)((q >> 3) * rows * 128 + row * 128 + (((q & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t sw32(int row, int blk, int half, int rows)
+{
+    return (uint32_t)(blk * rows * 32 + row * 32 + ((half ^ ((row >> 2) & 1)) << 4));
+}
+
+// K-major SW128 operand, k-step s (16 elements)
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int s, int rows)
+{
+    return smem_desc(base + (uint32_t)((s >> 2) * rows * 128 + (s & 3) * 32), 16, 1024, SW_128B);
+}
+
+// MN-major SW128 operand whose K dimension runs along rows (128 B each), k-step s.
+__device__ __forceinline__ uint64_t mn128desc(uint32_t base, int s, int rows)
+{
+    return smem_desc(base + (uint32_t)(s * 16 * 128), (uint32_t)(rows * 128), 1024, SW_128B);
+}
+
+// K-major SW32 operand of one k-step (rows of 16 two-byte elements, 32 B each).
+__device__ __forceinline__ uint64_t kdesc32(uint32_t base)
+{
+    return smem_desc(base, 16, 256, SW_32B);
+}
+
+// MN-major SW32 operand (blocks of 16 MN elements), k-step s.
+__device__ __forceinline__ uint64_t mn32desc(uint32_t base, int s, int rows)
+{
+    return smem_desc(base + (uint32_t)(s * 16 * 32), (uint32_t)(rows * 32), 256, SW_32B);
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float a, float b)
+{
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+
+// Builds [x^2, x] (fp16, K-major SW128, ka columns) for token row `row` from its bf16 vector.
+template <int DR>
+__device__ __forceinline__ void build_a(uint8_t *abuf, int row, const uint4 (&x)[DR / 8])
+{
+    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
+#pragma unroll
+    for (int q = 0; q < KA / 8; ++q) {
+        uint4 v;
+        if (q < DR / 8) {
+            const bf16 *e = reinterpret_cast<const bf16 *>(&x[q]);
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+            v.x = pack_f16(f[0] * f[0], f[1] * f[1]);
+            v.y = pack_f16(f[2] * f[2], f[3] * f[3]);
+            v.z = pack_f16(f[4] * f[4], f[5] * f[5]);
+            v.w = pack_f16(f[6] * f[6], f[7] * f[7]);
+        } else if (q < DR / 4) {
+            const bf16 *e = reinterpret_cast<const bf16 *>(&x[q - DR / 8]);
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+            v.x = pack_f16(f[0], f[1]);
+            v.y = pack_f16(f[2], f[3]);
+            v.z = pack_f16(f[4], f[5]);
+            v.w = pack_f16(f[6], f[7]);
+        } else {
+            v = make_uint4(0, 0, 0, 0);
+        }
+        *reinterpret_cast<uint4 *>(abuf + sw128(row, q, C)) = v;
+    }
+}
+
+template <int DR>
+__device__ __forceinline__ void load_x(const bf16 *X, long long row, bool valid, uint4 (&x)[DR / 8])
+{
+#pragma unroll
+    for (int q = 0; q < DR / 8; ++q)
+        x[q] = valid ? __ldg(reinterpret_cast<const uint4 *>(X + row * DR) + q) : make_uint4(0, 0, 0, 0);
+}
+
+// TMA of V rows [tok, tok + 128) of slice bh into the MN-major SW32 blocks of `ve`.
+__device__ __forceinline__ void load_v_chunk(uint8_t *ve, const CUtensorMap *vmap, uint64_t *bar,
+                                             int d_v, int tok, int bh)
+{
+    mbar_arrive_expect_tx(bar, (uint32_t)(C * d_v * 2));
+    for (int b = 0; b < d_v / 16; ++b) {
+        // 3-D map {d_v, N, BH}, box {16, 128, 1}
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(ve + b * C * 32)),
+            "l"((uint64_t)vmap), "r"(smem_u32(bar)), "r"(b * 16), "r"(tok), "r"(bh)
+            : "memory");
+    }
+}
+
+
+// ------------------------------------------------------------------ the pipelined causal kernel
+uint32_t causal_pipelined_smem(int d_r, int kn16, int d_v);
+template <int DR>
+gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st);
+
+// ------------------------------------------------------------------ host helpers (gma_tc.cu)
+bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v);
+uint32_t smem_for(uint32_t need, uint32_t tmem_cols);
+bool encode_available();
+
+template <typename KernelT>
+bool set_smem(KernelT kernel, uint32_t bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
+}
+
+}  // namespace tck
+}  // namespace gma
