@@ -144,52 +144,8 @@ __device__ __noinline__ float softmax_row(uint32_t taddr, const float *cst_, int
     return s;
 }
 
-__device__ __forceinline__ void zero_region(uint8_t *p, uint32_t bytes)
-{
-    for (uint32_t o = threadIdx.x * 16; o < bytes; o += THREADS * 16)
-        *reinterpret_cast<uint4 *>(p + o) = make_uint4(0, 0, 0, 0);
-}
 
-// [V | 1]: fills the block of ones after the d_v/16 value blocks (all 16 columns are ones, so
-// every one of the 16 extra accumulator columns receives the normaliser).
-__device__ __forceinline__ void fill_ones(uint8_t *ve, int d_v)
-{
-    const uint32_t o0 = (uint32_t)(d_v / 16) * C * 32;
-    const uint32_t one2 = 0x3F803F80u;
-    for (uint32_t o = threadIdx.x * 16; o < (uint32_t)C * 32; o += THREADS * 16)
-        *reinterpret_cast<uint4 *>(ve + o0 + o) = make_uint4(one2, one2, one2, one2);
-}
 
-// Reads this thread's row (component k) of the memory S from TMEM: ne fp32 columns, writes them
-// as bf16 into the MN-major SW32 B-operand tile `sp` (KMAX rows), and optionally to `out`.
-__device__ __forceinline__ void readout_state(uint32_t taddr, int ne, int k, uint8_t *sp, float *out)
-{
-    for (int b = 0; b < ne / 16; ++b) {
-        uint32_t r[16];
-        tmem_ld16(taddr + b * 16, r);
-        tmem_ld_wait();
-        if (sp) {
-            uint4 lo, hi;
-            lo.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
-            lo.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
-            lo.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
-            lo.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
-            hi.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
-            hi.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
-            hi.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
-            hi.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
-            *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
-            *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
-        }
-        if (out) {
-            float4 *o4 = reinterpret_cast<float4 *>(out + b * 16);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                o4[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-        }
-    }
-}
 
 // Loads an fp32 memory row (ne columns) from global into TMEM (this thread's lane) and, as
 // bf16, into the SW32 tile `sp`.
@@ -259,31 +215,6 @@ __device__ __forceinline__ void write_out(uint32_t taddr, int d_v, float eps_s, 
     }
 }
 
-// Masked affinity row i: P_ij for j <= i (else 0), as bf16 into the K-major SW128 tile `ps`.
-__device__ __forceinline__ void mask_row(uint32_t taddr, int i, uint8_t *ps)
-{
-#pragma unroll
-    for (int c = 0; c < C / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float f[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int col = c * 32 + q * 8 + j;
-                f[j] = col <= i ? __uint_as_float(r[q * 8 + j]) : 0.f;
-            }
-            uint4 w;
-            w.x = pack_bf16(f[0], f[1]);
-            w.y = pack_bf16(f[2], f[3]);
-            w.z = pack_bf16(f[4], f[5]);
-            w.w = pack_bf16(f[6], f[7]);
-            *reinterpret_cast<uint4 *>(ps + sw128(i, c * 4 + q, C)) = w;
-        }
-    }
-}
 
 __device__ __forceinline__ void sync_tc()
 {
@@ -338,15 +269,6 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase, WsHeade
     return !__syncthreads_or(!ok);
 }
 
-// After a timed-out wait: give copies and MMAs still in flight a bounded chance to finish
-// before the CTA releases its tensor memory and exits.  (The phases passed are the ones the
-// abandoned waits were for; wait_all already flipped them, so flip back.)
-__device__ __forceinline__ void drain(const Bars &bars, bool v_pending, uint32_t ph_v,
-                                      bool mma_pending, uint32_t ph_m, WsHeader *hdr)
-{
-    if (v_pending) mbar_wait(bars.v, ph_v ^ 1u, hdr, 90);
-    if (mma_pending) mbar_wait(bars.mma, ph_m ^ 1u, hdr, 91);
-}
 
 // ================================================================== kernels
 
@@ -447,75 +369,6 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
     if (!range_ok) record_error(hdr, GMA_ERR_RANGE, 1u);
 }
 
-// Segment memories: agg[bh][seg] = sum over the segment's tokens of gamma_K^T [v, 1]
-// (KMAX x ne, fp32).  Used by both variants (the bidirectional one sums all segments).
-template <int DR>
-__global__ void __launch_bounds__(THREADS, 1) tc_segment_memory_kernel(const Args a,
-                                                                       const __grid_constant__ CUtensorMap vmap)
-{
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const Smem L(DR, a.kn16, a.d_v, true, false, false);
-    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
-    const int t = threadIdx.x, warp = t >> 5;
-    const int tok0 = seg * a.cps * C;
-    const int tok_end = min(a.N, tok0 + a.cps * C);
-    const uint32_t R_L = 0, R_S = 128;
-    Bars bars;
-    uint32_t tmem;
-    uint32_t ph_b = 0, ph_v = 0, ph_m = 0;
-    zero_region(smem + L.gk, 2u * C * 128u);
-    fill_ones(smem + L.ve, a.d_v);
-    cta_setup(smem, L, bars, 512, a, h, tmem);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t idesc_s = idesc_f16(128, (uint32_t)a.ne, 1, 1, 1, 1);
-    bool ok = wait_all(bars.bimg, ph_b, a.hdr, 10);
-    float *cst = reinterpret_cast<float *>(smem + L.cst);
-    uint4 x[DR / 8];
-    if (ok) load_x<DR>(a.KX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, x);
-    int nchunk = 0;
-    bool v_pending = false, mma_pending = false;
-    for (int base = tok0; ok && base < tok_end; base += C, ++nchunk) {
-        if (t == 0) load_v_chunk(smem + L.ve, &vmap, bars.v, a.d_v, base, bh);
-        v_pending = true;
-        build_a<DR>(smem + L.abuf, t, x);
-        publish_smem();
-        if (t == 0) {
-            issue_logits<DR>(tmem + R_L, sb + L.abuf, sb + L.bimg, a.kn16);
-            mma_commit(bars.mma);
-        }
-        mma_pending = true;
-        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 11))) break;
-        mma_pending = false;
-        softmax_row(tmem + lane_off + R_L, cst, a.K, t, base + t < tok_end, true, smem + L.gk);
-        const int nb = base + C;
-        load_x<DR>(a.KX, (long long)bh * a.N + nb + t, nb + t < tok_end, x);
-        publish_smem();
-        if (!(ok = wait_all(bars.v, ph_v, a.hdr, 12))) break;
-        v_pending = false;
-        if (t == 0) {
-            for (int s = 0; s < C / 16; ++s)
-                mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(sb + L.ve, s, C), idesc_s,
-                        (nchunk > 0 || s > 0) ? 1u : 0u);
-            mma_commit(bars.mma);
-        }
-        mma_pending = true;
-        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 13))) break;
-        mma_pending = false;
-    }
-    drain(bars, v_pending, ph_v, mma_pending, ph_m, a.hdr);
-    if (ok) {
-        float *dst = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + t) * a.ne;
-        if (nchunk == 0) {
-            for (int c = 0; c < a.ne; ++c) dst[c] = 0.f;
-        } else {
-            readout_state(tmem + lane_off + R_S, a.ne, t, nullptr, dst);
-        }
-    }
-    cta_teardown(tmem, 512);
-}
-
 // Causal: exclusive prefix of the segment memories within each slice (in place).
 // Bidirectional: the total over all segments, written to segment 0.
 // One thread per 4 consecutive floats of one slice; segments are read 8 at a time so that the
@@ -545,106 +398,6 @@ __global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, l
         }
     }
     if (!causal) base[0] = run;
-}
-
-// Chunked causal forward for one segment, starting from the exclusive prefix memory.
-template <int DR>
-__global__ void __launch_bounds__(THREADS, 1) tc_causal_chunked_kernel(const Args a,
-                                                                       const __grid_constant__ CUtensorMap vmap)
-{
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const Smem L(DR, a.kn16, a.d_v, true, true, true);
-    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
-    const int t = threadIdx.x, warp = t >> 5;
-    const int tok0 = seg * a.cps * C;
-    const int tok_end = min(a.N, tok0 + a.cps * C);
-    const uint32_t R_L = 0, R_O = 128, R_S = 288;    // L_K then P | L_Q then O | S
-    Bars bars;
-    uint32_t tmem;
-    uint32_t ph_b = 0, ph_v = 0, ph_m = 0, ph_m2 = 0;
-    zero_region(smem + L.gk, 2u * C * 128u);
-    fill_ones(smem + L.ve, a.d_v);
-    cta_setup(smem, L, bars, 512, a, h, tmem);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t id_p = idesc_f16(128, 128, 1, 1, 0, 0);
-    const uint32_t id_o = idesc_f16(128, (uint32_t)a.ne, 1, 1, 0, 1);
-    const uint32_t id_s = idesc_f16(128, (uint32_t)a.ne, 1, 1, 1, 1);
-    float *cst = reinterpret_cast<float *>(smem + L.cst);
-    // the segment's starting memory: TMEM (fp32, accumulated further) and bf16 operand copy
-    load_state(a.agg + (((size_t)bh * a.nseg + seg) * KMAX + t) * a.ne, tmem + lane_off + R_S, a.ne,
-               t, smem + L.sp);
-    bool ok = wait_all(bars.bimg, ph_b, a.hdr, 20);
-    uint4 xk[DR / 8], xq[DR / 8];
-    if (ok) {
-        load_x<DR>(a.KX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, xk);
-        load_x<DR>(a.QX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, xq);
-    }
-    bool v_pending = false, mma_pending = false;
-    for (int base = tok0; ok && base < tok_end; base += C) {
-        const bool valid = base + t < tok_end;
-        if (t == 0) load_v_chunk(smem + L.ve, &vmap, bars.v, a.d_v, base, bh);
-        v_pending = true;
-        // keys: logits -> Gamma_K
-        build_a<DR>(smem + L.abuf, t, xk);
-        publish_smem();
-        if (t == 0) {
-            issue_logits<DR>(tmem + R_L, sb + L.abuf, sb + L.bimg, a.kn16);
-            mma_commit(bars.mma);
-        }
-        mma_pending = true;
-        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 21))) break;
-        mma_pending = false;
-        // queries: logits (tensor cores) while the CUDA cores turn the key logits into Gamma_K
-        build_a<DR>(smem + L.abuf, t, xq);
-        publish_smem();
-        if (t == 0) {
-            issue_logits<DR>(tmem + R_O, sb + L.abuf, sb + L.bimg, a.kn16);
-            mma_commit(bars.mma2);
-        }
-        softmax_row(tmem + lane_off + R_L, cst, a.K, t, valid, true, smem + L.gk);
-        if (!(ok = wait_all(bars.mma2, ph_m2, a.hdr, 22))) {
-            mbar_wait(bars.mma2, ph_m2 ^ 1u, a.hdr, 92);   // bounded drain of the query logits
-            break;
-        }
-        const float srow = softmax_row(tmem + lane_off + R_O, cst, a.K, t, valid, false, smem + L.gq);
-        const int nb = base + C;   // next chunk's routing vectors, in flight behind the MMAs
-        load_x<DR>(a.KX, (long long)bh * a.N + nb + t, nb + t < tok_end, xk);
-        load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, xq);
-        publish_smem();
-        if (!(ok = wait_all(bars.v, ph_v, a.hdr, 23))) break;
-        v_pending = false;
-        if (t == 0) {
-            const uint32_t gq = sb + L.gq, gk = sb + L.gk, ve = sb + L.ve, sp = sb + L.sp;
-            for (int s = 0; s < a.kn16 / 16; ++s)   // P = Gamma_Q Gamma_K^T
-                mma_f16(tmem + R_L, kdesc(gq, s, C), kdesc(gk, s, C), id_p, s > 0);
-            for (int s = 0; s < a.kn16 / 16; ++s)   // O = Gamma_Q [S | Z]_{c-1}
-                mma_f16(tmem + R_O, kdesc(gq, s, C), mn32desc(sp, s, KMAX), id_o, s > 0);
-            for (int s = 0; s < C / 16; ++s)         // S += Gamma_K^T [V | 1]
-                mma_f16(tmem + R_S, mn128desc(gk, s, C), mn32desc(ve, s, C), id_s, 1u);
-            mma_commit(bars.mma);
-        }
-        mma_pending = true;
-        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 24))) break;
-        mma_pending = false;
-        mask_row(tmem + lane_off + R_L, t, smem + L.gq);                     // P -> bf16, j <= i
-        readout_state(tmem + lane_off + R_S, a.ne, t, smem + L.sp, nullptr);  // S_c for the next chunk
-        publish_smem();
-        if (t == 0) {
-            for (int s = 0; s < C / 16; ++s)         // O += tril(P) [V | 1]
-                mma_f16(tmem + R_O, kdesc(sb + L.gq, s, C), mn32desc(sb + L.ve, s, C), id_o, 1u);
-            mma_commit(bars.mma);
-        }
-        mma_pending = true;
-        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 25))) break;
-        mma_pending = false;
-        write_out(tmem + lane_off + R_O, a.d_v, a.eps * srow, valid, a.O, (long long)bh * a.N + base + t,
-                  a.out_f32);
-        sync_tc();
-    }
-    drain(bars, v_pending, ph_v, mma_pending, ph_m, a.hdr);
-    cta_teardown(tmem, 512);
 }
 
 // Bidirectional read: O = Gamma_Q [V~ | Z] / (.. + eps) for `cps` chunks of one slice.
@@ -870,6 +623,21 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
 // Dynamic shared memory for a kernel that allocates `tmem_cols` TMEM columns: at least enough
 // that no more CTAs fit on one SM (228 KB of shared memory) than its 512 columns can serve,
 // so no CTA ever waits inside tcgen05.alloc for a co-resident CTA.
+bool make_xmap(CUtensorMap *m, const void *X, int BH, int N, int d_r)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d_r, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d_r * 2, (cuuint64_t)N * d_r * 2};
+    cuuint32_t box[3] = {(cuuint32_t)d_r, (cuuint32_t)C, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = d_r == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : d_r == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(X), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_available() { return encode_fn() != nullptr; }
 
 uint32_t smem_for(uint32_t need, uint32_t tmem_cols)
@@ -902,17 +670,19 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     const int BH = s.B * s.H;
     CUtensorMap vmap;
     if (!make_vmap(&vmap, V, BH, s.N, s.d_v)) return GMA_ERR_CUDA;
-    const uint32_t sm_seg = smem_for(Smem(DR, p.kn16, s.d_v, true, false, false).total + 1024, 512);
-    if (!set_smem(tc_segment_memory_kernel<DR>, sm_seg)) return GMA_ERR_CUDA;
-    GMA_LAUNCH(KID_TC_CAUSAL_AGG, st,
-               (tc_segment_memory_kernel<DR><<<BH * p.nseg, THREADS, sm_seg, st>>>(a, vmap)));
+    {
+        const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, BH * p.nseg, st);
+        if (r != GMA_OK) return r;
+    }
     const int KD4 = KMAX * p.ne / 4;
     const long long tot4 = (long long)BH * KD4;
     GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st,
                (tc_scan_kernel<<<(unsigned)((tot4 + 255) / 256), 256, 0, st>>>(a.agg, tot4, p.nseg, KD4,
                                                                                 causal ? 1 : 0)));
     if (causal) {
-        const gma_status_t r = launch_causal_pipelined<DR>(a, vmap, BH * p.nseg, st);
+        CUtensorMap kmap, qmap;
+        if (!make_xmap(&kmap, a.KX, BH, s.N, DR) || !make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
+        const gma_status_t r = launch_causal_pipelined<DR>(a, vmap, kmap, qmap, BH * p.nseg, st);
         if (r != GMA_OK) return r;
     } else {
         const uint32_t sm = smem_for(Smem(DR, p.kn16, s.d_v, false, true, true).total + 1024, 256);

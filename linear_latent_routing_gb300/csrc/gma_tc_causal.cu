@@ -15,29 +15,30 @@
 //   S_c    = S_{c-1} + Gamma_K^T V_c                 (tensor cores, fp32 in TMEM)
 //   Z_c    = Z_{c-1} + column sums of Gamma_K        (CUDA cores, fp32)
 //
-// Warp roles (288 threads):
-//   warps 0-3  key side:   [x^2, x] of the keys, softmax -> Gamma_K (shared memory), column sums
-//                          (Z), readout of S_c into the bf16 operand copy used by the next chunk;
-//   warps 4-7  query side: [x^2, x] of the queries, softmax -> Gamma_Q (bf16, back into TMEM as the
-//                          A operand), normaliser, causal mask of P (bf16, back into TMEM), output;
-//   warp 8     control:    TMA of the value tiles (double-buffered) and every tcgen05.mma, issued
-//                          as soon as its operands are ready (mbarrier handshakes).
+// Warp roles (416 threads):
+//   warps 0-3   key side:   [x^2, x] of the keys, softmax -> Gamma_K (shared memory), column sums
+//                           (Z), readout of S_c into the bf16 operand copy used by the next chunk;
+//   warps 4-7   query side: [x^2, x] of the queries, softmax -> Gamma_Q (bf16, back into TMEM as
+//                           the A operand), normaliser, causal mask of P (bf16, back into TMEM);
+//   warps 8-11  output:     numerator rows from TMEM, divided by the normaliser, stored to O;
+//   warp 12     control:    TMA of the value tiles (double-buffered) and every tcgen05.mma, issued
+//                           as soon as its operands are ready (mbarrier handshakes).
 // Tensor memory (512 columns): [0,128) key logits, then P; [128,256) query logits, then Gamma_Q;
 // [256,384) output numerator; [384,512) the running memory S.
 // Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all roles leave their loops.
-#include "tc_common.cuh"
+#include "tc_rows.cuh"
 
 namespace gma {
 namespace tck {
 
 namespace {
 
-constexpr int CTHREADS = 288;
-enum BarId { B_BIMG, B_V0, B_V1, B_AK, B_AQ, B_GK, B_GQ, B_PS, B_SP, B_OF, B_LK, B_LQ, B_S, B_PQ, B_PV, NBAR };
+constexpr int CTHREADS = 416;   // key side 0-3, query side 4-7, output 8-11, control 12
+enum BarId { B_BIMG, B_V, B_XK, B_XQ, B_AK, B_AQ, B_GK, B_GQ, B_PS, B_SP, B_OF, B_LK, B_LQ, B_S, B_PQ, B_PV, NBAR };
 constexpr uint32_t R_LK = 0, R_LQ = 128, R_O = 256, R_S = 384;
 
 struct CausalSmem {
-    uint32_t bimg, ax, abuf, gk, sp, ve0, ve1, zbuf, bars, misc, total;
+    uint32_t bimg, ax, abuf, gk, sp, ve, xk, xq, zbuf, dsm, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ CausalSmem(int DR, int kn16, int d_v)
     {
@@ -49,101 +50,16 @@ struct CausalSmem {
         abuf = o; o = al(o + tile * (uint32_t)C);
         gk = o; o = al(o + 2u * C * 128u);
         sp = o; o = al(o + (uint32_t)d_v * KMAX * 2u);
-        ve0 = o; o = al(o + (uint32_t)d_v * C * 2u);
-        ve1 = o; o = al(o + (uint32_t)d_v * C * 2u);
+        ve = o; o = al(o + (uint32_t)d_v * C * 2u);
+        xk = o; o = al(o + (uint32_t)C * DR * 2u);   // staged key rows (TMA, swizzled)
+        xq = o; o = al(o + (uint32_t)C * DR * 2u);   // staged query rows
         zbuf = o; o += 2u * KMAX * 4u;
+        dsm = o; o += 2u * C * 8u;    // (row sum, normaliser) per row, by chunk parity
         bars = o; o += NBAR * 8u;
         misc = o; o += 16u;
         total = o;
     }
 };
-
-// Row maximum over the first K fp32 columns of this thread's TMEM lane (kc = ceil(K/32) chunks
-// of 32 columns, read two chunks per wait).
-__device__ __forceinline__ float row_max(uint32_t taddr, int K, int kc)
-{
-    float m = NEG_BIG;
-#pragma unroll
-    for (int c0 = 0; c0 < 4; c0 += 2) {
-        if (c0 < kc) {
-            uint32_t ra[32], rb[32];
-            tmem_ld32(taddr + 32 * c0, ra);
-            if (c0 + 1 < kc) tmem_ld32(taddr + 32 * (c0 + 1), rb);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if ((c0 + 1) * 32 <= K || 32 * c0 + j < K) m = fmaxf(m, __uint_as_float(ra[j]));
-            if (c0 + 1 < kc) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if ((c0 + 2) * 32 <= K || 32 * (c0 + 1) + j < K) m = fmaxf(m, __uint_as_float(rb[j]));
-            }
-        }
-    }
-    return m;
-}
-
-// exp2(L - m) of one chunk of 32 columns (0 beyond K), accumulating the sum.
-__device__ __forceinline__ void chunk_exp(uint32_t (&r)[32], int c, int K, float m, float &s)
-{
-    const bool full = (c + 1) * 32 <= K;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float e = (full || 32 * c + j < K) ? ex2(__uint_as_float(r[j]) - m) : 0.f;
-        r[j] = __float_as_uint(e);
-        s += e;
-    }
-}
-
-__device__ __forceinline__ uint32_t pk2(uint32_t a, uint32_t b, float sc)
-{
-    return pack_bf16(__uint_as_float(a) * sc, __uint_as_float(b) * sc);
-}
-
-// Key side: Gamma_K row `row` = softmax of the TMEM logits at tl, normalised (zeros when not
-// valid), as bf16 into the K-major SW128 tile gk.
-__device__ __noinline__ void key_softmax(uint32_t tl, int K, int kc, bool valid, uint8_t *gk, int k)
-{
-    const float m = row_max(tl, K, kc);
-    float sum = 0.f;
-    // exp2(L - m) as bf16 pairs straight into the row of the tile ...
-#pragma unroll
-    for (int c0 = 0; c0 < 4; c0 += 2) {
-        if (c0 < kc) {
-            uint32_t r2[2][32];
-            tmem_ld32(tl + 32 * c0, r2[0]);
-            if (c0 + 1 < kc) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int c2 = c0 + h2;
-                if (c2 < kc) {
-                    chunk_exp(r2[h2], c2, K, m, sum);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int e = 8 * q;
-                        *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c2 + q, C)) =
-                            make_uint4(pk2(r2[h2][e], r2[h2][e + 1], 1.f), pk2(r2[h2][e + 2], r2[h2][e + 3], 1.f),
-                                       pk2(r2[h2][e + 4], r2[h2][e + 5], 1.f), pk2(r2[h2][e + 6], r2[h2][e + 7], 1.f));
-                    }
-                }
-            }
-        }
-    }
-    // ... then divided by the row sum in place (zeros for rows beyond the sequence)
-    const float scf = valid ? 1.0f / sum : 0.f;
-    const __nv_bfloat162 sc2 = __floats2bfloat162_rn(scf, scf);
-    for (int q = 0; q < 4 * kc; ++q) {
-        uint4 *p4 = reinterpret_cast<uint4 *>(gk + sw128(k, q, C));
-        uint4 v = *p4;
-        __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&v);
-        b2[0] = __hmul2(b2[0], sc2);
-        b2[1] = __hmul2(b2[1], sc2);
-        b2[2] = __hmul2(b2[2], sc2);
-        b2[3] = __hmul2(b2[3], sc2);
-        *p4 = v;
-    }
-}
 
 // Key side: row k of the running memory S (d_v fp32 columns of TMEM at tl) as bf16 into the
 // MN-major SW32 operand tile sp.
@@ -199,15 +115,17 @@ __device__ __noinline__ float2 query_softmax(uint32_t tl, int K, int kc, bool va
                         for (int h2 = 0; h2 < 2; ++h2) {
                             const int c2 = c0 + h2;
                             if (c2 < kc) {
-                                chunk_exp(r2[h2], c2, K, m, srow);
+                                srow += chunk_exp(r2[h2], c2, K, m);
+                                float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                                 for (int q = 0; q < 8; ++q) {
                                     const float4 z = z4[8 * c2 + q];
-                                    den = fmaf(__uint_as_float(r2[h2][4 * q]), z.x, den);
-                                    den = fmaf(__uint_as_float(r2[h2][4 * q + 1]), z.y, den);
-                                    den = fmaf(__uint_as_float(r2[h2][4 * q + 2]), z.z, den);
-                                    den = fmaf(__uint_as_float(r2[h2][4 * q + 3]), z.w, den);
+                                    d4[0] = fmaf(__uint_as_float(r2[h2][4 * q]), z.x, d4[0]);
+                                    d4[1] = fmaf(__uint_as_float(r2[h2][4 * q + 1]), z.y, d4[1]);
+                                    d4[2] = fmaf(__uint_as_float(r2[h2][4 * q + 2]), z.z, d4[2]);
+                                    d4[3] = fmaf(__uint_as_float(r2[h2][4 * q + 3]), z.w, d4[3]);
                                 }
+                                den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
                                 uint32_t w[16];
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) w[j] = pk2(r2[h2][2 * j], r2[h2][2 * j + 1], sc);
@@ -224,7 +142,7 @@ __device__ __noinline__ float2 query_softmax(uint32_t tl, int K, int kc, bool va
 // pairs in place; returns the sum of the kept fp32 values.
 __device__ __noinline__ float causal_mask(uint32_t tl, int i)
 {
-    float den = 0.f;
+    float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c0 = 0; c0 < 4; c0 += 2) {
                 uint32_t r2[2][32];
@@ -240,14 +158,14 @@ __device__ __noinline__ float causal_mask(uint32_t tl, int i)
                         const int col = 32 * c2 + 2 * j;
                         const float p0 = col <= i ? __uint_as_float(r2[h2][2 * j]) : 0.f;
                         const float p1 = col + 1 <= i ? __uint_as_float(r2[h2][2 * j + 1]) : 0.f;
-                        den += p0 + p1;
+                        d4[j & 3] += p0 + p1;
                         w[j] = pack_bf16(p0, p1);
                     }
                     tmem_st16(tl + 16 * c2, w);
                 }
             }
             tmem_st_wait();
-    return den;
+    return (d4[0] + d4[1]) + (d4[2] + d4[3]);
 }
 
 // Query side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.
@@ -296,22 +214,13 @@ __device__ __noinline__ void write_output(uint32_t tl, int d_v, float inv, bool 
                 }
             }
 
-template <int DR>
-__device__ __forceinline__ void issue_logits_c(uint32_t d, uint32_t abuf, uint32_t bimg, uint32_t bconst,
-                                               uint32_t ax, int kn16)
-{
-    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
-    const uint32_t id = idesc_f16(128, (uint32_t)kn16, 0, 0, 0, 0);
-#pragma unroll
-    for (int s = 0; s < KA / 16; ++s) mma_f16(d, kdesc(abuf, s, C), kdesc(bimg, s, kn16), id, s > 0);
-    mma_f16(d, kdesc32(ax), kdesc32(bconst), id, 1u);   // + per-component constant
-}
-
 }  // namespace
 
 template <int DR>
 __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const Args a,
-                                                                          const __grid_constant__ CUtensorMap vmap)
+                                                                          const __grid_constant__ CUtensorMap vmap,
+                                                                          const __grid_constant__ CUtensorMap kmap,
+                                                                          const __grid_constant__ CUtensorMap qmap)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -320,6 +229,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 4);
     float *zbuf = reinterpret_cast<float *>(smem + L.zbuf);
+    float2 *dsm = reinterpret_cast<float2 *>(smem + L.dsm);
     const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
     const int t = threadIdx.x, warp = t >> 5;
     const int tok0 = seg * a.cps * C;
@@ -329,9 +239,9 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
     const int kc = (a.K + 31) >> 5;
 
     // ---------------------------------------------------------------- set-up (all threads)
-    if (warp == 8) {
-        if (t == 256) {
-            static const uint32_t counts[NBAR] = {1, 1, 1, 128, 128, 128, 128, 128, 128, 128, 1, 1, 1, 1, 1};
+    if (warp == 12) {
+        if (t == 384) {
+            static const uint32_t counts[NBAR] = {1, 1, 1, 1, 128, 128, 128, 128, 128, 128, 128, 1, 1, 1, 1, 1};
             for (int i = 0; i < NBAR; ++i) mbar_init(bars + i, counts[i]);
             *abort = 0;
             fence_mbar_init();
@@ -342,7 +252,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
         // Gamma_K tile: components the softmax never writes must read as zero
         for (uint32_t o = t * 16; o < 2u * C * 128u; o += 128 * 16)
             *reinterpret_cast<uint4 *>(smem + L.gk + o) = make_uint4(0, 0, 0, 0);
-    } else {
+    } else if (warp < 8) {
         // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
         const int i = t - 128;
         const uint32_t one2 = 0x3C003C00u;   // fp16 pair (1, 1)
@@ -357,95 +267,88 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ============================================================ control warp
-        if (t == 256) {
-            // value-tile ring of two buffers, selected by chunk parity (no runtime-indexed arrays)
-            auto ve = [&](int c) { return (c & 1) ? sb + L.ve1 : sb + L.ve0; };
-            auto vep = [&](int c) { return (c & 1) ? smem + L.ve1 : smem + L.ve0; };
+        if (t == 384) {
             const uint32_t id_p = idesc_f16(128, 128, 1, 1, 0, 0);
             const uint32_t id_o = idesc_f16(128, (uint32_t)d_v, 1, 1, 0, 1);
             const uint32_t id_s = idesc_f16(128, (uint32_t)d_v, 1, 1, 1, 1);
             const int ksteps = a.kn16 / 16;
-            bool vpend0 = false, vpend1 = false;   // a value-tile load in flight per buffer
+            // TMA loads in flight: the chunk index of the last one issued per buffer (each buffer's
+            // barrier completes one phase per load, and a load is issued only after the previous
+            // one into that buffer was consumed)
+            int last_v = -1, last_xk = -1, last_xq = -1;
             int last_pv = -1;
             bool ok = true;
             mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
             bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + B_BIMG);
             if (nch > 0) {
-                load_v_chunk(vep(0), &vmap, bars + B_V0, d_v, tok0, bh);
-                vpend0 = true;
+                load_x_tile(smem + L.xk, &kmap, bars + B_XK, DR, tok0, bh);
+                load_x_tile(smem + L.xq, &qmap, bars + B_XQ, DR, tok0, bh);
+                load_v_chunk(smem + L.ve, &vmap, bars + B_V, d_v, tok0, bh);
+                last_xk = last_xq = last_v = 0;
             }
             ok = mbar_wait_abortable(bars + B_BIMG, 0, a.hdr, 50, abort);
             const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
+            const uint32_t ve = sb + L.ve;
             for (int c = 0; ok && c < nch; ++c) {
                 const uint32_t ph = c & 1;
-                if (c > 0 && !(ok = mbar_wait_abortable(bars + B_PV, (c - 1) & 1, a.hdr, 51, abort))) break;
-                if (c + 1 < nch) {
-                    load_v_chunk(vep(c + 1), &vmap, bars + B_V0 + ((c + 1) & 1), d_v, tok0 + (c + 1) * C, bh);
-                    if ((c + 1) & 1) vpend1 = true; else vpend0 = true;
+                const int nxt = tok0 + (c + 1) * C;
+                if (c > 0) {
+                    // the previous chunk's tril(P) V is done with P (key logits region) and V
+                    if (!(ok = mbar_wait_abortable(bars + B_PV, (c - 1) & 1, a.hdr, 51, abort))) break;
+                    load_v_chunk(smem + L.ve, &vmap, bars + B_V, d_v, tok0 + c * C, bh);
+                    last_v = c;
                 }
-                // key logits
+                // key logits; the key rows are in the A tile, so the next chunk's may be staged
                 if (!(ok = mbar_wait_abortable(bars + B_AK, ph, a.hdr, 52, abort))) break;
+                if (c + 1 < nch) {
+                    load_x_tile(smem + L.xk, &kmap, bars + B_XK, DR, nxt, bh);
+                    last_xk = c + 1;
+                }
                 tc_fence_after();
                 issue_logits_c<DR>(tmem + R_LK, sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
                 mma_commit(bars + B_LK);
                 // query logits (query-side softmax of the previous chunk is done with R_LQ)
                 if (!(ok = mbar_wait_abortable(bars + B_AQ, ph, a.hdr, 53, abort))) break;
+                if (c + 1 < nch) {
+                    load_x_tile(smem + L.xq, &qmap, bars + B_XQ, DR, nxt, bh);
+                    last_xq = c + 1;
+                }
                 if (c > 0 && !(ok = mbar_wait_abortable(bars + B_PQ, (c - 1) & 1, a.hdr, 54, abort))) break;
                 tc_fence_after();
                 issue_logits_c<DR>(tmem + R_LQ, sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
                 mma_commit(bars + B_LQ);
-                // S update and the P / inter-chunk read, whichever has its operands first
-                bool s_done = false, pq_done = false;
-                const long long t0 = clock64();
-                while (!(s_done && pq_done)) {
-                    const bool gk = mbar_try_wait(bars + B_GK, ph);
-                    const bool spr = mbar_try_wait(bars + B_SP, ph);
-                    if (!s_done && gk && spr && mbar_try_wait(bars + B_V0 + (c & 1), (c >> 1) & 1)) {
-                        if (c & 1) vpend1 = false; else vpend0 = false;
-                        tc_fence_after();
-                        for (int s = 0; s < C / 16; ++s)   // S += Gamma_K^T V
-                            mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(ve(c), s, C), id_s, 1u);
-                        mma_commit(bars + B_S);
-                        s_done = true;
-                    }
-                    if (!pq_done && gk && spr && mbar_try_wait(bars + B_GQ, ph) &&
-                        (c == 0 || mbar_try_wait(bars + B_OF, (c - 1) & 1))) {
-                        tc_fence_after();
-                        for (int s = 0; s < ksteps; ++s)   // P = Gamma_Q Gamma_K^T
-                            mma_f16_tmem_a(tmem + R_LK, tmem + R_LQ + 8 * s, kdesc(sb + L.gk, s, C), id_p, s > 0);
-                        for (int s = 0; s < ksteps; ++s)   // O = Gamma_Q S_{c-1}
-                            mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + 8 * s, mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
-                        mma_commit(bars + B_PQ);
-                        pq_done = true;
-                    }
-                    if (*abort) { ok = false; break; }
-                    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-                        record_error(a.hdr, GMA_ERR_TIMEOUT, 55);
-                        *abort = 1;
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!ok) break;
+                // S update (its operands are usually ready first), then P and the inter-chunk read
+                if (!(ok = mbar_wait_abortable(bars + B_GK, ph, a.hdr, 55, abort))) break;
+                if (!(ok = mbar_wait_abortable(bars + B_SP, ph, a.hdr, 58, abort))) break;
+                if (!(ok = mbar_wait_abortable(bars + B_V, ph, a.hdr, 59, abort))) break;
+                tc_fence_after();
+                for (int s = 0; s < C / 16; ++s)   // S += Gamma_K^T V
+                    mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(ve, s, C), id_s, 1u);
+                mma_commit(bars + B_S);
+                if (!(ok = mbar_wait_abortable(bars + B_GQ, ph, a.hdr, 60, abort))) break;
+                if (c > 0 && !(ok = mbar_wait_abortable(bars + B_OF, (c - 1) & 1, a.hdr, 61, abort))) break;
+                tc_fence_after();
+                for (int s = 0; s < ksteps; ++s)   // P = Gamma_Q Gamma_K^T
+                    mma_f16_tmem_a(tmem + R_LK, tmem + R_LQ + 8 * s, kdesc(sb + L.gk, s, C), id_p, s > 0);
+                for (int s = 0; s < ksteps; ++s)   // O = Gamma_Q S_{c-1}
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + 8 * s, mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
+                mma_commit(bars + B_PQ);
                 // intra-chunk: O += tril(P) V
                 if (!(ok = mbar_wait_abortable(bars + B_PS, ph, a.hdr, 56, abort))) break;
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s)
-                    mma_f16_tmem_a(tmem + R_O, tmem + R_LK + 8 * s, mn32desc(ve(c), s, C), id_o, 1u);
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_LK + 8 * s, mn32desc(ve, s, C), id_o, 1u);
                 mma_commit(bars + B_PV);
                 last_pv = c;
             }
-            // drain: MMAs complete in issue order, so the last commit covers them all
+            // drain: MMAs complete in issue order, so the last commit covers them all; TMA loads
+            // still in flight (only after a timeout) complete before shared memory is released
             if (last_pv >= 0) mbar_wait(bars + B_PV, last_pv & 1, a.hdr, 57);
-            // a value-tile load that was issued but never consumed (only after a timeout): the most
-            // recent chunk of that buffer's parity
-            if (vpend0 || vpend1) {
-                for (int c = nch - 1; c >= 0 && c >= nch - 2; --c) {
-                    if ((c & 1) ? vpend1 : vpend0) mbar_wait(bars + B_V0 + (c & 1), (c >> 1) & 1, a.hdr, 58);
-                }
-            }
+            if (last_v >= 0) mbar_wait(bars + B_V, last_v & 1, a.hdr, 58);
+            if (last_xk >= 0) mbar_wait(bars + B_XK, last_xk & 1, a.hdr, 58);
+            if (last_xq >= 0) mbar_wait(bars + B_XQ, last_xq & 1, a.hdr, 58);
         }
     } else if (warp < 4) {
         // ============================================================ key side
@@ -476,20 +379,19 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bars + B_SP);   // phase 0: S_start ready
-        uint4 x[DR / 8];
-        load_x<DR>(a.KX, (long long)bh * a.N + tok0 + k, tok0 + k < tok_end, x);
         for (int c = 0; c < nch; ++c) {
             const uint32_t ph = c & 1;
             const int base = tok0 + c * C;
             if (c > 0 && !mbar_wait_abortable(bars + B_LQ, (c - 1) & 1, a.hdr, 60, abort)) break;
-            build_a<DR>(smem + L.abuf, k, x);
+            if (!mbar_wait_abortable(bars + B_XK, ph, a.hdr, 67, abort)) break;
+            build_a_s<DR>(smem + L.abuf, k, smem + L.xk);
             fence_proxy_async_smem();
             mbar_arrive(bars + B_AK);
             if (!mbar_wait_abortable(bars + B_LK, ph, a.hdr, 61, abort)) break;
             if (c > 0 && !mbar_wait_abortable(bars + B_S, (c - 1) & 1, a.hdr, 62, abort)) break;
             if (c > 0 && !mbar_wait_abortable(bars + B_PQ, (c - 1) & 1, a.hdr, 63, abort)) break;
             tc_fence_after();
-            key_softmax(lane + R_LK, a.K, kc, base + k < tok_end, smem + L.gk, k);
+            key_softmax<false>(lane + R_LK, a.K, kc, base + k < tok_end, smem + L.gk, k);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bars + B_GK);
@@ -499,10 +401,13 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             {
                 const int q = k >> 3;
                 const uint32_t col = (uint32_t)(k & 7) * 2;
-                float zs = 0.f;
-                for (int j = 0; j < C; ++j)
-                    zs += __bfloat162float(*reinterpret_cast<const bf16 *>(smem + L.gk + sw128(j, q, C) + col));
-                zrun += zs;
+                float zs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int j = 0; j < C; j += 8) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        zs[u] += __bfloat162float(*reinterpret_cast<const bf16 *>(smem + L.gk + sw128(j + u, q, C) + col));
+                }
+                zrun += ((zs[0] + zs[1]) + (zs[2] + zs[3])) + ((zs[4] + zs[5]) + (zs[6] + zs[7]));
             }
             // readout of S_c (after the update and the read of S_{c-1} that it overwrites)
             if (!mbar_wait_abortable(bars + B_S, ph, a.hdr, 64, abort)) break;
@@ -513,21 +418,18 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bars + B_SP);
-            // next chunk's keys: in flight while the control warp waits for this chunk's output
-            load_x<DR>(a.KX, (long long)bh * a.N + base + C + k, base + C + k < tok_end, x);
         }
-    } else {
+    } else if (warp < 8) {
         // ============================================================ query side
         const int i = t - 128;
         const uint32_t lane = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-        uint4 x[DR / 8];
-        load_x<DR>(a.QX, (long long)bh * a.N + tok0 + i, tok0 + i < tok_end, x);
         for (int c = 0; c < nch; ++c) {
             const uint32_t ph = c & 1;
             const int base = tok0 + c * C;
             const bool valid = base + i < tok_end;
             if (!mbar_wait_abortable(bars + B_LK, ph, a.hdr, 70, abort)) break;
-            build_a<DR>(smem + L.abuf, i, x);
+            if (!mbar_wait_abortable(bars + B_XQ, ph, a.hdr, 75, abort)) break;
+            build_a_s<DR>(smem + L.abuf, i, smem + L.xq);
             fence_proxy_async_smem();
             mbar_arrive(bars + B_AQ);
             if (!mbar_wait_abortable(bars + B_LQ, ph, a.hdr, 71, abort)) break;
@@ -545,23 +447,31 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             if (!mbar_wait_abortable(bars + B_PQ, ph, a.hdr, 73, abort)) break;
             tc_fence_after();
             den += causal_mask(lane + R_LK, i);
+            dsm[ph * C + i] = make_float2(srow, den);
             tc_fence_before();
             mbar_arrive(bars + B_PS);
-            // output
-            if (!mbar_wait_abortable(bars + B_PV, ph, a.hdr, 74, abort)) break;
+        }
+    } else {
+        // ============================================================ output
+        const int i = t - 256;
+        const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            const int base = tok0 + c * C;
+            if (!mbar_wait_abortable(bars + B_PS, ph, a.hdr, 77, abort)) break;   // (sum, normaliser)
+            if (!mbar_wait_abortable(bars + B_PV, ph, a.hdr, 74, abort)) break;   // numerator done
             tc_fence_after();
-            write_output(lane + R_O, d_v, 1.0f / (den + a.eps * srow), valid, a.O,
+            const float2 sd = dsm[ph * C + i];
+            write_output(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), base + i < tok_end, a.O,
                          (long long)bh * a.N + base + i, a.out_f32);
             tc_fence_before();
             mbar_arrive(bars + B_OF);
-            // next chunk's queries: in flight while the next key logits are computed
-            load_x<DR>(a.QX, (long long)bh * a.N + base + C + i, base + C + i < tok_end, x);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 8) tmem_dealloc(tmem, 512);
+    if (warp == 12) tmem_dealloc(tmem, 512);
 }
 
 // Shared memory the pipelined causal kernel needs (0 if the shape does not fit).
@@ -572,18 +482,22 @@ uint32_t causal_pipelined_smem(int d_r, int kn16, int d_v)
 }
 
 template <int DR>
-gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st)
+gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap,
+                                     const CUtensorMap &qmap, int nblocks, cudaStream_t st)
 {
     const uint32_t sm = causal_pipelined_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_causal_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st, (tc_causal_pipelined_kernel<DR><<<nblocks, CTHREADS, sm, st>>>(a, vmap)));
+    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st, (tc_causal_pipelined_kernel<DR><<<nblocks, CTHREADS, sm, st>>>(a, vmap, kmap, qmap)));
     return GMA_OK;
 }
 
-template gma_status_t launch_causal_pipelined<16>(const Args &, const CUtensorMap &, int, cudaStream_t);
-template gma_status_t launch_causal_pipelined<32>(const Args &, const CUtensorMap &, int, cudaStream_t);
-template gma_status_t launch_causal_pipelined<64>(const Args &, const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_pipelined<16>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                                     const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_pipelined<32>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                                     const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_pipelined<64>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                                     const CUtensorMap &, int, cudaStream_t);
 
 }  // namespace tck
 }  // namespace gma

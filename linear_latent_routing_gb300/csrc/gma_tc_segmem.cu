@@ -1,0 +1,236 @@
+// gma_tc_segmem.cu -- segment memories for the tcgen05 family (sm_103a), warp-specialised.
+//
+// Method: page "Attention par Mélange Gaussien (GMA)" (gist.science/fr/paper/2606.18283),
+// Méthodologie §2, write phase: keys write the latent memory V~ = Gamma_K^T V and its
+// normaliser Z = Gamma_K^T 1.  Here over one segment of one (batch, head) slice:
+//   agg[bh][seg][k][c] = sum_{j in segment} gamma_K[j][k] * [v_j | 1][c]   (fp32; c = d_v is Z).
+// The bidirectional variant sums all segments of a slice; the causal variant scans them into
+// exclusive prefixes, each the starting memory of the chunked kernel's segment.
+//
+// Warp roles (288 threads): two key-side groups of four warps take alternate chunks of 128
+// tokens ([x^2, x], softmax -> Gamma_K in their own shared-memory tile); warp 8 issues the TMA of
+// the value tiles and the tcgen05.mma's: the logits into the chunk's own TMEM columns and
+// S += Gamma_K^T [V | 1] into the running memory.  Logits, Gamma_K and value tiles are double
+// buffered, so one group's softmax overlaps the other group's logits and memory update.
+// Barriers are per buffer, so no waiter can fall two phases behind.
+#include "tc_rows.cuh"
+
+namespace gma {
+namespace tck {
+
+namespace {
+
+constexpr int STHREADS = 288;
+enum SBar { S_BIMG, S_AK, S_LK0, S_LK1, S_GK0, S_GK1, S_SD0, S_SD1, S_V0, S_V1, S_NBAR };
+constexpr uint32_t SR_L0 = 0, SR_L1 = 128, SR_S = 256;
+
+struct SegSmem {
+    uint32_t bimg, ax, abuf, gk0, gk1, ve0, ve1, bars, misc, total;
+    __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    __host__ __device__ SegSmem(int DR, int kn16, int d_v)
+    {
+        const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
+        const uint32_t tile = ka / 64u * 128u;
+        const uint32_t vbytes = (uint32_t)(d_v + 16) * C * 2u;   // value blocks + one block of ones
+        uint32_t o = 0;
+        bimg = o; o = al(o + tile * (uint32_t)kn16 + 32u * (uint32_t)kn16);
+        ax = o; o = al(o + (uint32_t)C * 32u);
+        abuf = o; o = al(o + tile * (uint32_t)C);
+        gk0 = o; o = al(o + 2u * C * 128u);
+        gk1 = o; o = al(o + 2u * C * 128u);
+        ve0 = o; o = al(o + vbytes);
+        ve1 = o; o = al(o + vbytes);
+        bars = o; o += S_NBAR * 8u;
+        misc = o; o += 16u;
+        total = o;
+    }
+};
+
+}  // namespace
+
+template <int DR>
+__global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kernel(const Args a,
+                                                                                  const __grid_constant__ CUtensorMap vmap)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const SegSmem L(DR, a.kn16, a.d_v);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 4);
+    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int tok0 = seg * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    const int nch = (tok_end - tok0 + C - 1) / C;
+    const int d_v = a.d_v, ne = a.ne;
+    const int kc = (a.K + 31) >> 5;
+
+    // ---------------------------------------------------------------- set-up
+    if (warp == 8) {
+        if (t == 256) {
+            for (int i = 0; i < S_NBAR; ++i) mbar_init(bars + i, (i == S_AK || i == S_GK0 || i == S_GK1) ? 128u : 1u);
+            *abort = 0;
+            fence_mbar_init();
+        }
+        __syncwarp();
+        tmem_alloc(tslot, 512);
+    } else {
+        // zero both Gamma_K tiles (components the softmax never writes), ones blocks of [V | 1],
+        // and the constant operand (1, 1, 0, ...) of the logits
+        const int u = t;   // 0..255
+        for (uint32_t o = u * 16; o < 2u * C * 128u; o += 256 * 16) {
+            *reinterpret_cast<uint4 *>(smem + L.gk0 + o) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(smem + L.gk1 + o) = make_uint4(0, 0, 0, 0);
+        }
+        const uint32_t one2 = 0x3F803F80u;   // bf16 pair (1, 1)
+        const uint32_t o1 = (uint32_t)(d_v / 16) * C * 32;
+        for (uint32_t o = u * 16; o < (uint32_t)C * 32; o += 256 * 16) {
+            *reinterpret_cast<uint4 *>(smem + L.ve0 + o1 + o) = make_uint4(one2, one2, one2, one2);
+            *reinterpret_cast<uint4 *>(smem + L.ve1 + o1 + o) = make_uint4(one2, one2, one2, one2);
+        }
+        if (u < C) {
+            const int flip = (u >> 2) & 1;
+            *reinterpret_cast<uint4 *>(smem + L.ax + u * 32 + (flip << 4)) = make_uint4(0x3C003C00u, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(smem + L.ax + u * 32 + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t sb = smem_u32(smem);
+
+    if (warp == 8) {
+        // ============================================================ control warp
+        if (t == 256) {
+            auto ve = [&](int c) { return (c & 1) ? L.ve1 : L.ve0; };
+            auto gk = [&](int c) { return (c & 1) ? L.gk1 : L.gk0; };
+            const uint32_t id_s = idesc_f16(128, (uint32_t)ne, 1, 1, 1, 1);
+            bool ok = true;
+            int last_sd = -1;
+            bool vpend0 = false, vpend1 = false;
+            mbar_arrive_expect_tx(bars + S_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + S_BIMG);
+            for (int c = 0; c < 2 && c < nch; ++c) {
+                load_v_chunk(smem + ve(c), &vmap, bars + S_V0 + c, d_v, tok0 + c * C, bh);
+                if (c) vpend1 = true; else vpend0 = true;
+            }
+            ok = mbar_wait_abortable(bars + S_BIMG, 0, a.hdr, 80, abort);
+            const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
+            // S update of chunk j: Gamma_K tile and value tile of buffer j & 1
+            auto update = [&](int j) -> bool {
+                const int g = j & 1, n = j >> 1;
+                if (!mbar_wait_abortable(bars + S_GK0 + g, n & 1, a.hdr, 81, abort)) return false;
+                if (!mbar_wait_abortable(bars + S_V0 + g, n & 1, a.hdr, 82, abort)) return false;
+                if (g) vpend1 = false; else vpend0 = false;
+                tc_fence_after();
+                for (int s = 0; s < C / 16; ++s)
+                    mma_f16(tmem + SR_S, mn128desc(sb + gk(j), s, C), mn32desc(sb + ve(j), s, C), id_s,
+                            (j > 0 || s > 0) ? 1u : 0u);
+                mma_commit(bars + S_SD0 + g);
+                last_sd = j;
+                return true;
+            };
+            for (int c = 0; ok && c < nch; ++c) {
+                const int g = c & 1;
+                if (!(ok = mbar_wait_abortable(bars + S_AK, c & 1, a.hdr, 83, abort))) break;
+                tc_fence_after();
+                issue_logits_c<DR>(tmem + (g ? SR_L1 : SR_L0), sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
+                mma_commit(bars + S_LK0 + g);
+                if (c >= 1) {
+                    if (!(ok = update(c - 1))) break;
+                    // the value buffer of chunk c-1 is free once its update is done: load chunk c+1
+                    if (c + 1 < nch) {
+                        if (!(ok = mbar_wait_abortable(bars + S_SD0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 84, abort)))
+                            break;
+                        load_v_chunk(smem + ve(c + 1), &vmap, bars + S_V0 + ((c + 1) & 1), d_v, tok0 + (c + 1) * C, bh);
+                        if ((c + 1) & 1) vpend1 = true; else vpend0 = true;
+                    }
+                }
+            }
+            if (ok && nch > 0) ok = update(nch - 1);
+            if (last_sd >= 0) mbar_wait(bars + S_SD0 + (last_sd & 1), (last_sd >> 1) & 1, a.hdr, 85);
+            if (vpend0 || vpend1) {
+                for (int c = nch - 1; c >= 0 && c >= nch - 2; --c)
+                    if ((c & 1) ? vpend1 : vpend0) mbar_wait(bars + S_V0 + (c & 1), (c >> 1) & 1, a.hdr, 86);
+            }
+        }
+    } else {
+        // ============================================================ key-side groups
+        const int g = warp >> 2;            // group: chunks c with c % 2 == g
+        const int k = t & 127;              // TMEM lane, token row, component row
+        const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        uint8_t *gk = smem + (g ? L.gk1 : L.gk0);
+        uint4 x[DR / 8];
+        if (g < nch) load_x<DR>(a.KX, (long long)bh * a.N + tok0 + g * C + k, tok0 + g * C + k < tok_end, x);
+        for (int c = g; c < nch; c += 2) {
+            const int n = c >> 1;
+            const int base = tok0 + c * C;
+            // the [x^2, x] buffer is free once the previous chunk's logits are done
+            if (c >= 1 && !mbar_wait_abortable(bars + S_LK0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 90, abort)) break;
+            build_a<DR>(smem + L.abuf, k, x);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + S_AK);
+            if (!mbar_wait_abortable(bars + S_LK0 + g, n & 1, a.hdr, 91, abort)) break;
+            if (c >= 2 && !mbar_wait_abortable(bars + S_SD0 + g, (n - 1) & 1, a.hdr, 92, abort)) break;
+            tc_fence_after();
+            key_softmax<true>(lane + (g ? SR_L1 : SR_L0), a.K, kc, base + k < tok_end, gk, k);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars + S_GK0 + g);
+            const int nb = base + 2 * C;
+            load_x<DR>(a.KX, (long long)bh * a.N + nb + k, nb + k < tok_end, x);
+        }
+        // group 0 writes the segment's memory once the last update is done
+        if (g == 0 && !*abort) {
+            float *dst = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + k) * ne;
+            const int last = nch - 1;
+            bool ok = nch > 0 && mbar_wait_abortable(bars + S_SD0 + (last & 1), (last >> 1) & 1, a.hdr, 93, abort);
+            if (nch == 0) {
+                for (int cc = 0; cc < ne; ++cc) dst[cc] = 0.f;
+            } else if (ok) {
+                tc_fence_after();
+                for (int b = 0; b < ne / 16; ++b) {
+                    uint32_t r[16];
+                    tmem_ld16(lane + SR_S + 16 * b, r);
+                    tmem_ld_wait();
+                    float4 *o4 = reinterpret_cast<float4 *>(dst + 16 * b);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        o4[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 8) tmem_dealloc(tmem, 512);
+}
+
+uint32_t segmem_pipelined_smem(int d_r, int kn16, int d_v)
+{
+    const uint32_t need = SegSmem(d_r, kn16, d_v).total + 1024;
+    return need <= 227u * 1024u ? smem_for(need, 512) : 0;
+}
+
+template <int DR>
+gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st)
+{
+    const uint32_t sm = segmem_pipelined_smem(DR, a.kn16, a.d_v);
+    if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!set_smem(tc_segment_memory_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    GMA_LAUNCH(KID_TC_CAUSAL_AGG, st,
+               (tc_segment_memory_pipelined_kernel<DR><<<nblocks, STHREADS, sm, st>>>(a, vmap)));
+    return GMA_OK;
+}
+
+template gma_status_t launch_segmem_pipelined<16>(const Args &, const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_segmem_pipelined<32>(const Args &, const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_segmem_pipelined<64>(const Args &, const CUtensorMap &, int, cudaStream_t);
+
+}  // namespace tck
+}  // namespace gma

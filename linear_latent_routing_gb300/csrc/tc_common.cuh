@@ -135,6 +135,53 @@ __device__ __forceinline__ void build_a(uint8_t *abuf, int row, const uint4 (&x)
     }
 }
 
+// Byte offset of 16-byte chunk s of row r in a staged x tile (rows of DR bf16 = 2*DR bytes, TMA
+// swizzle of the same width: 32, 64 or 128 bytes).
+template <int DR>
+__device__ __forceinline__ uint32_t xs_off(int r, int s)
+{
+    constexpr uint32_t M = DR == 64 ? 7u : DR == 32 ? 3u : 1u;
+    const uint32_t o = (uint32_t)r * (DR * 2) + (uint32_t)s * 16u;
+    return o ^ (((o >> 7) & M) << 4);
+}
+
+// build_a for token row `row` from the staged (TMA, swizzled) x tile xs: each 16-byte chunk of
+// the row (8 bf16) gives one chunk of x^2 and one of x (fp16).
+template <int DR>
+__device__ __forceinline__ void build_a_s(uint8_t *abuf, int row, const uint8_t *xs)
+{
+    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
+#pragma unroll
+    for (int q = 0; q < DR / 8; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(xs + xs_off<DR>(row, q));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t sq[4], li[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            sq[j] = pack_f16(lo * lo, hi * hi);
+            li[j] = pack_f16(lo, hi);
+        }
+        *reinterpret_cast<uint4 *>(abuf + sw128(row, q, C)) = make_uint4(sq[0], sq[1], sq[2], sq[3]);
+        *reinterpret_cast<uint4 *>(abuf + sw128(row, DR / 8 + q, C)) = make_uint4(li[0], li[1], li[2], li[3]);
+    }
+#pragma unroll
+    for (int q = DR / 4; q < KA / 8; ++q) *reinterpret_cast<uint4 *>(abuf + sw128(row, q, C)) = make_uint4(0, 0, 0, 0);
+}
+
+// TMA of the x rows [tok, tok + 128) of slice bh (3-D map {DR, N, BH}, box {DR, 128, 1}; rows past
+// the sequence read as zeros) into the staging tile xs.
+__device__ __forceinline__ void load_x_tile(uint8_t *xs, const CUtensorMap *map, uint64_t *bar, int DR, int tok,
+                                            int bh)
+{
+    mbar_arrive_expect_tx(bar, (uint32_t)(C * DR * 2));
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(xs)),
+        "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(0), "r"(tok), "r"(bh)
+        : "memory");
+}
+
 template <int DR>
 __device__ __forceinline__ void load_x(const bf16 *X, long long row, bool valid, uint4 (&x)[DR / 8])
 {
@@ -162,10 +209,16 @@ __device__ __forceinline__ void load_v_chunk(uint8_t *ve, const CUtensorMap *vma
 // ------------------------------------------------------------------ the pipelined causal kernel
 uint32_t causal_pipelined_smem(int d_r, int kn16, int d_v);
 template <int DR>
-gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st);
+gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap,
+                                     const CUtensorMap &qmap, int nblocks, cudaStream_t st);
+
+uint32_t segmem_pipelined_smem(int d_r, int kn16, int d_v);
+template <int DR>
+gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st);
 
 // ------------------------------------------------------------------ host helpers (gma_tc.cu)
 bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v);
+bool make_xmap(CUtensorMap *m, const void *X, int BH, int N, int d_r);
 uint32_t smem_for(uint32_t need, uint32_t tmem_cols);
 bool encode_available();
 

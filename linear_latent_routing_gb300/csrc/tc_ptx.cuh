@@ -51,6 +51,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the same condition (never suspends the thread); for polling several
+// barriers at once.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes or about
+// `hint_ns` nanoseconds pass, instead of coming back to poll.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+                 : "memory");
+    return ok != 0;
+}
+
 // About one second at GB300 clocks.
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000ll;
 
@@ -77,13 +105,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 
 // Like mbar_wait, but also gives up as soon as another thread of the CTA has set *abort after
 // a timeout of its own, so one lost wait does not cost every other wait a full second.
+// The waiting thread sleeps inside try_wait (up to ~1 ms per round), so waiting warps take no
+// issue slots or shared-memory bandwidth from the warps that are working.
 __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t parity, WsHeader *hdr,
                                                     unsigned where, volatile int *abort)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
         if (*abort) return false;
         if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
             record_error(hdr, GMA_ERR_TIMEOUT, where);

@@ -1,0 +1,168 @@
+// tc_rows.cuh -- per-row softmax helpers and the logits MMA shared by the tcgen05 kernels that
+// work one chunk of 128 tokens at a time (one thread per TMEM lane / token row).
+#pragma once
+
+#include "tc_common.cuh"
+
+namespace gma {
+namespace tck {
+namespace {
+
+// The row phases below run on one warp per SM sub-partition, so their speed is set by
+// instruction latency: loads are issued together and reductions use independent accumulators.
+
+// Row maximum over the first K fp32 columns of this thread's TMEM lane (kc = ceil(K/32) chunks
+// of 32 columns, read two chunks per wait).
+__device__ __forceinline__ float row_max(uint32_t taddr, int K, int kc)
+{
+    float m[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m[u] = NEG_BIG;
+#pragma unroll
+    for (int c0 = 0; c0 < 4; c0 += 2) {
+        if (c0 < kc) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32(taddr + 32 * c0, ra);
+            if (c0 + 1 < kc) tmem_ld32(taddr + 32 * (c0 + 1), rb);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if ((c0 + 1) * 32 <= K || 32 * c0 + j < K) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(ra[j]));
+            if (c0 + 1 < kc) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if ((c0 + 2) * 32 <= K || 32 * (c0 + 1) + j < K) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(rb[j]));
+            }
+        }
+    }
+    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+// exp2(L - m) of one chunk of 32 columns (0 beyond K), in place; returns the chunk's sum.
+__device__ __forceinline__ float chunk_exp(uint32_t (&r)[32], int c, int K, float m)
+{
+    const bool full = (c + 1) * 32 <= K;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float e = (full || 32 * c + j < K) ? ex2(__uint_as_float(r[j]) - m) : 0.f;
+        r[j] = __float_as_uint(e);
+        s[j & 3] += e;
+    }
+    return (s[0] + s[1]) + (s[2] + s[3]);
+}
+
+// Elementwise product of two bf16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pk2(uint32_t a, uint32_t b, float sc)
+{
+    return pack_bf16(__uint_as_float(a) * sc, __uint_as_float(b) * sc);
+}
+
+// Key side: Gamma_K row `row` = softmax of the TMEM logits at tl, normalised (zeros when not
+// valid), as bf16 into the K-major SW128 tile gk.  PAIR: maximum first, then two 32-column chunks
+// per TMEM wait, the bf16 exponentials rescaled in shared memory; otherwise two passes over the
+// row with a running maximum and sum, each tile element written once.
+template <bool PAIR>
+__device__ __noinline__ void key_softmax(uint32_t tl, int K, int kc, bool valid, uint8_t *gk, int k)
+{
+    float m = 0.f, sum = 0.f;
+    // exp2(L - m) as bf16 pairs straight into the row of the tile ...
+    if (PAIR) {
+        m = row_max(tl, K, kc);
+#pragma unroll
+        for (int c0 = 0; c0 < 4; c0 += 2) {
+            if (c0 < kc) {
+                uint32_t r2[2][32];
+                tmem_ld32(tl + 32 * c0, r2[0]);
+                if (c0 + 1 < kc) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c2 = c0 + h2;
+                    if (c2 < kc) {
+                        sum += chunk_exp(r2[h2], c2, K, m);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int e = 8 * q;
+                            *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c2 + q, C)) =
+                                make_uint4(pk2(r2[h2][e], r2[h2][e + 1], 1.f), pk2(r2[h2][e + 2], r2[h2][e + 3], 1.f),
+                                           pk2(r2[h2][e + 4], r2[h2][e + 5], 1.f), pk2(r2[h2][e + 6], r2[h2][e + 7], 1.f));
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // first pass: running maximum and sum of exp2(L - max); second pass: the normalised
+        // values, written to the tile once (the exponentials are evaluated twice)
+        float mx = NEG_BIG, sm = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (c < kc) {
+                uint32_t r[32];
+                tmem_ld32(tl + 32 * c, r);
+                tmem_ld_wait();
+                float cm[4] = {NEG_BIG, NEG_BIG, NEG_BIG, NEG_BIG};
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if ((c + 1) * 32 <= K || 32 * c + j < K) cm[j & 3] = fmaxf(cm[j & 3], __uint_as_float(r[j]));
+                const float mn = fmaxf(mx, fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3])));
+                sm = sm * ex2(mx - mn) + chunk_exp(r, c, K, mn);
+                mx = mn;
+            }
+        }
+        const float scf = valid ? 1.0f / sm : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (c < kc) {
+                uint32_t r[32];
+                tmem_ld32(tl + 32 * c, r);
+                tmem_ld_wait();
+                const bool full = (c + 1) * 32 <= K;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int j = 8 * q + 2 * h;
+                        const float e0 = (full || 32 * c + j < K) ? ex2(__uint_as_float(r[j]) - mx) * scf : 0.f;
+                        const float e1 = (full || 32 * c + j + 1 < K) ? ex2(__uint_as_float(r[j + 1]) - mx) * scf : 0.f;
+                        w[h] = pack_bf16(e0, e1);
+                    }
+                    *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c + q, C)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+        return;
+    }
+    // ... then divided by the row sum in place (zeros for rows beyond the sequence)
+    const float scf = valid ? 1.0f / sum : 0.f;
+    const uint32_t sc2 = pack_bf16(scf, scf);
+    for (int q = 0; q < 4 * kc; ++q) {
+        uint4 *p4 = reinterpret_cast<uint4 *>(gk + sw128(k, q, C));
+        const uint4 v = *p4;
+        *p4 = make_uint4(mul_bf16x2(v.x, sc2), mul_bf16x2(v.y, sc2), mul_bf16x2(v.z, sc2), mul_bf16x2(v.w, sc2));
+    }
+}
+
+template <int DR>
+__device__ __forceinline__ void issue_logits_c(uint32_t d, uint32_t abuf, uint32_t bimg, uint32_t bconst,
+                                               uint32_t ax, int kn16)
+{
+    constexpr int KA = DR * 2 < 64 ? 64 : DR * 2;
+    const uint32_t id = idesc_f16(128, (uint32_t)kn16, 0, 0, 0, 0);
+#pragma unroll
+    for (int s = 0; s < KA / 16; ++s) mma_f16(d, kdesc(abuf, s, C), kdesc(bimg, s, kn16), id, s > 0);
+    mma_f16(d, kdesc32(ax), kdesc32(bconst), id, 1u);   // + per-component constant
+}
+
+}  // namespace
+}  // namespace tck
+}  // namespace gma
