@@ -713,6 +713,9 @@ bool tc_supported(const gma_shape_t &s, int variant)
     if (s.dtype != GMA_BF16 || (s.flags & GMA_FLAG_SIMT)) return false;
     if (!(s.d_r == 16 || s.d_r == 32 || s.d_r == 64)) return false;
     if (s.K > tck::KMAX) return false;
+    // value tiles move in 16-column TMA boxes, and the numerator and memory hold d_v <= 128
+    // TMEM columns each
+    if (s.d_v % 16 != 0 || s.d_v > 128) return false;
     (void)variant;
     return tck::encode_fn() != nullptr;
 }

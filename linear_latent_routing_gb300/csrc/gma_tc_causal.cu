@@ -6,24 +6,27 @@
 // read phase O = Gamma_Q V~ / (Gamma_Q Z + eps)).
 //
 // One CTA handles one segment of one (batch, head) slice, starting from the segment's exclusive
-// prefix memory S_start (V~ part and Z part), in chunks of C = 128 tokens:
-//   Gamma_K, Gamma_Q       responsibilities of the chunk's keys and queries
-//   P      = Gamma_Q Gamma_K^T                       (tensor cores, fp32 in TMEM)
-//   O_num  = Gamma_Q S_{c-1} + tril(P) V_c           (tensor cores)
-//   den    = Gamma_Q . Z_{c-1} + rowsum(tril(P))     (CUDA cores, fp32)
-//   O      = O_num / (den + eps * s)                 (s: row sum of the unnormalised Gamma_Q)
-//   S_c    = S_{c-1} + Gamma_K^T V_c                 (tensor cores, fp32 in TMEM)
-//   Z_c    = Z_{c-1} + column sums of Gamma_K        (CUDA cores, fp32)
+// prefix memory S_start (V~ part and Z part), in chunks of C = 128 tokens.  With E_K = exp2 of the
+// key logits minus their row maximum, r_j = 1 / (row sum of E_K) (so Gamma_K = diag(r) E_K), and
+// E_Q the same for the queries (row sums s_i, kept unnormalised):
+//   V'     = diag(r) V_c                             (value rows scaled in shared memory)
+//   P      = E_Q E_K^T                               (tensor cores, fp32 in TMEM)
+//   O_num  = E_Q S_{c-1} + tril(P) V'                (tensor cores)
+//   den    = E_Q . Z_{c-1} + sum_{j<=i} P_ij r_j     (CUDA cores, fp32)
+//   O      = O_num / (den + eps * s)
+//   S_c    = S_{c-1} + E_K^T V'                      (tensor cores, fp32 in TMEM)
+//   Z_c    = Z_{c-1} + E_K^T r                       (CUDA cores, fp32)
 //
 // Warp roles (416 threads):
-//   warps 0-3   key side:   [x^2, x] of the keys, softmax -> Gamma_K (shared memory), column sums
-//                           (Z), readout of S_c into the bf16 operand copy used by the next chunk;
-//   warps 4-7   query side: [x^2, x] of the queries, softmax -> Gamma_Q (bf16, back into TMEM as
-//                           the A operand), normaliser, causal mask of P (bf16, back into TMEM);
-//   warps 8-11  output:     numerator rows from TMEM, divided by the normaliser, stored to O;
-//   warp 12     control:    TMA of the value tiles (double-buffered) and every tcgen05.mma, issued
-//                           as soon as its operands are ready (mbarrier handshakes).
-// Tensor memory (512 columns): [0,128) key logits, then P; [128,256) query logits, then Gamma_Q;
+//   warps 0-3   key side:   [x^2, x] of the keys (in place in the TMA-filled A tile), E_K into
+//                           shared memory with r, the value rows scaled by r;
+//   warps 4-7   query side: [x^2, x] of the queries, E_Q (bf16, back into TMEM as the A operand),
+//                           its row sums and E_Q . Z, causal mask of P (bf16, back into TMEM);
+//   warps 8-11  state/out:  the starting memory, Z_c, the bf16 operand copy of S_c, and the
+//                           output rows (numerator from TMEM divided by the normaliser);
+//   warp 12     control:    TMA of the routing rows and value tiles, and every tcgen05.mma,
+//                           issued as soon as its operands are ready (mbarrier handshakes).
+// Tensor memory (512 columns): [0,128) key logits, then P; [128,256) query logits, then E_Q;
 // [256,384) output numerator; [384,512) the running memory S.
 // Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all roles leave their loops.
 #include "tc_rows.cuh"
@@ -33,12 +36,17 @@ namespace tck {
 
 namespace {
 
-constexpr int CTHREADS = 416;   // key side 0-3, query side 4-7, output 8-11, control 12
-enum BarId { B_BIMG, B_V, B_XK, B_XQ, B_AK, B_AQ, B_GK, B_GQ, B_PS, B_SP, B_OF, B_LK, B_LQ, B_S, B_PQ, B_PV, NBAR };
+constexpr int CTHREADS = 416;   // key side 0-3, query side 4-7, state/output 8-11, control 12
+enum BarId {
+    B_BIMG, B_V, B_XK, B_XQ,                                  // TMA (transaction counts)
+    B_AK, B_AQ, B_GK, B_VS, B_GQ, B_PS, B_ZP, B_SP, B_OF,     // 128 threads of one role
+    B_LK, B_LQ, B_S, B_PQ, B_PV,                              // tcgen05.commit
+    NBAR
+};
 constexpr uint32_t R_LK = 0, R_LQ = 128, R_O = 256, R_S = 384;
 
 struct CausalSmem {
-    uint32_t bimg, ax, abuf, gk, sp, ve, xk, xq, zbuf, dsm, bars, misc, total;
+    uint32_t bimg, ax, abk, abq, gk, sp, ve, zbuf, zpart, rbuf, dsm, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ CausalSmem(int DR, int kn16, int d_v)
     {
@@ -47,172 +55,218 @@ struct CausalSmem {
         uint32_t o = 0;
         bimg = o; o = al(o + tile * (uint32_t)kn16 + 32u * (uint32_t)kn16);
         ax = o; o = al(o + (uint32_t)C * 32u);
-        abuf = o; o = al(o + tile * (uint32_t)C);
+        abk = o; o = al(o + (uint32_t)C * DR * 4u);   // keys [x^2 | x]
+        abq = o; o = al(o + (uint32_t)C * DR * 4u);   // queries [x^2 | x]
         gk = o; o = al(o + 2u * C * 128u);
         sp = o; o = al(o + (uint32_t)d_v * KMAX * 2u);
         ve = o; o = al(o + (uint32_t)d_v * C * 2u);
-        xk = o; o = al(o + (uint32_t)C * DR * 2u);   // staged key rows (TMA, swizzled)
-        xq = o; o = al(o + (uint32_t)C * DR * 2u);   // staged query rows
-        zbuf = o; o += 2u * KMAX * 4u;
-        dsm = o; o += 2u * C * 8u;    // (row sum, normaliser) per row, by chunk parity
+        zbuf = o; o += 2u * KMAX * 4u;        // Z_{c-1} by chunk parity
+        zpart = o; o += 2u * 8u * KMAX * 4u;  // partial column sums by chunk parity
+        rbuf = o; o += (uint32_t)C * 4u;      // r of the chunk's keys
+        dsm = o; o += 2u * C * 8u;            // (row sum, normaliser) per query row, by chunk parity
         bars = o; o += NBAR * 8u;
         misc = o; o += 16u;
         total = o;
     }
 };
 
-// Key side: row k of the running memory S (d_v fp32 columns of TMEM at tl) as bf16 into the
-// MN-major SW32 operand tile sp.
-__device__ __noinline__ void state_readout(uint32_t tl, int d_v, uint8_t *sp, int k)
+// Key side: E_K row k = exp2(L - row max) (bf16; 0 beyond K) into the K-major SW128 tile gk;
+// returns the row sum of the fp32 values.
+__device__ __forceinline__ float key_exp(uint32_t tl, int K, int kc, uint8_t *gk, int k)
 {
-            for (int b0 = 0; b0 < d_v / 16; b0 += 4) {   // 64 columns per wait
-                uint32_t ra[32], rb[32];
-                if (d_v == 16) {
-                    uint32_t r16[16];
-                    tmem_ld16(tl, r16);
-                    tmem_ld_wait();
+    const float m = row_max(tl, K, kc);
+    float sum = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) ra[j] = r16[j];
-                } else {
-                    tmem_ld32(tl + 16 * b0, ra);
-                    if (b0 + 2 < d_v / 16) tmem_ld32(tl + 16 * b0 + 32, rb);
-                    tmem_ld_wait();
-                }
+    for (int c = 0; c < 4; ++c) {
+        if (c < kc) {
+            uint32_t r[32];
+            tmem_ld32(tl + 32 * c, r);
+            tmem_ld_wait();
+            sum += chunk_exp(r, c, K, m);
 #pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    const int b = b0 + bb;
-                    if (b < d_v / 16) {
-                        uint32_t r[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) r[j] = bb < 2 ? ra[16 * bb + j] : rb[16 * (bb - 2) + j];
-                        const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f),
-                                                    pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
-                        const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f),
-                                                    pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
-                        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
-                        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
-                    }
-                }
+            for (int q = 0; q < 4; ++q) {
+                const int e = 8 * q;
+                *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c + q, C)) =
+                    make_uint4(pk2(r[e], r[e + 1], 1.f), pk2(r[e + 2], r[e + 3], 1.f),
+                               pk2(r[e + 4], r[e + 5], 1.f), pk2(r[e + 6], r[e + 7], 1.f));
             }
+        }
+    }
+    return sum;
 }
 
-// Query side: unnormalised Gamma_Q of this row (zeros when not valid) back into TMEM at tl as
-// bf16 pairs; returns (row sum of the fp32 values, Gamma_Q . Z) with Z the fp32 normaliser z.
-__device__ __noinline__ float2 query_softmax(uint32_t tl, int K, int kc, bool valid, const float *z)
+// Key side: value row k of the chunk (MN-major SW32 blocks of 16 columns) times r, in place.
+__device__ __forceinline__ void scale_v_row(uint8_t *ve, int k, int d_v, float r)
 {
-                const float m = row_max(tl, K, kc);
-                const float sc = valid ? 1.f : 0.f;
-                const float4 *z4 = reinterpret_cast<const float4 *>(z);
-                float srow = 0.f, den = 0.f;
+    const uint32_t r2 = pack_bf16(r, r);
+    for (int b = 0; b < d_v / 16; ++b) {
 #pragma unroll
-                for (int c0 = 0; c0 < 4; c0 += 2) {
-                    if (c0 < kc) {
-                        uint32_t r2[2][32];
-                        tmem_ld32(tl + 32 * c0, r2[0]);
-                        if (c0 + 1 < kc) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
-                        tmem_ld_wait();
+        for (int hf = 0; hf < 2; ++hf) {
+            uint4 *p = reinterpret_cast<uint4 *>(ve + sw32(k, b, hf, C));
+            const uint4 v = *p;
+            *p = make_uint4(mul_bf16x2(v.x, r2), mul_bf16x2(v.y, r2), mul_bf16x2(v.z, r2), mul_bf16x2(v.w, r2));
+        }
+    }
+}
+
+// State side: row k of the running memory S (d_v fp32 columns of TMEM at tl) as bf16 into the
+// MN-major SW32 operand tile sp.
+__device__ __forceinline__ void state_readout(uint32_t tl, int d_v, uint8_t *sp, int k)
+{
+    for (int b0 = 0; b0 < d_v / 16; b0 += 4) {   // 64 columns per wait
+        uint32_t ra[32], rb[32];
+        if (d_v == 16) {
+            uint32_t r16[16];
+            tmem_ld16(tl, r16);
+            tmem_ld_wait();
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int c2 = c0 + h2;
-                            if (c2 < kc) {
-                                srow += chunk_exp(r2[h2], c2, K, m);
-                                float d4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < 16; ++j) ra[j] = r16[j];
+        } else {
+            tmem_ld32(tl + 16 * b0, ra);
+            if (b0 + 2 < d_v / 16) tmem_ld32(tl + 16 * b0 + 32, rb);
+            tmem_ld_wait();
+        }
 #pragma unroll
-                                for (int q = 0; q < 8; ++q) {
-                                    const float4 z = z4[8 * c2 + q];
-                                    d4[0] = fmaf(__uint_as_float(r2[h2][4 * q]), z.x, d4[0]);
-                                    d4[1] = fmaf(__uint_as_float(r2[h2][4 * q + 1]), z.y, d4[1]);
-                                    d4[2] = fmaf(__uint_as_float(r2[h2][4 * q + 2]), z.z, d4[2]);
-                                    d4[3] = fmaf(__uint_as_float(r2[h2][4 * q + 3]), z.w, d4[3]);
-                                }
-                                den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
-                                uint32_t w[16];
+        for (int bb = 0; bb < 4; ++bb) {
+            const int b = b0 + bb;
+            if (b < d_v / 16) {
+                uint32_t r[16];
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) w[j] = pk2(r2[h2][2 * j], r2[h2][2 * j + 1], sc);
-                                tmem_st16(tl + 16 * c2, w);   // Gamma_Q (bf16 pairs), in place
-                            }
-                        }
-                    }
-                }
-                tmem_st_wait();
-                return make_float2(srow, den);
+                for (int j = 0; j < 16; ++j) r[j] = bb < 2 ? ra[16 * bb + j] : rb[16 * (bb - 2) + j];
+                const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f),
+                                            pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
+                const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f),
+                                            pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
+                *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
+                *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
+            }
+        }
+    }
+}
+
+// State side: this thread's share of Z_c - Z_{c-1} = E_K^T r: components 8q..8q+7 over the rows
+// g, g+8, ..., g+120 of the chunk (t = 16 g + q), into zp[g][8q .. 8q+7].
+__device__ __forceinline__ void colsum_part(const uint8_t *gk, const float *rb, float *zp, int t)
+{
+    const int q = t & 15, g = t >> 4;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int u = 0; u < C / 8; ++u) {
+        const int j = g + 8 * u;
+        const uint4 v = *reinterpret_cast<const uint4 *>(gk + sw128(j, q, C));
+        const float r = rb[j];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc[2 * e] = fmaf(__uint_as_float(w[e] << 16), r, acc[2 * e]);
+            acc[2 * e + 1] = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), r, acc[2 * e + 1]);
+        }
+    }
+    float4 *o = reinterpret_cast<float4 *>(zp + g * KMAX + 8 * q);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+// Query side: unnormalised E_Q of this row (zeros when not valid) back into TMEM at tl as bf16
+// pairs; returns (row sum of the fp32 values, E_Q . z) with z the fp32 normaliser Z_{c-1}.
+__device__ __forceinline__ float2 query_softmax(uint32_t tl, int K, int kc, bool valid, const float *z)
+{
+    const float m = row_max(tl, K, kc);
+    const float sc = valid ? 1.f : 0.f;
+    const float4 *z4 = reinterpret_cast<const float4 *>(z);
+    float srow = 0.f, den = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c < kc) {
+            uint32_t r[32];
+            tmem_ld32(tl + 32 * c, r);
+            tmem_ld_wait();
+            srow += chunk_exp(r, c, K, m);
+            float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 zz = z4[8 * c + q];
+                d4[0] = fmaf(__uint_as_float(r[4 * q]), zz.x, d4[0]);
+                d4[1] = fmaf(__uint_as_float(r[4 * q + 1]), zz.y, d4[1]);
+                d4[2] = fmaf(__uint_as_float(r[4 * q + 2]), zz.z, d4[2]);
+                d4[3] = fmaf(__uint_as_float(r[4 * q + 3]), zz.w, d4[3]);
+            }
+            den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = pk2(r[2 * j], r[2 * j + 1], sc);
+            tmem_st16(tl + 16 * c, w);   // E_Q (bf16 pairs), in place
+        }
+    }
+    tmem_st_wait();
+    return make_float2(srow, den);
 }
 
 // Query side: row i of P (fp32 in TMEM at tl) masked to columns j <= i, written back as bf16
-// pairs in place; returns the sum of the kept fp32 values.
-__device__ __noinline__ float causal_mask(uint32_t tl, int i)
+// pairs in place; returns sum_{j<=i} P_ij r_j.
+__device__ __forceinline__ float causal_mask(uint32_t tl, int i, const float *rb)
 {
+    const float4 *r4 = reinterpret_cast<const float4 *>(rb);
     float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c0 = 0; c0 < 4; c0 += 2) {
-                uint32_t r2[2][32];
-                tmem_ld32(tl + 32 * c0, r2[0]);
-                tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
-                tmem_ld_wait();
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
+        tmem_ld_wait();
+        uint32_t w[16];
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int c2 = c0 + h2;
-                    uint32_t w[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = 32 * c2 + 2 * j;
-                        const float p0 = col <= i ? __uint_as_float(r2[h2][2 * j]) : 0.f;
-                        const float p1 = col + 1 <= i ? __uint_as_float(r2[h2][2 * j + 1]) : 0.f;
-                        d4[j & 3] += p0 + p1;
-                        w[j] = pack_bf16(p0, p1);
-                    }
-                    tmem_st16(tl + 16 * c2, w);
-                }
-            }
-            tmem_st_wait();
+        for (int q = 0; q < 8; ++q) {
+            const float4 rr = r4[8 * c + q];
+            const int col = 32 * c + 4 * q;
+            const float p0 = col <= i ? __uint_as_float(r[4 * q]) : 0.f;
+            const float p1 = col + 1 <= i ? __uint_as_float(r[4 * q + 1]) : 0.f;
+            const float p2 = col + 2 <= i ? __uint_as_float(r[4 * q + 2]) : 0.f;
+            const float p3 = col + 3 <= i ? __uint_as_float(r[4 * q + 3]) : 0.f;
+            d4[0] = fmaf(p0, rr.x, d4[0]);
+            d4[1] = fmaf(p1, rr.y, d4[1]);
+            d4[2] = fmaf(p2, rr.z, d4[2]);
+            d4[3] = fmaf(p3, rr.w, d4[3]);
+            w[2 * q] = pack_bf16(p0, p1);
+            w[2 * q + 1] = pack_bf16(p2, p3);
+        }
+        tmem_st16(tl + 16 * c, w);
+    }
+    tmem_st_wait();
     return (d4[0] + d4[1]) + (d4[2] + d4[3]);
 }
 
-// Query side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.
-__device__ __noinline__ void write_output(uint32_t tl, int d_v, float inv, bool valid, void *O,
+// Output side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.
+__device__ __forceinline__ void write_output(uint32_t tl, int d_v, float inv, bool valid, void *O,
                                           long long orow, int out_f32)
 {
-                for (int c0 = 0; c0 < (d_v + 31) / 32; c0 += 2) {   // 64 columns per wait
-                    uint32_t r2[2][32];
-                    if (d_v == 16) {
-                        uint32_t r16[16];
-                        tmem_ld16(tl, r16);
-                        tmem_ld_wait();
+    for (int c = 0; c < (d_v + 31) / 32; ++c) {   // 32 columns per wait
+        uint32_t r[32];
+        if (d_v == 16) {
+            tmem_ld16(tl, *reinterpret_cast<uint32_t(*)[16]>(r));
+        } else {
+            tmem_ld32(tl + 32 * c, r);
+        }
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int col0 = 32 * c;
+        const int ncol = d_v - col0 < 32 ? d_v - col0 : 32;
+        if (out_f32) {
+            float4 *o4 = reinterpret_cast<float4 *>((float *)O + orow * d_v + col0);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) r2[0][j] = r16[j];
-                    } else {
-                        tmem_ld32(tl + 32 * c0, r2[0]);
-                        if (32 * (c0 + 1) < d_v) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
-                        tmem_ld_wait();
-                    }
-                    if (!valid) continue;
+            for (int q = 0; q < 8; ++q)
+                if (4 * q < ncol)
+                    o4[q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                        __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+        } else {
+            uint4 *o4 = reinterpret_cast<uint4 *>((bf16 *)O + orow * d_v + col0);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int col0 = 32 * (c0 + h2);
-                        if (col0 >= d_v) continue;
-                        const int ncol = d_v - col0 < 32 ? d_v - col0 : 32;
-                        if (out_f32) {
-                            float4 *o4 = reinterpret_cast<float4 *>((float *)O + orow * d_v + col0);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                if (4 * q < ncol)
-                                    o4[q] = make_float4(__uint_as_float(r2[h2][4 * q]) * inv,
-                                                        __uint_as_float(r2[h2][4 * q + 1]) * inv,
-                                                        __uint_as_float(r2[h2][4 * q + 2]) * inv,
-                                                        __uint_as_float(r2[h2][4 * q + 3]) * inv);
-                        } else {
-                            uint4 *o4 = reinterpret_cast<uint4 *>((bf16 *)O + orow * d_v + col0);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (8 * q < ncol)
-                                    o4[q] = make_uint4(pk2(r2[h2][8 * q], r2[h2][8 * q + 1], inv),
-                                                       pk2(r2[h2][8 * q + 2], r2[h2][8 * q + 3], inv),
-                                                       pk2(r2[h2][8 * q + 4], r2[h2][8 * q + 5], inv),
-                                                       pk2(r2[h2][8 * q + 6], r2[h2][8 * q + 7], inv));
-                        }
-                    }
-                }
-            }
+            for (int q = 0; q < 4; ++q)
+                if (8 * q < ncol)
+                    o4[q] = make_uint4(pk2(r[8 * q], r[8 * q + 1], inv), pk2(r[8 * q + 2], r[8 * q + 3], inv),
+                                       pk2(r[8 * q + 4], r[8 * q + 5], inv), pk2(r[8 * q + 6], r[8 * q + 7], inv));
+        }
+    }
+}
 
 }  // namespace
 
@@ -229,6 +283,8 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 4);
     float *zbuf = reinterpret_cast<float *>(smem + L.zbuf);
+    float *zpart = reinterpret_cast<float *>(smem + L.zpart);
+    float *rbuf = reinterpret_cast<float *>(smem + L.rbuf);
     float2 *dsm = reinterpret_cast<float2 *>(smem + L.dsm);
     const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
     const int t = threadIdx.x, warp = t >> 5;
@@ -237,11 +293,13 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
     const int nch = (tok_end - tok0 + C - 1) / C;
     const int d_v = a.d_v;
     const int kc = (a.K + 31) >> 5;
+    constexpr uint32_t XT = (uint32_t)C * DR * 2;   // bytes of one [x] tile (the TMA destination)
 
     // ---------------------------------------------------------------- set-up (all threads)
     if (warp == 12) {
         if (t == 384) {
-            static const uint32_t counts[NBAR] = {1, 1, 1, 1, 128, 128, 128, 128, 128, 128, 128, 1, 1, 1, 1, 1};
+            static const uint32_t counts[NBAR] = {1,   1,   1,   1,   128, 128, 128, 128, 128,
+                                                  128, 128, 128, 128, 1,   1,   1,   1,   1};
             for (int i = 0; i < NBAR; ++i) mbar_init(bars + i, counts[i]);
             *abort = 0;
             fence_mbar_init();
@@ -249,7 +307,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
         __syncwarp();
         tmem_alloc(tslot, 512);
     } else if (warp < 4) {
-        // Gamma_K tile: components the softmax never writes must read as zero
+        // E_K tile: components the exponentials never write must read as zero
         for (uint32_t o = t * 16; o < 2u * C * 128u; o += 128 * 16)
             *reinterpret_cast<uint4 *>(smem + L.gk + o) = make_uint4(0, 0, 0, 0);
     } else if (warp < 8) {
@@ -283,8 +341,8 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
             bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + B_BIMG);
             if (nch > 0) {
-                load_x_tile(smem + L.xk, &kmap, bars + B_XK, DR, tok0, bh);
-                load_x_tile(smem + L.xq, &qmap, bars + B_XQ, DR, tok0, bh);
+                load_x_tile(smem + L.abk + XT, &kmap, bars + B_XK, DR, tok0, bh);
+                load_x_tile(smem + L.abq + XT, &qmap, bars + B_XQ, DR, tok0, bh);
                 load_v_chunk(smem + L.ve, &vmap, bars + B_V, d_v, tok0, bh);
                 last_xk = last_xq = last_v = 0;
             }
@@ -295,47 +353,52 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
                 const uint32_t ph = c & 1;
                 const int nxt = tok0 + (c + 1) * C;
                 if (c > 0) {
-                    // the previous chunk's tril(P) V is done with P (key logits region) and V
+                    // the previous chunk's tril(P) V' is done with P (key logits region) and V'
                     if (!(ok = mbar_wait_abortable(bars + B_PV, (c - 1) & 1, a.hdr, 51, abort))) break;
                     load_v_chunk(smem + L.ve, &vmap, bars + B_V, d_v, tok0 + c * C, bh);
                     last_v = c;
                 }
-                // key logits; the key rows are in the A tile, so the next chunk's may be staged
+                // key logits
                 if (!(ok = mbar_wait_abortable(bars + B_AK, ph, a.hdr, 52, abort))) break;
-                if (c + 1 < nch) {
-                    load_x_tile(smem + L.xk, &kmap, bars + B_XK, DR, nxt, bh);
-                    last_xk = c + 1;
-                }
                 tc_fence_after();
-                issue_logits_c<DR>(tmem + R_LK, sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
+                issue_logits_x<DR>(tmem + R_LK, sb + L.abk, bimg, bconst, sb + L.ax, a.kn16);
                 mma_commit(bars + B_LK);
-                // query logits (query-side softmax of the previous chunk is done with R_LQ)
+                // query logits (the query side of the previous chunk is done with R_LQ)
                 if (!(ok = mbar_wait_abortable(bars + B_AQ, ph, a.hdr, 53, abort))) break;
-                if (c + 1 < nch) {
-                    load_x_tile(smem + L.xq, &qmap, bars + B_XQ, DR, nxt, bh);
-                    last_xq = c + 1;
-                }
                 if (c > 0 && !(ok = mbar_wait_abortable(bars + B_PQ, (c - 1) & 1, a.hdr, 54, abort))) break;
                 tc_fence_after();
-                issue_logits_c<DR>(tmem + R_LQ, sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
+                issue_logits_x<DR>(tmem + R_LQ, sb + L.abq, bimg, bconst, sb + L.ax, a.kn16);
                 mma_commit(bars + B_LQ);
-                // S update (its operands are usually ready first), then P and the inter-chunk read
+                // the key A tile has been read: stage the next chunk's key rows
+                if (!(ok = mbar_wait_abortable(bars + B_LK, ph, a.hdr, 62, abort))) break;
+                if (c + 1 < nch) {
+                    load_x_tile(smem + L.abk + XT, &kmap, bars + B_XK, DR, nxt, bh);
+                    last_xk = c + 1;
+                }
+                // S update: E_K and V' ready, S_{c-1} read out
                 if (!(ok = mbar_wait_abortable(bars + B_GK, ph, a.hdr, 55, abort))) break;
                 if (!(ok = mbar_wait_abortable(bars + B_SP, ph, a.hdr, 58, abort))) break;
-                if (!(ok = mbar_wait_abortable(bars + B_V, ph, a.hdr, 59, abort))) break;
+                if (!(ok = mbar_wait_abortable(bars + B_VS, ph, a.hdr, 59, abort))) break;
                 tc_fence_after();
-                for (int s = 0; s < C / 16; ++s)   // S += Gamma_K^T V
+                for (int s = 0; s < C / 16; ++s)   // S += E_K^T V'
                     mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(ve, s, C), id_s, 1u);
                 mma_commit(bars + B_S);
+                // the query A tile has been read: stage the next chunk's query rows
+                if (!(ok = mbar_wait_abortable(bars + B_LQ, ph, a.hdr, 63, abort))) break;
+                if (c + 1 < nch) {
+                    load_x_tile(smem + L.abq + XT, &qmap, bars + B_XQ, DR, nxt, bh);
+                    last_xq = c + 1;
+                }
+                // P and the inter-chunk read (the output side is done with R_O)
                 if (!(ok = mbar_wait_abortable(bars + B_GQ, ph, a.hdr, 60, abort))) break;
                 if (c > 0 && !(ok = mbar_wait_abortable(bars + B_OF, (c - 1) & 1, a.hdr, 61, abort))) break;
                 tc_fence_after();
-                for (int s = 0; s < ksteps; ++s)   // P = Gamma_Q Gamma_K^T
+                for (int s = 0; s < ksteps; ++s)   // P = E_Q E_K^T
                     mma_f16_tmem_a(tmem + R_LK, tmem + R_LQ + 8 * s, kdesc(sb + L.gk, s, C), id_p, s > 0);
-                for (int s = 0; s < ksteps; ++s)   // O = Gamma_Q S_{c-1}
+                for (int s = 0; s < ksteps; ++s)   // O = E_Q S_{c-1}
                     mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + 8 * s, mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
                 mma_commit(bars + B_PQ);
-                // intra-chunk: O += tril(P) V
+                // intra-chunk: O += tril(P) V'
                 if (!(ok = mbar_wait_abortable(bars + B_PS, ph, a.hdr, 56, abort))) break;
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s)
@@ -352,8 +415,77 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
         }
     } else if (warp < 4) {
         // ============================================================ key side
-        const int k = t;   // TMEM lane, token row of the chunk, and component row of S
+        const int k = t;   // TMEM lane and token row of the chunk
         const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+        uint8_t *abk = smem + L.abk;
+        if (nch > 0 && mbar_wait_abortable(bars + B_XK, 0, a.hdr, 67, abort)) {
+            build_inplace<DR>(abk, k);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + B_AK);
+        }
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            const int base = tok0 + c * C;
+            if (!mbar_wait_abortable(bars + B_LK, ph, a.hdr, 61, abort)) break;
+            if (c > 0) {
+                // the E_K tile and r are free once P, the S update and the column sums of the
+                // previous chunk have read them
+                if (!mbar_wait_abortable(bars + B_PQ, (c - 1) & 1, a.hdr, 63, abort)) break;
+                if (!mbar_wait_abortable(bars + B_S, (c - 1) & 1, a.hdr, 62, abort)) break;
+                if (!mbar_wait_abortable(bars + B_ZP, (c - 1) & 1, a.hdr, 64, abort)) break;
+            }
+            tc_fence_after();
+            const float sum = key_exp(lane + R_LK, a.K, kc, smem + L.gk, k);
+            const float r = base + k < tok_end ? 1.0f / sum : 0.f;
+            rbuf[k] = r;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars + B_GK);
+            // V' = diag(r) V for this chunk
+            if (!mbar_wait_abortable(bars + B_V, ph, a.hdr, 65, abort)) break;
+            scale_v_row(smem + L.ve, k, d_v, r);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + B_VS);
+            // the next chunk's keys
+            if (c + 1 < nch) {
+                if (!mbar_wait_abortable(bars + B_XK, (c + 1) & 1, a.hdr, 67, abort)) break;
+                build_inplace<DR>(abk, k);
+                fence_proxy_async_smem();
+                mbar_arrive(bars + B_AK);
+            }
+        }
+    } else if (warp < 8) {
+        // ============================================================ query side
+        const int i = t - 128;
+        const uint32_t lane = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        uint8_t *abq = smem + L.abq;
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            const int base = tok0 + c * C;
+            const bool valid = base + i < tok_end;
+            if (!mbar_wait_abortable(bars + B_XQ, ph, a.hdr, 75, abort)) break;
+            build_inplace<DR>(abq, i);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + B_AQ);
+            if (!mbar_wait_abortable(bars + B_LQ, ph, a.hdr, 71, abort)) break;
+            if (!mbar_wait_abortable(bars + B_SP, ph, a.hdr, 72, abort)) break;
+            tc_fence_after();
+            const float2 sd = query_softmax(lane + R_LQ, a.K, kc, valid, zbuf + ph * KMAX);
+            tc_fence_before();
+            mbar_arrive(bars + B_GQ);
+            // causal mask of P; P (bf16 pairs) back into TMEM as the A operand of tril(P) V'
+            if (!mbar_wait_abortable(bars + B_PQ, ph, a.hdr, 73, abort)) break;
+            if (!mbar_wait_abortable(bars + B_GK, ph, a.hdr, 76, abort)) break;   // r of this chunk
+            tc_fence_after();
+            const float den = sd.y + causal_mask(lane + R_LK, i, rbuf);
+            dsm[ph * C + i] = make_float2(sd.x, den);
+            tc_fence_before();
+            mbar_arrive(bars + B_PS);
+        }
+    } else {
+        // ============================================================ state and output side
+        const int k = t - 256;   // TMEM lane: component row of S, and token row of the output
+        const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
         // starting memory: V~ part to TMEM and as the bf16 operand, Z part to the running sum
         const float *src = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + k) * a.ne;
         for (int b = 0; b < d_v / 16; ++b) {
@@ -368,8 +500,8 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
                 r[4 * q + 3] = __float_as_uint(f.w);
             }
             tmem_st16(lane + R_S + 16 * b, r);
-            uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
-            uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
+            const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
+            const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
             *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 0, KMAX)) = lo;
             *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 1, KMAX)) = hi;
         }
@@ -379,39 +511,39 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bars + B_SP);   // phase 0: S_start ready
+        // output of chunk cc (numerator complete, normaliser from the query side)
+        auto output = [&](int cc) -> bool {
+            const uint32_t pc = cc & 1;
+            if (!mbar_wait_abortable(bars + B_PS, pc, a.hdr, 77, abort)) return false;
+            if (!mbar_wait_abortable(bars + B_PV, pc, a.hdr, 74, abort)) return false;
+            tc_fence_after();
+            const float2 sd = dsm[pc * C + k];
+            const int row = tok0 + cc * C + k;
+            write_output(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), row < tok_end, a.O,
+                         (long long)bh * a.N + row, a.out_f32);
+            tc_fence_before();
+            mbar_arrive(bars + B_OF);
+            return true;
+        };
+        bool ok = true;
         for (int c = 0; c < nch; ++c) {
             const uint32_t ph = c & 1;
-            const int base = tok0 + c * C;
-            if (c > 0 && !mbar_wait_abortable(bars + B_LQ, (c - 1) & 1, a.hdr, 60, abort)) break;
-            if (!mbar_wait_abortable(bars + B_XK, ph, a.hdr, 67, abort)) break;
-            build_a_s<DR>(smem + L.abuf, k, smem + L.xk);
-            fence_proxy_async_smem();
-            mbar_arrive(bars + B_AK);
-            if (!mbar_wait_abortable(bars + B_LK, ph, a.hdr, 61, abort)) break;
-            if (c > 0 && !mbar_wait_abortable(bars + B_S, (c - 1) & 1, a.hdr, 62, abort)) break;
-            if (c > 0 && !mbar_wait_abortable(bars + B_PQ, (c - 1) & 1, a.hdr, 63, abort)) break;
-            tc_fence_after();
-            key_softmax<false>(lane + R_LK, a.K, kc, base + k < tok_end, smem + L.gk, k);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bars + B_GK);
-            // Z_c = Z_{c-1} + column k of Gamma_K (the bf16 values the tensor cores use), once all
-            // 128 rows are in (the same barrier the control warp waits on)
-            if (!mbar_wait_abortable(bars + B_GK, ph, a.hdr, 66, abort)) break;
+            if (c > 0 && !(ok = output(c - 1))) break;
+            // Z_c = Z_{c-1} + E_K^T r
+            if (!(ok = mbar_wait_abortable(bars + B_GK, ph, a.hdr, 66, abort))) break;
+            float *zp = zpart + ph * 8 * KMAX;
+            colsum_part(smem + L.gk, rbuf, zp, k);
+            mbar_arrive(bars + B_ZP);
+            if (!(ok = mbar_wait_abortable(bars + B_ZP, ph, a.hdr, 68, abort))) break;
             {
-                const int q = k >> 3;
-                const uint32_t col = (uint32_t)(k & 7) * 2;
-                float zs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                for (int j = 0; j < C; j += 8) {
+                float zs = 0.f;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        zs[u] += __bfloat162float(*reinterpret_cast<const bf16 *>(smem + L.gk + sw128(j + u, q, C) + col));
-                }
-                zrun += ((zs[0] + zs[1]) + (zs[2] + zs[3])) + ((zs[4] + zs[5]) + (zs[6] + zs[7]));
+                for (int g = 0; g < 8; ++g) zs += zp[g * KMAX + k];
+                zrun += zs;
             }
-            // readout of S_c (after the update and the read of S_{c-1} that it overwrites)
-            if (!mbar_wait_abortable(bars + B_S, ph, a.hdr, 64, abort)) break;
-            if (!mbar_wait_abortable(bars + B_PQ, ph, a.hdr, 65, abort)) break;
+            // readout of S_c (after the update, and after the read of S_{c-1} that it overwrites)
+            if (!(ok = mbar_wait_abortable(bars + B_S, ph, a.hdr, 69, abort))) break;
+            if (!(ok = mbar_wait_abortable(bars + B_PQ, ph, a.hdr, 70, abort))) break;
             tc_fence_after();
             state_readout(lane + R_S, d_v, smem + L.sp, k);
             zbuf[((c + 1) & 1) * KMAX + k] = zrun;
@@ -419,54 +551,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             tc_fence_before();
             mbar_arrive(bars + B_SP);
         }
-    } else if (warp < 8) {
-        // ============================================================ query side
-        const int i = t - 128;
-        const uint32_t lane = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-        for (int c = 0; c < nch; ++c) {
-            const uint32_t ph = c & 1;
-            const int base = tok0 + c * C;
-            const bool valid = base + i < tok_end;
-            if (!mbar_wait_abortable(bars + B_LK, ph, a.hdr, 70, abort)) break;
-            if (!mbar_wait_abortable(bars + B_XQ, ph, a.hdr, 75, abort)) break;
-            build_a_s<DR>(smem + L.abuf, i, smem + L.xq);
-            fence_proxy_async_smem();
-            mbar_arrive(bars + B_AQ);
-            if (!mbar_wait_abortable(bars + B_LQ, ph, a.hdr, 71, abort)) break;
-            if (!mbar_wait_abortable(bars + B_SP, ph, a.hdr, 72, abort)) break;
-            tc_fence_after();
-            float srow, den;
-            {
-                const float2 r = query_softmax(lane + R_LQ, a.K, kc, valid, zbuf + ph * KMAX);
-                srow = r.x;
-                den = r.y;
-            }
-            tc_fence_before();
-            mbar_arrive(bars + B_GQ);
-            // causal mask of P; P (bf16 pairs) back into TMEM as the A operand of tril(P) V
-            if (!mbar_wait_abortable(bars + B_PQ, ph, a.hdr, 73, abort)) break;
-            tc_fence_after();
-            den += causal_mask(lane + R_LK, i);
-            dsm[ph * C + i] = make_float2(srow, den);
-            tc_fence_before();
-            mbar_arrive(bars + B_PS);
-        }
-    } else {
-        // ============================================================ output
-        const int i = t - 256;
-        const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
-        for (int c = 0; c < nch; ++c) {
-            const uint32_t ph = c & 1;
-            const int base = tok0 + c * C;
-            if (!mbar_wait_abortable(bars + B_PS, ph, a.hdr, 77, abort)) break;   // (sum, normaliser)
-            if (!mbar_wait_abortable(bars + B_PV, ph, a.hdr, 74, abort)) break;   // numerator done
-            tc_fence_after();
-            const float2 sd = dsm[ph * C + i];
-            write_output(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), base + i < tok_end, a.O,
-                         (long long)bh * a.N + base + i, a.out_f32);
-            tc_fence_before();
-            mbar_arrive(bars + B_OF);
-        }
+        if (ok && nch > 0) output(nch - 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -488,16 +573,17 @@ gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, con
     const uint32_t sm = causal_pipelined_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_causal_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st, (tc_causal_pipelined_kernel<DR><<<nblocks, CTHREADS, sm, st>>>(a, vmap, kmap, qmap)));
+    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st,
+               (tc_causal_pipelined_kernel<DR><<<nblocks, CTHREADS, sm, st>>>(a, vmap, kmap, qmap)));
     return GMA_OK;
 }
 
 template gma_status_t launch_causal_pipelined<16>(const Args &, const CUtensorMap &, const CUtensorMap &,
-                                                     const CUtensorMap &, int, cudaStream_t);
+                                                  const CUtensorMap &, int, cudaStream_t);
 template gma_status_t launch_causal_pipelined<32>(const Args &, const CUtensorMap &, const CUtensorMap &,
-                                                     const CUtensorMap &, int, cudaStream_t);
+                                                  const CUtensorMap &, int, cudaStream_t);
 template gma_status_t launch_causal_pipelined<64>(const Args &, const CUtensorMap &, const CUtensorMap &,
-                                                     const CUtensorMap &, int, cudaStream_t);
+                                                  const CUtensorMap &, int, cudaStream_t);
 
 }  // namespace tck
 }  // namespace gma

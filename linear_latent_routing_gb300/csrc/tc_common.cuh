@@ -169,6 +169,52 @@ __device__ __forceinline__ void build_a_s(uint8_t *abuf, int row, const uint8_t 
     for (int q = DR / 4; q < KA / 8; ++q) *reinterpret_cast<uint4 *>(abuf + sw128(row, q, C)) = make_uint4(0, 0, 0, 0);
 }
 
+// ------------------------------------------------------------------ [x^2, x] tile built in place
+// The A operand of the logits as two K-major tiles of 128 rows x DR fp16 columns (rows of 2*DR
+// bytes, swizzle of the same width): x^2 at ab, x at ab + 128 * 2 * DR.  TMA writes the bf16 rows
+// into the x tile; the builder reads them, writes x^2 and rewrites x as fp16 in place.
+template <int DR>
+__device__ __forceinline__ void build_inplace(uint8_t *ab, int row)
+{
+    uint8_t *abx = ab + C * DR * 2;
+#pragma unroll
+    for (int q = 0; q < DR / 8; ++q) {
+        const uint32_t o = xs_off<DR>(row, q);
+        const uint4 v = *reinterpret_cast<const uint4 *>(abx + o);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t sq[4], li[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            sq[j] = pack_f16(lo * lo, hi * hi);
+            li[j] = pack_f16(lo, hi);
+        }
+        *reinterpret_cast<uint4 *>(ab + o) = make_uint4(sq[0], sq[1], sq[2], sq[3]);
+        *reinterpret_cast<uint4 *>(abx + o) = make_uint4(li[0], li[1], li[2], li[3]);
+    }
+}
+
+// Descriptor of k-step s (16 columns) of the in-place A tiles.
+template <int DR>
+__device__ __forceinline__ uint64_t abdesc(uint32_t ab, int s)
+{
+    constexpr int KPS = DR / 16;   // k-steps per tile
+    constexpr uint32_t RB = DR * 2;
+    return smem_desc(ab + (uint32_t)(s / KPS) * (uint32_t)C * RB + (uint32_t)(s % KPS) * 32u, 16, 8u * RB,
+                     DR == 64 ? SW_128B : DR == 32 ? SW_64B : SW_32B);
+}
+
+// Logits of 128 tokens: [x^2, x] (in-place tiles at ab) times the head's table, plus the constant.
+template <int DR>
+__device__ __forceinline__ void issue_logits_x(uint32_t d, uint32_t ab, uint32_t bimg, uint32_t bconst, uint32_t ax,
+                                               int kn16)
+{
+    const uint32_t id = idesc_f16(128, (uint32_t)kn16, 0, 0, 0, 0);
+#pragma unroll
+    for (int s = 0; s < DR / 8; ++s) mma_f16(d, abdesc<DR>(ab, s), kdesc(bimg, s, kn16), id, s > 0);
+    mma_f16(d, kdesc32(ax), kdesc32(bconst), id, 1u);   // + per-component constant
+}
+
 // TMA of the x rows [tok, tok + 128) of slice bh (3-D map {DR, N, BH}, box {DR, 128, 1}; rows past
 // the sequence read as zeros) into the staging tile xs.
 __device__ __forceinline__ void load_x_tile(uint8_t *xs, const CUtensorMap *map, uint64_t *bar, int DR, int tok,

@@ -19,20 +19,14 @@ __device__ __forceinline__ float row_max(uint32_t taddr, int K, int kc)
 #pragma unroll
     for (int u = 0; u < 8; ++u) m[u] = NEG_BIG;
 #pragma unroll
-    for (int c0 = 0; c0 < 4; c0 += 2) {
-        if (c0 < kc) {
-            uint32_t ra[32], rb[32];
-            tmem_ld32(taddr + 32 * c0, ra);
-            if (c0 + 1 < kc) tmem_ld32(taddr + 32 * (c0 + 1), rb);
+    for (int c = 0; c < 4; ++c) {
+        if (c < kc) {
+            uint32_t ra[32];
+            tmem_ld32(taddr + 32 * c, ra);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if ((c0 + 1) * 32 <= K || 32 * c0 + j < K) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(ra[j]));
-            if (c0 + 1 < kc) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if ((c0 + 2) * 32 <= K || 32 * (c0 + 1) + j < K) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(rb[j]));
-            }
+                if ((c + 1) * 32 <= K || 32 * c + j < K) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(ra[j]));
         }
     }
     return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));

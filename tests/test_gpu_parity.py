@@ -45,6 +45,8 @@ SMALL = [
     W.scaled(W.LM_CAUSAL, B=1, H=1, N=129, K=1),
     W.scaled(W.LRA_BIDIR, B=1, H=1, N=130, K=1),
     W.scaled(W.LM_CAUSAL, B=1, H=1, N=300, d_r=16, K=8, d_v=16),
+    W.scaled(W.LM_CAUSAL, B=1, H=2, N=700, d_r=32, K=32, d_v=64),
+    W.scaled(W.LM_CAUSAL, B=1, H=1, N=520, d_r=32, K=100, d_v=32),
     W.scaled(W.LM_CAUSAL, B=1, H=1, N=300, d_r=128, K=24, d_v=128),
     W.scaled(W.LRA_BIDIR, B=1, H=1, N=257, d_r=128, K=40, d_v=32),
     W.scaled(W.K_SWEEP[2], B=1, H=1, N=400),
