@@ -67,6 +67,9 @@ typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype_t;
 /* Bits of gma_shape_t.flags. */
 #define GMA_FLAG_SIMT 0x1u     /* force the fp32 CUDA-core kernels (the path fp32 inputs take) */
 #define GMA_FLAG_OUT_F32 0x2u  /* write O (or gamma) as fp32 even for bf16 inputs              */
+#define GMA_FLAG_RECOMPUTE_KEYS 0x4u /* causal, tensor-core path: recompute the key
+                                      * responsibilities in the output pass instead of keeping
+                                      * them in the workspace (smaller workspace, slower)     */
 
 typedef struct {
     int B, H, N;     /* batch, heads, sequence length                                       */
@@ -86,7 +89,9 @@ typedef struct {
 
 /* Bytes of device workspace one call of `variant` with `shape` needs (0 for an invalid shape).
  * The workspace must be 256-byte aligned.  Its first 256 bytes hold the error word that
- * gma_check_workspace reads. */
+ * gma_check_workspace reads.  For the causal variant on the tensor-core path (bf16, no
+ * GMA_FLAG_SIMT) it includes the key responsibilities of every token, B*H*N*Kp bf16 values
+ * (Kp = 64 for K <= 64, else 128), unless GMA_FLAG_RECOMPUTE_KEYS is set. */
 size_t gma_workspace_size(const gma_shape_t *shape, int variant);
 
 /* Posterior responsibilities (Méthodologie §1):
@@ -119,8 +124,9 @@ gma_status_t gma_forward_causal(const gma_shape_t *shape, const void *QX, const 
  *   - Computes exactly what gma_forward_causal computes, with the same arguments minus the
  *     workspace, which comes from a fixed array of GMA_NOALLOC_SCRATCH_BYTES inside the library's
  *     device image.  Every GPU that loads libgma.so holds that array until the process exits.
- *   - A shape whose gma_workspace_size(shape, GMA_VARIANT_CAUSAL) exceeds
- *     GMA_NOALLOC_SCRATCH_BYTES returns GMA_ERR_WORKSPACE before anything is enqueued.
+ *   - If gma_workspace_size(shape, GMA_VARIANT_CAUSAL) exceeds GMA_NOALLOC_SCRATCH_BYTES, the
+ *     call runs as if GMA_FLAG_RECOMPUTE_KEYS were set; if that workspace exceeds it too, the
+ *     call returns GMA_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on each device (with that device current) looks up the array's device
  *     address once; make that first call before any stream capture.  No call allocates or frees
  *     memory (no cudaMalloc, cudaFree or allocating library routine).

@@ -17,7 +17,7 @@ gma_status_t validate_shape(const gma_shape_t *s, int variant)
     if (s->B < 1 || s->H < 1 || s->N < 1 || s->K < 1) return GMA_ERR_INVALID_ARG;
     if (s->dtype != GMA_F32 && s->dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
     if (!(s->var_floor >= 0.f) || !(s->eps >= 0.f)) return GMA_ERR_INVALID_ARG;
-    if (s->flags & ~(GMA_FLAG_SIMT | GMA_FLAG_OUT_F32)) return GMA_ERR_INVALID_ARG;
+    if (s->flags & ~(GMA_FLAG_SIMT | GMA_FLAG_OUT_F32 | GMA_FLAG_RECOMPUTE_KEYS)) return GMA_ERR_INVALID_ARG;
     if (!valid_dim(s->d_r) || s->K > 1024) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (variant != GMA_VARIANT_RESPONSIBILITIES && !valid_dim(s->d_v))
         return GMA_ERR_UNSUPPORTED_SHAPE;

@@ -55,10 +55,15 @@ extern "C" gma_status_t gma_forward_causal_noalloc(const gma_shape_t *shape, con
     if (need == 0)   // invalid shape: the regular entry point names the error, enqueuing nothing
         return gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, nullptr, 0,
                                   stream);
-    if (need > kScratchBytes) return GMA_ERR_WORKSPACE;
+    gma_shape_t s = *shape;
+    if (need > kScratchBytes) {
+        // the smaller workspace of the same computation, if that one fits
+        s.flags |= GMA_FLAG_RECOMPUTE_KEYS;
+        if (gma_workspace_size(&s, GMA_VARIANT_CAUSAL) > kScratchBytes) return GMA_ERR_WORKSPACE;
+    }
     void *scratch = nullptr;
     const gma_status_t r = scratch_for_current_device(&scratch);
     if (r != GMA_OK) return r;
-    return gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, scratch,
-                              kScratchBytes, stream);
+    return gma_forward_causal(&s, QX, KX, V, mu, raw_var, prior_logits, O, scratch, kScratchBytes,
+                              stream);
 }

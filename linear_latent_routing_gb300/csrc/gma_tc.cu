@@ -34,6 +34,8 @@
 #include <cuda.h>
 #include <mutex>
 
+#include <cstring>
+
 #include "tc_common.cuh"
 
 namespace gma {
@@ -569,7 +571,8 @@ bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v)
 struct Plan {
     int kn16, ne, ka, bimg_bytes, bimg_main_bytes;
     int nseg, cps;              // forward: segments per slice and chunks per segment
-    size_t off_bimg, off_cst, off_agg, total;
+    int kg;                     // causal: components per stored key-responsibility row (64 or 128)
+    size_t off_bimg, off_cst, off_agg, off_gam, total;
 };
 
 constexpr int kTargetCtas = 152 * 4;
@@ -594,6 +597,11 @@ Plan make_plan(const gma_shape_t &s, int variant)
     p.off_cst = c.take(sizeof(float) * (size_t)s.H * p.kn16);
     if (variant != GMA_VARIANT_RESPONSIBILITIES)
         p.off_agg = c.take(sizeof(float) * (size_t)BH * p.nseg * KMAX * p.ne);
+    if (variant == GMA_VARIANT_CAUSAL && !(s.flags & GMA_FLAG_RECOMPUTE_KEYS)) {
+        // Gamma_K of every token, written by the segment pass and read by the output pass
+        p.kg = p.kn16 <= 64 ? 64 : 128;
+        p.off_gam = c.take((size_t)2 * BH * s.N * p.kg);
+    }
     p.total = c.total();
     return p;
 }
@@ -617,6 +625,8 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
     a.bimg_main_bytes = p.bimg_main_bytes;
     a.eps = s.eps;
     a.out_f32 = (s.flags & GMA_FLAG_OUT_F32) ? 1 : 0;
+    a.gam = p.off_gam ? (bf16 *)(ws + p.off_gam) : nullptr;
+    a.kg = p.kg;
     return a;
 }
 
@@ -635,6 +645,21 @@ bool make_xmap(CUtensorMap *m, const void *X, int BH, int N, int d_r)
                                 : d_r == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(X), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Key responsibilities [BH][N][kg] bf16: boxes of 64 components x 128 tokens, 128-byte swizzle
+// (the K-major operand layout of the kernels' Gamma_K tile).
+bool make_gmap(CUtensorMap *m, const void *G, int BH, int N, int kg)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kg, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)kg * 2, (cuuint64_t)N * kg * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(G), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -668,10 +693,12 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     a.KX = (const bf16 *)KX;
     a.O = O;
     const int BH = s.B * s.H;
-    CUtensorMap vmap;
+    CUtensorMap vmap, gmap;
     if (!make_vmap(&vmap, V, BH, s.N, s.d_v)) return GMA_ERR_CUDA;
+    memset(&gmap, 0, sizeof(gmap));
+    if (a.gam && !make_gmap(&gmap, a.gam, BH, s.N, p.kg)) return GMA_ERR_CUDA;
     {
-        const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, BH * p.nseg, st);
+        const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, gmap, BH * p.nseg, st);
         if (r != GMA_OK) return r;
     }
     const int KD4 = KMAX * p.ne / 4;
@@ -681,9 +708,16 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
                                                                                 causal ? 1 : 0)));
     if (causal) {
         CUtensorMap kmap, qmap;
-        if (!make_xmap(&kmap, a.KX, BH, s.N, DR) || !make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
-        const gma_status_t r = launch_causal_pipelined<DR>(a, vmap, kmap, qmap, BH * p.nseg, st);
-        if (r != GMA_OK) return r;
+        if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
+        if (a.gam) {
+            // Gamma_K was stored by the segment pass
+            const gma_status_t r = launch_causal_gamma<DR>(a, vmap, qmap, gmap, BH * p.nseg, st);
+            if (r != GMA_OK) return r;
+        } else {
+            if (!make_xmap(&kmap, a.KX, BH, s.N, DR)) return GMA_ERR_CUDA;
+            const gma_status_t r = launch_causal_pipelined<DR>(a, vmap, kmap, qmap, BH * p.nseg, st);
+            if (r != GMA_OK) return r;
+        }
     } else {
         const uint32_t sm = smem_for(Smem(DR, p.kn16, s.d_v, false, true, true).total + 1024, 256);
         if (!set_smem(tc_bidir_read_kernel<DR>, sm)) return GMA_ERR_CUDA;

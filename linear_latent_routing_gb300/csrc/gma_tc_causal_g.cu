@@ -1,0 +1,516 @@
+// gma_tc_causal_g.cu -- the chunked causal GMA kernel fed with stored key responsibilities
+// (tcgen05, sm_103a), warp-specialised.
+//
+// Method: page "Attention par Mélange Gaussien (GMA)" (gist.science/fr/paper/2606.18283),
+// Méthodologie §3 (causal variant: prefix sums of the latent memory and its normaliser) on top
+// of §1 (posterior responsibilities) and §2 (write and read phases).
+//
+// The segment pass has already computed Gamma_K of every token (bf16, normalised) and stored it
+// in the workspace; this pass reads it back by TMA instead of recomputing it.  One CTA handles
+// one segment of one (batch, head) slice from the segment's exclusive prefix memory S_start, in
+// chunks of C = 128 tokens.  With E_Q = exp2 of the query logits minus their row maximum (row
+// sums s_i, kept unnormalised):
+//   P      = E_Q Gamma_K^T                          (tensor cores, fp32 in TMEM)
+//   O_num  = E_Q S_{c-1} + tril(P) V_c              (tensor cores)
+//   den    = E_Q . Z_{c-1} + sum_{j<=i} P_ij        (CUDA cores, fp32)
+//   O      = O_num / (den + eps * s)
+//   S_c    = S_{c-1} + Gamma_K^T V_c                (tensor cores, fp32 in TMEM)
+//   Z_c    = Z_{c-1} + column sums of Gamma_K       (CUDA cores, fp32)
+//
+// Warp roles (416 threads):
+//   warps 0-3   mask:       causal mask of P (bf16, back into TMEM as the A operand of tril(P) V)
+//                           and the intra-chunk part of the normaliser;
+//   warps 4-7   query side: [x^2, x] of the queries (in place in the TMA-filled A tile), E_Q
+//                           (bf16, back into TMEM), its row sums and E_Q . Z_{c-1};
+//   warps 8-11  state/out:  the starting memory, Z_c, the bf16 operand copy of S_c, and the
+//                           output rows;
+//   warp 12     control:    TMA of the query rows, Gamma_K and value tiles, and every tcgen05.mma.
+// Tensor memory (512 columns): [0,128) query logits, then E_Q; [128,256) P; [256,384) output
+// numerator; [384,512) the running memory S.  The next chunk's query logits are computed while
+// the current chunk is masked, so the query softmax is the only long step between chunks.
+// Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all roles leave their loops.
+#include "tc_rows.cuh"
+
+namespace gma {
+namespace tck {
+
+namespace {
+
+constexpr int GTHREADS = 416;
+enum GBar {
+    G_BIMG, G_V, G_XQ, G_GT,                                    // TMA (transaction counts)
+    G_AQ, G_GQ0, G_GQ1, G_PS0, G_PS1, G_ZP, G_SP, G_OF,         // 128 threads of one role
+    G_LQ, G_P, G_PQ, G_S, G_PV0, G_PV1,                         // tcgen05.commit
+    G_NBAR
+};
+// Barriers completed once per chunk but waited on by a role that could in principle fall a
+// chunk behind come in pairs by chunk parity (GQ, PS, PV): each completes once per two chunks.
+constexpr uint32_t R_LQ = 0, R_P = 128, R_O = 256, R_S = 384;
+
+struct GSmem {
+    uint32_t bimg, ax, abq, gk, sp, ve, zbuf, zpart, dsq, dsm, bars, misc, total;
+    __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    __host__ __device__ GSmem(int DR, int kn16, int d_v)
+    {
+        const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
+        const uint32_t tile = ka / 64u * 128u;
+        uint32_t o = 0;
+        bimg = o; o = al(o + tile * (uint32_t)kn16 + 32u * (uint32_t)kn16);
+        ax = o; o = al(o + (uint32_t)C * 32u);
+        abq = o; o = al(o + (uint32_t)C * DR * 4u);   // queries [x^2 | x]
+        gk = o; o = al(o + 2u * C * 128u);            // Gamma_K (TMA)
+        sp = o; o = al(o + (uint32_t)d_v * KMAX * 2u);
+        ve = o; o = al(o + (uint32_t)d_v * C * 2u);
+        zbuf = o; o += 2u * KMAX * 4u;         // Z_{c-1} by chunk parity
+        zpart = o; o += 2u * 8u * KMAX * 4u;   // partial column sums by chunk parity
+        dsq = o; o += 2u * C * 8u;             // (row sum, E_Q . Z) per query row, by chunk parity
+        dsm = o; o += 2u * C * 8u;             // (row sum, normaliser) per query row, by chunk parity
+        bars = o; o += G_NBAR * 8u;
+        misc = o; o += 16u;
+        total = o;
+    }
+};
+
+// TMA of the Gamma_K rows [tok, tok + 128) of slice bh: kg / 64 boxes of 64 components, each
+// the 128-byte-swizzled K-major layout of one 64-component half of the tile.
+__device__ __forceinline__ void load_g_tile(uint8_t *gk, const CUtensorMap *map, uint64_t *bar, int kg, int tok, int bh)
+{
+    mbar_arrive_expect_tx(bar, (uint32_t)(C * kg * 2));
+    for (int hf = 0; hf < kg / 64; ++hf)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(gk + hf * C * 128)),
+            "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(64 * hf), "r"(tok), "r"(bh)
+            : "memory");
+}
+
+// Query side: unnormalised E_Q of this row (zeros when not valid) back into TMEM at tl as bf16
+// pairs; returns (row sum of the fp32 values, E_Q . z) with z the fp32 normaliser Z_{c-1}.
+__device__ __forceinline__ float2 query_exp(uint32_t tl, int K, int kc, bool valid, const float *z)
+{
+    const float m = row_max(tl, K, kc);
+    const float sc = valid ? 1.f : 0.f;
+    const float4 *z4 = reinterpret_cast<const float4 *>(z);
+    float srow = 0.f, den = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c < kc) {
+            uint32_t r[32];
+            tmem_ld32(tl + 32 * c, r);
+            tmem_ld_wait();
+            srow += chunk_exp(r, c, K, m);
+            float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 zz = z4[8 * c + q];
+                d4[0] = fmaf(__uint_as_float(r[4 * q]), zz.x, d4[0]);
+                d4[1] = fmaf(__uint_as_float(r[4 * q + 1]), zz.y, d4[1]);
+                d4[2] = fmaf(__uint_as_float(r[4 * q + 2]), zz.z, d4[2]);
+                d4[3] = fmaf(__uint_as_float(r[4 * q + 3]), zz.w, d4[3]);
+            }
+            den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = pk2(r[2 * j], r[2 * j + 1], sc);
+            tmem_st16(tl + 16 * c, w);   // E_Q (bf16 pairs), in place
+        }
+    }
+    tmem_st_wait();
+    return make_float2(srow, den);
+}
+
+// Mask side: row i of P (fp32 in TMEM at tl) masked to columns j <= i, written back as bf16
+// pairs in place; returns the sum of the kept fp32 values.
+__device__ __forceinline__ float mask_row(uint32_t tl, int i)
+{
+    float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int col = 32 * c + 2 * j;
+            const float p0 = col <= i ? __uint_as_float(r[2 * j]) : 0.f;
+            const float p1 = col + 1 <= i ? __uint_as_float(r[2 * j + 1]) : 0.f;
+            d4[j & 3] += p0 + p1;
+            w[j] = pack_bf16(p0, p1);
+        }
+        tmem_st16(tl + 16 * c, w);
+    }
+    tmem_st_wait();
+    return (d4[0] + d4[1]) + (d4[2] + d4[3]);
+}
+
+// State side: row k of the running memory S (d_v fp32 columns of TMEM at tl) as bf16 into the
+// MN-major SW32 operand tile sp.
+__device__ __forceinline__ void state_rows(uint32_t tl, int d_v, uint8_t *sp, int k)
+{
+    for (int b = 0; b < d_v / 16; ++b) {
+        uint32_t r[16];
+        tmem_ld16(tl + 16 * b, r);
+        tmem_ld_wait();
+        const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f),
+                                    pk2(r[6], r[7], 1.f));
+        const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f),
+                                    pk2(r[14], r[15], 1.f));
+        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
+        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
+    }
+}
+
+// State side: this thread's share of the column sums of the Gamma_K tile: components 8q..8q+7
+// over the rows g, g+8, ..., g+120 (t = 16 g + q), into zp[g][8q .. 8q+7].
+__device__ __forceinline__ void colsum_rows(const uint8_t *gk, float *zp, int t)
+{
+    const int q = t & 15, g = t >> 4;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int u = 0; u < C / 8; ++u) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(gk + sw128(g + 8 * u, q, C));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc[2 * e] += __uint_as_float(w[e] << 16);
+            acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+    }
+    float4 *o = reinterpret_cast<float4 *>(zp + g * KMAX + 8 * q);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+// Output side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.
+__device__ __forceinline__ void out_row(uint32_t tl, int d_v, float inv, bool valid, void *O, long long orow,
+                                        int out_f32)
+{
+    for (int c = 0; c < (d_v + 31) / 32; ++c) {   // 32 columns per wait
+        uint32_t r[32];
+        if (d_v == 16) {
+            tmem_ld16(tl, *reinterpret_cast<uint32_t(*)[16]>(r));
+        } else {
+            tmem_ld32(tl + 32 * c, r);
+        }
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int col0 = 32 * c;
+        const int ncol = d_v - col0 < 32 ? d_v - col0 : 32;
+        if (out_f32) {
+            float4 *o4 = reinterpret_cast<float4 *>((float *)O + orow * d_v + col0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (4 * q < ncol)
+                    o4[q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                        __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+        } else {
+            uint4 *o4 = reinterpret_cast<uint4 *>((bf16 *)O + orow * d_v + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (8 * q < ncol)
+                    o4[q] = make_uint4(pk2(r[8 * q], r[8 * q + 1], inv), pk2(r[8 * q + 2], r[8 * q + 3], inv),
+                                       pk2(r[8 * q + 4], r[8 * q + 5], inv), pk2(r[8 * q + 6], r[8 * q + 7], inv));
+        }
+    }
+}
+
+}  // namespace
+
+template <int DR>
+__global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args a,
+                                                                      const __grid_constant__ CUtensorMap vmap,
+                                                                      const __grid_constant__ CUtensorMap qmap,
+                                                                      const __grid_constant__ CUtensorMap gmap)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const GSmem L(DR, a.kn16, a.d_v);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 4);
+    float *zbuf = reinterpret_cast<float *>(smem + L.zbuf);
+    float *zpart = reinterpret_cast<float *>(smem + L.zpart);
+    float2 *dsq = reinterpret_cast<float2 *>(smem + L.dsq);
+    float2 *dsm = reinterpret_cast<float2 *>(smem + L.dsm);
+    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int tok0 = seg * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    const int nch = (tok_end - tok0 + C - 1) / C;
+    const int d_v = a.d_v;
+    const int kc = (a.K + 31) >> 5;
+    constexpr uint32_t XT = (uint32_t)C * DR * 2;   // bytes of one [x] tile (the TMA destination)
+
+    // ---------------------------------------------------------------- set-up (all threads)
+    if (warp == 12) {
+        if (t == 384) {
+            static const uint32_t counts[G_NBAR] = {1,   1,   1,   1,   128, 128, 128, 128, 128,
+                                                    128, 128, 128, 1,   1,   1,   1,   1,   1};
+            for (int i = 0; i < G_NBAR; ++i) mbar_init(bars + i, counts[i]);
+            *abort = 0;
+            fence_mbar_init();
+        }
+        __syncwarp();
+        tmem_alloc(tslot, 512);
+    } else if (warp < 4) {
+        // Gamma_K tile: with 64 stored components the second half is never loaded and must be 0
+        for (uint32_t o = t * 16; o < 2u * C * 128u; o += 128 * 16)
+            *reinterpret_cast<uint4 *>(smem + L.gk + o) = make_uint4(0, 0, 0, 0);
+    } else if (warp < 8) {
+        // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
+        const int i = t - 128;
+        const uint32_t one2 = 0x3C003C00u;   // fp16 pair (1, 1)
+        const int flip = (i >> 2) & 1;
+        *reinterpret_cast<uint4 *>(smem + L.ax + i * 32 + (flip << 4)) = make_uint4(one2, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(smem + L.ax + i * 32 + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t sb = smem_u32(smem);
+
+    if (warp == 12) {
+        // ============================================================ control warp
+        if (t == 384) {
+            const uint32_t id_p = idesc_f16(128, 128, 1, 1, 0, 0);
+            const uint32_t id_o = idesc_f16(128, (uint32_t)d_v, 1, 1, 0, 1);
+            const uint32_t id_s = idesc_f16(128, (uint32_t)d_v, 1, 1, 1, 1);
+            const int ksteps = a.kn16 / 16;
+            // TMA loads in flight: the chunk index of the last one issued per buffer (each buffer's
+            // barrier completes one phase per load, and a load is issued only after the previous
+            // one into that buffer was consumed)
+            int last_v = -1, last_xq = -1, last_gt = -1, last_pv = -1;
+            bool ok = true;
+            mbar_arrive_expect_tx(bars + G_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + G_BIMG);
+            if (nch > 0) {
+                load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0, bh);
+                load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0, bh);
+                load_v_chunk(smem + L.ve, &vmap, bars + G_V, d_v, tok0, bh);
+                last_xq = last_gt = last_v = 0;
+            }
+            ok = mbar_wait_abortable(bars + G_BIMG, 0, a.hdr, 100, abort);
+            const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
+            const uint32_t ve = sb + L.ve;
+            // query logits of chunk cq; once they are computed its A tile takes chunk cq + 1's rows
+            auto query_logits = [&](int cq) -> bool {
+                if (!mbar_wait_abortable(bars + G_AQ, cq & 1, a.hdr, 101, abort)) return false;
+                tc_fence_after();
+                issue_logits_x<DR>(tmem + R_LQ, sb + L.abq, bimg, bconst, sb + L.ax, a.kn16);
+                mma_commit(bars + G_LQ);
+                return true;
+            };
+            auto stage_queries = [&](int cq) -> bool {   // after the logits of chunk cq - 1
+                if (!mbar_wait_abortable(bars + G_LQ, (cq - 1) & 1, a.hdr, 102, abort)) return false;
+                load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0 + cq * C, bh);
+                last_xq = cq;
+                return true;
+            };
+            if (ok && nch > 0) ok = query_logits(0);
+            if (ok && nch > 1) ok = stage_queries(1);
+            for (int c = 0; ok && c < nch; ++c) {
+                const uint32_t ph = c & 1;
+                // P: E_Q and Gamma_K ready, S_{c-1} read out (for the read below), R_P free
+                if (!(ok = mbar_wait_abortable(bars + G_GQ0 + ph, (c >> 1) & 1, a.hdr, 103, abort))) break;
+                if (!(ok = mbar_wait_abortable(bars + G_GT, ph, a.hdr, 104, abort))) break;
+                if (!(ok = mbar_wait_abortable(bars + G_SP, ph, a.hdr, 105, abort))) break;
+                if (c > 0 && !(ok = mbar_wait_abortable(bars + G_PV0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 106,
+                                                        abort)))
+                    break;
+                tc_fence_after();
+                for (int s = 0; s < ksteps; ++s)   // P = E_Q Gamma_K^T
+                    mma_f16_tmem_a(tmem + R_P, tmem + R_LQ + 8 * s, kdesc(sb + L.gk, s, C), id_p, s > 0);
+                mma_commit(bars + G_P);
+                // the inter-chunk read (the output side is done with R_O)
+                if (c > 0 && !(ok = mbar_wait_abortable(bars + G_OF, (c - 1) & 1, a.hdr, 107, abort))) break;
+                tc_fence_after();
+                for (int s = 0; s < ksteps; ++s)   // O = E_Q S_{c-1}
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + 8 * s, mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
+                mma_commit(bars + G_PQ);
+                // S update
+                if (!(ok = mbar_wait_abortable(bars + G_V, ph, a.hdr, 108, abort))) break;
+                tc_fence_after();
+                for (int s = 0; s < C / 16; ++s)   // S += Gamma_K^T V
+                    mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(ve, s, C), id_s, 1u);
+                mma_commit(bars + G_S);
+                // the next chunk's query logits once E_Q is consumed (they run while P is masked)
+                if (c + 1 < nch) {
+                    if (!(ok = mbar_wait_abortable(bars + G_PQ, ph, a.hdr, 109, abort))) break;
+                    if (!(ok = query_logits(c + 1))) break;
+                }
+                // intra-chunk: O += tril(P) V
+                if (!(ok = mbar_wait_abortable(bars + G_PS0 + ph, (c >> 1) & 1, a.hdr, 110, abort))) break;
+                tc_fence_after();
+                for (int s = 0; s < C / 16; ++s)
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_P + 8 * s, mn32desc(ve, s, C), id_o, 1u);
+                mma_commit(bars + G_PV0 + ph);
+                last_pv = c;
+                // refill: Gamma_K once P, the S update and the column sums have read it; values once
+                // tril(P) V has; query rows once the next chunk's logits are done
+                if (c + 1 < nch) {
+                    if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 111, abort))) break;
+                    if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 112, abort))) break;
+                    load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0 + (c + 1) * C, bh);
+                    last_gt = c + 1;
+                    if (!(ok = mbar_wait_abortable(bars + G_PV0 + ph, (c >> 1) & 1, a.hdr, 113, abort))) break;
+                    load_v_chunk(smem + L.ve, &vmap, bars + G_V, d_v, tok0 + (c + 1) * C, bh);
+                    last_v = c + 1;
+                    if (c + 2 < nch && !(ok = stage_queries(c + 2))) break;
+                }
+            }
+            // drain: MMAs complete in issue order, so the last commit covers them all; TMA loads
+            // still in flight (only after a timeout) complete before shared memory is released
+            if (last_pv >= 0) mbar_wait(bars + G_PV0 + (last_pv & 1), (last_pv >> 1) & 1, a.hdr, 114);
+            if (last_v >= 0) mbar_wait(bars + G_V, last_v & 1, a.hdr, 115);
+            if (last_xq >= 0) mbar_wait(bars + G_XQ, last_xq & 1, a.hdr, 115);
+            if (last_gt >= 0) mbar_wait(bars + G_GT, last_gt & 1, a.hdr, 115);
+        }
+    } else if (warp < 4) {
+        // ============================================================ mask side
+        const int i = t;
+        const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            if (!mbar_wait_abortable(bars + G_P, ph, a.hdr, 120, abort)) break;
+            if (!mbar_wait_abortable(bars + G_GQ0 + ph, (c >> 1) & 1, a.hdr, 121, abort)) break;   // dsq
+            tc_fence_after();
+            const float intra = mask_row(lane + R_P, i);
+            const float2 q = dsq[ph * C + i];
+            dsm[ph * C + i] = make_float2(q.x, q.y + intra);
+            tc_fence_before();
+            mbar_arrive(bars + G_PS0 + ph);
+        }
+    } else if (warp < 8) {
+        // ============================================================ query side
+        const int i = t - 128;
+        const uint32_t lane = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        uint8_t *abq = smem + L.abq;
+        if (nch > 0 && mbar_wait_abortable(bars + G_XQ, 0, a.hdr, 130, abort)) {
+            build_inplace<DR>(abq, i);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + G_AQ);
+        }
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            const bool valid = tok0 + c * C + i < tok_end;
+            if (!mbar_wait_abortable(bars + G_LQ, ph, a.hdr, 131, abort)) break;
+            if (!mbar_wait_abortable(bars + G_SP, ph, a.hdr, 132, abort)) break;
+            tc_fence_after();
+            dsq[ph * C + i] = query_exp(lane + R_LQ, a.K, kc, valid, zbuf + ph * KMAX);
+            tc_fence_before();
+            mbar_arrive(bars + G_GQ0 + ph);
+            // the next chunk's queries, while P, the inter-chunk read and the mask run
+            if (c + 1 < nch) {
+                if (!mbar_wait_abortable(bars + G_XQ, (c + 1) & 1, a.hdr, 133, abort)) break;
+                build_inplace<DR>(abq, i);
+                fence_proxy_async_smem();
+                mbar_arrive(bars + G_AQ);
+            }
+        }
+    } else {
+        // ============================================================ state and output side
+        const int k = t - 256;   // TMEM lane: component row of S, and token row of the output
+        const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
+        // starting memory: V~ part to TMEM and as the bf16 operand, Z part to the running sum
+        const float *src = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + k) * a.ne;
+        for (int b = 0; b < d_v / 16; ++b) {
+            uint32_t r[16];
+            const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = s4[q];
+                r[4 * q] = __float_as_uint(f.x);
+                r[4 * q + 1] = __float_as_uint(f.y);
+                r[4 * q + 2] = __float_as_uint(f.z);
+                r[4 * q + 3] = __float_as_uint(f.w);
+            }
+            tmem_st16(lane + R_S + 16 * b, r);
+            const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
+            const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
+            *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 0, KMAX)) = lo;
+            *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 1, KMAX)) = hi;
+        }
+        float zrun = src[d_v];
+        zbuf[k] = zrun;
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bars + G_SP);   // phase 0: S_start ready
+        // output of chunk cc (numerator complete, normaliser from the mask side)
+        auto output = [&](int cc) -> bool {
+            const uint32_t pc = cc & 1;
+            if (!mbar_wait_abortable(bars + G_PS0 + pc, (cc >> 1) & 1, a.hdr, 140, abort)) return false;
+            if (!mbar_wait_abortable(bars + G_PV0 + pc, (cc >> 1) & 1, a.hdr, 141, abort)) return false;
+            tc_fence_after();
+            const float2 sd = dsm[pc * C + k];
+            const int row = tok0 + cc * C + k;
+            out_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), row < tok_end, a.O, (long long)bh * a.N + row,
+                    a.out_f32);
+            tc_fence_before();
+            mbar_arrive(bars + G_OF);
+            return true;
+        };
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t ph = c & 1;
+            if (c > 0 && !(ok = output(c - 1))) break;
+            // Z_c = Z_{c-1} + column sums of Gamma_K
+            if (!(ok = mbar_wait_abortable(bars + G_GT, ph, a.hdr, 142, abort))) break;
+            float *zp = zpart + ph * 8 * KMAX;
+            colsum_rows(smem + L.gk, zp, k);
+            mbar_arrive(bars + G_ZP);
+            if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 143, abort))) break;
+            {
+                float zs = 0.f;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) zs += zp[g * KMAX + k];
+                zrun += zs;
+            }
+            // readout of S_c (after the update, and after the read of S_{c-1} that it overwrites)
+            if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 144, abort))) break;
+            if (!(ok = mbar_wait_abortable(bars + G_PQ, ph, a.hdr, 145, abort))) break;
+            tc_fence_after();
+            state_rows(lane + R_S, d_v, smem + L.sp, k);
+            zbuf[((c + 1) & 1) * KMAX + k] = zrun;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars + G_SP);
+        }
+        if (ok && nch > 0) output(nch - 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 12) tmem_dealloc(tmem, 512);
+}
+
+// Shared memory the kernel needs (0 if the shape does not fit).
+uint32_t causal_gamma_smem(int d_r, int kn16, int d_v)
+{
+    const uint32_t need = GSmem(d_r, kn16, d_v).total + 1024;
+    return need <= 227u * 1024u ? smem_for(need, 512) : 0;
+}
+
+template <int DR>
+gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const CUtensorMap &qmap,
+                                 const CUtensorMap &gmap, int nblocks, cudaStream_t st)
+{
+    const uint32_t sm = causal_gamma_smem(DR, a.kn16, a.d_v);
+    if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!set_smem(tc_causal_gamma_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st, (tc_causal_gamma_kernel<DR><<<nblocks, GTHREADS, sm, st>>>(a, vmap, qmap, gmap)));
+    return GMA_OK;
+}
+
+template gma_status_t launch_causal_gamma<16>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_gamma<32>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_gamma<64>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, int, cudaStream_t);
+
+}  // namespace tck
+}  // namespace gma

@@ -13,6 +13,8 @@
 // S += Gamma_K^T [V | 1] into the running memory.  Logits, Gamma_K and value tiles are double
 // buffered, so one group's softmax overlaps the other group's logits and memory update.
 // Barriers are per buffer, so no waiter can fall two phases behind.
+// For the causal variant the kernel also stores each chunk's Gamma_K tile (bf16, normalised) to
+// the workspace with a TMA store, so that the output pass reads it instead of recomputing it.
 #include "tc_rows.cuh"
 
 namespace gma {
@@ -50,7 +52,8 @@ struct SegSmem {
 
 template <int DR>
 __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kernel(const Args a,
-                                                                                  const __grid_constant__ CUtensorMap vmap)
+                                                                                  const __grid_constant__ CUtensorMap vmap,
+                                                                                  const __grid_constant__ CUtensorMap gmap)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -119,16 +122,23 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             }
             ok = mbar_wait_abortable(bars + S_BIMG, 0, a.hdr, 80, abort);
             const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
-            // S update of chunk j: Gamma_K tile and value tile of buffer j & 1
+            // S update of chunk j: Gamma_K tile and value tile of buffer j & 1 (and the store of the
+            // tile; its buffer is released with the update's commit once the store has read it)
             auto update = [&](int j) -> bool {
                 const int g = j & 1, n = j >> 1;
                 if (!mbar_wait_abortable(bars + S_GK0 + g, n & 1, a.hdr, 81, abort)) return false;
                 if (!mbar_wait_abortable(bars + S_V0 + g, n & 1, a.hdr, 82, abort)) return false;
                 if (g) vpend1 = false; else vpend0 = false;
+                if (a.gam) {
+                    for (int h = 0; h < a.kg / 64; ++h)
+                        tma_store_3d(&gmap, smem + gk(j) + h * C * 128, 64 * h, tok0 + j * C, bh);
+                    bulk_commit_group();
+                }
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s)
                     mma_f16(tmem + SR_S, mn128desc(sb + gk(j), s, C), mn32desc(sb + ve(j), s, C), id_s,
                             (j > 0 || s > 0) ? 1u : 0u);
+                if (a.gam) bulk_wait_read();
                 mma_commit(bars + S_SD0 + g);
                 last_sd = j;
                 return true;
@@ -152,6 +162,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             }
             if (ok && nch > 0) ok = update(nch - 1);
             if (last_sd >= 0) mbar_wait(bars + S_SD0 + (last_sd & 1), (last_sd >> 1) & 1, a.hdr, 85);
+            if (a.gam) bulk_wait_all();
             if (vpend0 || vpend1) {
                 for (int c = nch - 1; c >= 0 && c >= nch - 2; --c)
                     if ((c & 1) ? vpend1 : vpend0) mbar_wait(bars + S_V0 + (c & 1), (c >> 1) & 1, a.hdr, 86);
@@ -218,19 +229,23 @@ uint32_t segmem_pipelined_smem(int d_r, int kn16, int d_v)
 }
 
 template <int DR>
-gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st)
+gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, const CUtensorMap &gmap,
+                                     int nblocks, cudaStream_t st)
 {
     const uint32_t sm = segmem_pipelined_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_segment_memory_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
     GMA_LAUNCH(KID_TC_CAUSAL_AGG, st,
-               (tc_segment_memory_pipelined_kernel<DR><<<nblocks, STHREADS, sm, st>>>(a, vmap)));
+               (tc_segment_memory_pipelined_kernel<DR><<<nblocks, STHREADS, sm, st>>>(a, vmap, gmap)));
     return GMA_OK;
 }
 
-template gma_status_t launch_segmem_pipelined<16>(const Args &, const CUtensorMap &, int, cudaStream_t);
-template gma_status_t launch_segmem_pipelined<32>(const Args &, const CUtensorMap &, int, cudaStream_t);
-template gma_status_t launch_segmem_pipelined<64>(const Args &, const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_segmem_pipelined<16>(const Args &, const CUtensorMap &, const CUtensorMap &, int,
+                                                    cudaStream_t);
+template gma_status_t launch_segmem_pipelined<32>(const Args &, const CUtensorMap &, const CUtensorMap &, int,
+                                                    cudaStream_t);
+template gma_status_t launch_segmem_pipelined<64>(const Args &, const CUtensorMap &, const CUtensorMap &, int,
+                                                    cudaStream_t);
 
 }  // namespace tck
 }  // namespace gma

@@ -45,6 +45,8 @@ struct Args {
     int bimg_bytes, bimg_main_bytes;
     float eps;
     int out_f32;
+    bf16 *gam;               // causal: key responsibilities [BH][N][kg] (null: recomputed)
+    int kg;
 };
 
 // ------------------------------------------------------------------ layout helpers
@@ -260,11 +262,17 @@ gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, con
 
 uint32_t segmem_pipelined_smem(int d_r, int kn16, int d_v);
 template <int DR>
-gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, int nblocks, cudaStream_t st);
+gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, const CUtensorMap &gmap,
+                                     int nblocks, cudaStream_t st);
+uint32_t causal_gamma_smem(int d_r, int kn16, int d_v);
+template <int DR>
+gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const CUtensorMap &qmap,
+                                 const CUtensorMap &gmap, int nblocks, cudaStream_t st);
 
 // ------------------------------------------------------------------ host helpers (gma_tc.cu)
 bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v);
 bool make_xmap(CUtensorMap *m, const void *X, int BH, int N, int d_r);
+bool make_gmap(CUtensorMap *m, const void *G, int BH, int N, int kg);
 uint32_t smem_for(uint32_t need, uint32_t tmem_cols);
 bool encode_available();
 

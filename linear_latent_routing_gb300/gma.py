@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "GMA_OK", 1: "GMA_ERR_INVALID_ARG", 2: "GMA_ERR_UNSUPPORTED_S
 GMA_F32, GMA_BF16 = 0, 1
 GMA_FLAG_SIMT = 0x1
 GMA_FLAG_OUT_F32 = 0x2
+GMA_FLAG_RECOMPUTE_KEYS = 0x4
 GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL = 0, 1, 2
 
 

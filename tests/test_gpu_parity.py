@@ -57,12 +57,35 @@ SMALL = [
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: f"{'c' if w.causal else 'b'}_{w.dtype}_"
                          f"B{w.B}H{w.H}N{w.N}r{w.d_r}K{w.K}v{w.d_v}")
-@pytest.mark.parametrize("flags", [0, 1], ids=["default", "simt"])
+@pytest.mark.parametrize("flags", [0, 1, 4], ids=["default", "simt", "recompute"])
 def test_small_cases_match_oracle(w, flags):
+    if flags == 4 and not w.causal:
+        pytest.skip("the flag only changes the causal path")
     O, ref = _run(w, flags=flags)
     err = normwise_error(O, ref)
     assert np.isfinite(O).all()
     assert err <= TOL[w.dtype], (err, rowwise_error(O, ref))
+
+
+def test_recompute_flag_shrinks_workspace_and_matches():
+    """Stored and recomputed key responsibilities give the same result; only the stored one
+    needs B*H*N*Kp bf16 values of workspace."""
+    gma = _gma()
+    w = W.scaled(W.LONG_CAUSAL, B=1, H=2, N=3000)
+    shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor)
+    small = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor,
+                           flags=gma.GMA_FLAG_RECOMPUTE_KEYS)
+    n_full = gma.gma_workspace_size(shape, gma.GMA_VARIANT_CAUSAL)
+    n_small = gma.gma_workspace_size(small, gma.GMA_VARIANT_CAUSAL)
+    assert n_full - n_small >= 2 * w.B * w.H * w.N * 128
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    a = gpu_forward(w, dev).float()
+    b = gpu_forward(w, dev, flags=gma.GMA_FLAG_RECOMPUTE_KEYS).float()
+    ref = oracle_forward(w, host)
+    assert normwise_error(a.cpu().numpy(), ref) <= TOL["bf16"]
+    assert normwise_error(b.cpu().numpy(), ref) <= TOL["bf16"]
+    assert (a - b).abs().max().item() <= 2e-2 * float(np.abs(ref).max())
 
 
 def test_fp32_output_flag():
