@@ -18,16 +18,21 @@
 //   Z_c    = Z_{c-1} + column sums of Gamma_K       (CUDA cores, fp32)
 //
 // Warp roles (416 threads):
-//   warps 0-3   mask:       causal mask of P (bf16, back into TMEM as the A operand of tril(P) V)
-//                           and the intra-chunk part of the normaliser;
-//   warps 4-7   query side: [x^2, x] of the queries (in place in the TMA-filled A tile), E_Q
-//                           (bf16, back into TMEM), its row sums and E_Q . Z_{c-1};
+//   warps 0-3   mask side:  E_Q of the upper half of the components (see below), then the causal
+//                           mask of P (bf16, back into TMEM as the A operand of tril(P) V) and
+//                           the complete normaliser;
+//   warps 4-7   query side: [x^2, x] of the queries (in place in the TMA-filled A tile), E_Q of
+//                           the lower half of the components, their row sums and E_Q . Z_{c-1};
 //   warps 8-11  state/out:  the starting memory, Z_c, the bf16 operand copy of S_c, and the
 //                           output rows;
 //   warp 12     control:    TMA of the query rows, Gamma_K and value tiles, and every tcgen05.mma.
 // Tensor memory (512 columns): [0,128) query logits, then E_Q; [128,256) P; [256,384) output
 // numerator; [384,512) the running memory S.  The next chunk's query logits are computed while
-// the current chunk is masked, so the query softmax is the only long step between chunks.
+// the current chunk is masked, so the query exponentials are the only long step between chunks;
+// two warps share each row of them (both take the row maximum, each exponentiates one half of
+// the components).  E_Q of 32-column group g (of kc groups, h = ceil(kc / 2) in the lower half)
+// is packed into 16 columns at 16 g (g < h) or 16 h + 16 g (g >= h): each half writes only
+// columns it has already read.
 // Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all roles leave their loops.
 #include "tc_rows.cuh"
 
@@ -38,8 +43,8 @@ namespace {
 
 constexpr int GTHREADS = 416;
 enum GBar {
-    G_BIMG, G_V, G_XQ, G_GT,                                    // TMA (transaction counts)
-    G_AQ, G_GQ0, G_GQ1, G_PS0, G_PS1, G_ZP, G_SP, G_OF,         // 128 threads of one role
+    G_BIMG, G_V0, G_V1, G_XQ, G_GT,                             // TMA (transaction counts)
+    G_AQ, G_XM, G_GQ0, G_GQ1, G_PS0, G_PS1, G_ZP, G_SP, G_OF,   // 128 threads (XM, GQ: 256)
     G_LQ, G_P, G_PQ, G_S, G_PV0, G_PV1,                         // tcgen05.commit
     G_NBAR
 };
@@ -48,7 +53,7 @@ enum GBar {
 constexpr uint32_t R_LQ = 0, R_P = 128, R_O = 256, R_S = 384;
 
 struct GSmem {
-    uint32_t bimg, ax, abq, gk, sp, ve, zbuf, zpart, dsq, dsm, bars, misc, total;
+    uint32_t bimg, ax, abq, gk, sp, ve0, ve1, zbuf, zpart, xmax, dsq, dsm, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ GSmem(int DR, int kn16, int d_v)
     {
@@ -60,10 +65,12 @@ struct GSmem {
         abq = o; o = al(o + (uint32_t)C * DR * 4u);   // queries [x^2 | x]
         gk = o; o = al(o + 2u * C * 128u);            // Gamma_K (TMA)
         sp = o; o = al(o + (uint32_t)d_v * KMAX * 2u);
-        ve = o; o = al(o + (uint32_t)d_v * C * 2u);
+        ve0 = o; o = al(o + (uint32_t)d_v * C * 2u);   // value tiles by chunk parity
+        ve1 = o; o = al(o + (uint32_t)d_v * C * 2u);
         zbuf = o; o += 2u * KMAX * 4u;         // Z_{c-1} by chunk parity
         zpart = o; o += 2u * 8u * KMAX * 4u;   // partial column sums by chunk parity
-        dsq = o; o += 2u * C * 8u;             // (row sum, E_Q . Z) per query row, by chunk parity
+        xmax = o; o += 4u * C * 4u;            // half-row maxima per half, by chunk parity
+        dsq = o; o += 2u * C * 8u;             // query side's (row sum, E_Q . Z), by chunk parity
         dsm = o; o += 2u * C * 8u;             // (row sum, normaliser) per query row, by chunk parity
         bars = o; o += G_NBAR * 8u;
         misc = o; o += 16u;
@@ -84,17 +91,19 @@ __device__ __forceinline__ void load_g_tile(uint8_t *gk, const CUtensorMap *map,
             : "memory");
 }
 
-// Query side: unnormalised E_Q of this row (zeros when not valid) back into TMEM at tl as bf16
-// pairs; returns (row sum of the fp32 values, E_Q . z) with z the fp32 normaliser Z_{c-1}.
-__device__ __forceinline__ float2 query_exp(uint32_t tl, int K, int kc, bool valid, const float *z)
+// Query rows: unnormalised E_Q of this row over the 32-column groups [g0, g1) (zeros when not
+// valid) back into TMEM at tl as bf16 pairs (group g at column 16 g + (g >= h ? 16 h : 0));
+// returns (row sum of the fp32 values, their dot product with z = Z_{c-1}).  m: the row maximum
+// over all groups; the caller waits for z (on `zbar`) only after computing it.
+__device__ __forceinline__ float2 query_exp_half(uint32_t tl, int K, int g0, int g1, int h, float m, bool valid,
+                                                 const float *z)
 {
-    const float m = row_max(tl, K, kc);
     const float sc = valid ? 1.f : 0.f;
     const float4 *z4 = reinterpret_cast<const float4 *>(z);
     float srow = 0.f, den = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        if (c < kc) {
+#pragma unroll 1
+    for (int c = g0; c < g1; ++c) {
+        {
             uint32_t r[32];
             tmem_ld32(tl + 32 * c, r);
             tmem_ld_wait();
@@ -112,7 +121,7 @@ __device__ __forceinline__ float2 query_exp(uint32_t tl, int K, int kc, bool val
             uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) w[j] = pk2(r[2 * j], r[2 * j + 1], sc);
-            tmem_st16(tl + 16 * c, w);   // E_Q (bf16 pairs), in place
+            tmem_st16(tl + 16 * c + (c >= h ? 16 * h : 0), w);   // E_Q (bf16 pairs)
         }
     }
     tmem_st_wait();
@@ -124,7 +133,7 @@ __device__ __forceinline__ float2 query_exp(uint32_t tl, int K, int kc, bool val
 __device__ __forceinline__ float mask_row(uint32_t tl, int i)
 {
     float d4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32(tl + 32 * c, r);
@@ -148,6 +157,7 @@ __device__ __forceinline__ float mask_row(uint32_t tl, int i)
 // MN-major SW32 operand tile sp.
 __device__ __forceinline__ void state_rows(uint32_t tl, int d_v, uint8_t *sp, int k)
 {
+#pragma unroll 1
     for (int b = 0; b < d_v / 16; ++b) {
         uint32_t r[16];
         tmem_ld16(tl + 16 * b, r);
@@ -186,6 +196,7 @@ __device__ __forceinline__ void colsum_rows(const uint8_t *gk, float *zp, int t)
 __device__ __forceinline__ void out_row(uint32_t tl, int d_v, float inv, bool valid, void *O, long long orow,
                                         int out_f32)
 {
+#pragma unroll 1
     for (int c = 0; c < (d_v + 31) / 32; ++c) {   // 32 columns per wait
         uint32_t r[32];
         if (d_v == 16) {
@@ -231,6 +242,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L.misc + 4);
     float *zbuf = reinterpret_cast<float *>(smem + L.zbuf);
     float *zpart = reinterpret_cast<float *>(smem + L.zpart);
+    float *xmax = reinterpret_cast<float *>(smem + L.xmax);
     float2 *dsq = reinterpret_cast<float2 *>(smem + L.dsq);
     float2 *dsm = reinterpret_cast<float2 *>(smem + L.dsm);
     const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
@@ -245,8 +257,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
     // ---------------------------------------------------------------- set-up (all threads)
     if (warp == 12) {
         if (t == 384) {
-            static const uint32_t counts[G_NBAR] = {1,   1,   1,   1,   128, 128, 128, 128, 128,
-                                                    128, 128, 128, 1,   1,   1,   1,   1,   1};
+            static const uint32_t counts[G_NBAR] = {1,   1,   1,   1,   1,   128, 256, 256, 256, 128,
+                                                    128, 128, 128, 128, 1,   1,   1,   1,   1,   1};
             for (int i = 0; i < G_NBAR; ++i) mbar_init(bars + i, counts[i]);
             *abort = 0;
             fence_mbar_init();
@@ -272,6 +284,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
 
+    const int hq = (kc + 1) >> 1;   // 32-column groups of E_Q taken by the query side
+
     if (warp == 12) {
         // ============================================================ control warp
         if (t == 384) {
@@ -279,23 +293,29 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             const uint32_t id_o = idesc_f16(128, (uint32_t)d_v, 1, 1, 0, 1);
             const uint32_t id_s = idesc_f16(128, (uint32_t)d_v, 1, 1, 1, 1);
             const int ksteps = a.kn16 / 16;
+            auto eq_col = [&](int s) -> uint32_t { return (uint32_t)(8 * s + (s >= 2 * hq ? 16 * hq : 0)); };
+            auto ve = [&](int c) -> uint32_t { return (c & 1) ? L.ve1 : L.ve0; };
             // TMA loads in flight: the chunk index of the last one issued per buffer (each buffer's
             // barrier completes one phase per load, and a load is issued only after the previous
             // one into that buffer was consumed)
-            int last_v = -1, last_xq = -1, last_gt = -1, last_pv = -1;
+            int last_v0 = -1, last_v1 = -1, last_xq = -1, last_gt = -1, last_pv = -1;
             bool ok = true;
+            auto load_v = [&](int c) {
+                load_v_chunk(smem + ve(c), &vmap, bars + G_V0 + (c & 1), d_v, tok0 + c * C, bh);
+                if (c & 1) last_v1 = c; else last_v0 = c;
+            };
             mbar_arrive_expect_tx(bars + G_BIMG, (uint32_t)a.bimg_bytes);
             bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + G_BIMG);
             if (nch > 0) {
                 load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0, bh);
                 load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0, bh);
-                load_v_chunk(smem + L.ve, &vmap, bars + G_V, d_v, tok0, bh);
-                last_xq = last_gt = last_v = 0;
+                last_xq = last_gt = 0;
+                load_v(0);
             }
+            if (nch > 1) load_v(1);
             ok = mbar_wait_abortable(bars + G_BIMG, 0, a.hdr, 100, abort);
             const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
-            const uint32_t ve = sb + L.ve;
-            // query logits of chunk cq; once they are computed its A tile takes chunk cq + 1's rows
+            // query logits of chunk cq
             auto query_logits = [&](int cq) -> bool {
                 if (!mbar_wait_abortable(bars + G_AQ, cq & 1, a.hdr, 101, abort)) return false;
                 tc_fence_after();
@@ -303,92 +323,91 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 mma_commit(bars + G_LQ);
                 return true;
             };
-            auto stage_queries = [&](int cq) -> bool {   // after the logits of chunk cq - 1
+            // the query rows of chunk cq, once the logits of chunk cq - 1 are done with the A tile
+            auto stage_queries = [&](int cq) -> bool {
                 if (!mbar_wait_abortable(bars + G_LQ, (cq - 1) & 1, a.hdr, 102, abort)) return false;
                 load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0 + cq * C, bh);
                 last_xq = cq;
                 return true;
             };
+            // S += Gamma_K^T V of chunk cc
+            auto update = [&](int cc) {
+                tc_fence_after();
+                for (int s = 0; s < C / 16; ++s)
+                    mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(sb + ve(cc), s, C), id_s, 1u);
+                mma_commit(bars + G_S);
+            };
             if (ok && nch > 0) ok = query_logits(0);
             if (ok && nch > 1) ok = stage_queries(1);
             for (int c = 0; ok && c < nch; ++c) {
                 const uint32_t ph = c & 1;
+                // the S update goes first if its operands are already there (it needs no query)
+                bool s_done = false;
+                if (mbar_test_wait(bars + G_GT, ph) && mbar_test_wait(bars + G_V0 + ph, (c >> 1) & 1) &&
+                    mbar_test_wait(bars + G_SP, ph)) {
+                    update(c);
+                    s_done = true;
+                }
                 // P: E_Q and Gamma_K ready, S_{c-1} read out (for the read below), R_P free
                 if (!(ok = mbar_wait_abortable(bars + G_GQ0 + ph, (c >> 1) & 1, a.hdr, 103, abort))) break;
                 if (!(ok = mbar_wait_abortable(bars + G_GT, ph, a.hdr, 104, abort))) break;
                 if (!(ok = mbar_wait_abortable(bars + G_SP, ph, a.hdr, 105, abort))) break;
-                if (c > 0 && !(ok = mbar_wait_abortable(bars + G_PV0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 106,
-                                                        abort)))
-                    break;
+                if (c > 0) {
+                    if (!(ok = mbar_wait_abortable(bars + G_PV0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 106,
+                                                   abort)))
+                        break;
+                    if (c + 1 < nch) load_v(c + 1);   // its buffer was read by chunk c - 1
+                }
                 tc_fence_after();
                 for (int s = 0; s < ksteps; ++s)   // P = E_Q Gamma_K^T
-                    mma_f16_tmem_a(tmem + R_P, tmem + R_LQ + 8 * s, kdesc(sb + L.gk, s, C), id_p, s > 0);
+                    mma_f16_tmem_a(tmem + R_P, tmem + R_LQ + eq_col(s), kdesc(sb + L.gk, s, C), id_p, s > 0);
                 mma_commit(bars + G_P);
                 // the inter-chunk read (the output side is done with R_O)
                 if (c > 0 && !(ok = mbar_wait_abortable(bars + G_OF, (c - 1) & 1, a.hdr, 107, abort))) break;
                 tc_fence_after();
                 for (int s = 0; s < ksteps; ++s)   // O = E_Q S_{c-1}
-                    mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + 8 * s, mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + eq_col(s), mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
                 mma_commit(bars + G_PQ);
-                // S update
-                if (!(ok = mbar_wait_abortable(bars + G_V, ph, a.hdr, 108, abort))) break;
-                tc_fence_after();
-                for (int s = 0; s < C / 16; ++s)   // S += Gamma_K^T V
-                    mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(ve, s, C), id_s, 1u);
-                mma_commit(bars + G_S);
-                // the next chunk's query logits once E_Q is consumed (they run while P is masked)
+                if (!s_done) {
+                    if (!(ok = mbar_wait_abortable(bars + G_V0 + ph, (c >> 1) & 1, a.hdr, 108, abort))) break;
+                    update(c);
+                }
                 if (c + 1 < nch) {
+                    // the next chunk's query logits once E_Q is consumed (they run while P is masked)
                     if (!(ok = mbar_wait_abortable(bars + G_PQ, ph, a.hdr, 109, abort))) break;
                     if (!(ok = query_logits(c + 1))) break;
+                    // Gamma_K once P, the S update and the column sums have read it
+                    if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 111, abort))) break;
+                    if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 112, abort))) break;
+                    load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0 + (c + 1) * C, bh);
+                    last_gt = c + 1;
                 }
                 // intra-chunk: O += tril(P) V
                 if (!(ok = mbar_wait_abortable(bars + G_PS0 + ph, (c >> 1) & 1, a.hdr, 110, abort))) break;
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s)
-                    mma_f16_tmem_a(tmem + R_O, tmem + R_P + 8 * s, mn32desc(ve, s, C), id_o, 1u);
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_P + 8 * s, mn32desc(sb + ve(c), s, C), id_o, 1u);
                 mma_commit(bars + G_PV0 + ph);
                 last_pv = c;
-                // refill: Gamma_K once P, the S update and the column sums have read it; values once
-                // tril(P) V has; query rows once the next chunk's logits are done
-                if (c + 1 < nch) {
-                    if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 111, abort))) break;
-                    if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 112, abort))) break;
-                    load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0 + (c + 1) * C, bh);
-                    last_gt = c + 1;
-                    if (!(ok = mbar_wait_abortable(bars + G_PV0 + ph, (c >> 1) & 1, a.hdr, 113, abort))) break;
-                    load_v_chunk(smem + L.ve, &vmap, bars + G_V, d_v, tok0 + (c + 1) * C, bh);
-                    last_v = c + 1;
-                    if (c + 2 < nch && !(ok = stage_queries(c + 2))) break;
-                }
+                if (c + 2 < nch && !(ok = stage_queries(c + 2))) break;
             }
             // drain: MMAs complete in issue order, so the last commit covers them all; TMA loads
             // still in flight (only after a timeout) complete before shared memory is released
             if (last_pv >= 0) mbar_wait(bars + G_PV0 + (last_pv & 1), (last_pv >> 1) & 1, a.hdr, 114);
-            if (last_v >= 0) mbar_wait(bars + G_V, last_v & 1, a.hdr, 115);
+            if (last_v0 >= 0) mbar_wait(bars + G_V0, (last_v0 >> 1) & 1, a.hdr, 115);
+            if (last_v1 >= 0) mbar_wait(bars + G_V1, (last_v1 >> 1) & 1, a.hdr, 115);
             if (last_xq >= 0) mbar_wait(bars + G_XQ, last_xq & 1, a.hdr, 115);
             if (last_gt >= 0) mbar_wait(bars + G_GT, last_gt & 1, a.hdr, 115);
         }
-    } else if (warp < 4) {
-        // ============================================================ mask side
-        const int i = t;
-        const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
-        for (int c = 0; c < nch; ++c) {
-            const uint32_t ph = c & 1;
-            if (!mbar_wait_abortable(bars + G_P, ph, a.hdr, 120, abort)) break;
-            if (!mbar_wait_abortable(bars + G_GQ0 + ph, (c >> 1) & 1, a.hdr, 121, abort)) break;   // dsq
-            tc_fence_after();
-            const float intra = mask_row(lane + R_P, i);
-            const float2 q = dsq[ph * C + i];
-            dsm[ph * C + i] = make_float2(q.x, q.y + intra);
-            tc_fence_before();
-            mbar_arrive(bars + G_PS0 + ph);
-        }
     } else if (warp < 8) {
-        // ============================================================ query side
-        const int i = t - 128;
-        const uint32_t lane = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        // ============================================================ query rows: mask side
+        // (warps 0-3, upper component groups) and query side (warps 4-7, lower groups)
+        const bool qs = warp >= 4;
+        const int i = t & 127;
+        const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const int g0 = qs ? 0 : hq, g1 = qs ? hq : kc;
         uint8_t *abq = smem + L.abq;
-        if (nch > 0 && mbar_wait_abortable(bars + G_XQ, 0, a.hdr, 130, abort)) {
+        if (qs && nch > 0 && mbar_wait_abortable(bars + G_XQ, 0, a.hdr, 130, abort)) {
             build_inplace<DR>(abq, i);
             fence_proxy_async_smem();
             mbar_arrive(bars + G_AQ);
@@ -396,18 +415,39 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
         for (int c = 0; c < nch; ++c) {
             const uint32_t ph = c & 1;
             const bool valid = tok0 + c * C + i < tok_end;
+            // E_Q: the row maximum from both halves, then each half's exponentials
             if (!mbar_wait_abortable(bars + G_LQ, ph, a.hdr, 131, abort)) break;
-            if (!mbar_wait_abortable(bars + G_SP, ph, a.hdr, 132, abort)) break;
             tc_fence_after();
-            dsq[ph * C + i] = query_exp(lane + R_LQ, a.K, kc, valid, zbuf + ph * KMAX);
+            const float mh = row_max_groups(lane + R_LQ, a.K, g0, g1);
+            xmax[(qs ? 0 : 2 * C) + ph * C + i] = mh;
+            tc_fence_before();
+            mbar_arrive(bars + G_XM);
+            if (!mbar_spin_wait(bars + G_XM, ph, a.hdr, 134, abort)) break;
+            tc_fence_after();
+            const float m = fmaxf(mh, xmax[(qs ? 2 * C : 0) + ph * C + i]);
+            if (!mbar_wait_abortable(bars + G_SP, ph, a.hdr, 132, abort)) break;
+            const float2 part = query_exp_half(lane + R_LQ, a.K, g0, g1, hq, m, valid, zbuf + ph * KMAX);
+            if (qs) dsq[ph * C + i] = part;
             tc_fence_before();
             mbar_arrive(bars + G_GQ0 + ph);
-            // the next chunk's queries, while P, the inter-chunk read and the mask run
-            if (c + 1 < nch) {
-                if (!mbar_wait_abortable(bars + G_XQ, (c + 1) & 1, a.hdr, 133, abort)) break;
-                build_inplace<DR>(abq, i);
-                fence_proxy_async_smem();
-                mbar_arrive(bars + G_AQ);
+            if (qs) {
+                // the next chunk's queries, while P, the inter-chunk read and the mask run
+                if (c + 1 < nch) {
+                    if (!mbar_wait_abortable(bars + G_XQ, (c + 1) & 1, a.hdr, 133, abort)) break;
+                    build_inplace<DR>(abq, i);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bars + G_AQ);
+                }
+            } else {
+                // causal mask of P; P (bf16 pairs) back into TMEM as the A operand of tril(P) V
+                if (!mbar_wait_abortable(bars + G_P, ph, a.hdr, 120, abort)) break;
+                if (!mbar_wait_abortable(bars + G_GQ0 + ph, (c >> 1) & 1, a.hdr, 121, abort)) break;   // dsq
+                tc_fence_after();
+                const float intra = mask_row(lane + R_P, i);
+                const float2 q = dsq[ph * C + i];
+                dsm[ph * C + i] = make_float2(q.x + part.x, q.y + part.y + intra);
+                tc_fence_before();
+                mbar_arrive(bars + G_PS0 + ph);
             }
         }
     } else {

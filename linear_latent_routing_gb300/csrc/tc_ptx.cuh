@@ -123,6 +123,23 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t pari
     }
 }
 
+// For waits expected to be short (a partner warp doing the same work): polls without
+// suspending, so the thread resumes as soon as the phase completes.  Same bounds as above.
+__device__ __forceinline__ bool mbar_spin_wait(uint64_t *bar, uint32_t parity, WsHeader *hdr, unsigned where,
+                                               volatile int *abort)
+{
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+            record_error(hdr, GMA_ERR_TIMEOUT, where);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Barrier among the `nthreads` threads (whole warps) that use hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {
