@@ -697,8 +697,10 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     if (!make_vmap(&vmap, V, BH, s.N, s.d_v)) return GMA_ERR_CUDA;
     memset(&gmap, 0, sizeof(gmap));
     if (a.gam && !make_gmap(&gmap, a.gam, BH, s.N, p.kg)) return GMA_ERR_CUDA;
+    CUtensorMap kmap;
+    if (!make_xmap(&kmap, a.KX, BH, s.N, DR)) return GMA_ERR_CUDA;
     {
-        const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, gmap, BH * p.nseg, st);
+        const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, kmap, gmap, BH * p.nseg, st);
         if (r != GMA_OK) return r;
     }
     const int KD4 = KMAX * p.ne / 4;
@@ -707,14 +709,13 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
                (tc_scan_kernel<<<(unsigned)((tot4 + 255) / 256), 256, 0, st>>>(a.agg, tot4, p.nseg, KD4,
                                                                                 causal ? 1 : 0)));
     if (causal) {
-        CUtensorMap kmap, qmap;
+        CUtensorMap qmap;
         if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
         if (a.gam) {
             // Gamma_K was stored by the segment pass
             const gma_status_t r = launch_causal_gamma<DR>(a, vmap, qmap, gmap, BH * p.nseg, st);
             if (r != GMA_OK) return r;
         } else {
-            if (!make_xmap(&kmap, a.KX, BH, s.N, DR)) return GMA_ERR_CUDA;
             const gma_status_t r = launch_causal_pipelined<DR>(a, vmap, kmap, qmap, BH * p.nseg, st);
             if (r != GMA_OK) return r;
         }

@@ -8,8 +8,9 @@
 // exclusive prefixes, each the starting memory of the chunked kernel's segment.
 //
 // Warp roles (288 threads): two key-side groups of four warps take alternate chunks of 128
-// tokens ([x^2, x], softmax -> Gamma_K in their own shared-memory tile); warp 8 issues the TMA of
-// the value tiles and the tcgen05.mma's: the logits into the chunk's own TMEM columns and
+// tokens ([x^2, x] from the TMA-staged key rows, softmax -> Gamma_K in their own shared-memory
+// tile); warp 8 issues the TMA of the key rows and value tiles and the tcgen05.mma's: the logits
+// into the chunk's own TMEM columns and
 // S += Gamma_K^T [V | 1] into the running memory.  Logits, Gamma_K and value tiles are double
 // buffered, so one group's softmax overlaps the other group's logits and memory update.
 // Barriers are per buffer, so no waiter can fall two phases behind.
@@ -23,11 +24,11 @@ namespace tck {
 namespace {
 
 constexpr int STHREADS = 288;
-enum SBar { S_BIMG, S_AK, S_LK0, S_LK1, S_GK0, S_GK1, S_SD0, S_SD1, S_V0, S_V1, S_NBAR };
+enum SBar { S_BIMG, S_AK, S_LK0, S_LK1, S_GK0, S_GK1, S_SD0, S_SD1, S_V0, S_V1, S_XK, S_NBAR };
 constexpr uint32_t SR_L0 = 0, SR_L1 = 128, SR_S = 256;
 
 struct SegSmem {
-    uint32_t bimg, ax, abuf, gk0, gk1, ve0, ve1, bars, misc, total;
+    uint32_t bimg, ax, abuf, xst, gk0, gk1, ve0, ve1, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ SegSmem(int DR, int kn16, int d_v)
     {
@@ -38,6 +39,7 @@ struct SegSmem {
         bimg = o; o = al(o + tile * (uint32_t)kn16 + 32u * (uint32_t)kn16);
         ax = o; o = al(o + (uint32_t)C * 32u);
         abuf = o; o = al(o + tile * (uint32_t)C);
+        xst = o; o = al(o + (uint32_t)C * DR * 2u);   // staged key rows (TMA, swizzled)
         gk0 = o; o = al(o + 2u * C * 128u);
         gk1 = o; o = al(o + 2u * C * 128u);
         ve0 = o; o = al(o + vbytes);
@@ -53,6 +55,7 @@ struct SegSmem {
 template <int DR>
 __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kernel(const Args a,
                                                                                   const __grid_constant__ CUtensorMap vmap,
+                                                                                  const __grid_constant__ CUtensorMap kmap,
                                                                                   const __grid_constant__ CUtensorMap gmap)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -120,6 +123,11 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
                 load_v_chunk(smem + ve(c), &vmap, bars + S_V0 + c, d_v, tok0 + c * C, bh);
                 if (c) vpend1 = true; else vpend0 = true;
             }
+            int last_xk = -1;
+            if (nch > 0) {
+                load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0, bh);
+                last_xk = 0;
+            }
             ok = mbar_wait_abortable(bars + S_BIMG, 0, a.hdr, 80, abort);
             const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
             // S update of chunk j: Gamma_K tile and value tile of buffer j & 1 (and the store of the
@@ -146,6 +154,10 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             for (int c = 0; ok && c < nch; ++c) {
                 const int g = c & 1;
                 if (!(ok = mbar_wait_abortable(bars + S_AK, c & 1, a.hdr, 83, abort))) break;
+                if (c + 1 < nch) {   // the staged rows of chunk c have been read
+                    load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0 + (c + 1) * C, bh);
+                    last_xk = c + 1;
+                }
                 tc_fence_after();
                 issue_logits_c<DR>(tmem + (g ? SR_L1 : SR_L0), sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
                 mma_commit(bars + S_LK0 + g);
@@ -162,6 +174,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             }
             if (ok && nch > 0) ok = update(nch - 1);
             if (last_sd >= 0) mbar_wait(bars + S_SD0 + (last_sd & 1), (last_sd >> 1) & 1, a.hdr, 85);
+            if (last_xk >= 0) mbar_wait(bars + S_XK, last_xk & 1, a.hdr, 86);
             if (a.gam) bulk_wait_all();
             if (vpend0 || vpend1) {
                 for (int c = nch - 1; c >= 0 && c >= nch - 2; --c)
@@ -174,25 +187,22 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
         const int k = t & 127;              // TMEM lane, token row, component row
         const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         uint8_t *gk = smem + (g ? L.gk1 : L.gk0);
-        uint4 x[DR / 8];
-        if (g < nch) load_x<DR>(a.KX, (long long)bh * a.N + tok0 + g * C + k, tok0 + g * C + k < tok_end, x);
         for (int c = g; c < nch; c += 2) {
             const int n = c >> 1;
             const int base = tok0 + c * C;
             // the [x^2, x] buffer is free once the previous chunk's logits are done
             if (c >= 1 && !mbar_wait_abortable(bars + S_LK0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 90, abort)) break;
-            build_a<DR>(smem + L.abuf, k, x);
+            if (!mbar_wait_abortable(bars + S_XK, c & 1, a.hdr, 94, abort)) break;
+            build_a_s<DR>(smem + L.abuf, k, smem + L.xst);
             fence_proxy_async_smem();
             mbar_arrive(bars + S_AK);
             if (!mbar_wait_abortable(bars + S_LK0 + g, n & 1, a.hdr, 91, abort)) break;
             if (c >= 2 && !mbar_wait_abortable(bars + S_SD0 + g, (n - 1) & 1, a.hdr, 92, abort)) break;
             tc_fence_after();
-            key_softmax<true>(lane + (g ? SR_L1 : SR_L0), a.K, kc, base + k < tok_end, gk, k);
+            key_softmax_reg(lane + (g ? SR_L1 : SR_L0), a.K, kc, base + k < tok_end, gk, k);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bars + S_GK0 + g);
-            const int nb = base + 2 * C;
-            load_x<DR>(a.KX, (long long)bh * a.N + nb + k, nb + k < tok_end, x);
         }
         // group 0 writes the segment's memory once the last update is done
         if (g == 0 && !*abort) {
@@ -229,23 +239,23 @@ uint32_t segmem_pipelined_smem(int d_r, int kn16, int d_v)
 }
 
 template <int DR>
-gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, const CUtensorMap &gmap,
-                                     int nblocks, cudaStream_t st)
+gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap,
+                                     const CUtensorMap &gmap, int nblocks, cudaStream_t st)
 {
     const uint32_t sm = segmem_pipelined_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_segment_memory_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
     GMA_LAUNCH(KID_TC_CAUSAL_AGG, st,
-               (tc_segment_memory_pipelined_kernel<DR><<<nblocks, STHREADS, sm, st>>>(a, vmap, gmap)));
+               (tc_segment_memory_pipelined_kernel<DR><<<nblocks, STHREADS, sm, st>>>(a, vmap, kmap, gmap)));
     return GMA_OK;
 }
 
-template gma_status_t launch_segmem_pipelined<16>(const Args &, const CUtensorMap &, const CUtensorMap &, int,
-                                                    cudaStream_t);
-template gma_status_t launch_segmem_pipelined<32>(const Args &, const CUtensorMap &, const CUtensorMap &, int,
-                                                    cudaStream_t);
-template gma_status_t launch_segmem_pipelined<64>(const Args &, const CUtensorMap &, const CUtensorMap &, int,
-                                                    cudaStream_t);
+template gma_status_t launch_segmem_pipelined<16>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                                    const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_segmem_pipelined<32>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                                    const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_segmem_pipelined<64>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                                    const CUtensorMap &, int, cudaStream_t);
 
 }  // namespace tck
 }  // namespace gma

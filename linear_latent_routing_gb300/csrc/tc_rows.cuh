@@ -164,6 +164,40 @@ __device__ __noinline__ void key_softmax(uint32_t tl, int K, int kc, bool valid,
     }
 }
 
+// Key side: Gamma_K row k = softmax of the TMEM logits at tl, normalised (zeros when not valid),
+// as bf16 into the K-major SW128 tile gk; the exponentials of the row are held in registers as
+// bf16 pairs until the row sum is known, so each tile element is written once.
+__device__ __forceinline__ void key_softmax_reg(uint32_t tl, int K, int kc, bool valid, uint8_t *gk, int k)
+{
+    const float m = row_max(tl, K, kc);
+    float sum = 0.f;
+    uint32_t pk[64];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c < kc) {
+            uint32_t r[32];
+            tmem_ld32(tl + 32 * c, r);
+            tmem_ld_wait();
+            sum += chunk_exp(r, c, K, m);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[16 * c + j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        }
+    }
+    const float scf = valid ? 1.0f / sum : 0.f;
+    const uint32_t sc2 = pack_bf16(scf, scf);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c < kc) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t *e = pk + 16 * c + 4 * q;
+                *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c + q, C)) =
+                    make_uint4(mul_bf16x2(e[0], sc2), mul_bf16x2(e[1], sc2), mul_bf16x2(e[2], sc2), mul_bf16x2(e[3], sc2));
+            }
+        }
+    }
+}
+
 template <int DR>
 __device__ __forceinline__ void issue_logits_c(uint32_t d, uint32_t abuf, uint32_t bimg, uint32_t bconst,
                                                uint32_t ax, int kn16)
