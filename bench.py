@@ -70,7 +70,9 @@ def kernel_work(w, name):
     th = w.token_heads
     esz = 2 if w.dtype == "bf16" else 4
     if name == "tc_causal_chunked":
-        return "hbm", th * esz * (2 * w.d_r + 2 * w.d_v), "GB/s"
+        # the output pass reads Q_X and V and writes O (K_X is read by the segment pass; the
+        # stored Gamma_K it also reads is not algorithmic traffic)
+        return "hbm", th * esz * (w.d_r + 2 * w.d_v), "GB/s"
     if name == "tc_causal_segment_memory":
         return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
     if name == "tc_bidir_write":
@@ -94,8 +96,8 @@ def kernel_work(w, name):
 def traffic_per_launch(kernel, w):
     """DRAM bytes (read + write) of one launch of `kernel` on workload `w`, from the committed
     ncu summary profiles/dram_traffic.json (captured per token-head on a smaller case of the same
-    kernel, scaled by the units one launch processes); None when no capture exists or the
-    kernel's source changed since it was taken."""
+    kernel, scaled by the units one launch processes); None when no capture exists or any of the
+    kernel's source files changed since it was taken."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
@@ -103,8 +105,13 @@ def traffic_per_launch(kernel, w):
     rec = json.load(open(p)).get(kernel)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        src = os.path.join(ROOT, f)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    if h.hexdigest() != rec["sources_sha256"]:
         return None
     if rec.get("workload_shape") != [w.d_r, w.K, w.d_v, w.dtype, w.causal]:
         return None
