@@ -373,29 +373,27 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
 
 // Causal: exclusive prefix of the segment memories within each slice (in place).
 // Bidirectional: the total over all segments, written to segment 0.
-// One thread per 4 consecutive floats of one slice; segments are read 8 at a time so that the
-// loads are in flight together.
-__global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, long long total4,
-                                                      int nseg, int KD4, int causal)
+// One thread per float of one slice's memory; consecutive threads take consecutive floats (each
+// load instruction of a warp reads 128 contiguous bytes), and 16 segments are read at a time so
+// that enough loads are in flight to cover DRAM latency.
+__global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, long long total, int nseg,
+                                                      int KD, int causal)
 {
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= total4) return;
-    const long long bh = idx / KD4, e = idx % KD4;
-    float4 *base = reinterpret_cast<float4 *>(agg) + bh * nseg * KD4 + e;
-    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < nseg; s0 += 8) {
-        float4 v[8];
+    if (idx >= total) return;
+    const long long bh = idx / KD, e = idx % KD;
+    float *base = agg + bh * nseg * KD + e;
+    float run = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += 16) {
+        float v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (s0 + u < nseg) v[u] = base[(size_t)(s0 + u) * KD4];
+        for (int u = 0; u < 16; ++u)
+            if (s0 + u < nseg) v[u] = base[(size_t)(s0 + u) * KD];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
             if (s0 + u < nseg) {
-                if (causal) base[(size_t)(s0 + u) * KD4] = run;
-                run.x += v[u].x;
-                run.y += v[u].y;
-                run.z += v[u].z;
-                run.w += v[u].w;
+                if (causal) base[(size_t)(s0 + u) * KD] = run;
+                run += v[u];
             }
         }
     }
@@ -703,11 +701,11 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
         const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, kmap, gmap, BH * p.nseg, st);
         if (r != GMA_OK) return r;
     }
-    const int KD4 = KMAX * p.ne / 4;
-    const long long tot4 = (long long)BH * KD4;
+    const int KD = KMAX * p.ne;
+    const long long tot = (long long)BH * KD;
     GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st,
-               (tc_scan_kernel<<<(unsigned)((tot4 + 255) / 256), 256, 0, st>>>(a.agg, tot4, p.nseg, KD4,
-                                                                                causal ? 1 : 0)));
+               (tc_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(a.agg, tot, p.nseg, KD,
+                                                                              causal ? 1 : 0)));
     if (causal) {
         CUtensorMap qmap;
         if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
