@@ -400,57 +400,6 @@ __global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, l
     if (!causal) base[0] = run;
 }
 
-// Bidirectional read: O = Gamma_Q [V~ | Z] / (.. + eps) for `cps` chunks of one slice.
-template <int DR>
-__global__ void __launch_bounds__(THREADS, 1) tc_bidir_read_kernel(const Args a)
-{
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const Smem L(DR, a.kn16, a.d_v, false, true, true);
-    const int ntile = a.nseg;   // tile groups per slice
-    const int bh = blockIdx.x / ntile, grp = blockIdx.x % ntile, h = bh % a.H;
-    const int t = threadIdx.x, warp = t >> 5;
-    const int tok0 = grp * a.cps * C;
-    const int tok_end = min(a.N, tok0 + a.cps * C);
-    const uint32_t R_O = 0;
-    Bars bars;
-    uint32_t tmem;
-    uint32_t ph_b = 0, ph_m = 0;
-    cta_setup(smem, L, bars, 256, a, h, tmem);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t id_o = idesc_f16(128, (uint32_t)a.ne, 1, 1, 0, 1);
-    float *cst = reinterpret_cast<float *>(smem + L.cst);
-    // the slice's total memory (segment 0 after the scan), bf16 operand only
-    load_state(a.agg + ((size_t)bh * a.nseg * KMAX + t) * a.ne, 0xFFFFFFFFu, a.ne, t, smem + L.sp);
-    bool ok = wait_all(bars.bimg, ph_b, a.hdr, 30);
-    uint4 xq[DR / 8];
-    if (ok) load_x<DR>(a.QX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, xq);
-    for (int base = tok0; ok && base < tok_end; base += C) {
-        const bool valid = base + t < tok_end;
-        build_a<DR>(smem + L.abuf, t, xq);
-        publish_smem();
-        if (t == 0) {
-            issue_logits<DR>(tmem + R_O, sb + L.abuf, sb + L.bimg, a.kn16);
-            mma_commit(bars.mma);
-        }
-        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 31))) break;
-        const float srow = softmax_row(tmem + lane_off + R_O, cst, a.K, t, valid, false, smem + L.gq);
-        const int nb = base + C;
-        load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, xq);
-        publish_smem();
-        if (t == 0) {
-            for (int s = 0; s < a.kn16 / 16; ++s)
-                mma_f16(tmem + R_O, kdesc(sb + L.gq, s, C), mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
-            mma_commit(bars.mma);
-        }
-        if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 32))) break;
-        write_out(tmem + lane_off + R_O, a.d_v, a.eps * srow, valid, a.O, (long long)bh * a.N + base + t,
-                  a.out_f32);
-        sync_tc();
-    }
-    cta_teardown(tmem, 256);
-}
 
 // Responsibilities only: gamma rows (normalised) straight from registers to global memory.
 template <int DR>
@@ -718,9 +667,10 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
             if (r != GMA_OK) return r;
         }
     } else {
-        const uint32_t sm = smem_for(Smem(DR, p.kn16, s.d_v, false, true, true).total + 1024, 256);
-        if (!set_smem(tc_bidir_read_kernel<DR>, sm)) return GMA_ERR_CUDA;
-        GMA_LAUNCH(KID_TC_BIDIR_READ, st, (tc_bidir_read_kernel<DR><<<BH * p.nseg, THREADS, sm, st>>>(a)));
+        CUtensorMap qmap;
+        if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
+        const gma_status_t r = launch_bidir_read2<DR>(a, qmap, BH * p.nseg, st);
+        if (r != GMA_OK) return r;
     }
     return GMA_OK;
 }

@@ -264,6 +264,9 @@ uint32_t segmem_pipelined_smem(int d_r, int kn16, int d_v);
 template <int DR>
 gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap,
                                      const CUtensorMap &gmap, int nblocks, cudaStream_t st);
+uint32_t bidir_read2_smem(int d_r, int kn16, int d_v);
+template <int DR>
+gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblocks, cudaStream_t st);
 uint32_t causal_gamma_smem(int d_r, int kn16, int d_v);
 template <int DR>
 gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const CUtensorMap &qmap,
