@@ -292,26 +292,22 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
     const int h = blockIdx.x;
     const int ka = d_r * 2 < 64 ? 64 : d_r * 2;
     const float *lh = logits + (size_t)h * K;
-    __shared__ float red[THREADS];
-    float m = -INFINITY;
-    for (int k = threadIdx.x; k < K; k += THREADS) m = fmaxf(m, lh[k]);
-    red[threadIdx.x] = m;
+    // log-sum-exp of the head's prior logits (K <= 128: one per thread), by warp shuffles and one
+    // exchange between the four warps
+    __shared__ float red[2][THREADS / 32];
+    const float lv = threadIdx.x < K ? lh[threadIdx.x] : -INFINITY;
+    float m = lv;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = m;
     __syncthreads();
-    for (int o = THREADS / 2; o > 0; o >>= 1) {
-        if (threadIdx.x < o) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + o]);
-        __syncthreads();
-    }
-    m = red[0];
+    m = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+    float sum = threadIdx.x < K ? expf(lv - m) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if ((threadIdx.x & 31) == 0) red[1][threadIdx.x >> 5] = sum;
     __syncthreads();
-    float sum = 0.f;
-    for (int k = threadIdx.x; k < K; k += THREADS) sum += expf(lh[k] - m);
-    red[threadIdx.x] = sum;
-    __syncthreads();
-    for (int o = THREADS / 2; o > 0; o >>= 1) {
-        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
-        __syncthreads();
-    }
-    const float lse = m + logf(red[0]);
+    const float lse = m + logf((red[1][0] + red[1][1]) + (red[1][2] + red[1][3]));
     uint8_t *img = bimg + (size_t)h * bimg_bytes;
     const int n = blockIdx.y * 16 + (threadIdx.x >> 3);   // component
     const int sub = threadIdx.x & 7;
@@ -374,8 +370,10 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
 // Causal: exclusive prefix of the segment memories within each slice (in place).
 // Bidirectional: the total over all segments, written to segment 0.
 // One thread per float of one slice's memory; consecutive threads take consecutive floats (each
-// load instruction of a warp reads 128 contiguous bytes), and 16 segments are read at a time so
-// that enough loads are in flight to cover DRAM latency.
+// load instruction of a warp reads 128 contiguous bytes).  All of a thread's segments (NB at a
+// time, NB chosen from the segment count) are loaded before any result is stored, so the loads
+// are in flight together.
+template <int NB>
 __global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, long long total, int nseg,
                                                       int KD, int causal)
 {
@@ -384,17 +382,14 @@ __global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, l
     const long long bh = idx / KD, e = idx % KD;
     float *base = agg + bh * nseg * KD + e;
     float run = 0.f;
-    for (int s0 = 0; s0 < nseg; s0 += 16) {
-        float v[16];
+    for (int s0 = 0; s0 < nseg; s0 += NB) {
+        float v[NB];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-            if (s0 + u < nseg) v[u] = base[(size_t)(s0 + u) * KD];
+        for (int u = 0; u < NB; ++u) v[u] = s0 + u < nseg ? __ldcg(base + (size_t)(s0 + u) * KD) : 0.f;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            if (s0 + u < nseg) {
-                if (causal) base[(size_t)(s0 + u) * KD] = run;
-                run += v[u];
-            }
+        for (int u = 0; u < NB; ++u) {
+            if (causal && s0 + u < nseg) base[(size_t)(s0 + u) * KD] = run;
+            run += v[u];
         }
     }
     if (!causal) base[0] = run;
@@ -522,7 +517,7 @@ struct Plan {
     size_t off_bimg, off_cst, off_agg, off_gam, total;
 };
 
-constexpr int kTargetCtas = 152 * 4;
+constexpr int kSms = 152;   // GB300
 
 Plan make_plan(const gma_shape_t &s, int variant)
 {
@@ -534,11 +529,28 @@ Plan make_plan(const gma_shape_t &s, int variant)
     p.bimg_bytes = p.bimg_main_bytes + 32 * p.kn16;
     const int BH = s.B * s.H;
     const int nchunks = (s.N + C - 1) / C;
-    int nseg = (kTargetCtas + BH - 1) / BH;
-    if (nseg > nchunks) nseg = nchunks;
-    if (nseg < 1) nseg = 1;
-    p.cps = (nchunks + nseg - 1) / nseg;
-    p.nseg = (nchunks + p.cps - 1) / p.cps;
+    // Segments per slice: one CTA per segment, one CTA per SM at a time.  Time model: waves of
+    // CTAs x (set-up + chunks per segment), with the set-up (operand tables, start memory, the
+    // first chunk's loads) worth about 0.6 chunk; the cheapest split wins (the larger one on a
+    // tie).
+    {
+        double best = 1e30;
+        int best_n = 1;
+        const int top = nchunks < 2048 ? nchunks : 2048;
+        for (int n = 1; n <= top; ++n) {
+            const int cps = (nchunks + n - 1) / n;
+            const int segs = (nchunks + cps - 1) / cps;
+            const long long ctas = (long long)BH * segs;
+            const long long waves = (ctas + kSms - 1) / kSms;
+            const double cost = (double)waves * (0.6 + cps);
+            if (cost <= best) {
+                best = cost;
+                best_n = segs;
+            }
+        }
+        p.cps = (nchunks + best_n - 1) / best_n;
+        p.nseg = (nchunks + p.cps - 1) / p.cps;
+    }
     Carve c;
     p.off_bimg = c.take((size_t)s.H * p.bimg_bytes);
     p.off_cst = c.take(sizeof(float) * (size_t)s.H * p.kn16);
@@ -652,9 +664,18 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     }
     const int KD = KMAX * p.ne;
     const long long tot = (long long)BH * KD;
-    GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st,
-               (tc_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(a.agg, tot, p.nseg, KD,
-                                                                              causal ? 1 : 0)));
+    {
+        const unsigned nb = (unsigned)((tot + 255) / 256);
+        const int cz = causal ? 1 : 0;
+        if (p.nseg <= 4)
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<4><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+        else if (p.nseg <= 8)
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<8><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+        else if (p.nseg <= 20)
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<20><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+        else
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<40><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+    }
     if (causal) {
         CUtensorMap qmap;
         if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;

@@ -62,10 +62,42 @@ def test_noalloc_matches_regular_entry_point_twice(gma):
     assert normwise_error(got, oracle_forward(w, host)) <= TOL["bf16"]
 
 
+def _sizes(gma, w):
+    full = _shape(gma, w)
+    small = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor,
+                           flags=gma.GMA_FLAG_RECOMPUTE_KEYS)
+    return (full, gma.gma_workspace_size(full, gma.GMA_VARIANT_CAUSAL),
+            gma.gma_workspace_size(small, gma.GMA_VARIANT_CAUSAL))
+
+
+def test_noalloc_falls_back_to_the_smaller_workspace(gma):
+    """A shape whose default workspace exceeds the array but whose recompute-keys workspace fits
+    runs as if GMA_FLAG_RECOMPUTE_KEYS were set."""
+    w = W.scaled(W.LM_CAUSAL, B=1, H=16, N=32768)
+    shape, n_full, n_small = _sizes(gma, w)
+    assert n_full > gma.GMA_NOALLOC_SCRATCH_BYTES >= n_small
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    ptrs = [dev[k].data_ptr() for k in ("QX", "KX", "V", "mu", "raw", "logits")]
+    stream = torch.cuda.current_stream().cuda_stream
+    O = torch.full((w.B, w.H, w.N, w.d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+    r = gma.gma_forward_causal_noalloc(shape, *ptrs, O.data_ptr(), stream)
+    assert r == 0, gma.gma_status_string(r)
+    from parity import gpu_forward
+    ref = gpu_forward(w, dev, flags=gma.GMA_FLAG_RECOMPUTE_KEYS)
+    torch.cuda.synchronize()
+    assert torch.equal(O, ref)
+    n = 2048
+    exact = oracle_forward(w, host, b=0, h=w.H - 1, n=n)
+    assert normwise_error(O[0:1, w.H - 1:w.H, :n].float().cpu().numpy(), exact) <= TOL["bf16"]
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(gma):
-    w = W.LONG_CAUSAL
-    shape = _shape(gma, w)
-    assert gma.gma_workspace_size(shape, gma.GMA_VARIANT_CAUSAL) > gma.GMA_NOALLOC_SCRATCH_BYTES
+    # 512 heads: the per-head tables and segment memories alone exceed the array, whatever the
+    # segment split, so the call must return before enqueuing anything
+    w = W.scaled(W.LONG_CAUSAL, H=512, N=4096)
+    shape, n_full, n_small = _sizes(gma, w)
+    assert n_small > gma.GMA_NOALLOC_SCRATCH_BYTES   # checked before any pointer is passed
     fake = 1 << 20   # never dereferenced: the size check fails first
     r = gma.gma_forward_causal_noalloc(shape, *([fake] * 7), None)
     assert r == 4   # GMA_ERR_WORKSPACE
