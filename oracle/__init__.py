@@ -33,6 +33,11 @@ def _load():
         lib.gmao_forward.argtypes = ([ctypes.c_int] * 7 + [dp] * 6
                                      + [ctypes.c_double, ctypes.c_double, dp, ctypes.c_int])
         lib.gmao_forward.restype = ctypes.c_int
+        lib.gmao_decode_step.argtypes = [ctypes.c_int] * 5 + [dp] * 6 + [ctypes.c_double] * 2 + [dp] * 2
+        lib.gmao_decode_step.restype = None
+        lib.gmao_forward_cross.argtypes = ([ctypes.c_int] * 7 + [dp] * 6
+                                           + [ctypes.c_double, ctypes.c_double, dp])
+        lib.gmao_forward_cross.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -98,3 +103,50 @@ def forward(causal, QX, KX, V, mu, raw, logits, var_floor, eps, nthreads=0, retu
                                 _p(mu), _p(raw), _p(logits), float(var_floor), float(eps), _p(O),
                                 int(nthreads))
     return (O, used) if return_threads else O
+
+
+def decode_step(qx, kx, v, mu, raw, logits, var_floor, eps, state):
+    """One autoregressive step of the causal variant for every (batch, head) slice.
+
+    qx, kx: [B, H, d_r]; v: [B, H, d_v]; state: [B, H, K, d_v + 1] (the prefix memory V~ and, in
+    the last column, the normaliser Z).  Returns (o [B, H, d_v], the updated state), float64;
+    the state passed in is not modified.
+    """
+    qx = _f64(qx)
+    kx = _f64(kx)
+    v = _f64(v)
+    mu = _f64(mu)
+    raw = _f64(raw)
+    logits = _f64(logits)
+    S = np.array(state, dtype=np.float64, copy=True, order="C")
+    B, H, d_r = qx.shape
+    d_v = v.shape[-1]
+    K = mu.shape[1]
+    assert S.shape == (B, H, K, d_v + 1)
+    o = np.empty((B, H, d_v))
+    _load().gmao_decode_step(B, H, d_r, K, d_v, _p(qx), _p(kx), _p(v), _p(mu), _p(raw), _p(logits),
+                             float(var_floor), float(eps), _p(S), _p(o))
+    return o, S
+
+
+def forward_cross(QX, KX, V, mu, raw, logits, var_floor, eps):
+    """Cross-attention on the bidirectional path: O [B, H, Nq, d_v] (float64).
+
+    QX: [B, H, Nq, d_r]; KX: [B, H, Nk, d_r]; V: [B, H, Nk, d_v].
+    """
+    QX = _f64(QX)
+    KX = _f64(KX)
+    V = _f64(V)
+    mu = _f64(mu)
+    raw = _f64(raw)
+    logits = _f64(logits)
+    B, H, Nq, d_r = QX.shape
+    Nk = KX.shape[2]
+    d_v = V.shape[-1]
+    K = mu.shape[1]
+    assert KX.shape == (B, H, Nk, d_r) and V.shape[:3] == (B, H, Nk)
+    O = np.empty((B, H, Nq, d_v))
+    _load().gmao_forward_cross(B, H, Nq, Nk, d_r, K, d_v, _p(QX), _p(KX), _p(V), _p(mu), _p(raw),
+                               _p(logits), float(var_floor), float(eps), _p(O))
+    return O
+

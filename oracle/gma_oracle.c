@@ -208,3 +208,102 @@ int gmao_forward(int causal, int B, int H, int N, int d_r, int K, int d_v, const
     free(logpi);
     return used;
 }
+
+/* One autoregressive decode step per (batch, head) slice: the causal variant (Méthodologie §3) for
+ * one new token whose key and value join the prefix before its query reads it.
+ *   gamma_K = p(z | kx);   S[k][c] += gamma_K[k] v[c]  (c < d_v);   S[k][d_v] += gamma_K[k]
+ *   gamma_Q = p(z | qx);   o[c] = (gamma_Q . S[:, c]) / (gamma_Q . S[:, d_v] + eps)
+ * qx, kx [B][H][d_r]; v [B][H][d_v]; state [B][H][K][d_v + 1], updated in place; o [B][H][d_v]. */
+void gmao_decode_step(int B, int H, int d_r, int K, int d_v, const double *qx, const double *kx,
+                      const double *v, const double *mu, const double *raw, const double *logits,
+                      double var_floor, double eps, double *state, double *o)
+{
+    double *var = (double *)malloc(sizeof(double) * (size_t)K * d_r);
+    double *logpi = (double *)malloc(sizeof(double) * (size_t)K);
+    double *gk = (double *)malloc(sizeof(double) * (size_t)K);
+    double *gq = (double *)malloc(sizeof(double) * (size_t)K);
+    double *work = (double *)malloc(sizeof(double) * (size_t)K);
+    const int ne = d_v + 1;
+    for (int bh = 0; bh < B * H; ++bh) {
+        const int h = bh % H;
+        gmao_params(K, d_r, raw + (size_t)h * K * d_r, logits + (size_t)h * K, var_floor, var, logpi);
+        const double *muh = mu + (size_t)h * K * d_r;
+        oracle_posterior(d_r, K, kx + (size_t)bh * d_r, muh, var, logpi, gk, work);
+        oracle_posterior(d_r, K, qx + (size_t)bh * d_r, muh, var, logpi, gq, work);
+        double *S = state + (size_t)bh * K * ne;
+        const double *vb = v + (size_t)bh * d_v;
+        for (int k = 0; k < K; ++k) {
+            for (int c = 0; c < d_v; ++c)
+                S[(size_t)k * ne + c] += gk[k] * vb[c];
+            S[(size_t)k * ne + d_v] += gk[k];
+        }
+        double den = 0.0;
+        for (int k = 0; k < K; ++k)
+            den += gq[k] * S[(size_t)k * ne + d_v];
+        for (int c = 0; c < d_v; ++c) {
+            double num = 0.0;
+            for (int k = 0; k < K; ++k)
+                num += gq[k] * S[(size_t)k * ne + c];
+            o[(size_t)bh * d_v + c] = num / (den + eps);
+        }
+    }
+    free(var);
+    free(logpi);
+    free(gk);
+    free(gq);
+    free(work);
+}
+
+/* Cross-attention on the bidirectional path: the Nk keys and values of a slice write the memory
+ * (Méthodologie §2, write phase) and the Nq queries read it (read phase).
+ * QX [B][H][Nq][d_r]; KX [B][H][Nk][d_r]; V [B][H][Nk][d_v]; O [B][H][Nq][d_v]. */
+int gmao_forward_cross(int B, int H, int Nq, int Nk, int d_r, int K, int d_v, const double *QX,
+                       const double *KX, const double *V, const double *mu, const double *raw,
+                       const double *logits, double var_floor, double eps, double *O)
+{
+    double *var = (double *)malloc(sizeof(double) * (size_t)K * d_r);
+    double *logpi = (double *)malloc(sizeof(double) * (size_t)K);
+    double *Vt = (double *)malloc(sizeof(double) * (size_t)K * d_v);
+    double *Z = (double *)malloc(sizeof(double) * (size_t)K);
+    double *g = (double *)malloc(sizeof(double) * (size_t)K);
+    double *work = (double *)malloc(sizeof(double) * (size_t)K);
+    for (int bh = 0; bh < B * H; ++bh) {
+        const int h = bh % H;
+        gmao_params(K, d_r, raw + (size_t)h * K * d_r, logits + (size_t)h * K, var_floor, var, logpi);
+        const double *muh = mu + (size_t)h * K * d_r;
+        for (int i = 0; i < K * d_v; ++i)
+            Vt[i] = 0.0;
+        for (int k = 0; k < K; ++k)
+            Z[k] = 0.0;
+        for (int j = 0; j < Nk; ++j) {
+            oracle_posterior(d_r, K, KX + ((size_t)bh * Nk + j) * d_r, muh, var, logpi, g, work);
+            const double *vj = V + ((size_t)bh * Nk + j) * d_v;
+            for (int k = 0; k < K; ++k) {
+                Z[k] += g[k];
+                for (int c = 0; c < d_v; ++c)
+                    Vt[(size_t)k * d_v + c] += g[k] * vj[c];
+            }
+        }
+        for (int i = 0; i < Nq; ++i) {
+            oracle_posterior(d_r, K, QX + ((size_t)bh * Nq + i) * d_r, muh, var, logpi, g, work);
+            double den = 0.0;
+            for (int k = 0; k < K; ++k)
+                den += g[k] * Z[k];
+            double *oi = O + ((size_t)bh * Nq + i) * d_v;
+            for (int c = 0; c < d_v; ++c) {
+                double num = 0.0;
+                for (int k = 0; k < K; ++k)
+                    num += g[k] * Vt[(size_t)k * d_v + c];
+                oi[c] = num / (den + eps);
+            }
+        }
+    }
+    free(var);
+    free(logpi);
+    free(Vt);
+    free(Z);
+    free(g);
+    free(work);
+    return 1;
+}
+

@@ -285,3 +285,76 @@ def test_pins_catch_planted_mistakes():
     assert np.abs(At @ V / (At.sum(1, keepdims=True) + 1e-6) - O).max() > 1e-3
     Ae = np.tril(A, -1)
     assert np.abs(Ae @ V / (Ae.sum(1, keepdims=True) + 1e-6) - O).max() > 1e-3
+
+
+# ---------------------------------------------------------------- decode step and cross-attention
+
+def test_decode_steps_reproduce_the_causal_affinity_form():
+    """N decode steps from an empty memory give the causal rows of the explicit affinity form
+    (Méthodologie §3), and the final memory is sum_j gamma_K,j [v_j, 1] by scipy's posterior."""
+    c = _rand_case(11, N=13)
+    B, H, N, d_r = c["QX"].shape
+    d_v = c["V"].shape[-1]
+    K = c["mu"].shape[1]
+    S = np.zeros((B, H, K, d_v + 1))
+    outs = []
+    for i in range(N):
+        o, S = oracle.decode_step(c["QX"][:, :, i], c["KX"][:, :, i], c["V"][:, :, i], c["mu"],
+                                  c["raw"], c["logits"], 1e-3, 1e-6, S)
+        outs.append(o)
+    got = np.stack(outs, axis=2)
+    ref = bruteforce.forward(True, c["QX"], c["KX"], c["V"], c["mu"], c["raw"], c["logits"], 1e-3, 1e-6)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    for b in range(B):
+        for h in range(H):
+            var = bruteforce.softplus(c["raw"][h]) + 1e-3
+            g = bruteforce.posterior(c["KX"][b, h], c["mu"][h], var, c["logits"][h])
+            mem = g.T @ np.concatenate([c["V"][b, h], np.ones((N, 1))], axis=1)
+            np.testing.assert_allclose(S[b, h], mem, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_step_leaves_the_input_state_alone_and_adds_one_token():
+    c = _rand_case(12, N=1)
+    B, H, _, d_r = c["QX"].shape
+    K = c["mu"].shape[1]
+    d_v = c["V"].shape[-1]
+    S0 = np.random.default_rng(3).random((B, H, K, d_v + 1))
+    keep = S0.copy()
+    o, S1 = oracle.decode_step(c["QX"][:, :, 0], c["KX"][:, :, 0], c["V"][:, :, 0], c["mu"],
+                               c["raw"], c["logits"], 1e-3, 0.0, S0)
+    assert np.array_equal(S0, keep)
+    for b in range(B):
+        for h in range(H):
+            var = bruteforce.softplus(c["raw"][h]) + 1e-3
+            gk = bruteforce.posterior(c["KX"][b, h], c["mu"][h], var, c["logits"][h])[0]
+            gq = bruteforce.posterior(c["QX"][b, h], c["mu"][h], var, c["logits"][h])[0]
+            add = np.outer(gk, np.append(c["V"][b, h, 0], 1.0))
+            np.testing.assert_allclose(S1[b, h] - S0[b, h], add, atol=1e-12)
+            np.testing.assert_allclose(o[b, h], gq @ S1[b, h][:, :d_v] / (gq @ S1[b, h][:, d_v]),
+                                       rtol=1e-12)
+
+
+@pytest.mark.parametrize("nq,nk", [(5, 23), (31, 4), (1, 1)])
+def test_cross_attention_equals_explicit_affinity(nq, nk):
+    """Nq queries reading the memory of Nk keys (the bidirectional path with N_q != N_k) equals
+    A~ V / (A~ 1 + eps) with the rectangular A~ = Gamma_Q Gamma_K^T."""
+    r = np.random.default_rng(nq * 100 + nk)
+    B, H, d_r, K, d_v = 2, 2, 5, 6, 3
+    QX = r.standard_normal((B, H, nq, d_r))
+    KX = r.standard_normal((B, H, nk, d_r))
+    V = r.standard_normal((B, H, nk, d_v))
+    mu = r.standard_normal((H, K, d_r))
+    raw = r.standard_normal((H, K, d_r)) * 0.5
+    logits = r.standard_normal((H, K))
+    got = oracle.forward_cross(QX, KX, V, mu, raw, logits, 1e-3, 1e-6)
+    for b in range(B):
+        for h in range(H):
+            ref = bruteforce.forward_slice(False, QX[b, h], KX[b, h], V[b, h], mu[h], raw[h], logits[h],
+                                   1e-3, 1e-6)
+            np.testing.assert_allclose(got[b, h], ref, rtol=0, atol=1e-12)
+
+
+def test_cross_attention_with_equal_lengths_is_the_bidirectional_forward():
+    c = _rand_case(13, N=17)
+    got = oracle.forward_cross(c["QX"], c["KX"], c["V"], c["mu"], c["raw"], c["logits"], 1e-3, 1e-6)
+    np.testing.assert_allclose(got, _fwd(c, False), rtol=0, atol=1e-13)
