@@ -90,7 +90,17 @@ def kernel_work(w, name):
         return "alu", th * f, "TFLOP/s"
     if name == "simt_segment_memory":
         return "alu", th * 2 * w.K * (w.d_v + 1), "TFLOP/s"
+    if name == "decode_step":
+        # the fp32 state is read and written once; q_x, k_x and v read, o written
+        return "hbm", decode_bytes(w), "GB/s"
     return "hbm", 0, "GB/s"
+
+
+def decode_bytes(w):
+    """Algorithmic bytes of one decode step: every slice's K x (d_v + 1) fp32 state read and
+    written once, plus this token's q_x, k_x, v and o."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return w.B * w.H * (2 * 4 * w.K * (w.d_v + 1) + esz * (2 * w.d_r + 2 * w.d_v))
 
 
 def traffic_per_launch(kernel, w):
@@ -396,6 +406,170 @@ def run_gma(args, ws, rank, local):
     }
 
 
+# ----------------------------------------------------------------------------- decode
+DECODE_METRIC = "GMA decode tokens/s (one new token per sequence per step), B=128,H=16,K=128,d_v=128"
+
+
+def is_decode(w):
+    return w.name.startswith("decode_")
+
+
+def oracle_decode_sample(w, budget_s):
+    """Time the fp64 oracle's decode step on all slices of the batch, repeated for about
+    budget_s.  Returns (tokens/s, cores, description, steps)."""
+    import oracle
+    a = W.to_numpy(W.make_inputs(w))
+    S = W.make_decode_state(w).double().numpy()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        t = n % w.N
+        _, S = oracle.decode_step(a["QX"][:, :, t], a["KX"][:, :, t], a["V"][:, :, t], a["mu"],
+                                  a["raw"], a["logits"], w.var_floor, w.eps, S)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    desc = (f"oracle decode step (fp64 C, one thread) over all {w.B}x{w.H} slices of {w.name}, "
+            f"{n} steps")
+    return w.B * n / dt, 1, desc, n
+
+
+def run_decode(args, ws, rank, local):
+    """One timed step = one gma_decode_step over the whole batch: every sequence takes one token.
+    The state (135 MB fp32) stays on the device between steps, as a serving cache does; it is
+    larger than L2, so nothing is flushed."""
+    from linear_latent_routing_gb300 import gma
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w0 = W.by_name(args.workload)
+    w = W.Workload(**{**w0.__dict__, "seed": w0.seed + 1000 * rank})
+    host = W.make_inputs(w)
+    rows = {k: [host[k][:, :, t].contiguous() for t in range(w.N)] for k in ("QX", "KX", "V")}
+    drows = {k: [r.to(device) for r in rows[k]] for k in rows}
+    par = {k: host[k].to(device) for k in ("mu", "raw", "logits")}
+    state = W.make_decode_state(w).to(device)
+    dt = gma.GMA_BF16 if w.dtype == "bf16" else gma.GMA_F32
+    shape = gma.make_shape(w.B, w.H, 1, w.d_r, w.K, w.d_v, dt, w.eps, w.var_floor)
+    ws_n = gma.gma_workspace_size(shape, gma.GMA_VARIANT_DECODE)
+    workspace = torch.empty(ws_n, dtype=torch.uint8, device=device)
+    o = torch.empty(w.B, w.H, w.d_v, dtype=host["V"].dtype, device=device)
+    stream = torch.cuda.Stream(device)
+    sh = stream.cuda_stream
+    it = [0]
+
+    def step(src=None):
+        t = it[0] % w.N
+        it[0] += 1
+        q, k, v = (src or drows)["QX"][t], (src or drows)["KX"][t], (src or drows)["V"][t]
+        r = gma.gma_decode_step(shape, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                par["mu"].data_ptr(), par["raw"].data_ptr(),
+                                par["logits"].data_ptr(), state.data_ptr(), o.data_ptr(),
+                                workspace.data_ptr(), ws_n, sh)
+        if r != 0:
+            raise gma.GmaError(r, "gma_decode_step")
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    steps = args.steps if args.steps > 0 else 2000
+    gma.gma_timing_enable(steps * 4 + 64)
+    clocks = ClockSampler(device)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    launches = gma.gma_timing_read(steps * 4 + 64)
+    gma.gma_timing_enable(0)
+    st = gma.gma_check_workspace(workspace.data_ptr(), sh)
+    if st != 0:
+        raise gma.GmaError(st, "timed region")
+    total_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    value = w.B * ws * steps / (total_ms / 1e3)
+    per_kernel = {}
+    for name, ms in launches:
+        per_kernel.setdefault(name, []).append(ms)
+    avg_ms = sum(per_kernel["decode_step"]) / len(per_kernel["decode_step"])
+    pk = peaks()
+    achieved = decode_bytes(w) / (avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "decode_step", "achieved": round(achieved, 3),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": traffic_per_launch("decode_step", w),
+                "avg_launch_us": round(avg_ms * 1e3, 3),
+                "launches": len(per_kernel["decode_step"]),
+                "peak_source": f"hbm_gbs of {pk['source']}"}
+    step_s = total_ms / steps / 1e3
+    path_roofline = {"roofline_step_us": round(decode_bytes(w) / (pk["hbm_gbs"] * 1e9) * 1e6, 3),
+                     "measured_step_us": round(step_s * 1e6, 3),
+                     "frac": round(decode_bytes(w) / (pk["hbm_gbs"] * 1e9) / step_s, 4),
+                     "alg_bytes": decode_bytes(w)}
+
+    # end to end: each step's q_x, k_x, v rows come from pinned host memory and o goes back
+    pin = {k: [r.pin_memory() for r in rows[k]] for k in rows}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(pin[k][0].numel() * pin[k][0].element_size() for k in pin)
+    d2h = o_host.numel() * o_host.element_size()
+    stage = {k: [torch.empty_like(drows[k][0])] * w.N for k in drows}
+
+    def e2e_step():
+        t = it[0] % w.N
+        for k in pin:
+            stage[k][t].copy_(pin[k][t], non_blocking=True)
+        step(stage)
+        o_host.copy_(o, non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = min(steps, 500)
+        with torch.cuda.stream(stream):
+            e2e_step()
+        stream.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), ws, device)
+        e2e = {"value": w.B * ws * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    if rank != 0:
+        return None
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_decode_sample(w0, args.cpu_budget)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    return {
+        "metric": DECODE_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) rows and a seeded non-zero starting state)",
+        "config": {"workload": w0.name, "variant": "decode", "B": w.B, "H": w.H, "d_r": w.d_r,
+                   "K": w.K, "d_v": w.d_v, "state_bytes": 4 * w.B * w.H * w.K * (w.d_v + 1),
+                   "l2": "state larger than L2 (%.0f MB > 129 MB), no flush"
+                         % (4 * w.B * w.H * w.K * (w.d_v + 1) / 1e6),
+                   "kernel_family": "fp32 cuda-core",
+                   "parallelism": f"replicas x{ws} (independent sequences per rank)"},
+        "roofline": roofline, "path_roofline": path_roofline,
+        "kernels": {k: {"launches": len(v), "total_ms": round(sum(v), 4)}
+                    for k, v in per_kernel.items()},
+        "gpu_launches": len(launches), "launches_per_step": len(launches) / steps,
+        "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+    }
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, ws, rank):
     if rank != 0:
@@ -404,6 +578,8 @@ def run_reference(args, ws, rank):
     steps = args.steps if args.steps > 0 else 5
     warm = max(args.warmup, 3)
     per_step_budget = min(5.0, 150.0 / (steps + warm))
+    if is_decode(w):
+        return run_reference_decode(args, w, ws, steps, warm, per_step_budget)
     rate, cores, desc, n = oracle_sample(w, per_step_budget)
     import oracle
     host = W.to_numpy(W.make_inputs(W.scaled(w, B=1)))
@@ -433,13 +609,36 @@ def run_reference(args, ws, rank):
     }
 
 
+def run_reference_decode(args, w, ws, steps, warm, per_step_budget):
+    for _ in range(warm):
+        oracle_decode_sample(w, per_step_budget / 4)
+    t0 = time.perf_counter()
+    n_all = 0
+    for _ in range(steps):
+        _, cores, desc, n = oracle_decode_sample(w, per_step_budget)
+        n_all += n
+    dt = time.perf_counter() - t0
+    value = w.B * n_all / dt
+    return {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "variant": "decode", "B": w.B, "H": w.H, "d_r": w.d_r,
+                   "K": w.K, "d_v": w.d_v},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 3 s of work)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[x.name for x in W.ALL_WORKLOADS])
+                    choices=[x.name for x in W.ALL_WORKLOADS + (W.DECODE,)])
     ap.add_argument("--impl", default="gma", choices=["gma", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline sample")
@@ -456,7 +655,8 @@ def main():
         from linear_latent_routing_gb300 import build
         build.build()
         ws, rank, local = dist_setup("nccl")
-        out = run_gma(args, ws, rank, local)
+        w = W.by_name(args.workload)
+        out = (run_decode if is_decode(w) else run_gma)(args, ws, rank, local)
     if out is not None:
         print(json.dumps(out), flush=True)
     if int(os.environ.get("WORLD_SIZE", "1")) > 1:

@@ -86,6 +86,7 @@ typedef struct {
 #define GMA_VARIANT_RESPONSIBILITIES 0
 #define GMA_VARIANT_BIDIRECTIONAL 1
 #define GMA_VARIANT_CAUSAL 2
+#define GMA_VARIANT_DECODE 3
 
 /* Bytes of device workspace one call of `variant` with `shape` needs (0 for an invalid shape).
  * The workspace must be 256-byte aligned.  Its first 256 bytes hold the error word that
@@ -117,6 +118,20 @@ gma_status_t gma_forward_causal(const gma_shape_t *shape, const void *QX, const 
                                 const float *prior_logits, void *O, void *workspace,
                                 size_t workspace_bytes, gma_stream_t stream);
 
+/* One autoregressive decode step of causal GMA (Méthodologie §3: the prefix memory V~ and its
+ * normaliser Z grow by one token, which then reads them), for every (b, h) slice at once:
+ *   gamma_K = p(z | kx),   S[k][c] += gamma_K[k] v[c] (c < d_v),   S[k][d_v] += gamma_K[k],
+ *   gamma_Q = p(z | qx),   o[c] = (gamma_Q . S[:, c]) / (gamma_Q . S[:, d_v] + eps).
+ * shape->N must be 1 (one new token per slice).  qx, kx [B][H][d_r] and v [B][H][d_v] in
+ * shape->dtype; state [B][H][K][d_v + 1] fp32, caller-owned, read and updated in place (all zeros
+ * for an empty prefix; after N steps it equals the causal forward's memory after N tokens);
+ * o [B][H][d_v] in shape->dtype (fp32 with GMA_FLAG_OUT_F32).  fp32 arithmetic on the CUDA cores
+ * for every shape; the workspace is gma_workspace_size(shape, GMA_VARIANT_DECODE) bytes. */
+gma_status_t gma_decode_step(const gma_shape_t *shape, const void *qx, const void *kx, const void *v,
+                             const float *mu, const float *raw_var, const float *prior_logits,
+                             float *state, void *o, void *workspace, size_t workspace_bytes,
+                             gma_stream_t stream);
+
 /* Causal GMA for callers that cannot allocate device memory.  The page has no counterpart to
  * this entry point: it exists for callers such as allocator or memory-pool callbacks, plugins
  * whose host application owns every device allocation, or loops that must not call cudaMalloc
@@ -145,7 +160,8 @@ gma_status_t gma_forward_causal_noalloc(const gma_shape_t *shape, const void *QX
 gma_status_t gma_check_workspace(const void *workspace, gma_stream_t stream);
 
 /* Which kernel family a call with this shape and variant runs: 0 = fp32 CUDA-core kernels,
- * 1 = tcgen05 tensor-core kernels, -1 = the shape is invalid. */
+ * 1 = tcgen05 tensor-core kernels, -1 = the shape is invalid.  The decode step (N == 1) always
+ * runs on the CUDA cores. */
 int gma_kernel_family(const gma_shape_t *shape, int variant);
 
 /* Static description of a status code. */

@@ -79,6 +79,10 @@ extern "C" {
 
 size_t gma_workspace_size(const gma_shape_t *s, int variant)
 {
+    if (variant == GMA_VARIANT_DECODE) {
+        if (validate_shape(s, GMA_VARIANT_CAUSAL) != GMA_OK || s->N != 1) return 0;
+        return decode_workspace_size(*s);
+    }
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return 0;
     if (validate_shape(s, variant) != GMA_OK) return 0;
     return family_of(*s, variant) == 1 ? tc_workspace_size(*s, variant)
@@ -87,6 +91,8 @@ size_t gma_workspace_size(const gma_shape_t *s, int variant)
 
 int gma_kernel_family(const gma_shape_t *s, int variant)
 {
+    if (variant == GMA_VARIANT_DECODE)
+        return (validate_shape(s, GMA_VARIANT_CAUSAL) == GMA_OK && s->N == 1) ? 0 : -1;
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return -1;
     if (validate_shape(s, variant) != GMA_OK) return -1;
     return family_of(*s, variant);
@@ -123,6 +129,22 @@ gma_status_t gma_forward_causal(const gma_shape_t *s, const void *QX, const void
                                 gma_stream_t stream)
 {
     return forward_common(true, s, QX, KX, V, mu, raw, logits, O, ws, ws_bytes, stream);
+}
+
+gma_status_t gma_decode_step(const gma_shape_t *s, const void *qx, const void *kx, const void *v,
+                             const float *mu, const float *raw, const float *logits, float *state,
+                             void *o, void *ws, size_t ws_bytes, gma_stream_t stream)
+{
+    gma_status_t r = validate_shape(s, GMA_VARIANT_CAUSAL);
+    if (r != GMA_OK) return r;
+    if (s->N != 1) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {qx, kx, v, mu, raw, logits, state, o};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return GMA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    r = begin_call(s, GMA_VARIANT_DECODE, ws, ws_bytes, st);
+    if (r != GMA_OK) return r;
+    return decode_step(*s, qx, kx, v, mu, raw, logits, state, o, ws, st);
 }
 
 gma_status_t gma_check_workspace(const void *ws, gma_stream_t stream)

@@ -21,47 +21,42 @@ namespace {
 constexpr int SEG = 64;        // tokens per segment
 constexpr int KT = 32;         // component tile for the staged dot products
 constexpr int THREADS = 256;
+constexpr int PARAM_THREADS = 256;
 
 // ---------------------------------------------------------------- reparametrisation
 // Per head h: inv_var[h][k][d] = 1 / (softplus(raw) + floor);
 //             cst[h][k]        = log pi_k - 1/2 sum_d log sigma^2_kd,  log pi = log softmax.
+// One warp per component row (grid H x ceil(K / 8)); every warp first reduces its head's
+// prior logits to their log-sum-exp (K <= 1024: at most 32 values per lane).
 __global__ void simt_params_kernel(const float *__restrict__ raw, const float *__restrict__ logits,
                                    float *__restrict__ inv_var, float *__restrict__ cst, int K,
                                    int d_r, float floor_)
 {
-    const int h = blockIdx.x;
-    const float *rh = raw + (size_t)h * K * d_r;
+    const int h = blockIdx.x, lane = threadIdx.x & 31;
+    const int k = blockIdx.y * (PARAM_THREADS / 32) + (threadIdx.x >> 5);
     const float *lh = logits + (size_t)h * K;
-    __shared__ float red[THREADS];
     float m = -INFINITY;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) m = fmaxf(m, lh[k]);
-    red[threadIdx.x] = m;
-    __syncthreads();
-    for (int o = blockDim.x / 2; o > 0; o >>= 1) {
-        if (threadIdx.x < o) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + o]);
-        __syncthreads();
-    }
-    m = red[0];
-    __syncthreads();
+    for (int j = lane; j < K; j += 32) m = fmaxf(m, lh[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float s = 0.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) s += expf(lh[k] - m);
-    red[threadIdx.x] = s;
-    __syncthreads();
-    for (int o = blockDim.x / 2; o > 0; o >>= 1) {
-        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
-        __syncthreads();
+    for (int j = lane; j < K; j += 32) s += expf(lh[j] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (k >= K) return;
+    const float lse = m + logf(s);
+    const float *rk = raw + ((size_t)h * K + k) * d_r;
+    float *ik = inv_var + ((size_t)h * K + k) * d_r;
+    float logdet = 0.f;
+    for (int d = lane; d < d_r; d += 32) {
+        const float r = rk[d];
+        const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
+        ik[d] = 1.0f / var;
+        logdet += logf(var);
     }
-    const float lse = m + logf(red[0]);
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        float logdet = 0.f;
-        for (int d = 0; d < d_r; ++d) {
-            const float r = rh[(size_t)k * d_r + d];
-            const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
-            inv_var[((size_t)h * K + k) * d_r + d] = 1.0f / var;
-            logdet += logf(var);
-        }
-        cst[(size_t)h * K + k] = (lh[k] - lse) - 0.5f * logdet;
-    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) logdet += __shfl_xor_sync(0xffffffffu, logdet, o);
+    if (lane == 0) cst[(size_t)h * K + k] = (lh[k] - lse) - 0.5f * logdet;
 }
 
 // ---------------------------------------------------------------- responsibilities
@@ -283,7 +278,7 @@ gma_status_t forward_typed(const gma_shape_t &s, bool causal, const Tin *QX, con
     float *iv = (float *)(ws + L.inv_var), *cst = (float *)(ws + L.cst);
     float *gq = (float *)(ws + L.gq), *gk = (float *)(ws + L.gk), *agg = (float *)(ws + L.agg);
     const long long rows = (long long)s.B * s.H * s.N;
-    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<s.H, THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
+    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
     gma_status_t r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
     if (r != GMA_OK) return r;
     r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, s.N, s.K, rows, st);
@@ -303,6 +298,14 @@ gma_status_t forward_typed(const gma_shape_t &s, bool causal, const Tin *QX, con
 
 size_t simt_workspace_size(const gma_shape_t &s, int variant) { return simt_layout(s, variant).total; }
 
+gma_status_t simt_params(const gma_shape_t &s, const float *raw, const float *logits, float *inv_var,
+                         float *cst, cudaStream_t st)
+{
+    GMA_LAUNCH(KID_SIMT_PARAMS, st,
+               (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, inv_var, cst, s.K, s.d_r, s.var_floor)));
+    return GMA_OK;
+}
+
 gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
                                    const float *raw, const float *logits, void *gamma, void *ws,
                                    cudaStream_t st)
@@ -310,7 +313,7 @@ gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const fl
     const SimtLayout L = simt_layout(s, GMA_VARIANT_RESPONSIBILITIES);
     char *w = (char *)ws;
     float *iv = (float *)(w + L.inv_var), *cst = (float *)(w + L.cst);
-    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<s.H, THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
+    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
     const long long rows = (long long)s.B * s.H * s.N;
     const bool out32 = (s.flags & GMA_FLAG_OUT_F32) || s.dtype == GMA_F32;
     if (s.dtype == GMA_F32)

@@ -42,6 +42,7 @@ const char *kernel_name(int id)
     case KID_TC_CAUSAL_AGG: return "tc_causal_segment_memory";
     case KID_TC_CAUSAL_SCAN: return "tc_causal_segment_scan";
     case KID_TC_CAUSAL_OUT: return "tc_causal_chunked";
+    case KID_DECODE: return "decode_step";
     }
     return "unknown";
 }

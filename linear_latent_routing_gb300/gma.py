@@ -16,11 +16,12 @@ GMA_OK = 0
 STATUS_NAMES = {0: "GMA_OK", 1: "GMA_ERR_INVALID_ARG", 2: "GMA_ERR_UNSUPPORTED_SHAPE",
                 3: "GMA_ERR_RANGE", 4: "GMA_ERR_WORKSPACE", 5: "GMA_ERR_CUDA",
                 6: "GMA_ERR_TIMEOUT", 7: "GMA_ERR_NO_DEVICE"}
+globals().update({name: code for code, name in STATUS_NAMES.items()})
 GMA_F32, GMA_BF16 = 0, 1
 GMA_FLAG_SIMT = 0x1
 GMA_FLAG_OUT_F32 = 0x2
 GMA_FLAG_RECOMPUTE_KEYS = 0x4
-GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL = 0, 1, 2
+GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL, GMA_VARIANT_DECODE = 0, 1, 2, 3
 
 
 class gma_shape_t(ctypes.Structure):
@@ -51,6 +52,8 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         fn.restype = ctypes.c_int
+    lib.gma_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.gma_decode_step.restype = ctypes.c_int
     lib.gma_forward_causal_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.gma_forward_causal_noalloc.restype = ctypes.c_int
     lib.gma_check_workspace.argtypes = [vp, vp]
@@ -107,6 +110,12 @@ def gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, workspace
                        workspace_bytes, stream):
     return int(_lib.gma_forward_causal(ctypes.byref(shape), QX, KX, V, mu, raw_var,
                                        prior_logits, O, workspace, int(workspace_bytes), stream))
+
+
+def gma_decode_step(shape, qx, kx, v, mu, raw_var, prior_logits, state, o, workspace,
+                    workspace_bytes, stream):
+    return int(_lib.gma_decode_step(ctypes.byref(shape), qx, kx, v, mu, raw_var, prior_logits,
+                                    state, o, workspace, int(workspace_bytes), stream))
 
 
 GMA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -253,3 +262,40 @@ def responsibilities(X, mu, raw_var, prior_logits, var_floor=1e-3, flags=0, out=
         if r != GMA_OK:
             raise GmaError(r, "gma_check_workspace")
     return out
+
+
+def decode_step(qx, kx, v, mu, raw_var, prior_logits, state, eps=1e-6, var_floor=1e-3, flags=0,
+                out=None, workspace=None, stream=None, check=False):
+    """One autoregressive decode step on torch CUDA tensors; returns o [B, H, d_v].
+
+    qx, kx [B, H, d_r] and v [B, H, d_v] share one dtype (bf16 or fp32); state [B, H, K, d_v + 1]
+    fp32 is updated in place; mu, raw_var [H, K, d_r] and prior_logits [H, K] are fp32.
+    """
+    torch = _torch()
+    for t, n in ((qx, "qx"), (kx, "kx"), (v, "v")):
+        _check(t, n, qx.dtype)
+    for t, n in ((mu, "mu"), (raw_var, "raw_var"), (prior_logits, "prior_logits"), (state, "state")):
+        _check(t, n, torch.float32)
+    B, H, d_r = qx.shape
+    d_v = v.shape[-1]
+    K = mu.shape[1]
+    if kx.shape != qx.shape or v.shape[:2] != qx.shape[:2] or state.shape != (B, H, K, d_v + 1):
+        raise ValueError("qx, kx [B, H, d_r], v [B, H, d_v] and state [B, H, K, d_v + 1] must agree")
+    shape = make_shape(B, H, 1, d_r, K, d_v, _dtype_code(qx), eps, var_floor, flags)
+    if out is None:
+        odt = torch.float32 if (flags & GMA_FLAG_OUT_F32) else qx.dtype
+        out = torch.empty(B, H, d_v, dtype=odt, device=qx.device)
+    if workspace is None:
+        workspace = workspace_for(shape, GMA_VARIANT_DECODE, qx.device)
+    st = _stream_handle(stream)
+    r = gma_decode_step(shape, qx.data_ptr(), kx.data_ptr(), v.data_ptr(), mu.data_ptr(),
+                        raw_var.data_ptr(), prior_logits.data_ptr(), state.data_ptr(), out.data_ptr(),
+                        workspace.data_ptr(), workspace.numel(), st)
+    if r != GMA_OK:
+        raise GmaError(r, "gma_decode_step")
+    if check:
+        r = gma_check_workspace(workspace.data_ptr(), st)
+        if r != GMA_OK:
+            raise GmaError(r, "gma_check_workspace")
+    return out
+

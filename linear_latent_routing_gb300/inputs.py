@@ -62,11 +62,16 @@ K_SWEEP = tuple(_ws(f"causal_bf16_b2h16_n16384_dr64_k{k}_dv128", True, 2, 16, 16
 N_SWEEP = tuple(_ws(f"causal_bf16_b2h16_n{n}_dr64_k64_dv128", True, 2, 16, n, 64, 64, 128,
                     seed=4) for n in (4096, 8192, 16384, 32768, 65536, 131072))
 
+# Autoregressive decoding with the long-context head shape: B sequences x H heads each take one
+# new token per step.  N is the number of steps drawn (one row of Q_X, K_X and V per step); the
+# per-slice state is K x (d_v + 1) fp32, 135 MB for the whole batch (above the 129 MB L2).
+DECODE = _ws("decode_bf16_b128h16_dr64_k128_dv128", True, 128, 16, 8, 64, 128, 128, seed=5)
+
 ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP
 
 
 def by_name(name: str) -> Workload:
-    for w in ALL_WORKLOADS:
+    for w in ALL_WORKLOADS + (DECODE,):
         if w.name == name:
             return w
     raise KeyError(name)
@@ -103,3 +108,15 @@ def make_inputs(w: Workload):
 def to_numpy(inputs):
     """fp32 numpy views of an input dict (bf16 widens to fp32 exactly)."""
     return {k: v.float().numpy() for k, v in inputs.items()}
+
+
+def make_decode_state(w: Workload, scale: float = 1.0, seed: int = 1000):
+    """A non-zero starting decode state [B, H, K, d_v + 1] fp32 on the CPU, drawn from its own
+    generator: memory columns ~ N(0, scale), the last (normaliser) column ~ U(0.5, 1.5) * scale,
+    positive like any sum of responsibilities."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed) + int(seed))
+    S = torch.randn(w.B, w.H, w.K, w.d_v + 1, generator=g, dtype=torch.float32) * scale
+    S[..., w.d_v] = (torch.rand(w.B, w.H, w.K, generator=g, dtype=torch.float32) + 0.5) * scale
+    return S
+

@@ -117,3 +117,17 @@ def test_no_device_is_reported_without_a_gpu(g):
     fake = 1 << 20
     r = g.gma_forward_causal(s, *([fake] * 7), fake, ws_n, None)
     assert r == 7
+
+
+def test_decode_step_validation(g):
+    """gma_decode_step takes N == 1 only and refuses null pointers before touching the device;
+    its workspace and kernel family follow the decode variant."""
+    s1 = _shape(g, N=1)
+    s2 = _shape(g, N=2)
+    assert g.gma_workspace_size(s1, g.GMA_VARIANT_DECODE) > 0
+    assert g.gma_workspace_size(s2, g.GMA_VARIANT_DECODE) == 0
+    assert g.gma_kernel_family(s1, g.GMA_VARIANT_DECODE) == 0
+    assert g.gma_kernel_family(s2, g.GMA_VARIANT_DECODE) == -1
+    assert g.gma_decode_step(s2, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
+    assert g.gma_decode_step(s1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
+    assert g.gma_decode_step(_shape(g, N=1, K=0), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) != g.GMA_OK
