@@ -65,7 +65,7 @@ inline bool valid_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128;
 enum KernelId {
     KID_SIMT_PARAMS = 1, KID_SIMT_RESP, KID_SIMT_STATE, KID_SIMT_SCAN, KID_SIMT_OUT,
     KID_TC_PARAMS = 16, KID_TC_RESP, KID_TC_BIDIR_WRITE, KID_TC_BIDIR_READ, KID_TC_CAUSAL_AGG,
-    KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_DECODE = 32, KID_COUNT
+    KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_DECODE = 32, KID_DECODE_PARAMS, KID_COUNT
 };
 const char *kernel_name(int id);
 void timing_begin(cudaStream_t st, int kernel_id);
@@ -81,8 +81,6 @@ gma_status_t simt_forward(const gma_shape_t &s, bool causal, const void *QX, con
                           void *O, void *ws, cudaStream_t st);
 
 // Per-head 1 / sigma^2 [H][K][d_r] and log pi - 1/2 sum log sigma^2 [H][K] (fp32, direct form).
-gma_status_t simt_params(const gma_shape_t &s, const float *raw, const float *logits, float *inv_var,
-                         float *cst, cudaStream_t st);
 
 // --------------------------------------------------------------- decode step
 size_t decode_workspace_size(const gma_shape_t &s);

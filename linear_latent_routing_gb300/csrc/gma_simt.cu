@@ -35,6 +35,11 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
     const int h = blockIdx.x, lane = threadIdx.x & 31;
     const int k = blockIdx.y * (PARAM_THREADS / 32) + (threadIdx.x >> 5);
     const float *lh = logits + (size_t)h * K;
+    const int kr = k < K ? k : K - 1;
+    const float *rk = raw + ((size_t)h * K + kr) * d_r;
+    float rv[4];   // d_r <= 128: this lane's raw variances, loaded before the reductions
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rv[i] = lane + 32 * i < d_r ? rk[lane + 32 * i] : 0.f;
     float m = -INFINITY;
     for (int j = lane; j < K; j += 32) m = fmaxf(m, lh[j]);
 #pragma unroll
@@ -45,14 +50,17 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (k >= K) return;
     const float lse = m + logf(s);
-    const float *rk = raw + ((size_t)h * K + k) * d_r;
     float *ik = inv_var + ((size_t)h * K + k) * d_r;
     float logdet = 0.f;
-    for (int d = lane; d < d_r; d += 32) {
-        const float r = rk[d];
-        const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
-        ik[d] = 1.0f / var;
-        logdet += logf(var);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int d = lane + 32 * i;
+        if (d < d_r) {
+            const float r = rv[i];
+            const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
+            ik[d] = 1.0f / var;
+            logdet += logf(var);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) logdet += __shfl_xor_sync(0xffffffffu, logdet, o);
@@ -297,14 +305,6 @@ gma_status_t forward_typed(const gma_shape_t &s, bool causal, const Tin *QX, con
 }  // namespace
 
 size_t simt_workspace_size(const gma_shape_t &s, int variant) { return simt_layout(s, variant).total; }
-
-gma_status_t simt_params(const gma_shape_t &s, const float *raw, const float *logits, float *inv_var,
-                         float *cst, cudaStream_t st)
-{
-    GMA_LAUNCH(KID_SIMT_PARAMS, st,
-               (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, inv_var, cst, s.K, s.d_r, s.var_floor)));
-    return GMA_OK;
-}
 
 gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
                                    const float *raw, const float *logits, void *gamma, void *ws,

@@ -62,6 +62,11 @@ CASES = [
     W.scaled(W.DECODE, B=1, H=2, N=4, d_r=128, K=1024, d_v=128),
     W.scaled(W.DECODE, B=2, H=1, N=5, d_r=16, K=1, d_v=16),
     W.scaled(W.DECODE, B=1, H=3, N=5, d_r=32, K=100, d_v=32, dtype="f32"),
+    # K not a multiple of 4: rows off 16-byte boundaries, the plain kernel (5 chunks, ragged tail)
+    W.scaled(W.DECODE, B=2, H=2, N=3, K=130),
+    W.scaled(W.DECODE, B=1, H=2, N=3, d_r=16, K=301, d_v=16),
+    # more slices than SMs: each persistent CTA streams several slices' chunks through its ring
+    W.scaled(W.DECODE, B=25, H=16, N=3, K=256),
 ]
 
 
