@@ -103,7 +103,7 @@ def decode_bytes(w):
     return w.B * w.H * (2 * 4 * w.K * (w.d_v + 1) + esz * (2 * w.d_r + 2 * w.d_v))
 
 
-def traffic_per_launch(kernel, w):
+def traffic_per_launch(kernel, w, units=None):
     """DRAM bytes (read + write) of one launch of `kernel` on workload `w`, from the committed
     ncu summary profiles/dram_traffic.json (captured per token-head on a smaller case of the same
     kernel, scaled by the units one launch processes); None when no capture exists or any of the
@@ -125,7 +125,7 @@ def traffic_per_launch(kernel, w):
         return None
     if rec.get("workload_shape") != [w.d_r, w.K, w.d_v, w.dtype, w.causal]:
         return None
-    return rec["dram_bytes_per_token_head"] * w.token_heads
+    return rec["dram_bytes_per_token_head"] * (w.token_heads if units is None else units)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -510,7 +510,7 @@ def run_decode(args, ws, rank, local):
     achieved = decode_bytes(w) / (avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "decode_step", "achieved": round(achieved, 3),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": traffic_per_launch("decode_step", w),
+                "traffic": traffic_per_launch("decode_step", w, units=w.B * w.H),
                 "avg_launch_us": round(avg_ms * 1e3, 3),
                 "launches": len(per_kernel["decode_step"]),
                 "peak_source": f"hbm_gbs of {pk['source']}"}

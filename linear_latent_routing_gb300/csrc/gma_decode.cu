@@ -130,49 +130,60 @@ __host__ __device__ inline int logit_parts(int K, int n, int d_r, int ud)
     return P;
 }
 
-// `base` points at head h's parameters, in global memory (GLOBAL) or a shared-memory copy.
-// Rows of `base` are `ldk` components apart; cst points at head h's constants c_k.
+// Sums for item `it` (component it / P, dimensions (it % P) d_r / P onward) of both rows,
+// merged over the P lanes of the component; every lane of the warp must call it.  `base` points
+// at head h's parameters (rows ldk components apart), in global memory (GLOBAL) or a
+// shared-memory copy.
+template <bool GLOBAL>
+__device__ __forceinline__ void item_sums(const float2 *base, int ldk, const float *xq, const float *xk, int K,
+                                          int d_r, int P, int it, float &sq, float &eq, float &sk, float &ek)
+{
+    constexpr int UD = GLOBAL ? 16 : 8;   // loads in flight per batch (d_r >= 16 is a multiple)
+    const int nd = d_r / P;               // a multiple of UD
+    const int k = min(it / P, K - 1), d_lo = (it % P) * nd;
+    sq = eq = sk = ek = 0.f;
+    for (int d0 = d_lo; d0 < d_lo + nd; d0 += UD) {
+        const float2 *pp = base + (size_t)d0 * ldk + k;
+        float2 pr[UD];
+#pragma unroll
+        for (int u = 0; u < UD; ++u) pr[u] = GLOBAL ? __ldg(pp + (size_t)u * ldk) : pp[(size_t)u * ldk];
+#pragma unroll
+        for (int u4 = 0; u4 < UD; u4 += 4) {
+            const float4 q4 = *reinterpret_cast<const float4 *>(xq + d0 + u4);
+            const float4 k4 = *reinterpret_cast<const float4 *>(xk + d0 + u4);
+            const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+            float bq = 0.f, bk = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 p = pr[u4 + u];
+                const float dq = qv[u] - p.x, dk = kv[u] - p.x;
+                bq = fmaf(__fmul_rn(dq, dq), p.y, bq);
+                bk = fmaf(__fmul_rn(dk, dk), p.y, bk);
+            }
+            add_pair(sq, eq, bq);
+            add_pair(sk, ek, bk);
+        }
+    }
+    for (int o = 1; o < P; o <<= 1) {
+        merge_pair(sq, eq, o);
+        merge_pair(sk, ek, o);
+    }
+}
+
 template <bool GLOBAL>
 __device__ __forceinline__ void logit_pairs(const float2 *base, int ldk, const float *cst, const float *xq,
                                             const float *xk, float *lq_a, float *lq_b, float *lk_a, float *lk_b,
                                             int K, int d_r, int gt, int n)
 {
-    constexpr int UD = GLOBAL ? 16 : 8;   // loads in flight per batch (d_r >= 16 is a multiple)
-    const int P = logit_parts(K, n, d_r, UD);
-    const int nd = d_r / P;   // a multiple of UD
+    const int P = logit_parts(K, n, d_r, GLOBAL ? 16 : 8);
     const int items = K * P, lane = gt & 31;
     // every lane of a warp runs the same iterations (the shuffles need all 32)
     for (int it0 = gt - lane; it0 < items; it0 += n) {
         const int it = it0 + lane;
-        const int k = min(it / P, K - 1), d_lo = (it % P) * nd;
-        float sq = 0.f, eq = 0.f, sk = 0.f, ek = 0.f;
-        for (int d0 = d_lo; d0 < d_lo + nd; d0 += UD) {
-            const float2 *pp = base + (size_t)d0 * ldk + k;
-            float2 pr[UD];
-#pragma unroll
-            for (int u = 0; u < UD; ++u) pr[u] = GLOBAL ? __ldg(pp + (size_t)u * ldk) : pp[(size_t)u * ldk];
-#pragma unroll
-            for (int u4 = 0; u4 < UD; u4 += 4) {
-                const float4 q4 = *reinterpret_cast<const float4 *>(xq + d0 + u4);
-                const float4 k4 = *reinterpret_cast<const float4 *>(xk + d0 + u4);
-                const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-                float bq = 0.f, bk = 0.f;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 p = pr[u4 + u];
-                    const float dq = qv[u] - p.x, dk = kv[u] - p.x;
-                    bq = fmaf(__fmul_rn(dq, dq), p.y, bq);
-                    bk = fmaf(__fmul_rn(dk, dk), p.y, bk);
-                }
-                add_pair(sq, eq, bq);
-                add_pair(sk, ek, bk);
-            }
-        }
-        for (int o = 1; o < P; o <<= 1) {
-            merge_pair(sq, eq, o);
-            merge_pair(sk, ek, o);
-        }
+        float sq, eq, sk, ek;
+        item_sums<GLOBAL>(base, ldk, xq, xk, K, d_r, P, it, sq, eq, sk, ek);
         if (it < items && it % P == 0) {
+            const int k = it / P;
             const float c = cst[k];
             lq_a[k] = -0.5f * sq;
             lq_b[k] = c - 0.5f * eq;
@@ -299,6 +310,71 @@ __device__ __forceinline__ void softmax_pairs2(float *qa, const float *qb, float
     }
 }
 
+// Both rows' responsibilities over a group of n threads (barrier `id`): gq[k] = p(z = k | q_x),
+// gk[k] = p(z = k | k_x).  When every component's P lanes fit in the group at once, each lane
+// keeps its logit pair in registers and the softmax needs two barriers; otherwise the pairs go
+// through shared memory (ga, gb) and softmax_pairs2.  red holds 4 n / 32 floats.  The caller
+// synchronises the group before reading gq, gk.
+template <bool GLOBAL>
+__device__ __forceinline__ void responsibilities(const float2 *base, int ldk, const float *cst, const float *xq,
+                                                 const float *xk, float *gq, float *qb, float *gk, float *kb,
+                                                 float *red, int K, int d_r, int gt, int n, int id)
+{
+    const int P = logit_parts(K, n, d_r, GLOBAL ? 16 : 8);
+    if (K * P > n) {
+        logit_pairs<GLOBAL>(base, ldk, cst, xq, xk, gq, qb, gk, kb, K, d_r, gt, n);
+        group_sync(id, n);
+        softmax_pairs2(gq, qb, gk, kb, K, red, gt, n, id);
+        return;
+    }
+    const int nw = n / 32, lane = gt & 31, w = gt >> 5, items = K * P;
+    const bool own = gt < items && gt % P == 0;
+    float sq = 0.f, eq = 0.f, sk = 0.f, ek = 0.f;
+    if (gt - lane < items) item_sums<GLOBAL>(base, ldk, xq, xk, K, d_r, P, gt, sq, eq, sk, ek);
+    const int k = min(gt / P, K - 1);
+    const float c = own ? cst[k] : 0.f;
+    const float aq = -0.5f * sq, bq = c - 0.5f * eq, ak = -0.5f * sk, bk = c - 0.5f * ek;
+    float mq = own ? aq + bq : -INFINITY, mk = own ? ak + bk : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+    }
+    if (lane == 0) {
+        red[w] = mq;
+        red[nw + w] = mk;
+    }
+    group_sync(id, n);
+    mq = red[0];
+    mk = red[nw];
+    for (int q = 1; q < nw; ++q) {
+        mq = fmaxf(mq, red[q]);
+        mk = fmaxf(mk, red[nw + q]);
+    }
+    const float xq_ = own ? expf((aq - mq) + bq) : 0.f, xk_ = own ? expf((ak - mk) + bk) : 0.f;
+    float s_q = xq_, s_k = xk_;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s_q += __shfl_xor_sync(0xffffffffu, s_q, o);
+        s_k += __shfl_xor_sync(0xffffffffu, s_k, o);
+    }
+    if (lane == 0) {
+        red[2 * nw + w] = s_q;
+        red[3 * nw + w] = s_k;
+    }
+    group_sync(id, n);
+    s_q = 0.f;
+    s_k = 0.f;
+    for (int q = 0; q < nw; ++q) {
+        s_q += red[2 * nw + q];
+        s_k += red[3 * nw + q];
+    }
+    if (own) {
+        gq[k] = xq_ * (1.f / s_q);
+        gk[k] = xk_ * (1.f / s_k);
+    }
+}
+
 // One chunk's rows for this thread's column: S[r][col] += gk[r] add, acc += gq[r] S[r][col]; rows
 // r = grp, grp + G, ...; U rows' loads are issued before they are used, and two accumulators
 // halve the dependent chain.  With G == 1 the rows are consecutive and gk, gq (16-byte aligned
@@ -307,7 +383,7 @@ template <int NE, int G>
 __device__ __forceinline__ void update_rows(float *st, const float *gk, const float *gq, int rows, int grp, int col,
                                             float add, float &acc)
 {
-    constexpr int U = 16;
+    constexpr int U = 8;
     float acc2 = 0.f;
     int r = grp;
     for (; r + (U - 1) * G < rows; r += U * G) {
@@ -366,7 +442,7 @@ __host__ __device__ inline PSmem persist_smem(int DV, int K, int d_r)
     L.gbuf = take(2 * L.gslot);
     L.part = take(4 * ST);
     L.red_s = take(4 * 32);
-    L.red_l = take(4 * 2 * (LT / 32));
+    L.red_l = take(4 * 4 * (LT / 32));
     L.bars = take(8 * (2 * MAX_STAGES + 4));
     L.flag = take(16);
     // a copy of one head's parameters, (mu, 1 / sigma^2) [d_r][K], when K d_r <= PAR_SMEM_MAX
@@ -495,12 +571,11 @@ __global__ void __launch_bounds__(WT, 1) decode_persistent_kernel(
             }
             named_bar_sync(BAR_LOGIT, LT);
             if (par)
-                logit_pairs<false>(par, K, cst + (size_t)h * K, xq, xk, qa, qb, ka, kb, K, d_r, lt, LT);
+                responsibilities<false>(par, K, cst + (size_t)h * K, xq, xk, qa, qb, ka, kb, red, K, d_r, lt, LT,
+                                        BAR_LOGIT);
             else
-                logit_pairs<true>(mw + (size_t)h * d_r * K, K, cst + (size_t)h * K, xq, xk, qa, qb, ka, kb, K, d_r,
-                                  lt, LT);
-            named_bar_sync(BAR_LOGIT, LT);
-            softmax_pairs2(qa, qb, ka, kb, K, red, lt, LT, BAR_LOGIT);
+                responsibilities<true>(mw + (size_t)h * d_r * K, K, cst + (size_t)h * K, xq, xk, qa, qb, ka, kb, red,
+                                       K, d_r, lt, LT, BAR_LOGIT);
             named_bar_sync(BAR_LOGIT, LT);
             if (lt == 0) mbar_arrive(gfull + j);
         }
@@ -540,16 +615,17 @@ __global__ void __launch_bounds__(WT, 1) decode_persistent_kernel(
                 mbar_arrive(done + s);
             }
             if (failed) break;
-            part[t] = acc;
+            if (G > 1) part[t] = acc;
+            // (its barriers also mean every state thread is done with slot j: it is free again;
+            // part[] and red[] are next written after the next slice's chunk barriers)
             const float den = group_sum(zacc, red, t, ST, BAR_STATE);
+            if (t == 0) mbar_arrive(gempty + j);
             if (t < DV) {
-                float num = 0.f;
+                float num = acc;
 #pragma unroll
-                for (int q = 0; q < G; ++q) num += part[q * DV + t];
+                for (int q = 1; q < G; ++q) num += part[q * DV + t];
                 from_f(o[(size_t)bh * DV + t], num / (den + eps));
             }
-            named_bar_sync(BAR_STATE, ST);   // slot j and part[] are free again
-            if (t == 0) mbar_arrive(gempty + j);
         }
     }
     __syncthreads();
@@ -583,9 +659,8 @@ __global__ void __launch_bounds__(PT) decode_plain_kernel(const Tin *__restrict_
     for (int c = t; c < DV; c += PT) vv[c] = to_f(v[(size_t)bh * DV + c]);
     grid_dependency_wait();   // the parameters come from the kernel before
     __syncthreads();
-    logit_pairs<true>(mw + (size_t)h * d_r * K, K, cst + (size_t)h * K, xq, xk, qa, qb, ka, kb, K, d_r, t, PT);
-    __syncthreads();
-    softmax_pairs2(qa, qb, ka, kb, K, red, t, PT, 0);
+    responsibilities<true>(mw + (size_t)h * d_r * K, K, cst + (size_t)h * K, xq, xk, qa, qb, ka, kb, red, K, d_r,
+                           t, PT, 0);
     __syncthreads();
     const int col = t % DV, grp = t / DV;
     const float add = vv[col];
