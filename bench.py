@@ -54,13 +54,13 @@ def peaks():
 def path_bytes(w):
     """Algorithmic bytes of one step: Q_X, K_X, V read once and O written once."""
     esz = 2 if w.dtype == "bf16" else 4
-    return w.token_heads * esz * (2 * w.d_r + 2 * w.d_v)
+    return (w.token_heads + w.key_heads) * esz * (w.d_r + w.d_v)
 
 
 def path_flops(w):
     """Algorithmic flops of one step: the two [x^2, x] contractions (8 d_r K) plus the write and
     read contractions including the normaliser (4 K (d_v + 1)), per token-head."""
-    return w.token_heads * (8 * w.d_r * w.K + 4 * w.K * (w.d_v + 1))
+    return (w.token_heads + w.key_heads) * (4 * w.d_r * w.K + 2 * w.K * (w.d_v + 1))
 
 
 def kernel_work(w, name):
@@ -73,10 +73,10 @@ def kernel_work(w, name):
         # the output pass reads Q_X and V and writes O (K_X is read by the segment pass; the
         # stored Gamma_K it also reads is not algorithmic traffic)
         return "hbm", th * esz * (w.d_r + 2 * w.d_v), "GB/s"
-    if name == "tc_causal_segment_memory":
-        return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
+    if name == "tc_causal_segment_memory":   # the write pass (key side)
+        return "hbm", w.key_heads * esz * (w.d_r + w.d_v), "GB/s"
     if name == "tc_bidir_write":
-        return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
+        return "hbm", w.key_heads * esz * (w.d_r + w.d_v), "GB/s"
     if name == "tc_bidir_read":
         return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
     if name == "tc_responsibilities":
@@ -218,6 +218,10 @@ def oracle_sample(w, budget_s, threads=0):
     def run(n):
         sl = slice(0, n)
         t0 = time.perf_counter()
+        if w.N_k:   # cross-attention: the first n queries against every key
+            oracle.forward_cross(host["QX"][:, :, sl], host["KX"], host["V"], host["mu"], host["raw"],
+                                 host["logits"], w.var_floor, w.eps)
+            return time.perf_counter() - t0, 1
         _, used = oracle.forward(w.causal, host["QX"][:, :, sl], host["KX"][:, :, sl],
                                  host["V"][:, :, sl], host["mu"], host["raw"], host["logits"],
                                  w.var_floor, w.eps, nthreads=threads, return_threads=True)
@@ -231,8 +235,12 @@ def oracle_sample(w, budget_s, threads=0):
     if t < budget_s / 2 and n < w.N:
         n = min(w.N, max(n, int(n * budget_s / max(t, 1e-3))))
         t, used = run(n)
-    desc = (f"oracle (fp64 C, OpenMP over heads) on tokens 0..{n - 1} of all {w.H} heads of one "
-            f"sequence of {w.name}; {'causal prefix: exact work for those tokens' if w.causal else 'bidirectional over the truncated sequence'}")
+    if w.N_k:
+        desc = (f"oracle cross-attention (fp64 C, one thread) on queries 0..{n - 1} against all "
+                f"{w.N_k} keys of all {w.H} heads of one sequence of {w.name}")
+    else:
+        desc = (f"oracle (fp64 C, OpenMP over heads) on tokens 0..{n - 1} of all {w.H} heads of one "
+                f"sequence of {w.name}; {'causal prefix: exact work for those tokens' if w.causal else 'bidirectional over the truncated sequence'}")
     return n / t, used, desc, n
 
 
@@ -251,12 +259,18 @@ def run_gma(args, ws, rank, local):
     shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v,
                            gma.GMA_BF16 if w.dtype == "bf16" else gma.GMA_F32, w.eps, w.var_floor)
     variant = gma.GMA_VARIANT_CAUSAL if w.causal else gma.GMA_VARIANT_BIDIRECTIONAL
-    ws_n = gma.gma_workspace_size(shape, variant)
+    ws_n = (gma.gma_workspace_size_cross(shape, w.N_k) if w.N_k
+            else gma.gma_workspace_size(shape, variant))
     workspace = torch.empty(ws_n, dtype=torch.uint8, device=device)
     O = torch.empty(w.B, w.H, w.N, w.d_v, dtype=dev["V"].dtype, device=device)
     stream = torch.cuda.Stream(device)
     sh = stream.cuda_stream
-    fn = gma.gma_forward_causal if w.causal else gma.gma_forward_bidirectional
+    if w.N_k:
+        def fn(*a):
+            return gma.gma_forward_cross(shape, w.N_k, *a[1:])
+        fn.__name__ = "gma_forward_cross"
+    else:
+        fn = gma.gma_forward_causal if w.causal else gma.gma_forward_bidirectional
     ptrs = [dev[k].data_ptr() for k in ("QX", "KX", "V", "mu", "raw", "logits")]
 
     def step():
@@ -386,12 +400,13 @@ def run_gma(args, ws, rank, local):
     fam = gma.gma_kernel_family(shape, variant)
     launches_per_step = len(launches) / steps
     return {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "metric": metric_for(w0), "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
         "warmup": max(args.warmup, 3), "ms_per_step": total_ms_max / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded N(0,1) routing vectors and values)",
-        "config": {"workload": w0.name, "variant": "causal" if w.causal else "bidirectional",
-                   "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r, "K": w.K, "d_v": w.d_v,
+        "config": {"workload": w0.name,
+                   "variant": "cross" if w.N_k else ("causal" if w.causal else "bidirectional"),
+                   "B": w.B, "H": w.H, "N": w.N, "N_k": w.keys, "d_r": w.d_r, "K": w.K, "d_v": w.d_v,
                    "eps": w.eps, "var_floor": w.var_floor,
                    "kernel_family": "tcgen05" if fam == 1 else "fp32 cuda-core",
                    "l2": ("inputs larger than L2 (%.0f MB > 129 MB), no flush"
@@ -408,6 +423,14 @@ def run_gma(args, ws, rank, local):
 
 # ----------------------------------------------------------------------------- decode
 DECODE_METRIC = "GMA decode tokens/s (one new token per sequence per step), B=128,H=16,K=128,d_v=128"
+
+
+def metric_for(w):
+    """The headline metric for the benchmark workload; a descriptive one for the others."""
+    if w.name == DEFAULT_WORKLOAD:
+        return METRIC
+    variant = "cross" if w.N_k else ("causal" if w.causal else "bidirectional")
+    return f"GMA {variant} fwd tokens/s, {w.name} on 1 GB300"
 
 
 def is_decode(w):
@@ -594,6 +617,10 @@ def run_reference(args, ws, rank):
     sl = slice(0, n)
 
     def one():
+        if w.N_k:
+            oracle.forward_cross(host["QX"][:, :, sl], host["KX"], host["V"], host["mu"], host["raw"],
+                                 host["logits"], w.var_floor, w.eps)
+            return
         oracle.forward(w.causal, host["QX"][:, :, sl], host["KX"][:, :, sl], host["V"][:, :, sl],
                        host["mu"], host["raw"], host["logits"], w.var_floor, w.eps)
 
@@ -605,12 +632,13 @@ def run_reference(args, ws, rank):
     dt = time.perf_counter() - t0
     value = n * steps / dt
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "impl": "reference", "metric": metric_for(w), "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded), truncated sample",
-        "config": {"workload": w.name, "variant": "causal" if w.causal else "bidirectional",
-                   "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r, "K": w.K, "d_v": w.d_v},
+        "config": {"workload": w.name,
+                   "variant": "cross" if w.N_k else ("causal" if w.causal else "bidirectional"),
+                   "B": w.B, "H": w.H, "N": w.N, "N_k": w.keys, "d_r": w.d_r, "K": w.K, "d_v": w.d_v},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -132,6 +132,19 @@ gma_status_t gma_decode_step(const gma_shape_t *shape, const void *qx, const voi
                              float *state, void *o, void *workspace, size_t workspace_bytes,
                              gma_stream_t stream);
 
+/* Cross-attention: bidirectional GMA with a separate key set (Méthodologie §2; the page's
+ * Conclusion names cross-attention as future work).  shape->N = N_q queries per slice; n_k keys:
+ *   QX [B][H][N_q][d_r], KX [B][H][n_k][d_r], V [B][H][n_k][d_v] (dtype), O [B][H][N_q][d_v];
+ *   V~ = Gamma_K^T V, Z = Gamma_K^T 1 over the n_k keys,  O = Gamma_Q V~ / (Gamma_Q Z + eps).
+ * The kernel family is that of gma_kernel_family(shape, GMA_VARIANT_BIDIRECTIONAL); the workspace
+ * is gma_workspace_size_cross(shape, n_k) bytes (0 for an invalid shape or n_k < 1).  With
+ * n_k == shape->N this computes what gma_forward_bidirectional computes. */
+size_t gma_workspace_size_cross(const gma_shape_t *shape, int n_k);
+gma_status_t gma_forward_cross(const gma_shape_t *shape, int n_k, const void *QX, const void *KX,
+                               const void *V, const float *mu, const float *raw_var,
+                               const float *prior_logits, void *O, void *workspace,
+                               size_t workspace_bytes, gma_stream_t stream);
+
 /* Causal GMA for callers that cannot allocate device memory.  The page has no counterpart to
  * this entry point: it exists for callers such as allocator or memory-pool callbacks, plugins
  * whose host application owns every device allocation, or loops that must not call cudaMalloc

@@ -43,15 +43,30 @@ gma_status_t check_device()
     return GMA_OK;
 }
 
-gma_status_t begin_call(const gma_shape_t *s, int variant, void *ws, size_t ws_bytes,
-                        cudaStream_t st)
+gma_status_t begin_call_sized(size_t need, void *ws, size_t ws_bytes, cudaStream_t st)
 {
     if (!ws || ((uintptr_t)ws & 255u)) return GMA_ERR_WORKSPACE;
-    if (ws_bytes < gma_workspace_size(s, variant)) return GMA_ERR_WORKSPACE;
+    if (need == 0 || ws_bytes < need) return GMA_ERR_WORKSPACE;
     gma_status_t d = check_device();
     if (d != GMA_OK) return d;
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return GMA_ERR_CUDA;
     return GMA_OK;
+}
+
+gma_status_t begin_call(const gma_shape_t *s, int variant, void *ws, size_t ws_bytes, cudaStream_t st)
+{
+    return begin_call_sized(gma_workspace_size(s, variant), ws, ws_bytes, st);
+}
+
+// The key side of a cross-attention call: the query shape with N = n_k.
+gma_status_t validate_cross(const gma_shape_t *s, int n_k, gma_shape_t *sk)
+{
+    gma_status_t r = validate_shape(s, GMA_VARIANT_BIDIRECTIONAL);
+    if (r != GMA_OK) return r;
+    if (n_k < 1) return GMA_ERR_INVALID_ARG;
+    *sk = *s;
+    sk->N = n_k;
+    return validate_shape(sk, GMA_VARIANT_BIDIRECTIONAL);
 }
 
 gma_status_t forward_common(bool causal, const gma_shape_t *s, const void *QX, const void *KX,
@@ -69,8 +84,8 @@ gma_status_t forward_common(bool causal, const gma_shape_t *s, const void *QX, c
     r = begin_call(s, variant, ws, ws_bytes, st);
     if (r != GMA_OK) return r;
     if (family_of(*s, variant) == 1)
-        return tc_forward(*s, causal, QX, KX, V, mu, raw, logits, O, ws, st);
-    return simt_forward(*s, causal, QX, KX, V, mu, raw, logits, O, ws, st);
+        return tc_forward(*s, causal, s->N, QX, KX, V, mu, raw, logits, O, ws, st);
+    return simt_forward(*s, causal, s->N, QX, KX, V, mu, raw, logits, O, ws, st);
 }
 
 }  // namespace
@@ -129,6 +144,32 @@ gma_status_t gma_forward_causal(const gma_shape_t *s, const void *QX, const void
                                 gma_stream_t stream)
 {
     return forward_common(true, s, QX, KX, V, mu, raw, logits, O, ws, ws_bytes, stream);
+}
+
+size_t gma_workspace_size_cross(const gma_shape_t *s, int n_k)
+{
+    gma_shape_t sk;
+    if (validate_cross(s, n_k, &sk) != GMA_OK) return 0;
+    return family_of(*s, GMA_VARIANT_BIDIRECTIONAL) == 1 ? tc_workspace_size_cross(*s, n_k)
+                                                         : simt_workspace_size_cross(*s, n_k);
+}
+
+gma_status_t gma_forward_cross(const gma_shape_t *s, int n_k, const void *QX, const void *KX, const void *V,
+                               const float *mu, const float *raw, const float *logits, void *O, void *ws,
+                               size_t ws_bytes, gma_stream_t stream)
+{
+    gma_shape_t sk;
+    gma_status_t r = validate_cross(s, n_k, &sk);
+    if (r != GMA_OK) return r;
+    const void *ptrs[] = {QX, KX, V, mu, raw, logits, O};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return GMA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    r = begin_call_sized(gma_workspace_size_cross(s, n_k), ws, ws_bytes, st);
+    if (r != GMA_OK) return r;
+    if (family_of(*s, GMA_VARIANT_BIDIRECTIONAL) == 1)
+        return tc_forward(*s, false, n_k, QX, KX, V, mu, raw, logits, O, ws, st);
+    return simt_forward(*s, false, n_k, QX, KX, V, mu, raw, logits, O, ws, st);
 }
 
 gma_status_t gma_decode_step(const gma_shape_t *s, const void *qx, const void *kx, const void *v,

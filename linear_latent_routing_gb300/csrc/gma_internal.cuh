@@ -76,11 +76,11 @@ size_t simt_workspace_size(const gma_shape_t &s, int variant);
 gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
                                    const float *raw, const float *logits, void *gamma, void *ws,
                                    cudaStream_t st);
-gma_status_t simt_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+// s.N queries and n_k keys per slice (n_k == s.N but for cross-attention, which is bidirectional).
+gma_status_t simt_forward(const gma_shape_t &s, bool causal, int n_k, const void *QX, const void *KX,
                           const void *V, const float *mu, const float *raw, const float *logits,
                           void *O, void *ws, cudaStream_t st);
-
-// Per-head 1 / sigma^2 [H][K][d_r] and log pi - 1/2 sum log sigma^2 [H][K] (fp32, direct form).
+size_t simt_workspace_size_cross(const gma_shape_t &s, int n_k);
 
 // --------------------------------------------------------------- decode step
 size_t decode_workspace_size(const gma_shape_t &s);
@@ -93,9 +93,10 @@ size_t tc_workspace_size(const gma_shape_t &s, int variant);
 gma_status_t tc_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
                                  const float *raw, const float *logits, void *gamma, void *ws,
                                  cudaStream_t st);
-gma_status_t tc_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *QX, const void *KX,
                         const void *V, const float *mu, const float *raw, const float *logits,
                         void *O, void *ws, cudaStream_t st);
+size_t tc_workspace_size_cross(const gma_shape_t &s, int n_k);
 
 }  // namespace gma
 

@@ -171,16 +171,17 @@ __global__ void simt_scan_kernel(float *__restrict__ agg, long long total, int n
 // ---------------------------------------------------------------- read phase, per segment
 // O_i = (gamma_Q,i S + sum_{j<=i in seg} P_ij v_j) / (gamma_Q,i Z + sum_{j<=i in seg} P_ij + eps)
 // with P = Gamma_Q Gamma_K^T on the segment (causal only) and [S | Z] the segment's memory.
+// agg_nseg: segments per slice in agg (the key side's; equal to nseg but for cross-attention).
 template <typename Tin, typename Tout>
 __global__ void simt_out_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                 const Tin *__restrict__ V, const float *__restrict__ agg,
-                                Tout *__restrict__ O, int N, int K, int d_v, int nseg, float eps,
-                                int causal)
+                                Tout *__restrict__ O, int N, int K, int d_v, int nseg, int agg_nseg,
+                                float eps, int causal)
 {
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
     const int i0 = seg * SEG, in = min(SEG, N - i0);
     const int DV1 = d_v + 1;
-    const float *S = agg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * DV1;
+    const float *S = agg + ((size_t)bh * agg_nseg + (causal ? seg : 0)) * K * DV1;
     const float *gqs = gq + ((size_t)bh * N + i0) * K;
     const float *gks = gk + ((size_t)bh * N + i0) * K;
     __shared__ float P[SEG][SEG + 1];
@@ -245,22 +246,26 @@ struct SimtLayout {
     int nseg;
 };
 
-SimtLayout simt_layout(const gma_shape_t &s, int variant)
+// n_k: keys per slice (s.N but for cross-attention); L.nseg splits the keys.
+SimtLayout simt_layout(const gma_shape_t &s, int variant, int n_k)
 {
     SimtLayout L{};
     Carve c;
     const size_t rows = (size_t)s.B * s.H * s.N;
+    const size_t rows_k = (size_t)s.B * s.H * n_k;
     L.inv_var = c.take(sizeof(float) * (size_t)s.H * s.K * s.d_r);
     L.cst = c.take(sizeof(float) * (size_t)s.H * s.K);
-    L.nseg = (s.N + SEG - 1) / SEG;
+    L.nseg = (n_k + SEG - 1) / SEG;
     if (variant != GMA_VARIANT_RESPONSIBILITIES) {
         L.gq = c.take(sizeof(float) * rows * s.K);
-        L.gk = c.take(sizeof(float) * rows * s.K);
+        L.gk = c.take(sizeof(float) * rows_k * s.K);
         L.agg = c.take(sizeof(float) * (size_t)s.B * s.H * L.nseg * s.K * (s.d_v + 1));
     }
     L.total = c.total();
     return L;
 }
+
+SimtLayout simt_layout(const gma_shape_t &s, int variant) { return simt_layout(s, variant, s.N); }
 
 template <typename Tin, typename Tout>
 gma_status_t launch_resp(int d_r, const Tin *X, const float *mu, const float *iv, const float *cst,
@@ -277,34 +282,41 @@ gma_status_t launch_resp(int d_r, const Tin *X, const float *mu, const float *iv
     return GMA_OK;
 }
 
+// s.N queries and n_k keys per slice (n_k == s.N for the causal variant).
 template <typename Tin, typename Tout>
-gma_status_t forward_typed(const gma_shape_t &s, bool causal, const Tin *QX, const Tin *KX,
+gma_status_t forward_typed(const gma_shape_t &s, bool causal, int n_k, const Tin *QX, const Tin *KX,
                            const Tin *V, const float *mu, const float *raw, const float *logits,
                            Tout *O, char *ws, cudaStream_t st)
 {
-    const SimtLayout L = simt_layout(s, causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL);
+    const SimtLayout L = simt_layout(s, causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL, n_k);
     float *iv = (float *)(ws + L.inv_var), *cst = (float *)(ws + L.cst);
     float *gq = (float *)(ws + L.gq), *gk = (float *)(ws + L.gk), *agg = (float *)(ws + L.agg);
-    const long long rows = (long long)s.B * s.H * s.N;
+    const long long rows = (long long)s.B * s.H * s.N, rows_k = (long long)s.B * s.H * n_k;
     GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
     gma_status_t r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
     if (r != GMA_OK) return r;
-    r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, s.N, s.K, rows, st);
+    r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, n_k, s.K, rows_k, st);
     if (r != GMA_OK) return r;
     const int BH = s.B * s.H;
     dim3 gs((unsigned)(BH * L.nseg), (unsigned)((s.K + KT - 1) / KT));
-    GMA_LAUNCH(KID_SIMT_STATE, st, (simt_state_kernel<Tin><<<gs, THREADS, 0, st>>>(gk, V, agg, s.N, s.K, s.d_v, L.nseg)));
+    GMA_LAUNCH(KID_SIMT_STATE, st, (simt_state_kernel<Tin><<<gs, THREADS, 0, st>>>(gk, V, agg, n_k, s.K, s.d_v, L.nseg)));
     const int KD = s.K * (s.d_v + 1);
     const long long tot = (long long)BH * KD;
     GMA_LAUNCH(KID_SIMT_SCAN, st, (simt_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(agg, tot, L.nseg, KD, causal ? 1 : 0)));
-    GMA_LAUNCH(KID_SIMT_OUT, st, (simt_out_kernel<Tin, Tout><<<(unsigned)(BH * L.nseg), THREADS, 0, st>>>(
-        gq, gk, V, agg, O, s.N, s.K, s.d_v, L.nseg, s.eps, causal ? 1 : 0)));
+    const int nseg_q = (s.N + SEG - 1) / SEG;
+    GMA_LAUNCH(KID_SIMT_OUT, st, (simt_out_kernel<Tin, Tout><<<(unsigned)(BH * nseg_q), THREADS, 0, st>>>(
+        gq, gk, V, agg, O, s.N, s.K, s.d_v, nseg_q, L.nseg, s.eps, causal ? 1 : 0)));
     return GMA_OK;
 }
 
 }  // namespace
 
 size_t simt_workspace_size(const gma_shape_t &s, int variant) { return simt_layout(s, variant).total; }
+
+size_t simt_workspace_size_cross(const gma_shape_t &s, int n_k)
+{
+    return simt_layout(s, GMA_VARIANT_BIDIRECTIONAL, n_k).total;
+}
 
 gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const float *mu,
                                    const float *raw, const float *logits, void *gamma, void *ws,
@@ -323,19 +335,19 @@ gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const fl
     return launch_resp<__nv_bfloat16, __nv_bfloat16>(s.d_r, (const __nv_bfloat16 *)X, mu, iv, cst, (__nv_bfloat16 *)gamma, s.H, s.N, s.K, rows, st);
 }
 
-gma_status_t simt_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+gma_status_t simt_forward(const gma_shape_t &s, bool causal, int n_k, const void *QX, const void *KX,
                           const void *V, const float *mu, const float *raw, const float *logits,
                           void *O, void *ws, cudaStream_t st)
 {
     char *w = (char *)ws;
     if (s.dtype == GMA_F32)
-        return forward_typed<float, float>(s, causal, (const float *)QX, (const float *)KX,
+        return forward_typed<float, float>(s, causal, n_k, (const float *)QX, (const float *)KX,
                                            (const float *)V, mu, raw, logits, (float *)O, w, st);
     typedef __nv_bfloat16 bf;
     if (s.flags & GMA_FLAG_OUT_F32)
-        return forward_typed<bf, float>(s, causal, (const bf *)QX, (const bf *)KX, (const bf *)V,
+        return forward_typed<bf, float>(s, causal, n_k, (const bf *)QX, (const bf *)KX, (const bf *)V,
                                         mu, raw, logits, (float *)O, w, st);
-    return forward_typed<bf, bf>(s, causal, (const bf *)QX, (const bf *)KX, (const bf *)V, mu,
+    return forward_typed<bf, bf>(s, causal, n_k, (const bf *)QX, (const bf *)KX, (const bf *)V, mu,
                                  raw, logits, (bf *)O, w, st);
 }
 

@@ -580,6 +580,7 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
     a.ne = p.ne;
     a.nseg = p.nseg;
     a.cps = p.cps;
+    a.agg_nseg = p.nseg;
     a.bimg_bytes = p.bimg_bytes;
     a.bimg_main_bytes = p.bimg_main_bytes;
     a.eps = s.eps;
@@ -643,9 +644,12 @@ gma_status_t launch_params(const gma_shape_t &s, const Plan &p, char *ws, const 
     return GMA_OK;
 }
 
+// `s` describes the keys (s.N keys); `pq` splits the queries, of which there are n_q (the same
+// as s.N but for cross-attention, which is bidirectional).
 template <int DR>
 gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
-                        const void *V, void *O, char *ws, const Plan &p, cudaStream_t st)
+                        const void *V, void *O, char *ws, const Plan &p, const Plan &pq, int n_q,
+                        cudaStream_t st)
 {
     Args a = make_args(s, p, ws);
     a.QX = (const bf16 *)QX;
@@ -688,9 +692,15 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
             if (r != GMA_OK) return r;
         }
     } else {
+        // the query side: its own length and split, reading the key side's total memory
+        Args aq = a;
+        aq.N = n_q;
+        aq.nseg = pq.nseg;
+        aq.cps = pq.cps;
+        aq.agg_nseg = p.nseg;
         CUtensorMap qmap;
-        if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
-        const gma_status_t r = launch_bidir_read2<DR>(a, qmap, BH * p.nseg, st);
+        if (!make_xmap(&qmap, aq.QX, BH, n_q, DR)) return GMA_ERR_CUDA;
+        const gma_status_t r = launch_bidir_read2<DR>(aq, qmap, BH * pq.nseg, st);
         if (r != GMA_OK) return r;
     }
     return GMA_OK;
@@ -742,18 +752,29 @@ gma_status_t tc_responsibilities(const gma_shape_t &s, const void *X, const floa
     return GMA_ERR_UNSUPPORTED_SHAPE;
 }
 
-gma_status_t tc_forward(const gma_shape_t &s, bool causal, const void *QX, const void *KX,
+size_t tc_workspace_size_cross(const gma_shape_t &s, int n_k)
+{
+    gma_shape_t sk = s;
+    sk.N = n_k;
+    return tck::make_plan(sk, GMA_VARIANT_BIDIRECTIONAL).total;
+}
+
+gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *QX, const void *KX,
                         const void *V, const float *mu, const float *raw, const float *logits,
                         void *O, void *ws, cudaStream_t st)
 {
-    const tck::Plan p = tck::make_plan(s, causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL);
+    gma_shape_t sk = s;   // the key side
+    sk.N = n_k;
+    const int variant = causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL;
+    const tck::Plan p = tck::make_plan(sk, variant);
+    const tck::Plan pq = n_k == s.N ? p : tck::make_plan(s, variant);
     char *w = (char *)ws;
     gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
     if (r != GMA_OK) return r;
     switch (s.d_r) {
-    case 16: return tck::forward_dr<16>(s, causal, QX, KX, V, O, w, p, st);
-    case 32: return tck::forward_dr<32>(s, causal, QX, KX, V, O, w, p, st);
-    case 64: return tck::forward_dr<64>(s, causal, QX, KX, V, O, w, p, st);
+    case 16: return tck::forward_dr<16>(sk, causal, QX, KX, V, O, w, p, pq, s.N, st);
+    case 32: return tck::forward_dr<32>(sk, causal, QX, KX, V, O, w, p, pq, s.N, st);
+    case 64: return tck::forward_dr<64>(sk, causal, QX, KX, V, O, w, p, pq, s.N, st);
     }
     return GMA_ERR_UNSUPPORTED_SHAPE;
 }

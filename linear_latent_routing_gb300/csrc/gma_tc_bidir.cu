@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(BTHREADS, 1) tc_bidir_read2_kernel(const Args 
     }
     if (g == 0) {
         // the slice's total memory: V~ rows as the bf16 operand, Z into shared memory
-        const float *src = a.agg + ((size_t)bh * a.nseg * KMAX + i) * a.ne;
+        const float *src = a.agg + ((size_t)bh * a.agg_nseg * KMAX + i) * a.ne;
         for (int b = 0; b < d_v / 16; ++b) {
             const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
             uint32_t r[16];

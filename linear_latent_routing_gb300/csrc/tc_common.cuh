@@ -42,6 +42,7 @@ struct Args {
     WsHeader *hdr;
     int H, N, K, kn16, d_v, ne;
     int nseg, cps;           // segments per slice, chunks per segment
+    int agg_nseg;            // segments per slice in agg (the key side's, for cross-attention)
     int bimg_bytes, bimg_main_bytes;
     float eps;
     int out_f32;

@@ -52,6 +52,10 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         fn.restype = ctypes.c_int
+    lib.gma_workspace_size_cross.argtypes = [sp, ctypes.c_int]
+    lib.gma_workspace_size_cross.restype = sz
+    lib.gma_forward_cross.argtypes = [sp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.gma_forward_cross.restype = ctypes.c_int
     lib.gma_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_decode_step.restype = ctypes.c_int
     lib.gma_forward_causal_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -110,6 +114,16 @@ def gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, workspace
                        workspace_bytes, stream):
     return int(_lib.gma_forward_causal(ctypes.byref(shape), QX, KX, V, mu, raw_var,
                                        prior_logits, O, workspace, int(workspace_bytes), stream))
+
+
+def gma_workspace_size_cross(shape, n_k):
+    return int(_lib.gma_workspace_size_cross(ctypes.byref(shape), int(n_k)))
+
+
+def gma_forward_cross(shape, n_k, QX, KX, V, mu, raw_var, prior_logits, O, workspace,
+                      workspace_bytes, stream):
+    return int(_lib.gma_forward_cross(ctypes.byref(shape), int(n_k), QX, KX, V, mu, raw_var,
+                                      prior_logits, O, workspace, int(workspace_bytes), stream))
 
 
 def gma_decode_step(shape, qx, kx, v, mu, raw_var, prior_logits, state, o, workspace,
@@ -229,6 +243,48 @@ def forward(QX, KX, V, mu, raw_var, prior_logits, causal, eps=1e-6, var_floor=1e
            prior_logits.data_ptr(), out.data_ptr(), workspace.data_ptr(), workspace.numel(), st)
     if r != GMA_OK:
         raise GmaError(r, fn.__name__)
+    if check:
+        r = gma_check_workspace(workspace.data_ptr(), st)
+        if r != GMA_OK:
+            raise GmaError(r, "gma_check_workspace")
+    return out
+
+
+def forward_cross(QX, KX, V, mu, raw_var, prior_logits, eps=1e-6, var_floor=1e-3, flags=0,
+                  out=None, workspace=None, stream=None, check=False):
+    """Cross-attention on torch CUDA tensors; returns O [B, H, N_q, d_v].
+
+    QX [B,H,N_q,d_r], KX [B,H,N_k,d_r] and V [B,H,N_k,d_v] share one dtype (bf16 or fp32); mu,
+    raw_var [H,K,d_r] and prior_logits [H,K] are fp32.
+    """
+    torch = _torch()
+    for t, n in ((QX, "QX"), (KX, "KX"), (V, "V")):
+        _check(t, n, QX.dtype)
+    for t, n in ((mu, "mu"), (raw_var, "raw_var"), (prior_logits, "prior_logits")):
+        _check(t, n, torch.float32)
+    B, H, N_q, d_r = QX.shape
+    N_k = KX.shape[2]
+    d_v = V.shape[-1]
+    K = mu.shape[1]
+    if KX.shape != (B, H, N_k, d_r) or V.shape[:3] != (B, H, N_k):
+        raise ValueError("KX must be [B, H, N_k, d_r] and V [B, H, N_k, d_v]")
+    if mu.shape != (H, K, d_r) or raw_var.shape != (H, K, d_r) or prior_logits.shape != (H, K):
+        raise ValueError("mu, raw_var must be [H, K, d_r] and prior_logits [H, K]")
+    shape = make_shape(B, H, N_q, d_r, K, d_v, _dtype_code(QX), eps, var_floor, flags)
+    if out is None:
+        odt = torch.float32 if (flags & GMA_FLAG_OUT_F32) else QX.dtype
+        out = torch.empty(B, H, N_q, d_v, dtype=odt, device=QX.device)
+    if workspace is None:
+        n = gma_workspace_size_cross(shape, N_k)
+        if n == 0:
+            raise GmaError(2, "gma_workspace_size_cross")
+        workspace = torch.empty(n, dtype=torch.uint8, device=QX.device)
+    st = _stream_handle(stream)
+    r = gma_forward_cross(shape, N_k, QX.data_ptr(), KX.data_ptr(), V.data_ptr(), mu.data_ptr(),
+                          raw_var.data_ptr(), prior_logits.data_ptr(), out.data_ptr(),
+                          workspace.data_ptr(), workspace.numel(), st)
+    if r != GMA_OK:
+        raise GmaError(r, "gma_forward_cross")
     if check:
         r = gma_check_workspace(workspace.data_ptr(), st)
         if r != GMA_OK:

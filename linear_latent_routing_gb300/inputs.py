@@ -35,6 +35,11 @@ class Workload:
     logit_std: float = 1.0
     eps: float = 1e-6
     var_floor: float = 1e-3
+    N_k: int = 0                 # cross-attention: keys per slice (0: the same N as the queries)
+
+    @property
+    def keys(self) -> int:
+        return self.N_k or self.N
 
     @property
     def tokens(self) -> int:
@@ -43,6 +48,10 @@ class Workload:
     @property
     def token_heads(self) -> int:
         return self.B * self.H * self.N
+
+    @property
+    def key_heads(self) -> int:
+        return self.B * self.H * self.keys
 
 
 def _ws(name, causal, B, H, N, d_r, K, d_v, **kw):
@@ -67,7 +76,12 @@ N_SWEEP = tuple(_ws(f"causal_bf16_b2h16_n{n}_dr64_k64_dv128", True, 2, 16, n, 64
 # per-slice state is K x (d_v + 1) fp32, 135 MB for the whole batch (above the 129 MB L2).
 DECODE = _ws("decode_bf16_b128h16_dr64_k128_dv128", True, 128, 16, 8, 64, 128, 128, seed=5)
 
-ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP
+# Cross-attention (bidirectional, separate key set): a short query sequence reading a long one,
+# as a decoder reads an encoder's output; N = 2048 queries, N_k = 16384 keys per slice.
+CROSS = _ws("cross_bf16_b8h16_nq2048_nk16384_dr64_k64_dv64", False, 8, 16, 2048, 64, 64, 64, seed=6,
+            N_k=16384)
+
+ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP + (CROSS,)
 
 
 def by_name(name: str) -> Workload:
@@ -85,18 +99,19 @@ def scaled(w: Workload, **changes) -> Workload:
 def make_inputs(w: Workload):
     """Draw one workload's inputs on the CPU.
 
-    Returns a dict of CPU tensors: QX, KX [B,H,N,d_r], V [B,H,N,d_v] (bf16 or fp32),
-    mu, raw [H,K,d_r] fp32, logits [H,K] fp32.
+    Returns a dict of CPU tensors: QX [B,H,N,d_r], KX [B,H,N_k,d_r], V [B,H,N_k,d_v] (bf16 or
+    fp32; N_k = N but for cross-attention workloads), mu, raw [H,K,d_r] fp32, logits [H,K] fp32.
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(int(w.seed))
     B, H, N, d_r, K, d_v = w.B, w.H, w.N, w.d_r, w.K, w.d_v
+    Nk = w.keys
     QX = torch.randn(B, H, N, d_r, generator=g, dtype=torch.float32)
-    KX = torch.randn(B, H, N, d_r, generator=g, dtype=torch.float32)
+    KX = torch.randn(B, H, Nk, d_r, generator=g, dtype=torch.float32)
     if w.v_dist == "uniform":
-        V = torch.rand(B, H, N, d_v, generator=g, dtype=torch.float32) * 2.0 - 1.0
+        V = torch.rand(B, H, Nk, d_v, generator=g, dtype=torch.float32) * 2.0 - 1.0
     else:
-        V = torch.randn(B, H, N, d_v, generator=g, dtype=torch.float32)
+        V = torch.randn(B, H, Nk, d_v, generator=g, dtype=torch.float32)
     mu = torch.randn(H, K, d_r, generator=g, dtype=torch.float32) * w.mu_std
     raw = torch.randn(H, K, d_r, generator=g, dtype=torch.float32) * w.raw_std
     logits = torch.randn(H, K, generator=g, dtype=torch.float32) * w.logit_std

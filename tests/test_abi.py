@@ -131,3 +131,17 @@ def test_decode_step_validation(g):
     assert g.gma_decode_step(s2, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
     assert g.gma_decode_step(s1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
     assert g.gma_decode_step(_shape(g, N=1, K=0), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) != g.GMA_OK
+
+
+def test_cross_workspace_and_validation(g):
+    """Cross-attention: n_k >= 1; with n_k == N the workspace is the bidirectional one; invalid
+    arguments are refused before anything is enqueued."""
+    s = _shape(g, N=100)
+    assert g.gma_workspace_size_cross(s, 0) == 0
+    assert g.gma_workspace_size_cross(s, -3) == 0
+    assert g.gma_workspace_size_cross(s, 100) == g.gma_workspace_size(s, g.GMA_VARIANT_BIDIRECTIONAL)
+    assert g.gma_workspace_size_cross(s, 5000) > g.gma_workspace_size_cross(s, 100)
+    f32 = _shape(g, N=100, dtype=g.GMA_F32)
+    assert g.gma_workspace_size_cross(f32, 7) > 0
+    assert g.gma_forward_cross(s, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
+    assert g.gma_forward_cross(s, 50, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
