@@ -150,3 +150,53 @@ def forward_cross(QX, KX, V, mu, raw, logits, var_floor, eps):
                                _p(logits), float(var_floor), float(eps), _p(O))
     return O
 
+
+
+def usage_from_assign(assign, K):
+    """Usage statistics of hard assignments, per head.
+
+    assign: [B, H, N] integer component indices.  Returns (counts [H, K] int64, used [H] int64,
+    entropy [H] float64): counts[h, k] = number of tokens of head h assigned to k; used = number
+    of components with a non-zero count; entropy = -sum_k p_k ln p_k / ln K with p = counts /
+    tokens (0 log 0 = 0), the usage entropy normalised to [0, 1] (0 for K = 1).
+    """
+    assign = np.asarray(assign)
+    B, H, N = assign.shape
+    counts = np.zeros((H, K), dtype=np.int64)
+    for h in range(H):
+        counts[h] = np.bincount(assign[:, h, :].reshape(-1), minlength=K)[:K]
+    used = (counts > 0).sum(axis=1)
+    entropy = np.zeros(H)
+    if K > 1:
+        for h in range(H):
+            p = counts[h] / max(counts[h].sum(), 1)
+            nz = p[p > 0]
+            entropy[h] = float(-(nz * np.log(nz)).sum() / np.log(K))
+    return counts, used, entropy
+
+
+def usage(X, mu, raw, logits, var_floor):
+    """Component-usage diagnostics of the rows of X under each head's GMM (the page's
+    interpretability measurements, Résultats et Performance: components used, usage entropy,
+    hard assignments).
+
+    X: [B, H, N, d_r]; mu, raw: [H, K, d_r]; logits: [H, K].  Returns a dict of
+    assign [B, H, N] int64 (argmax_k of the posterior, the lowest k on ties), mass [H, K] float64
+    (sum over tokens of the responsibilities), gamma_max [B, H, N] float64 (the largest
+    responsibility of each token) and counts, used, entropy as in usage_from_assign.
+    """
+    X = _f64(X)
+    B, H, N, _ = X.shape
+    K = np.asarray(mu).shape[1]
+    assign = np.empty((B, H, N), dtype=np.int64)
+    gmax = np.empty((B, H, N))
+    mass = np.zeros((H, K))
+    for h in range(H):
+        for b in range(B):
+            g = responsibilities(X[b, h], mu[h], raw[h], logits[h], var_floor)
+            assign[b, h] = np.argmax(g, axis=1)
+            gmax[b, h] = g.max(axis=1)
+            mass[h] += g.sum(axis=0)
+    counts, used, entropy = usage_from_assign(assign, K)
+    return {"assign": assign, "mass": mass, "gamma_max": gmax, "counts": counts, "used": used,
+            "entropy": entropy}

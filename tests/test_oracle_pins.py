@@ -358,3 +358,58 @@ def test_cross_attention_with_equal_lengths_is_the_bidirectional_forward():
     c = _rand_case(13, N=17)
     got = oracle.forward_cross(c["QX"], c["KX"], c["V"], c["mu"], c["raw"], c["logits"], 1e-3, 1e-6)
     np.testing.assert_allclose(got, _fwd(c, False), rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------------------------ usage diagnostics
+def test_usage_histogram_closed_forms():
+    """Hand-countable assignments: counts, used components and the normalised entropy."""
+    K = 4
+    a = np.array([[[0, 0, 1, 1], [3, 3, 3, 3]]])            # B=1, H=2, N=4
+    counts, used, ent = oracle.usage_from_assign(a, K)
+    assert counts.tolist() == [[2, 2, 0, 0], [0, 0, 0, 4]]
+    assert used.tolist() == [2, 1]
+    assert ent[0] == pytest.approx(np.log(2) / np.log(4), abs=1e-15)   # two equal halves: 1/2
+    assert ent[1] == 0.0                                                # one component: 0
+    uniform = np.arange(8 * K).reshape(1, 1, -1) % K
+    _, used_u, ent_u = oracle.usage_from_assign(uniform, K)
+    assert used_u[0] == K and ent_u[0] == pytest.approx(1.0, abs=1e-15)
+    _, _, ent_1 = oracle.usage_from_assign(np.zeros((2, 1, 3), dtype=int), 1)
+    assert ent_1[0] == 0.0
+
+
+def test_usage_of_hard_clusters_recovers_the_clusters():
+    """Well-separated components, tokens drawn near one mean each: the hard assignment is the
+    cluster, the mass is the cluster size (responsibilities ~ one-hot)."""
+    rng = np.random.default_rng(5)
+    K, d_r = 3, 4
+    mu = np.array([[0.0] * d_r, [12.0] * d_r, [-12.0] * d_r])[None]
+    raw = np.full((1, K, d_r), -2.0)      # small variances
+    logits = np.zeros((1, K))
+    labels = np.array([0, 1, 2, 2, 1, 0, 0, 2, 1, 1])
+    X = (mu[0][labels] + 0.05 * rng.standard_normal((labels.size, d_r)))[None, None]
+    u = oracle.usage(X, mu, raw, logits, 1e-3)
+    assert u["assign"][0, 0].tolist() == labels.tolist()
+    assert u["counts"][0].tolist() == np.bincount(labels, minlength=K).tolist()
+    assert np.allclose(u["mass"][0], np.bincount(labels, minlength=K), atol=1e-9)
+    assert np.allclose(u["gamma_max"], 1.0, atol=1e-9)
+
+
+def test_usage_invariants_and_component_permutation():
+    """Counts and masses sum to the token count; assignments are the argmax of the oracle's
+    posterior; permuting the components permutes counts and masses."""
+    c = _rand_case(11, B=2, H=3, N=41, d_r=5, K=6)
+    u = oracle.usage(c["QX"], c["mu"], c["raw"], c["logits"], 1e-3)
+    assert (u["counts"].sum(axis=1) == 2 * 41).all()
+    assert np.allclose(u["mass"].sum(axis=1), 2 * 41, rtol=1e-12)
+    assert ((u["used"] >= 1) & (u["used"] <= 6)).all()
+    assert ((u["entropy"] >= 0) & (u["entropy"] <= 1)).all()
+    for b, h in [(0, 0), (1, 2)]:
+        var = bruteforce.softplus(c["raw"][h]) + 1e-3
+        g = bruteforce.posterior(c["QX"][b, h], c["mu"][h], var, c["logits"][h])
+        assert (np.argmax(g, axis=1) == u["assign"][b, h]).all()
+        assert np.allclose(g.max(axis=1), u["gamma_max"][b, h], rtol=1e-12)
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    up = oracle.usage(c["QX"], c["mu"][:, perm], c["raw"][:, perm], c["logits"][:, perm], 1e-3)
+    assert (up["counts"] == u["counts"][:, perm]).all()
+    assert np.allclose(up["mass"], u["mass"][:, perm], rtol=1e-12)
+    assert np.allclose(up["entropy"], u["entropy"], rtol=1e-12)
