@@ -79,8 +79,11 @@ def kernel_work(w, name):
         return "hbm", w.key_heads * esz * (w.d_r + w.d_v), "GB/s"
     if name == "tc_bidir_read":
         return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
-    if name == "tc_responsibilities":
-        return "hbm", th * (esz * w.d_r + esz * w.K), "GB/s"
+    if name == "tc_responsibilities":   # fp32 responsibilities when they feed the diagnostics
+        osz = 4 if w.name.startswith("usage_") else esz
+        return "hbm", th * (esz * w.d_r + osz * w.K), "GB/s"
+    if name == "usage_rows":
+        return "hbm", th * (4 * w.K + 4), "GB/s"
     if name == "simt_responsibilities":      # one launch covers one side (queries or keys)
         return "alu", th * 2 * w.K * w.d_r * 3, "TFLOP/s"
     if name == "simt_read":
@@ -601,6 +604,158 @@ def run_decode(args, ws, rank, local):
     }
 
 
+# ----------------------------------------------------------------------------- usage diagnostics
+def usage_bytes(w):
+    """Algorithmic bytes of one diagnostics call: the routing rows read, one int32 assignment per
+    token written (the per-head counts, masses and statistics are negligible)."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return w.token_heads * (esz * w.d_r + 4)
+
+
+def oracle_usage_sample(w, budget_s):
+    import oracle
+    a = W.to_numpy(W.make_inputs(W.scaled(w, B=1, H=1)))
+    n = min(256, w.N)
+    while True:
+        t0 = time.perf_counter()
+        oracle.usage(a["QX"][:, :, :n], a["mu"], a["raw"], a["logits"], w.var_floor)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or n >= w.N:
+            break
+        n = min(w.N, n * 4)
+    desc = f"oracle usage diagnostics (fp64 C posterior + numpy) on tokens 0..{n - 1} of head 0 of {w.name}"
+    return n / dt, 1, desc, n
+
+
+def run_usage(args, ws, rank, local):
+    """One step = one gma_usage call over the workload's Q_X rows (all heads)."""
+    from linear_latent_routing_gb300 import gma
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w0 = W.by_name(args.workload)
+    w = W.Workload(**{**w0.__dict__, "seed": w0.seed + 1000 * rank})
+    host = W.make_inputs(w)
+    X = host["QX"].to(device)
+    par = {k: host[k].to(device) for k in ("mu", "raw", "logits")}
+    shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, 16, gma.GMA_BF16 if w.dtype == "bf16" else gma.GMA_F32,
+                           w.eps, w.var_floor)
+    ws_n = gma.gma_workspace_size(shape, gma.GMA_VARIANT_USAGE)
+    workspace = torch.empty(ws_n, dtype=torch.uint8, device=device)
+    out = {"assign": torch.empty(w.B, w.H, w.N, dtype=torch.int32, device=device),
+           "counts": torch.empty(w.H, w.K, dtype=torch.int32, device=device),
+           "mass": torch.empty(w.H, w.K, dtype=torch.float32, device=device),
+           "used": torch.empty(w.H, dtype=torch.int32, device=device),
+           "entropy": torch.empty(w.H, dtype=torch.float32, device=device)}
+    stream = torch.cuda.Stream(device)
+    sh = stream.cuda_stream
+
+    def step(xp=None):
+        r = gma.gma_usage(shape, (xp or X).data_ptr(), par["mu"].data_ptr(), par["raw"].data_ptr(),
+                          par["logits"].data_ptr(), out["assign"].data_ptr(), out["counts"].data_ptr(),
+                          out["mass"].data_ptr(), out["used"].data_ptr(), out["entropy"].data_ptr(),
+                          workspace.data_ptr(), ws_n, sh)
+        if r != 0:
+            raise gma.GmaError(r, "gma_usage")
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    steps = args.steps if args.steps > 0 else 200
+    gma.gma_timing_enable(steps * 8 + 64)
+    clocks = ClockSampler(device)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    launches = gma.gma_timing_read(steps * 8 + 64)
+    gma.gma_timing_enable(0)
+    st = gma.gma_check_workspace(workspace.data_ptr(), sh)
+    if st != 0:
+        raise gma.GmaError(st, "timed region")
+    total_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    value = w.tokens * ws * steps / (total_ms / 1e3)
+    per_kernel = {}
+    for name, ms in launches:
+        per_kernel.setdefault(name, []).append(ms)
+    dom = max(per_kernel, key=lambda k: sum(per_kernel[k]))
+    avg_ms = sum(per_kernel[dom]) / len(per_kernel[dom])
+    bound, amount, unit = kernel_work(w, dom)
+    pk = peaks()
+    achieved = amount / (avg_ms / 1e3) / 1e9
+    roofline = {"bound": bound, "kernel": dom, "achieved": round(achieved, 3), "peak": pk["hbm_gbs"],
+                "unit": unit, "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                "avg_launch_us": round(avg_ms * 1e3, 3), "launches": len(per_kernel[dom]),
+                "peak_source": f"hbm_gbs of {pk['source']}"}
+    step_s = total_ms / steps / 1e3
+    ub = usage_bytes(w)
+    path_roofline = {"roofline_step_us": round(ub / (pk["hbm_gbs"] * 1e9) * 1e6, 3),
+                     "measured_step_us": round(step_s * 1e6, 3),
+                     "frac": round(ub / (pk["hbm_gbs"] * 1e9) / step_s, 4), "alg_bytes": ub}
+    # end to end: the rows from pinned host memory, the per-head statistics back
+    pin = host["QX"].pin_memory()
+    stage = torch.empty_like(X)
+    res = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in ("counts", "used", "entropy")}
+    h2d = pin.numel() * pin.element_size()
+    d2h = sum(res[k].numel() * res[k].element_size() for k in res)
+
+    def e2e_step():
+        stage.copy_(pin, non_blocking=True)
+        step(stage)
+        for k in res:
+            res[k].copy_(out[k], non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        n_e = min(steps, 20)
+        with torch.cuda.stream(stream):
+            e2e_step()
+        stream.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(n_e):
+                e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), ws, device)
+        e2e = {"value": w.tokens * ws * n_e / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e}
+    if rank != 0:
+        return None
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_usage_sample(w0, args.cpu_budget)
+        cpu = {"value": v / w.H, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": desc + f"; divided by the {w.H} heads a token carries"}
+    return {
+        "metric": f"GMA usage diagnostics tokens/s, {w0.name} on 1 GB300", "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) routing rows)",
+        "config": {"workload": w0.name, "variant": "usage", "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r,
+                   "K": w.K, "kernel_family": "tcgen05" if gma.gma_kernel_family(shape, gma.GMA_VARIANT_USAGE) == 1
+                   else "fp32 cuda-core",
+                   "l2": "fp32 responsibilities (537 MB) larger than L2, no flush",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roofline, "path_roofline": path_roofline,
+        "kernels": {k: {"launches": len(v), "total_ms": round(sum(v), 4)} for k, v in per_kernel.items()},
+        "gpu_launches": len(launches), "launches_per_step": len(launches) / steps,
+        "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+    }
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, ws, rank):
     if rank != 0:
@@ -611,6 +766,8 @@ def run_reference(args, ws, rank):
     per_step_budget = min(5.0, 150.0 / (steps + warm))
     if is_decode(w):
         return run_reference_decode(args, w, ws, steps, warm, per_step_budget)
+    if w.name.startswith("usage_"):
+        return run_reference_usage(args, w, ws, steps, warm, per_step_budget)
     rate, cores, desc, n = oracle_sample(w, per_step_budget)
     import oracle
     host = W.to_numpy(W.make_inputs(W.scaled(w, B=1)))
@@ -641,6 +798,26 @@ def run_reference(args, ws, rank):
                    "B": w.B, "H": w.H, "N": w.N, "N_k": w.keys, "d_r": w.d_r, "K": w.K, "d_v": w.d_v},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_usage(args, w, ws, steps, warm, per_step_budget):
+    rates = []
+    for i in range(warm + steps):
+        rate, cores, desc, n = oracle_usage_sample(w, per_step_budget)
+        if i >= warm:
+            rates.append(rate)
+    value = sum(rates) / len(rates) / w.H   # a token carries H heads
+    return {
+        "impl": "reference", "metric": f"GMA usage diagnostics tokens/s, {w.name} on 1 GB300",
+        "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps, "warmup": warm,
+        "ms_per_step": w.tokens / value * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded), truncated sample",
+        "config": {"workload": w.name, "variant": "usage", "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r,
+                   "K": w.K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc + f"; divided by the {w.H} heads a token carries"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -692,7 +869,8 @@ def main():
         build.build()
         ws, rank, local = dist_setup("nccl")
         w = W.by_name(args.workload)
-        out = (run_decode if is_decode(w) else run_gma)(args, ws, rank, local)
+        runner = run_decode if is_decode(w) else (run_usage if w.name.startswith("usage_") else run_gma)
+        out = runner(args, ws, rank, local)
     if out is not None:
         print(json.dumps(out), flush=True)
     if int(os.environ.get("WORLD_SIZE", "1")) > 1:

@@ -42,6 +42,7 @@
 #define GMA_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -87,6 +88,7 @@ typedef struct {
 #define GMA_VARIANT_BIDIRECTIONAL 1
 #define GMA_VARIANT_CAUSAL 2
 #define GMA_VARIANT_DECODE 3
+#define GMA_VARIANT_USAGE 4
 
 /* Bytes of device workspace one call of `variant` with `shape` needs (0 for an invalid shape).
  * The workspace must be 256-byte aligned.  Its first 256 bytes hold the error word that
@@ -131,6 +133,23 @@ gma_status_t gma_decode_step(const gma_shape_t *shape, const void *qx, const voi
                              const float *mu, const float *raw_var, const float *prior_logits,
                              float *state, void *o, void *workspace, size_t workspace_bytes,
                              gma_stream_t stream);
+
+/* Component-usage diagnostics of the responsibilities of X (Résultats et Performance,
+ * interpretability: components used, usage entropy, hard assignments), per head h:
+ *   assign [B][H][N] int32  argmax_k gamma_{b,h,i,k}, the lowest k on ties
+ *   counts [H][K] int32     tokens assigned to each component (over the batch and the sequence)
+ *   mass [H][K] fp32        sum over tokens of gamma_{.,h,.,k}
+ *   used [H] int32          components with a non-zero count
+ *   entropy [H] fp32        -sum_k p_k ln p_k / ln K with p = counts / (B N); 0 when K = 1
+ * X [B][H][N][d_r] dtype; gamma is computed by the family gma_kernel_family(shape,
+ * GMA_VARIANT_RESPONSIBILITIES) names (tensor-core logits for bf16 inputs it covers, so a token
+ * whose two largest responsibilities nearly tie may be assigned either way), kept in fp32 in the
+ * workspace, gma_workspace_size(shape, GMA_VARIANT_USAGE) bytes.  shape->d_v and eps are
+ * ignored.  Every output is caller-owned device memory, 16-byte aligned; counts are overwritten. */
+gma_status_t gma_usage(const gma_shape_t *shape, const void *X, const float *mu, const float *raw_var,
+                       const float *prior_logits, int32_t *assign, int32_t *counts, float *mass,
+                       int32_t *used, float *entropy, void *workspace, size_t workspace_bytes,
+                       gma_stream_t stream);
 
 /* Cross-attention: bidirectional GMA with a separate key set (Méthodologie §2; the page's
  * Conclusion names cross-attention as future work).  shape->N = N_q queries per slice; n_k keys:

@@ -98,6 +98,10 @@ size_t gma_workspace_size(const gma_shape_t *s, int variant)
         if (validate_shape(s, GMA_VARIANT_CAUSAL) != GMA_OK || s->N != 1) return 0;
         return decode_workspace_size(*s);
     }
+    if (variant == GMA_VARIANT_USAGE) {
+        if (validate_shape(s, GMA_VARIANT_RESPONSIBILITIES) != GMA_OK) return 0;
+        return usage_workspace_size(*s);
+    }
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return 0;
     if (validate_shape(s, variant) != GMA_OK) return 0;
     return family_of(*s, variant) == 1 ? tc_workspace_size(*s, variant)
@@ -108,6 +112,7 @@ int gma_kernel_family(const gma_shape_t *s, int variant)
 {
     if (variant == GMA_VARIANT_DECODE)
         return (validate_shape(s, GMA_VARIANT_CAUSAL) == GMA_OK && s->N == 1) ? 0 : -1;
+    if (variant == GMA_VARIANT_USAGE) variant = GMA_VARIANT_RESPONSIBILITIES;
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return -1;
     if (validate_shape(s, variant) != GMA_OK) return -1;
     return family_of(*s, variant);
@@ -170,6 +175,21 @@ gma_status_t gma_forward_cross(const gma_shape_t *s, int n_k, const void *QX, co
     if (family_of(*s, GMA_VARIANT_BIDIRECTIONAL) == 1)
         return tc_forward(*s, false, n_k, QX, KX, V, mu, raw, logits, O, ws, st);
     return simt_forward(*s, false, n_k, QX, KX, V, mu, raw, logits, O, ws, st);
+}
+
+gma_status_t gma_usage(const gma_shape_t *s, const void *X, const float *mu, const float *raw, const float *logits,
+                       int32_t *assign, int32_t *counts, float *mass, int32_t *used, float *entropy, void *ws,
+                       size_t ws_bytes, gma_stream_t stream)
+{
+    gma_status_t r = validate_shape(s, GMA_VARIANT_RESPONSIBILITIES);
+    if (r != GMA_OK) return r;
+    const void *ptrs[] = {X, mu, raw, logits, assign, counts, mass, used, entropy};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return GMA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    r = begin_call(s, GMA_VARIANT_USAGE, ws, ws_bytes, st);
+    if (r != GMA_OK) return r;
+    return usage(*s, X, mu, raw, logits, assign, counts, mass, used, entropy, ws, st);
 }
 
 gma_status_t gma_decode_step(const gma_shape_t *s, const void *qx, const void *kx, const void *v,

@@ -65,7 +65,7 @@ inline bool valid_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128;
 enum KernelId {
     KID_SIMT_PARAMS = 1, KID_SIMT_RESP, KID_SIMT_STATE, KID_SIMT_SCAN, KID_SIMT_OUT,
     KID_TC_PARAMS = 16, KID_TC_RESP, KID_TC_BIDIR_WRITE, KID_TC_BIDIR_READ, KID_TC_CAUSAL_AGG,
-    KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_DECODE = 32, KID_DECODE_PARAMS, KID_COUNT
+    KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_DECODE = 32, KID_DECODE_PARAMS, KID_USAGE_ROWS, KID_USAGE_MASS, KID_USAGE_STATS, KID_COUNT
 };
 const char *kernel_name(int id);
 void timing_begin(cudaStream_t st, int kernel_id);
@@ -86,6 +86,11 @@ size_t simt_workspace_size_cross(const gma_shape_t &s, int n_k);
 size_t decode_workspace_size(const gma_shape_t &s);
 gma_status_t decode_step(const gma_shape_t &s, const void *qx, const void *kx, const void *v, const float *mu,
                          const float *raw, const float *logits, float *state, void *o, void *ws, cudaStream_t st);
+
+// --------------------------------------------------------------- usage diagnostics
+size_t usage_workspace_size(const gma_shape_t &s);
+gma_status_t usage(const gma_shape_t &s, const void *X, const float *mu, const float *raw, const float *logits,
+                   int *assign, int *counts, float *mass, int *used, float *entropy, void *ws, cudaStream_t st);
 
 // --------------------------------------------------------------- tcgen05 kernel family
 bool tc_supported(const gma_shape_t &s, int variant);

@@ -44,6 +44,9 @@ const char *kernel_name(int id)
     case KID_TC_CAUSAL_OUT: return "tc_causal_chunked";
     case KID_DECODE: return "decode_step";
     case KID_DECODE_PARAMS: return "decode_params";
+    case KID_USAGE_ROWS: return "usage_rows";
+    case KID_USAGE_MASS: return "usage_mass";
+    case KID_USAGE_STATS: return "usage_stats";
     }
     return "unknown";
 }

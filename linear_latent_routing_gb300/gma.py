@@ -21,7 +21,8 @@ GMA_F32, GMA_BF16 = 0, 1
 GMA_FLAG_SIMT = 0x1
 GMA_FLAG_OUT_F32 = 0x2
 GMA_FLAG_RECOMPUTE_KEYS = 0x4
-GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL, GMA_VARIANT_DECODE = 0, 1, 2, 3
+(GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL, GMA_VARIANT_DECODE,
+ GMA_VARIANT_USAGE) = 0, 1, 2, 3, 4
 
 
 class gma_shape_t(ctypes.Structure):
@@ -52,6 +53,8 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         fn.restype = ctypes.c_int
+    lib.gma_usage.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.gma_usage.restype = ctypes.c_int
     lib.gma_workspace_size_cross.argtypes = [sp, ctypes.c_int]
     lib.gma_workspace_size_cross.restype = sz
     lib.gma_forward_cross.argtypes = [sp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -114,6 +117,12 @@ def gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, workspace
                        workspace_bytes, stream):
     return int(_lib.gma_forward_causal(ctypes.byref(shape), QX, KX, V, mu, raw_var,
                                        prior_logits, O, workspace, int(workspace_bytes), stream))
+
+
+def gma_usage(shape, X, mu, raw_var, prior_logits, assign, counts, mass, used, entropy, workspace,
+              workspace_bytes, stream):
+    return int(_lib.gma_usage(ctypes.byref(shape), X, mu, raw_var, prior_logits, assign, counts,
+                              mass, used, entropy, workspace, int(workspace_bytes), stream))
 
 
 def gma_workspace_size_cross(shape, n_k):
@@ -349,6 +358,44 @@ def decode_step(qx, kx, v, mu, raw_var, prior_logits, state, eps=1e-6, var_floor
                         workspace.data_ptr(), workspace.numel(), st)
     if r != GMA_OK:
         raise GmaError(r, "gma_decode_step")
+    if check:
+        r = gma_check_workspace(workspace.data_ptr(), st)
+        if r != GMA_OK:
+            raise GmaError(r, "gma_check_workspace")
+    return out
+
+
+def usage(X, mu, raw_var, prior_logits, var_floor=1e-3, flags=0, workspace=None, stream=None,
+          check=False):
+    """Component-usage diagnostics of X [B, H, N, d_r] (torch CUDA tensor) under each head's GMM.
+
+    Returns a dict of CUDA tensors: assign [B, H, N] int32, counts [H, K] int32, mass [H, K]
+    fp32, used [H] int32, entropy [H] fp32 (see gma_usage in include/gma.h).
+    """
+    torch = _torch()
+    _check(X, "X")
+    for t, n in ((mu, "mu"), (raw_var, "raw_var"), (prior_logits, "prior_logits")):
+        _check(t, n, torch.float32)
+    B, H, N, d_r = X.shape
+    K = mu.shape[1]
+    if mu.shape != (H, K, d_r) or raw_var.shape != (H, K, d_r) or prior_logits.shape != (H, K):
+        raise ValueError("mu, raw_var must be [H, K, d_r] and prior_logits [H, K]")
+    shape = make_shape(B, H, N, d_r, K, 16, _dtype_code(X), 1e-6, var_floor, flags)
+    dev = X.device
+    out = {"assign": torch.empty(B, H, N, dtype=torch.int32, device=dev),
+           "counts": torch.empty(H, K, dtype=torch.int32, device=dev),
+           "mass": torch.empty(H, K, dtype=torch.float32, device=dev),
+           "used": torch.empty(H, dtype=torch.int32, device=dev),
+           "entropy": torch.empty(H, dtype=torch.float32, device=dev)}
+    if workspace is None:
+        workspace = workspace_for(shape, GMA_VARIANT_USAGE, dev)
+    st = _stream_handle(stream)
+    r = gma_usage(shape, X.data_ptr(), mu.data_ptr(), raw_var.data_ptr(), prior_logits.data_ptr(),
+                  out["assign"].data_ptr(), out["counts"].data_ptr(), out["mass"].data_ptr(),
+                  out["used"].data_ptr(), out["entropy"].data_ptr(), workspace.data_ptr(),
+                  workspace.numel(), st)
+    if r != GMA_OK:
+        raise GmaError(r, "gma_usage")
     if check:
         r = gma_check_workspace(workspace.data_ptr(), st)
         if r != GMA_OK:

@@ -81,7 +81,11 @@ DECODE = _ws("decode_bf16_b128h16_dr64_k128_dv128", True, 128, 16, 8, 64, 128, 1
 CROSS = _ws("cross_bf16_b8h16_nq2048_nk16384_dr64_k64_dv64", False, 8, 16, 2048, 64, 64, 64, seed=6,
             N_k=16384)
 
-ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP + (CROSS,)
+# Component-usage diagnostics of one long sequence's routing rows (Q_X of this workload), with
+# the long-context head shape: B=1, H=16, N=65536, d_r=64, K=128 (d_v unused).
+USAGE = _ws("usage_bf16_b1h16_n65536_dr64_k128", False, 1, 16, 65536, 64, 128, 16, seed=7)
+
+ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP + (CROSS, USAGE)
 
 
 def by_name(name: str) -> Workload:

@@ -145,3 +145,12 @@ def test_cross_workspace_and_validation(g):
     assert g.gma_workspace_size_cross(f32, 7) > 0
     assert g.gma_forward_cross(s, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
     assert g.gma_forward_cross(s, 50, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
+
+
+def test_usage_workspace_and_validation(g):
+    s = _shape(g, N=100, K=100)
+    n = g.gma_workspace_size(s, g.GMA_VARIANT_USAGE)
+    assert n >= 2 * 3 * 100 * 100 * 4   # fp32 responsibilities of every token
+    assert g.gma_kernel_family(s, g.GMA_VARIANT_USAGE) == g.gma_kernel_family(s, g.GMA_VARIANT_RESPONSIBILITIES)
+    assert g.gma_workspace_size(_shape(g, N=100, K=0), g.GMA_VARIANT_USAGE) == 0
+    assert g.gma_usage(s, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
