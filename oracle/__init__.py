@@ -200,3 +200,63 @@ def usage(X, mu, raw, logits, var_floor):
     counts, used, entropy = usage_from_assign(assign, K)
     return {"assign": assign, "mass": mass, "gamma_max": gmax, "counts": counts, "used": used,
             "entropy": entropy}
+
+
+def backward(causal, QX, KX, V, mu, raw, logits, var_floor, eps, dO):
+    """Gradients of sum(dO * O) with respect to every input of the forward pass (the page's
+    training path: Méthodologie §3, end-to-end training by backpropagation through the softmax
+    posteriors and the ratio), written out from the explicit affinity form, one slice at a time.
+
+    QX, KX: [B, H, N, d_r]; V, dO: [B, H, N, d_v]; mu, raw: [H, K, d_r]; logits: [H, K].
+    Returns (dQX, dKX, dV, dmu, draw, dlogits) in float64, the parameter gradients summed over
+    the batch.
+
+    Per slice, with A = Gamma_Q Gamma_K^T (lower triangle kept for the causal variant),
+    num = A V, den = A 1 + eps, O = num / den:
+      dnum = dO / den,  dden = -rowsum(dO * num) / den^2,  dA = dnum V^T + dden 1^T (masked),
+      dV = A^T dnum,  dGamma_Q = dA Gamma_K,  dGamma_K = dA^T Gamma_Q,
+      dL = Gamma * (dGamma - rowsum(Gamma * dGamma))             (softmax over components),
+    and through L_k = log pi_k - 1/2 sum_d [(x_d - mu_kd)^2 / s_kd + log s_kd], s = softplus(raw)
+    + floor, log pi = logits - logsumexp(logits):
+      dx_d   = -sum_k dL_k (x_d - mu_kd) / s_kd
+      dmu_kd = sum_rows dL_k (x_d - mu_kd) / s_kd
+      ds_kd  = sum_rows dL_k [ (x_d - mu_kd)^2 / (2 s_kd^2) - 1 / (2 s_kd) ],  draw = ds * sigmoid(raw)
+      dlogits_j = sum_rows dL_j - pi_j sum_rows sum_k dL_k.
+    """
+    QX, KX, V, dO = _f64(QX), _f64(KX), _f64(V), _f64(dO)
+    mu, raw, logits = _f64(mu), _f64(raw), _f64(logits)
+    B, H, N, d_r = QX.shape
+    K = mu.shape[1]
+    dQX = np.zeros_like(QX)
+    dKX = np.zeros_like(KX)
+    dV = np.zeros_like(V)
+    dmu = np.zeros_like(mu)
+    ds = np.zeros_like(raw)
+    dlogpi = np.zeros((H, K))
+    mask = np.tril(np.ones((N, N))) if causal else np.ones((N, N))
+    for h in range(H):
+        var, logpi = params(raw[h], logits[h], var_floor)
+        w = 1.0 / var
+        for b in range(B):
+            GQ = responsibilities(QX[b, h], mu[h], raw[h], logits[h], var_floor)
+            GK = responsibilities(KX[b, h], mu[h], raw[h], logits[h], var_floor)
+            A = (GQ @ GK.T) * mask
+            num = A @ V[b, h]
+            den = A.sum(axis=1) + eps
+            dnum = dO[b, h] / den[:, None]
+            dden = -(dO[b, h] * num).sum(axis=1) / den ** 2
+            dA = (dnum @ V[b, h].T + dden[:, None]) * mask
+            dV[b, h] = A.T @ dnum
+            for X, G, dG, dX in ((QX[b, h], GQ, dA @ GK, dQX[b, h]), (KX[b, h], GK, dA.T @ GQ, dKX[b, h])):
+                dL = G * (dG - (G * dG).sum(axis=1, keepdims=True))
+                diff = X[:, None, :] - mu[h][None, :, :]                  # [N, K, d_r]
+                t = dL[:, :, None] * w[None, :, :] * diff
+                dX[...] = -t.sum(axis=1)
+                dmu[h] += t.sum(axis=0)
+                ds[h] += (dL[:, :, None] * (0.5 * w[None] ** 2 * diff ** 2 - 0.5 * w[None])).sum(axis=0)
+                dlogpi[h] += dL.sum(axis=0)
+    pi = np.exp(logits - logits.max(axis=1, keepdims=True))
+    pi /= pi.sum(axis=1, keepdims=True)
+    dlogits = dlogpi - pi * dlogpi.sum(axis=1, keepdims=True)
+    draw = ds / (1.0 + np.exp(-raw))
+    return dQX, dKX, dV, dmu, draw, dlogits

@@ -413,3 +413,51 @@ def test_usage_invariants_and_component_permutation():
     assert (up["counts"] == u["counts"][:, perm]).all()
     assert np.allclose(up["mass"], u["mass"][:, perm], rtol=1e-12)
     assert np.allclose(up["entropy"], u["entropy"], rtol=1e-12)
+
+
+# ------------------------------------------------------------------ backward pass
+def _loss(causal, c, dO, floor=1e-3, eps=1e-6):
+    return float((_fwd(c, causal, floor, eps) * dO).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_central_differences(causal):
+    """Every gradient of sum(dO * O) against central differences of the forward oracle (fp64,
+    step 1e-6): a dropped term, a wrong sign or a transposed operand anywhere fails this."""
+    c = _rand_case(21, B=2, H=2, N=6, d_r=3, K=4, d_v=2)
+    rng = np.random.default_rng(22)
+    dO = rng.standard_normal((2, 2, 6, 2))
+    grads = oracle.backward(causal, c["QX"], c["KX"], c["V"], c["mu"], c["raw"], c["logits"], 1e-3,
+                            1e-6, dO)
+    names = ["QX", "KX", "V", "mu", "raw", "logits"]
+    h = 1e-6
+    for name, g in zip(names, grads):
+        base = c[name]
+        flat = base.reshape(-1)
+        num = np.empty(flat.size)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + h
+            lp = _loss(causal, c, dO)
+            flat[i] = old - h
+            lm = _loss(causal, c, dO)
+            flat[i] = old
+            num[i] = (lp - lm) / (2 * h)
+        scale = max(np.abs(num).max(), 1e-3)
+        assert np.abs(g.reshape(-1) - num).max() <= 1e-6 * scale + 1e-8, name
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_invariants(causal):
+    """Translation x -> x + t, mu -> mu + t leaves the output unchanged, so the gradients of the
+    routing rows and of the means sum to zero per head and dimension; the prior gradient sums to
+    zero over the components (log softmax); dV is linear in dO."""
+    c = _rand_case(23, B=2, H=2, N=9, d_r=4, K=5, d_v=3)
+    dO = np.random.default_rng(24).standard_normal((2, 2, 9, 3))
+    g = oracle.backward(causal, c["QX"], c["KX"], c["V"], c["mu"], c["raw"], c["logits"], 1e-3, 1e-6, dO)
+    dQX, dKX, dV, dmu, draw, dlog = g
+    tot = dQX.sum(axis=(0, 2)) + dKX.sum(axis=(0, 2)) + dmu.sum(axis=1)
+    assert np.abs(tot).max() <= 1e-10 * max(1.0, np.abs(dmu).max())
+    assert np.abs(dlog.sum(axis=1)).max() <= 1e-12 * max(1.0, np.abs(dlog).max())
+    g2 = oracle.backward(causal, c["QX"], c["KX"], c["V"], c["mu"], c["raw"], c["logits"], 1e-3, 1e-6, 2.5 * dO)
+    assert np.allclose(g2[2], 2.5 * dV, rtol=1e-12, atol=1e-14)
