@@ -84,6 +84,18 @@ def kernel_work(w, name):
         return "hbm", th * (esz * w.d_r + osz * w.K), "GB/s"
     if name == "usage_rows":
         return "hbm", th * (4 * w.K + 4), "GB/s"
+    # backward (fp32 CUDA cores): flops of each kernel's arithmetic, in-segment (64-token) terms included
+    dv1 = w.d_v + 1
+    if name == "bwd_numden":
+        return "alu", th * 2 * (w.K * dv1 + (64 * w.K + 32 * dv1 if w.causal else 0)), "TFLOP/s"
+    if name == "bwd_dgamma_q":
+        return "alu", th * 2 * (w.K * dv1 + (32 * w.K + 32 * dv1 if w.causal else 0)), "TFLOP/s"
+    if name == "bwd_dgamma_k_dv":
+        return "alu", th * 2 * (w.K * w.d_v + w.K * dv1 + (64 * w.K + 32 * w.d_v + 32 * w.K + 32 * dv1 if w.causal else 0)), "TFLOP/s"
+    if name == "bwd_param_partials":
+        return "alu", 2 * th * w.K * w.d_r * 7, "TFLOP/s"
+    if name == "bwd_dx":            # one launch covers one side
+        return "alu", th * w.K * w.d_r * 4, "TFLOP/s"
     if name == "simt_responsibilities":      # one launch covers one side (queries or keys)
         return "alu", th * 2 * w.K * w.d_r * 3, "TFLOP/s"
     if name == "simt_read":
@@ -756,6 +768,170 @@ def run_usage(args, ws, rank, local):
     }
 
 
+# ----------------------------------------------------------------------------- backward pass
+def backward_bytes(w):
+    """Algorithmic bytes of one backward call: Q_X, K_X, V and dO read, dQ_X, dK_X, dV written."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return w.token_heads * esz * (4 * w.d_r + 3 * w.d_v)
+
+
+def _bwd_dO(w):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed) + 2024)
+    d = torch.randn(w.B, w.H, w.N, w.d_v, generator=g, dtype=torch.float32)
+    return d.to(torch.bfloat16) if w.dtype == "bf16" else d
+
+
+def oracle_backward_sample(w, budget_s):
+    import oracle
+    ws_ = W.scaled(w, B=1, H=1)
+    a = W.to_numpy(W.make_inputs(ws_))
+    dO = _bwd_dO(w)[:1, :1].float().numpy()
+    n = 64
+    while True:
+        t0 = time.perf_counter()
+        oracle.backward(w.causal, a["QX"][:, :, :n], a["KX"][:, :, :n], a["V"][:, :, :n], a["mu"], a["raw"],
+                        a["logits"], w.var_floor, w.eps, dO[:, :, :n])
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or n >= w.N:
+            break
+        n = min(w.N, n * 2)
+    desc = (f"oracle backward (fp64, explicit affinity form) on tokens 0..{n - 1} of one head of {w.name}; "
+            f"its work grows as N^2, so longer prefixes would be slower per token")
+    return n / dt, 1, desc, n
+
+
+def run_backward(args, ws, rank, local):
+    """One step = one gma_backward call (the whole layer's gradients) on the workload."""
+    from linear_latent_routing_gb300 import gma
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w0 = W.by_name(args.workload)
+    w = W.Workload(**{**w0.__dict__, "seed": w0.seed + 1000 * rank})
+    host = W.make_inputs(w)
+    host["dO"] = _bwd_dO(w)
+    dev = {k: v.to(device) for k, v in host.items()}
+    shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16 if w.dtype == "bf16" else gma.GMA_F32,
+                           w.eps, w.var_floor)
+    ws_n = gma.gma_workspace_size(shape, gma.GMA_VARIANT_BACKWARD)
+    workspace = torch.empty(ws_n, dtype=torch.uint8, device=device)
+    outs = [torch.empty_like(dev["QX"]), torch.empty_like(dev["KX"]), torch.empty_like(dev["V"]),
+            torch.empty_like(dev["mu"]), torch.empty_like(dev["raw"]), torch.empty_like(dev["logits"])]
+    stream = torch.cuda.Stream(device)
+    sh = stream.cuda_stream
+
+    def step(src=None):
+        d = src or dev
+        r = gma.gma_backward(shape, 1 if w.causal else 0, *[d[k].data_ptr() for k in ("QX", "KX", "V")],
+                             *[dev[k].data_ptr() for k in ("mu", "raw", "logits")], d["dO"].data_ptr(),
+                             *[t.data_ptr() for t in outs], workspace.data_ptr(), ws_n, sh)
+        if r != 0:
+            raise gma.GmaError(r, "gma_backward")
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    steps = args.steps if args.steps > 0 else 50
+    gma.gma_timing_enable(steps * 16 + 64)
+    clocks = ClockSampler(device)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    launches = gma.gma_timing_read(steps * 16 + 64)
+    gma.gma_timing_enable(0)
+    st = gma.gma_check_workspace(workspace.data_ptr(), sh)
+    if st != 0:
+        raise gma.GmaError(st, "timed region")
+    total_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    value = w.tokens * ws * steps / (total_ms / 1e3)
+    per_kernel = {}
+    for name, ms in launches:
+        per_kernel.setdefault(name, []).append(ms)
+    dom = max(per_kernel, key=lambda k: sum(per_kernel[k]))
+    avg_ms = sum(per_kernel[dom]) / len(per_kernel[dom])
+    bound, amount, unit = kernel_work(w, dom)
+    pk = peaks()
+    if bound == "alu":
+        achieved = amount / (avg_ms / 1e3) / 1e12
+        peak = SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+        src = "fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock"
+    else:
+        achieved = amount / (avg_ms / 1e3) / 1e9
+        peak = pk["hbm_gbs"]
+        src = f"hbm_gbs of {pk['source']}"
+    roofline = {"bound": bound, "kernel": dom, "achieved": round(achieved, 3), "peak": round(peak, 3),
+                "unit": unit, "frac": round(achieved / peak, 4), "traffic": None,
+                "avg_launch_us": round(avg_ms * 1e3, 3), "launches": len(per_kernel[dom]), "peak_source": src}
+    bb = backward_bytes(w)
+    step_s = total_ms / steps / 1e3
+    path_roofline = {"roofline_step_us": round(bb / (pk["hbm_gbs"] * 1e9) * 1e6, 3),
+                     "measured_step_us": round(step_s * 1e6, 3),
+                     "frac": round(bb / (pk["hbm_gbs"] * 1e9) / step_s, 4), "alg_bytes": bb}
+    pin = {k: host[k].pin_memory() for k in ("QX", "KX", "V", "dO")}
+    stage = {k: torch.empty_like(dev[k]) for k in pin}
+    res = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in res)
+
+    def e2e_step():
+        for k in pin:
+            stage[k].copy_(pin[k], non_blocking=True)
+        step(stage)
+        for a, b in zip(res, outs):
+            a.copy_(b, non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        n_e = min(steps, 10)
+        with torch.cuda.stream(stream):
+            e2e_step()
+        stream.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(n_e):
+                e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), ws, device)
+        e2e = {"value": w.tokens * ws * n_e / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e}
+    if rank != 0:
+        return None
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_backward_sample(w0, args.cpu_budget)
+        cpu = {"value": v / w.H, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": desc + f"; divided by the {w.H} heads a token carries"}
+    return {
+        "metric": f"GMA backward tokens/s, {w0.name} on 1 GB300", "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 in/out)",
+        "data": "synthetic (seeded N(0,1) rows, values and output gradients)",
+        "config": {"workload": w0.name, "variant": "backward, causal" if w.causal else "backward, bidirectional",
+                   "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r, "K": w.K, "d_v": w.d_v,
+                   "kernel_family": "fp32 cuda-core", "l2": "not flushed (workspace > L2)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roofline, "path_roofline": path_roofline,
+        "kernels": {k: {"launches": len(v), "total_ms": round(sum(v), 4)} for k, v in per_kernel.items()},
+        "gpu_launches": len(launches), "launches_per_step": len(launches) / steps,
+        "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+    }
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, ws, rank):
     if rank != 0:
@@ -768,6 +944,8 @@ def run_reference(args, ws, rank):
         return run_reference_decode(args, w, ws, steps, warm, per_step_budget)
     if w.name.startswith("usage_"):
         return run_reference_usage(args, w, ws, steps, warm, per_step_budget)
+    if w.name.startswith("backward_"):
+        return run_reference_backward(args, w, ws, steps, warm, per_step_budget)
     rate, cores, desc, n = oracle_sample(w, per_step_budget)
     import oracle
     host = W.to_numpy(W.make_inputs(W.scaled(w, B=1)))
@@ -798,6 +976,26 @@ def run_reference(args, ws, rank):
                    "B": w.B, "H": w.H, "N": w.N, "N_k": w.keys, "d_r": w.d_r, "K": w.K, "d_v": w.d_v},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_backward(args, w, ws, steps, warm, per_step_budget):
+    rates = []
+    for i in range(warm + steps):
+        rate, cores, desc, n = oracle_backward_sample(w, per_step_budget)
+        if i >= warm:
+            rates.append(rate)
+    value = sum(rates) / len(rates) / w.H
+    return {
+        "impl": "reference", "metric": f"GMA backward tokens/s, {w.name} on 1 GB300",
+        "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps, "warmup": warm,
+        "ms_per_step": w.tokens / value * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded), truncated sample",
+        "config": {"workload": w.name, "variant": "backward", "B": w.B, "H": w.H, "N": w.N, "d_r": w.d_r,
+                   "K": w.K, "d_v": w.d_v},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc + f"; divided by the {w.H} heads a token carries"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -869,7 +1067,8 @@ def main():
         build.build()
         ws, rank, local = dist_setup("nccl")
         w = W.by_name(args.workload)
-        runner = run_decode if is_decode(w) else (run_usage if w.name.startswith("usage_") else run_gma)
+        runner = (run_decode if is_decode(w) else run_usage if w.name.startswith("usage_")
+                  else run_backward if w.name.startswith("backward_") else run_gma)
         out = runner(args, ws, rank, local)
     if out is not None:
         print(json.dumps(out), flush=True)

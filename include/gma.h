@@ -89,6 +89,7 @@ typedef struct {
 #define GMA_VARIANT_CAUSAL 2
 #define GMA_VARIANT_DECODE 3
 #define GMA_VARIANT_USAGE 4
+#define GMA_VARIANT_BACKWARD 5
 
 /* Bytes of device workspace one call of `variant` with `shape` needs (0 for an invalid shape).
  * The workspace must be 256-byte aligned.  Its first 256 bytes hold the error word that
@@ -133,6 +134,21 @@ gma_status_t gma_decode_step(const gma_shape_t *shape, const void *qx, const voi
                              const float *mu, const float *raw_var, const float *prior_logits,
                              float *state, void *o, void *workspace, size_t workspace_bytes,
                              gma_stream_t stream);
+
+/* Backward pass (Méthodologie §3: end-to-end training by backpropagation through the softmax
+ * posteriors and the ratio): the gradients of sum(dO * O) for the bidirectional (causal = 0) or
+ * causal (causal = 1) forward pass with the same arguments.
+ *   dO, and the outputs dQX, dKX [B][H][N][d_r], dV [B][H][N][d_v]: dtype (bf16 or fp32);
+ *   dmu, draw_var [H][K][d_r] and dprior_logits [H][K]: fp32, summed over the batch.
+ * Every step runs in fp32 on the CUDA cores (the forward's own preparation, then the reverse
+ * passes over 64-token segments); gma_kernel_family(shape, GMA_VARIANT_BACKWARD) is 0.  The
+ * workspace is gma_workspace_size(shape, GMA_VARIANT_BACKWARD) bytes: fp32 responsibilities and
+ * their gradients for every token (4 B*H*N*K floats) and the segment memories.  Outputs are
+ * written, not accumulated; results repeat exactly from call to call. */
+gma_status_t gma_backward(const gma_shape_t *shape, int causal, const void *QX, const void *KX, const void *V,
+                          const float *mu, const float *raw_var, const float *prior_logits, const void *dO,
+                          void *dQX, void *dKX, void *dV, float *dmu, float *draw_var, float *dprior_logits,
+                          void *workspace, size_t workspace_bytes, gma_stream_t stream);
 
 /* Component-usage diagnostics of the responsibilities of X (Résultats et Performance,
  * interpretability: components used, usage entropy, hard assignments), per head h:

@@ -102,6 +102,10 @@ size_t gma_workspace_size(const gma_shape_t *s, int variant)
         if (validate_shape(s, GMA_VARIANT_RESPONSIBILITIES) != GMA_OK) return 0;
         return usage_workspace_size(*s);
     }
+    if (variant == GMA_VARIANT_BACKWARD) {
+        if (validate_shape(s, GMA_VARIANT_CAUSAL) != GMA_OK) return 0;
+        return backward_workspace_size(*s);
+    }
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return 0;
     if (validate_shape(s, variant) != GMA_OK) return 0;
     return family_of(*s, variant) == 1 ? tc_workspace_size(*s, variant)
@@ -113,6 +117,7 @@ int gma_kernel_family(const gma_shape_t *s, int variant)
     if (variant == GMA_VARIANT_DECODE)
         return (validate_shape(s, GMA_VARIANT_CAUSAL) == GMA_OK && s->N == 1) ? 0 : -1;
     if (variant == GMA_VARIANT_USAGE) variant = GMA_VARIANT_RESPONSIBILITIES;
+    if (variant == GMA_VARIANT_BACKWARD) return validate_shape(s, GMA_VARIANT_CAUSAL) == GMA_OK ? 0 : -1;
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return -1;
     if (validate_shape(s, variant) != GMA_OK) return -1;
     return family_of(*s, variant);
@@ -175,6 +180,23 @@ gma_status_t gma_forward_cross(const gma_shape_t *s, int n_k, const void *QX, co
     if (family_of(*s, GMA_VARIANT_BIDIRECTIONAL) == 1)
         return tc_forward(*s, false, n_k, QX, KX, V, mu, raw, logits, O, ws, st);
     return simt_forward(*s, false, n_k, QX, KX, V, mu, raw, logits, O, ws, st);
+}
+
+gma_status_t gma_backward(const gma_shape_t *s, int causal, const void *QX, const void *KX, const void *V,
+                          const float *mu, const float *raw, const float *logits, const void *dO, void *dQX, void *dKX,
+                          void *dV, float *dmu, float *draw, float *dlogits, void *ws, size_t ws_bytes,
+                          gma_stream_t stream)
+{
+    gma_status_t r = validate_shape(s, GMA_VARIANT_CAUSAL);
+    if (r != GMA_OK) return r;
+    if (causal != 0 && causal != 1) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {QX, KX, V, mu, raw, logits, dO, dQX, dKX, dV, dmu, draw, dlogits};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return GMA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    r = begin_call(s, GMA_VARIANT_BACKWARD, ws, ws_bytes, st);
+    if (r != GMA_OK) return r;
+    return backward(*s, causal != 0, QX, KX, V, mu, raw, logits, dO, dQX, dKX, dV, dmu, draw, dlogits, ws, st);
 }
 
 gma_status_t gma_usage(const gma_shape_t *s, const void *X, const float *mu, const float *raw, const float *logits,

@@ -65,7 +65,9 @@ inline bool valid_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128;
 enum KernelId {
     KID_SIMT_PARAMS = 1, KID_SIMT_RESP, KID_SIMT_STATE, KID_SIMT_SCAN, KID_SIMT_OUT,
     KID_TC_PARAMS = 16, KID_TC_RESP, KID_TC_BIDIR_WRITE, KID_TC_BIDIR_READ, KID_TC_CAUSAL_AGG,
-    KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_DECODE = 32, KID_DECODE_PARAMS, KID_USAGE_ROWS, KID_USAGE_MASS, KID_USAGE_STATS, KID_COUNT
+    KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_DECODE = 32, KID_DECODE_PARAMS, KID_USAGE_ROWS, KID_USAGE_MASS, KID_USAGE_STATS, KID_BWD_NUMDEN,
+    KID_BWD_DQ, KID_BWD_SEG, KID_BWD_SCAN, KID_BWD_DK, KID_BWD_SOFTMAX, KID_BWD_DX, KID_BWD_PARAMS,
+    KID_BWD_PFINAL, KID_COUNT
 };
 const char *kernel_name(int id);
 void timing_begin(cudaStream_t st, int kernel_id);
@@ -81,6 +83,18 @@ gma_status_t simt_forward(const gma_shape_t &s, bool causal, int n_k, const void
                           const void *V, const float *mu, const float *raw, const float *logits,
                           void *O, void *ws, cudaStream_t st);
 size_t simt_workspace_size_cross(const gma_shape_t &s, int n_k);
+// The read phase's inputs (fp32 CUDA cores, direct form): per-head 1/sigma^2 [H][K][d_r] and
+// constants [H][K]; Gamma_Q, Gamma_K [B*H*N][K]; segment memories [B*H][ceil(N/64)][K][d_v+1],
+// scanned (causal: exclusive prefix per 64-token segment; bidirectional: the total in segment 0).
+gma_status_t simt_prepare(const gma_shape_t &s, bool causal, const void *QX, const void *KX, const void *V,
+                          const float *mu, const float *raw, const float *logits, float *iv, float *cst, float *gq,
+                          float *gk, float *agg, cudaStream_t st);
+
+// --------------------------------------------------------------- backward pass
+size_t backward_workspace_size(const gma_shape_t &s);
+gma_status_t backward(const gma_shape_t &s, bool causal, const void *QX, const void *KX, const void *V,
+                      const float *mu, const float *raw, const float *logits, const void *dO, void *dQX, void *dKX,
+                      void *dV, float *dmu, float *draw, float *dlogits, void *ws, cudaStream_t st);
 
 // --------------------------------------------------------------- decode step
 size_t decode_workspace_size(const gma_shape_t &s);

@@ -282,6 +282,29 @@ gma_status_t launch_resp(int d_r, const Tin *X, const float *mu, const float *iv
     return GMA_OK;
 }
 
+// Everything the read phase needs: the parameters, Gamma_Q and Gamma_K (fp32), and the segment
+// memories [S | Z] scanned (causal: exclusive prefix per segment; bidirectional: the total in
+// segment 0).  s.N queries and n_k keys per slice; nseg splits the keys into SEG-token segments.
+template <typename Tin>
+gma_status_t prepare_typed(const gma_shape_t &s, bool causal, int n_k, const Tin *QX, const Tin *KX,
+                           const Tin *V, const float *mu, const float *raw, const float *logits, float *iv,
+                           float *cst, float *gq, float *gk, float *agg, int nseg, cudaStream_t st)
+{
+    const long long rows = (long long)s.B * s.H * s.N, rows_k = (long long)s.B * s.H * n_k;
+    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
+    gma_status_t r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
+    if (r != GMA_OK) return r;
+    r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, n_k, s.K, rows_k, st);
+    if (r != GMA_OK) return r;
+    const int BH = s.B * s.H;
+    dim3 gs((unsigned)(BH * nseg), (unsigned)((s.K + KT - 1) / KT));
+    GMA_LAUNCH(KID_SIMT_STATE, st, (simt_state_kernel<Tin><<<gs, THREADS, 0, st>>>(gk, V, agg, n_k, s.K, s.d_v, nseg)));
+    const int KD = s.K * (s.d_v + 1);
+    const long long tot = (long long)BH * KD;
+    GMA_LAUNCH(KID_SIMT_SCAN, st, (simt_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(agg, tot, nseg, KD, causal ? 1 : 0)));
+    return GMA_OK;
+}
+
 // s.N queries and n_k keys per slice (n_k == s.N for the causal variant).
 template <typename Tin, typename Tout>
 gma_status_t forward_typed(const gma_shape_t &s, bool causal, int n_k, const Tin *QX, const Tin *KX,
@@ -291,25 +314,30 @@ gma_status_t forward_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
     const SimtLayout L = simt_layout(s, causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL, n_k);
     float *iv = (float *)(ws + L.inv_var), *cst = (float *)(ws + L.cst);
     float *gq = (float *)(ws + L.gq), *gk = (float *)(ws + L.gk), *agg = (float *)(ws + L.agg);
-    const long long rows = (long long)s.B * s.H * s.N, rows_k = (long long)s.B * s.H * n_k;
-    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
-    gma_status_t r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
-    if (r != GMA_OK) return r;
-    r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, n_k, s.K, rows_k, st);
+    gma_status_t r = prepare_typed<Tin>(s, causal, n_k, QX, KX, V, mu, raw, logits, iv, cst, gq, gk, agg, L.nseg, st);
     if (r != GMA_OK) return r;
     const int BH = s.B * s.H;
-    dim3 gs((unsigned)(BH * L.nseg), (unsigned)((s.K + KT - 1) / KT));
-    GMA_LAUNCH(KID_SIMT_STATE, st, (simt_state_kernel<Tin><<<gs, THREADS, 0, st>>>(gk, V, agg, n_k, s.K, s.d_v, L.nseg)));
-    const int KD = s.K * (s.d_v + 1);
-    const long long tot = (long long)BH * KD;
-    GMA_LAUNCH(KID_SIMT_SCAN, st, (simt_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(agg, tot, L.nseg, KD, causal ? 1 : 0)));
     const int nseg_q = (s.N + SEG - 1) / SEG;
     GMA_LAUNCH(KID_SIMT_OUT, st, (simt_out_kernel<Tin, Tout><<<(unsigned)(BH * nseg_q), THREADS, 0, st>>>(
         gq, gk, V, agg, O, s.N, s.K, s.d_v, nseg_q, L.nseg, s.eps, causal ? 1 : 0)));
     return GMA_OK;
 }
 
+
 }  // namespace
+
+gma_status_t simt_prepare(const gma_shape_t &s, bool causal, const void *QX, const void *KX, const void *V,
+                          const float *mu, const float *raw, const float *logits, float *iv, float *cst, float *gq,
+                          float *gk, float *agg, cudaStream_t st)
+{
+    const int nseg = (s.N + SEG - 1) / SEG;
+    if (s.dtype == GMA_F32)
+        return prepare_typed<float>(s, causal, s.N, (const float *)QX, (const float *)KX, (const float *)V, mu, raw,
+                                    logits, iv, cst, gq, gk, agg, nseg, st);
+    typedef __nv_bfloat16 bf;
+    return prepare_typed<bf>(s, causal, s.N, (const bf *)QX, (const bf *)KX, (const bf *)V, mu, raw, logits, iv, cst,
+                             gq, gk, agg, nseg, st);
+}
 
 size_t simt_workspace_size(const gma_shape_t &s, int variant) { return simt_layout(s, variant).total; }
 

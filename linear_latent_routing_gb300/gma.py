@@ -22,7 +22,7 @@ GMA_FLAG_SIMT = 0x1
 GMA_FLAG_OUT_F32 = 0x2
 GMA_FLAG_RECOMPUTE_KEYS = 0x4
 (GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL, GMA_VARIANT_DECODE,
- GMA_VARIANT_USAGE) = 0, 1, 2, 3, 4
+ GMA_VARIANT_USAGE, GMA_VARIANT_BACKWARD) = 0, 1, 2, 3, 4, 5
 
 
 class gma_shape_t(ctypes.Structure):
@@ -53,6 +53,8 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         fn.restype = ctypes.c_int
+    lib.gma_backward.argtypes = [sp, ctypes.c_int] + [vp] * 14 + [sz, vp]
+    lib.gma_backward.restype = ctypes.c_int
     lib.gma_usage.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_usage.restype = ctypes.c_int
     lib.gma_workspace_size_cross.argtypes = [sp, ctypes.c_int]
@@ -117,6 +119,13 @@ def gma_forward_causal(shape, QX, KX, V, mu, raw_var, prior_logits, O, workspace
                        workspace_bytes, stream):
     return int(_lib.gma_forward_causal(ctypes.byref(shape), QX, KX, V, mu, raw_var,
                                        prior_logits, O, workspace, int(workspace_bytes), stream))
+
+
+def gma_backward(shape, causal, QX, KX, V, mu, raw_var, prior_logits, dO, dQX, dKX, dV, dmu, draw_var,
+                 dprior_logits, workspace, workspace_bytes, stream):
+    return int(_lib.gma_backward(ctypes.byref(shape), int(causal), QX, KX, V, mu, raw_var, prior_logits,
+                                 dO, dQX, dKX, dV, dmu, draw_var, dprior_logits, workspace,
+                                 int(workspace_bytes), stream))
 
 
 def gma_usage(shape, X, mu, raw_var, prior_logits, assign, counts, mass, used, entropy, workspace,
@@ -401,4 +410,39 @@ def usage(X, mu, raw_var, prior_logits, var_floor=1e-3, flags=0, workspace=None,
         if r != GMA_OK:
             raise GmaError(r, "gma_check_workspace")
     return out
+
+
+def backward(QX, KX, V, mu, raw_var, prior_logits, dO, causal, eps=1e-6, var_floor=1e-3, workspace=None,
+             stream=None, check=False):
+    """Gradients of sum(dO * O) for the forward pass with the same arguments (torch CUDA tensors).
+
+    Returns (dQX, dKX, dV, dmu, draw_var, dprior_logits): the first three in the inputs' dtype,
+    the parameter gradients fp32 and summed over the batch.
+    """
+    torch = _torch()
+    for t, n in ((QX, "QX"), (KX, "KX"), (V, "V"), (dO, "dO")):
+        _check(t, n, QX.dtype)
+    for t, n in ((mu, "mu"), (raw_var, "raw_var"), (prior_logits, "prior_logits")):
+        _check(t, n, torch.float32)
+    B, H, N, d_r = QX.shape
+    d_v = V.shape[-1]
+    K = mu.shape[1]
+    if KX.shape != QX.shape or V.shape[:3] != QX.shape[:3] or dO.shape != V.shape:
+        raise ValueError("QX, KX [B,H,N,d_r] and V, dO [B,H,N,d_v] must agree")
+    shape = make_shape(B, H, N, d_r, K, d_v, _dtype_code(QX), eps, var_floor, 0)
+    outs = [torch.empty_like(QX), torch.empty_like(KX), torch.empty_like(V), torch.empty_like(mu),
+            torch.empty_like(raw_var), torch.empty_like(prior_logits)]
+    if workspace is None:
+        workspace = workspace_for(shape, GMA_VARIANT_BACKWARD, QX.device)
+    st = _stream_handle(stream)
+    r = gma_backward(shape, 1 if causal else 0, QX.data_ptr(), KX.data_ptr(), V.data_ptr(), mu.data_ptr(),
+                     raw_var.data_ptr(), prior_logits.data_ptr(), dO.data_ptr(),
+                     *[t.data_ptr() for t in outs], workspace.data_ptr(), workspace.numel(), st)
+    if r != GMA_OK:
+        raise GmaError(r, "gma_backward")
+    if check:
+        r = gma_check_workspace(workspace.data_ptr(), st)
+        if r != GMA_OK:
+            raise GmaError(r, "gma_check_workspace")
+    return tuple(outs)
 

@@ -85,7 +85,13 @@ CROSS = _ws("cross_bf16_b8h16_nq2048_nk16384_dr64_k64_dv64", False, 8, 16, 2048,
 # the long-context head shape: B=1, H=16, N=65536, d_r=64, K=128 (d_v unused).
 USAGE = _ws("usage_bf16_b1h16_n65536_dr64_k128", False, 1, 16, 65536, 64, 128, 16, seed=7)
 
-ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP + (CROSS, USAGE)
+# Backward pass of the LM-shaped causal layer (the page's training path): B=4, H=8, N=2048,
+# d_r=64, K=64, d_v=64, bf16 activations; the output gradient dO is drawn after the inputs from
+# its own generator (seed + 2024), N(0, 1).
+BACKWARD = _ws("backward_causal_bf16_b4h8_n2048_dr64_k64_dv64", True, 4, 8, 2048, 64, 64, 64, seed=8)
+
+ALL_WORKLOADS = (TINY_BIDIR_F32, LM_CAUSAL, LRA_BIDIR, LONG_CAUSAL) + K_SWEEP + N_SWEEP + (CROSS, USAGE,
+                                                                                         BACKWARD)
 
 
 def by_name(name: str) -> Workload:

@@ -154,3 +154,11 @@ def test_usage_workspace_and_validation(g):
     assert g.gma_kernel_family(s, g.GMA_VARIANT_USAGE) == g.gma_kernel_family(s, g.GMA_VARIANT_RESPONSIBILITIES)
     assert g.gma_workspace_size(_shape(g, N=100, K=0), g.GMA_VARIANT_USAGE) == 0
     assert g.gma_usage(s, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == g.GMA_ERR_INVALID_ARG
+
+
+def test_backward_workspace_and_validation(g):
+    s = _shape(g, N=100)
+    assert g.gma_workspace_size(s, g.GMA_VARIANT_BACKWARD) >= 4 * 2 * 3 * 100 * 64 * 4
+    assert g.gma_kernel_family(s, g.GMA_VARIANT_BACKWARD) == 0
+    assert g.gma_backward(s, 0, *([0] * 15), None) == g.GMA_ERR_INVALID_ARG
+    assert g.gma_backward(s, 2, *([0] * 15), None) == g.GMA_ERR_INVALID_ARG
