@@ -715,24 +715,6 @@ struct DecodeArgs {
 
 inline bool persistent_path(const gma_shape_t &s) { return (s.K & 3) == 0; }
 
-// Launch with programmatic stream serialisation: the kernel may start while the parameter kernel
-// ahead of it is still running (it calls grid_dependency_wait before reading the parameters).
-template <typename... Params, typename... Args>
-cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 template <int DV, typename Tin, typename Tout>
 gma_status_t launch_typed(const gma_shape_t &s, const DecodeArgs &a, cudaStream_t st)
 {

@@ -73,6 +73,26 @@ const char *kernel_name(int id);
 void timing_begin(cudaStream_t st, int kernel_id);
 void timing_end(cudaStream_t st);
 
+// Launch with programmatic stream serialisation: the kernel may start once the kernel ahead of
+// it in the stream has let it (griddepcontrol.launch_dependents) or finished; it must execute
+// griddepcontrol.wait before it reads anything that kernel writes.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
+
 // --------------------------------------------------------------- fp32 CUDA-core kernel family
 size_t simt_workspace_size(const gma_shape_t &s, int variant);
 gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const float *mu,

@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
                                                             int d_r, int bimg_bytes, int main_bytes,
                                                             float floor_, WsHeader *hdr)
 {
+    grid_dependency_launch();   // the segment pass may start; it waits for this grid before reading
     const int h = blockIdx.x;
     const int ka = d_r * 2 < 64 ? 64 : d_r * 2;
     const float *lh = logits + (size_t)h * K;
@@ -377,6 +378,8 @@ template <int NB>
 __global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, long long total, int nseg,
                                                       int KD, int causal)
 {
+    grid_dependency_wait();     // the segment memories come from the kernel before
+    grid_dependency_launch();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const long long bh = idx / KD, e = idx % KD;
@@ -671,14 +674,16 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     {
         const unsigned nb = (unsigned)((tot + 255) / 256);
         const int cz = causal ? 1 : 0;
+        cudaError_t e = cudaSuccess;
         if (p.nseg <= 4)
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<4><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<4>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
         else if (p.nseg <= 8)
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<8><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<8>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
         else if (p.nseg <= 20)
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<20><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<20>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
         else
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (tc_scan_kernel<40><<<nb, 256, 0, st>>>(a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<40>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
+        if (e != cudaSuccess) return GMA_ERR_CUDA;
     }
     if (causal) {
         CUtensorMap qmap;

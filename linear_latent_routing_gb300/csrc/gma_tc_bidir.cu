@@ -118,6 +118,7 @@ template <int DR>
 __global__ void __launch_bounds__(BTHREADS, 1) tc_bidir_read2_kernel(const Args a,
                                                                      const __grid_constant__ CUtensorMap qmap)
 {
+    grid_dependency_wait();   // the total memory comes from the kernels before
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const BidirSmem L(DR, a.kn16, a.d_v);
@@ -257,7 +258,10 @@ gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblo
     const uint32_t sm = bidir_read2_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_bidir_read2_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    GMA_LAUNCH(KID_TC_BIDIR_READ, st, (tc_bidir_read2_kernel<DR><<<nblocks, BTHREADS, sm, st>>>(a, qmap)));
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_TC_BIDIR_READ, st,
+               (e = launch_pdl(tc_bidir_read2_kernel<DR>, dim3(nblocks), dim3(BTHREADS), sm, st, a, qmap)));
+    if (e != cudaSuccess) return GMA_ERR_CUDA;
     return GMA_OK;
 }
 

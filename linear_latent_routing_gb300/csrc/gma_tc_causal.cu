@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
                                                                           const __grid_constant__ CUtensorMap kmap,
                                                                           const __grid_constant__ CUtensorMap qmap)
 {
+    grid_dependency_wait();   // the scanned memories come from the kernels before
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const CausalSmem L(DR, a.kn16, a.d_v);
@@ -573,9 +574,11 @@ gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, con
     const uint32_t sm = causal_pipelined_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_causal_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_CAUSAL_OUT, st,
-               (tc_causal_pipelined_kernel<DR><<<nblocks, CTHREADS, sm, st>>>(a, vmap, kmap, qmap)));
-    return GMA_OK;
+               (e = launch_pdl(tc_causal_pipelined_kernel<DR>, dim3(nblocks), dim3(CTHREADS), sm, st, a, vmap, kmap,
+                               qmap)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 template gma_status_t launch_causal_pipelined<16>(const Args &, const CUtensorMap &, const CUtensorMap &,

@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                                                                       const __grid_constant__ CUtensorMap qmap,
                                                                       const __grid_constant__ CUtensorMap gmap)
 {
+    grid_dependency_wait();   // the scanned memories (and, before them, Gamma_K) come from the kernels before
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const GSmem L(DR, a.kn16, a.d_v);
@@ -541,8 +542,10 @@ gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const C
     const uint32_t sm = causal_gamma_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_causal_gamma_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st, (tc_causal_gamma_kernel<DR><<<nblocks, GTHREADS, sm, st>>>(a, vmap, qmap, gmap)));
-    return GMA_OK;
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_TC_CAUSAL_OUT, st,
+               (e = launch_pdl(tc_causal_gamma_kernel<DR>, dim3(nblocks), dim3(GTHREADS), sm, st, a, vmap, qmap, gmap)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 template gma_status_t launch_causal_gamma<16>(const Args &, const CUtensorMap &, const CUtensorMap &,

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
                                                                                   const __grid_constant__ CUtensorMap kmap,
                                                                                   const __grid_constant__ CUtensorMap gmap)
 {
+    grid_dependency_wait();     // the parameter tables come from the kernel before
+    grid_dependency_launch();   // the scan may start (it waits for this grid)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const SegSmem L(DR, a.kn16, a.d_v);
@@ -245,9 +247,11 @@ gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, con
     const uint32_t sm = segmem_pipelined_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_segment_memory_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_CAUSAL_AGG, st,
-               (tc_segment_memory_pipelined_kernel<DR><<<nblocks, STHREADS, sm, st>>>(a, vmap, kmap, gmap)));
-    return GMA_OK;
+               (e = launch_pdl(tc_segment_memory_pipelined_kernel<DR>, dim3(nblocks), dim3(STHREADS), sm, st, a, vmap,
+                               kmap, gmap)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 template gma_status_t launch_segmem_pipelined<16>(const Args &, const CUtensorMap &, const CUtensorMap &,
