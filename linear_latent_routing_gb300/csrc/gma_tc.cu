@@ -318,16 +318,26 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
     bool range_ok = true;
     if (in_table) {
         for (int q = sub; q < ka / 8; q += 8) {
+            // this chunk's raw variances and means, all loaded before any is used
+            float rr[8], mm[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int f = q * 8 + j;
+                const int d = f < d_r ? f : f - d_r;
+                const bool ld = real && f < 2 * d_r;
+                rr[j] = ld ? raw[((size_t)h * K + n) * d_r + d] : 0.f;
+                mm[j] = ld ? mu[((size_t)h * K + n) * d_r + d] : 0.f;
+            }
             uint16_t hv[8];
+#pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int f = q * 8 + j;
                 float val = 0.f;
                 if (real && f < 2 * d_r) {
-                    const int d = f < d_r ? f : f - d_r;
-                    const float r = raw[((size_t)h * K + n) * d_r + d];
+                    const float r = rr[j];
                     const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
                     const float w = 1.0f / var;
-                    const float mv = mu[((size_t)h * K + n) * d_r + d];
+                    const float mv = mm[j];
                     if (f < d_r) {
                         val = -0.5f * w * LOG2E;
                         acc += mv * mv * w + logf(var);
@@ -375,14 +385,16 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
 // time, NB chosen from the segment count) are loaded before any result is stored, so the loads
 // are in flight together.
 template <int NB>
+// KD: floats per segment memory (the stride); KDu: the leading floats that carry components
+// (kn16 rows; the rows beyond are zero in every segment and stay so).
 __global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, long long total, int nseg,
-                                                      int KD, int causal)
+                                                      int KD, int KDu, int causal)
 {
     grid_dependency_wait();     // the segment memories come from the kernel before
     grid_dependency_launch();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
-    const long long bh = idx / KD, e = idx % KD;
+    const long long bh = idx / KDu, e = idx % KDu;
     float *base = agg + bh * nseg * KD + e;
     float run = 0.f;
     for (int s0 = 0; s0 < nseg; s0 += NB) {
@@ -669,20 +681,20 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
         const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, kmap, gmap, BH * p.nseg, st);
         if (r != GMA_OK) return r;
     }
-    const int KD = KMAX * p.ne;
-    const long long tot = (long long)BH * KD;
-    {
+    const int KD = KMAX * p.ne, KDu = p.kn16 * p.ne;
+    const long long tot = (long long)BH * KDu;
+    if (causal || p.nseg > 1) {   // (a bidirectional slice of one segment already holds its total)
         const unsigned nb = (unsigned)((tot + 255) / 256);
         const int cz = causal ? 1 : 0;
         cudaError_t e = cudaSuccess;
         if (p.nseg <= 4)
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<4>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<4>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, cz)));
         else if (p.nseg <= 8)
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<8>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<8>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, cz)));
         else if (p.nseg <= 20)
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<20>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<20>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, cz)));
         else
-            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<40>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, cz)));
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<40>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, cz)));
         if (e != cudaSuccess) return GMA_ERR_CUDA;
     }
     if (causal) {
