@@ -430,6 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t sb = smem_u32(smem);
     float *cst = reinterpret_cast<float *>(smem + L.cst);
+    float *stage = reinterpret_cast<float *>(smem + ((L.total + 127u) & ~127u));   // [C][33]
     bool ok = wait_all(bars.bimg, ph_b, a.hdr, 40);
     uint4 x[DR / 8];
     if (ok) load_x<DR>(a.QX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, x);
@@ -471,20 +472,31 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
             }
         }
         const float inv = 1.0f / s;
-        if (valid) {
-            const long long row = (long long)bh * a.N + base + t;
-            if (a.out_f32) {
-                float *g = (float *)a.gamma + row * a.K;
+        // the tile's rows leave through shared memory, 32 components at a time, so that a warp's
+        // global stores cover whole row segments (one thread per row would scatter them)
+        const long long row0 = (long long)bh * a.N + base;
+        const int nrows = min(C, tok_end - base);
 #pragma unroll
-                for (int k = 0; k < KMAX; ++k)
-                    if (k < a.K) g[k] = v[k] * inv;
-            } else {
-                bf16 *g = (bf16 *)a.gamma + row * a.K;
+        for (int c = 0; c < KMAX / 32; ++c) {
+            if (c < kc) {
 #pragma unroll
-                for (int k = 0; k < KMAX; ++k)
-                    if (k < a.K) g[k] = __float2bfloat16_rn(v[k] * inv);
+                for (int j = 0; j < 32; ++j) stage[t * 33 + j] = v[c * 32 + j] * inv;
+                __syncthreads();
+                const int ncol = min(32, a.K - c * 32);
+                for (int e = t; e < nrows * 32; e += THREADS) {
+                    const int r = e >> 5, j = e & 31;
+                    if (j < ncol) {
+                        const long long at = (row0 + r) * a.K + c * 32 + j;
+                        if (a.out_f32)
+                            ((float *)a.gamma)[at] = stage[r * 33 + j];
+                        else
+                            ((bf16 *)a.gamma)[at] = __float2bfloat16_rn(stage[r * 33 + j]);
+                    }
+                }
+                __syncthreads();
             }
         }
+        (void)valid;
         sync_tc();
     }
     cta_teardown(tmem, 128);
@@ -730,7 +742,8 @@ gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws,
     Args a = make_args(s, p, ws);
     a.QX = (const bf16 *)X;
     a.gamma = gamma;
-    const uint32_t sm = smem_for(Smem(DR, p.kn16, 16, false, true, false).total + 1024, 128);
+    const uint32_t stage = (uint32_t)C * 33u * 4u;   // the output staging tile
+    const uint32_t sm = smem_for(((Smem(DR, p.kn16, 16, false, true, false).total + 127u) & ~127u) + stage + 1024, 128);
     if (!set_smem(tc_resp_kernel<DR>, sm)) return GMA_ERR_CUDA;
     GMA_LAUNCH(KID_TC_RESP, st, (tc_resp_kernel<DR><<<s.B * s.H * p.nseg, THREADS, sm, st>>>(a)));
     return GMA_OK;
