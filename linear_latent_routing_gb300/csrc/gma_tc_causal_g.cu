@@ -17,7 +17,7 @@
 //   S_c    = S_{c-1} + Gamma_K^T V_c                (tensor cores, fp32 in TMEM)
 //   Z_c    = Z_{c-1} + column sums of Gamma_K       (CUDA cores, fp32)
 //
-// Warp roles (416 threads):
+// Warp roles (448 threads):
 //   warps 0-3   mask side:  E_Q of the upper half of the components (see below), then the causal
 //                           mask of P (bf16, back into TMEM as the A operand of tril(P) V) and
 //                           the complete normaliser;
@@ -25,7 +25,9 @@
 //                           the lower half of the components, their row sums and E_Q . Z_{c-1};
 //   warps 8-11  state/out:  the starting memory, Z_c, the bf16 operand copy of S_c, and the
 //                           output rows;
-//   warp 12     control:    TMA of the query rows, Gamma_K and value tiles, and every tcgen05.mma.
+//   warp 12     control:    every tcgen05.mma, each as soon as its inputs are complete;
+//   warp 13     loader:     every TMA load (query rows, Gamma_K and value tiles), each as soon
+//                           as its buffer is free, so that no load waits behind an MMA issue.
 // Tensor memory (512 columns): [0,128) query logits, then E_Q; [128,256) P; [256,384) output
 // numerator; [384,512) the running memory S.  The next chunk's query logits are computed while
 // the current chunk is masked, so the query exponentials are the only long step between chunks;
@@ -41,7 +43,7 @@ namespace tck {
 
 namespace {
 
-constexpr int GTHREADS = 416;
+constexpr int GTHREADS = 448;
 enum GBar {
     G_BIMG, G_V0, G_V1, G_XQ, G_GT,                             // TMA (transaction counts)
     G_AQ, G_XM, G_GQ0, G_GQ1, G_PS0, G_PS1, G_ZP, G_SP, G_OF,   // 128 threads (XM, GQ: 256)
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
     const int hq = (kc + 1) >> 1;   // 32-column groups of E_Q taken by the query side
 
     if (warp == 12) {
-        // ============================================================ control warp
+        // ============================================================ control warp: tcgen05.mma
         if (t == 384) {
             const uint32_t id_p = idesc_f16(128, 128, 1, 1, 0, 0);
             const uint32_t id_o = idesc_f16(128, (uint32_t)d_v, 1, 1, 0, 1);
@@ -296,25 +298,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             const int ksteps = a.kn16 / 16;
             auto eq_col = [&](int s) -> uint32_t { return (uint32_t)(8 * s + (s >= 2 * hq ? 16 * hq : 0)); };
             auto ve = [&](int c) -> uint32_t { return (c & 1) ? L.ve1 : L.ve0; };
-            // TMA loads in flight: the chunk index of the last one issued per buffer (each buffer's
-            // barrier completes one phase per load, and a load is issued only after the previous
-            // one into that buffer was consumed)
-            int last_v0 = -1, last_v1 = -1, last_xq = -1, last_gt = -1, last_pv = -1;
-            bool ok = true;
-            auto load_v = [&](int c) {
-                load_v_chunk(smem + ve(c), &vmap, bars + G_V0 + (c & 1), d_v, tok0 + c * C, bh);
-                if (c & 1) last_v1 = c; else last_v0 = c;
-            };
-            mbar_arrive_expect_tx(bars + G_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + G_BIMG);
-            if (nch > 0) {
-                load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0, bh);
-                load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0, bh);
-                last_xq = last_gt = 0;
-                load_v(0);
-            }
-            if (nch > 1) load_v(1);
-            ok = mbar_wait_abortable(bars + G_BIMG, 0, a.hdr, 100, abort);
+            int last_pv = -1;
+            bool ok = mbar_wait_abortable(bars + G_BIMG, 0, a.hdr, 100, abort);
             const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
             // query logits of chunk cq
             auto query_logits = [&](int cq) -> bool {
@@ -322,13 +307,6 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 tc_fence_after();
                 issue_logits_x<DR>(tmem + R_LQ, sb + L.abq, bimg, bconst, sb + L.ax, a.kn16);
                 mma_commit(bars + G_LQ);
-                return true;
-            };
-            // the query rows of chunk cq, once the logits of chunk cq - 1 are done with the A tile
-            auto stage_queries = [&](int cq) -> bool {
-                if (!mbar_wait_abortable(bars + G_LQ, (cq - 1) & 1, a.hdr, 102, abort)) return false;
-                load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0 + cq * C, bh);
-                last_xq = cq;
                 return true;
             };
             // S += Gamma_K^T V of chunk cc
@@ -339,7 +317,6 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 mma_commit(bars + G_S);
             };
             if (ok && nch > 0) ok = query_logits(0);
-            if (ok && nch > 1) ok = stage_queries(1);
             for (int c = 0; ok && c < nch; ++c) {
                 const uint32_t ph = c & 1;
                 // the S update goes first if its operands are already there (it needs no query)
@@ -353,12 +330,9 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 if (!(ok = mbar_wait_abortable(bars + G_GQ0 + ph, (c >> 1) & 1, a.hdr, 103, abort))) break;
                 if (!(ok = mbar_wait_abortable(bars + G_GT, ph, a.hdr, 104, abort))) break;
                 if (!(ok = mbar_wait_abortable(bars + G_SP, ph, a.hdr, 105, abort))) break;
-                if (c > 0) {
-                    if (!(ok = mbar_wait_abortable(bars + G_PV0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 106,
-                                                   abort)))
-                        break;
-                    if (c + 1 < nch) load_v(c + 1);   // its buffer was read by chunk c - 1
-                }
+                if (c > 0 && !(ok = mbar_wait_abortable(bars + G_PV0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr,
+                                                        106, abort)))
+                    break;
                 tc_fence_after();
                 for (int s = 0; s < ksteps; ++s)   // P = E_Q Gamma_K^T
                     mma_f16_tmem_a(tmem + R_P, tmem + R_LQ + eq_col(s), kdesc(sb + L.gk, s, C), id_p, s > 0);
@@ -373,15 +347,10 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                     if (!(ok = mbar_wait_abortable(bars + G_V0 + ph, (c >> 1) & 1, a.hdr, 108, abort))) break;
                     update(c);
                 }
+                // the next chunk's query logits once E_Q is consumed (they run while P is masked)
                 if (c + 1 < nch) {
-                    // the next chunk's query logits once E_Q is consumed (they run while P is masked)
                     if (!(ok = mbar_wait_abortable(bars + G_PQ, ph, a.hdr, 109, abort))) break;
                     if (!(ok = query_logits(c + 1))) break;
-                    // Gamma_K once P, the S update and the column sums have read it
-                    if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 111, abort))) break;
-                    if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 112, abort))) break;
-                    load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0 + (c + 1) * C, bh);
-                    last_gt = c + 1;
                 }
                 // intra-chunk: O += tril(P) V
                 if (!(ok = mbar_wait_abortable(bars + G_PS0 + ph, (c >> 1) & 1, a.hdr, 110, abort))) break;
@@ -390,11 +359,60 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                     mma_f16_tmem_a(tmem + R_O, tmem + R_P + 8 * s, mn32desc(sb + ve(c), s, C), id_o, 1u);
                 mma_commit(bars + G_PV0 + ph);
                 last_pv = c;
+            }
+            // drain: MMAs complete in issue order, so the last commit covers them all
+            if (last_pv >= 0) mbar_wait(bars + G_PV0 + (last_pv & 1), (last_pv >> 1) & 1, a.hdr, 114);
+        }
+    } else if (warp == 13) {
+        // ============================================================ loader warp: every TMA load
+        if (t == 416) {
+            // TMA loads in flight: the chunk index of the last one issued per buffer (each buffer's
+            // barrier completes one phase per load, and a load is issued only after the previous
+            // one into that buffer was consumed)
+            int last_v0 = -1, last_v1 = -1, last_xq = -1, last_gt = -1;
+            bool ok = true;
+            auto load_v = [&](int c) {
+                load_v_chunk(smem + ((c & 1) ? L.ve1 : L.ve0), &vmap, bars + G_V0 + (c & 1), d_v, tok0 + c * C, bh);
+                if (c & 1) last_v1 = c; else last_v0 = c;
+            };
+            // the query rows of chunk cq, once the logits of chunk cq - 1 are done with the A tile
+            auto stage_queries = [&](int cq) -> bool {
+                if (!mbar_wait_abortable(bars + G_LQ, (cq - 1) & 1, a.hdr, 102, abort)) return false;
+                load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0 + cq * C, bh);
+                last_xq = cq;
+                return true;
+            };
+            mbar_arrive_expect_tx(bars + G_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + G_BIMG);
+            if (nch > 0) {
+                load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0, bh);
+                load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0, bh);
+                last_xq = last_gt = 0;
+                load_v(0);
+            }
+            if (nch > 1) load_v(1);
+            if (nch > 1) ok = stage_queries(1);
+            for (int c = 0; ok && c < nch; ++c) {
+                const uint32_t ph = c & 1;
+                // the value buffer of chunk c - 1 is free once tril(P_{c-1}) V has read it
+                if (c > 0 && c + 1 < nch) {
+                    if (!(ok = mbar_wait_abortable(bars + G_PV0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 116,
+                                                   abort)))
+                        break;
+                    load_v(c + 1);
+                }
+                // Gamma_K of chunk c + 1 once P, the S update and the column sums have read chunk c's
+                if (c + 1 < nch) {
+                    if (!(ok = mbar_wait_abortable(bars + G_PQ, ph, a.hdr, 117, abort))) break;
+                    if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 111, abort))) break;
+                    if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 112, abort))) break;
+                    load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0 + (c + 1) * C, bh);
+                    last_gt = c + 1;
+                }
                 if (c + 2 < nch && !(ok = stage_queries(c + 2))) break;
             }
-            // drain: MMAs complete in issue order, so the last commit covers them all; TMA loads
-            // still in flight (only after a timeout) complete before shared memory is released
-            if (last_pv >= 0) mbar_wait(bars + G_PV0 + (last_pv & 1), (last_pv >> 1) & 1, a.hdr, 114);
+            // TMA loads still in flight (only after a timeout) complete before shared memory is
+            // released
             if (last_v0 >= 0) mbar_wait(bars + G_V0, (last_v0 >> 1) & 1, a.hdr, 115);
             if (last_v1 >= 0) mbar_wait(bars + G_V1, (last_v1 >> 1) & 1, a.hdr, 115);
             if (last_xq >= 0) mbar_wait(bars + G_XQ, last_xq & 1, a.hdr, 115);
