@@ -7,12 +7,13 @@
 // The bidirectional variant sums all segments of a slice; the causal variant scans them into
 // exclusive prefixes, each the starting memory of the chunked kernel's segment.
 //
-// Warp roles (288 threads): two key-side groups of four warps take alternate chunks of 128
+// Warp roles (320 threads): two key-side groups of four warps take alternate chunks of 128
 // tokens ([x^2, x] from the TMA-staged key rows, softmax -> Gamma_K in their own shared-memory
-// tile); warp 8 issues the TMA of the key rows and value tiles and the tcgen05.mma's: the logits
-// into the chunk's own TMEM columns and
-// S += Gamma_K^T [V | 1] into the running memory.  Logits, Gamma_K and value tiles are double
-// buffered, so one group's softmax overlaps the other group's logits and memory update.
+// tile); warp 9 issues the TMA loads of the key rows and value tiles as soon as their buffers are
+// free; warp 8 issues the tcgen05.mma's (the logits into the chunk's own TMEM columns and
+// S += Gamma_K^T [V | 1] into the running memory) and the stores of Gamma_K.  Logits, Gamma_K
+// and value tiles are double buffered, so one group's softmax overlaps the other group's logits
+// and memory update.
 // Barriers are per buffer, so no waiter can fall two phases behind.
 // For the causal variant the kernel also stores each chunk's Gamma_K tile (bf16, normalised) to
 // the workspace with a TMA store, so that the output pass reads it instead of recomputing it.
@@ -23,7 +24,7 @@ namespace tck {
 
 namespace {
 
-constexpr int STHREADS = 288;
+constexpr int STHREADS = 320;
 enum SBar { S_BIMG, S_AK, S_LK0, S_LK1, S_GK0, S_GK1, S_SD0, S_SD1, S_V0, S_V1, S_XK, S_NBAR };
 constexpr uint32_t SR_L0 = 0, SR_L1 = 128, SR_S = 256;
 
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
         }
         __syncwarp();
         tmem_alloc(tslot, 512);
-    } else {
+    } else if (warp < 8) {
         // zero both Gamma_K tiles (components the softmax never writes), ones blocks of [V | 1],
         // and the constant operand (1, 1, 0, ...) of the logits
         const int u = t;   // 0..255
@@ -111,26 +112,13 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
     const uint32_t sb = smem_u32(smem);
 
     if (warp == 8) {
-        // ============================================================ control warp
+        // ============================================================ control warp: MMAs, stores
         if (t == 256) {
             auto ve = [&](int c) { return (c & 1) ? L.ve1 : L.ve0; };
             auto gk = [&](int c) { return (c & 1) ? L.gk1 : L.gk0; };
             const uint32_t id_s = idesc_f16(128, (uint32_t)ne, 1, 1, 1, 1);
-            bool ok = true;
+            bool ok = mbar_wait_abortable(bars + S_BIMG, 0, a.hdr, 80, abort);
             int last_sd = -1;
-            bool vpend0 = false, vpend1 = false;
-            mbar_arrive_expect_tx(bars + S_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + S_BIMG);
-            for (int c = 0; c < 2 && c < nch; ++c) {
-                load_v_chunk(smem + ve(c), &vmap, bars + S_V0 + c, d_v, tok0 + c * C, bh);
-                if (c) vpend1 = true; else vpend0 = true;
-            }
-            int last_xk = -1;
-            if (nch > 0) {
-                load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0, bh);
-                last_xk = 0;
-            }
-            ok = mbar_wait_abortable(bars + S_BIMG, 0, a.hdr, 80, abort);
             const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
             // S update of chunk j: Gamma_K tile and value tile of buffer j & 1 (and the store of the
             // tile; its buffer is released with the update's commit once the store has read it)
@@ -138,7 +126,6 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
                 const int g = j & 1, n = j >> 1;
                 if (!mbar_wait_abortable(bars + S_GK0 + g, n & 1, a.hdr, 81, abort)) return false;
                 if (!mbar_wait_abortable(bars + S_V0 + g, n & 1, a.hdr, 82, abort)) return false;
-                if (g) vpend1 = false; else vpend0 = false;
                 if (a.gam) {
                     for (int h = 0; h < a.kg / 64; ++h)
                         tma_store_3d(&gmap, smem + gk(j) + h * C * 128, 64 * h, tok0 + j * C, bh);
@@ -156,32 +143,52 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             for (int c = 0; ok && c < nch; ++c) {
                 const int g = c & 1;
                 if (!(ok = mbar_wait_abortable(bars + S_AK, c & 1, a.hdr, 83, abort))) break;
-                if (c + 1 < nch) {   // the staged rows of chunk c have been read
-                    load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0 + (c + 1) * C, bh);
-                    last_xk = c + 1;
-                }
                 tc_fence_after();
                 issue_logits_c<DR>(tmem + (g ? SR_L1 : SR_L0), sb + L.abuf, bimg, bconst, sb + L.ax, a.kn16);
                 mma_commit(bars + S_LK0 + g);
-                if (c >= 1) {
-                    if (!(ok = update(c - 1))) break;
-                    // the value buffer of chunk c-1 is free once its update is done: load chunk c+1
-                    if (c + 1 < nch) {
-                        if (!(ok = mbar_wait_abortable(bars + S_SD0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 84, abort)))
-                            break;
-                        load_v_chunk(smem + ve(c + 1), &vmap, bars + S_V0 + ((c + 1) & 1), d_v, tok0 + (c + 1) * C, bh);
-                        if ((c + 1) & 1) vpend1 = true; else vpend0 = true;
-                    }
-                }
+                if (c >= 1 && !(ok = update(c - 1))) break;
             }
             if (ok && nch > 0) ok = update(nch - 1);
             if (last_sd >= 0) mbar_wait(bars + S_SD0 + (last_sd & 1), (last_sd >> 1) & 1, a.hdr, 85);
-            if (last_xk >= 0) mbar_wait(bars + S_XK, last_xk & 1, a.hdr, 86);
             if (a.gam) bulk_wait_all();
-            if (vpend0 || vpend1) {
-                for (int c = nch - 1; c >= 0 && c >= nch - 2; --c)
-                    if ((c & 1) ? vpend1 : vpend0) mbar_wait(bars + S_V0 + (c & 1), (c >> 1) & 1, a.hdr, 86);
+        }
+    } else if (warp == 9) {
+        // ============================================================ loader warp: TMA loads
+        if (t == 288) {
+            auto ve = [&](int c) { return (c & 1) ? L.ve1 : L.ve0; };
+            bool ok = true;
+            bool vpend0 = false, vpend1 = false;   // loads whose update has not been seen yet
+            int vlast0 = -1, vlast1 = -1, last_xk = -1;
+            auto load_v = [&](int c) {
+                load_v_chunk(smem + ve(c), &vmap, bars + S_V0 + (c & 1), d_v, tok0 + c * C, bh);
+                if (c & 1) { vpend1 = true; vlast1 = c; } else { vpend0 = true; vlast0 = c; }
+            };
+            mbar_arrive_expect_tx(bars + S_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + S_BIMG);
+            for (int c = 0; c < 2 && c < nch; ++c) load_v(c);
+            if (nch > 0) {
+                load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0, bh);
+                last_xk = 0;
             }
+            for (int c = 0; ok && c < nch; ++c) {
+                if (c + 1 < nch) {   // the staged rows of chunk c have been read into its A tile
+                    if (!(ok = mbar_wait_abortable(bars + S_AK, c & 1, a.hdr, 87, abort))) break;
+                    load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0 + (c + 1) * C, bh);
+                    last_xk = c + 1;
+                }
+                // the value buffer of chunk c - 1 is free once its update is done: load chunk c + 1
+                if (c >= 1 && c + 1 < nch) {
+                    if (!(ok = mbar_wait_abortable(bars + S_SD0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 84,
+                                                   abort)))
+                        break;
+                    if ((c - 1) & 1) vpend1 = false; else vpend0 = false;
+                    load_v(c + 1);
+                }
+            }
+            // loads still in flight (only after a timeout) complete before shared memory is released
+            if (last_xk >= 0) mbar_wait(bars + S_XK, last_xk & 1, a.hdr, 86);
+            if (vpend0 && vlast0 >= 0) mbar_wait(bars + S_V0, (vlast0 >> 1) & 1, a.hdr, 86);
+            if (vpend1 && vlast1 >= 0) mbar_wait(bars + S_V1, (vlast1 >> 1) & 1, a.hdr, 86);
         }
     } else {
         // ============================================================ key-side groups
