@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const Smem L(DR, a.kn16, 16, false, true, false);
+    const Smem L(DR, a.kn16, 16, false, false, false);
     const int ntile = a.nseg;
     const int bh = blockIdx.x / ntile, grp = blockIdx.x % ntile, h = bh % a.H;
     const int t = threadIdx.x, warp = t >> 5;
@@ -446,55 +446,56 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
         if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 41))) break;
         const int nb = base + C;
         load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, x);
-        // softmax in registers, then store K values of this row
-        float v[KMAX];
+        // softmax over the row in three passes over TMEM, 32 components at a time (the maximum,
+        // the sum, then the normalised values), so no thread holds the whole row in registers
         float m = NEG_BIG;
+#pragma unroll 1
+        for (int c = 0; c < kc; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + c * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < KMAX / 32; ++c) {
-            if (c < kc) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + c * 32, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int k = c * 32 + j;
-                    v[k] = k < a.K ? __uint_as_float(r[j]) + cst[k] : NEG_BIG;
-                    m = fmaxf(m, v[k]);
-                }
-            }
+            for (int j = 0; j < 32; ++j)
+                if (c * 32 + j < a.K) m = fmaxf(m, __uint_as_float(r[j]) + cst[c * 32 + j]);
         }
         float s = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kc; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + c * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < KMAX; ++k) {
-            if ((k >> 5) < kc) {
-                v[k] = k < a.K ? ex2(v[k] - m) : 0.f;
-                s += v[k];
-            }
+            for (int j = 0; j < 32; ++j)
+                if (c * 32 + j < a.K) s += ex2(__uint_as_float(r[j]) + cst[c * 32 + j] - m);
         }
         const float inv = 1.0f / s;
         // the tile's rows leave through shared memory, 32 components at a time, so that a warp's
         // global stores cover whole row segments (one thread per row would scatter them)
         const long long row0 = (long long)bh * a.N + base;
         const int nrows = min(C, tok_end - base);
+#pragma unroll 1
+        for (int c = 0; c < kc; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + c * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < KMAX / 32; ++c) {
-            if (c < kc) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) stage[t * 33 + j] = v[c * 32 + j] * inv;
-                __syncthreads();
-                const int ncol = min(32, a.K - c * 32);
-                for (int e = t; e < nrows * 32; e += THREADS) {
-                    const int r = e >> 5, j = e & 31;
-                    if (j < ncol) {
-                        const long long at = (row0 + r) * a.K + c * 32 + j;
-                        if (a.out_f32)
-                            ((float *)a.gamma)[at] = stage[r * 33 + j];
-                        else
-                            ((bf16 *)a.gamma)[at] = __float2bfloat16_rn(stage[r * 33 + j]);
-                    }
-                }
-                __syncthreads();
+            for (int j = 0; j < 32; ++j) {
+                const int k = c * 32 + j;
+                stage[t * 33 + j] = k < a.K ? ex2(__uint_as_float(r[j]) + cst[k] - m) * inv : 0.f;
             }
+            __syncthreads();
+            const int ncol = min(32, a.K - c * 32);
+            for (int e = t; e < nrows * 32; e += THREADS) {
+                const int rr = e >> 5, j = e & 31;
+                if (j < ncol) {
+                    const long long at = (row0 + rr) * a.K + c * 32 + j;
+                    if (a.out_f32)
+                        ((float *)a.gamma)[at] = stage[rr * 33 + j];
+                    else
+                        ((bf16 *)a.gamma)[at] = __float2bfloat16_rn(stage[rr * 33 + j]);
+                }
+            }
+            __syncthreads();
         }
         (void)valid;
         sync_tc();
@@ -560,7 +561,14 @@ Plan make_plan(const gma_shape_t &s, int variant)
     // CTAs x (set-up + chunks per segment), with the set-up (operand tables, start memory, the
     // first chunk's loads) worth about 0.6 chunk; the cheapest split wins (the larger one on a
     // tie).
-    {
+    if (variant == GMA_VARIANT_RESPONSIBILITIES) {
+        // up to four CTAs per SM (128 TMEM columns each): about four per SM in one wave
+        int n = (4 * kSms + BH - 1) / BH;
+        if (n > nchunks) n = nchunks;
+        if (n < 1) n = 1;
+        p.cps = (nchunks + n - 1) / n;
+        p.nseg = (nchunks + p.cps - 1) / p.cps;
+    } else {
         double best = 1e30;
         int best_n = 1;
         const int top = nchunks < 2048 ? nchunks : 2048;
@@ -743,7 +751,7 @@ gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws,
     a.QX = (const bf16 *)X;
     a.gamma = gamma;
     const uint32_t stage = (uint32_t)C * 33u * 4u;   // the output staging tile
-    const uint32_t sm = smem_for(((Smem(DR, p.kn16, 16, false, true, false).total + 127u) & ~127u) + stage + 1024, 128);
+    const uint32_t sm = smem_for(((Smem(DR, p.kn16, 16, false, false, false).total + 127u) & ~127u) + stage + 1024, 128);
     if (!set_smem(tc_resp_kernel<DR>, sm)) return GMA_ERR_CUDA;
     GMA_LAUNCH(KID_TC_RESP, st, (tc_resp_kernel<DR><<<s.B * s.H * p.nseg, THREADS, sm, st>>>(a)));
     return GMA_OK;
