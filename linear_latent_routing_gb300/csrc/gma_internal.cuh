@@ -136,6 +136,12 @@ gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *
                         const void *V, const float *mu, const float *raw, const float *logits,
                         void *O, void *ws, cudaStream_t st);
 size_t tc_workspace_size_cross(const gma_shape_t &s, int n_k);
+// Usage diagnostics fused into the tensor-core responsibilities pass: per row the argmax, the
+// per-head histogram (atomic adds into counts, zeroed by the caller), and per-CTA sums of the
+// responsibilities mass_part [B*H*tc_usage_blocks(s)][K] (CTA = slice * blocks + block).
+int tc_usage_blocks(const gma_shape_t &s);
+gma_status_t tc_usage(const gma_shape_t &s, const void *X, const float *mu, const float *raw, const float *logits,
+                      int *assign, int *counts, float *mass_part, void *ws, cudaStream_t st);
 
 }  // namespace gma
 

@@ -431,6 +431,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
     const uint32_t sb = smem_u32(smem);
     float *cst = reinterpret_cast<float *>(smem + L.cst);
     float *stage = reinterpret_cast<float *>(smem + ((L.total + 127u) & ~127u));   // [C][33]
+    // usage diagnostics: histogram and column sums of this CTA's rows
+    const bool usage = a.assign != nullptr;
+    int *hist = reinterpret_cast<int *>(stage + C * 33);
+    float *msum = reinterpret_cast<float *>(hist + KMAX);
+    if (usage) {
+        for (int k = t; k < KMAX; k += THREADS) {
+            hist[k] = 0;
+            msum[k] = 0.f;
+        }
+        __syncthreads();
+    }
     bool ok = wait_all(bars.bimg, ph_b, a.hdr, 40);
     uint4 x[DR / 8];
     if (ok) load_x<DR>(a.QX, (long long)bh * a.N + tok0 + t, tok0 + t < tok_end, x);
@@ -449,6 +460,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
         // softmax over the row in three passes over TMEM, 32 components at a time (the maximum,
         // the sum, then the normalised values), so no thread holds the whole row in registers
         float m = NEG_BIG;
+        int arg = 0;   // the first component of largest responsibility
 #pragma unroll 1
         for (int c = 0; c < kc; ++c) {
             uint32_t r[32];
@@ -456,7 +468,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (c * 32 + j < a.K) m = fmaxf(m, __uint_as_float(r[j]) + cst[c * 32 + j]);
+                if (c * 32 + j < a.K) {
+                    const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
+                    if (l > m) {
+                        m = l;
+                        arg = c * 32 + j;
+                    }
+                }
+        }
+        if (usage && valid) {
+            a.assign[(long long)bh * a.N + base + t] = arg;
+            atomicAdd(&hist[arg], 1);
         }
         float s = 0.f;
 #pragma unroll 1
@@ -485,20 +507,35 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
             }
             __syncthreads();
             const int ncol = min(32, a.K - c * 32);
-            for (int e = t; e < nrows * 32; e += THREADS) {
-                const int rr = e >> 5, j = e & 31;
-                if (j < ncol) {
-                    const long long at = (row0 + rr) * a.K + c * 32 + j;
-                    if (a.out_f32)
-                        ((float *)a.gamma)[at] = stage[rr * 33 + j];
-                    else
-                        ((bf16 *)a.gamma)[at] = __float2bfloat16_rn(stage[rr * 33 + j]);
+            if (usage) {
+                // column sums of the tile (rows beyond the sequence hold zeros), one warp
+                if (t < 32) {
+                    float cs = 0.f;
+                    for (int rr = 0; rr < nrows; ++rr) cs += stage[rr * 33 + t];
+                    msum[c * 32 + t] += cs;
+                }
+            } else {
+                for (int e = t; e < nrows * 32; e += THREADS) {
+                    const int rr = e >> 5, j = e & 31;
+                    if (j < ncol) {
+                        const long long at = (row0 + rr) * a.K + c * 32 + j;
+                        if (a.out_f32)
+                            ((float *)a.gamma)[at] = stage[rr * 33 + j];
+                        else
+                            ((bf16 *)a.gamma)[at] = __float2bfloat16_rn(stage[rr * 33 + j]);
+                    }
                 }
             }
             __syncthreads();
         }
-        (void)valid;
         sync_tc();
+    }
+    if (usage) {
+        __syncthreads();
+        for (int k = t; k < a.K; k += THREADS) {
+            if (hist[k]) atomicAdd(&a.counts[(size_t)h * a.K + k], hist[k]);
+            a.mass_part[(size_t)blockIdx.x * a.K + k] = msum[k];
+        }
     }
     cta_teardown(tmem, 128);
 }
@@ -745,12 +782,15 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
 
 template <int DR>
 gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws, const Plan &p,
-                     cudaStream_t st)
+                     cudaStream_t st, int *assign = nullptr, int *counts = nullptr, float *mass_part = nullptr)
 {
     Args a = make_args(s, p, ws);
     a.QX = (const bf16 *)X;
     a.gamma = gamma;
-    const uint32_t stage = (uint32_t)C * 33u * 4u;   // the output staging tile
+    a.assign = assign;
+    a.counts = counts;
+    a.mass_part = mass_part;
+    const uint32_t stage = (uint32_t)C * 33u * 4u + KMAX * 8u;   // the staging tile; usage sums
     const uint32_t sm = smem_for(((Smem(DR, p.kn16, 16, false, false, false).total + 127u) & ~127u) + stage + 1024, 128);
     if (!set_smem(tc_resp_kernel<DR>, sm)) return GMA_ERR_CUDA;
     GMA_LAUNCH(KID_TC_RESP, st, (tc_resp_kernel<DR><<<s.B * s.H * p.nseg, THREADS, sm, st>>>(a)));
@@ -786,6 +826,27 @@ gma_status_t tc_responsibilities(const gma_shape_t &s, const void *X, const floa
     case 16: return tck::resp_dr<16>(s, X, gamma, w, p, st);
     case 32: return tck::resp_dr<32>(s, X, gamma, w, p, st);
     case 64: return tck::resp_dr<64>(s, X, gamma, w, p, st);
+    }
+    return GMA_ERR_UNSUPPORTED_SHAPE;
+}
+
+int tc_usage_blocks(const gma_shape_t &s)
+{
+    const tck::Plan p = tck::make_plan(s, GMA_VARIANT_RESPONSIBILITIES);
+    return p.nseg;
+}
+
+gma_status_t tc_usage(const gma_shape_t &s, const void *X, const float *mu, const float *raw, const float *logits,
+                      int *assign, int *counts, float *mass_part, void *ws, cudaStream_t st)
+{
+    const tck::Plan p = tck::make_plan(s, GMA_VARIANT_RESPONSIBILITIES);
+    char *w = (char *)ws;
+    gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
+    if (r != GMA_OK) return r;
+    switch (s.d_r) {
+    case 16: return tck::resp_dr<16>(s, X, nullptr, w, p, st, assign, counts, mass_part);
+    case 32: return tck::resp_dr<32>(s, X, nullptr, w, p, st, assign, counts, mass_part);
+    case 64: return tck::resp_dr<64>(s, X, nullptr, w, p, st, assign, counts, mass_part);
     }
     return GMA_ERR_UNSUPPORTED_SHAPE;
 }

@@ -9,10 +9,11 @@
 //   used[h]         = #{k : counts[h][k] > 0}
 //   entropy[h]      = -sum_k p_k ln p_k / ln K,  p = counts[h] / (B N)   (0 for K = 1)
 //
-// Steps: the responsibilities (fp32) by the same kernel family gma_responsibilities uses, into
-// the workspace; one pass over them (a warp per token row: argmax by shuffles, a shared-memory
-// histogram per block, per-block partial masses); a fixed-order reduction of the partial masses;
-// per-head used count and entropy.  Counts are integer sums, so the order of the atomic
+// Steps, tensor-core family: the responsibilities pass itself keeps each row's argmax, a shared-
+// memory histogram and the column sums of its tiles (no responsibilities reach HBM).  CUDA-core
+// family: the responsibilities (fp32) into the workspace, then one pass over them (a warp per
+// token row: argmax by shuffles, a shared-memory histogram per block, per-block partial masses).
+// Both: a fixed-order reduction of the partial masses; per-head used count and entropy.  Counts are integer sums, so the order of the atomic
 // additions does not matter; the masses are summed in a fixed order, so results repeat exactly.
 #include "gma_internal.cuh"
 
@@ -150,6 +151,7 @@ __global__ void usage_stats_kernel(const int *__restrict__ counts, int *__restri
 struct UsageLayout {
     size_t gamma, part, total;
     int nblk;
+    bool fused;       // tensor-core family: diagnostics in the responsibilities pass itself
     gma_shape_t rs;   // the responsibilities call: fp32 output
 };
 
@@ -158,14 +160,15 @@ UsageLayout usage_layout(const gma_shape_t &s)
     UsageLayout L{};
     L.rs = s;
     L.rs.flags |= GMA_FLAG_OUT_F32;
-    L.nblk = (s.N + UROWS - 1) / UROWS;
+    L.fused = tc_supported(L.rs, GMA_VARIANT_RESPONSIBILITIES);
+    L.nblk = L.fused ? tc_usage_blocks(L.rs) : (s.N + UROWS - 1) / UROWS;
     // the responsibilities' own workspace first, so its header is this call's header
-    const size_t resp = tc_supported(L.rs, GMA_VARIANT_RESPONSIBILITIES)
-                            ? tc_workspace_size(L.rs, GMA_VARIANT_RESPONSIBILITIES)
-                            : simt_workspace_size(L.rs, GMA_VARIANT_RESPONSIBILITIES);
+    const size_t resp = L.fused ? tc_workspace_size(L.rs, GMA_VARIANT_RESPONSIBILITIES)
+                                : simt_workspace_size(L.rs, GMA_VARIANT_RESPONSIBILITIES);
     size_t off = (resp + 255) & ~(size_t)255;
     L.gamma = off;
-    off += ((size_t)s.B * s.H * s.N * s.K * sizeof(float) + 255) & ~(size_t)255;
+    if (!L.fused)   // the CUDA-core family writes the responsibilities, then a pass reads them
+        off += ((size_t)s.B * s.H * s.N * s.K * sizeof(float) + 255) & ~(size_t)255;
     L.part = off;
     off += ((size_t)s.B * s.H * L.nblk * s.K * sizeof(float) + 255) & ~(size_t)255;
     L.total = off;
@@ -193,13 +196,14 @@ gma_status_t usage(const gma_shape_t &s, const void *X, const float *mu, const f
     char *w = (char *)ws;
     float *gamma = (float *)(w + L.gamma);
     float *part = (float *)(w + L.part);
-    gma_status_t r = tc_supported(L.rs, GMA_VARIANT_RESPONSIBILITIES)
-                         ? tc_responsibilities(L.rs, X, mu, raw, logits, gamma, ws, st)
-                         : simt_responsibilities(L.rs, X, mu, raw, logits, gamma, ws, st);
-    if (r != GMA_OK) return r;
     if (cudaMemsetAsync(counts, 0, sizeof(int) * (size_t)s.H * s.K, st) != cudaSuccess) return GMA_ERR_CUDA;
+    gma_status_t r = GMA_OK;
     const int kpl = (s.K + 31) / 32;
-    if (kpl <= 1) r = launch_rows<1>(gamma, assign, counts, part, s, L.nblk, st);
+    if (L.fused)
+        r = tc_usage(L.rs, X, mu, raw, logits, assign, counts, part, ws, st);
+    else if ((r = simt_responsibilities(L.rs, X, mu, raw, logits, gamma, ws, st)) != GMA_OK)
+        return r;
+    else if (kpl <= 1) r = launch_rows<1>(gamma, assign, counts, part, s, L.nblk, st);
     else if (kpl <= 2) r = launch_rows<2>(gamma, assign, counts, part, s, L.nblk, st);
     else if (kpl <= 4) r = launch_rows<4>(gamma, assign, counts, part, s, L.nblk, st);
     else if (kpl <= 8) r = launch_rows<8>(gamma, assign, counts, part, s, L.nblk, st);

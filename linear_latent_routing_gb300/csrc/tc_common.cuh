@@ -35,6 +35,9 @@ struct Args {
     const bf16 *QX, *KX;
     void *O;                 // output (bf16 or fp32)
     void *gamma;             // responsibilities output (bf16 or fp32)
+    int *assign;             // usage diagnostics (non-null: no gamma written): argmax per row,
+    int *counts;             //   per-head histogram [H][K] (atomic adds), and per-CTA sums of
+    float *mass_part;        //   the responsibilities [grid][K]
     const uint8_t *bimg;     // per-head Gaussian table image [H][bimg_bytes]: the [x^2, x] part
                              // (bimg_main_bytes), then the constant part (kn16 rows x 32 B)
     const float *cst;        // per-head log2-domain constants [H][kn16]
