@@ -31,10 +31,10 @@
 // Tensor memory (512 columns): [0,128) query logits, then E_Q; [128,256) P; [256,384) output
 // numerator; [384,512) the running memory S.  The next chunk's query logits are computed while
 // the current chunk is masked, so the query exponentials are the only long step between chunks;
-// two warps share each row of them (both take the row maximum, each exponentiates one half of
-// the components).  E_Q of 32-column group g (of kc groups, h = ceil(kc / 2) in the lower half)
-// is packed into 16 columns at 16 g (g < h) or 16 h + 16 g (g >= h): each half writes only
-// columns it has already read.
+// two warps share each row of them: each takes the maximum of one half of the components'
+// logits, the two half-row maxima are exchanged, and each exponentiates its half.  E_Q of 32-column group g (of kc groups, h = ceil(kc / 2) in the lower half) is
+// packed into 16 columns at 16 g (g < h) or 16 h + 16 g (g >= h), after both halves have read
+// all of their logits.
 // Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all roles leave their loops.
 #include "tc_rows.cuh"
 
@@ -93,41 +93,58 @@ __device__ __forceinline__ void load_g_tile(uint8_t *gk, const CUtensorMap *map,
             : "memory");
 }
 
-// Query rows: unnormalised E_Q of this row over the 32-column groups [g0, g1) (zeros when not
-// valid) back into TMEM at tl as bf16 pairs (group g at column 16 g + (g >= h ? 16 h : 0));
-// returns (row sum of the fp32 values, their dot product with z = Z_{c-1}).  m: the row maximum
-// over all groups; the caller waits for z (on `zbar`) only after computing it.
-__device__ __forceinline__ float2 query_exp_half(uint32_t tl, int K, int g0, int g1, int h, float m, bool valid,
-                                                 const float *z)
+// Query rows: the maximum of this row's logits over the 32-column groups [g0, g1) and the columns
+// below K (one group per wait: holding two groups at once would not fit the register budget).
+__device__ __forceinline__ float query_max_half(uint32_t tl, int K, int g0, int g1)
 {
-    const float sc = valid ? 1.f : 0.f;
-    const float4 *z4 = reinterpret_cast<const float4 *>(z);
-    float srow = 0.f, den = 0.f;
+    float m[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m[u] = NEG_BIG;
 #pragma unroll 1
     for (int c = g0; c < g1; ++c) {
-        {
-            uint32_t r[32];
-            tmem_ld32(tl + 32 * c, r);
-            tmem_ld_wait();
-            srow += chunk_exp(r, c, K, m);
-            float d4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
+        tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 zz = z4[8 * c + q];
-                d4[0] = fmaf(__uint_as_float(r[4 * q]), zz.x, d4[0]);
-                d4[1] = fmaf(__uint_as_float(r[4 * q + 1]), zz.y, d4[1]);
-                d4[2] = fmaf(__uint_as_float(r[4 * q + 2]), zz.z, d4[2]);
-                d4[3] = fmaf(__uint_as_float(r[4 * q + 3]), zz.w, d4[3]);
-            }
-            den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = pk2(r[2 * j], r[2 * j + 1], sc);
-            tmem_st16(tl + 16 * c + (c >= h ? 16 * h : 0), w);   // E_Q (bf16 pairs)
-        }
+        for (int j = 0; j < 32; ++j)
+            if ((c + 1) * 32 <= K || 32 * c + j < K) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(r[j]));
     }
-    tmem_st_wait();
-    return make_float2(srow, den);
+    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+// Four consecutive floats of shared memory, read in program order with respect to the other
+// inline-assembly statements (so that the loads of one group are not hoisted above the previous
+// group's tensor-memory store, which would keep both groups' values live at once).
+__device__ __forceinline__ float4 lds4_ordered(const float *p)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
+// Query rows: unnormalised E_Q = exp2(L - m) of one 32-column group c held in r, zero beyond K,
+// back into TMEM at tl as bf16 pairs (group c at column 16 c + (c >= h ? 16 h : 0)); adds the
+// group's sum and its dot product with z = Z_{c-1} to *srow and *den.
+__device__ __forceinline__ void query_exp_group(uint32_t tl, int K, int c, int h, float m, uint32_t (&r)[32],
+                                                const float *z, float &srow, float &den)
+{
+    srow += chunk_exp(r, c, K, m);
+    float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 zz = lds4_ordered(z + 32 * c + 4 * q);
+        d4[0] = fmaf(__uint_as_float(r[4 * q]), zz.x, d4[0]);
+        d4[1] = fmaf(__uint_as_float(r[4 * q + 1]), zz.y, d4[1]);
+        d4[2] = fmaf(__uint_as_float(r[4 * q + 2]), zz.z, d4[2]);
+        d4[3] = fmaf(__uint_as_float(r[4 * q + 3]), zz.w, d4[3]);
+    }
+    den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    tmem_st16(tl + 16 * c + (c >= h ? 16 * h : 0), w);   // E_Q (bf16 pairs)
 }
 
 // Mask side: row i of P (fp32 in TMEM at tl) masked to columns j <= i, written back as bf16
@@ -437,15 +454,26 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             // E_Q: the row maximum from both halves, then each half's exponentials
             if (!mbar_wait_abortable(bars + G_LQ, ph, a.hdr, 131, abort)) break;
             tc_fence_after();
-            const float mh = row_max_groups(lane + R_LQ, a.K, g0, g1);
+            const float mh = query_max_half(lane + R_LQ, a.K, g0, g1);
             xmax[(qs ? 0 : 2 * C) + ph * C + i] = mh;
             tc_fence_before();
             mbar_arrive(bars + G_XM);
             if (!mbar_spin_wait(bars + G_XM, ph, a.hdr, 134, abort)) break;
             tc_fence_after();
-            const float m = fmaxf(mh, xmax[(qs ? 2 * C : 0) + ph * C + i]);
+            const float m = valid ? fmaxf(mh, xmax[(qs ? 2 * C : 0) + ph * C + i]) : __int_as_float(0x7f800000);
             if (!mbar_wait_abortable(bars + G_SP, ph, a.hdr, 132, abort)) break;
-            const float2 part = query_exp_half(lane + R_LQ, a.K, g0, g1, hq, m, valid, zbuf + ph * KMAX);
+            // E_Q of this half, one group per wait: a row past the end of the sequence has
+            // m = +inf, so all of its values are exp2(-inf) = 0; both halves have read all of
+            // their logits before either writes (the maxima were exchanged in between)
+            float2 part = make_float2(0.f, 0.f);
+#pragma unroll 1
+            for (int c = g0; c < g1; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane + R_LQ + 32 * c, r);
+                tmem_ld_wait();
+                query_exp_group(lane + R_LQ, a.K, c, hq, m, r, zbuf + ph * KMAX, part.x, part.y);
+            }
+            tmem_st_wait();
             if (qs) dsq[ph * C + i] = part;
             tc_fence_before();
             mbar_arrive(bars + G_GQ0 + ph);

@@ -32,24 +32,6 @@ __device__ __forceinline__ float row_max(uint32_t taddr, int K, int kc)
     return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
-// Row maximum over the 32-column groups [g0, g1) of the first K columns (NEG_BIG if empty).
-__device__ __forceinline__ float row_max_groups(uint32_t taddr, int K, int g0, int g1)
-{
-    float m[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) m[u] = NEG_BIG;
-#pragma unroll 1
-    for (int c = g0; c < g1; ++c) {
-        uint32_t ra[32];
-        tmem_ld32(taddr + 32 * c, ra);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if ((c + 1) * 32 <= K || 32 * c + j < K) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(ra[j]));
-    }
-    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-}
-
 // exp2(L - m) of one chunk of 32 columns (0 beyond K), in place; returns the chunk's sum.
 __device__ __forceinline__ float chunk_exp(uint32_t (&r)[32], int c, int K, float m)
 {
