@@ -467,11 +467,11 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             // their logits before either writes (the maxima were exchanged in between)
             float2 part = make_float2(0.f, 0.f);
 #pragma unroll 1
-            for (int c = g0; c < g1; ++c) {
+            for (int gq = g0; gq < g1; ++gq) {
                 uint32_t r[32];
-                tmem_ld32(lane + R_LQ + 32 * c, r);
+                tmem_ld32(lane + R_LQ + 32 * gq, r);
                 tmem_ld_wait();
-                query_exp_group(lane + R_LQ, a.K, c, hq, m, r, zbuf + ph * KMAX, part.x, part.y);
+                query_exp_group(lane + R_LQ, a.K, gq, hq, m, r, zbuf + ph * KMAX, part.x, part.y);
             }
             tmem_st_wait();
             if (qs) dsq[ph * C + i] = part;
