@@ -584,7 +584,7 @@ struct Plan {
 
 constexpr int kSms = 152;   // GB300
 
-Plan make_plan(const gma_shape_t &s, int variant)
+Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1)
 {
     Plan p{};
     p.kn16 = (s.K + 15) / 16 * 16;
@@ -594,8 +594,8 @@ Plan make_plan(const gma_shape_t &s, int variant)
     p.bimg_bytes = p.bimg_main_bytes + 32 * p.kn16;
     const int BH = s.B * s.H;
     const int nchunks = (s.N + C - 1) / C;
-    // Segments per slice: one CTA per segment, one CTA per SM at a time.  Time model: waves of
-    // CTAs x (set-up + chunks per segment), with the set-up (operand tables, start memory, the
+    // Segments per slice: one CTA per segment, per_sm CTAs per SM at a time.  Time model: waves
+    // of CTAs x (set-up + chunks per segment), with the set-up (operand tables, start memory, the
     // first chunk's loads) worth about 0.6 chunk; the cheapest split wins (the larger one on a
     // tie).
     if (variant == GMA_VARIANT_RESPONSIBILITIES) {
@@ -613,7 +613,7 @@ Plan make_plan(const gma_shape_t &s, int variant)
             const int cps = (nchunks + n - 1) / n;
             const int segs = (nchunks + cps - 1) / cps;
             const long long ctas = (long long)BH * segs;
-            const long long waves = (ctas + kSms - 1) / kSms;
+            const long long waves = (ctas + (long long)per_sm * kSms - 1) / ((long long)per_sm * kSms);
             const double cost = (double)waves * (0.6 + cps);
             if (cost <= best) {
                 best = cost;
@@ -858,6 +858,10 @@ size_t tc_workspace_size_cross(const gma_shape_t &s, int n_k)
     return tck::make_plan(sk, GMA_VARIANT_BIDIRECTIONAL).total;
 }
 
+namespace tck {
+int bidir_read2_ctas_per_sm(int d_r, int kn16, int d_v);   // gma_tc_bidir.cu
+}
+
 gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *QX, const void *KX,
                         const void *V, const float *mu, const float *raw, const float *logits,
                         void *O, void *ws, cudaStream_t st)
@@ -866,7 +870,10 @@ gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *
     sk.N = n_k;
     const int variant = causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL;
     const tck::Plan p = tck::make_plan(sk, variant);
-    const tck::Plan pq = n_k == s.N ? p : tck::make_plan(s, variant);
+    // the bidirectional read pass runs two CTAs per SM on shapes small enough for that; its split
+    // is planned for it (it only sets the query segments: the workspace follows the key plan)
+    const tck::Plan pq = causal ? p
+                                : tck::make_plan(s, variant, tck::bidir_read2_ctas_per_sm(s.d_r, p.kn16, s.d_v));
     char *w = (char *)ws;
     gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
     if (r != GMA_OK) return r;

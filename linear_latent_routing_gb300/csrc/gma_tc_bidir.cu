@@ -45,13 +45,25 @@ struct BidirSmem {
     }
 };
 
+// Tensor-memory columns of one CTA: two groups, each with its logits (kn16 rounded up to 32) and
+// numerator (d_v rounded up to 32), as a power of two of at least 32.  Small shapes fit in 256
+// columns or fewer, so that two CTAs share an SM and one's latency hides behind the other's work.
+__host__ __device__ inline uint32_t bidir_tmem_cols(int kn16, int d_v)
+{
+    const uint32_t need = 2u * ((uint32_t)((kn16 + 31) & ~31) + (uint32_t)((d_v + 31) & ~31));
+    uint32_t cols = 32;
+    while (cols < need) cols *= 2;
+    return cols;
+}
+
 // Unnormalised E_Q of this row over all kc 32-column groups (zeros when not valid), back into
 // TMEM at tl as bf16 pairs (group c at column 16 c); returns (row sum, dot product with z).
 __device__ __forceinline__ float2 exp_row(uint32_t tl, int K, int kc, bool valid, const float *z)
 {
-    const float m = row_max(tl, K, kc);
-    const float sc = valid ? 1.f : 0.f;
-    const float4 *z4 = reinterpret_cast<const float4 *>(z);
+    // a row past the end of the sequence exponentiates against +inf: all of its values are 0 (the
+    // maximum is taken by every lane: its tensor-memory loads are warp-collective)
+    const float mr = row_max(tl, K, kc);
+    const float m = valid ? mr : __int_as_float(0x7f800000);
     float srow = 0.f, den = 0.f;
 #pragma unroll 1
     for (int c = 0; c < kc; ++c) {
@@ -62,7 +74,11 @@ __device__ __forceinline__ float2 exp_row(uint32_t tl, int K, int kc, bool valid
         float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const float4 zz = z4[8 * c + q];
+            // read in program order, so that no group's z values are held ahead of its use
+            float4 zz;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(zz.x), "=f"(zz.y), "=f"(zz.z), "=f"(zz.w)
+                         : "r"(smem_u32(z + 32 * c + 4 * q)));
             d4[0] = fmaf(__uint_as_float(r[4 * q]), zz.x, d4[0]);
             d4[1] = fmaf(__uint_as_float(r[4 * q + 1]), zz.y, d4[1]);
             d4[2] = fmaf(__uint_as_float(r[4 * q + 2]), zz.z, d4[2]);
@@ -71,7 +87,7 @@ __device__ __forceinline__ float2 exp_row(uint32_t tl, int K, int kc, bool valid
         den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
         uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pk2(r[2 * j], r[2 * j + 1], sc);
+        for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
         tmem_st16(tl + 16 * c, w);
     }
     tmem_st_wait();
@@ -114,8 +130,10 @@ __device__ __forceinline__ void store_row(uint32_t tl, int d_v, float inv, bool 
 
 }  // namespace
 
-template <int DR>
-__global__ void __launch_bounds__(BTHREADS, 1) tc_bidir_read2_kernel(const Args a,
+// MINB: CTAs per SM the register allocation is sized for (two for shapes whose tensor memory
+// and shared memory let two CTAs share an SM, one otherwise).
+template <int DR, int MINB>
+__global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Args a,
                                                                      const __grid_constant__ CUtensorMap qmap)
 {
     grid_dependency_wait();   // the total memory comes from the kernels before
@@ -142,7 +160,8 @@ __global__ void __launch_bounds__(BTHREADS, 1) tc_bidir_read2_kernel(const Args 
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tslot, 512);
+    const uint32_t ncols = bidir_tmem_cols(a.kn16, a.d_v);
+    if (warp == 0) tmem_alloc(tslot, ncols);
     if (g == 1) {
         // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
         const int flip = (i >> 2) & 1;
@@ -155,7 +174,9 @@ __global__ void __launch_bounds__(BTHREADS, 1) tc_bidir_read2_kernel(const Args 
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
-    const uint32_t R_L = (uint32_t)(256 * g), R_O = R_L + 128;
+    // per group: the logits (E_Q in place) then the numerator, each rounded up to 32 columns
+    const uint32_t lw = (uint32_t)((a.kn16 + 31) & ~31), ow = (uint32_t)((d_v + 31) & ~31);
+    const uint32_t R_L = (uint32_t)g * (lw + ow), R_O = R_L + lw;
     const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint8_t *ab = smem + (g ? L.ab1 : L.ab0);
     uint64_t *bx = bars + B_X0 + g, *ba = bars + B_A0 + g, *be = bars + B_E0 + g;
@@ -243,13 +264,35 @@ __global__ void __launch_bounds__(BTHREADS, 1) tc_bidir_read2_kernel(const Args 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
 uint32_t bidir_read2_smem(int d_r, int kn16, int d_v)
 {
     const uint32_t need = BidirSmem(d_r, kn16, d_v).total + 1024;
-    return need <= 227u * 1024u ? smem_for(need, 512) : 0;
+    return need <= 227u * 1024u ? smem_for(need, bidir_tmem_cols(kn16, d_v)) : 0;
+}
+
+int bidir_read2_ctas_per_sm(int d_r, int kn16, int d_v)
+{
+    const uint32_t cols = bidir_tmem_cols(kn16, d_v);
+    const uint32_t sm = bidir_read2_smem(d_r, kn16, d_v);
+    // two CTAs need the kernel within 128 registers a thread: it then spills 20-30 bytes at
+    // d_r <= 32, a net gain (LRA-shaped workload: read pass 103 -> 93 us), but 40 bytes at
+    // d_r = 64, a net loss (cross-attention workload: 37.5 -> 41.7 us)
+    int n = (cols <= 256 && d_r <= 32) ? 2 : 1;
+    if (sm == 0 || (uint32_t)n * sm > 228u * 1024u) n = 1;
+    return n;
+}
+
+template <int DR, int MINB>
+gma_status_t launch_bidir_read2_n(const Args &a, const CUtensorMap &qmap, int nblocks, uint32_t sm, cudaStream_t st)
+{
+    if (!set_smem(tc_bidir_read2_kernel<DR, MINB>, sm)) return GMA_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_TC_BIDIR_READ, st,
+               (e = launch_pdl(tc_bidir_read2_kernel<DR, MINB>, dim3(nblocks), dim3(BTHREADS), sm, st, a, qmap)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 template <int DR>
@@ -257,12 +300,8 @@ gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblo
 {
     const uint32_t sm = bidir_read2_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
-    if (!set_smem(tc_bidir_read2_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    cudaError_t e = cudaSuccess;
-    GMA_LAUNCH(KID_TC_BIDIR_READ, st,
-               (e = launch_pdl(tc_bidir_read2_kernel<DR>, dim3(nblocks), dim3(BTHREADS), sm, st, a, qmap)));
-    if (e != cudaSuccess) return GMA_ERR_CUDA;
-    return GMA_OK;
+    return bidir_read2_ctas_per_sm(DR, a.kn16, a.d_v) == 2 ? launch_bidir_read2_n<DR, 2>(a, qmap, nblocks, sm, st)
+                                                           : launch_bidir_read2_n<DR, 1>(a, qmap, nblocks, sm, st);
 }
 
 template gma_status_t launch_bidir_read2<16>(const Args &, const CUtensorMap &, int, cudaStream_t);
