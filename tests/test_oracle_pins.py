@@ -354,6 +354,35 @@ def test_cross_attention_equals_explicit_affinity(nq, nk):
             np.testing.assert_allclose(got[b, h], ref, rtol=0, atol=1e-12)
 
 
+def test_cross_attention_row_symmetries():
+    """The read sums over keys (Methodologie §2: V~ = Gamma_K^T V, Z = Gamma_K^T 1), so permuting
+    the key rows jointly with their value rows leaves O unchanged, permuting the query rows
+    permutes the output rows the same way, and appending a key whose value row is zero only adds
+    its responsibilities to the normaliser (O shrinks row by row, never changes sign)."""
+    r = np.random.default_rng(41)
+    B, H, nq, nk, d_r, K, d_v = 2, 2, 7, 11, 4, 5, 3
+    QX = r.standard_normal((B, H, nq, d_r))
+    KX = r.standard_normal((B, H, nk, d_r))
+    V = r.standard_normal((B, H, nk, d_v))
+    mu = r.standard_normal((H, K, d_r))
+    raw = r.standard_normal((H, K, d_r)) * 0.5
+    logits = r.standard_normal((H, K))
+    base = oracle.forward_cross(QX, KX, V, mu, raw, logits, 1e-3, 1e-6)
+    pk = r.permutation(nk)
+    got = oracle.forward_cross(QX, KX[:, :, pk], V[:, :, pk], mu, raw, logits, 1e-3, 1e-6)
+    np.testing.assert_allclose(got, base, rtol=0, atol=1e-13)
+    pq = r.permutation(nq)
+    got = oracle.forward_cross(QX[:, :, pq], KX, V, mu, raw, logits, 1e-3, 1e-6)
+    np.testing.assert_allclose(got, base[:, :, pq], rtol=0, atol=1e-13)
+    KX2 = np.concatenate([KX, r.standard_normal((B, H, 1, d_r))], axis=2)
+    V2 = np.concatenate([V, np.zeros((B, H, 1, d_v))], axis=2)
+    got = oracle.forward_cross(QX, KX2, V2, mu, raw, logits, 1e-3, 1e-6)
+    ratio = got / base
+    assert np.all(ratio > 0) and np.all(ratio < 1)
+    # the shrink factor is one number per query row: the same for every value column
+    np.testing.assert_allclose(ratio, np.broadcast_to(ratio[..., :1], ratio.shape), rtol=1e-10)
+
+
 def test_cross_attention_with_equal_lengths_is_the_bidirectional_forward():
     c = _rand_case(13, N=17)
     got = oracle.forward_cross(c["QX"], c["KX"], c["V"], c["mu"], c["raw"], c["logits"], 1e-3, 1e-6)
