@@ -79,144 +79,6 @@ __device__ __forceinline__ void issue_logits(uint32_t d, uint32_t abuf, uint32_t
     for (int s = 0; s < KA / 16; ++s) mma_f16(d, kdesc(abuf, s, C), kdesc(bimg, s, kn16), id, s > 0);
 }
 
-// Softmax over the K logits of this thread's TMEM row (log2 domain), in two passes over TMEM:
-// the row maximum first, then exp2(L - max) packed straight to bf16 pairs.  Writes the values
-// (unnormalised, or divided by their sum when `normalize`) into row `row` of the K-major SW128
-// tile `g`; invalid rows get zeros.  Returns the row sum of the unnormalised fp32 values.
-__device__ __noinline__ float softmax_row(uint32_t taddr, const float *cst_, int K, int row,
-                                             bool valid, bool normalize, uint8_t *g)
-{
-    // re-read the constants from shared memory in each pass instead of holding 128 registers
-    const volatile float *cst = cst_;
-    const int kc = (K + 31) >> 5;
-    float m = NEG_BIG;
-#pragma unroll
-    for (int c = 0; c < KMAX / 32; ++c) {
-        if (c < kc) {
-            uint32_t r[32];
-            tmem_ld32(taddr + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int k = c * 32 + j;
-                if (k < K) m = fmaxf(m, __uint_as_float(r[j]) + cst[k]);
-            }
-        }
-    }
-    float s = 0.f;
-    uint32_t pk[KMAX / 2];
-#pragma unroll
-    for (int c = 0; c < KMAX / 32; ++c) {
-        if (c < kc) {
-            uint32_t r[32];
-            tmem_ld32(taddr + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const int k = c * 32 + j;
-                const float e0 = k < K ? ex2(__uint_as_float(r[j]) + cst[k] - m) : 0.f;
-                const float e1 = k + 1 < K ? ex2(__uint_as_float(r[j + 1]) + cst[k + 1] - m) : 0.f;
-                s += e0 + e1;
-                pk[k / 2] = pack_bf16(e0, e1);
-            }
-        }
-    }
-    const bool rescale = normalize || !valid;
-    const float sc = valid ? 1.0f / s : 0.f;
-#pragma unroll
-    for (int c = 0; c < KMAX / 32; ++c) {
-        if (c < kc) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t w[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint32_t v = pk[c * 16 + q * 4 + u];
-                    if (rescale) {
-                        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&v);
-                        const float2 f = __bfloat1622float2(b);
-                        v = pack_bf16(f.x * sc, f.y * sc);
-                    }
-                    w[u] = v;
-                }
-                *reinterpret_cast<uint4 *>(g + sw128(row, c * 4 + q, C)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-    }
-    return s;
-}
-
-
-
-
-// Loads an fp32 memory row (ne columns) from global into TMEM (this thread's lane) and, as
-// bf16, into the SW32 tile `sp`.
-__device__ __forceinline__ void load_state(const float *src, uint32_t taddr, int ne, int k, uint8_t *sp)
-{
-    for (int b = 0; b < ne / 16; ++b) {
-        uint32_t r[16];
-        const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 f = s4[q];
-            r[4 * q] = __float_as_uint(f.x);
-            r[4 * q + 1] = __float_as_uint(f.y);
-            r[4 * q + 2] = __float_as_uint(f.z);
-            r[4 * q + 3] = __float_as_uint(f.w);
-        }
-        if (taddr != 0xFFFFFFFFu) tmem_st16(taddr + b * 16, r);
-        uint4 lo, hi;
-        lo.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
-        lo.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
-        lo.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
-        lo.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
-        hi.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
-        hi.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
-        hi.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
-        hi.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
-        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
-        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
-    }
-    if (taddr != 0xFFFFFFFFu) tmem_st_wait();
-}
-
-// Epilogue: O_i = num_i / (den_i + eps * s_i) from this thread's TMEM row (d_v numerator
-// columns, the normaliser in column d_v), stored to global row `orow` when valid.
-__device__ __forceinline__ void write_out(uint32_t taddr, int d_v, float eps_s, bool valid,
-                                          void *O, long long orow, int out_f32)
-{
-    uint32_t dr[16];
-    tmem_ld16(taddr + d_v, dr);
-    tmem_ld_wait();
-    const float inv = 1.0f / (__uint_as_float(dr[0]) + eps_s);
-    for (int b = 0; b < d_v / 16; ++b) {
-        uint32_t r[16];
-        tmem_ld16(taddr + b * 16, r);
-        tmem_ld_wait();
-        if (!valid) continue;
-        if (out_f32) {
-            float4 *o4 = reinterpret_cast<float4 *>((float *)O + orow * d_v + b * 16);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                o4[q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                                    __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
-        } else {
-            uint4 lo, hi;
-            lo.x = pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
-            lo.y = pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
-            lo.z = pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
-            lo.w = pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
-            hi.x = pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
-            hi.y = pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
-            hi.z = pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
-            hi.w = pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
-            uint4 *o4 = reinterpret_cast<uint4 *>((bf16 *)O + orow * d_v + b * 16);
-            o4[0] = lo;
-            o4[1] = hi;
-        }
-    }
-}
-
 
 __device__ __forceinline__ void sync_tc()
 {
