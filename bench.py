@@ -313,21 +313,35 @@ def run_gma(args, ws, rank, local):
         per = max(e0.elapsed_time(e1) / 5.0, 1e-3)
         steps = int(min(20000, max(20, 3000.0 / per)))
 
+    # inputs that fit in L2 would stay there from step to step: such workloads write a buffer of
+    # twice the L2 size before every timed step, outside that step's own event pair
+    flush = path_bytes(w) <= L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if flush else None
     clocks = ClockSampler(device)
     torch.cuda.synchronize()
     barrier(ws)
     clocks.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
+    if flush:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                flush_buf.fill_(i & 0xFF)
+                pairs[i][0].record(stream)
+                step()
+                pairs[i][1].record(stream)
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                step()
+            e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop()
-    total_ms = e0.elapsed_time(e1)
+    total_ms = sum(a.elapsed_time(b) for a, b in pairs) if flush else e0.elapsed_time(e1)
     st = gma.gma_check_workspace(workspace.data_ptr(), sh)
     if st != 0:
         raise gma.GmaError(st, "timed region")
@@ -336,11 +350,14 @@ def run_gma(args, ws, rank, local):
     n_bd = min(steps, 100)
     gma.gma_timing_enable(n_bd * 8 + 64)
     with torch.cuda.stream(stream):
-        for _ in range(n_bd):
+        for i in range(n_bd):
+            if flush:
+                flush_buf.fill_(i & 0xFF)
             step()
     stream.synchronize()
     launches = gma.gma_timing_read(n_bd * 8 + 64)
     gma.gma_timing_enable(0)
+    del flush_buf
 
     total_ms_max = max_over_ranks(total_ms, ws, device)
     tokens_all = w.tokens * ws * steps
@@ -432,8 +449,10 @@ def run_gma(args, ws, rank, local):
                    "eps": w.eps, "var_floor": w.var_floor,
                    "kernel_family": "tcgen05" if fam == 1 else "fp32 cuda-core",
                    "l2": ("inputs larger than L2 (%.0f MB > 129 MB), no flush"
-                          % (path_bytes(w) / 1e6)) if path_bytes(w) > L2_BYTES else
-                         "inputs smaller than L2: not flushed",
+                          % (path_bytes(w) / 1e6)) if not flush else
+                         ("inputs smaller than L2 (%.1f MB): a %d MB buffer written before every "
+                          "timed step, outside its event pair; value = steps / sum of the per-step "
+                          "event times" % (path_bytes(w) / 1e6, 2 * L2_BYTES // 2 ** 20)),
                    "parallelism": f"replicas x{ws} (independent heads per rank)"},
         "roofline": roofline, "path_roofline": path_roofline,
         "kernels": {k: {"launches": len(v), "total_ms": round(sum(v), 4)}

@@ -71,6 +71,14 @@ typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype_t;
 #define GMA_FLAG_RECOMPUTE_KEYS 0x4u /* causal, tensor-core path: recompute the key
                                       * responsibilities in the output pass instead of keeping
                                       * them in the workspace (smaller workspace, slower)     */
+#define GMA_FLAG_TEST_WITHHOLD 0x80000000u
+/* For tests of the device-side timeout path only; never set it in production.  The call's
+ * bounded waits give up after about a millisecond instead of a second, and the tensor-core
+ * causal and bidirectional key passes withhold one row-phase hand-off (the signal that the
+ * first chunk's [x^2, x] tile is built), so the waits on it run out: every role of the kernel
+ * leaves its loop, tensor memory is released, and gma_check_workspace then reports
+ * GMA_ERR_TIMEOUT.  The output of such a call is undefined; the next call without the flag on
+ * the same stream runs normally. */
 
 typedef struct {
     int B, H, N;     /* batch, heads, sequence length                                       */
@@ -191,17 +199,26 @@ gma_status_t gma_forward_cross(const gma_shape_t *shape, int n_k, const void *QX
  *     call runs as if GMA_FLAG_RECOMPUTE_KEYS were set; if that workspace exceeds it too, the
  *     call returns GMA_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on each device (with that device current) looks up the array's device
- *     address once; make that first call before any stream capture.  No call allocates or frees
+ *     address; make that first call before any stream capture.  The address is looked up again
+ *     when the current CUDA context changes (after cudaDeviceReset, for instance): make the
+ *     first call after such a change outside stream capture too.  No call allocates or frees
  *     memory (no cudaMalloc, cudaFree or allocating library routine).
  *   - All calls on a device share the one array, which keeps the last call's contents; the call
  *     clears what must start at zero.  Calls that overlap on the GPU (other streams, other host
  *     threads) race on the array: order them on one stream or with events.
- *   - Device-side conditions are recorded in the array's header, which this entry point does not
- *     report; argument, shape and launch errors are returned as usual. */
+ *   - Argument, shape and launch errors are returned as usual.  Conditions found on the device
+ *     (a parameter outside the range the tensor-core path holds, a bounded wait that timed out)
+ *     are recorded in the array's header; gma_noalloc_check reports them. */
 #define GMA_NOALLOC_SCRATCH_BYTES (32u << 20)
 gma_status_t gma_forward_causal_noalloc(const gma_shape_t *shape, const void *QX, const void *KX,
                                         const void *V, const float *mu, const float *raw_var,
                                         const float *prior_logits, void *O, gma_stream_t stream);
+
+/* gma_check_workspace for the array behind gma_forward_causal_noalloc on the current device:
+ * waits for `stream`, then returns the condition the device recorded during the last no-alloc
+ * call on this device (GMA_OK if none), or GMA_ERR_CUDA if the stream reported an error.  Like
+ * the entry point itself, it allocates nothing. */
+gma_status_t gma_noalloc_check(gma_stream_t stream);
 
 /* Waits for `stream`, then returns the condition the device recorded in `workspace` during the
  * last call that used it (GMA_OK if none), or GMA_ERR_CUDA if the stream reported an error. */

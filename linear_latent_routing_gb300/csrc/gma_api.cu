@@ -1,5 +1,6 @@
 // gma_api.cu -- the extern "C" entry points of libgma.so (declared in include/gma.h):
 // argument validation, workspace sizing and the choice of kernel family.
+#include <stddef.h>
 #include <string.h>
 
 #include "gma_internal.cuh"
@@ -17,7 +18,8 @@ gma_status_t validate_shape(const gma_shape_t *s, int variant)
     if (s->B < 1 || s->H < 1 || s->N < 1 || s->K < 1) return GMA_ERR_INVALID_ARG;
     if (s->dtype != GMA_F32 && s->dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
     if (!(s->var_floor >= 0.f) || !(s->eps >= 0.f)) return GMA_ERR_INVALID_ARG;
-    if (s->flags & ~(GMA_FLAG_SIMT | GMA_FLAG_OUT_F32 | GMA_FLAG_RECOMPUTE_KEYS)) return GMA_ERR_INVALID_ARG;
+    if (s->flags & ~(GMA_FLAG_SIMT | GMA_FLAG_OUT_F32 | GMA_FLAG_RECOMPUTE_KEYS | GMA_FLAG_TEST_WITHHOLD))
+        return GMA_ERR_INVALID_ARG;
     if (!valid_dim(s->d_r) || s->K > 1024) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (variant != GMA_VARIANT_RESPONSIBILITIES && !valid_dim(s->d_v))
         return GMA_ERR_UNSUPPORTED_SHAPE;
@@ -43,19 +45,27 @@ gma_status_t check_device()
     return GMA_OK;
 }
 
-gma_status_t begin_call_sized(size_t need, void *ws, size_t ws_bytes, cudaStream_t st)
+// The word a test-of-timeouts call puts in the header (static storage: the copy reads it after
+// the call has returned).
+const unsigned kShortWaits = 1u;
+
+gma_status_t begin_call_sized(size_t need, void *ws, size_t ws_bytes, cudaStream_t st, unsigned flags = 0)
 {
     if (!ws || ((uintptr_t)ws & 255u)) return GMA_ERR_WORKSPACE;
     if (need == 0 || ws_bytes < need) return GMA_ERR_WORKSPACE;
     gma_status_t d = check_device();
     if (d != GMA_OK) return d;
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return GMA_ERR_CUDA;
+    if ((flags & GMA_FLAG_TEST_WITHHOLD) &&
+        cudaMemcpyAsync((char *)ws + offsetof(WsHeader, reserved), &kShortWaits, sizeof(kShortWaits),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return GMA_ERR_CUDA;
     return GMA_OK;
 }
 
 gma_status_t begin_call(const gma_shape_t *s, int variant, void *ws, size_t ws_bytes, cudaStream_t st)
 {
-    return begin_call_sized(gma_workspace_size(s, variant), ws, ws_bytes, st);
+    return begin_call_sized(gma_workspace_size(s, variant), ws, ws_bytes, st, s->flags);
 }
 
 // The key side of a cross-attention call: the query shape with N = n_k.

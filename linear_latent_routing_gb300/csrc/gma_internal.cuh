@@ -14,6 +14,7 @@ namespace gma {
 // ------------------------------------------------------------------ workspace header
 // The first 256 bytes of every workspace.  `error` holds the first device-side condition that a
 // kernel recorded (a gma_status_t), `detail` a kernel-specific code for diagnostics.
+// reserved[0] != 0 asks the bounded waits for their short limit (GMA_FLAG_TEST_WITHHOLD).
 struct WsHeader {
     unsigned error;
     unsigned detail;

@@ -51,7 +51,9 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
     if (k >= K) return;
     const float lse = m + logf(s);
     float *ik = inv_var + ((size_t)h * K + k) * d_r;
-    float logdet = 0.f;
+    // the log-determinant is summed in double (once per component per call), so that the
+    // constant carries only its final fp32 rounding into the logits
+    double logdet = 0.0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int d = lane + 32 * i;
@@ -59,12 +61,12 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
             const float r = rv[i];
             const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
             ik[d] = 1.0f / var;
-            logdet += logf(var);
+            logdet += log((double)var);
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) logdet += __shfl_xor_sync(0xffffffffu, logdet, o);
-    if (lane == 0) cst[(size_t)h * K + k] = (lh[k] - lse) - 0.5f * logdet;
+    if (lane == 0) cst[(size_t)h * K + k] = (float)(((double)lh[k] - (double)lse) - 0.5 * logdet);
 }
 
 // ---------------------------------------------------------------- responsibilities
@@ -81,13 +83,51 @@ __device__ __forceinline__ float logit_direct(const float (&x)[DR], const float 
     return fmaf(-0.5f, q, c_k);
 }
 
+// hi + lo += b, exactly: Knuth's TwoSum gives the rounding error of hi + b, which joins lo.
+__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float b)
+{
+    const float s = hi + b;
+    const float bb = s - hi;
+    const float e = (hi - (s - bb)) + (b - bb);
+    hi = s;
+    lo += e;
+}
+
+// The same logit as an unevaluated sum hi + lo, for fp32 inputs.  A logit of a few hundred
+// summed in fp32 one term at a time keeps only ~1e-5 of absolute accuracy, which the 1e-5
+// tolerance of fp32 outputs cannot afford at d_r = 128.  Here the quadratic form is summed in
+// four-term FMA partials (each small, so rounded finely), and their running total starting from
+// c_k is kept as a TwoSum pair (Knuth, TAOCP vol. 2, 4.2.2; the "accurate sum" of Ogita, Rump
+// and Oishi, 2005).  Differences of nearby logits, hi_k - hi_j + (lo_k - lo_j), then carry the
+// accuracy of the four-term partials instead of that of a number of size |L|.
+template <int DR>
+__device__ __forceinline__ float2 logit_direct_pair(const float (&x)[DR], const float *__restrict__ mu_k,
+                                                    const float *__restrict__ iv_k, float c_k)
+{
+    float hi = c_k, lo = 0.f;
+#pragma unroll
+    for (int d0 = 0; d0 < DR; d0 += 4) {
+        float p = 0.f;
+#pragma unroll
+        for (int d = d0; d < d0 + 4; ++d) {
+            const float t = x[d] - __ldg(mu_k + d);
+            p = fmaf(t * t, __ldg(iv_k + d), p);
+        }
+        two_sum_acc(hi, lo, -0.5f * p);   // (the factor is a power of two: exact)
+    }
+    return make_float2(hi, lo);
+}
+
 // One thread per routing vector: online max/sum over K, then a second pass writes
-// gamma_k = exp(L_k - max) / sum.
+// gamma_k = exp(L_k - max) / sum.  fp32 inputs take the logits as TwoSum pairs (above): the
+// maximum m is taken over the high parts, and exp((hi_k - m) + lo_k) is evaluated with the
+// subtraction first, which is exact for every logit within a factor of two of the maximum.
 template <int DR, typename Tin, typename Tout>
 __global__ void simt_resp_kernel(const Tin *__restrict__ X, const float *__restrict__ mu,
                                  const float *__restrict__ inv_var, const float *__restrict__ cst,
                                  Tout *__restrict__ gamma, int H, int N, int K, long long rows)
 {
+    constexpr bool PRECISE = sizeof(Tin) == 4;
     const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows) return;
     const int h = (int)((r / N) % H);
@@ -97,21 +137,25 @@ __global__ void simt_resp_kernel(const Tin *__restrict__ X, const float *__restr
     const float *muh = mu + (size_t)h * K * DR;
     const float *ivh = inv_var + (size_t)h * K * DR;
     const float *ch = cst + (size_t)h * K;
+    auto logit = [&](int k) -> float2 {
+        if (PRECISE) return logit_direct_pair<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k));
+        return make_float2(logit_direct<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k)), 0.f);
+    };
     float m = -INFINITY, s = 0.f;
     for (int k = 0; k < K; ++k) {
-        const float L = logit_direct<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k));
-        if (L > m) {
-            s = s * expf(m - L) + 1.f;
-            m = L;
+        const float2 L = logit(k);
+        if (L.x > m) {
+            s = s * expf(m - L.x) + expf(L.y);
+            m = L.x;
         } else {
-            s += expf(L - m);
+            s += expf((L.x - m) + L.y);
         }
     }
     const float inv = 1.f / s;
     Tout *g = gamma + r * K;
     for (int k = 0; k < K; ++k) {
-        const float L = logit_direct<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k));
-        g[k] = from_f32<Tout>(expf(L - m) * inv);
+        const float2 L = logit(k);
+        g[k] = from_f32<Tout>(expf((L.x - m) + L.y) * inv);
     }
 }
 

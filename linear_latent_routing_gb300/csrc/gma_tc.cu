@@ -521,6 +521,7 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
     a.out_f32 = (s.flags & GMA_FLAG_OUT_F32) ? 1 : 0;
     a.gam = p.off_gam ? (bf16 *)(ws + p.off_gam) : nullptr;
     a.kg = p.kg;
+    a.test_withhold = (s.flags & GMA_FLAG_TEST_WITHHOLD) ? 1 : 0;
     return a;
 }
 

@@ -10,12 +10,17 @@
 // one segment of one (batch, head) slice from the segment's exclusive prefix memory S_start, in
 // chunks of C = 128 tokens.  With E_Q = exp2 of the query logits minus their row maximum (row
 // sums s_i, kept unnormalised):
-//   P      = E_Q Gamma_K^T                          (tensor cores, fp32 in TMEM)
-//   O_num  = E_Q S_{c-1} + tril(P) V_c              (tensor cores)
-//   den    = E_Q . Z_{c-1} + sum_{j<=i} P_ij        (CUDA cores, fp32)
+//   [P | O_num] = E_Q [Gamma_K^T | S_{c-1}]          (tensor cores, one N = 128 + d_v chain)
+//   O_num += tril(P) V_c                             (tensor cores)
+//   den    = E_Q . Z_{c-1} + sum_{j<=i} P_ij         (CUDA cores, fp32)
 //   O      = O_num / (den + eps * s)
-//   S_c    = S_{c-1} + Gamma_K^T V_c                (tensor cores, fp32 in TMEM)
-//   Z_c    = Z_{c-1} + column sums of Gamma_K       (CUDA cores, fp32)
+//   S_c^T  = S_{c-1}^T + V_c^T Gamma_K               (tensor cores, fp32 in TMEM)
+//   Z_c    = Z_{c-1} + column sums of Gamma_K        (CUDA cores, fp32)
+// The running memory is kept transposed (TMEM lane = value column, columns = components), so
+// that its bf16 copy is written row by row as K-major rows next to Gamma_K's in one operand tile
+// [Gamma_K ; S^T] (128 + d_v rows): P and the inter-chunk read E_Q S_{c-1} come out of the same
+// MMA chain.  Value tiles are held 128 columns wide (zeros beyond d_v), so that V^T is an M = 128
+// operand for every d_v.
 //
 // Warp roles (448 threads):
 //   warps 0-3   mask side:  E_Q of the upper half of the components (see below), then the causal
@@ -23,13 +28,13 @@
 //                           the complete normaliser;
 //   warps 4-7   query side: [x^2, x] of the queries (in place in the TMA-filled A tile), E_Q of
 //                           the lower half of the components, their row sums and E_Q . Z_{c-1};
-//   warps 8-11  state/out:  the starting memory, Z_c, the bf16 operand copy of S_c, and the
+//   warps 8-11  state/out:  the starting memory, Z_c, the bf16 operand copy of S_c^T, and the
 //                           output rows;
 //   warp 12     control:    every tcgen05.mma, each as soon as its inputs are complete;
 //   warp 13     loader:     every TMA load (query rows, Gamma_K and value tiles), each as soon
 //                           as its buffer is free, so that no load waits behind an MMA issue.
 // Tensor memory (512 columns): [0,128) query logits, then E_Q; [128,256) P; [256,384) output
-// numerator; [384,512) the running memory S.  The next chunk's query logits are computed while
+// numerator; [384,512) the running memory S^T.  The next chunk's query logits are computed while
 // the current chunk is masked, so the query exponentials are the only long step between chunks;
 // two warps share each row of them: each takes the maximum of one half of the components'
 // logits, the two half-row maxima are exchanged, and each exponentiates its half.  E_Q of 32-column group g (of kc groups, h = ceil(kc / 2) in the lower half) is
@@ -47,6 +52,7 @@ constexpr int GTHREADS = 448;
 enum GBar {
     G_BIMG, G_V0, G_V1, G_XQ, G_GT,                             // TMA (transaction counts)
     G_AQ, G_XM, G_GQ0, G_GQ1, G_PS0, G_PS1, G_ZP, G_SP, G_OF,   // 128 threads (XM, GQ: 256)
+    G_ZB0, G_ZB1,                                               // 128 threads
     G_LQ, G_P, G_PQ, G_S, G_PV0, G_PV1,                         // tcgen05.commit
     G_NBAR
 };
@@ -55,7 +61,7 @@ enum GBar {
 constexpr uint32_t R_LQ = 0, R_P = 128, R_O = 256, R_S = 384;
 
 struct GSmem {
-    uint32_t bimg, ax, abq, gk, sp, ve0, ve1, zbuf, zpart, xmax, dsq, dsm, bars, misc, total;
+    uint32_t bimg, ax, abq, gk, ve0, ve1, zbuf, zpart, xmax, dsq, dsm, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ GSmem(int DR, int kn16, int d_v)
     {
@@ -65,10 +71,9 @@ struct GSmem {
         bimg = o; o = al(o + tile * (uint32_t)kn16 + 32u * (uint32_t)kn16);
         ax = o; o = al(o + (uint32_t)C * 32u);
         abq = o; o = al(o + (uint32_t)C * DR * 4u);   // queries [x^2 | x]
-        gk = o; o = al(o + 2u * C * 128u);            // Gamma_K (TMA)
-        sp = o; o = al(o + (uint32_t)d_v * KMAX * 2u);
-        ve0 = o; o = al(o + (uint32_t)d_v * C * 2u);   // value tiles by chunk parity
-        ve1 = o; o = al(o + (uint32_t)d_v * C * 2u);
+        gk = o; o = al(o + 2u * (uint32_t)(C + d_v) * 128u);   // [Gamma_K (TMA) ; S^T], two atoms
+        ve0 = o; o = al(o + (uint32_t)KMAX * C * 2u);   // value tiles by chunk parity, 128 columns
+        ve1 = o; o = al(o + (uint32_t)KMAX * C * 2u);
         zbuf = o; o += 2u * KMAX * 4u;         // Z_{c-1} by chunk parity
         zpart = o; o += 2u * 8u * KMAX * 4u;   // partial column sums by chunk parity
         xmax = o; o += 4u * C * 4u;            // half-row maxima per half, by chunk parity
@@ -81,14 +86,16 @@ struct GSmem {
 };
 
 // TMA of the Gamma_K rows [tok, tok + 128) of slice bh: kg / 64 boxes of 64 components, each
-// the 128-byte-swizzled K-major layout of one 64-component half of the tile.
-__device__ __forceinline__ void load_g_tile(uint8_t *gk, const CUtensorMap *map, uint64_t *bar, int kg, int tok, int bh)
+// the 128-byte-swizzled K-major layout of one 64-component atom of the [Gamma_K ; S^T] tile
+// (nb = 128 + d_v rows per atom; Gamma_K takes the first 128).
+__device__ __forceinline__ void load_g_tile(uint8_t *gk, const CUtensorMap *map, uint64_t *bar, int kg, int nb, int tok,
+                                            int bh)
 {
     mbar_arrive_expect_tx(bar, (uint32_t)(C * kg * 2));
     for (int hf = 0; hf < kg / 64; ++hf)
         asm volatile(
             "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(gk + hf * C * 128)),
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(gk + hf * nb * 128)),
             "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(64 * hf), "r"(tok), "r"(bh)
             : "memory");
 }
@@ -172,33 +179,37 @@ __device__ __forceinline__ float mask_row(uint32_t tl, int i)
     return (d4[0] + d4[1]) + (d4[2] + d4[3]);
 }
 
-// State side: row k of the running memory S (d_v fp32 columns of TMEM at tl) as bf16 into the
-// MN-major SW32 operand tile sp.
-__device__ __forceinline__ void state_rows(uint32_t tl, int d_v, uint8_t *sp, int k)
+// State side: row n of the running memory S^T (the 128 component columns of TMEM lane n at tl)
+// as bf16 into row 128 + n of the [Gamma_K ; S^T] tile gk (nb rows per atom).  Every lane loads
+// (the loads are warp-collective); only rows n < d_v are written.
+__device__ __forceinline__ void state_rows_t(uint32_t tl, uint8_t *gk, int nb, int n, bool write)
 {
 #pragma unroll 1
-    for (int b = 0; b < d_v / 16; ++b) {
-        uint32_t r[16];
-        tmem_ld16(tl + 16 * b, r);
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
         tmem_ld_wait();
-        const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f),
-                                    pk2(r[6], r[7], 1.f));
-        const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f),
-                                    pk2(r[14], r[15], 1.f));
-        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 0, KMAX)) = lo;
-        *reinterpret_cast<uint4 *>(sp + sw32(k, b, 1, KMAX)) = hi;
+        if (write) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = 8 * q;
+                *reinterpret_cast<uint4 *>(gk + sw128(C + n, 4 * c + q, nb)) =
+                    make_uint4(pk2(r[e], r[e + 1], 1.f), pk2(r[e + 2], r[e + 3], 1.f), pk2(r[e + 4], r[e + 5], 1.f),
+                               pk2(r[e + 6], r[e + 7], 1.f));
+            }
+        }
     }
 }
 
 // State side: this thread's share of the column sums of the Gamma_K tile: components 8q..8q+7
 // over the rows g, g+8, ..., g+120 (t = 16 g + q), into zp[g][8q .. 8q+7].
-__device__ __forceinline__ void colsum_rows(const uint8_t *gk, float *zp, int t)
+__device__ __forceinline__ void colsum_rows(const uint8_t *gk, int nb, float *zp, int t)
 {
     const int q = t & 15, g = t >> 4;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int u = 0; u < C / 8; ++u) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(gk + sw128(g + 8 * u, q, C));
+        const uint4 v = *reinterpret_cast<const uint4 *>(gk + sw128(g + 8 * u, q, nb));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -272,13 +283,15 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
     const int nch = (tok_end - tok0 + C - 1) / C;
     const int d_v = a.d_v;
     const int kc = (a.K + 31) >> 5;
+    const int nb = C + d_v;                         // rows of the [Gamma_K ; S^T] operand tile
     constexpr uint32_t XT = (uint32_t)C * DR * 2;   // bytes of one [x] tile (the TMA destination)
 
     // ---------------------------------------------------------------- set-up (all threads)
     if (warp == 12) {
         if (t == 384) {
             static const uint32_t counts[G_NBAR] = {1,   1,   1,   1,   1,   128, 256, 256, 256, 128,
-                                                    128, 128, 128, 128, 1,   1,   1,   1,   1,   1};
+                                                    128, 128, 128, 128, 128, 128, 1,   1,   1,   1,
+                                                    1,   1};
             for (int i = 0; i < G_NBAR; ++i) mbar_init(bars + i, counts[i]);
             *abort = 0;
             fence_mbar_init();
@@ -286,9 +299,14 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
         __syncwarp();
         tmem_alloc(tslot, 512);
     } else if (warp < 4) {
-        // Gamma_K tile: with 64 stored components the second half is never loaded and must be 0
-        for (uint32_t o = t * 16; o < 2u * C * 128u; o += 128 * 16)
+        // [Gamma_K ; S^T] tile (with 64 stored components the second atom's Gamma_K rows are never
+        // loaded) and both value tiles (their blocks beyond d_v are never loaded): zeros
+        for (uint32_t o = t * 16; o < 2u * (uint32_t)(C + d_v) * 128u; o += 128 * 16)
             *reinterpret_cast<uint4 *>(smem + L.gk + o) = make_uint4(0, 0, 0, 0);
+        for (uint32_t o = t * 16; o < (uint32_t)KMAX * C * 2u; o += 128 * 16) {
+            *reinterpret_cast<uint4 *>(smem + L.ve0 + o) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(smem + L.ve1 + o) = make_uint4(0, 0, 0, 0);
+        }
     } else if (warp < 8) {
         // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
         const int i = t - 128;
@@ -309,9 +327,9 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
     if (warp == 12) {
         // ============================================================ control warp: tcgen05.mma
         if (t == 384) {
-            const uint32_t id_p = idesc_f16(128, 128, 1, 1, 0, 0);
+            const uint32_t id_pq = idesc_f16(128, (uint32_t)nb, 1, 1, 0, 0);
             const uint32_t id_o = idesc_f16(128, (uint32_t)d_v, 1, 1, 0, 1);
-            const uint32_t id_s = idesc_f16(128, (uint32_t)d_v, 1, 1, 1, 1);
+            const uint32_t id_s = idesc_f16(128, (uint32_t)a.kn16, 1, 1, 1, 1);
             const int ksteps = a.kn16 / 16;
             auto eq_col = [&](int s) -> uint32_t { return (uint32_t)(8 * s + (s >= 2 * hq ? 16 * hq : 0)); };
             auto ve = [&](int c) -> uint32_t { return (c & 1) ? L.ve1 : L.ve0; };
@@ -326,11 +344,11 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 mma_commit(bars + G_LQ);
                 return true;
             };
-            // S += Gamma_K^T V of chunk cc
+            // S^T += V^T Gamma_K of chunk cc (M = 128 value columns, zeros beyond d_v)
             auto update = [&](int cc) {
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s)
-                    mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(sb + ve(cc), s, C), id_s, 1u);
+                    mma_f16(tmem + R_S, mn32desc(sb + ve(cc), s, C), mn128desc(sb + L.gk, s, nb), id_s, 1u);
                 mma_commit(bars + G_S);
             };
             if (ok && nch > 0) ok = query_logits(0);
@@ -343,22 +361,19 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                     update(c);
                     s_done = true;
                 }
-                // P: E_Q and Gamma_K ready, S_{c-1} read out (for the read below), R_P free
+                // [P | O] = E_Q [Gamma_K^T | S_{c-1}]: E_Q and Gamma_K ready, S_{c-1}^T read out
+                // into its rows of the tile, R_P free (tril(P_{c-1}) V done) and R_O read out
                 if (!(ok = mbar_wait_abortable(bars + G_GQ0 + ph, (c >> 1) & 1, a.hdr, 103, abort))) break;
                 if (!(ok = mbar_wait_abortable(bars + G_GT, ph, a.hdr, 104, abort))) break;
-                if (!(ok = mbar_wait_abortable(bars + G_SP, ph, a.hdr, 105, abort))) break;
                 if (c > 0 && !(ok = mbar_wait_abortable(bars + G_PV0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr,
                                                         106, abort)))
                     break;
-                tc_fence_after();
-                for (int s = 0; s < ksteps; ++s)   // P = E_Q Gamma_K^T
-                    mma_f16_tmem_a(tmem + R_P, tmem + R_LQ + eq_col(s), kdesc(sb + L.gk, s, C), id_p, s > 0);
-                mma_commit(bars + G_P);
-                // the inter-chunk read (the output side is done with R_O)
+                if (!(ok = mbar_wait_abortable(bars + G_SP, ph, a.hdr, 105, abort))) break;
                 if (c > 0 && !(ok = mbar_wait_abortable(bars + G_OF, (c - 1) & 1, a.hdr, 107, abort))) break;
                 tc_fence_after();
-                for (int s = 0; s < ksteps; ++s)   // O = E_Q S_{c-1}
-                    mma_f16_tmem_a(tmem + R_O, tmem + R_LQ + eq_col(s), mn32desc(sb + L.sp, s, KMAX), id_o, s > 0);
+                for (int s = 0; s < ksteps; ++s)
+                    mma_f16_tmem_a(tmem + R_P, tmem + R_LQ + eq_col(s), kdesc(sb + L.gk, s, nb), id_pq, s > 0);
+                mma_commit(bars + G_P);
                 mma_commit(bars + G_PQ);
                 if (!s_done) {
                     if (!(ok = mbar_wait_abortable(bars + G_V0 + ph, (c >> 1) & 1, a.hdr, 108, abort))) break;
@@ -403,7 +418,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + G_BIMG);
             if (nch > 0) {
                 load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0, bh);
-                load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0, bh);
+                load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, nb, tok0, bh);
                 last_xq = last_gt = 0;
                 load_v(0);
             }
@@ -423,7 +438,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                     if (!(ok = mbar_wait_abortable(bars + G_PQ, ph, a.hdr, 117, abort))) break;
                     if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 111, abort))) break;
                     if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 112, abort))) break;
-                    load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, tok0 + (c + 1) * C, bh);
+                    load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, nb, tok0 + (c + 1) * C, bh);
                     last_gt = c + 1;
                 }
                 if (c + 2 < nch && !(ok = stage_queries(c + 2))) break;
@@ -461,7 +476,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             if (!mbar_spin_wait(bars + G_XM, ph, a.hdr, 134, abort)) break;
             tc_fence_after();
             const float m = valid ? fmaxf(mh, xmax[(qs ? 2 * C : 0) + ph * C + i]) : __int_as_float(0x7f800000);
-            if (!mbar_wait_abortable(bars + G_SP, ph, a.hdr, 132, abort)) break;
+            // Z_{c-1} (published by the state side as soon as Gamma_K's column sums give it)
+            if (!mbar_wait_abortable(bars + G_ZB0 + ph, (c >> 1) & 1, a.hdr, 132, abort)) break;
             // E_Q of this half, one group per wait: a row past the end of the sequence has
             // m = +inf, so all of its values are exp2(-inf) = 0; both halves have read all of
             // their logits before either writes (the maxima were exchanged in between)
@@ -499,29 +515,31 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
         }
     } else {
         // ============================================================ state and output side
-        const int k = t - 256;   // TMEM lane: component row of S, and token row of the output
+        // t - 256: the TMEM lane, which is value column n of S^T and token row of the output; also
+        // component k of the running normaliser Z
+        const int k = t - 256, n = t - 256;
         const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
-        // starting memory: V~ part to TMEM and as the bf16 operand, Z part to the running sum
-        const float *src = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + k) * a.ne;
-        for (int b = 0; b < d_v / 16; ++b) {
+        // starting memory: S_start^T to TMEM and as bf16 rows of the operand tile (column n of the
+        // segment's memory, read component by component: consecutive lanes, consecutive floats)
+        const float *seg_mem = a.agg + ((size_t)bh * a.nseg + seg) * KMAX * a.ne;
+        const bool vrow = n < d_v;
+#pragma unroll 1
+        for (int b = 0; b < KMAX / 16; ++b) {
             uint32_t r[16];
-            const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 f = s4[q];
-                r[4 * q] = __float_as_uint(f.x);
-                r[4 * q + 1] = __float_as_uint(f.y);
-                r[4 * q + 2] = __float_as_uint(f.z);
-                r[4 * q + 3] = __float_as_uint(f.w);
-            }
+            for (int j = 0; j < 16; ++j) r[j] = vrow ? __float_as_uint(seg_mem[(size_t)(16 * b + j) * a.ne + n]) : 0u;
             tmem_st16(lane + R_S + 16 * b, r);
-            const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
-            const uint4 hi = make_uint4(pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
-            *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 0, KMAX)) = lo;
-            *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 1, KMAX)) = hi;
+            if (vrow) {
+                *reinterpret_cast<uint4 *>(smem + L.gk + sw128(C + n, 2 * b, nb)) =
+                    make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
+                *reinterpret_cast<uint4 *>(smem + L.gk + sw128(C + n, 2 * b + 1, nb)) = make_uint4(
+                    pk2(r[8], r[9], 1.f), pk2(r[10], r[11], 1.f), pk2(r[12], r[13], 1.f), pk2(r[14], r[15], 1.f));
+            }
         }
+        const float *src = seg_mem + (size_t)k * a.ne;
         float zrun = src[d_v];
         zbuf[k] = zrun;
+        mbar_arrive(bars + G_ZB0);   // Z_start, for chunk 0's normalisers
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -547,7 +565,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             // Z_c = Z_{c-1} + column sums of Gamma_K
             if (!(ok = mbar_wait_abortable(bars + G_GT, ph, a.hdr, 142, abort))) break;
             float *zp = zpart + ph * 8 * KMAX;
-            colsum_rows(smem + L.gk, zp, k);
+            colsum_rows(smem + L.gk, nb, zp, k);
             mbar_arrive(bars + G_ZP);
             if (!(ok = mbar_wait_abortable(bars + G_ZP, ph, a.hdr, 143, abort))) break;
             {
@@ -556,12 +574,16 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 for (int g = 0; g < 8; ++g) zs += zp[g * KMAX + k];
                 zrun += zs;
             }
-            // readout of S_c (after the update, and after the read of S_{c-1} that it overwrites)
+            // Z_c for chunk c + 1's normalisers.  Its buffer last held Z_{c-2}, which chunk c - 1
+            // read before its mask side finished (output(c - 1) above waited for that); the pair
+            // of barriers by parity keeps a waiter from seeing a phase two ahead.
+            zbuf[((c + 1) & 1) * KMAX + k] = zrun;
+            mbar_arrive(bars + G_ZB0 + ((c + 1) & 1));
+            // readout of S_c^T (after the update, and after the read of S_{c-1} that it overwrites)
             if (!(ok = mbar_wait_abortable(bars + G_S, ph, a.hdr, 144, abort))) break;
             if (!(ok = mbar_wait_abortable(bars + G_PQ, ph, a.hdr, 145, abort))) break;
             tc_fence_after();
-            state_rows(lane + R_S, d_v, smem + L.sp, k);
-            zbuf[((c + 1) & 1) * KMAX + k] = zrun;
+            state_rows_t(lane + R_S, smem + L.gk, nb, n, vrow);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bars + G_SP);

@@ -204,7 +204,9 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             if (!mbar_wait_abortable(bars + S_XK, c & 1, a.hdr, 94, abort)) break;
             build_a_s<DR>(smem + L.abuf, k, smem + L.xst);
             fence_proxy_async_smem();
-            mbar_arrive(bars + S_AK);
+            // (a test of the timeout path withholds the first chunk's signal: every wait on it
+            // runs out, and all roles leave their loops)
+            if (!(a.test_withhold && c == 0)) mbar_arrive(bars + S_AK);
             if (!mbar_wait_abortable(bars + S_LK0 + g, n & 1, a.hdr, 91, abort)) break;
             if (c >= 2 && !mbar_wait_abortable(bars + S_SD0 + g, (n - 1) & 1, a.hdr, 92, abort)) break;
             tc_fence_after();

@@ -51,6 +51,7 @@ struct Args {
     int out_f32;
     bf16 *gam;               // causal: key responsibilities [BH][N][kg] (null: recomputed)
     int kg;
+    int test_withhold;       // GMA_FLAG_TEST_WITHHOLD: the key pass withholds one hand-off
 };
 
 // ------------------------------------------------------------------ layout helpers

@@ -81,6 +81,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 
 // About one second at GB300 clocks.
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000ll;
+// About a millisecond: the limit when the workspace header asks for short waits (a test of the
+// timeout path, GMA_FLAG_TEST_WITHHOLD).  The header is read only once a wait has lasted this
+// long, so normal waits never touch it.
+constexpr long long TEST_WAIT_LIMIT_CYCLES = 2000000ll;
+
+__device__ __forceinline__ bool wait_expired(long long waited, const WsHeader *hdr)
+{
+    if (waited <= TEST_WAIT_LIMIT_CYCLES) return false;
+    if (waited > WAIT_LIMIT_CYCLES) return true;
+    return *reinterpret_cast<const volatile unsigned *>(&hdr->reserved[0]) != 0u;
+}
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns false (and records
 // a timeout with `where` as detail) if it does not within WAIT_LIMIT_CYCLES.
@@ -91,7 +102,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WsHead
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+        if (wait_expired(clock64() - t0, hdr)) {
             record_error(hdr, GMA_ERR_TIMEOUT, where);
             return false;
         }
@@ -115,7 +126,7 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t pari
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+        if (wait_expired(clock64() - t0, hdr)) {
             record_error(hdr, GMA_ERR_TIMEOUT, where);
             *abort = 1;
             return false;
@@ -131,7 +142,7 @@ __device__ __forceinline__ bool mbar_spin_wait(uint64_t *bar, uint32_t parity, W
     const long long t0 = clock64();
     while (!mbar_test_wait(bar, parity)) {
         if (*abort) return false;
-        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+        if (wait_expired(clock64() - t0, hdr)) {
             record_error(hdr, GMA_ERR_TIMEOUT, where);
             *abort = 1;
             return false;
@@ -168,17 +179,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Tiled 4-D tensor load, completing on `bar`.  c0 must keep the copy 16-byte aligned.
-__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int c0, int c1, int c2, int c3)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
-        "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-        : "memory");
-}
-
 // TMA store of a 3-D box from shared memory (bulk-group completion), and the group waits:
 // wait_read returns once the stores have read their shared-memory source, wait_all once they
 // have completed.  Both are hardware waits on this thread's own copies.
@@ -199,8 +199,6 @@ __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t by
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// All but the most recent bulk group have read their shared-memory source.
-__device__ __forceinline__ void bulk_wait_read_but1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream serialisation may
@@ -210,10 +208,6 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependency_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
-{
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
-}
 
 // ------------------------------------------------------------------ tcgen05: tensor memory
 // Executed by one full warp.  Writes the allocated TMEM base address to *slot (shared memory).
@@ -272,20 +266,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-                 "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-                     taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-                 "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-                 "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-                 "r"(r[29]), "r"(r[30]), "r"(r[31])
-                 : "memory");
-}
 
 // ------------------------------------------------------------------ tcgen05: mma
 // D[tmem] (+)= A[smem] * B[smem], cta_group::1, kind::f16 (fp16 or bf16 operands, fp32 D).

@@ -59,93 +59,6 @@ __device__ __forceinline__ uint32_t pk2(uint32_t a, uint32_t b, float sc)
     return pack_bf16(__uint_as_float(a) * sc, __uint_as_float(b) * sc);
 }
 
-// Key side: Gamma_K row `row` = softmax of the TMEM logits at tl, normalised (zeros when not
-// valid), as bf16 into the K-major SW128 tile gk.  PAIR: maximum first, then two 32-column chunks
-// per TMEM wait, the bf16 exponentials rescaled in shared memory; otherwise two passes over the
-// row with a running maximum and sum, each tile element written once.
-template <bool PAIR>
-__device__ __noinline__ void key_softmax(uint32_t tl, int K, int kc, bool valid, uint8_t *gk, int k)
-{
-    float m = 0.f, sum = 0.f;
-    // exp2(L - m) as bf16 pairs straight into the row of the tile ...
-    if (PAIR) {
-        m = row_max(tl, K, kc);
-#pragma unroll
-        for (int c0 = 0; c0 < 4; c0 += 2) {
-            if (c0 < kc) {
-                uint32_t r2[2][32];
-                tmem_ld32(tl + 32 * c0, r2[0]);
-                if (c0 + 1 < kc) tmem_ld32(tl + 32 * (c0 + 1), r2[1]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int c2 = c0 + h2;
-                    if (c2 < kc) {
-                        sum += chunk_exp(r2[h2], c2, K, m);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int e = 8 * q;
-                            *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c2 + q, C)) =
-                                make_uint4(pk2(r2[h2][e], r2[h2][e + 1], 1.f), pk2(r2[h2][e + 2], r2[h2][e + 3], 1.f),
-                                           pk2(r2[h2][e + 4], r2[h2][e + 5], 1.f), pk2(r2[h2][e + 6], r2[h2][e + 7], 1.f));
-                        }
-                    }
-                }
-            }
-        }
-    } else {
-        // first pass: running maximum and sum of exp2(L - max); second pass: the normalised
-        // values, written to the tile once (the exponentials are evaluated twice)
-        float mx = NEG_BIG, sm = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if (c < kc) {
-                uint32_t r[32];
-                tmem_ld32(tl + 32 * c, r);
-                tmem_ld_wait();
-                float cm[4] = {NEG_BIG, NEG_BIG, NEG_BIG, NEG_BIG};
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if ((c + 1) * 32 <= K || 32 * c + j < K) cm[j & 3] = fmaxf(cm[j & 3], __uint_as_float(r[j]));
-                const float mn = fmaxf(mx, fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3])));
-                sm = sm * ex2(mx - mn) + chunk_exp(r, c, K, mn);
-                mx = mn;
-            }
-        }
-        const float scf = valid ? 1.0f / sm : 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if (c < kc) {
-                uint32_t r[32];
-                tmem_ld32(tl + 32 * c, r);
-                tmem_ld_wait();
-                const bool full = (c + 1) * 32 <= K;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int j = 8 * q + 2 * h;
-                        const float e0 = (full || 32 * c + j < K) ? ex2(__uint_as_float(r[j]) - mx) * scf : 0.f;
-                        const float e1 = (full || 32 * c + j + 1 < K) ? ex2(__uint_as_float(r[j + 1]) - mx) * scf : 0.f;
-                        w[h] = pack_bf16(e0, e1);
-                    }
-                    *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c + q, C)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-        return;
-    }
-    // ... then divided by the row sum in place (zeros for rows beyond the sequence)
-    const float scf = valid ? 1.0f / sum : 0.f;
-    const uint32_t sc2 = pack_bf16(scf, scf);
-    for (int q = 0; q < 4 * kc; ++q) {
-        uint4 *p4 = reinterpret_cast<uint4 *>(gk + sw128(k, q, C));
-        const uint4 v = *p4;
-        *p4 = make_uint4(mul_bf16x2(v.x, sc2), mul_bf16x2(v.y, sc2), mul_bf16x2(v.z, sc2), mul_bf16x2(v.w, sc2));
-    }
-}
-
 // Key side: Gamma_K row k = softmax of the TMEM logits at tl, normalised (zeros when not valid),
 // as bf16 into the K-major SW128 tile gk; the exponentials of the row are held in registers as
 // bf16 pairs until the row sum is known, so each tile element is written once.

@@ -21,6 +21,7 @@ GMA_F32, GMA_BF16 = 0, 1
 GMA_FLAG_SIMT = 0x1
 GMA_FLAG_OUT_F32 = 0x2
 GMA_FLAG_RECOMPUTE_KEYS = 0x4
+GMA_FLAG_TEST_WITHHOLD = 0x80000000   # tests of the timeout path only (see include/gma.h)
 (GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL, GMA_VARIANT_DECODE,
  GMA_VARIANT_USAGE, GMA_VARIANT_BACKWARD) = 0, 1, 2, 3, 4, 5
 
@@ -65,6 +66,8 @@ def _load():
     lib.gma_decode_step.restype = ctypes.c_int
     lib.gma_forward_causal_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.gma_forward_causal_noalloc.restype = ctypes.c_int
+    lib.gma_noalloc_check.argtypes = [vp]
+    lib.gma_noalloc_check.restype = ctypes.c_int
     lib.gma_check_workspace.argtypes = [vp, vp]
     lib.gma_check_workspace.restype = ctypes.c_int
     lib.gma_kernel_family.argtypes = [sp, ctypes.c_int]
@@ -156,6 +159,10 @@ GMA_NOALLOC_SCRATCH_BYTES = 32 << 20
 def gma_forward_causal_noalloc(shape, QX, KX, V, mu, raw_var, prior_logits, O, stream):
     return int(_lib.gma_forward_causal_noalloc(ctypes.byref(shape), QX, KX, V, mu, raw_var,
                                                prior_logits, O, stream))
+
+
+def gma_noalloc_check(stream):
+    return int(_lib.gma_noalloc_check(stream))
 
 
 def gma_check_workspace(workspace, stream):

@@ -104,3 +104,29 @@ def test_backward_is_deterministic():
                      check=True)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_backward_full_size_heads():
+    """The benchmarked backward workload (causal, B=4, H=8, N=2048, K=64) in one call, as the
+    benchmark runs it; every gradient of two heads against the oracle: all four batch rows of
+    each head, so that the parameter gradients (summed over the batch) are complete."""
+    gma = _gma()
+    w = W.BACKWARD
+    host = W.make_inputs(w)
+    dO = _dO(w)
+    dev = {k: v.cuda() for k, v in host.items()}
+    got = gma.backward(dev["QX"], dev["KX"], dev["V"], dev["mu"], dev["raw"], dev["logits"], dO.cuda(),
+                       True, eps=w.eps, var_floor=w.var_floor, check=True)
+    got = [t.float().cpu().numpy() for t in got]
+    a = W.to_numpy(host)
+    d = dO.float().numpy()
+    names = ["dQX", "dKX", "dV", "dmu", "draw", "dlogits"]
+    for h in (0, w.H - 1):
+        hs = slice(h, h + 1)
+        ref = oracle.backward(True, a["QX"][:, hs], a["KX"][:, hs], a["V"][:, hs], a["mu"][hs], a["raw"][hs],
+                              a["logits"][hs], w.var_floor, w.eps, d[:, hs])
+        for i, (name, r) in enumerate(zip(names, ref)):
+            g = got[i][:, hs] if i < 3 else got[i][hs]
+            assert np.isfinite(g).all(), name
+            err = normwise_error(g, r) if i < 3 else _head_err(g, r)
+            assert err <= (TOL[w.dtype] if i < 3 else TOL["f32"]), (h, name, err)

@@ -54,6 +54,7 @@ def test_noalloc_matches_regular_entry_point_twice(gma):
         O = torch.full((w.B, w.H, w.N, w.d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
         r = gma.gma_forward_causal_noalloc(shape, *ptrs, O.data_ptr(), stream)
         assert r == 0, gma.gma_status_string(r)
+        assert gma.gma_noalloc_check(stream) == 0
         torch.cuda.synchronize()
         got = O.float().cpu().numpy()
         assert np.isfinite(got).all()
@@ -94,12 +95,38 @@ def test_noalloc_falls_back_to_the_smaller_workspace(gma):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(gma):
     # 512 heads: the per-head tables and segment memories alone exceed the array, whatever the
-    # segment split, so the call must return before enqueuing anything
+    # segment split, so the call must return before enqueuing anything.  Every pointer is null:
+    # if a change ever let such a call past the size check, the regular entry point would reject
+    # the null pointers (GMA_ERR_INVALID_ARG) before anything is enqueued.
     w = W.scaled(W.LONG_CAUSAL, H=512, N=4096)
     shape, n_full, n_small = _sizes(gma, w)
-    assert n_small > gma.GMA_NOALLOC_SCRATCH_BYTES   # checked before any pointer is passed
-    fake = 1 << 20   # never dereferenced: the size check fails first
-    r = gma.gma_forward_causal_noalloc(shape, *([fake] * 7), None)
+    assert n_small > gma.GMA_NOALLOC_SCRATCH_BYTES
+    r = gma.gma_forward_causal_noalloc(shape, *([None] * 7), None)
     assert r == 4   # GMA_ERR_WORKSPACE
     bad = gma.make_shape(1, 1, 10, 48, 8, 16, gma.GMA_BF16)
-    assert gma.gma_forward_causal_noalloc(bad, *([fake] * 7), None) == 2
+    assert gma.gma_forward_causal_noalloc(bad, *([None] * 7), None) == 2   # unsupported d_r
+    ok_shape = _shape(gma, W.scaled(W.LM_CAUSAL, B=1, H=1, N=100))
+    assert gma.gma_forward_causal_noalloc(ok_shape, *([None] * 7), None) == 1   # null pointers
+
+
+def test_noalloc_check_reports_a_device_side_condition(gma):
+    """A condition only the device can find reaches the caller through gma_noalloc_check: raw
+    variances of -20 with no floor give 1/sigma^2 near 5e8, beyond the fp16 table the tensor
+    cores read, which the table kernel records as GMA_ERR_RANGE.  A normal call afterwards
+    reports GMA_OK again (each call clears the condition)."""
+    w = W.scaled(W.LM_CAUSAL, B=1, H=1, N=300)
+    host = W.make_inputs(w)
+    host["raw"] = torch.full_like(host["raw"], -20.0)
+    dev = to_device(host)
+    shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, 0.0)
+    assert gma.gma_kernel_family(shape, gma.GMA_VARIANT_CAUSAL) == 1
+    ptrs = [dev[k].data_ptr() for k in ("QX", "KX", "V", "mu", "raw", "logits")]
+    stream = torch.cuda.current_stream().cuda_stream
+    O = torch.empty(w.B, w.H, w.N, w.d_v, dtype=torch.bfloat16, device="cuda")
+    assert gma.gma_forward_causal_noalloc(shape, *ptrs, O.data_ptr(), stream) == 0
+    assert gma.gma_noalloc_check(stream) == 3   # GMA_ERR_RANGE
+    good = to_device(W.make_inputs(w))
+    shape = _shape(gma, w)
+    ptrs = [good[k].data_ptr() for k in ("QX", "KX", "V", "mu", "raw", "logits")]
+    assert gma.gma_forward_causal_noalloc(shape, *ptrs, O.data_ptr(), stream) == 0
+    assert gma.gma_noalloc_check(stream) == 0
