@@ -437,6 +437,21 @@ bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v)
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same tensor with boxes of 64 columns and the 128-byte swizzle (d_v a multiple of 64): the
+// MN-major operand atoms that the tensor cores read most efficiently.
+bool make_vmap128(CUtensorMap *m, const void *V, int BH, int N, int d_v)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || d_v % 64 != 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d_v, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d_v * 2, (cuuint64_t)N * d_v * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(V), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Plan {
     int kn16, ne, ka, bimg_bytes, bimg_main_bytes;
     int nseg, cps;              // forward: segments per slice and chunks per segment
@@ -621,8 +636,15 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
         CUtensorMap qmap;
         if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
         if (a.gam) {
-            // Gamma_K was stored by the segment pass
-            const gma_status_t r = launch_causal_gamma<DR>(a, vmap, qmap, gmap, BH * p.nseg, st);
+            // Gamma_K was stored by the segment pass; value tiles with the 128-byte swizzle where
+            // d_v allows
+            CUtensorMap vmap_o = vmap;
+            Args ao = a;
+            if (s.d_v % 64 == 0) {
+                if (!make_vmap128(&vmap_o, V, BH, s.N, s.d_v)) return GMA_ERR_CUDA;
+                ao.v128 = 1;
+            }
+            const gma_status_t r = launch_causal_gamma<DR>(ao, vmap_o, qmap, gmap, BH * p.nseg, st);
             if (r != GMA_OK) return r;
         } else {
             const gma_status_t r = launch_causal_pipelined<DR>(a, vmap, kmap, qmap, BH * p.nseg, st);

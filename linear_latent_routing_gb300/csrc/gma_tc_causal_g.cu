@@ -333,6 +333,10 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             const int ksteps = a.kn16 / 16;
             auto eq_col = [&](int s) -> uint32_t { return (uint32_t)(8 * s + (s >= 2 * hq ? 16 * hq : 0)); };
             auto ve = [&](int c) -> uint32_t { return (c & 1) ? L.ve1 : L.ve0; };
+            // value tile of chunk c, k-step s (16 tokens), as an MN-major operand
+            auto vdesc = [&](int c, int s) -> uint64_t {
+                return a.v128 ? mn128desc(sb + ve(c), s, C) : mn32desc(sb + ve(c), s, C);
+            };
             int last_pv = -1;
             bool ok = mbar_wait_abortable(bars + G_BIMG, 0, a.hdr, 100, abort);
             const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             auto update = [&](int cc) {
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s)
-                    mma_f16(tmem + R_S, mn32desc(sb + ve(cc), s, C), mn128desc(sb + L.gk, s, nb), id_s, 1u);
+                    mma_f16(tmem + R_S, vdesc(cc, s), mn128desc(sb + L.gk, s, nb), id_s, 1u);
                 mma_commit(bars + G_S);
             };
             if (ok && nch > 0) ok = query_logits(0);
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 if (!(ok = mbar_wait_abortable(bars + G_PS0 + ph, (c >> 1) & 1, a.hdr, 110, abort))) break;
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s)
-                    mma_f16_tmem_a(tmem + R_O, tmem + R_P + 8 * s, mn32desc(sb + ve(c), s, C), id_o, 1u);
+                    mma_f16_tmem_a(tmem + R_O, tmem + R_P + 8 * s, vdesc(c, s), id_o, 1u);
                 mma_commit(bars + G_PV0 + ph);
                 last_pv = c;
             }
@@ -404,7 +408,11 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             int last_v0 = -1, last_v1 = -1, last_xq = -1, last_gt = -1;
             bool ok = true;
             auto load_v = [&](int c) {
-                load_v_chunk(smem + ((c & 1) ? L.ve1 : L.ve0), &vmap, bars + G_V0 + (c & 1), d_v, tok0 + c * C, bh);
+                uint8_t *dst = smem + ((c & 1) ? L.ve1 : L.ve0);
+                if (a.v128)
+                    load_v_chunk128(dst, &vmap, bars + G_V0 + (c & 1), d_v, tok0 + c * C, bh);
+                else
+                    load_v_chunk(dst, &vmap, bars + G_V0 + (c & 1), d_v, tok0 + c * C, bh);
                 if (c & 1) last_v1 = c; else last_v0 = c;
             };
             // the query rows of chunk cq, once the logits of chunk cq - 1 are done with the A tile

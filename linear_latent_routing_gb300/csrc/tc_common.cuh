@@ -52,6 +52,7 @@ struct Args {
     bf16 *gam;               // causal: key responsibilities [BH][N][kg] (null: recomputed)
     int kg;
     int test_withhold;       // GMA_FLAG_TEST_WITHHOLD: the key pass withholds one hand-off
+    int v128;                // value tiles in 64-column boxes with the 128-byte swizzle (d_v >= 64)
 };
 
 // ------------------------------------------------------------------ layout helpers
@@ -259,6 +260,21 @@ __device__ __forceinline__ void load_v_chunk(uint8_t *ve, const CUtensorMap *vma
 }
 
 
+// TMA of V rows [tok, tok + 128) of slice bh as d_v / 64 MN-major atoms of 64 columns with the
+// 128-byte swizzle (3-D map {d_v, N, BH}, box {64, 128, 1}), atom b at ve + b * 16 KB.
+__device__ __forceinline__ void load_v_chunk128(uint8_t *ve, const CUtensorMap *vmap, uint64_t *bar, int d_v, int tok,
+                                                int bh)
+{
+    mbar_arrive_expect_tx(bar, (uint32_t)(C * d_v * 2));
+    for (int b = 0; b < d_v / 64; ++b) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(ve + b * C * 128)),
+            "l"((uint64_t)vmap), "r"(smem_u32(bar)), "r"(b * 64), "r"(tok), "r"(bh)
+            : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ the pipelined causal kernel
 uint32_t causal_pipelined_smem(int d_r, int kn16, int d_v);
 template <int DR>
@@ -279,6 +295,7 @@ gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const C
 
 // ------------------------------------------------------------------ host helpers (gma_tc.cu)
 bool make_vmap(CUtensorMap *m, const void *V, int BH, int N, int d_v);
+bool make_vmap128(CUtensorMap *m, const void *V, int BH, int N, int d_v);
 bool make_xmap(CUtensorMap *m, const void *X, int BH, int N, int d_r);
 bool make_gmap(CUtensorMap *m, const void *G, int BH, int N, int kg);
 uint32_t smem_for(uint32_t need, uint32_t tmem_cols);
