@@ -110,12 +110,13 @@ __device__ __forceinline__ void cta_setup(uint8_t *smem, const Smem &L, Bars &ba
     }
     if (threadIdx.x < 32) tmem_alloc(tslot, ncols);
     float *cst = reinterpret_cast<float *>(smem + L.cst);
-    for (int k = threadIdx.x; k < KMAX; k += THREADS) cst[k] = k < a.kn16 ? a.cst[(size_t)h * a.kn16 + k] : NEG_BIG;
+    for (int k = threadIdx.x; k < KMAX; k += THREADS)
+        cst[k] = k < a.kn16 ? a.cst[(size_t)h * (a.bimg_head / a.bimg_bytes) * a.kn16 + a.tile * a.kn16 + k] : NEG_BIG;
     sync_tc();
     tmem = *tslot;
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(bars.bimg, (uint32_t)a.bimg_bytes);
-        bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars.bimg);
+        bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars.bimg);
     }
 }
 
@@ -149,32 +150,36 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
                                                             uint8_t *__restrict__ bimg,
                                                             float *__restrict__ cst, int K, int kn16,
                                                             int d_r, int bimg_bytes, int main_bytes,
-                                                            float floor_, WsHeader *hdr)
+                                                            int ntile, float floor_, WsHeader *hdr)
 {
+    // With more than 128 components (ntile > 1) the head's image is ntile complete images of 128
+    // rows each (kn16 = 128): component n sits in tile n / 128, row n % 128.
     grid_dependency_launch();   // the segment pass may start; it waits for this grid before reading
     const int h = blockIdx.x;
     const int ka = d_r * 2 < 64 ? 64 : d_r * 2;
     const float *lh = logits + (size_t)h * K;
-    // log-sum-exp of the head's prior logits (K <= 128: one per thread), by warp shuffles and one
-    // exchange between the four warps
+    // log-sum-exp of the head's prior logits (K <= 1024: up to eight per thread), by warp
+    // shuffles and one exchange between the four warps
     __shared__ float red[2][THREADS / 32];
-    const float lv = threadIdx.x < K ? lh[threadIdx.x] : -INFINITY;
-    float m = lv;
+    float m = -INFINITY;
+    for (int j = threadIdx.x; j < K; j += THREADS) m = fmaxf(m, lh[j]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = m;
     __syncthreads();
     m = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-    float sum = threadIdx.x < K ? expf(lv - m) : 0.f;
+    float sum = 0.f;
+    for (int j = threadIdx.x; j < K; j += THREADS) sum += expf(lh[j] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if ((threadIdx.x & 31) == 0) red[1][threadIdx.x >> 5] = sum;
     __syncthreads();
     const float lse = m + logf((red[1][0] + red[1][1]) + (red[1][2] + red[1][3]));
-    uint8_t *img = bimg + (size_t)h * bimg_bytes;
     const int n = blockIdx.y * 16 + (threadIdx.x >> 3);   // component
+    uint8_t *img = bimg + (size_t)h * ntile * bimg_bytes + (size_t)(n / kn16) * bimg_bytes;
+    const int nr = n % kn16;                               // its row in its tile's image
     const int sub = threadIdx.x & 7;
-    const bool in_table = n < kn16;
+    const bool in_table = n < kn16 * ntile;
     const bool real = n < K;
     float acc = 0.f;
     bool range_ok = true;
@@ -216,7 +221,7 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
             v.y = hv[2] | ((uint32_t)hv[3] << 16);
             v.z = hv[4] | ((uint32_t)hv[5] << 16);
             v.w = hv[6] | ((uint32_t)hv[7] << 16);
-            *reinterpret_cast<uint4 *>(img + sw128(n, q, kn16)) = v;
+            *reinterpret_cast<uint4 *>(img + sw128(nr, q, kn16)) = v;
         }
     }
     // sum the 8 partial sums of this component (lanes 8g .. 8g+7 of the warp)
@@ -231,11 +236,11 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
         uint4 half0 = make_uint4(0, 0, 0, 0);
         half0.x = (uint32_t)(*reinterpret_cast<const uint16_t *>(&hi)) |
                   ((uint32_t)(*reinterpret_cast<const uint16_t *>(&lo)) << 16);
-        uint8_t *row = img + main_bytes + n * 32;
-        const int flip = (n >> 2) & 1;
+        uint8_t *row = img + main_bytes + nr * 32;
+        const int flip = (nr >> 2) & 1;
         *reinterpret_cast<uint4 *>(row + (flip << 4)) = half0;
         *reinterpret_cast<uint4 *>(row + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
-        cst[(size_t)h * kn16 + n] = real ? c : NEG_BIG;
+        cst[(size_t)h * kn16 * ntile + n] = real ? c : NEG_BIG;
     }
     if (!range_ok) record_error(hdr, GMA_ERR_RANGE, 1u);
 }
@@ -454,6 +459,8 @@ bool make_vmap128(CUtensorMap *m, const void *V, int BH, int N, int d_v)
 
 struct Plan {
     int kn16, ne, ka, bimg_bytes, bimg_main_bytes;
+    int ntile;                  // component tiles of 128 (1 when K <= 128)
+    size_t off_lse_q, off_lse_k, off_part, off_pden;
     int nseg, cps;              // forward: segments per slice and chunks per segment
     int kg;                     // causal: components per stored key-responsibility row (64 or 128)
     size_t off_bimg, off_cst, off_agg, off_gam, total;
@@ -464,7 +471,8 @@ constexpr int kSms = 152;   // GB300
 Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1)
 {
     Plan p{};
-    p.kn16 = (s.K + 15) / 16 * 16;
+    p.ntile = s.K > KMAX ? (s.K + KMAX - 1) / KMAX : 1;
+    p.kn16 = p.ntile > 1 ? KMAX : (s.K + 15) / 16 * 16;
     p.ne = s.d_v + 16;
     p.ka = s.d_r * 2 < 64 ? 64 : s.d_r * 2;
     p.bimg_main_bytes = p.ka / 64 * 128 * p.kn16;
@@ -501,14 +509,21 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1)
         p.nseg = (nchunks + p.cps - 1) / p.cps;
     }
     Carve c;
-    p.off_bimg = c.take((size_t)s.H * p.bimg_bytes);
-    p.off_cst = c.take(sizeof(float) * (size_t)s.H * p.kn16);
+    p.off_bimg = c.take((size_t)s.H * p.ntile * p.bimg_bytes);
+    p.off_cst = c.take(sizeof(float) * (size_t)s.H * p.ntile * p.kn16);
     if (variant != GMA_VARIANT_RESPONSIBILITIES)
         p.off_agg = c.take(sizeof(float) * (size_t)BH * p.nseg * KMAX * p.ne);
     if (variant == GMA_VARIANT_CAUSAL && !(s.flags & GMA_FLAG_RECOMPUTE_KEYS)) {
         // Gamma_K of every token, written by the segment pass and read by the output pass
         p.kg = p.kn16 <= 64 ? 64 : 128;
         p.off_gam = c.take((size_t)2 * BH * s.N * p.kg);
+    }
+    if (p.ntile > 1 && variant == GMA_VARIANT_CAUSAL) {
+        // components in tiles: every row's log2-sum-exp, and the output pass's partial sums
+        p.off_lse_q = c.take(sizeof(float) * (size_t)BH * s.N);
+        p.off_lse_k = c.take(sizeof(float) * (size_t)BH * s.N);
+        p.off_part = c.take(sizeof(float) * (size_t)BH * s.N * s.d_v);
+        p.off_pden = c.take(sizeof(float) * (size_t)BH * s.N);
     }
     p.total = c.total();
     return p;
@@ -532,6 +547,13 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
     a.agg_nseg = p.nseg;
     a.bimg_bytes = p.bimg_bytes;
     a.bimg_main_bytes = p.bimg_main_bytes;
+    a.bimg_head = p.bimg_bytes * p.ntile;
+    a.tile = 0;
+    a.lse_q = p.off_lse_q ? (const float *)(ws + p.off_lse_q) : nullptr;
+    a.lse_k = p.off_lse_k ? (const float *)(ws + p.off_lse_k) : nullptr;
+    a.part = p.off_part ? (float *)(ws + p.off_part) : nullptr;
+    a.pden = p.off_pden ? (float *)(ws + p.off_pden) : nullptr;
+    a.pmode = 0;
     a.eps = s.eps;
     a.out_f32 = (s.flags & GMA_FLAG_OUT_F32) ? 1 : 0;
     a.gam = p.off_gam ? (bf16 *)(ws + p.off_gam) : nullptr;
@@ -588,9 +610,9 @@ gma_status_t launch_params(const gma_shape_t &s, const Plan &p, char *ws, const 
                            const float *raw, const float *logits, cudaStream_t st)
 {
     GMA_LAUNCH(KID_TC_PARAMS, st,
-               (tc_params_kernel<<<dim3(s.H, (p.kn16 + 15) / 16), THREADS, 0, st>>>(mu, raw, logits, (uint8_t *)(ws + p.off_bimg),
+               (tc_params_kernel<<<dim3(s.H, p.ntile * p.kn16 / 16), THREADS, 0, st>>>(mu, raw, logits, (uint8_t *)(ws + p.off_bimg),
                                                           (float *)(ws + p.off_cst), s.K, p.kn16, s.d_r,
-                                                          p.bimg_bytes, p.bimg_main_bytes, s.var_floor, (WsHeader *)ws)));
+                                                          p.bimg_bytes, p.bimg_main_bytes, p.ntile, s.var_floor, (WsHeader *)ws)));
     return GMA_OK;
 }
 
@@ -632,6 +654,7 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
             GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<40>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, cz)));
         if (e != cudaSuccess) return GMA_ERR_CUDA;
     }
+    if (causal && p.ntile > 1) return GMA_ERR_UNSUPPORTED_SHAPE;   // (tiled_causal_dr handles those)
     if (causal) {
         CUtensorMap qmap;
         if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
@@ -665,6 +688,56 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     return GMA_OK;
 }
 
+// Causal, more than 128 components: the log2-sum-exp of every query and key row over all
+// components first; then per tile of 128 components the segment pass (Gamma_K of the tile as
+// exp2(L - lse)), the scan, and the output pass, which adds the tile's numerators and normalisers
+// to the partial sums and, after the last tile, divides and writes O.  Exact: the numerator and
+// the normaliser of the page's read are sums over the components, and so are their tiles' parts.
+template <int DR>
+gma_status_t tiled_causal_dr(const gma_shape_t &s, const void *QX, const void *KX, const void *V, void *O, char *ws,
+                             const Plan &p, cudaStream_t st)
+{
+    Args a = make_args(s, p, ws);
+    a.QX = (const bf16 *)QX;
+    a.KX = (const bf16 *)KX;
+    a.O = O;
+    const int BH = s.B * s.H;
+    CUtensorMap vmap, gmap, kmap, qmap, vmap_o;
+    if (!make_vmap(&vmap, V, BH, s.N, s.d_v)) return GMA_ERR_CUDA;
+    if (!make_gmap(&gmap, a.gam, BH, s.N, p.kg)) return GMA_ERR_CUDA;
+    if (!make_xmap(&kmap, a.KX, BH, s.N, DR)) return GMA_ERR_CUDA;
+    if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
+    vmap_o = vmap;
+    if (s.d_v % 64 == 0) {
+        if (!make_vmap128(&vmap_o, V, BH, s.N, s.d_v)) return GMA_ERR_CUDA;
+    }
+    gma_status_t r = launch_lse<DR>(a, a.QX, a.KX, (float *)a.lse_q, (float *)a.lse_k, s.K, BH, st);
+    if (r != GMA_OK) return r;
+    const int KD = KMAX * p.ne, KDu = KMAX * p.ne;
+    const long long tot = (long long)BH * KDu;
+    const unsigned nb = (unsigned)((tot + 255) / 256);
+    for (int t = 0; t < p.ntile; ++t) {
+        Args at = a;
+        at.tile = t;
+        at.K = s.K - KMAX * t < KMAX ? s.K - KMAX * t : KMAX;
+        if ((r = launch_segmem_pipelined<DR>(at, vmap, kmap, gmap, BH * p.nseg, st)) != GMA_OK) return r;
+        cudaError_t e = cudaSuccess;
+        if (p.nseg <= 4)
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<4>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 1)));
+        else if (p.nseg <= 8)
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<8>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 1)));
+        else if (p.nseg <= 20)
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<20>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 1)));
+        else
+            GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<40>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 1)));
+        if (e != cudaSuccess) return GMA_ERR_CUDA;
+        at.pmode = t == 0 ? 1 : (t == p.ntile - 1 ? 3 : 2);
+        at.v128 = s.d_v % 64 == 0 ? 1 : 0;
+        if ((r = launch_causal_gamma<DR>(at, vmap_o, qmap, gmap, BH * p.nseg, st)) != GMA_OK) return r;
+    }
+    return GMA_OK;
+}
+
 template <int DR>
 gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws, const Plan &p,
                      cudaStream_t st, int *assign = nullptr, int *counts = nullptr, float *mass_part = nullptr)
@@ -689,7 +762,11 @@ bool tc_supported(const gma_shape_t &s, int variant)
 {
     if (s.dtype != GMA_BF16 || (s.flags & GMA_FLAG_SIMT)) return false;
     if (!(s.d_r == 16 || s.d_r == 32 || s.d_r == 64)) return false;
-    if (s.K > tck::KMAX) return false;
+    // more than 128 components: in tiles of 128 on the causal path with stored key
+    // responsibilities
+    if (s.K > tck::KMAX &&
+        (variant != GMA_VARIANT_CAUSAL || (s.flags & GMA_FLAG_RECOMPUTE_KEYS)))
+        return false;
     // value tiles move in 16-column TMA boxes, and the numerator and memory hold d_v <= 128
     // TMEM columns each
     if (s.d_v % 16 != 0 || s.d_v > 128) return false;
@@ -762,6 +839,14 @@ gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *
     char *w = (char *)ws;
     gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
     if (r != GMA_OK) return r;
+    if (p.ntile > 1) {
+        switch (s.d_r) {
+        case 16: return tck::tiled_causal_dr<16>(s, QX, KX, V, O, w, p, st);
+        case 32: return tck::tiled_causal_dr<32>(s, QX, KX, V, O, w, p, st);
+        case 64: return tck::tiled_causal_dr<64>(s, QX, KX, V, O, w, p, st);
+        }
+        return GMA_ERR_UNSUPPORTED_SHAPE;
+    }
     switch (s.d_r) {
     case 16: return tck::forward_dr<16>(sk, causal, QX, KX, V, O, w, p, pq, s.N, st);
     case 32: return tck::forward_dr<32>(sk, causal, QX, KX, V, O, w, p, pq, s.N, st);

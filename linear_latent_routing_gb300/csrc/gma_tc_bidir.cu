@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
     if (leader) {
         if (t == 0) {
             mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + B_BIMG);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + B_BIMG);
         }
         if (g < nch) {
             load_x_tile(ab + XT, &qmap, bx, DR, tok0 + g * C, bh);

@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             int last_pv = -1;
             bool ok = true;
             mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + B_BIMG);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + B_BIMG);
             if (nch > 0) {
                 load_x_tile(smem + L.abk + XT, &kmap, bars + B_XK, DR, tok0, bh);
                 load_x_tile(smem + L.abq + XT, &qmap, bars + B_XQ, DR, tok0, bh);

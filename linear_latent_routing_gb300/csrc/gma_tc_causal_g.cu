@@ -222,6 +222,55 @@ __device__ __forceinline__ void colsum_rows(const uint8_t *gk, int nb, float *zp
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
+// Output side, components in tiles: this tile's numerator row (d_v columns of TMEM at tl) and its
+// normaliser den_eps (the tile's E_Q . Z + sum of masked P, plus eps times its E_Q row sum) join
+// the partial sums of the tiles before (pmode 1: the first tile writes them, 2: adds); the last
+// tile (pmode 3) divides the complete numerator by the complete normaliser and writes O.
+__device__ __forceinline__ void out_row_tiled(uint32_t tl, int d_v, float den_eps, bool valid, const Args &a,
+                                              long long orow)
+{
+    float *pr = a.part + orow * d_v;
+    float inv = 0.f;
+    if (valid && a.pmode == 3) inv = 1.0f / (a.pden[orow] + den_eps);
+#pragma unroll 1
+    for (int c = 0; c < (d_v + 31) / 32; ++c) {   // 32 columns per wait
+        uint32_t r[32];
+        if (d_v == 16) {
+            tmem_ld16(tl, *reinterpret_cast<uint32_t(*)[16]>(r));
+        } else {
+            tmem_ld32(tl + 32 * c, r);
+        }
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int col0 = 32 * c;
+        const int ncol = d_v - col0 < 32 ? d_v - col0 : 32;
+        float4 *p4 = reinterpret_cast<float4 *>(pr + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (4 * q >= ncol) continue;
+            float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                                   __uint_as_float(r[4 * q + 3]));
+            if (a.pmode != 1) {
+                const float4 o = p4[q];
+                v.x += o.x;
+                v.y += o.y;
+                v.z += o.z;
+                v.w += o.w;
+            }
+            if (a.pmode != 3) {
+                p4[q] = v;
+            } else if (a.out_f32) {
+                reinterpret_cast<float4 *>((float *)a.O + orow * d_v + col0)[q] =
+                    make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+            } else {
+                uint2 *o2 = reinterpret_cast<uint2 *>((bf16 *)a.O + orow * d_v + col0);
+                o2[q] = make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+            }
+        }
+    }
+    if (valid && a.pmode != 3) a.pden[orow] = a.pmode == 1 ? den_eps : a.pden[orow] + den_eps;
+}
+
 // Output side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.
 __device__ __forceinline__ void out_row(uint32_t tl, int d_v, float inv, bool valid, void *O, long long orow,
                                         int out_f32)
@@ -282,7 +331,9 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
     const int tok_end = min(a.N, tok0 + a.cps * C);
     const int nch = (tok_end - tok0 + C - 1) / C;
     const int d_v = a.d_v;
-    const int kc = (a.K + 31) >> 5;
+    // 32-column groups of E_Q: as many as the table's rows need (with components in tiles, the
+    // last tile's E_Q beyond its K components is written as zeros, not left over from the logits)
+    const int kc = (a.kn16 + 31) >> 5;
     const int nb = C + d_v;                         // rows of the [Gamma_K ; S^T] operand tile
     constexpr uint32_t XT = (uint32_t)C * DR * 2;   // bytes of one [x] tile (the TMA destination)
 
@@ -423,7 +474,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 return true;
             };
             mbar_arrive_expect_tx(bars + G_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + G_BIMG);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + G_BIMG);
             if (nch > 0) {
                 load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0, bh);
                 load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, nb, tok0, bh);
@@ -474,16 +525,24 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
         for (int c = 0; c < nch; ++c) {
             const uint32_t ph = c & 1;
             const bool valid = tok0 + c * C + i < tok_end;
+            // (components in tiles: the row's log2-sum-exp over all components, read ahead; E_Q is
+            // then the row's normalised responsibilities and needs no maximum)
+            const float lse = (a.lse_q && valid) ? a.lse_q[(long long)bh * a.N + tok0 + c * C + i] : 0.f;
             // E_Q: the row maximum from both halves, then each half's exponentials
             if (!mbar_wait_abortable(bars + G_LQ, ph, a.hdr, 131, abort)) break;
             tc_fence_after();
-            const float mh = query_max_half(lane + R_LQ, a.K, g0, g1);
-            xmax[(qs ? 0 : 2 * C) + ph * C + i] = mh;
-            tc_fence_before();
-            mbar_arrive(bars + G_XM);
-            if (!mbar_spin_wait(bars + G_XM, ph, a.hdr, 134, abort)) break;
-            tc_fence_after();
-            const float m = valid ? fmaxf(mh, xmax[(qs ? 2 * C : 0) + ph * C + i]) : __int_as_float(0x7f800000);
+            float m;
+            if (a.lse_q) {
+                m = valid ? lse : __int_as_float(0x7f800000);
+            } else {
+                const float mh = query_max_half(lane + R_LQ, a.K, g0, g1);
+                xmax[(qs ? 0 : 2 * C) + ph * C + i] = mh;
+                tc_fence_before();
+                mbar_arrive(bars + G_XM);
+                if (!mbar_spin_wait(bars + G_XM, ph, a.hdr, 134, abort)) break;
+                tc_fence_after();
+                m = valid ? fmaxf(mh, xmax[(qs ? 2 * C : 0) + ph * C + i]) : __int_as_float(0x7f800000);
+            }
             // Z_{c-1} (published by the state side as soon as Gamma_K's column sums give it)
             if (!mbar_wait_abortable(bars + G_ZB0 + ph, (c >> 1) & 1, a.hdr, 132, abort)) break;
             // E_Q of this half, one group per wait: a row past the end of the sequence has
@@ -560,8 +619,11 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             tc_fence_after();
             const float2 sd = dsm[pc * C + k];
             const int row = tok0 + cc * C + k;
-            out_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), row < tok_end, a.O, (long long)bh * a.N + row,
-                    a.out_f32);
+            if (a.pmode)
+                out_row_tiled(lane + R_O, d_v, sd.y + a.eps * sd.x, row < tok_end, a, (long long)bh * a.N + row);
+            else
+                out_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), row < tok_end, a.O, (long long)bh * a.N + row,
+                        a.out_f32);
             tc_fence_before();
             mbar_arrive(bars + G_OF);
             return true;

@@ -1,0 +1,206 @@
+// gma_tc_lse.cu -- log-sum-exp of every routing row's logits over more than 128 components
+// (tcgen05, sm_103a).
+//
+// Method: page "Attention par Mélange Gaussien (GMA)" (gist.science/fr/paper/2606.18283),
+// Méthodologie §1: gamma_k = p(z = k | x) = exp(L_k) / sum_j exp(L_j), L_k = log pi_k N(x; mu_k,
+// sigma_k^2).  With more than 128 components the logits of one row no longer fit one tensor-memory
+// tile next to everything else a pass keeps there, so the passes take gamma tile by tile as
+// exp2(L_k - lse), where lse = log2 sum_j exp2(L_j) over all components is computed here first
+// (the table holds log2e-scaled logits, so everything is in the log2 domain).
+//
+// One CTA works through a flat list of 128-row chunks of two row sets (the queries and the keys
+// of a causal call).  Per chunk, [x^2, x] is built once in shared memory; the head's 128-component
+// table tiles stream through two shared-memory buffers (bulk copies), each tile's logits go into
+// one of two TMEM regions (the next tile's MMA is issued before the rows read the current one),
+// and one thread per row keeps a running maximum and sum over 32-column groups.
+#include "tc_rows.cuh"
+
+namespace gma {
+namespace tck {
+
+namespace {
+
+constexpr int LTHREADS = 128;
+constexpr int LSE_CTAS = 2 * 152;   // two CTAs per GB300 SM (shared memory and 256 TMEM columns each)
+enum LBar { L_TB0, L_TB1, L_MMA0, L_MMA1, L_NBAR };
+
+struct LseSmem {
+    uint32_t tb0, tb1, abuf, ax, bars, misc, total;
+    __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    __host__ __device__ LseSmem(int DR, int bimg_bytes)
+    {
+        const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
+        uint32_t o = 0;
+        tb0 = o; o = al(o + (uint32_t)bimg_bytes);
+        tb1 = o; o = al(o + (uint32_t)bimg_bytes);
+        abuf = o; o = al(o + ka / 64u * 128u * (uint32_t)C);
+        ax = o; o = al(o + (uint32_t)C * 32u);
+        bars = o; o += L_NBAR * 8u;
+        misc = o; o += 16u;
+        total = o;
+    }
+};
+
+}  // namespace
+
+// rows0 / rows1: the two row sets (B*H*N rows of d_r bf16 each), lse0 / lse1 their outputs; the
+// chunk list is every 128-row chunk of every slice of rows0, then of rows1.
+template <int DR>
+__global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
+                                                             float *lse0, float *lse1, int K_all, int BH)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const LseSmem L(DR, a.bimg_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
+    volatile int *stop = reinterpret_cast<volatile int *>(smem + L.misc + 4);
+    const int t = threadIdx.x, warp = t >> 5;
+    const int ntile = (K_all + KMAX - 1) / KMAX;
+    const int cpn = (a.N + C - 1) / C;                 // chunks per slice
+    const long long side_chunks = (long long)BH * cpn;
+    if (t == 0) {
+        for (int i = 0; i < L_NBAR; ++i) mbar_init(bars + i, 1);
+        *stop = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    {   // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
+        const uint32_t one2 = 0x3C003C00u;   // fp16 pair (1, 1)
+        const int flip = (t >> 2) & 1;
+        *reinterpret_cast<uint4 *>(smem + L.ax + t * 32 + (flip << 4)) = make_uint4(one2, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(smem + L.ax + t * 32 + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
+    }
+    grid_dependency_wait();   // the tables come from the parameter kernel
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tb[2] = {L.tb0, L.tb1};
+    uint32_t ph_tb[2] = {0, 0}, ph_mma[2] = {0, 0};   // (ph_tb: thread 0 alone loads and waits)
+    bool pending[2] = {false, false};                 // thread 0: a table load not waited for yet
+    const int main_bytes = a.bimg_main_bytes;
+
+    for (long long c = blockIdx.x; c < 2 * side_chunks; c += gridDim.x) {
+        const int side = c >= side_chunks;
+        const long long cc = side ? c - side_chunks : c;
+        const int bh = (int)(cc / cpn), tok0 = (int)(cc % cpn) * C, h = bh % a.H;
+        const bf16 *X = side ? rows1 : rows0;
+        float *out = side ? lse1 : lse0;
+        const int row = tok0 + t;
+        const bool valid = row < a.N;
+        const uint8_t *img = a.bimg + (size_t)h * a.bimg_head;
+        uint4 x[DR / 8];
+        load_x<DR>(X, (long long)bh * a.N + row, valid, x);
+        build_a<DR>(smem + L.abuf, t, x);
+        fence_proxy_async_smem();
+        if (t == 0) {
+            for (int j = 0; j < 2 && j < ntile; ++j) {
+                mbar_arrive_expect_tx(bars + L_TB0 + j, (uint32_t)a.bimg_bytes);
+                bulk_g2s(smem + tb[j], img + (size_t)j * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + L_TB0 + j);
+                pending[j] = true;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // thread 0: the logits of tile j, once its table is in
+        auto issue = [&](int j) {
+            const int b = j & 1;
+            if (!mbar_wait(bars + L_TB0 + b, ph_tb[b], a.hdr, 60)) {
+                *stop = 1;
+                return;
+            }
+            ph_tb[b] ^= 1u;
+            pending[b] = false;
+            tc_fence_after();
+            issue_logits_c<DR>(tmem + 128u * b, sb + L.abuf, sb + tb[b], sb + tb[b] + (uint32_t)main_bytes, sb + L.ax,
+                               KMAX);
+            mma_commit(bars + L_MMA0 + b);
+        };
+        if (t == 0) issue(0);
+        float m = NEG_BIG, s = 0.f;
+        for (int j = 0; j < ntile; ++j) {
+            const int b = j & 1;
+            const bool ok = !*stop && mbar_wait(bars + L_MMA0 + b, ph_mma[b], a.hdr, 61);
+            ph_mma[b] ^= 1u;
+            if (__syncthreads_or(!ok)) break;
+            tc_fence_after();
+            if (t == 0) {
+                if (j + 2 < ntile) {   // this buffer's table has been read by the MMA just completed
+                    mbar_arrive_expect_tx(bars + L_TB0 + b, (uint32_t)a.bimg_bytes);
+                    bulk_g2s(smem + tb[b], img + (size_t)(j + 2) * a.bimg_bytes, (uint32_t)a.bimg_bytes,
+                             bars + L_TB0 + b);
+                    pending[b] = true;
+                }
+                if (j + 1 < ntile) issue(j + 1);
+            }
+            // running maximum and sum over this tile's valid components, 32 at a time
+            const int kvalid = min(KMAX, K_all - KMAX * j);
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                uint32_t r[32];
+                tmem_ld32(lane + 128u * b + 32u * g, r);   // (every lane loads: warp-collective)
+                tmem_ld_wait();
+                if (32 * g >= kvalid) continue;
+                float gm = NEG_BIG;
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    if (32 * g + q < kvalid) gm = fmaxf(gm, __uint_as_float(r[q]));
+                const float mn = fmaxf(m, gm);
+                float gs = 0.f;
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    if (32 * g + q < kvalid) gs += ex2(__uint_as_float(r[q]) - mn);
+                s = s * ex2(m - mn) + gs;
+                m = mn;
+            }
+            tc_fence_before();
+            __syncthreads();   // region b read by every row before the MMA of tile j + 2 writes it
+            tc_fence_after();
+        }
+        if (*stop) break;
+        if (valid) out[(long long)bh * a.N + row] = m + log2f(s);
+    }
+    // table loads still in flight (only after a stop) complete before shared memory is released;
+    // an MMA that was issued has completed or been waited for by every thread
+    if (t == 0)
+        for (int b = 0; b < 2; ++b)
+            if (pending[b]) mbar_wait(bars + L_TB0 + b, ph_tb[b], a.hdr, 62);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+uint32_t lse_smem(int d_r, int bimg_bytes)
+{
+    const uint32_t need = LseSmem(d_r, bimg_bytes).total + 1024;
+    return need <= 227u * 1024u ? smem_for(need, 256) : 0;
+}
+
+template <int DR>
+gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
+                        int BH, cudaStream_t st)
+{
+    const uint32_t sm = lse_smem(DR, a.bimg_bytes);
+    if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!set_smem(tc_lse_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    const long long chunks = 2ll * BH * ((a.N + C - 1) / C);
+    const int grid = (int)(chunks < LSE_CTAS ? chunks : LSE_CTAS);
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_TC_LSE, st,
+               (e = launch_pdl(tc_lse_kernel<DR>, dim3(grid), dim3(LTHREADS), sm, st, a, rows0, rows1, lse0, lse1,
+                               K_all, BH)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
+template gma_status_t launch_lse<16>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t);
+template gma_status_t launch_lse<32>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t);
+template gma_status_t launch_lse<64>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t);
+
+}  // namespace tck
+}  // namespace gma

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
                 if (c & 1) { vpend1 = true; vlast1 = c; } else { vpend0 = true; vlast0 = c; }
             };
             mbar_arrive_expect_tx(bars + S_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, a.bimg + (size_t)h * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + S_BIMG);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + S_BIMG);
             for (int c = 0; c < 2 && c < nch; ++c) load_v(c);
             if (nch > 0) {
                 load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0, bh);
@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             const int n = c >> 1;
             const int base = tok0 + c * C;
             // the [x^2, x] buffer is free once the previous chunk's logits are done
+            const bool kvalid = base + k < tok_end;
             if (c >= 1 && !mbar_wait_abortable(bars + S_LK0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 90, abort)) break;
             if (!mbar_wait_abortable(bars + S_XK, c & 1, a.hdr, 94, abort)) break;
             build_a_s<DR>(smem + L.abuf, k, smem + L.xst);
@@ -210,7 +211,11 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             if (!mbar_wait_abortable(bars + S_LK0 + g, n & 1, a.hdr, 91, abort)) break;
             if (c >= 2 && !mbar_wait_abortable(bars + S_SD0 + g, (n - 1) & 1, a.hdr, 92, abort)) break;
             tc_fence_after();
-            key_softmax_reg(lane + (g ? SR_L1 : SR_L0), a.K, kc, base + k < tok_end, gk, k);
+            if (a.lse_k)   // components in tiles: the row's log2-sum-exp over all components
+                key_gamma_lse(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k,
+                              kvalid ? a.lse_k[(long long)bh * a.N + base + k] : 0.f);
+            else
+                key_softmax_reg(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bars + S_GK0 + g);

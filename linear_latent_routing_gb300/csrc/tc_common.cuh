@@ -53,7 +53,24 @@ struct Args {
     int kg;
     int test_withhold;       // GMA_FLAG_TEST_WITHHOLD: the key pass withholds one hand-off
     int v128;                // value tiles in 64-column boxes with the 128-byte swizzle (d_v >= 64)
+    // More than 128 components: the components are cut into tiles of 128 and each pass works on
+    // one tile (components [128 tile, 128 tile + K) of the head's K_all, K being the tile's count)
+    // with every routing row's log2-sum-exp over all components precomputed (lse_q for the
+    // queries, lse_k for the keys; null when K_all <= 128).  The causal output pass then adds
+    // each tile's numerator and normaliser into part / pden (pmode 1: first tile writes, 2: adds,
+    // 3: last tile adds and writes O; 0: one tile, O written directly).
+    int bimg_head;           // bytes of one head's table images (tiles x bimg_bytes)
+    int tile;
+    const float *lse_q, *lse_k;
+    float *part, *pden;
+    int pmode;
 };
+
+// The Gaussian table image of head h for the tile a pass works on.
+__device__ __forceinline__ const uint8_t *table_of(const Args &a, int h)
+{
+    return a.bimg + (size_t)h * a.bimg_head + (size_t)a.tile * a.bimg_bytes;
+}
 
 // ------------------------------------------------------------------ layout helpers
 __device__ __forceinline__ uint32_t sw128(int row, int q, int rows)
@@ -289,6 +306,9 @@ uint32_t bidir_read2_smem(int d_r, int kn16, int d_v);
 template <int DR>
 gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblocks, cudaStream_t st);
 uint32_t causal_gamma_smem(int d_r, int kn16, int d_v);
+template <int DR>
+gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
+                        int BH, cudaStream_t st);
 template <int DR>
 gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const CUtensorMap &qmap,
                                  const CUtensorMap &gmap, int nblocks, cudaStream_t st);

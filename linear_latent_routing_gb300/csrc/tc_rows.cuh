@@ -93,6 +93,33 @@ __device__ __forceinline__ void key_softmax_reg(uint32_t tl, int K, int kc, bool
     }
 }
 
+// Key side, components in tiles (more than 128 in all): Gamma_K row k of this tile is
+// exp2(L - lse) with lse the row's log2-sum-exp over every component (zeros beyond the tile's K
+// components and for rows past the sequence), as bf16 into the K-major SW128 tile gk.
+__device__ __forceinline__ void key_gamma_lse(uint32_t tl, int K, int kc, bool valid, uint8_t *gk, int k, float lse)
+{
+    const float on = valid ? 1.f : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kc; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
+        tmem_ld_wait();
+        const bool full = (c + 1) * 32 <= K;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int j = 8 * q + 2 * h;
+                const float e0 = (full || 32 * c + j < K) ? ex2(__uint_as_float(r[j]) - lse) * on : 0.f;
+                const float e1 = (full || 32 * c + j + 1 < K) ? ex2(__uint_as_float(r[j + 1]) - lse) * on : 0.f;
+                w[h] = pack_bf16(e0, e1);
+            }
+            *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c + q, C)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
 template <int DR>
 __device__ __forceinline__ void issue_logits_c(uint32_t d, uint32_t abuf, uint32_t bimg, uint32_t bconst,
                                                uint32_t ax, int kn16)

@@ -67,6 +67,25 @@ def test_small_cases_match_oracle(w, flags):
     assert err <= TOL[w.dtype], (err, rowwise_error(O, ref))
 
 
+# more than 128 components on the tensor cores (causal): tiles of 128 components, the last one
+# partial, every tile's part added; ragged sequences, and each d_r / d_v the family takes
+TILED = [W.scaled(W.LM_CAUSAL, B=1, H=2, N=777, K=200),
+         W.scaled(W.LM_CAUSAL, B=2, H=1, N=300, d_r=32, K=300, d_v=32),
+         W.scaled(W.LM_CAUSAL, B=1, H=1, N=129, d_r=16, K=129, d_v=16),
+         W.scaled(W.K_SWEEP[3], B=1, H=2, N=1000),
+         W.scaled(W.K_SWEEP[2], B=1, H=1, N=4000)]
+
+
+@pytest.mark.parametrize("w", TILED, ids=lambda w: f"B{w.B}H{w.H}N{w.N}r{w.d_r}K{w.K}v{w.d_v}")
+def test_component_tiles_causal_match_oracle(w):
+    gma = _gma()
+    shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor)
+    assert gma.gma_kernel_family(shape, gma.GMA_VARIANT_CAUSAL) == 1
+    O, ref = _run(w)
+    assert np.isfinite(O).all()
+    assert normwise_error(O, ref) <= TOL["bf16"], (normwise_error(O, ref), rowwise_error(O, ref))
+
+
 def test_fp32_elementwise_relative_error_reported():
     """The stated tolerance is a "max relative error"; the parity tests measure it normwise per
     slice (tests/parity.py says why).  For the fp32 workload this also reports the element-wise
