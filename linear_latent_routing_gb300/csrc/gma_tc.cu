@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
     float *stage = reinterpret_cast<float *>(smem + ((L.total + 127u) & ~127u));   // [C][33]
     // usage diagnostics: histogram and column sums of this CTA's rows
     const bool usage = a.assign != nullptr;
+    const bool tiled = a.lse_q != nullptr;   // more than 128 components: this launch does one tile
     int *hist = reinterpret_cast<int *>(stage + C * 33);
     float *msum = reinterpret_cast<float *>(hist + KMAX);
     if (usage) {
@@ -321,43 +322,49 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
             issue_logits<DR>(tmem, sb + L.abuf, sb + L.bimg, a.kn16);
             mma_commit(bars.mma);
         }
+        // (components in tiles: the row's log2-sum-exp over all components)
+        const float lse = (tiled && valid) ? a.lse_q[(long long)bh * a.N + base + t] : 0.f;
         if (!(ok = wait_all(bars.mma, ph_m, a.hdr, 41))) break;
         const int nb = base + C;
         load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, x);
         // softmax over the row in three passes over TMEM, 32 components at a time (the maximum,
-        // the sum, then the normalised values), so no thread holds the whole row in registers
-        float m = NEG_BIG;
+        // the sum, then the normalised values), so no thread holds the whole row in registers;
+        // with components in tiles, one pass: gamma = exp2(L - lse)
+        float m = tiled ? lse : NEG_BIG;
         int arg = 0;   // the first component of largest responsibility
+        float inv = 1.f;
+        if (!tiled) {
 #pragma unroll 1
-        for (int c = 0; c < kc; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + c * 32, r);
-            tmem_ld_wait();
+            for (int c = 0; c < kc; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + c * 32, r);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (c * 32 + j < a.K) {
-                    const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
-                    if (l > m) {
-                        m = l;
-                        arg = c * 32 + j;
+                for (int j = 0; j < 32; ++j)
+                    if (c * 32 + j < a.K) {
+                        const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
+                        if (l > m) {
+                            m = l;
+                            arg = c * 32 + j;
+                        }
                     }
-                }
-        }
-        if (usage && valid) {
-            a.assign[(long long)bh * a.N + base + t] = arg;
-            atomicAdd(&hist[arg], 1);
-        }
-        float s = 0.f;
+            }
+            if (usage && valid) {
+                a.assign[(long long)bh * a.N + base + t] = arg;
+                atomicAdd(&hist[arg], 1);
+            }
+            float s = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < kc; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + c * 32, r);
-            tmem_ld_wait();
+            for (int c = 0; c < kc; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + c * 32, r);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (c * 32 + j < a.K) s += ex2(__uint_as_float(r[j]) + cst[c * 32 + j] - m);
+                for (int j = 0; j < 32; ++j)
+                    if (c * 32 + j < a.K) s += ex2(__uint_as_float(r[j]) + cst[c * 32 + j] - m);
+            }
+            inv = 1.0f / s;
         }
-        const float inv = 1.0f / s;
         // the tile's rows leave through shared memory, 32 components at a time, so that a warp's
         // global stores cover whole row segments (one thread per row would scatter them)
         const long long row0 = (long long)bh * a.N + base;
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
                 for (int e = t; e < nrows * 32; e += THREADS) {
                     const int rr = e >> 5, j = e & 31;
                     if (j < ncol) {
-                        const long long at = (row0 + rr) * a.K + c * 32 + j;
+                        const long long at = (row0 + rr) * a.kall + a.tile * KMAX + c * 32 + j;
                         if (a.out_f32)
                             ((float *)a.gamma)[at] = stage[rr * 33 + j];
                         else
@@ -400,8 +407,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
     if (usage) {
         __syncthreads();
         for (int k = t; k < a.K; k += THREADS) {
-            if (hist[k]) atomicAdd(&a.counts[(size_t)h * a.K + k], hist[k]);
-            a.mass_part[(size_t)blockIdx.x * a.K + k] = msum[k];
+            if (hist[k] && !tiled) atomicAdd(&a.counts[(size_t)h * a.K + k], hist[k]);
+            a.mass_part[(size_t)blockIdx.x * a.kall + a.tile * KMAX + k] = msum[k];
         }
     }
     cta_teardown(tmem, 128);
@@ -518,6 +525,8 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1)
         p.kg = p.kn16 <= 64 ? 64 : 128;
         p.off_gam = c.take((size_t)2 * BH * s.N * p.kg);
     }
+    if (p.ntile > 1 && variant == GMA_VARIANT_RESPONSIBILITIES)   // the rows' log2-sum-exp
+        p.off_lse_q = c.take(sizeof(float) * (size_t)BH * s.N);
     if (p.ntile > 1 && variant == GMA_VARIANT_CAUSAL) {
         // components in tiles: every row's log2-sum-exp, and the output pass's partial sums
         p.off_lse_q = c.take(sizeof(float) * (size_t)BH * s.N);
@@ -549,6 +558,7 @@ Args make_args(const gma_shape_t &s, const Plan &p, char *ws)
     a.bimg_main_bytes = p.bimg_main_bytes;
     a.bimg_head = p.bimg_bytes * p.ntile;
     a.tile = 0;
+    a.kall = s.K;
     a.lse_q = p.off_lse_q ? (const float *)(ws + p.off_lse_q) : nullptr;
     a.lse_k = p.off_lse_k ? (const float *)(ws + p.off_lse_k) : nullptr;
     a.part = p.off_part ? (float *)(ws + p.off_part) : nullptr;
@@ -688,6 +698,24 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     return GMA_OK;
 }
 
+// Components in tiles: O = numerator / normaliser, both summed over the tiles in part / pden
+// (one thread per four output values).
+__global__ void __launch_bounds__(256) tc_divide_kernel(const float *__restrict__ part, const float *__restrict__ pden,
+                                                        void *__restrict__ O, long long rows, int d_v, int out_f32)
+{
+    grid_dependency_wait();   // the partial sums come from the output passes before
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of four values
+    const int per_row = d_v / 4;
+    if (i >= rows * per_row) return;
+    const long long row = i / per_row;
+    const float inv = 1.0f / pden[row];
+    const float4 v = reinterpret_cast<const float4 *>(part)[i];
+    if (out_f32)
+        reinterpret_cast<float4 *>(O)[i] = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+    else
+        reinterpret_cast<uint2 *>(O)[i] = make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+}
+
 // Causal, more than 128 components: the log2-sum-exp of every query and key row over all
 // components first; then per tile of 128 components the segment pass (Gamma_K of the tile as
 // exp2(L - lse)), the scan, and the output pass, which adds the tile's numerators and normalisers
@@ -731,13 +759,22 @@ gma_status_t tiled_causal_dr(const gma_shape_t &s, const void *QX, const void *K
         else
             GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<40>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 1)));
         if (e != cudaSuccess) return GMA_ERR_CUDA;
-        at.pmode = t == 0 ? 1 : (t == p.ntile - 1 ? 3 : 2);
+        at.pmode = t == 0 ? 1 : 2;
         at.v128 = s.d_v % 64 == 0 ? 1 : 0;
         if ((r = launch_causal_gamma<DR>(at, vmap_o, qmap, gmap, BH * p.nseg, st)) != GMA_OK) return r;
     }
-    return GMA_OK;
+    const long long groups = (long long)BH * s.N * (s.d_v / 4);
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_TC_DIVIDE, st,
+               (e = launch_pdl(tc_divide_kernel, dim3((unsigned)((groups + 255) / 256)), dim3(256), 0, st,
+                               (const float *)a.part, (const float *)a.pden, O, (long long)BH * s.N, s.d_v,
+                               a.out_f32)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
+// Responsibilities (or the usage diagnostics' pass over them).  More than 128 components: every
+// row's log2-sum-exp (and, for the diagnostics, its argmax and the counts) first, then one
+// launch per tile of 128 components writing that tile's columns of gamma (or of the mass sums).
 template <int DR>
 gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws, const Plan &p,
                      cudaStream_t st, int *assign = nullptr, int *counts = nullptr, float *mass_part = nullptr)
@@ -751,7 +788,18 @@ gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws,
     const uint32_t stage = (uint32_t)C * 33u * 4u + KMAX * 8u;   // the staging tile; usage sums
     const uint32_t sm = smem_for(((Smem(DR, p.kn16, 16, false, false, false).total + 127u) & ~127u) + stage + 1024, 128);
     if (!set_smem(tc_resp_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    GMA_LAUNCH(KID_TC_RESP, st, (tc_resp_kernel<DR><<<s.B * s.H * p.nseg, THREADS, sm, st>>>(a)));
+    if (p.ntile > 1) {
+        float *lse = (float *)(ws + p.off_lse_q);
+        const gma_status_t r = launch_lse<DR>(a, a.QX, nullptr, lse, nullptr, s.K, s.B * s.H, st, assign, counts);
+        if (r != GMA_OK) return r;
+        a.lse_q = lse;
+    }
+    for (int t = 0; t < p.ntile; ++t) {
+        Args at = a;
+        at.tile = t;
+        at.K = s.K - KMAX * t < KMAX ? s.K - KMAX * t : KMAX;
+        GMA_LAUNCH(KID_TC_RESP, st, (tc_resp_kernel<DR><<<s.B * s.H * p.nseg, THREADS, sm, st>>>(at)));
+    }
     return GMA_OK;
 }
 
@@ -765,7 +813,8 @@ bool tc_supported(const gma_shape_t &s, int variant)
     // more than 128 components: in tiles of 128 on the causal path with stored key
     // responsibilities
     if (s.K > tck::KMAX &&
-        (variant != GMA_VARIANT_CAUSAL || (s.flags & GMA_FLAG_RECOMPUTE_KEYS)))
+        !((variant == GMA_VARIANT_CAUSAL && !(s.flags & GMA_FLAG_RECOMPUTE_KEYS)) ||
+          variant == GMA_VARIANT_RESPONSIBILITIES))
         return false;
     // value tiles move in 16-column TMA boxes, and the numerator and memory hold d_v <= 128
     // TMEM columns each

@@ -223,15 +223,13 @@ __device__ __forceinline__ void colsum_rows(const uint8_t *gk, int nb, float *zp
 }
 
 // Output side, components in tiles: this tile's numerator row (d_v columns of TMEM at tl) and its
-// normaliser den_eps (the tile's E_Q . Z + sum of masked P, plus eps times its E_Q row sum) join
-// the partial sums of the tiles before (pmode 1: the first tile writes them, 2: adds); the last
-// tile (pmode 3) divides the complete numerator by the complete normaliser and writes O.
+// normaliser den_eps (the tile's E_Q . Z + sum of masked P, plus eps times its E_Q row sum) go to
+// the partial sums: the first tile (pmode 1) writes them, every later one adds to them with
+// reductions in L2 (no value comes back, so nothing waits on the round trip); a last kernel divides.
 __device__ __forceinline__ void out_row_tiled(uint32_t tl, int d_v, float den_eps, bool valid, const Args &a,
                                               long long orow)
 {
     float *pr = a.part + orow * d_v;
-    float inv = 0.f;
-    if (valid && a.pmode == 3) inv = 1.0f / (a.pden[orow] + den_eps);
 #pragma unroll 1
     for (int c = 0; c < (d_v + 31) / 32; ++c) {   // 32 columns per wait
         uint32_t r[32];
@@ -248,27 +246,20 @@ __device__ __forceinline__ void out_row_tiled(uint32_t tl, int d_v, float den_ep
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             if (4 * q >= ncol) continue;
-            float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
-                                   __uint_as_float(r[4 * q + 3]));
-            if (a.pmode != 1) {
-                const float4 o = p4[q];
-                v.x += o.x;
-                v.y += o.y;
-                v.z += o.z;
-                v.w += o.w;
-            }
-            if (a.pmode != 3) {
+            const float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            if (a.pmode == 1)
                 p4[q] = v;
-            } else if (a.out_f32) {
-                reinterpret_cast<float4 *>((float *)a.O + orow * d_v + col0)[q] =
-                    make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
-            } else {
-                uint2 *o2 = reinterpret_cast<uint2 *>((bf16 *)a.O + orow * d_v + col0);
-                o2[q] = make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
-            }
+            else
+                atomicAdd(p4 + q, v);   // (result unused: a reduction in L2)
         }
     }
-    if (valid && a.pmode != 3) a.pden[orow] = a.pmode == 1 ? den_eps : a.pden[orow] + den_eps;
+    if (valid) {
+        if (a.pmode == 1)
+            a.pden[orow] = den_eps;
+        else
+            atomicAdd(a.pden + orow, den_eps);
+    }
 }
 
 // Output side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.

@@ -43,11 +43,14 @@ struct LseSmem {
 
 }  // namespace
 
-// rows0 / rows1: the two row sets (B*H*N rows of d_r bf16 each), lse0 / lse1 their outputs; the
-// chunk list is every 128-row chunk of every slice of rows0, then of rows1.
+// rows0 / rows1: the row sets (B*H*N rows of d_r bf16 each; rows1 may be null), lse0 / lse1 their
+// outputs; the chunk list is every 128-row chunk of every slice of rows0, then of rows1.  With
+// assign non-null (usage diagnostics of rows0) each row's argmax over all components (the lowest
+// index on ties) is written there and counted into counts [H][K_all].
 template <int DR>
 __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
-                                                             float *lse0, float *lse1, int K_all, int BH)
+                                                             float *lse0, float *lse1, int K_all, int BH,
+                                                             int *assign, int *counts)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -84,25 +87,55 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
     bool pending[2] = {false, false};                 // thread 0: a table load not waited for yet
     const int main_bytes = a.bimg_main_bytes;
 
-    for (long long c = blockIdx.x; c < 2 * side_chunks; c += gridDim.x) {
+    // each CTA takes a contiguous range of the chunk list, so that consecutive chunks mostly share
+    // a head: with two tiles, both table images then stay in shared memory from chunk to chunk
+    const int nsets = rows1 ? 2 : 1;
+    const long long total = nsets * side_chunks;
+    const long long per = (total + gridDim.x - 1) / gridDim.x;
+    const long long c_begin = (long long)blockIdx.x * per, c_end = min(total, c_begin + per);
+    // the chunk list: chunk c's slice, first token, head, rows and output
+    auto chunk_at = [&](long long c, int &bh, int &tok0, const bf16 *&X, float *&out) {
         const int side = c >= side_chunks;
         const long long cc = side ? c - side_chunks : c;
-        const int bh = (int)(cc / cpn), tok0 = (int)(cc % cpn) * C, h = bh % a.H;
-        const bf16 *X = side ? rows1 : rows0;
-        float *out = side ? lse1 : lse0;
+        bh = (int)(cc / cpn);
+        tok0 = (int)(cc % cpn) * C;
+        X = side ? rows1 : rows0;
+        out = side ? lse1 : lse0;
+    };
+    int resident_h = -1;   // thread 0: the head whose two table images are in the buffers
+    uint4 x[DR / 8];       // this chunk's routing row, loaded during the chunk before
+    if (c_begin < c_end) {
+        int bh0, tk0;
+        const bf16 *X0;
+        float *o0;
+        chunk_at(c_begin, bh0, tk0, X0, o0);
+        load_x<DR>(X0, (long long)bh0 * a.N + tk0 + t, tk0 + t < a.N, x);
+    }
+    for (long long c = c_begin; c < c_end; ++c) {
+        int bh, tok0;
+        const bf16 *X;
+        float *out;
+        chunk_at(c, bh, tok0, X, out);
+        const int h = bh % a.H;
         const int row = tok0 + t;
         const bool valid = row < a.N;
         const uint8_t *img = a.bimg + (size_t)h * a.bimg_head;
-        uint4 x[DR / 8];
-        load_x<DR>(X, (long long)bh * a.N + row, valid, x);
         build_a<DR>(smem + L.abuf, t, x);
         fence_proxy_async_smem();
-        if (t == 0) {
+        if (c + 1 < c_end) {   // the next chunk's row, in flight while this one is computed
+            int bh1, tk1;
+            const bf16 *X1;
+            float *o1;
+            chunk_at(c + 1, bh1, tk1, X1, o1);
+            load_x<DR>(X1, (long long)bh1 * a.N + tk1 + t, tk1 + t < a.N, x);
+        }
+        if (t == 0 && !(ntile <= 2 && h == resident_h)) {
             for (int j = 0; j < 2 && j < ntile; ++j) {
                 mbar_arrive_expect_tx(bars + L_TB0 + j, (uint32_t)a.bimg_bytes);
                 bulk_g2s(smem + tb[j], img + (size_t)j * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + L_TB0 + j);
                 pending[j] = true;
             }
+            resident_h = ntile <= 2 ? h : -1;
         }
         tc_fence_before();
         __syncthreads();
@@ -110,19 +143,22 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
         // thread 0: the logits of tile j, once its table is in
         auto issue = [&](int j) {
             const int b = j & 1;
-            if (!mbar_wait(bars + L_TB0 + b, ph_tb[b], a.hdr, 60)) {
-                *stop = 1;
-                return;
+            if (pending[b]) {   // (with two tiles and the same head as before, nothing was loaded)
+                if (!mbar_wait(bars + L_TB0 + b, ph_tb[b], a.hdr, 60)) {
+                    *stop = 1;
+                    return;
+                }
+                ph_tb[b] ^= 1u;
+                pending[b] = false;
             }
-            ph_tb[b] ^= 1u;
-            pending[b] = false;
             tc_fence_after();
             issue_logits_c<DR>(tmem + 128u * b, sb + L.abuf, sb + tb[b], sb + tb[b] + (uint32_t)main_bytes, sb + L.ax,
                                KMAX);
             mma_commit(bars + L_MMA0 + b);
         };
         if (t == 0) issue(0);
-        float m = NEG_BIG, s = 0.f;
+        float m = NEG_BIG, s = 0.f, best = NEG_BIG;
+        int arg = 0;
         for (int j = 0; j < ntile; ++j) {
             const int b = j & 1;
             const bool ok = !*stop && mbar_wait(bars + L_MMA0 + b, ph_mma[b], a.hdr, 61);
@@ -150,6 +186,14 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
 #pragma unroll
                 for (int q = 0; q < 32; ++q)
                     if (32 * g + q < kvalid) gm = fmaxf(gm, __uint_as_float(r[q]));
+                if (assign) {   // the first component of largest logit
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (32 * g + q < kvalid && __uint_as_float(r[q]) > best) {
+                            best = __uint_as_float(r[q]);
+                            arg = KMAX * j + 32 * g + q;
+                        }
+                }
                 const float mn = fmaxf(m, gm);
                 float gs = 0.f;
 #pragma unroll
@@ -163,7 +207,13 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
             tc_fence_after();
         }
         if (*stop) break;
-        if (valid) out[(long long)bh * a.N + row] = m + log2f(s);
+        if (valid) {
+            out[(long long)bh * a.N + row] = m + log2f(s);
+            if (assign) {
+                assign[(long long)bh * a.N + row] = arg;
+                atomicAdd(counts + (size_t)h * K_all + arg, 1);
+            }
+        }
     }
     // table loads still in flight (only after a stop) complete before shared memory is released;
     // an MMA that was issued has completed or been waited for by every thread
@@ -184,23 +234,26 @@ uint32_t lse_smem(int d_r, int bimg_bytes)
 
 template <int DR>
 gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
-                        int BH, cudaStream_t st)
+                        int BH, cudaStream_t st, int *assign, int *counts)
 {
     const uint32_t sm = lse_smem(DR, a.bimg_bytes);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_lse_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    const long long chunks = 2ll * BH * ((a.N + C - 1) / C);
+    const long long chunks = (rows1 ? 2ll : 1ll) * BH * ((a.N + C - 1) / C);
     const int grid = (int)(chunks < LSE_CTAS ? chunks : LSE_CTAS);
     cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_LSE, st,
                (e = launch_pdl(tc_lse_kernel<DR>, dim3(grid), dim3(LTHREADS), sm, st, a, rows0, rows1, lse0, lse1,
-                               K_all, BH)));
+                               K_all, BH, assign, counts)));
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
-template gma_status_t launch_lse<16>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t);
-template gma_status_t launch_lse<32>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t);
-template gma_status_t launch_lse<64>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t);
+template gma_status_t launch_lse<16>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t,
+                                     int *, int *);
+template gma_status_t launch_lse<32>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t,
+                                     int *, int *);
+template gma_status_t launch_lse<64>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t,
+                                     int *, int *);
 
 }  // namespace tck
 }  // namespace gma

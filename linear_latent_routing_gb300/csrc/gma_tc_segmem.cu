@@ -200,7 +200,9 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             const int n = c >> 1;
             const int base = tok0 + c * C;
             // the [x^2, x] buffer is free once the previous chunk's logits are done
+            // (components in tiles: the row's log2-sum-exp over all components, read ahead)
             const bool kvalid = base + k < tok_end;
+            const float lse = (a.lse_k && kvalid) ? a.lse_k[(long long)bh * a.N + base + k] : 0.f;
             if (c >= 1 && !mbar_wait_abortable(bars + S_LK0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 90, abort)) break;
             if (!mbar_wait_abortable(bars + S_XK, c & 1, a.hdr, 94, abort)) break;
             build_a_s<DR>(smem + L.abuf, k, smem + L.xst);
@@ -211,9 +213,8 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             if (!mbar_wait_abortable(bars + S_LK0 + g, n & 1, a.hdr, 91, abort)) break;
             if (c >= 2 && !mbar_wait_abortable(bars + S_SD0 + g, (n - 1) & 1, a.hdr, 92, abort)) break;
             tc_fence_after();
-            if (a.lse_k)   // components in tiles: the row's log2-sum-exp over all components
-                key_gamma_lse(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k,
-                              kvalid ? a.lse_k[(long long)bh * a.N + base + k] : 0.f);
+            if (a.lse_k)
+                key_gamma_lse(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k, lse);
             else
                 key_softmax_reg(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k);
             fence_proxy_async_smem();

@@ -57,10 +57,11 @@ struct Args {
     // one tile (components [128 tile, 128 tile + K) of the head's K_all, K being the tile's count)
     // with every routing row's log2-sum-exp over all components precomputed (lse_q for the
     // queries, lse_k for the keys; null when K_all <= 128).  The causal output pass then adds
-    // each tile's numerator and normaliser into part / pden (pmode 1: first tile writes, 2: adds,
-    // 3: last tile adds and writes O; 0: one tile, O written directly).
+    // each tile's numerator and normaliser into part / pden (pmode 1: the first tile writes,
+    // 2: a later tile adds; 0: one tile, O written directly); a last kernel divides the sums.
     int bimg_head;           // bytes of one head's table images (tiles x bimg_bytes)
     int tile;
+    int kall;                // components in all (the row length of gamma and of the usage sums)
     const float *lse_q, *lse_k;
     float *part, *pden;
     int pmode;
@@ -308,7 +309,7 @@ gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblo
 uint32_t causal_gamma_smem(int d_r, int kn16, int d_v);
 template <int DR>
 gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
-                        int BH, cudaStream_t st);
+                        int BH, cudaStream_t st, int *assign = nullptr, int *counts = nullptr);
 template <int DR>
 gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const CUtensorMap &qmap,
                                  const CUtensorMap &gmap, int nblocks, cudaStream_t st);

@@ -136,10 +136,14 @@ def test_fp32_output_flag():
 @pytest.mark.parametrize("w,tol", [(W.TINY_BIDIR_F32, 1e-5),
                                    (W.scaled(W.LONG_CAUSAL, B=1, H=2, N=600), 2e-2),
                                    (W.scaled(W.K_SWEEP[3], B=1, H=1, N=200), 2e-2),
+                                   (W.scaled(W.LM_CAUSAL, B=2, H=2, N=333, d_r=32, K=200), 2e-2),
                                    (W.scaled(W.LM_CAUSAL, B=1, H=1, N=77, K=1), 2e-2)])
 def test_responsibilities_match_oracle(w, tol):
     import oracle
     gma = _gma()
+    if w.dtype == "bf16" and w.d_r <= 64:   # bf16 routing rows take the tensor cores for any K
+        shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, 16, gma.GMA_BF16, w.eps, w.var_floor)
+        assert gma.gma_kernel_family(shape, gma.GMA_VARIANT_RESPONSIBILITIES) == 1
     host = W.make_inputs(w)
     dev = to_device(host)
     g = gma.responsibilities(dev["QX"], dev["mu"], dev["raw"], dev["logits"],

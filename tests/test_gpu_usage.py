@@ -77,6 +77,7 @@ CASES = [
     W.scaled(W.LM_CAUSAL, B=1, H=1, N=1, K=16),
     W.scaled(W.K_SWEEP[3], B=1, H=1, N=300),
     W.scaled(W.LM_CAUSAL, B=1, H=2, N=257, d_r=128, K=48),
+    W.scaled(W.LM_CAUSAL, B=2, H=2, N=500, d_r=32, K=300),   # tensor cores, components in tiles
 ]
 
 
