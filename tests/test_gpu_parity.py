@@ -63,6 +63,7 @@ def test_small_cases_match_oracle(w, flags):
         pytest.skip("the flag only changes the causal path")
     O, ref = _run(w, flags=flags)
     err = normwise_error(O, ref)
+    print(f"{w.name} flags={flags}: normwise {err:.3e}, rowwise {rowwise_error(O, ref):.3e}")
     assert np.isfinite(O).all()
     assert err <= TOL[w.dtype], (err, rowwise_error(O, ref))
 
@@ -196,6 +197,7 @@ def test_full_size_every_token(w):
     torch.cuda.synchronize()
     del dev
     err = _compare_every_token(w, O, host)
+    print(f"{w.name}: normwise {err:.3e} over every token of every slice")
     assert err <= TOL[w.dtype], err
 
 
@@ -221,6 +223,7 @@ def test_sweep_points_whole_slices(w, picks):
         for b, h in picks:
             ref = _oracle_heads(w, a, h, h + 1, b, b + 1)
             err = max(err, normwise_error(O[b:b + 1, h:h + 1].float().cpu().numpy(), ref))
+    print(f"{w.name}: normwise {err:.3e} over {'every slice' if picks is None else picks}")
     assert err <= TOL[w.dtype], err
 
 
