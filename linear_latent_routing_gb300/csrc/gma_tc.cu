@@ -475,8 +475,10 @@ struct Plan {
 
 constexpr int kSms = 152;   // GB300
 
-Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1)
+// `s` describes the keys; n_q is the number of queries per slice (cross-attention), s.N if < 0.
+Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1, int n_q = -1)
 {
+    if (n_q < 0) n_q = s.N;
     Plan p{};
     p.ntile = s.K > KMAX ? (s.K + KMAX - 1) / KMAX : 1;
     p.kn16 = p.ntile > 1 ? KMAX : (s.K + 15) / 16 * 16;
@@ -527,12 +529,13 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1)
     }
     if (p.ntile > 1 && variant == GMA_VARIANT_RESPONSIBILITIES)   // the rows' log2-sum-exp
         p.off_lse_q = c.take(sizeof(float) * (size_t)BH * s.N);
-    if (p.ntile > 1 && variant == GMA_VARIANT_CAUSAL) {
-        // components in tiles: every row's log2-sum-exp, and the output pass's partial sums
-        p.off_lse_q = c.take(sizeof(float) * (size_t)BH * s.N);
+    if (p.ntile > 1 && (variant == GMA_VARIANT_CAUSAL || variant == GMA_VARIANT_BIDIRECTIONAL)) {
+        // components in tiles: every query and key row's log2-sum-exp, and the partial sums of the
+        // queries' numerators and normalisers
+        p.off_lse_q = c.take(sizeof(float) * (size_t)BH * n_q);
         p.off_lse_k = c.take(sizeof(float) * (size_t)BH * s.N);
-        p.off_part = c.take(sizeof(float) * (size_t)BH * s.N * s.d_v);
-        p.off_pden = c.take(sizeof(float) * (size_t)BH * s.N);
+        p.off_part = c.take(sizeof(float) * (size_t)BH * n_q * s.d_v);
+        p.off_pden = c.take(sizeof(float) * (size_t)BH * n_q);
     }
     p.total = c.total();
     return p;
@@ -775,6 +778,66 @@ gma_status_t tiled_causal_dr(const gma_shape_t &s, const void *QX, const void *K
 // Responsibilities (or the usage diagnostics' pass over them).  More than 128 components: every
 // row's log2-sum-exp (and, for the diagnostics, its argmax and the counts) first, then one
 // launch per tile of 128 components writing that tile's columns of gamma (or of the mass sums).
+// Bidirectional (and cross-attention: n_q queries, sk.N keys), more than 128 components: the
+// rows' log2-sum-exp first; per tile of 128 components the key pass (Gamma_K = exp2(L - lse)),
+// the sum of the segment memories, and the read pass adding the tile's numerators and
+// normalisers to the partial sums; then the divide.
+template <int DR>
+gma_status_t tiled_bidir_dr(const gma_shape_t &sk, const void *QX, const void *KX, const void *V, void *O, char *ws,
+                            const Plan &p, const Plan &pq, int n_q, cudaStream_t st)
+{
+    Args a = make_args(sk, p, ws);
+    a.QX = (const bf16 *)QX;
+    a.KX = (const bf16 *)KX;
+    a.O = O;
+    const int BH = sk.B * sk.H;
+    CUtensorMap vmap, gmap, kmap, qmap;
+    memset(&gmap, 0, sizeof(gmap));
+    if (!make_vmap(&vmap, V, BH, sk.N, sk.d_v)) return GMA_ERR_CUDA;
+    if (!make_xmap(&kmap, a.KX, BH, sk.N, DR)) return GMA_ERR_CUDA;
+    if (!make_xmap(&qmap, a.QX, BH, n_q, DR)) return GMA_ERR_CUDA;
+    Args al = a;   // the pre-pass: queries (n_q per slice) then keys (sk.N per slice)
+    al.N = n_q;
+    gma_status_t r = launch_lse<DR>(al, a.QX, a.KX, (float *)a.lse_q, (float *)a.lse_k, sk.K, BH, st, nullptr,
+                                    nullptr, sk.N);
+    if (r != GMA_OK) return r;
+    const int KD = KMAX * p.ne, KDu = KMAX * p.ne;
+    const long long tot = (long long)BH * KDu;
+    const unsigned nb = (unsigned)((tot + 255) / 256);
+    for (int t = 0; t < p.ntile; ++t) {
+        Args at = a;
+        at.tile = t;
+        at.K = sk.K - KMAX * t < KMAX ? sk.K - KMAX * t : KMAX;
+        if ((r = launch_segmem_pipelined<DR>(at, vmap, kmap, gmap, BH * p.nseg, st)) != GMA_OK) return r;
+        if (p.nseg > 1) {   // (a slice of one segment already holds its total)
+            cudaError_t e = cudaSuccess;
+            if (p.nseg <= 4)
+                GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<4>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 0)));
+            else if (p.nseg <= 8)
+                GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<8>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 0)));
+            else if (p.nseg <= 20)
+                GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<20>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 0)));
+            else
+                GMA_LAUNCH(KID_TC_CAUSAL_SCAN, st, (e = launch_pdl(tc_scan_kernel<40>, dim3(nb), dim3(256), 0, st, a.agg, tot, p.nseg, KD, KDu, 0)));
+            if (e != cudaSuccess) return GMA_ERR_CUDA;
+        }
+        Args aq = at;
+        aq.N = n_q;
+        aq.nseg = pq.nseg;
+        aq.cps = pq.cps;
+        aq.agg_nseg = p.nseg;
+        aq.pmode = t == 0 ? 1 : 2;
+        if ((r = launch_bidir_read2<DR>(aq, qmap, BH * pq.nseg, st)) != GMA_OK) return r;
+    }
+    const long long groups = (long long)BH * n_q * (sk.d_v / 4);
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_TC_DIVIDE, st,
+               (e = launch_pdl(tc_divide_kernel, dim3((unsigned)((groups + 255) / 256)), dim3(256), 0, st,
+                               (const float *)a.part, (const float *)a.pden, O, (long long)BH * n_q, sk.d_v,
+                               a.out_f32)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
 template <int DR>
 gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws, const Plan &p,
                      cudaStream_t st, int *assign = nullptr, int *counts = nullptr, float *mass_part = nullptr)
@@ -810,12 +873,9 @@ bool tc_supported(const gma_shape_t &s, int variant)
 {
     if (s.dtype != GMA_BF16 || (s.flags & GMA_FLAG_SIMT)) return false;
     if (!(s.d_r == 16 || s.d_r == 32 || s.d_r == 64)) return false;
-    // more than 128 components: in tiles of 128 on the causal path with stored key
-    // responsibilities
-    if (s.K > tck::KMAX &&
-        !((variant == GMA_VARIANT_CAUSAL && !(s.flags & GMA_FLAG_RECOMPUTE_KEYS)) ||
-          variant == GMA_VARIANT_RESPONSIBILITIES))
-        return false;
+    // more than 128 components: in tiles of 128 (the causal path only with stored key
+    // responsibilities)
+    if (s.K > tck::KMAX && variant == GMA_VARIANT_CAUSAL && (s.flags & GMA_FLAG_RECOMPUTE_KEYS)) return false;
     // value tiles move in 16-column TMA boxes, and the numerator and memory hold d_v <= 128
     // TMEM columns each
     if (s.d_v % 16 != 0 || s.d_v > 128) return false;
@@ -866,7 +926,7 @@ size_t tc_workspace_size_cross(const gma_shape_t &s, int n_k)
 {
     gma_shape_t sk = s;
     sk.N = n_k;
-    return tck::make_plan(sk, GMA_VARIANT_BIDIRECTIONAL).total;
+    return tck::make_plan(sk, GMA_VARIANT_BIDIRECTIONAL, 1, s.N).total;
 }
 
 namespace tck {
@@ -880,7 +940,7 @@ gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *
     gma_shape_t sk = s;   // the key side
     sk.N = n_k;
     const int variant = causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL;
-    const tck::Plan p = tck::make_plan(sk, variant);
+    const tck::Plan p = tck::make_plan(sk, variant, 1, s.N);
     // the bidirectional read pass runs two CTAs per SM on shapes small enough for that; its split
     // is planned for it (it only sets the query segments: the workspace follows the key plan)
     const tck::Plan pq = causal ? p
@@ -888,11 +948,19 @@ gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *
     char *w = (char *)ws;
     gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
     if (r != GMA_OK) return r;
-    if (p.ntile > 1) {
+    if (p.ntile > 1 && causal) {
         switch (s.d_r) {
         case 16: return tck::tiled_causal_dr<16>(s, QX, KX, V, O, w, p, st);
         case 32: return tck::tiled_causal_dr<32>(s, QX, KX, V, O, w, p, st);
         case 64: return tck::tiled_causal_dr<64>(s, QX, KX, V, O, w, p, st);
+        }
+        return GMA_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (p.ntile > 1) {
+        switch (s.d_r) {
+        case 16: return tck::tiled_bidir_dr<16>(sk, QX, KX, V, O, w, p, pq, s.N, st);
+        case 32: return tck::tiled_bidir_dr<32>(sk, QX, KX, V, O, w, p, pq, s.N, st);
+        case 64: return tck::tiled_bidir_dr<64>(sk, QX, KX, V, O, w, p, pq, s.N, st);
         }
         return GMA_ERR_UNSUPPORTED_SHAPE;
     }

@@ -58,11 +58,14 @@ __host__ __device__ inline uint32_t bidir_tmem_cols(int kn16, int d_v)
 
 // Unnormalised E_Q of this row over all kc 32-column groups (zeros when not valid), back into
 // TMEM at tl as bf16 pairs (group c at column 16 c); returns (row sum, dot product with z).
-__device__ __forceinline__ float2 exp_row(uint32_t tl, int K, int kc, bool valid, const float *z)
+// With components in tiles (use_lse), E_Q = exp2(L - lse) with the row's log2-sum-exp over all
+// components: the normalised responsibilities of this tile, no maximum needed.
+__device__ __forceinline__ float2 exp_row(uint32_t tl, int K, int kc, bool valid, const float *z, bool use_lse,
+                                          float lse)
 {
     // a row past the end of the sequence exponentiates against +inf: all of its values are 0 (the
     // maximum is taken by every lane: its tensor-memory loads are warp-collective)
-    const float mr = row_max(tl, K, kc);
+    const float mr = use_lse ? lse : row_max(tl, K, kc);
     const float m = valid ? mr : __int_as_float(0x7f800000);
     float srow = 0.f, den = 0.f;
 #pragma unroll 1
@@ -151,7 +154,9 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
     const int tok_end = min(a.N, tok0 + a.cps * C);
     const int nch = (tok_end - tok0 + C - 1) / C;
     const int d_v = a.d_v;
-    const int kc = (a.K + 31) >> 5;
+    // 32-column groups of E_Q: as many as the table's rows need (with components in tiles, the last
+    // tile's E_Q beyond its K components is written as zeros)
+    const int kc = (a.kn16 + 31) >> 5;
     constexpr uint32_t XT = (uint32_t)C * DR * 2;
     const bool leader = i == 0;
 
@@ -236,6 +241,8 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
                                sb + L.bimg + (uint32_t)a.bimg_main_bytes, sb + L.ax, a.kn16);
             mma_commit(bl);
         }
+        // (components in tiles: the row's log2-sum-exp over all components, read ahead)
+        const float lse_row = (a.lse_q && valid) ? a.lse_q[(long long)bh * a.N + row] : 0.f;
         if (!(ok = mbar_wait_abortable(bl, n, a.hdr, 153, abort))) break;
         if (leader && c + 2 < nch) {   // the A tile is read: this group's next rows
             load_x_tile(ab + XT, &qmap, bx, DR, tok0 + (c + 2) * C, bh);
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
         }
         if (c < 2 && !(ok = mbar_wait_abortable(bars + B_SP, 0, a.hdr, 154, abort))) break;
         tc_fence_after();
-        const float2 sd = exp_row(lane + R_L, a.K, kc, valid, z);
+        const float2 sd = exp_row(lane + R_L, a.K, kc, valid, z, a.lse_q != nullptr, lse_row);
         tc_fence_before();
         mbar_arrive(be);
         if (leader) {
@@ -255,7 +262,12 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
         }
         if (!(ok = mbar_wait_abortable(bo, n, a.hdr, 156, abort))) break;
         tc_fence_after();
-        store_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), valid, a.O, (long long)bh * a.N + row, a.out_f32);
+        if (a.pmode)
+            tile_partial_row(lane + R_O, d_v, sd.y + a.eps * sd.x, valid, a.part, a.pden, (long long)bh * a.N + row,
+                             a.pmode);
+        else
+            store_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), valid, a.O, (long long)bh * a.N + row,
+                      a.out_f32);
     }
     // a TMA load issued but not consumed (only after a timeout) completes before shared memory
     // is released

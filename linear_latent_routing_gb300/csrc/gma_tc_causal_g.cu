@@ -222,46 +222,6 @@ __device__ __forceinline__ void colsum_rows(const uint8_t *gk, int nb, float *zp
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
-// Output side, components in tiles: this tile's numerator row (d_v columns of TMEM at tl) and its
-// normaliser den_eps (the tile's E_Q . Z + sum of masked P, plus eps times its E_Q row sum) go to
-// the partial sums: the first tile (pmode 1) writes them, every later one adds to them with
-// reductions in L2 (no value comes back, so nothing waits on the round trip); a last kernel divides.
-__device__ __forceinline__ void out_row_tiled(uint32_t tl, int d_v, float den_eps, bool valid, const Args &a,
-                                              long long orow)
-{
-    float *pr = a.part + orow * d_v;
-#pragma unroll 1
-    for (int c = 0; c < (d_v + 31) / 32; ++c) {   // 32 columns per wait
-        uint32_t r[32];
-        if (d_v == 16) {
-            tmem_ld16(tl, *reinterpret_cast<uint32_t(*)[16]>(r));
-        } else {
-            tmem_ld32(tl + 32 * c, r);
-        }
-        tmem_ld_wait();
-        if (!valid) continue;
-        const int col0 = 32 * c;
-        const int ncol = d_v - col0 < 32 ? d_v - col0 : 32;
-        float4 *p4 = reinterpret_cast<float4 *>(pr + col0);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (4 * q >= ncol) continue;
-            const float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-            if (a.pmode == 1)
-                p4[q] = v;
-            else
-                atomicAdd(p4 + q, v);   // (result unused: a reduction in L2)
-        }
-    }
-    if (valid) {
-        if (a.pmode == 1)
-            a.pden[orow] = den_eps;
-        else
-            atomicAdd(a.pden + orow, den_eps);
-    }
-}
-
 // Output side: output row orow = (d_v numerator columns of TMEM at tl) * inv, bf16 or fp32.
 __device__ __forceinline__ void out_row(uint32_t tl, int d_v, float inv, bool valid, void *O, long long orow,
                                         int out_f32)
@@ -611,7 +571,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             const float2 sd = dsm[pc * C + k];
             const int row = tok0 + cc * C + k;
             if (a.pmode)
-                out_row_tiled(lane + R_O, d_v, sd.y + a.eps * sd.x, row < tok_end, a, (long long)bh * a.N + row);
+                tile_partial_row(lane + R_O, d_v, sd.y + a.eps * sd.x, row < tok_end, a.part, a.pden,
+                                 (long long)bh * a.N + row, a.pmode);
             else
                 out_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), row < tok_end, a.O, (long long)bh * a.N + row,
                         a.out_f32);

@@ -43,14 +43,15 @@ struct LseSmem {
 
 }  // namespace
 
-// rows0 / rows1: the row sets (B*H*N rows of d_r bf16 each; rows1 may be null), lse0 / lse1 their
-// outputs; the chunk list is every 128-row chunk of every slice of rows0, then of rows1.  With
+// rows0 / rows1: the row sets (B*H slices of a.N and N1 rows of d_r bf16 each; rows1 may be null),
+// lse0 / lse1 their outputs; the chunk list is every 128-row chunk of every slice of rows0, then
+// of rows1.  With
 // assign non-null (usage diagnostics of rows0) each row's argmax over all components (the lowest
 // index on ties) is written there and counted into counts [H][K_all].
 template <int DR>
 __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
                                                              float *lse0, float *lse1, int K_all, int BH,
-                                                             int *assign, int *counts)
+                                                             int N1, int *assign, int *counts)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -60,8 +61,8 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
     volatile int *stop = reinterpret_cast<volatile int *>(smem + L.misc + 4);
     const int t = threadIdx.x, warp = t >> 5;
     const int ntile = (K_all + KMAX - 1) / KMAX;
-    const int cpn = (a.N + C - 1) / C;                 // chunks per slice
-    const long long side_chunks = (long long)BH * cpn;
+    const int cpn0 = (a.N + C - 1) / C, cpn1 = (N1 + C - 1) / C;   // chunks per slice of each set
+    const long long side_chunks = (long long)BH * cpn0;
     if (t == 0) {
         for (int i = 0; i < L_NBAR; ++i) mbar_init(bars + i, 1);
         *stop = 0;
@@ -90,44 +91,46 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
     // each CTA takes a contiguous range of the chunk list, so that consecutive chunks mostly share
     // a head: with two tiles, both table images then stay in shared memory from chunk to chunk
     const int nsets = rows1 ? 2 : 1;
-    const long long total = nsets * side_chunks;
+    const long long total = side_chunks + (nsets > 1 ? (long long)BH * cpn1 : 0ll);
     const long long per = (total + gridDim.x - 1) / gridDim.x;
     const long long c_begin = (long long)blockIdx.x * per, c_end = min(total, c_begin + per);
-    // the chunk list: chunk c's slice, first token, head, rows and output
-    auto chunk_at = [&](long long c, int &bh, int &tok0, const bf16 *&X, float *&out) {
+    // the chunk list: chunk c's slice, first token, rows per slice, rows and output
+    auto chunk_at = [&](long long c, int &bh, int &tok0, int &n, const bf16 *&X, float *&out) {
         const int side = c >= side_chunks;
         const long long cc = side ? c - side_chunks : c;
+        const int cpn = side ? cpn1 : cpn0;
         bh = (int)(cc / cpn);
         tok0 = (int)(cc % cpn) * C;
+        n = side ? N1 : a.N;
         X = side ? rows1 : rows0;
         out = side ? lse1 : lse0;
     };
     int resident_h = -1;   // thread 0: the head whose two table images are in the buffers
     uint4 x[DR / 8];       // this chunk's routing row, loaded during the chunk before
     if (c_begin < c_end) {
-        int bh0, tk0;
+        int bh0, tk0, n0;
         const bf16 *X0;
         float *o0;
-        chunk_at(c_begin, bh0, tk0, X0, o0);
-        load_x<DR>(X0, (long long)bh0 * a.N + tk0 + t, tk0 + t < a.N, x);
+        chunk_at(c_begin, bh0, tk0, n0, X0, o0);
+        load_x<DR>(X0, (long long)bh0 * n0 + tk0 + t, tk0 + t < n0, x);
     }
     for (long long c = c_begin; c < c_end; ++c) {
-        int bh, tok0;
+        int bh, tok0, nrow;
         const bf16 *X;
         float *out;
-        chunk_at(c, bh, tok0, X, out);
+        chunk_at(c, bh, tok0, nrow, X, out);
         const int h = bh % a.H;
         const int row = tok0 + t;
-        const bool valid = row < a.N;
+        const bool valid = row < nrow;
         const uint8_t *img = a.bimg + (size_t)h * a.bimg_head;
         build_a<DR>(smem + L.abuf, t, x);
         fence_proxy_async_smem();
         if (c + 1 < c_end) {   // the next chunk's row, in flight while this one is computed
-            int bh1, tk1;
+            int bh1, tk1, n1;
             const bf16 *X1;
             float *o1;
-            chunk_at(c + 1, bh1, tk1, X1, o1);
-            load_x<DR>(X1, (long long)bh1 * a.N + tk1 + t, tk1 + t < a.N, x);
+            chunk_at(c + 1, bh1, tk1, n1, X1, o1);
+            load_x<DR>(X1, (long long)bh1 * n1 + tk1 + t, tk1 + t < n1, x);
         }
         if (t == 0 && !(ntile <= 2 && h == resident_h)) {
             for (int j = 0; j < 2 && j < ntile; ++j) {
@@ -208,9 +211,9 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
         }
         if (*stop) break;
         if (valid) {
-            out[(long long)bh * a.N + row] = m + log2f(s);
+            out[(long long)bh * nrow + row] = m + log2f(s);
             if (assign) {
-                assign[(long long)bh * a.N + row] = arg;
+                assign[(long long)bh * nrow + row] = arg;
                 atomicAdd(counts + (size_t)h * K_all + arg, 1);
             }
         }
@@ -234,26 +237,27 @@ uint32_t lse_smem(int d_r, int bimg_bytes)
 
 template <int DR>
 gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
-                        int BH, cudaStream_t st, int *assign, int *counts)
+                        int BH, cudaStream_t st, int *assign, int *counts, int N1)
 {
     const uint32_t sm = lse_smem(DR, a.bimg_bytes);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (!set_smem(tc_lse_kernel<DR>, sm)) return GMA_ERR_CUDA;
-    const long long chunks = (rows1 ? 2ll : 1ll) * BH * ((a.N + C - 1) / C);
+    if (N1 < 0) N1 = a.N;
+    const long long chunks = (long long)BH * ((a.N + C - 1) / C) + (rows1 ? (long long)BH * ((N1 + C - 1) / C) : 0ll);
     const int grid = (int)(chunks < LSE_CTAS ? chunks : LSE_CTAS);
     cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_LSE, st,
                (e = launch_pdl(tc_lse_kernel<DR>, dim3(grid), dim3(LTHREADS), sm, st, a, rows0, rows1, lse0, lse1,
-                               K_all, BH, assign, counts)));
+                               K_all, BH, N1, assign, counts)));
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 template gma_status_t launch_lse<16>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t,
-                                     int *, int *);
+                                     int *, int *, int);
 template gma_status_t launch_lse<32>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t,
-                                     int *, int *);
+                                     int *, int *, int);
 template gma_status_t launch_lse<64>(const Args &, const bf16 *, const bf16 *, float *, float *, int, int, cudaStream_t,
-                                     int *, int *);
+                                     int *, int *, int);
 
 }  // namespace tck
 }  // namespace gma

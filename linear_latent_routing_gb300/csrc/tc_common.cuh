@@ -309,7 +309,7 @@ gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblo
 uint32_t causal_gamma_smem(int d_r, int kn16, int d_v);
 template <int DR>
 gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
-                        int BH, cudaStream_t st, int *assign = nullptr, int *counts = nullptr);
+                        int BH, cudaStream_t st, int *assign = nullptr, int *counts = nullptr, int N1 = -1);
 template <int DR>
 gma_status_t launch_causal_gamma(const Args &a, const CUtensorMap &vmap, const CUtensorMap &qmap,
                                  const CUtensorMap &gmap, int nblocks, cudaStream_t st);

@@ -93,6 +93,47 @@ __device__ __forceinline__ void key_softmax_reg(uint32_t tl, int K, int kc, bool
     }
 }
 
+// Output rows, components in tiles (more than 128 in all): this tile's numerator row (d_v columns
+// of TMEM at tl) and its normaliser den_eps (the tile's E_Q . Z (+ masked P sums), plus eps times
+// its E_Q row sum) go to the fp32 partial sums part [rows][d_v] and pden [rows]: the first tile
+// (pmode 1) writes them, every later one adds to them with reductions in L2 (no value comes back,
+// so nothing waits on the round trip); a last kernel divides.  Every lane loads (warp-collective).
+__device__ __forceinline__ void tile_partial_row(uint32_t tl, int d_v, float den_eps, bool valid, float *part,
+                                                 float *pden, long long orow, int pmode)
+{
+    float *pr = part + orow * d_v;
+#pragma unroll 1
+    for (int c = 0; c < (d_v + 31) / 32; ++c) {   // 32 columns per wait
+        uint32_t r[32];
+        if (d_v == 16) {
+            tmem_ld16(tl, *reinterpret_cast<uint32_t(*)[16]>(r));
+        } else {
+            tmem_ld32(tl + 32 * c, r);
+        }
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int col0 = 32 * c;
+        const int ncol = d_v - col0 < 32 ? d_v - col0 : 32;
+        float4 *p4 = reinterpret_cast<float4 *>(pr + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (4 * q >= ncol) continue;
+            const float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            if (pmode == 1)
+                p4[q] = v;
+            else
+                atomicAdd(p4 + q, v);   // (result unused: a reduction in L2)
+        }
+    }
+    if (valid) {
+        if (pmode == 1)
+            pden[orow] = den_eps;
+        else
+            atomicAdd(pden + orow, den_eps);
+    }
+}
+
 // Key side, components in tiles (more than 128 in all): Gamma_K row k of this tile is
 // exp2(L - lse) with lse the row's log2-sum-exp over every component (zeros beyond the tile's K
 // components and for rows past the sequence), as bf16 into the K-major SW128 tile gk.

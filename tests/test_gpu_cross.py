@@ -67,6 +67,8 @@ CASES = [
     (W.scaled(W.TINY_BIDIR_F32), 1, 1),
     (W.scaled(W.LM_CAUSAL, B=1, H=1, d_r=128, K=40, d_v=32, causal=False), 200, 333),
     (W.scaled(W.K_SWEEP[3], B=1, H=1, causal=False), 130, 260),
+    (W.scaled(W.LRA_BIDIR, B=2, H=1, K=200), 777, 300),              # components in tiles
+    (W.scaled(W.LM_CAUSAL, B=1, H=2, K=300, causal=False), 129, 1000),
 ]
 
 

@@ -68,20 +68,24 @@ def test_small_cases_match_oracle(w, flags):
     assert err <= TOL[w.dtype], (err, rowwise_error(O, ref))
 
 
-# more than 128 components on the tensor cores (causal): tiles of 128 components, the last one
-# partial, every tile's part added; ragged sequences, and each d_r / d_v the family takes
+# more than 128 components on the tensor cores: tiles of 128 components, the last one partial,
+# every tile's part added; ragged sequences, and each d_r / d_v the family takes; both variants
 TILED = [W.scaled(W.LM_CAUSAL, B=1, H=2, N=777, K=200),
          W.scaled(W.LM_CAUSAL, B=2, H=1, N=300, d_r=32, K=300, d_v=32),
          W.scaled(W.LM_CAUSAL, B=1, H=1, N=129, d_r=16, K=129, d_v=16),
          W.scaled(W.K_SWEEP[3], B=1, H=2, N=1000),
-         W.scaled(W.K_SWEEP[2], B=1, H=1, N=4000)]
+         W.scaled(W.K_SWEEP[2], B=1, H=1, N=4000),
+         W.scaled(W.LRA_BIDIR, B=2, H=2, N=777, K=200),
+         W.scaled(W.LM_CAUSAL, B=1, H=1, N=1500, d_r=16, K=400, d_v=16, causal=False),
+         W.scaled(W.K_SWEEP[3], B=1, H=2, N=1000, causal=False)]
 
 
-@pytest.mark.parametrize("w", TILED, ids=lambda w: f"B{w.B}H{w.H}N{w.N}r{w.d_r}K{w.K}v{w.d_v}")
-def test_component_tiles_causal_match_oracle(w):
+@pytest.mark.parametrize("w", TILED, ids=lambda w: f"{'c' if w.causal else 'b'}_B{w.B}H{w.H}N{w.N}r{w.d_r}K{w.K}v{w.d_v}")
+def test_component_tiles_match_oracle(w):
     gma = _gma()
     shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor)
-    assert gma.gma_kernel_family(shape, gma.GMA_VARIANT_CAUSAL) == 1
+    variant = gma.GMA_VARIANT_CAUSAL if w.causal else gma.GMA_VARIANT_BIDIRECTIONAL
+    assert gma.gma_kernel_family(shape, variant) == 1
     O, ref = _run(w)
     assert np.isfinite(O).all()
     assert normwise_error(O, ref) <= TOL["bf16"], (normwise_error(O, ref), rowwise_error(O, ref))
