@@ -399,36 +399,66 @@ def run_gma(args, ws, rank, local):
     traffic = traffic_per_launch(dom, w)
     roofline["traffic"] = traffic
 
-    # end to end through the C ABI with pinned host buffers
-    e2e_steps = max(3, min(steps, 10))
+    # end to end through the C ABI with pinned host buffers.  Every step copies its own inputs from
+    # pinned host memory, runs the call, and reads its output back.  Steps are pipelined over one
+    # copy stream and the compute stream, with two device sets of inputs and outputs: step i + 1's
+    # inputs cross the host link while step i computes, then step i's output comes back.  (The
+    # copies themselves stay in one stream: copies in both directions at once ran slower on the
+    # largest workload.)  A set is refilled only after its previous step finished with it.
+    e2e_steps = max(4, min(steps, 12))
     pin = {k: host[k].pin_memory() for k in ("QX", "KX", "V", "mu", "raw", "logits")}
-    O_host = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    O_host = [torch.empty(O.shape, dtype=O.dtype).pin_memory() for _ in range(2)]
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in pin)
-    d2h = O_host.numel() * O_host.element_size()
+    d2h = O_host[0].numel() * O_host[0].element_size()
+    sets = [(dev, O), ({k: torch.empty_like(dev[k]) for k in pin}, torch.empty_like(O))]
+    s_copy = torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k in pin:
-            dev[k].copy_(pin[k], non_blocking=True)
-        step()
-        O_host.copy_(O, non_blocking=True)
+    def e2e_run(n):
+        def copy_in(i):
+            d, _ = sets[i % 2]
+            with torch.cuda.stream(s_copy):   # (after step i - 2's output left: same stream)
+                for k in pin:
+                    d[k].copy_(pin[k], non_blocking=True)
+                ev_in[i % 2].record(s_copy)
+
+        copy_in(0)
+        for i in range(n):
+            b = i % 2
+            d, o = sets[b]
+            if i + 1 < n:
+                copy_in(i + 1)
+            stream.wait_event(ev_in[b])
+            p = [d[k].data_ptr() for k in ("QX", "KX", "V", "mu", "raw", "logits")]
+            r = fn(shape, *p, o.data_ptr(), workspace.data_ptr(), ws_n, sh)
+            if r != 0:
+                raise gma.GmaError(r, fn.__name__)
+            ev_done[b].record(stream)
+            s_copy.wait_event(ev_done[b])
+            with torch.cuda.stream(s_copy):
+                O_host[b].copy_(o, non_blocking=True)
 
     e2e = None
     if not args.no_e2e:
-        with torch.cuda.stream(stream):
-            e2e_step()
-        stream.synchronize()
+        e2e_run(2)
+        torch.cuda.synchronize()
         barrier(ws)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for _ in range(e2e_steps):
-                e2e_step()
-            b.record(stream)
+        a.record(s_copy)
+        stream.wait_event(a)
+        e2e_run(e2e_steps)
+        s_copy.wait_stream(stream)
+        b.record(s_copy)
         torch.cuda.synchronize()
         barrier(ws)
         e2e_ms = max_over_ranks(a.elapsed_time(b), ws, device)
+        e2e_ok = torch.equal(O_host[0], O_host[1])   # the same inputs every step: the same bits
         e2e = {"value": w.tokens * ws * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "pipelined": "one copy stream and the compute stream: step i+1's inputs cross the "
+                            "host link while step i computes, then step i's output comes back",
+               "outputs_repeat": bool(e2e_ok)}
 
     if rank != 0:
         return None

@@ -702,21 +702,32 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
 }
 
 // Components in tiles: O = numerator / normaliser, both summed over the tiles in part / pden
-// (one thread per four output values).
+// (one thread per sixteen output values, four 16-byte streaming loads in flight each).
 __global__ void __launch_bounds__(256) tc_divide_kernel(const float *__restrict__ part, const float *__restrict__ pden,
                                                         void *__restrict__ O, long long rows, int d_v, int out_f32)
 {
-    grid_dependency_wait();   // the partial sums come from the output passes before
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of four values
-    const int per_row = d_v / 4;
+    grid_dependency_wait();   // the partial sums come from the passes before
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // group of sixteen values
+    const int per_row = d_v / 16;
     if (i >= rows * per_row) return;
-    const long long row = i / per_row;
-    const float inv = 1.0f / pden[row];
-    const float4 v = reinterpret_cast<const float4 *>(part)[i];
-    if (out_f32)
-        reinterpret_cast<float4 *>(O)[i] = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
-    else
-        reinterpret_cast<uint2 *>(O)[i] = make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+    const float inv = 1.0f / pden[i / per_row];
+    const float4 *src = reinterpret_cast<const float4 *>(part) + 4 * i;
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = __ldcs(src + j);
+    if (out_f32) {
+        float4 *dst = reinterpret_cast<float4 *>(O) + 4 * i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) __stcs(dst + j, make_float4(v[j].x * inv, v[j].y * inv, v[j].z * inv, v[j].w * inv));
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(O) + 2 * i;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            __stcs(dst + j, make_uint4(pack_bf16(v[2 * j].x * inv, v[2 * j].y * inv),
+                                       pack_bf16(v[2 * j].z * inv, v[2 * j].w * inv),
+                                       pack_bf16(v[2 * j + 1].x * inv, v[2 * j + 1].y * inv),
+                                       pack_bf16(v[2 * j + 1].z * inv, v[2 * j + 1].w * inv)));
+    }
 }
 
 // Causal, more than 128 components: the log2-sum-exp of every query and key row over all
@@ -766,7 +777,7 @@ gma_status_t tiled_causal_dr(const gma_shape_t &s, const void *QX, const void *K
         at.v128 = s.d_v % 64 == 0 ? 1 : 0;
         if ((r = launch_causal_gamma<DR>(at, vmap_o, qmap, gmap, BH * p.nseg, st)) != GMA_OK) return r;
     }
-    const long long groups = (long long)BH * s.N * (s.d_v / 4);
+    const long long groups = (long long)BH * s.N * (s.d_v / 16);
     cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_DIVIDE, st,
                (e = launch_pdl(tc_divide_kernel, dim3((unsigned)((groups + 255) / 256)), dim3(256), 0, st,
@@ -829,7 +840,7 @@ gma_status_t tiled_bidir_dr(const gma_shape_t &sk, const void *QX, const void *K
         aq.pmode = t == 0 ? 1 : 2;
         if ((r = launch_bidir_read2<DR>(aq, qmap, BH * pq.nseg, st)) != GMA_OK) return r;
     }
-    const long long groups = (long long)BH * n_q * (sk.d_v / 4);
+    const long long groups = (long long)BH * n_q * (sk.d_v / 16);
     cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_DIVIDE, st,
                (e = launch_pdl(tc_divide_kernel, dim3((unsigned)((groups + 255) / 256)), dim3(256), 0, st,
