@@ -103,7 +103,10 @@ typedef struct {
  * The workspace must be 256-byte aligned.  Its first 256 bytes hold the error word that
  * gma_check_workspace reads.  For the causal variant on the tensor-core path (bf16, no
  * GMA_FLAG_SIMT) it includes the key responsibilities of every token, B*H*N*Kp bf16 values
- * (Kp = 64 for K <= 64, else 128), unless GMA_FLAG_RECOMPUTE_KEYS is set. */
+ * (Kp = 64 for K <= 64, else 128), unless GMA_FLAG_RECOMPUTE_KEYS is set.  With K > 128 on the
+ * tensor-core path (components in tiles of 128) it also holds every routing row's log-sum-exp
+ * over all components (fp32) and, for the forward passes, fp32 partial sums of the queries'
+ * numerators and normalisers (B*H*N*(d_v + 1) floats). */
 size_t gma_workspace_size(const gma_shape_t *shape, int variant);
 
 /* Posterior responsibilities (Méthodologie §1):
@@ -225,8 +228,10 @@ gma_status_t gma_noalloc_check(gma_stream_t stream);
 gma_status_t gma_check_workspace(const void *workspace, gma_stream_t stream);
 
 /* Which kernel family a call with this shape and variant runs: 0 = fp32 CUDA-core kernels,
- * 1 = tcgen05 tensor-core kernels, -1 = the shape is invalid.  The decode step (N == 1) always
- * runs on the CUDA cores. */
+ * 1 = tcgen05 tensor-core kernels, -1 = the shape is invalid.  The tensor-core family takes bf16
+ * inputs with d_r <= 64 and d_v <= 128 (a multiple of 16) for every K up to 1024; fp32 inputs,
+ * d_r = 128 and GMA_FLAG_SIMT take the CUDA cores.  The decode step (N == 1) and the backward
+ * pass always run on the CUDA cores. */
 int gma_kernel_family(const gma_shape_t *shape, int variant);
 
 /* Static description of a status code. */
