@@ -73,6 +73,11 @@ def kernel_work(w, name):
         # the output pass reads Q_X and V and writes O (K_X is read by the segment pass; the
         # stored Gamma_K it also reads is not algorithmic traffic)
         return "hbm", th * esz * (w.d_r + 2 * w.d_v), "GB/s"
+    if name == "tc_causal_single_launch":
+        # the whole causal path in one launch: Q_X, K_X and V read once, O written (its second
+        # sweep's re-read of K_X and V, and the segment memories it exchanges, are not
+        # algorithmic traffic)
+        return "hbm", th * esz * (2 * w.d_r + 2 * w.d_v), "GB/s"
     if name == "tc_causal_segment_memory":   # the write pass (key side)
         return "hbm", w.key_heads * esz * (w.d_r + w.d_v), "GB/s"
     if name == "tc_bidir_write":
@@ -271,8 +276,13 @@ def run_gma(args, ws, rank, local):
     w = W.Workload(**{**w0.__dict__, **over})
     host = W.make_inputs(w)
     dev = {k: v.to(device) for k, v in host.items()}
+    single, recompute = bool(args.single_pass), bool(args.recompute_keys)
+    if (single or recompute) and not w.causal:
+        raise SystemExit("--single-pass and --recompute-keys apply to causal workloads only")
     shape = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v,
-                           gma.GMA_BF16 if w.dtype == "bf16" else gma.GMA_F32, w.eps, w.var_floor)
+                           gma.GMA_BF16 if w.dtype == "bf16" else gma.GMA_F32, w.eps, w.var_floor,
+                           flags=(gma.GMA_FLAG_SINGLE_PASS if single else 0)
+                           | (gma.GMA_FLAG_RECOMPUTE_KEYS if recompute else 0))
     variant = gma.GMA_VARIANT_CAUSAL if w.causal else gma.GMA_VARIANT_BIDIRECTIONAL
     ws_n = (gma.gma_workspace_size_cross(shape, w.N_k) if w.N_k
             else gma.gma_workspace_size(shape, variant))
@@ -474,7 +484,9 @@ def run_gma(args, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded N(0,1) routing vectors and values)",
         "config": {"workload": w0.name,
-                   "variant": "cross" if w.N_k else ("causal" if w.causal else "bidirectional"),
+                   "variant": "cross" if w.N_k else ("causal single-launch (GMA_FLAG_SINGLE_PASS)" if single
+                                                     else "causal, keys recomputed (GMA_FLAG_RECOMPUTE_KEYS)"
+                                                     if recompute else "causal" if w.causal else "bidirectional"),
                    "B": w.B, "H": w.H, "N": w.N, "N_k": w.keys, "d_r": w.d_r, "K": w.K, "d_v": w.d_v,
                    "eps": w.eps, "var_floor": w.var_floor,
                    "kernel_family": "tcgen05" if fam == 1 else "fp32 cuda-core",
@@ -1114,6 +1126,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: run the workload with this many heads instead")
+    ap.add_argument("--single-pass", action="store_true",
+                    help="causal workloads: time the single-launch variant (GMA_FLAG_SINGLE_PASS)")
+    ap.add_argument("--recompute-keys", action="store_true",
+                    help="causal workloads: time the variant that recomputes Gamma_K (GMA_FLAG_RECOMPUTE_KEYS)")
     args = ap.parse_args()
 
     if args.impl == "reference":

@@ -71,14 +71,25 @@ typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype_t;
 #define GMA_FLAG_RECOMPUTE_KEYS 0x4u /* causal, tensor-core path: recompute the key
                                       * responsibilities in the output pass instead of keeping
                                       * them in the workspace (smaller workspace, slower)     */
+#define GMA_FLAG_SINGLE_PASS 0x8u /* causal, tensor-core path: the fused variant (page's
+                                   * Méthodologie §2-§3): one kernel launch after the parameter
+                                   * kernel, the responsibilities never written to memory.
+                                   * Each CTA sweeps its segment's keys for the segment's own
+                                   * memory, exchanges memories with the preceding segments of
+                                   * its slice through the workspace (decoupled look-back, every
+                                   * wait bounded), then runs the output sweep.  Needs K <= 128
+                                   * and a shape the tensor-core family covers: otherwise the
+                                   * call returns GMA_ERR_UNSUPPORTED_SHAPE.  Other entry points
+                                   * ignore it.                                              */
 #define GMA_FLAG_TEST_WITHHOLD 0x80000000u
 /* For tests of the device-side timeout path only; never set it in production.  The call's
  * bounded waits give up after about a millisecond instead of a second, and the tensor-core
  * causal and bidirectional key passes withhold one row-phase hand-off (the signal that the
  * first chunk's [x^2, x] tile is built), so the waits on it run out: every role of the kernel
  * leaves its loop, tensor memory is released, and gma_check_workspace then reports
- * GMA_ERR_TIMEOUT.  The output of such a call is undefined; the next call without the flag on
- * the same stream runs normally. */
+ * GMA_ERR_TIMEOUT.  With GMA_FLAG_SINGLE_PASS only the first segment of each slice withholds
+ * it; the other segments learn of its failure through the look-back and stop.  The output of
+ * such a call is undefined; the next call without the flag on the same stream runs normally. */
 
 typedef struct {
     int B, H, N;     /* batch, heads, sequence length                                       */

@@ -18,7 +18,8 @@ gma_status_t validate_shape(const gma_shape_t *s, int variant)
     if (s->B < 1 || s->H < 1 || s->N < 1 || s->K < 1) return GMA_ERR_INVALID_ARG;
     if (s->dtype != GMA_F32 && s->dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
     if (!(s->var_floor >= 0.f) || !(s->eps >= 0.f)) return GMA_ERR_INVALID_ARG;
-    if (s->flags & ~(GMA_FLAG_SIMT | GMA_FLAG_OUT_F32 | GMA_FLAG_RECOMPUTE_KEYS | GMA_FLAG_TEST_WITHHOLD))
+    if (s->flags & ~(GMA_FLAG_SIMT | GMA_FLAG_OUT_F32 | GMA_FLAG_RECOMPUTE_KEYS | GMA_FLAG_SINGLE_PASS |
+                     GMA_FLAG_TEST_WITHHOLD))
         return GMA_ERR_INVALID_ARG;
     if (!valid_dim(s->d_r) || s->K > 1024) return GMA_ERR_UNSUPPORTED_SHAPE;
     if (variant != GMA_VARIANT_RESPONSIBILITIES && !valid_dim(s->d_v))
@@ -32,6 +33,12 @@ gma_status_t validate_shape(const gma_shape_t *s, int variant)
 
 // 1 = tcgen05 tensor-core family (bf16 inputs it covers), 0 = fp32 CUDA-core family.
 int family_of(const gma_shape_t &s, int variant) { return tc_supported(s, variant) ? 1 : 0; }
+
+// The single-launch causal variant exists in the tensor-core family only.
+bool single_pass_unsupported(const gma_shape_t &s, int variant)
+{
+    return variant == GMA_VARIANT_CAUSAL && (s.flags & GMA_FLAG_SINGLE_PASS) && family_of(s, variant) != 1;
+}
 
 gma_status_t check_device()
 {
@@ -87,6 +94,7 @@ gma_status_t forward_common(bool causal, const gma_shape_t *s, const void *QX, c
     const int variant = causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL;
     gma_status_t r = validate_shape(s, variant);
     if (r != GMA_OK) return r;
+    if (single_pass_unsupported(*s, variant)) return GMA_ERR_UNSUPPORTED_SHAPE;
     const void *ptrs[] = {QX, KX, V, mu, raw, logits, O};
     for (const void *p : ptrs)
         if (!p || !aligned16(p)) return GMA_ERR_INVALID_ARG;
@@ -117,7 +125,7 @@ size_t gma_workspace_size(const gma_shape_t *s, int variant)
         return backward_workspace_size(*s);
     }
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return 0;
-    if (validate_shape(s, variant) != GMA_OK) return 0;
+    if (validate_shape(s, variant) != GMA_OK || single_pass_unsupported(*s, variant)) return 0;
     return family_of(*s, variant) == 1 ? tc_workspace_size(*s, variant)
                                        : simt_workspace_size(*s, variant);
 }
@@ -129,7 +137,7 @@ int gma_kernel_family(const gma_shape_t *s, int variant)
     if (variant == GMA_VARIANT_USAGE) variant = GMA_VARIANT_RESPONSIBILITIES;
     if (variant == GMA_VARIANT_BACKWARD) return validate_shape(s, GMA_VARIANT_CAUSAL) == GMA_OK ? 0 : -1;
     if (variant < GMA_VARIANT_RESPONSIBILITIES || variant > GMA_VARIANT_CAUSAL) return -1;
-    if (validate_shape(s, variant) != GMA_OK) return -1;
+    if (validate_shape(s, variant) != GMA_OK || single_pass_unsupported(*s, variant)) return -1;
     return family_of(*s, variant);
 }
 

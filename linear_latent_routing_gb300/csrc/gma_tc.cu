@@ -471,6 +471,7 @@ struct Plan {
     int nseg, cps;              // forward: segments per slice and chunks per segment
     int kg;                     // causal: components per stored key-responsibility row (64 or 128)
     size_t off_bimg, off_cst, off_agg, off_gam, total;
+    size_t off_flags, off_incl; // single-launch causal: ticket and flags, inclusive prefixes
 };
 
 constexpr int kSms = 152;   // GB300
@@ -500,6 +501,9 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1, int n_q = -1)
         p.cps = (nchunks + n - 1) / n;
         p.nseg = (nchunks + p.cps - 1) / p.cps;
     } else {
+        // (The single-launch causal kernel takes the same split.  Its second sweep re-reads each
+        // segment's key rows and values; segments short enough for those of all CTAs in flight to
+        // stay in L2 were measured slower: the look-back and the per-segment set-up cost more.)
         double best = 1e30;
         int best_n = 1;
         const int top = nchunks < 2048 ? nchunks : 2048;
@@ -522,7 +526,11 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1, int n_q = -1)
     p.off_cst = c.take(sizeof(float) * (size_t)s.H * p.ntile * p.kn16);
     if (variant != GMA_VARIANT_RESPONSIBILITIES)
         p.off_agg = c.take(sizeof(float) * (size_t)BH * p.nseg * KMAX * p.ne);
-    if (variant == GMA_VARIANT_CAUSAL && !(s.flags & GMA_FLAG_RECOMPUTE_KEYS)) {
+    if (variant == GMA_VARIANT_CAUSAL && (s.flags & GMA_FLAG_SINGLE_PASS)) {
+        // the single-launch kernel: segment tickets and flags; agg holds the segments' own memories
+        p.off_flags = c.take(sizeof(int) * (1 + (size_t)BH * p.nseg));
+        p.off_incl = c.take(sizeof(float) * (size_t)BH * p.nseg * KMAX * p.ne);
+    } else if (variant == GMA_VARIANT_CAUSAL && !(s.flags & GMA_FLAG_RECOMPUTE_KEYS)) {
         // Gamma_K of every token, written by the segment pass and read by the output pass
         p.kg = p.kn16 <= 64 ? 64 : 128;
         p.off_gam = c.take((size_t)2 * BH * s.N * p.kg);
@@ -629,6 +637,10 @@ gma_status_t launch_params(const gma_shape_t &s, const Plan &p, char *ws, const 
     return GMA_OK;
 }
 
+template <int DR>   // gma_tc_causal.cu
+gma_status_t launch_causal_fused(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap,
+                                 const CUtensorMap &qmap, int *ticket_flags, float *incl, int nblocks, cudaStream_t st);
+
 // `s` describes the keys (s.N keys); `pq` splits the queries, of which there are n_q (the same
 // as s.N but for cross-attention, which is bidirectional).
 template <int DR>
@@ -647,6 +659,13 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
     if (a.gam && !make_gmap(&gmap, a.gam, BH, s.N, p.kg)) return GMA_ERR_CUDA;
     CUtensorMap kmap;
     if (!make_xmap(&kmap, a.KX, BH, s.N, DR)) return GMA_ERR_CUDA;
+    if (causal && p.off_flags) {
+        // one launch: segment memories by look-back (ticket and flags zeroed by the caller)
+        CUtensorMap qmap;
+        if (!make_xmap(&qmap, a.QX, BH, s.N, DR)) return GMA_ERR_CUDA;
+        return launch_causal_fused<DR>(a, vmap, kmap, qmap, (int *)(ws + p.off_flags), (float *)(ws + p.off_incl),
+                                       BH * p.nseg, st);
+    }
     {
         const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, kmap, gmap, BH * p.nseg, st);
         if (r != GMA_OK) return r;
@@ -886,7 +905,8 @@ bool tc_supported(const gma_shape_t &s, int variant)
     if (!(s.d_r == 16 || s.d_r == 32 || s.d_r == 64)) return false;
     // more than 128 components: in tiles of 128 (the causal path only with stored key
     // responsibilities)
-    if (s.K > tck::KMAX && variant == GMA_VARIANT_CAUSAL && (s.flags & GMA_FLAG_RECOMPUTE_KEYS)) return false;
+    if (s.K > tck::KMAX && variant == GMA_VARIANT_CAUSAL && (s.flags & (GMA_FLAG_RECOMPUTE_KEYS | GMA_FLAG_SINGLE_PASS)))
+        return false;
     // value tiles move in 16-column TMA boxes, and the numerator and memory hold d_v <= 128
     // TMEM columns each
     if (s.d_v % 16 != 0 || s.d_v > 128) return false;
@@ -957,6 +977,9 @@ gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *
     const tck::Plan pq = causal ? p
                                 : tck::make_plan(s, variant, tck::bidir_read2_ctas_per_sm(s.d_r, p.kn16, s.d_v));
     char *w = (char *)ws;
+    if (p.off_flags &&   // the single-launch kernel's ticket and flags start at zero
+        cudaMemsetAsync(w + p.off_flags, 0, sizeof(int) * (1 + (size_t)s.B * s.H * p.nseg), st) != cudaSuccess)
+        return GMA_ERR_CUDA;
     gma_status_t r = tck::launch_params(s, p, w, mu, raw, logits, st);
     if (r != GMA_OK) return r;
     if (p.ntile > 1 && causal) {

@@ -29,6 +29,22 @@
 // Tensor memory (512 columns): [0,128) key logits, then P; [128,256) query logits, then E_Q;
 // [256,384) output numerator; [384,512) the running memory S.
 // Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all roles leave their loops.
+//
+// Single-launch variant (FUSED): the CTAs take their segments from a ticket counter (all slices'
+// first segments, then their second ones, ...), and each computes its own segment memory before
+// the sweep above:
+//   sweep 1:  S_own = sum over the segment's chunks of E_K^T V' (tensor cores, TMEM [384,512)),
+//             Z_own = sum of E_K^T r (CUDA cores), with two key-row and value buffers (the query
+//             tile and the S operand tile are free until sweep 2);
+//   look-back: S_own is published; the exclusive prefix S_start is summed backwards over the
+//             published memories of the preceding segments of the slice, into TMEM [256,384),
+//             until a segment whose inclusive prefix is published; S_start + S_own is then
+//             published as this segment's inclusive prefix;
+//   sweep 2:  the chunk loop above, from S_start held in TMEM.
+// The key responsibilities never leave the chip; the memories pass through global memory (L2).
+// A CTA only waits on segments with an earlier ticket, which are resident or finished, so the
+// waits always end; they are bounded all the same, and a segment that fails publishes that, so
+// that its successors stop waiting for it.
 #include "tc_rows.cuh"
 
 namespace gma {
@@ -43,7 +59,23 @@ enum BarId {
     B_LK, B_LQ, B_S, B_PQ, B_PV,                              // tcgen05.commit
     NBAR
 };
+// Sweep 1 of the single-launch variant: key rows and value tiles of chunk c in buffer c & 1.
+enum FBar {
+    F_X0 = NBAR, F_X1, F_V0, F_V1,   // TMA (transaction counts)
+    F_AK, F_GK, F_VS, F_ZP,          // 128 threads of one role
+    F_LK0, F_LK1, F_S,               // tcgen05.commit
+    F_END
+};
 constexpr uint32_t R_LK = 0, R_LQ = 128, R_O = 256, R_S = 384;
+static_assert(KMAX == C, "the S operand tile doubles as a value buffer in sweep 1");
+
+// Segment memories of the single-launch variant, exchanged between CTAs (global memory).
+struct LookBack {
+    int *ticket;    // one counter, zero before the launch: segments in start order
+    int *flag;      // [BH][nseg]: 0 nothing yet, 1 own memory, 2 inclusive prefix, 3 failed
+    float *own;     // [BH][nseg][KMAX][ne]: the segment's own memory (d_v columns, Z at d_v)
+    float *incl;    // [BH][nseg][KMAX][ne]: the memory of the slice's segments up to this one
+};
 
 struct CausalSmem {
     uint32_t bimg, ax, abk, abq, gk, sp, ve, zbuf, zpart, rbuf, dsm, bars, misc, total;
@@ -64,8 +96,8 @@ struct CausalSmem {
         zpart = o; o += 2u * 8u * KMAX * 4u;  // partial column sums by chunk parity
         rbuf = o; o += (uint32_t)C * 4u;      // r of the chunk's keys
         dsm = o; o += 2u * C * 8u;            // (row sum, normaliser) per query row, by chunk parity
-        bars = o; o += NBAR * 8u;
-        misc = o; o += 16u;
+        bars = o; o += F_END * 8u;
+        misc = o; o += 16u;   // TMEM base, abort word, ticket, look-back broadcast
         total = o;
     }
 };
@@ -268,15 +300,139 @@ __device__ __forceinline__ void write_output(uint32_t tl, int d_v, float inv, bo
     }
 }
 
+// ------------------------------------------------------------------ look-back (FUSED)
+__device__ __forceinline__ int flag_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void flag_release(int *p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A predecessor's flag once it is set (1 or 2), or 3 if it failed, this CTA is aborting, or the
+// wait ran out (recorded as a timeout).
+__device__ __forceinline__ int wait_flag(const int *p, WsHeader *hdr, volatile int *abort)
+{
+    int v = flag_acquire(p);
+    if (v) return v;
+    const long long t0 = clock64();
+    while (true) {
+        __nanosleep(100);
+        v = flag_acquire(p);
+        if (v) return v;
+        if (*abort) return 3;
+        if (wait_expired(clock64() - t0, hdr)) {
+            record_error(hdr, GMA_ERR_TIMEOUT, 130);
+            return 3;
+        }
+    }
+}
+
+// Row k of a memory, d_v fp32 columns of TMEM at tl plus its Z entry z, into the global row dst.
+__device__ __forceinline__ void row_to_global(uint32_t tl, int d_v, float z, float *dst)
+{
+    for (int b = 0; b < d_v / 16; ++b) {
+        uint32_t r[16];
+        tmem_ld16(tl + 16 * b, r);
+        tmem_ld_wait();
+        float4 *o4 = reinterpret_cast<float4 *>(dst + 16 * b);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            o4[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+    }
+    dst[d_v] = z;
+}
+
+// TMEM row at tl (d_v fp32 columns) = (first ? 0 : itself) + the sum of the published rows k of
+// the n segments in list (entry 2 j + 1: segment j's inclusive prefix, 2 j: its own memory; slot0
+// = the slice's first segment); returns the sum of their Z entries.  The rows were published by
+// other CTAs: read through L2, four segments' loads in flight at a time.
+__device__ __forceinline__ float rows_add_list(uint32_t tl, int d_v, const int *list, int n, const LookBack &lb,
+                                               size_t slot0, int k, int ne, bool first)
+{
+    for (int b = 0; b < d_v / 16; ++b) {
+        uint32_t r[16];
+        if (first) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = 0u;
+        } else {
+            tmem_ld16(tl + 16 * b, r);
+            tmem_ld_wait();
+        }
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = __uint_as_float(r[j]);
+#pragma unroll 4
+        for (int i = 0; i < n; ++i) {
+            const int e = list[i];
+            const float4 *s4 = reinterpret_cast<const float4 *>(
+                ((e & 1) ? lb.incl : lb.own) + ((slot0 + (size_t)(e >> 1)) * KMAX + k) * ne + 16 * b);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = __ldcg(s4 + q);
+                acc[4 * q] += f.x;
+                acc[4 * q + 1] += f.y;
+                acc[4 * q + 2] += f.z;
+                acc[4 * q + 3] += f.w;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(acc[j]);
+        tmem_st16(tl + 16 * b, r);
+    }
+    tmem_st_wait();
+    float z = 0.f;
+    for (int i = 0; i < n; ++i) {
+        const int e = list[i];
+        z += __ldcg(((e & 1) ? lb.incl : lb.own) + ((slot0 + (size_t)(e >> 1)) * KMAX + k) * ne + d_v);
+    }
+    return z;
+}
+
+// TMEM row at tl (d_v fp32 columns) = 0.
+__device__ __forceinline__ void row_zero(uint32_t tl, int d_v)
+{
+    uint32_t r[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) r[j] = 0u;
+    for (int b = 0; b < d_v / 16; ++b) tmem_st16(tl + 16 * b, r);
+    tmem_st_wait();
+}
+
+// Global row dst = TMEM rows at ta + tb (d_v fp32 columns each) and Z entry z.
+__device__ __forceinline__ void rows_sum_to_global(uint32_t ta, uint32_t tb, int d_v, float z, float *dst)
+{
+    for (int b = 0; b < d_v / 16; ++b) {
+        uint32_t ra[16], rb[16];
+        tmem_ld16(ta + 16 * b, ra);
+        tmem_ld16(tb + 16 * b, rb);
+        tmem_ld_wait();
+        float4 *o4 = reinterpret_cast<float4 *>(dst + 16 * b);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            o4[q] = make_float4(__uint_as_float(ra[4 * q]) + __uint_as_float(rb[4 * q]),
+                                __uint_as_float(ra[4 * q + 1]) + __uint_as_float(rb[4 * q + 1]),
+                                __uint_as_float(ra[4 * q + 2]) + __uint_as_float(rb[4 * q + 2]),
+                                __uint_as_float(ra[4 * q + 3]) + __uint_as_float(rb[4 * q + 3]));
+    }
+    dst[d_v] = z;
+}
+
 }  // namespace
 
-template <int DR>
+template <int DR, bool FUSED>
 __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const Args a,
                                                                           const __grid_constant__ CUtensorMap vmap,
                                                                           const __grid_constant__ CUtensorMap kmap,
-                                                                          const __grid_constant__ CUtensorMap qmap)
+                                                                          const __grid_constant__ CUtensorMap qmap,
+                                                                          const LookBack lb)
 {
-    grid_dependency_wait();   // the scanned memories come from the kernels before
+    grid_dependency_wait();   // the scanned memories (or, FUSED, the parameter tables) come from the kernels before
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const CausalSmem L(DR, a.kn16, a.d_v);
@@ -287,21 +443,22 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
     float *zpart = reinterpret_cast<float *>(smem + L.zpart);
     float *rbuf = reinterpret_cast<float *>(smem + L.rbuf);
     float2 *dsm = reinterpret_cast<float2 *>(smem + L.dsm);
-    const int bh = blockIdx.x / a.nseg, seg = blockIdx.x % a.nseg, h = bh % a.H;
+    volatile int *tkslot = reinterpret_cast<volatile int *>(smem + L.misc + 8);
+    volatile int *lbcast = reinterpret_cast<volatile int *>(smem + L.misc + 12);
     const int t = threadIdx.x, warp = t >> 5;
-    const int tok0 = seg * a.cps * C;
-    const int tok_end = min(a.N, tok0 + a.cps * C);
-    const int nch = (tok_end - tok0 + C - 1) / C;
     const int d_v = a.d_v;
     const int kc = (a.K + 31) >> 5;
     constexpr uint32_t XT = (uint32_t)C * DR * 2;   // bytes of one [x] tile (the TMA destination)
 
     // ---------------------------------------------------------------- set-up (all threads)
+    if (FUSED && t == 0) *tkslot = atomicAdd(lb.ticket, 1);
     if (warp == 12) {
         if (t == 384) {
-            static const uint32_t counts[NBAR] = {1,   1,   1,   1,   128, 128, 128, 128, 128,
-                                                  128, 128, 128, 128, 1,   1,   1,   1,   1};
-            for (int i = 0; i < NBAR; ++i) mbar_init(bars + i, counts[i]);
+            static const uint32_t counts[F_END] = {1,   1,   1,   1,   128, 128, 128, 128, 128,
+                                                   128, 128, 128, 128, 1,   1,   1,   1,   1,
+                                                   1,   1,   1,   1,   128, 128, 128, 128, 1, 1, 1};
+            const int nb = FUSED ? (int)F_END : (int)NBAR;
+            for (int i = 0; i < nb; ++i) mbar_init(bars + i, counts[i]);
             *abort = 0;
             fence_mbar_init();
         }
@@ -325,7 +482,195 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
+    // the segment: by block index, or (FUSED) by ticket, segment-major (ticket = seg * BH + bh), so
+    // that the segments running at once spread over all slices and each one's look-back meets an
+    // inclusive prefix within a few steps
+    const int nbh = (int)gridDim.x / a.nseg;
+    const int tk = FUSED ? *tkslot : (int)blockIdx.x;
+    const int bh = FUSED ? tk % nbh : tk / a.nseg, seg = FUSED ? tk / nbh : tk % a.nseg, h = bh % a.H;
+    const int tok0 = seg * a.cps * C;
+    const int tok_end = min(a.N, tok0 + a.cps * C);
+    const int nch = (tok_end - tok0 + C - 1) / C;
 
+    float zexcl = 0.f;   // FUSED, state side: the Z entry of this row of S_start
+    if constexpr (FUSED) {
+        // ============================================================ sweep 1 and look-back
+        uint8_t *const xb0 = smem + L.abk, *const xb1 = smem + L.abq;   // key rows by chunk parity
+        uint8_t *const vb0 = smem + L.ve, *const vb1 = smem + L.sp;     // value tiles by chunk parity
+        if (warp == 12) {
+            if (t == 384) {
+                const uint32_t id_s = idesc_f16(128, (uint32_t)d_v, 1, 1, 1, 1);
+                int last_s = -1, last_x[2] = {-1, -1};
+                auto load = [&](int c) {
+                    const int b = c & 1;
+                    load_x_tile((b ? xb1 : xb0) + XT, &kmap, bars + F_X0 + b, DR, tok0 + c * C, bh);
+                    load_v_chunk(b ? vb1 : vb0, &vmap, bars + F_V0 + b, d_v, tok0 + c * C, bh);
+                    last_x[b] = c;
+                };
+                mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
+                bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + B_BIMG);
+                for (int c = 0; c < 2 && c < nch; ++c) load(c);
+                bool ok = mbar_wait_abortable(bars + B_BIMG, 0, a.hdr, 100, abort);
+                const uint32_t bimg = sb + L.bimg, bconst = sb + L.bimg + (uint32_t)a.bimg_main_bytes;
+                // S_own += E_K^T V' of chunk j; the chunk's buffers then take chunk j + 2 (its key
+                // rows were read by its logits, complete before its E_K was written)
+                auto update = [&](int j) -> bool {
+                    if (!mbar_wait_abortable(bars + F_GK, j & 1, a.hdr, 101, abort)) return false;
+                    if (!mbar_wait_abortable(bars + F_VS, j & 1, a.hdr, 102, abort)) return false;
+                    tc_fence_after();
+                    const uint32_t vb = sb + ((j & 1) ? L.sp : L.ve);
+                    for (int s = 0; s < C / 16; ++s)
+                        mma_f16(tmem + R_S, mn128desc(sb + L.gk, s, C), mn32desc(vb, s, C), id_s,
+                                (j > 0 || s > 0) ? 1u : 0u);
+                    mma_commit(bars + F_S);
+                    last_s = j;
+                    if (j + 2 < nch) {
+                        if (!mbar_wait_abortable(bars + F_S, j & 1, a.hdr, 103, abort)) return false;
+                        load(j + 2);
+                    }
+                    return true;
+                };
+                for (int c = 0; ok && c < nch; ++c) {
+                    const int b = c & 1;
+                    if (!(ok = mbar_wait_abortable(bars + F_AK, c & 1, a.hdr, 104, abort))) break;
+                    tc_fence_after();
+                    issue_logits_x<DR>(tmem + (b ? R_LQ : R_LK), sb + (b ? L.abq : L.abk), bimg, bconst, sb + L.ax,
+                                       a.kn16);
+                    mma_commit(bars + F_LK0 + b);
+                    if (c >= 1 && !(ok = update(c - 1))) break;
+                }
+                if (ok && nch > 0) ok = update(nch - 1);
+                // drain: the last update, and loads still in flight (only after a timeout)
+                if (last_s >= 0) mbar_wait(bars + F_S, last_s & 1, a.hdr, 105);
+                for (int b = 0; b < 2; ++b)
+                    if (last_x[b] >= 0) {
+                        mbar_wait(bars + F_X0 + b, (last_x[b] >> 1) & 1, a.hdr, 106);
+                        mbar_wait(bars + F_V0 + b, (last_x[b] >> 1) & 1, a.hdr, 106);
+                    }
+            }
+        } else if (warp < 4) {
+            // key side: [x^2, x], E_K and r, V' = diag(r) V
+            const int k = t;
+            const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+            for (int c = 0; c < nch; ++c) {
+                const int b = c & 1;
+                const uint32_t pb = (c >> 1) & 1;
+                if (!mbar_wait_abortable(bars + F_X0 + b, pb, a.hdr, 110, abort)) break;
+                build_inplace<DR>(b ? xb1 : xb0, k);
+                fence_proxy_async_smem();
+                // (a test of the timeout path withholds the first segment's first signal: that
+                // segment's waits run out, and its successors learn of it by the look-back)
+                if (!(a.test_withhold && seg == 0 && c == 0)) mbar_arrive(bars + F_AK);
+                if (!mbar_wait_abortable(bars + F_LK0 + b, pb, a.hdr, 111, abort)) break;
+                if (c >= 1) {
+                    // E_K and r are free once the previous update and column sums have read them
+                    if (!mbar_wait_abortable(bars + F_S, (c - 1) & 1, a.hdr, 112, abort)) break;
+                    if (!mbar_wait_abortable(bars + F_ZP, (c - 1) & 1, a.hdr, 113, abort)) break;
+                }
+                tc_fence_after();
+                const float sum = key_exp(lane + (b ? R_LQ : R_LK), a.K, kc, smem + L.gk, k);
+                const float r = tok0 + c * C + k < tok_end ? 1.0f / sum : 0.f;
+                rbuf[k] = r;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bars + F_GK);
+                if (!mbar_wait_abortable(bars + F_V0 + b, pb, a.hdr, 114, abort)) break;
+                scale_v_row(b ? vb1 : vb0, k, d_v, r);
+                fence_proxy_async_smem();
+                mbar_arrive(bars + F_VS);
+            }
+        } else if (warp >= 8) {
+            // state side: Z_own, then the publication of S_own and the look-back
+            const int k = t - 256;
+            const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
+            float zown = 0.f;
+            bool ok = true;
+            for (int c = 0; c < nch; ++c) {
+                if (!(ok = mbar_wait_abortable(bars + F_GK, c & 1, a.hdr, 120, abort))) break;
+                float *zp = zpart + (c & 1) * 8 * KMAX;
+                colsum_part(smem + L.gk, rbuf, zp, k);
+                mbar_arrive(bars + F_ZP);
+                if (!(ok = mbar_wait_abortable(bars + F_ZP, c & 1, a.hdr, 121, abort))) break;
+                float zs = 0.f;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) zs += zp[g * KMAX + k];
+                zown += zs;
+            }
+            if (ok) ok = nch > 0 && mbar_wait_abortable(bars + F_S, (nch - 1) & 1, a.hdr, 122, abort);
+            if (!ok) *abort = 1;
+            named_bar_sync(1, 128);   // (every state thread's abort is visible to thread 0)
+            // one decision for the 128 threads (each broadcast: write, sync, read, sync)
+            auto bcast = [&](int v) -> int {
+                if (k == 0) *lbcast = v;
+                named_bar_sync(1, 128);
+                const int r = *lbcast;
+                named_bar_sync(1, 128);
+                return r;
+            };
+            ok = bcast(*abort ? 0 : 1) != 0;
+            int *flags = lb.flag + (size_t)bh * a.nseg;
+            const size_t row = ((size_t)bh * a.nseg + seg) * KMAX + k;
+            if (ok) {
+                tc_fence_after();
+                if (seg > 0) {
+                    row_to_global(lane + R_S, d_v, zown, lb.own + row * a.ne);
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (k == 0) flag_release(flags + seg, 1);
+                    // S_start into TMEM [256,384): the predecessors' memories, backwards until an
+                    // inclusive prefix (segment 0 always publishes one).  Thread 0 walks the flags
+                    // and lists the segments (in zbuf, free until sweep 2); then every thread adds
+                    // its rows of all of them.
+                    int *list = reinterpret_cast<int *>(zbuf);
+                    int j = seg - 1;
+                    for (bool first = true; ok; first = false) {
+                        int n = 0;
+                        if (k == 0) {
+                            for (int jj = j; jj >= 0 && n < 64; --jj) {
+                                const int f = wait_flag(flags + jj, a.hdr, abort);
+                                if (f != 1 && f != 2) {
+                                    n = -1;
+                                    break;
+                                }
+                                list[n++] = 2 * jj + (f == 2 ? 1 : 0);
+                                if (f == 2) break;
+                            }
+                        }
+                        n = bcast(n);
+                        if (n <= 0) {
+                            ok = false;
+                            break;
+                        }
+                        const float z = rows_add_list(lane + R_O, d_v, list, n, lb, (size_t)bh * a.nseg, k, a.ne, first);
+                        zexcl = first ? z : zexcl + z;
+                        const int last = list[n - 1];
+                        if (last & 1) break;   // an inclusive prefix: S_start is complete
+                        named_bar_sync(1, 128);   // (every thread has read the list)
+                        j = (last >> 1) - 1;
+                        if (j < 0) ok = false;   // (cannot happen: segment 0 publishes its prefix)
+                    }
+                } else {
+                    row_zero(lane + R_O, d_v);
+                    zexcl = 0.f;
+                }
+                if (ok) {
+                    rows_sum_to_global(lane + R_O, lane + R_S, d_v, zexcl + zown, lb.incl + row * a.ne);
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (k == 0) flag_release(flags + seg, 2);
+                }
+            }
+            if (!ok) {
+                *abort = 1;
+                if (k == 0) flag_release(flags + seg, 3);   // the successors stop waiting for it
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    if (!FUSED || !*abort) {
     if (warp == 12) {
         // ============================================================ control warp
         if (t == 384) {
@@ -339,8 +684,10 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             int last_v = -1, last_xk = -1, last_xq = -1;
             int last_pv = -1;
             bool ok = true;
-            mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + B_BIMG);
+            if (!FUSED) {   // (FUSED: loaded for sweep 1)
+                mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
+                bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + B_BIMG);
+            }
             if (nch > 0) {
                 load_x_tile(smem + L.abk + XT, &kmap, bars + B_XK, DR, tok0, bh);
                 load_x_tile(smem + L.abq + XT, &qmap, bars + B_XQ, DR, tok0, bh);
@@ -487,18 +834,24 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
         // ============================================================ state and output side
         const int k = t - 256;   // TMEM lane: component row of S, and token row of the output
         const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
-        // starting memory: V~ part to TMEM and as the bf16 operand, Z part to the running sum
+        // starting memory (from the scan, or FUSED from the look-back in TMEM [256,384)): V~ part
+        // to TMEM and as the bf16 operand, Z part to the running sum
         const float *src = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + k) * a.ne;
         for (int b = 0; b < d_v / 16; ++b) {
             uint32_t r[16];
-            const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
+            if (FUSED) {
+                tmem_ld16(lane + R_O + 16 * b, r);
+                tmem_ld_wait();
+            } else {
+                const float4 *s4 = reinterpret_cast<const float4 *>(src + b * 16);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 f = s4[q];
-                r[4 * q] = __float_as_uint(f.x);
-                r[4 * q + 1] = __float_as_uint(f.y);
-                r[4 * q + 2] = __float_as_uint(f.z);
-                r[4 * q + 3] = __float_as_uint(f.w);
+                for (int q = 0; q < 4; ++q) {
+                    const float4 f = s4[q];
+                    r[4 * q] = __float_as_uint(f.x);
+                    r[4 * q + 1] = __float_as_uint(f.y);
+                    r[4 * q + 2] = __float_as_uint(f.z);
+                    r[4 * q + 3] = __float_as_uint(f.w);
+                }
             }
             tmem_st16(lane + R_S + 16 * b, r);
             const uint4 lo = make_uint4(pk2(r[0], r[1], 1.f), pk2(r[2], r[3], 1.f), pk2(r[4], r[5], 1.f), pk2(r[6], r[7], 1.f));
@@ -506,7 +859,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
             *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 0, KMAX)) = lo;
             *reinterpret_cast<uint4 *>(smem + L.sp + sw32(k, b, 1, KMAX)) = hi;
         }
-        float zrun = src[d_v];
+        float zrun = FUSED ? zexcl : src[d_v];
         zbuf[k] = zrun;
         tmem_st_wait();
         fence_proxy_async_smem();
@@ -554,6 +907,7 @@ __global__ void __launch_bounds__(CTHREADS, 1) tc_causal_pipelined_kernel(const 
         }
         if (ok && nch > 0) output(nch - 1);
     }
+    }   // (sweep 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -573,11 +927,29 @@ gma_status_t launch_causal_pipelined(const Args &a, const CUtensorMap &vmap, con
 {
     const uint32_t sm = causal_pipelined_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
-    if (!set_smem(tc_causal_pipelined_kernel<DR>, sm)) return GMA_ERR_CUDA;
+    if (!set_smem(tc_causal_pipelined_kernel<DR, false>, sm)) return GMA_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_CAUSAL_OUT, st,
-               (e = launch_pdl(tc_causal_pipelined_kernel<DR>, dim3(nblocks), dim3(CTHREADS), sm, st, a, vmap, kmap,
-                               qmap)));
+               (e = launch_pdl(tc_causal_pipelined_kernel<DR, false>, dim3(nblocks), dim3(CTHREADS), sm, st, a, vmap,
+                               kmap, qmap, LookBack{})));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
+// The single-launch causal kernel: one CTA per segment, nblocks = BH * nseg; ticket and flags
+// (1 + BH * nseg ints) must be zero when it starts; a.agg takes the segments' own memories and
+// incl their inclusive prefixes (BH * nseg * KMAX * ne floats each).
+template <int DR>
+gma_status_t launch_causal_fused(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap,
+                                 const CUtensorMap &qmap, int *ticket_flags, float *incl, int nblocks, cudaStream_t st)
+{
+    const uint32_t sm = causal_pipelined_smem(DR, a.kn16, a.d_v);
+    if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
+    if (!set_smem(tc_causal_pipelined_kernel<DR, true>, sm)) return GMA_ERR_CUDA;
+    const LookBack lb{ticket_flags, ticket_flags + 1, a.agg, incl};
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_TC_CAUSAL_FUSED, st,
+               (e = launch_pdl(tc_causal_pipelined_kernel<DR, true>, dim3(nblocks), dim3(CTHREADS), sm, st, a, vmap,
+                               kmap, qmap, lb)));
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
@@ -587,6 +959,12 @@ template gma_status_t launch_causal_pipelined<32>(const Args &, const CUtensorMa
                                                   const CUtensorMap &, int, cudaStream_t);
 template gma_status_t launch_causal_pipelined<64>(const Args &, const CUtensorMap &, const CUtensorMap &,
                                                   const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_causal_fused<16>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, int *, float *, int, cudaStream_t);
+template gma_status_t launch_causal_fused<32>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, int *, float *, int, cudaStream_t);
+template gma_status_t launch_causal_fused<64>(const Args &, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, int *, float *, int, cudaStream_t);
 
 }  // namespace tck
 }  // namespace gma

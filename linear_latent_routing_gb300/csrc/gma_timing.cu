@@ -44,6 +44,7 @@ const char *kernel_name(int id)
     case KID_TC_CAUSAL_OUT: return "tc_causal_chunked";
     case KID_TC_LSE: return "tc_row_lse";
     case KID_TC_DIVIDE: return "tc_tile_divide";
+    case KID_TC_CAUSAL_FUSED: return "tc_causal_single_launch";
     case KID_DECODE: return "decode_step";
     case KID_DECODE_PARAMS: return "decode_params";
     case KID_USAGE_ROWS: return "usage_rows";

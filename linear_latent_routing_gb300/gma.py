@@ -21,6 +21,7 @@ GMA_F32, GMA_BF16 = 0, 1
 GMA_FLAG_SIMT = 0x1
 GMA_FLAG_OUT_F32 = 0x2
 GMA_FLAG_RECOMPUTE_KEYS = 0x4
+GMA_FLAG_SINGLE_PASS = 0x8
 GMA_FLAG_TEST_WITHHOLD = 0x80000000   # tests of the timeout path only (see include/gma.h)
 (GMA_VARIANT_RESPONSIBILITIES, GMA_VARIANT_BIDIRECTIONAL, GMA_VARIANT_CAUSAL, GMA_VARIANT_DECODE,
  GMA_VARIANT_USAGE, GMA_VARIANT_BACKWARD) = 0, 1, 2, 3, 4, 5

@@ -57,3 +57,24 @@ def oracle_forward(w, host, b=None, h=None, n=None):
 def case(w):
     host = make_inputs(w)
     return host
+
+
+def compare_every_token(w, O, host, heads_per_call=4):
+    """Every token of every slice of O against the oracle, a few heads per oracle call (the
+    oracle runs one slice per host thread)."""
+    worst = 0.0
+    a = to_numpy(host)
+    for h0 in range(0, w.H, heads_per_call):
+        h1 = min(w.H, h0 + heads_per_call)
+        ref = oracle_heads(w, a, h0, h1)
+        got = O[:, h0:h1].float().cpu().numpy()
+        assert np.isfinite(got).all()
+        worst = max(worst, normwise_error(got, ref))
+    return worst
+
+
+def oracle_heads(w, a, h0, h1, b0=0, b1=None):
+    """Oracle output of heads [h0, h1) and batch rows [b0, b1); `a` holds the inputs as numpy."""
+    b1 = w.B if b1 is None else b1
+    return oracle.forward(w.causal, a["QX"][b0:b1, h0:h1], a["KX"][b0:b1, h0:h1], a["V"][b0:b1, h0:h1],
+                          a["mu"][h0:h1], a["raw"][h0:h1], a["logits"][h0:h1], w.var_floor, w.eps)

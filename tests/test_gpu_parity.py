@@ -6,7 +6,8 @@ import pytest
 import torch
 
 from linear_latent_routing_gb300 import inputs as W
-from parity import (TOL, gpu_forward, normwise_error, oracle_forward, rowwise_error, to_device)
+from parity import (TOL, compare_every_token, gpu_forward, normwise_error, oracle_forward, oracle_heads,
+                    rowwise_error, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -165,28 +166,6 @@ def test_responsibilities_match_oracle(w, tol):
 
 # ------------------------------------------------------------- the benchmark workloads, full size
 
-def _compare_every_token(w, O, host, heads_per_call=4):
-    """Every token of every slice of O against the oracle, a few heads per oracle call (the
-    oracle runs one slice per host thread)."""
-    worst = 0.0
-    a = W.to_numpy(host)
-    for h0 in range(0, w.H, heads_per_call):
-        h1 = min(w.H, h0 + heads_per_call)
-        ref = _oracle_heads(w, a, h0, h1)
-        got = O[:, h0:h1].float().cpu().numpy()
-        assert np.isfinite(got).all()
-        worst = max(worst, normwise_error(got, ref))
-    return worst
-
-
-def _oracle_heads(w, a, h0, h1, b0=0, b1=None):
-    """Oracle output of heads [h0, h1) and batch rows [b0, b1); `a` holds the inputs as numpy."""
-    import oracle
-    b1 = w.B if b1 is None else b1
-    return oracle.forward(w.causal, a["QX"][b0:b1, h0:h1], a["KX"][b0:b1, h0:h1], a["V"][b0:b1, h0:h1],
-                          a["mu"][h0:h1], a["raw"][h0:h1], a["logits"][h0:h1], w.var_floor, w.eps)
-
-
 FULL = [W.LM_CAUSAL, W.LRA_BIDIR, W.LONG_CAUSAL]
 
 
@@ -200,7 +179,7 @@ def test_full_size_every_token(w):
     O = gpu_forward(w, dev)
     torch.cuda.synchronize()
     del dev
-    err = _compare_every_token(w, O, host)
+    err = compare_every_token(w, O, host)
     print(f"{w.name}: normwise {err:.3e} over every token of every slice")
     assert err <= TOL[w.dtype], err
 
@@ -220,12 +199,12 @@ def test_sweep_points_whole_slices(w, picks):
     torch.cuda.synchronize()
     assert torch.isfinite(O).all()
     if picks is None:
-        err = _compare_every_token(w, O, host)
+        err = compare_every_token(w, O, host)
     else:
         err = 0.0
         a = W.to_numpy(host)
         for b, h in picks:
-            ref = _oracle_heads(w, a, h, h + 1, b, b + 1)
+            ref = oracle_heads(w, a, h, h + 1, b, b + 1)
             err = max(err, normwise_error(O[b:b + 1, h:h + 1].float().cpu().numpy(), ref))
     print(f"{w.name}: normwise {err:.3e} over {'every slice' if picks is None else picks}")
     assert err <= TOL[w.dtype], err

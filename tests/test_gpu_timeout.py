@@ -29,17 +29,22 @@ def gma():
     return g
 
 
-@pytest.mark.parametrize("w", [W.scaled(W.LONG_CAUSAL, B=1, H=2, N=1500),
-                               W.scaled(W.LRA_BIDIR, B=2, H=1, N=900)],
-                         ids=["causal", "bidirectional"])
-def test_withheld_handoff_times_out_and_next_call_is_clean(gma, w):
+@pytest.mark.parametrize("w,single", [(W.scaled(W.LONG_CAUSAL, B=1, H=2, N=1500), False),
+                                      (W.scaled(W.LRA_BIDIR, B=2, H=1, N=900), False),
+                                      (W.scaled(W.LONG_CAUSAL, B=2, H=2, N=1500), True)],
+                         ids=["causal", "bidirectional", "causal_single_pass"])
+def test_withheld_handoff_times_out_and_next_call_is_clean(gma, w, single):
+    """With the single-launch causal kernel only the first segment of each slice withholds the
+    hand-off; every other segment (twelve per slice here) must learn of it through the look-back
+    and stop instead of waiting for a prefix that never comes."""
     host = W.make_inputs(w)
     dev = to_device(host)
     variant = gma.GMA_VARIANT_CAUSAL if w.causal else gma.GMA_VARIANT_BIDIRECTIONAL
     fn = gma.gma_forward_causal if w.causal else gma.gma_forward_bidirectional
+    base = gma.GMA_FLAG_SINGLE_PASS if single else 0
     test = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor,
-                          flags=gma.GMA_FLAG_TEST_WITHHOLD)
-    normal = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor)
+                          flags=base | gma.GMA_FLAG_TEST_WITHHOLD)
+    normal = gma.make_shape(w.B, w.H, w.N, w.d_r, w.K, w.d_v, gma.GMA_BF16, w.eps, w.var_floor, flags=base)
     assert gma.gma_kernel_family(test, variant) == 1
     ws_n = gma.gma_workspace_size(normal, variant)
     assert gma.gma_workspace_size(test, variant) == ws_n
