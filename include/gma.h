@@ -114,7 +114,9 @@ typedef struct {
  * The workspace must be 256-byte aligned.  Its first 256 bytes hold the error word that
  * gma_check_workspace reads.  For the causal variant on the tensor-core path (bf16, no
  * GMA_FLAG_SIMT) it includes the key responsibilities of every token, B*H*N*Kp bf16 values
- * (Kp = 64 for K <= 64, else 128), unless GMA_FLAG_RECOMPUTE_KEYS is set.  With K > 128 on the
+ * (Kp = 64 for K <= 64, else 128), unless GMA_FLAG_RECOMPUTE_KEYS or GMA_FLAG_SINGLE_PASS is
+ * set; with GMA_FLAG_SINGLE_PASS it holds instead a segment counter, one flag per segment and the
+ * segments' inclusive prefix memories (the call zeroes the counter and flags).  With K > 128 on the
  * tensor-core path (components in tiles of 128) it also holds every routing row's log-sum-exp
  * over all components (fp32) and, for the forward passes, fp32 partial sums of the queries'
  * numerators and normalisers (B*H*N*(d_v + 1) floats). */
@@ -137,7 +139,10 @@ gma_status_t gma_forward_bidirectional(const gma_shape_t *shape, const void *QX,
                                        size_t workspace_bytes, gma_stream_t stream);
 
 /* Causal GMA (Méthodologie §3): as above with V~ and Z replaced by inclusive prefix sums,
- *   O_i = gamma_Q,i (sum_{j<=i} gamma_K,j^T v_j) / (gamma_Q,i . sum_{j<=i} gamma_K,j + eps). */
+ *   O_i = gamma_Q,i (sum_{j<=i} gamma_K,j^T v_j) / (gamma_Q,i . sum_{j<=i} gamma_K,j + eps).
+ * Repeated calls on the same inputs give the same bits, except with GMA_FLAG_SINGLE_PASS: its
+ * segments add their predecessors' memories in the order they find them published, so the
+ * rounding can differ from call to call. */
 gma_status_t gma_forward_causal(const gma_shape_t *shape, const void *QX, const void *KX,
                                 const void *V, const float *mu, const float *raw_var,
                                 const float *prior_logits, void *O, void *workspace,
