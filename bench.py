@@ -380,6 +380,9 @@ def run_gma(args, ws, rank, local):
     dom = max(per_kernel, key=lambda k: sum(per_kernel[k]))
     avg_ms = sum(per_kernel[dom]) / len(per_kernel[dom])
     bound, amount, unit = kernel_work(w, dom)
+    if recompute and dom == "tc_causal_chunked":
+        # (the recompute kernel is timed under the output pass's name; it also reads K_X)
+        amount += w.token_heads * (2 if w.dtype == "bf16" else 4) * w.d_r
     pk = peaks()
     if bound == "hbm":
         achieved = amount / (avg_ms / 1e3) / 1e9
@@ -406,7 +409,8 @@ def run_gma(args, ws, rank, local):
                      "frac": round(roof_s / step_s, 4),
                      "alg_bytes": step_bytes, "alg_flops": step_flops}
 
-    traffic = traffic_per_launch(dom, w)
+    # (traffic records are keyed by kernel name, and the recompute kernel shares the output pass's)
+    traffic = None if recompute else traffic_per_launch(dom, w)
     roofline["traffic"] = traffic
 
     # end to end through the C ABI with pinned host buffers.  Every step copies its own inputs from
