@@ -476,10 +476,20 @@ struct Plan {
 
 constexpr int kSms = 152;   // GB300
 
+uint32_t keysmall_smem(int d_r, int K, int d_v);   // gma_tc_keysmall.cu
+
+// The bidirectional key pass runs two CTAs per SM (gma_tc_keysmall.cu) where the shape allows.
+bool key_pass_small(const gma_shape_t &s, int variant)
+{
+    return variant == GMA_VARIANT_BIDIRECTIONAL && s.K <= 64 && keysmall_smem(s.d_r, s.K, s.d_v) != 0;
+}
+
 // `s` describes the keys; n_q is the number of queries per slice (cross-attention), s.N if < 0.
-Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1, int n_q = -1)
+// per_sm: CTAs per SM the split is planned for (0: that of the variant's key pass).
+Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 0, int n_q = -1)
 {
     if (n_q < 0) n_q = s.N;
+    if (per_sm <= 0) per_sm = key_pass_small(s, variant) ? 2 : 1;
     Plan p{};
     p.ntile = s.K > KMAX ? (s.K + KMAX - 1) / KMAX : 1;
     p.kn16 = p.ntile > 1 ? KMAX : (s.K + 15) / 16 * 16;
@@ -504,6 +514,10 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1, int n_q = -1)
         // (The single-launch causal kernel takes the same split.  Its second sweep re-reads each
         // segment's key rows and values; segments short enough for those of all CTAs in flight to
         // stay in L2 were measured slower: the look-back and the per-segment set-up cost more.)
+        // (bidirectional shapes whose key pass runs two CTAs per SM: a set-up of 2 chunks, which
+        // gives one segment per slice at the classification-shaped workload; measured 184 -> 160 µs
+        // per step against the 0.6 of the other passes, the read pass included)
+        const double setup = key_pass_small(s, variant) ? 2.0 : 0.6;
         double best = 1e30;
         int best_n = 1;
         const int top = nchunks < 2048 ? nchunks : 2048;
@@ -512,7 +526,7 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 1, int n_q = -1)
             const int segs = (nchunks + cps - 1) / cps;
             const long long ctas = (long long)BH * segs;
             const long long waves = (ctas + (long long)per_sm * kSms - 1) / ((long long)per_sm * kSms);
-            const double cost = (double)waves * (0.6 + cps);
+            const double cost = (double)waves * (setup + cps);
             if (cost <= best) {
                 best = cost;
                 best_n = segs;
@@ -637,6 +651,10 @@ gma_status_t launch_params(const gma_shape_t &s, const Plan &p, char *ws, const 
     return GMA_OK;
 }
 
+template <int DR>   // gma_tc_keysmall.cu
+gma_status_t launch_keysmall(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap, int nblocks,
+                             cudaStream_t st);
+
 template <int DR>   // gma_tc_causal.cu
 gma_status_t launch_causal_fused(const Args &a, const CUtensorMap &vmap, const CUtensorMap &kmap,
                                  const CUtensorMap &qmap, int *ticket_flags, float *incl, int nblocks, cudaStream_t st);
@@ -667,7 +685,9 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
                                        BH * p.nseg, st);
     }
     {
-        const gma_status_t r = launch_segmem_pipelined<DR>(a, vmap, kmap, gmap, BH * p.nseg, st);
+        const gma_status_t r = !causal && key_pass_small(s, GMA_VARIANT_BIDIRECTIONAL)
+                                   ? launch_keysmall<DR>(a, vmap, kmap, BH * p.nseg, st)
+                                   : launch_segmem_pipelined<DR>(a, vmap, kmap, gmap, BH * p.nseg, st);
         if (r != GMA_OK) return r;
     }
     const int KD = KMAX * p.ne, KDu = p.kn16 * p.ne;
@@ -957,7 +977,7 @@ size_t tc_workspace_size_cross(const gma_shape_t &s, int n_k)
 {
     gma_shape_t sk = s;
     sk.N = n_k;
-    return tck::make_plan(sk, GMA_VARIANT_BIDIRECTIONAL, 1, s.N).total;
+    return tck::make_plan(sk, GMA_VARIANT_BIDIRECTIONAL, 0, s.N).total;
 }
 
 namespace tck {
@@ -971,7 +991,7 @@ gma_status_t tc_forward(const gma_shape_t &s, bool causal, int n_k, const void *
     gma_shape_t sk = s;   // the key side
     sk.N = n_k;
     const int variant = causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL;
-    const tck::Plan p = tck::make_plan(sk, variant, 1, s.N);
+    const tck::Plan p = tck::make_plan(sk, variant, 0, s.N);
     // the bidirectional read pass runs two CTAs per SM on shapes small enough for that; its split
     // is planned for it (it only sets the query segments: the workspace follows the key plan)
     const tck::Plan pq = causal ? p

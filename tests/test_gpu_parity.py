@@ -53,6 +53,11 @@ SMALL = [
     W.scaled(W.K_SWEEP[2], B=1, H=1, N=400),
     W.scaled(W.K_SWEEP[3], B=1, H=1, N=300),
     W.scaled(W.K_SWEEP[3], B=1, H=1, N=300, causal=False),
+    # bidirectional key pass with two CTAs per SM (K <= 64, small d_r and d_v): 16, 48 and 64
+    # components, the widest padding of the value operand (d_v = 16), several segments per slice
+    W.scaled(W.LRA_BIDIR, B=1, H=2, N=900, d_r=16, K=48, d_v=16),
+    W.scaled(W.LRA_BIDIR, B=2, H=3, N=1300, d_r=32, K=64, d_v=32),
+    W.scaled(W.LRA_BIDIR, B=1, H=1, N=2000, d_r=16, K=17, d_v=64),
 ]
 
 
@@ -90,6 +95,23 @@ def test_component_tiles_match_oracle(w):
     O, ref = _run(w)
     assert np.isfinite(O).all()
     assert normwise_error(O, ref) <= TOL["bf16"], (normwise_error(O, ref), rowwise_error(O, ref))
+
+
+def test_small_bidirectional_key_pass_is_the_one_launched():
+    """The classification-shaped workload's key pass runs the two-CTAs-per-SM kernel."""
+    gma = _gma()
+    w = W.scaled(W.LRA_BIDIR, B=2, H=2, N=1000)
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    gpu_forward(w, dev)
+    torch.cuda.synchronize()
+    gma.gma_timing_enable(64)
+    O = gpu_forward(w, dev)
+    torch.cuda.synchronize()
+    names = [n for n, _ in gma.gma_timing_read(64)]
+    gma.gma_timing_enable(0)
+    assert "tc_bidir_write" in names and "tc_causal_segment_memory" not in names, names
+    assert normwise_error(O.float().cpu().numpy(), oracle_forward(w, host)) <= TOL["bf16"]
 
 
 def test_fp32_elementwise_relative_error_reported():
