@@ -139,7 +139,8 @@ template <int DR, int MINB>
 __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Args a,
                                                                      const __grid_constant__ CUtensorMap qmap)
 {
-    grid_dependency_wait();   // the total memory comes from the kernels before
+    // (no wait here: the set-up and the first query rows, which no kernel writes, overlap the
+    // kernel before; the threads that read its results wait below)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const BidirSmem L(DR, a.kn16, a.d_v);
@@ -188,16 +189,20 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
     uint64_t *bl = bars + B_L0 + g, *bo = bars + B_O0 + g;
     int last_x = -1;   // leader: chunk of this group's TMA load still possibly in flight
     if (leader) {
-        if (t == 0) {
-            mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + B_BIMG);
-        }
         if (g < nch) {
             load_x_tile(ab + XT, &qmap, bx, DR, tok0 + g * C, bh);
             last_x = g;
         }
+        if (t == 0) {
+            grid_dependency_wait();   // the tables come from the kernels before
+            mbar_arrive_expect_tx(bars + B_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + B_BIMG);
+        }
     }
+    // (components in tiles: the rows' log2-sum-exp, and the partial sums of the tiles before)
+    if (a.lse_q && g == 1) grid_dependency_wait();
     if (g == 0) {
+        grid_dependency_wait();   // the slice's total memory comes from the kernels before
         // the slice's total memory: V~ rows as the bf16 operand, Z into shared memory
         const float *src = a.agg + ((size_t)bh * a.agg_nseg * KMAX + i) * a.ne;
         for (int b = 0; b < d_v / 16; ++b) {

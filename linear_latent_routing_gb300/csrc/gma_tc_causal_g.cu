@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                                                                       const __grid_constant__ CUtensorMap qmap,
                                                                       const __grid_constant__ CUtensorMap gmap)
 {
-    grid_dependency_wait();   // the scanned memories (and, before them, Gamma_K) come from the kernels before
+    // (no wait here: the set-up and the first loads of Q_X and V, which no kernel writes, overlap
+    // the kernel before; the threads that read its results wait below)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const GSmem L(DR, a.kn16, a.d_v);
@@ -424,15 +425,20 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
                 last_xq = cq;
                 return true;
             };
-            mbar_arrive_expect_tx(bars + G_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + G_BIMG);
             if (nch > 0) {
                 load_x_tile(smem + L.abq + XT, &qmap, bars + G_XQ, DR, tok0, bh);
-                load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, nb, tok0, bh);
-                last_xq = last_gt = 0;
+                last_xq = 0;
                 load_v(0);
             }
             if (nch > 1) load_v(1);
+            // Gamma_K and the tables come from the kernels before (the scan is the last of them)
+            grid_dependency_wait();
+            mbar_arrive_expect_tx(bars + G_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + G_BIMG);
+            if (nch > 0) {
+                load_g_tile(smem + L.gk, &gmap, bars + G_GT, a.kg, nb, tok0, bh);
+                last_gt = 0;
+            }
             if (nch > 1) ok = stage_queries(1);
             for (int c = 0; ok && c < nch; ++c) {
                 const uint32_t ph = c & 1;
@@ -473,6 +479,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
             fence_proxy_async_smem();
             mbar_arrive(bars + G_AQ);
         }
+        if (a.lse_q) grid_dependency_wait();   // (the rows' log2-sum-exp come from the kernels before)
         for (int c = 0; c < nch; ++c) {
             const uint32_t ph = c & 1;
             const bool valid = tok0 + c * C + i < tok_end;
@@ -539,6 +546,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) tc_causal_gamma_kernel(const Args
         const uint32_t lane = tmem + ((uint32_t)((warp - 8) * 32) << 16);
         // starting memory: S_start^T to TMEM and as bf16 rows of the operand tile (column n of the
         // segment's memory, read component by component: consecutive lanes, consecutive floats)
+        grid_dependency_wait();   // the segment's starting memory comes from the scan
         const float *seg_mem = a.agg + ((size_t)bh * a.nseg + seg) * KMAX * a.ne;
         const bool vrow = n < d_v;
 #pragma unroll 1

@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
                                                                          const __grid_constant__ CUtensorMap vmap,
                                                                          const __grid_constant__ CUtensorMap kmap)
 {
-    grid_dependency_wait();     // the parameter tables come from the kernel before
-    grid_dependency_launch();   // the sum over segments (or the read pass) may start; it waits for this grid
+    // (no wait here: the set-up and the first loads of K_X and V, which no kernel writes, overlap
+    // the kernel before; the loader waits before the tables, and every write follows that)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const SmallSmem L(DR, a.kn16, a.d_v);
@@ -149,6 +149,9 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
+    // the next kernel may start now: this CTA holds its tensor memory, so a CTA of the next kernel
+    // that allocates before it waits for this grid can never take the columns this one needs
+    grid_dependency_launch();
 
     if (warp == 8) {
         // ============================================================ control warp: MMAs
@@ -194,13 +197,14 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
                 load_v_chunk(smem + ve(c), &vmap, bars + K_V0 + (c & 1), d_v, tok0 + c * C, bh);
                 if (c & 1) { vpend1 = true; vlast1 = c; } else { vpend0 = true; vlast0 = c; }
             };
-            mbar_arrive_expect_tx(bars + K_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + K_BIMG);
             for (int c = 0; c < 2 && c < nch; ++c) load_v(c);
             if (nch > 0) {
                 load_x_tile(smem + L.xst, &kmap, bars + K_XK, DR, tok0, bh);
                 last_xk = 0;
             }
+            grid_dependency_wait();   // the parameter tables come from the kernel before
+            mbar_arrive_expect_tx(bars + K_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + K_BIMG);
             for (int c = 0; ok && c < nch; ++c) {
                 if (c + 1 < nch) {   // the staged rows of chunk c have been read into its A tile
                     if (!(ok = mbar_wait_abortable(bars + K_AK, c & 1, a.hdr, 145, abort))) break;

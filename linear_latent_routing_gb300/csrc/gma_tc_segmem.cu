@@ -59,8 +59,8 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
                                                                                   const __grid_constant__ CUtensorMap kmap,
                                                                                   const __grid_constant__ CUtensorMap gmap)
 {
-    grid_dependency_wait();     // the parameter tables come from the kernel before
-    grid_dependency_launch();   // the scan may start (it waits for this grid)
+    // (no wait here: the set-up and the first loads of K_X and V, which no kernel writes, overlap
+    // the kernel before; the threads that read its results wait below)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const SegSmem L(DR, a.kn16, a.d_v);
@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
+    // the next kernel may start now: this CTA holds its tensor memory, so a CTA of the next kernel
+    // that allocates before it waits for this grid can never take the columns this one needs
+    grid_dependency_launch();
 
     if (warp == 8) {
         // ============================================================ control warp: MMAs, stores
@@ -163,13 +166,16 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
                 load_v_chunk(smem + ve(c), &vmap, bars + S_V0 + (c & 1), d_v, tok0 + c * C, bh);
                 if (c & 1) { vpend1 = true; vlast1 = c; } else { vpend0 = true; vlast0 = c; }
             };
-            mbar_arrive_expect_tx(bars + S_BIMG, (uint32_t)a.bimg_bytes);
-            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + S_BIMG);
             for (int c = 0; c < 2 && c < nch; ++c) load_v(c);
             if (nch > 0) {
                 load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0, bh);
                 last_xk = 0;
             }
+            // the parameter tables come from the kernel before: every MMA, and so every write of
+            // this kernel (Gamma_K stores, segment memories), follows this wait
+            grid_dependency_wait();
+            mbar_arrive_expect_tx(bars + S_BIMG, (uint32_t)a.bimg_bytes);
+            bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + S_BIMG);
             for (int c = 0; ok && c < nch; ++c) {
                 if (c + 1 < nch) {   // the staged rows of chunk c have been read into its A tile
                     if (!(ok = mbar_wait_abortable(bars + S_AK, c & 1, a.hdr, 87, abort))) break;
@@ -196,6 +202,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
         const int k = t & 127;              // TMEM lane, token row, component row
         const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         uint8_t *gk = smem + (g ? L.gk1 : L.gk0);
+        if (a.lse_k) grid_dependency_wait();   // (the rows' log2-sum-exp come from the kernel before)
         for (int c = g; c < nch; c += 2) {
             const int n = c >> 1;
             const int base = tok0 + c * C;
