@@ -16,9 +16,27 @@
 // carried memory D or S for the rest, exactly as the forward read phase splits its work; the
 // parameter gradients are summed per row chunk and then in a fixed order, so results repeat.
 #include "gma_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gma {
 namespace {
+
+// Every kernel of this file starts by waiting for the grid before it (programmatic dependent
+// launch; nothing is read or written before) and lets the next one be scheduled, so that the
+// launch latencies of the backward pass's kernels overlap.
+__device__ __forceinline__ void chain_enter()
+{
+    tc::grid_dependency_wait();
+    tc::grid_dependency_launch();
+}
+
+template <typename... P, typename... A>
+gma_status_t launch_chained(int kid, cudaStream_t st, void (*k)(P...), dim3 g, dim3 b, size_t smem, A... args)
+{
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(kid, st, (e = launch_pdl(k, g, b, smem, st, args...)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
 
 constexpr int SEG = 64;        // tokens per segment (the forward preparation's split)
 constexpr int KT = 32;         // component tile
@@ -77,6 +95,7 @@ __global__ void __launch_bounds__(BT) bwd_numden_kernel(const float *__restrict_
                                                         const Tin *__restrict__ dO, float *__restrict__ dnd, int N,
                                                         int K, int d_v, int nseg, float eps, int causal)
 {
+    chain_enter();
     extern __shared__ float sm[];
     const int dv1 = d_v + 1;
     float(*P)[SEG + 1] = reinterpret_cast<float(*)[SEG + 1]>(sm);
@@ -125,6 +144,7 @@ __global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ g
                                                      float *__restrict__ dgq, int N, int K, int d_v, int nseg,
                                                      int causal)
 {
+    chain_enter();
     extern __shared__ float sm[];
     const int dv1 = d_v + 1;
     float(*A)[SEG + 1] = reinterpret_cast<float(*)[SEG + 1]>(sm);
@@ -164,6 +184,7 @@ __global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ g
 __global__ void __launch_bounds__(BT) bwd_seg_kernel(const float *__restrict__ gq, const float *__restrict__ dnd,
                                                      float *__restrict__ dagg, int N, int K, int d_v, int nseg)
 {
+    chain_enter();
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
     const int k0 = blockIdx.y * KT;
     const int j0 = seg * SEG, jn = min(SEG, N - j0);
@@ -193,6 +214,7 @@ __global__ void __launch_bounds__(BT) bwd_seg_kernel(const float *__restrict__ g
 // keys of the segment see from queries after it).  Bidirectional: the total into segment 0.
 __global__ void bwd_scan_kernel(float *__restrict__ dagg, long long total, int nseg, int KD, int causal)
 {
+    chain_enter();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const long long bh = idx / KD, e = idx % KD;
@@ -216,6 +238,7 @@ __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq
                                                     Tin *__restrict__ dV, int N, int K, int d_v, int nseg,
                                                     int causal)
 {
+    chain_enter();
     extern __shared__ float sm[];
     const int dv1 = d_v + 1;
     float(*P)[SEG + 1] = reinterpret_cast<float(*)[SEG + 1]>(sm);
@@ -272,6 +295,7 @@ __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq
 __global__ void __launch_bounds__(BT) bwd_softmax_kernel(const float *__restrict__ g, float *__restrict__ dg,
                                                          long long rows, int K)
 {
+    chain_enter();
     const long long r = (long long)blockIdx.x * (BT / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
@@ -290,6 +314,7 @@ __global__ void __launch_bounds__(BT) bwd_dx_kernel(const Tin *__restrict__ X, c
                                                     const float *__restrict__ mu, const float *__restrict__ iv,
                                                     Tin *__restrict__ dX, int H, int N, int K, long long rows)
 {
+    chain_enter();
     const long long r = (long long)blockIdx.x * BT + threadIdx.x;
     if (r >= rows) return;
     const int h = (int)((r / N) % H);
@@ -324,6 +349,7 @@ __global__ void __launch_bounds__(BT) bwd_param_partial_kernel(const Tin *__rest
                                                                float *__restrict__ ps, float *__restrict__ pl, int B,
                                                                int H, int N, int K, int d_r, int kchunks, int R)
 {
+    chain_enter();
     __shared__ float red[BT / 32][32][33];
     const int h = blockIdx.x, kc = blockIdx.y % kchunks, dc = blockIdx.y / kchunks, ch = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -397,6 +423,7 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
                                                              float *__restrict__ draw, float *__restrict__ dlogits,
                                                              int K, int d_r, int R)
 {
+    chain_enter();
     __shared__ float red[BT / 32][2];
     const int h = blockIdx.x;
     const int KD = K * d_r;
@@ -493,11 +520,12 @@ gma_status_t launch_dx(int d_r, const Tin *X, const float *dL, const float *mu, 
                        int K, long long rows, cudaStream_t st)
 {
     const unsigned blocks = (unsigned)((rows + BT - 1) / BT);
+    gma_status_t rr = GMA_OK;
     switch (d_r) {
-    case 16: GMA_LAUNCH(KID_BWD_DX, st, (bwd_dx_kernel<16, Tin><<<blocks, BT, 0, st>>>(X, dL, mu, iv, dX, H, N, K, rows))); break;
-    case 32: GMA_LAUNCH(KID_BWD_DX, st, (bwd_dx_kernel<32, Tin><<<blocks, BT, 0, st>>>(X, dL, mu, iv, dX, H, N, K, rows))); break;
-    case 64: GMA_LAUNCH(KID_BWD_DX, st, (bwd_dx_kernel<64, Tin><<<blocks, BT, 0, st>>>(X, dL, mu, iv, dX, H, N, K, rows))); break;
-    case 128: GMA_LAUNCH(KID_BWD_DX, st, (bwd_dx_kernel<128, Tin><<<blocks, BT, 0, st>>>(X, dL, mu, iv, dX, H, N, K, rows))); break;
+    case 16: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<16, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
+    case 32: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<32, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
+    case 64: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<64, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
+    case 128: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<128, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
     default: return GMA_ERR_UNSUPPORTED_SHAPE;
     }
     return GMA_OK;
@@ -516,6 +544,7 @@ gma_status_t backward_typed(const gma_shape_t &s, bool causal, const Tin *QX, co
     float *pmu = (float *)(ws + L.pmu), *ps = (float *)(ws + L.ps), *pl = (float *)(ws + L.pl);
     gma_status_t r = simt_prepare(s, causal, QX, KX, V, mu, raw, logits, iv, cst, gq, gk, agg, st);
     if (r != GMA_OK) return r;
+    gma_status_t rr = GMA_OK;
     const int BH = s.B * s.H, cz = causal ? 1 : 0;
     const unsigned nblk = (unsigned)(BH * L.nseg);
     const size_t smem = sizeof(float) * (size_t)seg_smem_floats(s.d_v);
@@ -523,24 +552,24 @@ gma_status_t backward_typed(const gma_shape_t &s, bool causal, const Tin *QX, co
         cudaFuncSetAttribute(bwd_dgq_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_dk_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GMA_ERR_CUDA;
-    GMA_LAUNCH(KID_BWD_NUMDEN, st, (bwd_numden_kernel<Tin><<<nblk, BT, smem, st>>>(gq, gk, V, agg, dO, dnd, s.N, s.K, s.d_v, L.nseg, s.eps, cz)));
-    GMA_LAUNCH(KID_BWD_DQ, st, (bwd_dgq_kernel<Tin><<<nblk, BT, smem, st>>>(gk, V, agg, dnd, dgq, s.N, s.K, s.d_v, L.nseg, cz)));
+    if ((rr = launch_chained(KID_BWD_NUMDEN, st, bwd_numden_kernel<Tin>, dim3(nblk), dim3(BT), smem, gq, gk, V, agg, dO, dnd, s.N, s.K, s.d_v, L.nseg, s.eps, cz)) != GMA_OK) return rr;
+    if ((rr = launch_chained(KID_BWD_DQ, st, bwd_dgq_kernel<Tin>, dim3(nblk), dim3(BT), smem, gk, V, agg, dnd, dgq, s.N, s.K, s.d_v, L.nseg, cz)) != GMA_OK) return rr;
     dim3 gs(nblk, (unsigned)((s.K + KT - 1) / KT));
-    GMA_LAUNCH(KID_BWD_SEG, st, (bwd_seg_kernel<<<gs, BT, 0, st>>>(gq, dnd, dagg, s.N, s.K, s.d_v, L.nseg)));
+    if ((rr = launch_chained(KID_BWD_SEG, st, bwd_seg_kernel, dim3(gs), dim3(BT), 0, gq, dnd, dagg, s.N, s.K, s.d_v, L.nseg)) != GMA_OK) return rr;
     const int KD = s.K * (s.d_v + 1);
     const long long tot = (long long)BH * KD;
-    GMA_LAUNCH(KID_BWD_SCAN, st, (bwd_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(dagg, tot, L.nseg, KD, cz)));
-    GMA_LAUNCH(KID_BWD_DK, st, (bwd_dk_kernel<Tin><<<nblk, BT, smem, st>>>(gq, gk, V, dagg, dnd, dgk, dV, s.N, s.K, s.d_v, L.nseg, cz)));
+    if ((rr = launch_chained(KID_BWD_SCAN, st, bwd_scan_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, dagg, tot, L.nseg, KD, cz)) != GMA_OK) return rr;
+    if ((rr = launch_chained(KID_BWD_DK, st, bwd_dk_kernel<Tin>, dim3(nblk), dim3(BT), smem, gq, gk, V, dagg, dnd, dgk, dV, s.N, s.K, s.d_v, L.nseg, cz)) != GMA_OK) return rr;
     const long long T = (long long)BH * s.N;
-    GMA_LAUNCH(KID_BWD_SOFTMAX, st, (bwd_softmax_kernel<<<(unsigned)((T + 7) / 8), BT, 0, st>>>(gq, dgq, T, s.K)));
-    GMA_LAUNCH(KID_BWD_SOFTMAX, st, (bwd_softmax_kernel<<<(unsigned)((T + 7) / 8), BT, 0, st>>>(gk, dgk, T, s.K)));
+    if ((rr = launch_chained(KID_BWD_SOFTMAX, st, bwd_softmax_kernel, dim3((unsigned)((T + 7) / 8)), dim3(BT), 0, gq, dgq, T, s.K)) != GMA_OK) return rr;
+    if ((rr = launch_chained(KID_BWD_SOFTMAX, st, bwd_softmax_kernel, dim3((unsigned)((T + 7) / 8)), dim3(BT), 0, gk, dgk, T, s.K)) != GMA_OK) return rr;
     r = launch_dx<Tin>(s.d_r, QX, dgq, mu, iv, dQX, s.H, s.N, s.K, T, st);
     if (r != GMA_OK) return r;
     r = launch_dx<Tin>(s.d_r, KX, dgk, mu, iv, dKX, s.H, s.N, s.K, T, st);
     if (r != GMA_OK) return r;
     dim3 gp((unsigned)s.H, (unsigned)(L.kchunks * L.dchunks), (unsigned)L.R);
-    GMA_LAUNCH(KID_BWD_PARAMS, st, (bwd_param_partial_kernel<Tin><<<gp, BT, 0, st>>>(QX, KX, dgq, dgk, mu, iv, pmu, ps, pl, s.B, s.H, s.N, s.K, s.d_r, L.kchunks, L.R)));
-    GMA_LAUNCH(KID_BWD_PFINAL, st, (bwd_param_final_kernel<<<(unsigned)s.H, BT, 0, st>>>(pmu, ps, pl, raw, logits, dmu, draw, dlogits, s.K, s.d_r, L.R)));
+    if ((rr = launch_chained(KID_BWD_PARAMS, st, bwd_param_partial_kernel<Tin>, dim3(gp), dim3(BT), 0, QX, KX, dgq, dgk, mu, iv, pmu, ps, pl, s.B, s.H, s.N, s.K, s.d_r, L.kchunks, L.R)) != GMA_OK) return rr;
+    if ((rr = launch_chained(KID_BWD_PFINAL, st, bwd_param_final_kernel, dim3((unsigned)s.H), dim3(BT), 0, pmu, ps, pl, raw, logits, dmu, draw, dlogits, s.K, s.d_r, L.R)) != GMA_OK) return rr;
     return GMA_OK;
 }
 

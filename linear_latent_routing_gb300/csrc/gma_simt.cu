@@ -14,9 +14,22 @@
 // exclusive-prefix-scanned (causal); each query segment then reads its memory and, for the
 // causal variant, adds the masked in-segment affinity (Gamma_Q Gamma_K^T restricted to j <= i).
 #include "gma_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gma {
 namespace {
+
+using tc::grid_dependency_launch;
+using tc::grid_dependency_wait;
+
+// Every kernel of this family starts by waiting for the grid before it (programmatic dependent
+// launch; nothing is read or written before) and lets the next one be scheduled, so that the
+// launch latencies of a call's kernels overlap.
+__device__ __forceinline__ void chain_enter()
+{
+    grid_dependency_wait();
+    grid_dependency_launch();
+}
 
 constexpr int SEG = 64;        // tokens per segment
 constexpr int KT = 32;         // component tile for the staged dot products
@@ -32,6 +45,7 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
                                    float *__restrict__ inv_var, float *__restrict__ cst, int K,
                                    int d_r, float floor_)
 {
+    chain_enter();
     const int h = blockIdx.x, lane = threadIdx.x & 31;
     const int k = blockIdx.y * (PARAM_THREADS / 32) + (threadIdx.x >> 5);
     const float *lh = logits + (size_t)h * K;
@@ -127,6 +141,7 @@ __global__ void simt_resp_kernel(const Tin *__restrict__ X, const float *__restr
                                  const float *__restrict__ inv_var, const float *__restrict__ cst,
                                  Tout *__restrict__ gamma, int H, int N, int K, long long rows)
 {
+    chain_enter();
     constexpr bool PRECISE = sizeof(Tin) == 4;
     const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows) return;
@@ -165,6 +180,7 @@ template <typename Tin>
 __global__ void simt_state_kernel(const float *__restrict__ gk, const Tin *__restrict__ V,
                                   float *__restrict__ agg, int N, int K, int d_v, int nseg)
 {
+    chain_enter();
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
     const int k0 = blockIdx.y * KT;
     const int j0 = seg * SEG, jn = min(SEG, N - j0);
@@ -199,6 +215,7 @@ __global__ void simt_state_kernel(const float *__restrict__ gk, const Tin *__res
 __global__ void simt_scan_kernel(float *__restrict__ agg, long long total, int nseg, int KD,
                                  int causal)
 {
+    chain_enter();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const long long bh = idx / KD, e = idx % KD;
@@ -222,6 +239,7 @@ __global__ void simt_out_kernel(const float *__restrict__ gq, const float *__res
                                 Tout *__restrict__ O, int N, int K, int d_v, int nseg, int agg_nseg,
                                 float eps, int causal)
 {
+    chain_enter();
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
     const int i0 = seg * SEG, in = min(SEG, N - i0);
     const int DV1 = d_v + 1;
@@ -311,19 +329,27 @@ SimtLayout simt_layout(const gma_shape_t &s, int variant, int n_k)
 
 SimtLayout simt_layout(const gma_shape_t &s, int variant) { return simt_layout(s, variant, s.N); }
 
+// A launch of this family's kernels: programmatic dependent launch (see chain_enter).
+template <typename... P, typename... A>
+gma_status_t launch_chained(int kid, cudaStream_t st, void (*k)(P...), dim3 g, dim3 b, A... args)
+{
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(kid, st, (e = launch_pdl(k, g, b, 0, st, args...)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
 template <typename Tin, typename Tout>
 gma_status_t launch_resp(int d_r, const Tin *X, const float *mu, const float *iv, const float *cst,
                          Tout *g, int H, int N, int K, long long rows, cudaStream_t st)
 {
     const unsigned blocks = (unsigned)((rows + 127) / 128);
     switch (d_r) {
-    case 16: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<16, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
-    case 32: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<32, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
-    case 64: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<64, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
-    case 128: GMA_LAUNCH(KID_SIMT_RESP, st, (simt_resp_kernel<128, Tin, Tout><<<blocks, 128, 0, st>>>(X, mu, iv, cst, g, H, N, K, rows))); break;
+    case 16: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<16, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
+    case 32: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<32, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
+    case 64: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<64, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
+    case 128: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<128, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
     default: return GMA_ERR_UNSUPPORTED_SHAPE;
     }
-    return GMA_OK;
 }
 
 // Everything the read phase needs: the parameters, Gamma_Q and Gamma_K (fp32), and the segment
@@ -335,18 +361,21 @@ gma_status_t prepare_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
                            float *cst, float *gq, float *gk, float *agg, int nseg, cudaStream_t st)
 {
     const long long rows = (long long)s.B * s.H * s.N, rows_k = (long long)s.B * s.H * n_k;
-    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
-    gma_status_t r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
+    gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel, dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)),
+                                    dim3(PARAM_THREADS), raw, logits, iv, cst, s.K, s.d_r, s.var_floor);
+    if (r != GMA_OK) return r;
+    r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
     if (r != GMA_OK) return r;
     r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, n_k, s.K, rows_k, st);
     if (r != GMA_OK) return r;
     const int BH = s.B * s.H;
     dim3 gs((unsigned)(BH * nseg), (unsigned)((s.K + KT - 1) / KT));
-    GMA_LAUNCH(KID_SIMT_STATE, st, (simt_state_kernel<Tin><<<gs, THREADS, 0, st>>>(gk, V, agg, n_k, s.K, s.d_v, nseg)));
+    r = launch_chained(KID_SIMT_STATE, st, simt_state_kernel<Tin>, gs, dim3(THREADS), gk, V, agg, n_k, s.K, s.d_v, nseg);
+    if (r != GMA_OK) return r;
     const int KD = s.K * (s.d_v + 1);
     const long long tot = (long long)BH * KD;
-    GMA_LAUNCH(KID_SIMT_SCAN, st, (simt_scan_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(agg, tot, nseg, KD, causal ? 1 : 0)));
-    return GMA_OK;
+    return launch_chained(KID_SIMT_SCAN, st, simt_scan_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), agg, tot,
+                          nseg, KD, causal ? 1 : 0);
 }
 
 // s.N queries and n_k keys per slice (n_k == s.N for the causal variant).
@@ -362,9 +391,8 @@ gma_status_t forward_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
     if (r != GMA_OK) return r;
     const int BH = s.B * s.H;
     const int nseg_q = (s.N + SEG - 1) / SEG;
-    GMA_LAUNCH(KID_SIMT_OUT, st, (simt_out_kernel<Tin, Tout><<<(unsigned)(BH * nseg_q), THREADS, 0, st>>>(
-        gq, gk, V, agg, O, s.N, s.K, s.d_v, nseg_q, L.nseg, s.eps, causal ? 1 : 0)));
-    return GMA_OK;
+    return launch_chained(KID_SIMT_OUT, st, simt_out_kernel<Tin, Tout>, dim3((unsigned)(BH * nseg_q)), dim3(THREADS), gq,
+                          gk, V, agg, O, s.N, s.K, s.d_v, nseg_q, L.nseg, s.eps, causal ? 1 : 0);
 }
 
 
@@ -397,7 +425,10 @@ gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const fl
     const SimtLayout L = simt_layout(s, GMA_VARIANT_RESPONSIBILITIES);
     char *w = (char *)ws;
     float *iv = (float *)(w + L.inv_var), *cst = (float *)(w + L.cst);
-    GMA_LAUNCH(KID_SIMT_PARAMS, st, (simt_params_kernel<<<dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), PARAM_THREADS, 0, st>>>(raw, logits, iv, cst, s.K, s.d_r, s.var_floor)));
+    const gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel,
+                                          dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), dim3(PARAM_THREADS), raw,
+                                          logits, iv, cst, s.K, s.d_r, s.var_floor);
+    if (r != GMA_OK) return r;
     const long long rows = (long long)s.B * s.H * s.N;
     const bool out32 = (s.flags & GMA_FLAG_OUT_F32) || s.dtype == GMA_F32;
     if (s.dtype == GMA_F32)
