@@ -103,6 +103,9 @@ def kernel_work(w, name):
         return "alu", th * w.K * w.d_r * 4, "TFLOP/s"
     if name == "simt_responsibilities":      # one launch covers one side (queries or keys)
         return "alu", th * 2 * w.K * w.d_r * 3, "TFLOP/s"
+    if name == "simt_small_one_launch":   # parameters, both sides' responsibilities, memory and read
+        f = th * 2 * w.K * w.d_r * 3 + w.key_heads * (2 * w.K * w.d_r * 3 + 2 * w.K * (w.d_v + 1))
+        return "alu", f + th * 2 * w.K * (w.d_v + 1), "TFLOP/s"
     if name == "simt_read":
         f = 2 * w.K * (w.d_v + 1)
         if w.causal:

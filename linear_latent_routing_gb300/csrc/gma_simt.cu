@@ -84,15 +84,17 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
 }
 
 // ---------------------------------------------------------------- responsibilities
-template <int DR>
+// (IVG: the inverse variances iv_k are in global memory, read through the read-only cache; else
+// in shared memory.)
+template <int DR, bool IVG = true>
 __device__ __forceinline__ float logit_direct(const float (&x)[DR], const float *__restrict__ mu_k,
-                                              const float *__restrict__ iv_k, float c_k)
+                                              const float *iv_k, float c_k)
 {
     float q = 0.f;
 #pragma unroll
     for (int d = 0; d < DR; ++d) {
         const float t = x[d] - __ldg(mu_k + d);
-        q = fmaf(t * t, __ldg(iv_k + d), q);
+        q = fmaf(t * t, IVG ? __ldg(iv_k + d) : iv_k[d], q);
     }
     return fmaf(-0.5f, q, c_k);
 }
@@ -114,9 +116,9 @@ __device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float b)
 // c_k is kept as a TwoSum pair (Knuth, TAOCP vol. 2, 4.2.2; the "accurate sum" of Ogita, Rump
 // and Oishi, 2005).  Differences of nearby logits, hi_k - hi_j + (lo_k - lo_j), then carry the
 // accuracy of the four-term partials instead of that of a number of size |L|.
-template <int DR>
+template <int DR, bool IVG = true>
 __device__ __forceinline__ float2 logit_direct_pair(const float (&x)[DR], const float *__restrict__ mu_k,
-                                                    const float *__restrict__ iv_k, float c_k)
+                                                    const float *iv_k, float c_k)
 {
     float hi = c_k, lo = 0.f;
 #pragma unroll
@@ -125,7 +127,7 @@ __device__ __forceinline__ float2 logit_direct_pair(const float (&x)[DR], const 
 #pragma unroll
         for (int d = d0; d < d0 + 4; ++d) {
             const float t = x[d] - __ldg(mu_k + d);
-            p = fmaf(t * t, __ldg(iv_k + d), p);
+            p = fmaf(t * t, IVG ? __ldg(iv_k + d) : iv_k[d], p);
         }
         two_sum_acc(hi, lo, -0.5f * p);   // (the factor is a power of two: exact)
     }
@@ -302,6 +304,153 @@ __global__ void simt_out_kernel(const float *__restrict__ gq, const float *__res
     }
 }
 
+// ---------------------------------------------------------------- one launch for short slices
+// Bidirectional and cross-attention calls whose slices are short: one CTA per (b, h) slice runs
+// every step above in shared memory, with the same arithmetic in the same order -- the head's
+// parameters (as simt_params_kernel), Gamma_Q and Gamma_K (as simt_resp_kernel), the memory
+// summed per SEG-token segment and the segments then added in order (as simt_state_kernel and
+// simt_scan_kernel), and the read (as simt_out_kernel) -- in one launch instead of five.
+// Shared memory (floats): 1/sigma^2 [K][DR], constants [K], Gamma_Q [N][K], Gamma_K [NK][K],
+// the value rows [NK][d_v], per-segment memories [nseg][K][d_v + 1], [S | Z] [K][d_v + 1],
+// normalisers [N].
+template <int DR>
+constexpr int small_threads() { return DR <= 32 ? 1024 : DR == 64 ? 512 : 256; }   // (registers: x[DR])
+
+template <int DR, typename Tin, typename Tout>
+__global__ void __launch_bounds__(small_threads<DR>()) simt_small_kernel(
+    const Tin *__restrict__ QX, const Tin *__restrict__ KX, const Tin *__restrict__ V, const float *__restrict__ mu,
+    const float *__restrict__ raw, const float *__restrict__ logits, Tout *__restrict__ O, int H, int N, int NK, int K,
+    int d_v, float floor_, float eps)
+{
+    chain_enter();
+    constexpr bool PRECISE = sizeof(Tin) == 4;
+    constexpr int NT = small_threads<DR>();
+    extern __shared__ float sm[];
+    const int bh = blockIdx.x, h = bh % H, DV1 = d_v + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nseg = (NK + SEG - 1) / SEG;
+    float *iv = sm;
+    float *cs = iv + (size_t)K * DR;
+    float *gq = cs + K;
+    float *gk = gq + (size_t)N * K;
+    float *vs = gk + (size_t)NK * K;
+    float *part = vs + (size_t)NK * d_v;
+    float *S = part + (size_t)nseg * K * DV1;
+    float *den = S + (size_t)K * DV1;
+
+    // the slice's value rows, by coalesced loads (used after the responsibilities)
+    const Tin *Vs = V + (size_t)bh * NK * d_v;
+    for (int e = threadIdx.x; e < NK * d_v; e += NT) vs[e] = to_f32(Vs[e]);
+    // the head's parameters: one warp per component
+    const float *lh = logits + (size_t)h * K;
+    for (int k = warp; k < K; k += NT / 32) {
+        const float *rk = raw + ((size_t)h * K + k) * DR;
+        float rv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rv[i] = lane + 32 * i < DR ? rk[lane + 32 * i] : 0.f;
+        float m = -INFINITY;
+        for (int j = lane; j < K; j += 32) m = fmaxf(m, lh[j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float sum = 0.f;
+        for (int j = lane; j < K; j += 32) sum += expf(lh[j] - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float lse = m + logf(sum);
+        double logdet = 0.0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int d = lane + 32 * i;
+            if (d < DR) {
+                const float r = rv[i];
+                const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
+                iv[k * DR + d] = 1.0f / var;
+                logdet += log((double)var);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) logdet += __shfl_xor_sync(0xffffffffu, logdet, o);
+        if (lane == 0) cs[k] = (float)(((double)lh[k] - (double)lse) - 0.5 * logdet);
+    }
+    __syncthreads();
+
+    // Gamma_Q and Gamma_K: one thread per routing vector
+    const float *muh = mu + (size_t)h * K * DR;
+    for (int r = threadIdx.x; r < N + NK; r += NT) {
+        const bool q = r < N;
+        const int row = q ? r : r - N;
+        const Tin *xr = q ? QX + ((size_t)bh * N + row) * DR : KX + ((size_t)bh * NK + row) * DR;
+        float x[DR];
+#pragma unroll
+        for (int d = 0; d < DR; ++d) x[d] = to_f32(xr[d]);
+        auto logit = [&](int k) -> float2 {
+            if (PRECISE) return logit_direct_pair<DR, false>(x, muh + (size_t)k * DR, iv + k * DR, cs[k]);
+            return make_float2(logit_direct<DR, false>(x, muh + (size_t)k * DR, iv + k * DR, cs[k]), 0.f);
+        };
+        float m = -INFINITY, sum = 0.f;
+        for (int k = 0; k < K; ++k) {
+            const float2 L = logit(k);
+            if (L.x > m) {
+                sum = sum * expf(m - L.x) + expf(L.y);
+                m = L.x;
+            } else {
+                sum += expf((L.x - m) + L.y);
+            }
+        }
+        const float inv = 1.f / sum;
+        float *g = (q ? gq : gk) + (size_t)row * K;
+        for (int k = 0; k < K; ++k) {
+            const float2 L = logit(k);
+            g[k] = expf((L.x - m) + L.y) * inv;
+        }
+    }
+    __syncthreads();
+
+    // [S | Z]: each segment's sum (as the segment pass), then the segments added in order
+    for (int e = threadIdx.x; e < nseg * K * DV1; e += NT) {
+        const int sg = e / (K * DV1), o = e % (K * DV1), kk = o / DV1, c = o % DV1;
+        const int j0 = sg * SEG, jn = min(SEG, NK - j0);
+        float acc = 0.f;
+        if (c < d_v) {
+            for (int j = 0; j < jn; ++j) acc = fmaf(gk[(size_t)(j0 + j) * K + kk], vs[(size_t)(j0 + j) * d_v + c], acc);
+        } else {
+            for (int j = 0; j < jn; ++j) acc += gk[(size_t)(j0 + j) * K + kk];
+        }
+        part[e] = acc;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < K * DV1; e += NT) {
+        float run = 0.f;
+        for (int sg = 0; sg < nseg; ++sg) run += part[(size_t)sg * K * DV1 + e];
+        S[e] = run;
+    }
+    __syncthreads();
+
+    // the read: normalisers, then numerators
+    for (int i = threadIdx.x; i < N; i += NT) {
+        float d = 0.f;
+        for (int k = 0; k < K; ++k) d = fmaf(gq[(size_t)i * K + k], S[(size_t)k * DV1 + d_v], d);
+        den[i] = d + eps;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < N * d_v; e += NT) {
+        const int i = e / d_v, c = e % d_v;
+        float n = 0.f;
+        for (int k = 0; k < K; ++k) n = fmaf(gq[(size_t)i * K + k], S[(size_t)k * DV1 + c], n);
+        O[((size_t)bh * N + i) * d_v + c] = from_f32<Tout>(n / den[i]);
+    }
+}
+
+// Shared memory of simt_small_kernel (0: the shape takes the five launches).
+size_t small_smem_bytes(const gma_shape_t &s, bool causal, int n_k)
+{
+    if (causal || s.N > 512 || n_k > 512) return 0;
+    const size_t dv1 = (size_t)s.d_v + 1, nseg = (size_t)(n_k + SEG - 1) / SEG;
+    const size_t f = (size_t)s.K * s.d_r + s.K + (size_t)s.N * s.K + (size_t)n_k * s.K + (size_t)n_k * s.d_v +
+                     nseg * s.K * dv1 + (size_t)s.K * dv1 + s.N;
+    return f * 4 <= 160 * 1024 ? f * 4 : 0;
+}
+
 // ---------------------------------------------------------------- host side
 struct SimtLayout {
     size_t inv_var, cst, gq, gk, agg, total;
@@ -378,12 +527,43 @@ gma_status_t prepare_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
                           nseg, KD, causal ? 1 : 0);
 }
 
+// The one-launch path for short bidirectional slices (simt_small_kernel).
+template <typename Tin, typename Tout>
+gma_status_t launch_small(const gma_shape_t &s, int n_k, const Tin *QX, const Tin *KX, const Tin *V, const float *mu,
+                          const float *raw, const float *logits, Tout *O, size_t smem, cudaStream_t st)
+{
+    const dim3 g((unsigned)(s.B * s.H));
+    cudaError_t e = cudaSuccess;
+    switch (s.d_r) {
+    case 16:
+        if (cudaFuncSetAttribute(simt_small_kernel<16, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return GMA_ERR_CUDA;
+        GMA_LAUNCH(KID_SIMT_SMALL, st, (e = launch_pdl(simt_small_kernel<16, Tin, Tout>, g, dim3(small_threads<16>()), smem, st, QX, KX, V, mu, raw, logits, O, s.H, s.N, n_k, s.K, s.d_v, s.var_floor, s.eps))); break;
+    case 32:
+        if (cudaFuncSetAttribute(simt_small_kernel<32, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return GMA_ERR_CUDA;
+        GMA_LAUNCH(KID_SIMT_SMALL, st, (e = launch_pdl(simt_small_kernel<32, Tin, Tout>, g, dim3(small_threads<32>()), smem, st, QX, KX, V, mu, raw, logits, O, s.H, s.N, n_k, s.K, s.d_v, s.var_floor, s.eps))); break;
+    case 64:
+        if (cudaFuncSetAttribute(simt_small_kernel<64, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return GMA_ERR_CUDA;
+        GMA_LAUNCH(KID_SIMT_SMALL, st, (e = launch_pdl(simt_small_kernel<64, Tin, Tout>, g, dim3(small_threads<64>()), smem, st, QX, KX, V, mu, raw, logits, O, s.H, s.N, n_k, s.K, s.d_v, s.var_floor, s.eps))); break;
+    case 128:
+        if (cudaFuncSetAttribute(simt_small_kernel<128, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return GMA_ERR_CUDA;
+        GMA_LAUNCH(KID_SIMT_SMALL, st, (e = launch_pdl(simt_small_kernel<128, Tin, Tout>, g, dim3(small_threads<128>()), smem, st, QX, KX, V, mu, raw, logits, O, s.H, s.N, n_k, s.K, s.d_v, s.var_floor, s.eps))); break;
+    default: return GMA_ERR_UNSUPPORTED_SHAPE;
+    }
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
 // s.N queries and n_k keys per slice (n_k == s.N for the causal variant).
 template <typename Tin, typename Tout>
 gma_status_t forward_typed(const gma_shape_t &s, bool causal, int n_k, const Tin *QX, const Tin *KX,
                            const Tin *V, const float *mu, const float *raw, const float *logits,
                            Tout *O, char *ws, cudaStream_t st)
 {
+    const size_t small = small_smem_bytes(s, causal, n_k);
+    if (small) return launch_small<Tin, Tout>(s, n_k, QX, KX, V, mu, raw, logits, O, small, st);
     const SimtLayout L = simt_layout(s, causal ? GMA_VARIANT_CAUSAL : GMA_VARIANT_BIDIRECTIONAL, n_k);
     float *iv = (float *)(ws + L.inv_var), *cst = (float *)(ws + L.cst);
     float *gq = (float *)(ws + L.gq), *gk = (float *)(ws + L.gk), *agg = (float *)(ws + L.agg);

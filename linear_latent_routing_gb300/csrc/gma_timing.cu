@@ -35,6 +35,7 @@ const char *kernel_name(int id)
     case KID_SIMT_STATE: return "simt_segment_memory";
     case KID_SIMT_SCAN: return "simt_segment_scan";
     case KID_SIMT_OUT: return "simt_read";
+    case KID_SIMT_SMALL: return "simt_small_one_launch";
     case KID_TC_PARAMS: return "tc_params";
     case KID_TC_RESP: return "tc_responsibilities";
     case KID_TC_BIDIR_WRITE: return "tc_bidir_write";

@@ -114,6 +114,27 @@ def test_small_bidirectional_key_pass_is_the_one_launched():
     assert normwise_error(O.float().cpu().numpy(), oracle_forward(w, host)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("n,one", [(512, True), (513, False)], ids=["N512_one_launch", "N513_five_launches"])
+def test_short_bidirectional_fp32_slices(n, one):
+    """Bidirectional fp32 slices of up to 512 tokens run the CUDA-core family in one launch (the
+    same arithmetic as its five launches); longer ones take the five.  Both meet 1e-5."""
+    gma = _gma()
+    w = W.scaled(W.TINY_BIDIR_F32, B=2, H=2, N=n)
+    host = W.make_inputs(w)
+    dev = to_device(host)
+    gpu_forward(w, dev)
+    torch.cuda.synchronize()
+    gma.gma_timing_enable(64)
+    O = gpu_forward(w, dev)
+    torch.cuda.synchronize()
+    names = [nm for nm, _ in gma.gma_timing_read(64)]
+    gma.gma_timing_enable(0)
+    assert (names == ["simt_small_one_launch"]) == one, names
+    err = normwise_error(O.float().cpu().numpy(), oracle_forward(w, host))
+    print(f"N={n}: {names}, normwise {err:.3e}")
+    assert err <= TOL["f32"], err
+
+
 def test_fp32_elementwise_relative_error_reported():
     """The stated tolerance is a "max relative error"; the parity tests measure it normwise per
     slice (tests/parity.py says why).  For the fp32 workload this also reports the element-wise
