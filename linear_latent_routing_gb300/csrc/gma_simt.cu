@@ -86,15 +86,29 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
 // ---------------------------------------------------------------- responsibilities
 // (IVG: the inverse variances iv_k are in global memory, read through the read-only cache; else
 // in shared memory.)
+// The rows of mu and 1/sigma^2 are read four floats at a time (16-byte aligned: the API checks the
+// parameter pointers, d_r is a multiple of 4 and the workspace is 256-byte aligned); the sums run
+// over d in order.
+template <bool IVG>
+__device__ __forceinline__ float4 iv4(const float *iv_k, int d)
+{
+    return IVG ? __ldg(reinterpret_cast<const float4 *>(iv_k + d)) : *reinterpret_cast<const float4 *>(iv_k + d);
+}
+
 template <int DR, bool IVG = true>
 __device__ __forceinline__ float logit_direct(const float (&x)[DR], const float *__restrict__ mu_k,
                                               const float *iv_k, float c_k)
 {
     float q = 0.f;
 #pragma unroll
-    for (int d = 0; d < DR; ++d) {
-        const float t = x[d] - __ldg(mu_k + d);
-        q = fmaf(t * t, IVG ? __ldg(iv_k + d) : iv_k[d], q);
+    for (int d = 0; d < DR; d += 4) {
+        const float4 m = __ldg(reinterpret_cast<const float4 *>(mu_k + d));
+        const float4 w = iv4<IVG>(iv_k, d);
+        const float t0 = x[d] - m.x, t1 = x[d + 1] - m.y, t2 = x[d + 2] - m.z, t3 = x[d + 3] - m.w;
+        q = fmaf(t0 * t0, w.x, q);
+        q = fmaf(t1 * t1, w.y, q);
+        q = fmaf(t2 * t2, w.z, q);
+        q = fmaf(t3 * t3, w.w, q);
     }
     return fmaf(-0.5f, q, c_k);
 }
@@ -123,12 +137,14 @@ __device__ __forceinline__ float2 logit_direct_pair(const float (&x)[DR], const 
     float hi = c_k, lo = 0.f;
 #pragma unroll
     for (int d0 = 0; d0 < DR; d0 += 4) {
+        const float4 m = __ldg(reinterpret_cast<const float4 *>(mu_k + d0));
+        const float4 w = iv4<IVG>(iv_k, d0);
+        const float t0 = x[d0] - m.x, t1 = x[d0 + 1] - m.y, t2 = x[d0 + 2] - m.z, t3 = x[d0 + 3] - m.w;
         float p = 0.f;
-#pragma unroll
-        for (int d = d0; d < d0 + 4; ++d) {
-            const float t = x[d] - __ldg(mu_k + d);
-            p = fmaf(t * t, IVG ? __ldg(iv_k + d) : iv_k[d], p);
-        }
+        p = fmaf(t0 * t0, w.x, p);
+        p = fmaf(t1 * t1, w.y, p);
+        p = fmaf(t2 * t2, w.z, p);
+        p = fmaf(t3 * t3, w.w, p);
         two_sum_acc(hi, lo, -0.5f * p);   // (the factor is a power of two: exact)
     }
     return make_float2(hi, lo);
@@ -158,21 +174,34 @@ __global__ void simt_resp_kernel(const Tin *__restrict__ X, const float *__restr
         if (PRECISE) return logit_direct_pair<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k));
         return make_float2(logit_direct<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k)), 0.f);
     };
+    // four components' logits at a time: independent chains of loads and FMAs, each summed in
+    // its own order as before; the online maximum and sum then take them one by one
     float m = -INFINITY, s = 0.f;
-    for (int k = 0; k < K; ++k) {
-        const float2 L = logit(k);
-        if (L.x > m) {
-            s = s * expf(m - L.x) + expf(L.y);
-            m = L.x;
-        } else {
-            s += expf((L.x - m) + L.y);
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        float2 L4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) L4[u] = k0 + u < K ? logit(k0 + u) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (k0 + u >= K) break;
+            const float2 L = L4[u];
+            if (L.x > m) {
+                s = s * expf(m - L.x) + expf(L.y);
+                m = L.x;
+            } else {
+                s += expf((L.x - m) + L.y);
+            }
         }
     }
     const float inv = 1.f / s;
     Tout *g = gamma + r * K;
-    for (int k = 0; k < K; ++k) {
-        const float2 L = logit(k);
-        g[k] = from_f32<Tout>(expf((L.x - m) + L.y) * inv);
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        float2 L4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) L4[u] = k0 + u < K ? logit(k0 + u) : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (k0 + u < K) g[k0 + u] = from_f32<Tout>(expf((L4[u].x - m) + L4[u].y) * inv);
     }
 }
 
