@@ -72,6 +72,27 @@ def test_invalid_shapes_have_no_workspace(g, bad):
     assert g.gma_kernel_family(s, g.GMA_VARIANT_CAUSAL) == -1
 
 
+def test_single_pass_flag_validation(g):
+    """GMA_FLAG_SINGLE_PASS exists in the tensor-core family only: a causal shape that family
+    cannot take (fp32 inputs here, on any machine) has no workspace and no family with it, while
+    the same shape without the flag is valid; the bidirectional entry points ignore the flag; an
+    undefined flag bit is still refused."""
+    sp = g.GMA_FLAG_SINGLE_PASS
+    f32 = _shape(g, dtype=g.GMA_F32, flags=sp)
+    assert g.gma_workspace_size(f32, g.GMA_VARIANT_CAUSAL) == 0
+    assert g.gma_kernel_family(f32, g.GMA_VARIANT_CAUSAL) == -1
+    assert g.gma_workspace_size(_shape(g, dtype=g.GMA_F32), g.GMA_VARIANT_CAUSAL) > 0
+    assert g.gma_workspace_size(f32, g.GMA_VARIANT_BIDIRECTIONAL) == \
+        g.gma_workspace_size(_shape(g, dtype=g.GMA_F32), g.GMA_VARIANT_BIDIRECTIONAL) > 0
+    assert g.gma_workspace_size(_shape(g, flags=0x10), g.GMA_VARIANT_CAUSAL) == 0
+
+
+def test_single_pass_header_value_matches_binding(g):
+    text = open(os.path.join(ROOT, "include", "gma.h")).read()
+    m = re.search(r"#define GMA_FLAG_SINGLE_PASS (0x[0-9a-fA-F]+)u", text)
+    assert m and int(m.group(1), 16) == g.GMA_FLAG_SINGLE_PASS
+
+
 def test_responsibilities_ignore_value_dimension(g):
     s = _shape(g, d_v=7)
     assert g.gma_workspace_size(s, g.GMA_VARIANT_RESPONSIBILITIES) > 0
