@@ -27,7 +27,7 @@ namespace tck {
 namespace {
 
 constexpr int KTHREADS = 320;
-enum KBar { K_BIMG, K_AK, K_LK0, K_LK1, K_GK0, K_GK1, K_SD0, K_SD1, K_V0, K_V1, K_XK, K_NBAR };
+enum KBar { K_BIMG, K_AK, K_LK0, K_LK1, K_GK0, K_GK1, K_SD0, K_SD1, K_V0, K_V1, K_XK, K_FIN, K_NBAR };
 
 struct SmallSmem {
     uint32_t ve0, ve1, abuf, xst, gk0, gk1, bimg, ax, bars, misc, total;
@@ -184,7 +184,11 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
                 if (c >= 1 && !(ok = update(c - 1))) break;
             }
             if (ok && nch > 0) ok = update(nch - 1);
-            if (last_sd >= 0) mbar_wait(bars + K_SD0 + (last_sd & 1), (last_sd >> 1) & 1, a.hdr, 144);
+            // one more commit, on a barrier of its own: it completes once every MMA above has, an
+            // unambiguous phase for the read-out of the memory and for releasing the tensor memory
+            // (the last chunk's own barrier can lag two phases behind, which its parity cannot tell)
+            mma_commit(bars + K_FIN);
+            if (last_sd >= 0) mbar_wait(bars + K_FIN, 0, a.hdr, 144);
         }
     } else if (warp == 9) {
         // ============================================================ loader warp: TMA loads
@@ -257,8 +261,7 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
         // normaliser's dot product) are written as zeros
         if (g == 0 && !*abort) {
             float *dst = a.agg + ((size_t)bh * a.nseg + seg) * KMAX * ne;
-            const int last = nch - 1;
-            const bool ok = nch > 0 && mbar_wait_abortable(bars + K_SD0 + (last & 1), (last >> 1) & 1, a.hdr, 154, abort);
+            const bool ok = nch > 0 && mbar_wait_abortable(bars + K_FIN, 0, a.hdr, 154, abort);
             if (ok) {
                 tc_fence_after();
                 for (int b = 0; b < nblk; ++b) {

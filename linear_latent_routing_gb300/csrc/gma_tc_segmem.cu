@@ -9,12 +9,16 @@
 //
 // Warp roles (320 threads): two key-side groups of four warps take alternate chunks of 128
 // tokens ([x^2, x] from the TMA-staged key rows, softmax -> Gamma_K in their own shared-memory
-// tile); warp 9 issues the TMA loads of the key rows and value tiles as soon as their buffers are
-// free; warp 8 issues the tcgen05.mma's (the logits into the chunk's own TMEM columns and
+// tile); warp 9 issues the TMA loads of the key rows and value tiles, each as soon as its buffer
+// is free (polling both, so neither kind of load waits behind the other); warp 8 issues the tcgen05.mma's (the logits into the chunk's own TMEM columns and
 // S += Gamma_K^T [V | 1] into the running memory) and the stores of Gamma_K.  Logits, Gamma_K
 // and value tiles are double buffered, so one group's softmax overlaps the other group's logits
 // and memory update.
-// Barriers are per buffer, so no waiter can fall two phases behind.
+// Barriers are per buffer, so no waiter can fall two phases behind.  A key group copies its
+// staged row into registers and releases the staging buffer before converting it, so that the
+// next chunk's rows load meanwhile (the key rows' TMA and the [x^2, x] build are the chunk-to-
+// chunk chain, measured); the softmax computes the exponentials again when it stores them
+// instead of holding them, which leaves the registers for that copy.
 // For the causal variant the kernel also stores each chunk's Gamma_K tile (bf16, normalised) to
 // the workspace with a TMA store, so that the output pass reads it instead of recomputing it.
 #include "tc_rows.cuh"
@@ -25,7 +29,7 @@ namespace tck {
 namespace {
 
 constexpr int STHREADS = 320;
-enum SBar { S_BIMG, S_AK, S_LK0, S_LK1, S_GK0, S_GK1, S_SD0, S_SD1, S_V0, S_V1, S_XK, S_NBAR };
+enum SBar { S_BIMG, S_AK, S_LK0, S_LK1, S_GK0, S_GK1, S_SD0, S_SD1, S_V0, S_V1, S_XK, S_XF, S_FIN, S_NBAR };
 constexpr uint32_t SR_L0 = 0, SR_L1 = 128, SR_S = 256;
 
 struct SegSmem {
@@ -50,6 +54,40 @@ struct SegSmem {
         total = o;
     }
 };
+
+// Key side: Gamma_K row k = softmax of the TMEM logits at tl, normalised (zeros when not valid),
+// as bf16 into the K-major SW128 tile gk: the maximum and the sum from the logits, then each
+// chunk of 32 exponentials computed again and stored, instead of holding all of them in
+// registers (the same values as key_softmax_reg, with fewer registers live).
+__device__ __forceinline__ void key_softmax_lean(uint32_t tl, int K, int kc, bool valid, uint8_t *gk, int k)
+{
+    const float m = row_max(tl, K, kc);
+    float sum = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kc; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
+        tmem_ld_wait();
+        sum += chunk_exp(r, c, K, m);
+    }
+    const float scf = valid ? 1.0f / sum : 0.f;
+    const uint32_t sc2 = pack_bf16(scf, scf);
+#pragma unroll 1
+    for (int c = 0; c < kc; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
+        tmem_ld_wait();
+        chunk_exp(r, c, K, m);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t e[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                e[j] = mul_bf16x2(pack_bf16(__uint_as_float(r[8 * q + 2 * j]), __uint_as_float(r[8 * q + 2 * j + 1])), sc2);
+            *reinterpret_cast<uint4 *>(gk + sw128(k, 4 * c + q, C)) = make_uint4(e[0], e[1], e[2], e[3]);
+        }
+    }
+}
 
 }  // namespace
 
@@ -78,7 +116,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
     // ---------------------------------------------------------------- set-up
     if (warp == 8) {
         if (t == 256) {
-            for (int i = 0; i < S_NBAR; ++i) mbar_init(bars + i, (i == S_AK || i == S_GK0 || i == S_GK1) ? 128u : 1u);
+            for (int i = 0; i < S_NBAR; ++i) mbar_init(bars + i, (i == S_AK || i == S_XF || i == S_GK0 || i == S_GK1) ? 128u : 1u);
             *abort = 0;
             fence_mbar_init();
         }
@@ -152,7 +190,11 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
                 if (c >= 1 && !(ok = update(c - 1))) break;
             }
             if (ok && nch > 0) ok = update(nch - 1);
-            if (last_sd >= 0) mbar_wait(bars + S_SD0 + (last_sd & 1), (last_sd >> 1) & 1, a.hdr, 85);
+            // one more commit, on a barrier of its own: it completes once every MMA above has, an
+            // unambiguous phase for the read-out of the memory and for releasing the tensor memory
+            // (the last chunk's own barrier can lag two phases behind, which its parity cannot tell)
+            mma_commit(bars + S_FIN);
+            if (last_sd >= 0) mbar_wait(bars + S_FIN, 0, a.hdr, 85);
             if (a.gam) bulk_wait_all();
         }
     } else if (warp == 9) {
@@ -176,19 +218,34 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             grid_dependency_wait();
             mbar_arrive_expect_tx(bars + S_BIMG, (uint32_t)a.bimg_bytes);
             bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + S_BIMG);
-            for (int c = 0; ok && c < nch; ++c) {
-                if (c + 1 < nch) {   // the staged rows of chunk c have been read into its A tile
-                    if (!(ok = mbar_wait_abortable(bars + S_AK, c & 1, a.hdr, 87, abort))) break;
-                    load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0 + (c + 1) * C, bh);
-                    last_xk = c + 1;
+            // each load as soon as its buffer is free, whichever comes first: the key rows of chunk
+            // nx once chunk nx - 1's were read, the values of chunk nv once the update of chunk
+            // nv - 2 is done (neither test can see a phase ahead: each next phase needs a load this
+            // loop has not issued yet); bounded like every wait
+            int nx = 1, nv = 2;
+            long long t0 = clock64();
+            while (ok && (nx < nch || nv < nch)) {
+                bool progress = false;
+                if (nx < nch && mbar_test_wait(bars + S_XF, (nx - 1) & 1)) {
+                    load_x_tile(smem + L.xst, &kmap, bars + S_XK, DR, tok0 + nx * C, bh);
+                    last_xk = nx++;
+                    progress = true;
                 }
-                // the value buffer of chunk c - 1 is free once its update is done: load chunk c + 1
-                if (c >= 1 && c + 1 < nch) {
-                    if (!(ok = mbar_wait_abortable(bars + S_SD0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 84,
-                                                   abort)))
-                        break;
-                    if ((c - 1) & 1) vpend1 = false; else vpend0 = false;
-                    load_v(c + 1);
+                if (nv < nch && mbar_test_wait(bars + S_SD0 + (nv & 1), ((nv - 2) >> 1) & 1)) {
+                    if (nv & 1) vpend1 = false; else vpend0 = false;
+                    load_v(nv++);
+                    progress = true;
+                }
+                if (progress) {
+                    t0 = clock64();
+                } else if (*abort) {
+                    ok = false;
+                } else if (wait_expired(clock64() - t0, a.hdr)) {
+                    record_error(a.hdr, GMA_ERR_TIMEOUT, 88);
+                    *abort = 1;
+                    ok = false;
+                } else {
+                    __nanosleep(32);
                 }
             }
             // loads still in flight (only after a timeout) complete before shared memory is released
@@ -212,7 +269,14 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             const float lse = (a.lse_k && kvalid) ? a.lse_k[(long long)bh * a.N + base + k] : 0.f;
             if (c >= 1 && !mbar_wait_abortable(bars + S_LK0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 90, abort)) break;
             if (!mbar_wait_abortable(bars + S_XK, c & 1, a.hdr, 94, abort)) break;
-            build_a_s<DR>(smem + L.abuf, k, smem + L.xst);
+            // the staged row into registers, the staging buffer released (the next chunk's rows
+            // load during this chunk's conversion), then [x^2, x] into the A tile
+            uint4 xr[DR / 8];
+#pragma unroll
+            for (int q = 0; q < DR / 8; ++q) xr[q] = *reinterpret_cast<const uint4 *>(smem + L.xst + xs_off<DR>(k, q));
+            fence_proxy_async_smem();   // (these reads come before the next chunk's TMA overwrites the rows)
+            mbar_arrive(bars + S_XF);
+            build_a<DR>(smem + L.abuf, k, xr);
             fence_proxy_async_smem();
             // (a test of the timeout path withholds the first chunk's signal: every wait on it
             // runs out, and all roles leave their loops)
@@ -223,7 +287,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
             if (a.lse_k)
                 key_gamma_lse(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k, lse);
             else
-                key_softmax_reg(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k);
+                key_softmax_lean(lane + (g ? SR_L1 : SR_L0), a.K, kc, kvalid, gk, k);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bars + S_GK0 + g);
@@ -231,8 +295,7 @@ __global__ void __launch_bounds__(STHREADS, 1) tc_segment_memory_pipelined_kerne
         // group 0 writes the segment's memory once the last update is done
         if (g == 0 && !*abort) {
             float *dst = a.agg + (((size_t)bh * a.nseg + seg) * KMAX + k) * ne;
-            const int last = nch - 1;
-            bool ok = nch > 0 && mbar_wait_abortable(bars + S_SD0 + (last & 1), (last >> 1) & 1, a.hdr, 93, abort);
+            bool ok = nch > 0 && mbar_wait_abortable(bars + S_FIN, 0, a.hdr, 93, abort);
             if (nch == 0) {
                 for (int cc = 0; cc < ne; ++cc) dst[cc] = 0.f;
             } else if (ok) {

@@ -227,6 +227,24 @@ def test_full_size_every_token(w):
     assert err <= TOL[w.dtype], err
 
 
+@pytest.mark.parametrize("w", [W.LRA_BIDIR, W.LM_CAUSAL], ids=lambda w: w.name)
+def test_repeated_full_size_calls(w):
+    """Eight calls at full size, each compared with the oracle on every token: a race between a
+    kernel's roles shows as an occasional wrong slice.  (This found one: the read-out of a
+    segment's memory waited on the last chunk's barrier by parity when that barrier could lag two
+    phases behind; it now waits on a barrier of its own committed after the last MMA.)"""
+    host = W.make_inputs(w)
+    a = W.to_numpy(host)
+    ref = oracle_heads(w, a, 0, w.H)
+    dev = to_device(host)
+    den = np.abs(ref).max(axis=(2, 3))
+    for it in range(8):
+        O = gpu_forward(w, dev).float().cpu().numpy()
+        err = np.abs(O - ref).max(axis=(2, 3)) / den
+        bad = np.argwhere(err > TOL[w.dtype])
+        assert len(bad) == 0, (it, float(err.max()), bad[:4].tolist())
+
+
 # config-5 points: one whole slice each (the last one, or every slice where that is cheap)
 SWEEP_FULL = [(W.N_SWEEP[-1], [(1, 15)]), (W.K_SWEEP[3], [(1, 15)]), (W.K_SWEEP[2], [(0, 3)]),
               (W.K_SWEEP[0], [(1, 9)]), (W.N_SWEEP[0], None)]
