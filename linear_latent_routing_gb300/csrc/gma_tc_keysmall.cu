@@ -15,9 +15,10 @@
 // columns, two CTAs share an SM, so one CTA's chunk latency overlaps the other's work.
 //
 // Roles (320 threads) and buffering follow the segment pass: two key groups of four warps take
-// alternate chunks of 128 tokens ([x^2, x] from the TMA-staged key rows, logits by tcgen05 into
-// the chunk's own TMEM columns, softmax -> the group's Gamma_K tile); warp 8 issues the MMAs,
-// warp 9 the TMA loads.  Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all
+// alternate chunks of 128 tokens ([x^2, x] from the TMA-staged key rows, which a group copies to
+// registers and releases before converting them, at d_r <= 32; logits by tcgen05 into the chunk's own TMEM
+// columns; softmax -> the group's Gamma_K tile); warp 8 issues the MMAs, warp 9 the TMA loads,
+// each as soon as its buffer is free.  Every wait is bounded; a timeout records GMA_ERR_TIMEOUT and makes all
 // roles leave their loops.
 #include "tc_rows.cuh"
 
@@ -27,7 +28,7 @@ namespace tck {
 namespace {
 
 constexpr int KTHREADS = 320;
-enum KBar { K_BIMG, K_AK, K_LK0, K_LK1, K_GK0, K_GK1, K_SD0, K_SD1, K_V0, K_V1, K_XK, K_FIN, K_NBAR };
+enum KBar { K_BIMG, K_AK, K_LK0, K_LK1, K_GK0, K_GK1, K_SD0, K_SD1, K_V0, K_V1, K_XK, K_XF, K_FIN, K_NBAR };
 
 struct SmallSmem {
     uint32_t ve0, ve1, abuf, xst, gk0, gk1, bimg, ax, bars, misc, total;
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
     // ---------------------------------------------------------------- set-up
     if (warp == 8) {
         if (t == 256) {
-            for (int i = 0; i < K_NBAR; ++i) mbar_init(bars + i, (i == K_AK || i == K_GK0 || i == K_GK1) ? 128u : 1u);
+            for (int i = 0; i < K_NBAR; ++i) mbar_init(bars + i, (i == K_AK || i == K_XF || i == K_GK0 || i == K_GK1) ? 128u : 1u);
             *abort = 0;
             fence_mbar_init();
         }
@@ -209,19 +210,34 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
             grid_dependency_wait();   // the parameter tables come from the kernel before
             mbar_arrive_expect_tx(bars + K_BIMG, (uint32_t)a.bimg_bytes);
             bulk_g2s(smem + L.bimg, table_of(a, h), (uint32_t)a.bimg_bytes, bars + K_BIMG);
-            for (int c = 0; ok && c < nch; ++c) {
-                if (c + 1 < nch) {   // the staged rows of chunk c have been read into its A tile
-                    if (!(ok = mbar_wait_abortable(bars + K_AK, c & 1, a.hdr, 145, abort))) break;
-                    load_x_tile(smem + L.xst, &kmap, bars + K_XK, DR, tok0 + (c + 1) * C, bh);
-                    last_xk = c + 1;
+            // each load as soon as its buffer is free, whichever comes first: the key rows of chunk
+            // nx once chunk nx - 1's were read, the values of chunk nv once the update of chunk
+            // nv - 2 is done (neither test can see a phase ahead: each next phase needs a load this
+            // loop has not issued yet); bounded like every wait
+            int nx = 1, nv = 2;
+            long long t0 = clock64();
+            while (ok && (nx < nch || nv < nch)) {
+                bool progress = false;
+                if (nx < nch && mbar_test_wait(bars + K_XF, (nx - 1) & 1)) {
+                    load_x_tile(smem + L.xst, &kmap, bars + K_XK, DR, tok0 + nx * C, bh);
+                    last_xk = nx++;
+                    progress = true;
                 }
-                // the value buffer of chunk c - 1 is free once its update is done: load chunk c + 1
-                if (c >= 1 && c + 1 < nch) {
-                    if (!(ok = mbar_wait_abortable(bars + K_SD0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 146,
-                                                   abort)))
-                        break;
-                    if ((c - 1) & 1) vpend1 = false; else vpend0 = false;
-                    load_v(c + 1);
+                if (nv < nch && mbar_test_wait(bars + K_SD0 + (nv & 1), ((nv - 2) >> 1) & 1)) {
+                    if (nv & 1) vpend1 = false; else vpend0 = false;
+                    load_v(nv++);
+                    progress = true;
+                }
+                if (progress) {
+                    t0 = clock64();
+                } else if (*abort) {
+                    ok = false;
+                } else if (wait_expired(clock64() - t0, a.hdr)) {
+                    record_error(a.hdr, GMA_ERR_TIMEOUT, 148);
+                    *abort = 1;
+                    ok = false;
+                } else {
+                    __nanosleep(32);
                 }
             }
             // loads still in flight (only after a timeout) complete before shared memory is released
@@ -242,7 +258,22 @@ __global__ void __launch_bounds__(KTHREADS, 2) tc_key_memory_small_kernel(const 
             // the [x^2, x] buffer is free once the previous chunk's logits are done
             if (c >= 1 && !mbar_wait_abortable(bars + K_LK0 + ((c - 1) & 1), ((c - 1) >> 1) & 1, a.hdr, 150, abort)) break;
             if (!mbar_wait_abortable(bars + K_XK, c & 1, a.hdr, 151, abort)) break;
-            build_a_s<DR>(smem + L.abuf, k, smem + L.xst);
+            if constexpr (DR <= 32) {
+                // the staged row into registers, the staging buffer released (the next chunk's
+                // rows load during this chunk's conversion), then [x^2, x] into the A tile
+                uint4 xr[DR / 8];
+#pragma unroll
+                for (int q = 0; q < DR / 8; ++q) xr[q] = *reinterpret_cast<const uint4 *>(smem + L.xst + xs_off<DR>(k, q));
+                fence_proxy_async_smem();   // (these reads come before the next chunk's TMA overwrites the rows)
+                mbar_arrive(bars + K_XF);
+                build_a<DR>(smem + L.abuf, k, xr);
+            } else {
+                // (at d_r = 64 the row held in registers would spill under the two-CTA budget:
+                // the tile is built from shared memory and the buffer released after)
+                build_a_s<DR>(smem + L.abuf, k, smem + L.xst);
+                fence_proxy_async_smem();
+                mbar_arrive(bars + K_XF);
+            }
             fence_proxy_async_smem();
             // (a test of the timeout path withholds the first chunk's signal: every wait on it
             // runs out, and all roles leave their loops)
