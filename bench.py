@@ -91,16 +91,16 @@ def kernel_work(w, name):
         return "hbm", th * (4 * w.K + 4), "GB/s"
     # backward (fp32 CUDA cores): flops of each kernel's arithmetic, in-segment (64-token) terms included
     dv1 = w.d_v + 1
-    if name == "bwd_numden":
-        return "alu", th * 2 * (w.K * dv1 + (64 * w.K + 32 * dv1 if w.causal else 0)), "TFLOP/s"
+    if name == "bwd_numden":        # num, den and dnd, then the segment partial Gamma_Q^T dnd
+        return "alu", th * 2 * (2 * w.K * dv1 + (32 * w.K + 32 * dv1 if w.causal else 0)), "TFLOP/s"
     if name == "bwd_dgamma_q":
         return "alu", th * 2 * (w.K * dv1 + (32 * w.K + 32 * dv1 if w.causal else 0)), "TFLOP/s"
     if name == "bwd_dgamma_k_dv":
-        return "alu", th * 2 * (w.K * w.d_v + w.K * dv1 + (64 * w.K + 32 * w.d_v + 32 * w.K + 32 * dv1 if w.causal else 0)), "TFLOP/s"
-    if name == "bwd_param_partials":
-        return "alu", 2 * th * w.K * w.d_r * 7, "TFLOP/s"
-    if name == "bwd_dx":            # one launch covers one side
-        return "alu", th * w.K * w.d_r * 4, "TFLOP/s"
+        return "alu", th * 2 * (w.K * w.d_v + w.K * dv1 + (64 * w.K + 32 * w.d_v + 32 * dv1 if w.causal else 0)), "TFLOP/s"
+    if name == "bwd_param_partials":   # both sides' rows: x - mu, one product, two additions per term
+        return "alu", 2 * th * w.K * w.d_r * 5, "TFLOP/s"
+    if name == "bwd_dx":            # one launch covers both sides: two FMAs per term, and the softmax step
+        return "alu", 2 * th * w.K * (4 * w.d_r + 2), "TFLOP/s"
     if name == "simt_responsibilities":      # one launch covers one side (queries or keys)
         return "alu", th * 2 * w.K * w.d_r * 3, "TFLOP/s"
     if name == "simt_small_one_launch":   # parameters, both sides' responsibilities, memory and read

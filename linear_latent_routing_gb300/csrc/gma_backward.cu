@@ -13,8 +13,15 @@
 //   dx_d = -sum_k dL_k (x_d - mu_kd) / s_kd;  dmu, d(raw), d(prior logits) summed over rows.
 // Structure: the forward's own preparation (parameters, Gamma_Q, Gamma_K, 64-token segment
 // memories, scanned), then per 64-token segment the in-segment (causal) terms explicitly and the
-// carried memory D or S for the rest, exactly as the forward read phase splits its work; the
-// parameter gradients are summed per row chunk and then in a fixed order, so results repeat.
+// carried memory D or S for the rest, exactly as the forward read phase splits its work.
+//
+// Every contraction is a register-tiled product over shared-memory tiles: the 256 threads of a
+// block form a 16 x 16 grid, each thread holding 4 rows x (W / 16) columns of a 64-row output W
+// columns wide, and both operands are staged with the contracted index as their row, so that a
+// step of the product is one 16-byte load of four rows of A, one or two loads of B and 4 W / 16
+// FMAs.  Each product is formed in the orientation its consumer reads (P^T where the next product
+// contracts over keys, for instance), so no result is transposed in memory.  All sums run in a
+// fixed order (no atomics): repeated calls give identical bits.
 #include "gma_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -38,181 +45,307 @@ gma_status_t launch_chained(int kid, cudaStream_t st, void (*k)(P...), dim3 g, d
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
-constexpr int SEG = 64;        // tokens per segment (the forward preparation's split)
-constexpr int KT = 32;         // component tile
-constexpr int BT = 256;        // threads per block
+constexpr int SEG = 64;   // tokens per segment (the forward preparation's split)
+constexpr int KT = 64;    // components per tile
+constexpr int BT = 256;   // threads per block
+constexpr int LT = 68;    // row stride of a transposed tile 64 wide (a multiple of 4 for 16-byte
+                          // loads, not of 8, which spreads its column-wise writes over the banks)
 
-// Dynamic shared memory per segment kernel: P [SEG][SEG+1] and a tile area.
-__host__ __device__ inline int seg_smem_floats(int d_v)
+// The thread's first output row and its c-th output column in an output W columns wide: groups
+// of four contiguous columns (two groups 64 apart at W = 128), narrower strips below 64.
+__device__ __forceinline__ int orow() { return (threadIdx.x >> 4) * 4; }
+template <int W>
+__device__ __forceinline__ int ocol(int c)
 {
-    const int dv1 = d_v + 1;
-    const int tile = 2 * SEG * (KT + 1) > SEG * (dv1 + 1) * 2 ? 2 * SEG * (KT + 1) : SEG * (dv1 + 1) * 2;
-    return SEG * (SEG + 1) + tile + SEG;
+    const int tx = threadIdx.x & 15;
+    if constexpr (W == 128) return (c >> 2) * 64 + tx * 4 + (c & 3);
+    else return tx * (W / 16) + c;
 }
 
-// P[i][j] = Gamma_A[i] . Gamma_B[j] over the segment rows (i from rows a0.., j from b0..), via
-// K tiles in shared memory; only entries with (upper ? j >= i : j <= i) are kept (both < n).
-__device__ void seg_gram(const float *__restrict__ ga, const float *__restrict__ gb, int K, int n, bool upper,
-                         float (*P)[SEG + 1], float (*sa)[KT + 1], float (*sb)[KT + 1])
+// The thread's W / 16 columns of one staged row.
+template <int W>
+__device__ __forceinline__ void ld_cols(float (&b)[W / 16], const float *row)
 {
-    constexpr int PER = SEG * SEG / BT;
-    float acc[PER];
+    const int tx = threadIdx.x & 15;
+    if constexpr (W == 16) {
+        b[0] = row[tx];
+    } else if constexpr (W == 32) {
+        const float2 v = *reinterpret_cast<const float2 *>(row + 2 * tx);
+        b[0] = v.x;
+        b[1] = v.y;
+    } else {
 #pragma unroll
-    for (int r = 0; r < PER; ++r) acc[r] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += KT) {
-        const int kn = min(KT, K - k0);
-        for (int e = threadIdx.x; e < SEG * KT; e += BT) {
-            const int i = e / KT, kk = e % KT;
-            const bool ok = i < n && kk < kn;
-            sa[i][kk] = ok ? ga[(size_t)i * K + k0 + kk] : 0.f;
-            sb[i][kk] = ok ? gb[(size_t)i * K + k0 + kk] : 0.f;
+        for (int g = 0; g < W / 64; ++g) {
+            const float4 v = *reinterpret_cast<const float4 *>(row + 64 * g + 4 * tx);
+            b[4 * g] = v.x;
+            b[4 * g + 1] = v.y;
+            b[4 * g + 2] = v.z;
+            b[4 * g + 3] = v.w;
         }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < PER; ++r) {
-            const int e = threadIdx.x + r * BT;
-            const int i = e / SEG, j = e % SEG;
-            float a = acc[r];
-            for (int kk = 0; kk < KT; ++kk) a = fmaf(sa[i][kk], sb[j][kk], a);
-            acc[r] = a;
-        }
-        __syncthreads();
     }
-#pragma unroll
-    for (int r = 0; r < PER; ++r) {
-        const int e = threadIdx.x + r * BT;
-        const int i = e / SEG, j = e % SEG;
-        const bool keep = i < n && j < n && (upper ? j >= i : j <= i);
-        P[i][j] = keep ? acc[r] : 0.f;
-    }
-    __syncthreads();
 }
 
-// dnd[row] = [dnum | dden] for the query rows of one segment.
-template <typename Tin>
+// acc[r][c] += sum_{q < nq} At[q][orow() + r] * Bt[q][ocol<W>(c)]: both operands in shared memory
+// with the contracted index as their row (row strides lda, ldb floats, multiples of 4).
+template <int W>
+__device__ __forceinline__ void mac(float (&acc)[4][W / 16], const float *At, int lda, const float *Bt, int ldb,
+                                    int nq)
+{
+    const int r0 = orow();
+#pragma unroll 4
+    for (int q = 0; q < nq; ++q) {
+        const float4 a = *reinterpret_cast<const float4 *>(At + q * lda + r0);
+        float b[W / 16];
+        ld_cols<W>(b, Bt + q * ldb);
+#pragma unroll
+        for (int c = 0; c < W / 16; ++c) {
+            acc[0][c] = fmaf(a.x, b[c], acc[0][c]);
+            acc[1][c] = fmaf(a.y, b[c], acc[1][c]);
+            acc[2][c] = fmaf(a.z, b[c], acc[2][c]);
+            acc[3][c] = fmaf(a.w, b[c], acc[3][c]);
+        }
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void zero(float (&acc)[4][W / 16])
+{
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < W / 16; ++c) acc[r][c] = 0.f;
+}
+
+// dst[r][c] = src[r * sld + c] for r < R, c < C (zero where r >= nr or c >= nc; those elements of
+// src are not read); dst has row stride ld.  Lanes run along c: coalesced reads, conflict-free
+// writes.
+template <int C, typename T>
+__device__ __forceinline__ void stage(float *dst, int ld, const T *src, long long sld, int R, int nr, int nc)
+{
+    for (int e = threadIdx.x; e < R * C; e += BT) {
+        const int r = e / C, c = e % C;
+        dst[r * ld + c] = (r < nr && c < nc) ? to_f32(src[(long long)r * sld + c]) : 0.f;
+    }
+}
+
+// The transpose: dst[c][r] = src[r * sld + c], dst with row stride ld.
+template <int C, typename T>
+__device__ __forceinline__ void stage_t(float *dst, int ld, const T *src, long long sld, int R, int nr, int nc)
+{
+    for (int e = threadIdx.x; e < R * C; e += BT) {
+        const int r = e / C, c = e % C;
+        dst[c * ld + r] = (r < nr && c < nc) ? to_f32(src[(long long)r * sld + c]) : 0.f;
+    }
+}
+
+// Sum over the 16 threads that share a row of the output grid (lanes xor 1, 2, 4, 8 of a warp).
+__device__ __forceinline__ float row_sum16(float v)
+{
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------- query side, per segment
+// num = Gamma_Q S + tril(P) V and den = Gamma_Q Z + tril(P) 1 + eps for the query rows of one
+// segment (P = Gamma_Q Gamma_K^T on the segment, causal only; [S | Z] the segment's memory), then
+//   dnd[i] = [dO_i / den_i | -(dO_i . num_i) / den_i^2]
+// and the segment's partial G[k][c] = sum_i Gamma_Q[i][k] dnd[i][c], whose suffix sums over later
+// segments are what the keys of a segment receive from the queries after it.
+template <int DV>
+__host__ __device__ constexpr int numden_smem_floats() { return 2 * KT * LT + KT * DV + KT + 2 * SEG; }
+
+template <int DV, typename Tin>
 __global__ void __launch_bounds__(BT) bwd_numden_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                         const Tin *__restrict__ V, const float *__restrict__ agg,
-                                                        const Tin *__restrict__ dO, float *__restrict__ dnd, int N,
-                                                        int K, int d_v, int nseg, float eps, int causal)
+                                                        const Tin *__restrict__ dO, float *__restrict__ dnd,
+                                                        float *__restrict__ dagg, int N, int K, int nseg, float eps,
+                                                        int causal)
 {
     chain_enter();
-    extern __shared__ float sm[];
-    const int dv1 = d_v + 1;
-    float(*P)[SEG + 1] = reinterpret_cast<float(*)[SEG + 1]>(sm);
-    float *tile = sm + SEG * (SEG + 1);
-    float *den = tile + (seg_smem_floats(d_v) - SEG * (SEG + 1) - SEG);
+    extern __shared__ __align__(16) float sm[];
+    constexpr int DV1 = DV + 1, NC = DV / 16;
+    float *gqT = sm;                 // [KT][LT] Gamma_Q^T tile; later Gamma_Q tiles [SEG][KT]
+    float *gkT = gqT + KT * LT;      // [KT][LT] Gamma_K^T tile; later P^T [SEG][LT]
+    float *sS = gkT + KT * LT;       // [KT][DV] S tile; later the value rows, then the dnum rows
+    float *zS = sS + KT * DV;        // [KT]     Z of the tile
+    float *den = zS + KT;            // [SEG]
+    float *dd = den + SEG;           // [SEG]    dden
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
     const int i0 = seg * SEG, n = min(SEG, N - i0);
-    const float *S = agg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * dv1;
-    const float *gqs = gq + ((size_t)bh * N + i0) * K;
-    const float *gks = gk + ((size_t)bh * N + i0) * K;
-    if (causal)
-        seg_gram(gqs, gks, K, n, false, P, reinterpret_cast<float(*)[KT + 1]>(tile),
-                 reinterpret_cast<float(*)[KT + 1]>(tile + SEG * (KT + 1)));
-    // nd[i][c]: numerator (c < d_v) and denominator without eps (c = d_v)
-    float *nd = tile;
-    for (int e = threadIdx.x; e < n * dv1; e += BT) {
-        const int i = e / dv1, c = e % dv1;
-        float a = 0.f;
-        for (int k = 0; k < K; ++k) a = fmaf(gqs[(size_t)i * K + k], S[(size_t)k * dv1 + c], a);
-        if (causal)
-            for (int j = 0; j <= i; ++j)
-                a = fmaf(P[i][j], c < d_v ? to_f32(V[((size_t)bh * N + i0 + j) * d_v + c]) : 1.f, a);
-        nd[i * dv1 + c] = a;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += BT) {
-        const float dn = nd[i * dv1 + d_v] + eps;
-        float dot = 0.f;
-        for (int c = 0; c < d_v; ++c) dot = fmaf(to_f32(dO[((size_t)bh * N + i0 + i) * d_v + c]), nd[i * dv1 + c], dot);
-        den[i] = dn;
-        nd[i * dv1 + d_v] = -dot / (dn * dn);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n * dv1; e += BT) {
-        const int i = e / dv1, c = e % dv1;
-        const float v = c < d_v ? to_f32(dO[((size_t)bh * N + i0 + i) * d_v + c]) / den[i] : nd[i * dv1 + d_v];
-        dnd[((size_t)bh * N + i0 + i) * dv1 + c] = v;
-    }
-}
-
-// dGamma_Q for the query rows of one segment:
-//   dgq[i][k] = dnd_i . [S | Z][k] + sum_{j <= i in segment} (dnd_i . [v_j | 1]) Gamma_K[j][k].
-template <typename Tin>
-__global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ gk, const Tin *__restrict__ V,
-                                                     const float *__restrict__ agg, const float *__restrict__ dnd,
-                                                     float *__restrict__ dgq, int N, int K, int d_v, int nseg,
-                                                     int causal)
-{
-    chain_enter();
-    extern __shared__ float sm[];
-    const int dv1 = d_v + 1;
-    float(*A)[SEG + 1] = reinterpret_cast<float(*)[SEG + 1]>(sm);
-    float *rows = sm + SEG * (SEG + 1);          // dnd rows [SEG][dv1]
-    float *vrows = rows + SEG * dv1;             // [v | 1] rows [SEG][dv1]
-    const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
-    const int i0 = seg * SEG, n = min(SEG, N - i0);
-    const float *S = agg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * dv1;
-    for (int e = threadIdx.x; e < SEG * dv1; e += BT) {
-        const int i = e / dv1, c = e % dv1;
-        rows[e] = i < n ? dnd[((size_t)bh * N + i0 + i) * dv1 + c] : 0.f;
-        vrows[e] = i < n ? (c < d_v ? to_f32(V[((size_t)bh * N + i0 + i) * d_v + c]) : 1.f) : 0.f;
+    const long long row0 = (long long)bh * N + i0;
+    const float *S = agg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * DV1;
+    const int t = threadIdx.x, r0 = orow();
+    float accP[4][4], accN[4][NC];
+    zero<64>(accP);
+    zero<DV>(accN);
+    float dpart = 0.f;
+    for (int k0 = 0; k0 < K; k0 += KT) {
+        const int kn = min(KT, K - k0);
+        __syncthreads();
+        stage_t<KT>(gqT, LT, gq + row0 * K + k0, K, SEG, n, kn);
+        if (causal) stage_t<KT>(gkT, LT, gk + row0 * K + k0, K, SEG, n, kn);
+        stage<DV>(sS, DV, S + (size_t)k0 * DV1, DV1, KT, kn, DV);
+        if (t < KT) zS[t] = t < kn ? S[(size_t)(k0 + t) * DV1 + DV] : 0.f;
+        __syncthreads();
+        if (causal) mac<64>(accP, gkT, LT, gqT, LT, KT);   // P^T: rows j, columns i
+        mac<DV>(accN, gqT, LT, sS, DV, KT);                // rows i, columns c
+        if (t < SEG) {
+            float a = 0.f;
+            for (int k = 0; k < KT; ++k) a = fmaf(gqT[k * LT + t], zS[k], a);
+            dpart += a;
+        }
     }
     __syncthreads();
     if (causal) {
-        for (int e = threadIdx.x; e < SEG * SEG; e += BT) {
-            const int i = e / SEG, j = e % SEG;
-            float a = 0.f;
-            if (j <= i && i < n)
-                for (int c = 0; c < dv1; ++c) a = fmaf(rows[i * dv1 + c], vrows[j * dv1 + c], a);
-            A[i][j] = a;
-        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = r0 + r, i = ocol<64>(c);
+                gkT[j * LT + i] = i >= j ? accP[r][c] : 0.f;
+            }
+        stage<DV>(sS, DV, V + row0 * DV, DV, SEG, n, DV);
         __syncthreads();
+        mac<DV>(accN, gkT, LT, sS, DV, SEG);
+        if (t < SEG) {
+            float a = 0.f;
+            for (int j = 0; j < SEG; ++j) a += gkT[j * LT + t];
+            dpart += a;
+        }
     }
-    const float *gks = gk + ((size_t)bh * N + i0) * K;
-    for (int e = threadIdx.x; e < n * K; e += BT) {
-        const int i = e / K, k = e % K;
-        float a = 0.f;
-        for (int c = 0; c < dv1; ++c) a = fmaf(rows[i * dv1 + c], S[(size_t)k * dv1 + c], a);
-        if (causal)
-            for (int j = 0; j <= i; ++j) a = fmaf(A[i][j], gks[(size_t)j * K + k], a);
-        dgq[((size_t)bh * N + i0 + i) * K + k] = a;
+    if (t < SEG) den[t] = dpart + eps;
+    __syncthreads();
+    // dnum over num, then dden: the rows' dot products are summed over the 16 threads of a row
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = r0 + r;
+        const float dn = den[i];
+        float dot = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const float o = i < n ? to_f32(dO[(row0 + i) * DV + ocol<DV>(c)]) : 0.f;
+            dot = fmaf(o, accN[r][c], dot);
+            accN[r][c] = o / dn;
+        }
+        dot = row_sum16(dot);
+        const float ddi = i < n ? -dot / (dn * dn) : 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            if (i < n) dnd[(row0 + i) * DV1 + ocol<DV>(c)] = accN[r][c];
+            sS[i * DV + ocol<DV>(c)] = accN[r][c];
+        }
+        if ((t & 15) == 0) {
+            if (i < n) dnd[(row0 + i) * DV1 + DV] = ddi;
+            dd[i] = ddi;
+        }
+    }
+    // G, one component tile at a time
+    float *G = dagg + ((size_t)bh * nseg + seg) * K * DV1;
+    for (int k0 = 0; k0 < K; k0 += KT) {
+        const int kn = min(KT, K - k0);
+        __syncthreads();
+        stage<KT>(gqT, KT, gq + row0 * K + k0, K, SEG, n, kn);
+        __syncthreads();
+        float accG[4][NC];
+        zero<DV>(accG);
+        mac<DV>(accG, gqT, KT, sS, DV, SEG);   // rows k, columns c
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int k = k0 + r0 + r;
+            if (k < K)
+#pragma unroll
+                for (int c = 0; c < NC; ++c) G[(size_t)k * DV1 + ocol<DV>(c)] = accG[r][c];
+        }
+        if (t < kn) {
+            float a = 0.f;
+            for (int i = 0; i < SEG; ++i) a = fmaf(gqT[i * KT + t], dd[i], a);
+            G[(size_t)(k0 + t) * DV1 + DV] = a;
+        }
     }
 }
 
-// Segment partials G[bh][seg][k][c] = sum_{i in segment} Gamma_Q[i][k] dnd[i][c].
-__global__ void __launch_bounds__(BT) bwd_seg_kernel(const float *__restrict__ gq, const float *__restrict__ dnd,
-                                                     float *__restrict__ dagg, int N, int K, int d_v, int nseg)
+// dGamma_Q[i][k] = dnd_i . [S | Z][k] + sum_{j <= i in segment} A[i][j] Gamma_K[j][k] for the query
+// rows of one segment, with A[i][j] = dnd_i . [v_j | 1] (causal only), and the row's
+// <Gamma_Q, dGamma_Q> for the softmax step.
+template <int DV>
+__host__ __device__ constexpr int dgq_smem_floats() { return 2 * DV * LT + SEG * LT + SEG * KT + KT + SEG; }
+
+template <int DV, typename Tin>
+__global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
+                                                     const Tin *__restrict__ V, const float *__restrict__ agg,
+                                                     const float *__restrict__ dnd, float *__restrict__ dgq,
+                                                     float *__restrict__ dotq, int N, int K, int nseg, int causal)
 {
     chain_enter();
+    extern __shared__ __align__(16) float sm[];
+    constexpr int DV1 = DV + 1;
+    float *dnT = sm;                 // [DV][LT]  dnum^T
+    float *VT = dnT + DV * LT;       // [DV][LT]  V^T; later the S^T tiles
+    float *AT = VT + DV * LT;        // [SEG][LT] A^T
+    float *gK = AT + SEG * LT;       // [SEG][KT] Gamma_K tile
+    float *zS = gK + SEG * KT;       // [KT]
+    float *dd = zS + KT;             // [SEG]
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
-    const int k0 = blockIdx.y * KT;
-    const int j0 = seg * SEG, jn = min(SEG, N - j0);
-    const int kn = min(KT, K - k0);
-    const int dv1 = d_v + 1;
-    __shared__ float sg[SEG][KT + 1];
-    __shared__ float sv[SEG][129 + 1];
-    for (int e = threadIdx.x; e < SEG * KT; e += BT) {
-        const int j = e / KT, kk = e % KT;
-        sg[j][kk] = (j < jn && kk < kn) ? gq[((size_t)bh * N + j0 + j) * K + k0 + kk] : 0.f;
+    const int i0 = seg * SEG, n = min(SEG, N - i0);
+    const long long row0 = (long long)bh * N + i0;
+    const float *S = agg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * DV1;
+    const int t = threadIdx.x, r0 = orow();
+    stage_t<DV>(dnT, LT, dnd + row0 * DV1, DV1, SEG, n, DV);
+    if (t < SEG) dd[t] = t < n ? dnd[(row0 + t) * DV1 + DV] : 0.f;
+    if (causal) {
+        stage_t<DV>(VT, LT, V + row0 * DV, DV, SEG, n, DV);
+        __syncthreads();
+        float accA[4][4];
+        zero<64>(accA);
+        mac<64>(accA, VT, LT, dnT, LT, DV);   // rows j, columns i: v_j . dnum_i
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = r0 + r, i = ocol<64>(c);
+                AT[j * LT + i] = i >= j ? accA[r][c] + dd[i] : 0.f;
+            }
     }
-    for (int e = threadIdx.x; e < SEG * dv1; e += BT) {
-        const int j = e / dv1, c = e % dv1;
-        sv[j][c] = j < jn ? dnd[((size_t)bh * N + j0 + j) * dv1 + c] : 0.f;
+    float dot[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < K; k0 += KT) {
+        const int kn = min(KT, K - k0);
+        __syncthreads();
+        stage_t<DV>(VT, LT, S + (size_t)k0 * DV1, DV1, KT, kn, DV);   // S^T: [c][k]
+        if (t < KT) zS[t] = t < kn ? S[(size_t)(k0 + t) * DV1 + DV] : 0.f;
+        if (causal) stage<KT>(gK, KT, gk + row0 * K + k0, K, SEG, n, kn);
+        __syncthreads();
+        float acc[4][4];
+        zero<64>(acc);
+        mac<64>(acc, dnT, LT, VT, LT, DV);                  // rows i, columns k
+        if (causal) mac<64>(acc, AT, LT, gK, KT, SEG);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = r0 + r;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int kk = ocol<64>(c), k = k0 + kk;
+                const float v = fmaf(dd[i], zS[kk], acc[r][c]);
+                if (i < n && k < K) {
+                    dgq[(row0 + i) * K + k] = v;
+                    dot[r] = fmaf(gq[(row0 + i) * K + k], v, dot[r]);
+                }
+            }
+        }
     }
-    __syncthreads();
-    float *out = dagg + ((size_t)bh * nseg + seg) * K * dv1;
-    for (int e = threadIdx.x; e < kn * dv1; e += BT) {
-        const int kk = e / dv1, c = e % dv1;
-        float acc = 0.f;
-        for (int j = 0; j < jn; ++j) acc = fmaf(sg[j][kk], sv[j][c], acc);
-        out[(size_t)(k0 + kk) * dv1 + c] = acc;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const float s = row_sum16(dot[r]);
+        if ((t & 15) == 0 && r0 + r < n) dotq[row0 + r0 + r] = s;
     }
 }
 
 // Causal: each segment's partial becomes the exclusive suffix over later segments (what the
 // keys of the segment see from queries after it).  Bidirectional: the total into segment 0.
-__global__ void bwd_scan_kernel(float *__restrict__ dagg, long long total, int nseg, int KD, int causal)
+// One thread per element of the K x (d_v + 1) memory; the loads of eight segments are issued
+// before their sums, so a thread waits once per eight segments.
+__global__ void __launch_bounds__(BT) bwd_scan_kernel(float *__restrict__ dagg, long long total, int nseg, int KD,
+                                                      int causal)
 {
     chain_enter();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -220,205 +353,308 @@ __global__ void bwd_scan_kernel(float *__restrict__ dagg, long long total, int n
     const long long bh = idx / KD, e = idx % KD;
     float *base = dagg + bh * nseg * KD + e;
     float run = 0.f;
-    for (int s = nseg - 1; s >= 0; --s) {
-        const float a = base[(size_t)s * KD];
-        if (causal) base[(size_t)s * KD] = run;
-        run += a;
+    for (int s1 = nseg; s1 > 0; s1 -= 8) {
+        float a[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a[u] = s1 - 1 - u >= 0 ? base[(size_t)(s1 - 1 - u) * KD] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (s1 - 1 - u < 0) break;
+            if (causal) base[(size_t)(s1 - 1 - u) * KD] = run;
+            run += a[u];
+        }
     }
     if (!causal) base[0] = run;
 }
 
-// The key rows of one segment: with D the carried memory (exclusive suffix or total),
-//   d[v_j | 1] = Gamma_K[j] D + sum_{i >= j in segment} (Gamma_K[j] . Gamma_Q[i]) dnd_i
-//   dgk[j][k]  = [v_j | 1] . D[k] + sum_{i >= j in segment} ([v_j | 1] . dnd_i) Gamma_Q[i][k]
-template <typename Tin>
+// The key rows of one segment, with D the carried memory (exclusive suffix or total):
+//   dV[j] = Gamma_K[j] D + sum_{i >= j in segment} P[i][j] dnum_i      (the first d_v columns
+//                                                                      of d[v_j | 1])
+//   dGamma_K[j][k] = [v_j | 1] . D[k] + sum_{i >= j in segment} A[i][j] Gamma_Q[i][k]
+// (P = Gamma_Q Gamma_K^T and A[i][j] = dnd_i . [v_j | 1], causal only), and the row's
+// <Gamma_K, dGamma_K>.
+template <int DV>
+__host__ __device__ constexpr int dk_smem_floats() { return 2 * KT * LT + 2 * DV * LT + KT + SEG; }
+
+template <int DV, typename Tin>
 __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                     const Tin *__restrict__ V, const float *__restrict__ dagg,
                                                     const float *__restrict__ dnd, float *__restrict__ dgk,
-                                                    Tin *__restrict__ dV, int N, int K, int d_v, int nseg,
-                                                    int causal)
+                                                    float *__restrict__ dotk, Tin *__restrict__ dV, int N, int K,
+                                                    int nseg, int causal)
 {
     chain_enter();
-    extern __shared__ float sm[];
-    const int dv1 = d_v + 1;
-    float(*P)[SEG + 1] = reinterpret_cast<float(*)[SEG + 1]>(sm);
-    float *tile = sm + SEG * (SEG + 1);
+    extern __shared__ __align__(16) float sm[];
+    constexpr int DV1 = DV + 1, NC = DV / 16;
+    float *gqT = sm;                 // [KT][LT] Gamma_Q^T tile; later P [SEG][LT], then A [SEG][LT]
+    float *gkT = gqT + KT * LT;      // [KT][LT] Gamma_K^T tile; later Gamma_Q tiles [SEG][KT]
+    float *VT = gkT + KT * LT;       // [DV][LT] V^T; before it, the D tiles [KT][DV], then the dnum rows
+    float *DT = VT + DV * LT;        // [DV][LT] dnum^T; later the D^T tiles
+    float *zD = DT + DV * LT;        // [KT]
+    float *dd = zD + KT;             // [SEG]
+    float *sD = VT;
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
     const int j0 = seg * SEG, n = min(SEG, N - j0);
-    const float *D = dagg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * dv1;
-    const float *gqs = gq + ((size_t)bh * N + j0) * K;
-    const float *gks = gk + ((size_t)bh * N + j0) * K;
-    // P[j][i] = Gamma_K[j] . Gamma_Q[i] for i >= j
-    if (causal)
-        seg_gram(gks, gqs, K, n, true, P, reinterpret_cast<float(*)[KT + 1]>(tile),
-                 reinterpret_cast<float(*)[KT + 1]>(tile + SEG * (KT + 1)));
-    float *rows = tile;                      // dnd rows [SEG][dv1]
-    float *vrows = rows + SEG * dv1;         // [v | 1] rows
-    for (int e = threadIdx.x; e < SEG * dv1; e += BT) {
-        const int i = e / dv1, c = e % dv1;
-        rows[e] = i < n ? dnd[((size_t)bh * N + j0 + i) * dv1 + c] : 0.f;
-        vrows[e] = i < n ? (c < d_v ? to_f32(V[((size_t)bh * N + j0 + i) * d_v + c]) : 1.f) : 0.f;
+    const long long row0 = (long long)bh * N + j0;
+    const float *D = dagg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * DV1;
+    const int t = threadIdx.x, r0 = orow();
+    // dV
+    float accP[4][4], accV[4][NC];
+    zero<64>(accP);
+    zero<DV>(accV);
+    for (int k0 = 0; k0 < K; k0 += KT) {
+        const int kn = min(KT, K - k0);
+        __syncthreads();
+        if (causal) stage_t<KT>(gqT, LT, gq + row0 * K + k0, K, SEG, n, kn);
+        stage_t<KT>(gkT, LT, gk + row0 * K + k0, K, SEG, n, kn);
+        stage<DV>(sD, DV, D + (size_t)k0 * DV1, DV1, KT, kn, DV);
+        __syncthreads();
+        if (causal) mac<64>(accP, gqT, LT, gkT, LT, KT);   // P: rows i, columns j
+        mac<DV>(accV, gkT, LT, sD, DV, KT);                // rows j, columns c
     }
     __syncthreads();
-    // dV (columns c < d_v of d[v | 1])
-    for (int e = threadIdx.x; e < n * d_v; e += BT) {
-        const int j = e / d_v, c = e % d_v;
-        float a = 0.f;
-        for (int k = 0; k < K; ++k) a = fmaf(gks[(size_t)j * K + k], D[(size_t)k * dv1 + c], a);
-        if (causal)
-            for (int i = j; i < n; ++i) a = fmaf(P[j][i], rows[i * dv1 + c], a);
-        dV[((size_t)bh * N + j0 + j) * d_v + c] = from_f32<Tin>(a);
-    }
-    __syncthreads();
-    // A[j][i] = [v_j | 1] . dnd_i for i >= j, into P's storage
     if (causal) {
-        for (int e = threadIdx.x; e < SEG * SEG; e += BT) {
-            const int j = e / SEG, i = e % SEG;
-            float a = 0.f;
-            if (i >= j && i < n)
-                for (int c = 0; c < dv1; ++c) a = fmaf(vrows[j * dv1 + c], rows[i * dv1 + c], a);
-            P[j][i] = a;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = r0 + r, j = ocol<64>(c);
+                gqT[i * LT + j] = i >= j ? accP[r][c] : 0.f;
+            }
+        stage<DV>(sD, DV, dnd + row0 * DV1, DV1, SEG, n, DV);
+        __syncthreads();
+        mac<DV>(accV, gqT, LT, sD, DV, SEG);   // sum_i P[i][j] dnum_i
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int j = r0 + r;
+        if (j < n)
+#pragma unroll
+            for (int c = 0; c < NC; ++c) dV[(row0 + j) * DV + ocol<DV>(c)] = from_f32<Tin>(accV[r][c]);
+    }
+    // dGamma_K
+    __syncthreads();
+    stage_t<DV>(VT, LT, V + row0 * DV, DV, SEG, n, DV);
+    if (causal) {
+        stage_t<DV>(DT, LT, dnd + row0 * DV1, DV1, SEG, n, DV);
+        if (t < SEG) dd[t] = t < n ? dnd[(row0 + t) * DV1 + DV] : 0.f;
+        __syncthreads();
+        float accA[4][4];
+        zero<64>(accA);
+        mac<64>(accA, DT, LT, VT, LT, DV);   // rows i, columns j: dnum_i . v_j
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = r0 + r, j = ocol<64>(c);
+                gqT[i * LT + j] = i >= j ? accA[r][c] + dd[i] : 0.f;
+            }
+    }
+    float dot[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < K; k0 += KT) {
+        const int kn = min(KT, K - k0);
+        __syncthreads();
+        stage_t<DV>(DT, LT, D + (size_t)k0 * DV1, DV1, KT, kn, DV);   // D^T: [c][k]
+        if (t < KT) zD[t] = t < kn ? D[(size_t)(k0 + t) * DV1 + DV] : 0.f;
+        if (causal) stage<KT>(gkT, KT, gq + row0 * K + k0, K, SEG, n, kn);
+        __syncthreads();
+        float acc[4][4];
+        zero<64>(acc);
+        mac<64>(acc, VT, LT, DT, LT, DV);                 // rows j, columns k
+        if (causal) mac<64>(acc, gqT, LT, gkT, KT, SEG);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int j = r0 + r;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int kk = ocol<64>(c), k = k0 + kk;
+                const float v = acc[r][c] + zD[kk];
+                if (j < n && k < K) {
+                    dgk[(row0 + j) * K + k] = v;
+                    dot[r] = fmaf(gk[(row0 + j) * K + k], v, dot[r]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const float s = row_sum16(dot[r]);
+        if ((t & 15) == 0 && r0 + r < n) dotk[row0 + r0 + r] = s;
+    }
+}
+
+// ---------------------------------------------------------------- through the responsibilities
+// The rows of one segment of one side (blockIdx.y: 0 queries, 1 keys):
+//   dL = Gamma (dGamma - <Gamma, dGamma>)     (written back over dGamma for the parameters)
+//   dx_d = sum_k dL_k (w_kd mu_kd - w_kd x_d)  (w = 1 / sigma^2)
+// The contraction over k runs as the products above, with the factor w_kd mu_kd - w_kd x_d formed
+// per step from the thread's own x (two FMAs per term).
+template <int DR>
+__host__ __device__ constexpr int dx_smem_floats() { return KT * LT + 2 * KT * DR + SEG; }
+
+template <int DR, typename Tin>
+__global__ void __launch_bounds__(BT) bwd_dx_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
+                                                    const float *__restrict__ gq, const float *__restrict__ gk,
+                                                    float *__restrict__ dgq, float *__restrict__ dgk,
+                                                    const float *__restrict__ dotq, const float *__restrict__ dotk,
+                                                    const float *__restrict__ mu, const float *__restrict__ iv,
+                                                    Tin *__restrict__ dQX, Tin *__restrict__ dKX, int H, int N, int K,
+                                                    int nseg)
+{
+    chain_enter();
+    extern __shared__ __align__(16) float sm[];
+    constexpr int NC = DR / 16;
+    float *dLT = sm;                 // [KT][LT] dL^T tile
+    float *sW = dLT + KT * LT;       // [KT][DR] w
+    float *sWM = sW + KT * DR;       // [KT][DR] w mu
+    float *sdot = sWM + KT * DR;     // [SEG]
+    const int side = blockIdx.y;
+    const Tin *X = side ? KX : QX;
+    const float *g = side ? gk : gq;
+    float *dg = side ? dgk : dgq;
+    Tin *dX = side ? dKX : dQX;
+    const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg, h = bh % H;
+    const int i0 = seg * SEG, n = min(SEG, N - i0);
+    const long long row0 = (long long)bh * N + i0;
+    const int t = threadIdx.x, r0 = orow();
+    if (t < SEG) sdot[t] = t < n ? (side ? dotk : dotq)[row0 + t] : 0.f;
+    float x[4][NC], acc[4][NC];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            x[r][c] = r0 + r < n ? to_f32(X[(row0 + r0 + r) * DR + ocol<DR>(c)]) : 0.f;
+            acc[r][c] = 0.f;
+        }
+    const float *muh = mu + (size_t)h * K * DR, *ivh = iv + (size_t)h * K * DR;
+    for (int k0 = 0; k0 < K; k0 += KT) {
+        const int kn = min(KT, K - k0);
+        __syncthreads();
+        for (int e = t; e < SEG * KT; e += BT) {
+            const int r = e / KT, kk = e % KT;
+            float v = 0.f;
+            if (r < n && kk < kn) {
+                const long long o = (row0 + r) * K + k0 + kk;
+                v = g[o] * (dg[o] - sdot[r]);
+                dg[o] = v;
+            }
+            dLT[kk * LT + r] = v;
+        }
+        for (int e = t; e < KT * DR; e += BT) {
+            const int kk = e / DR, d = e % DR;
+            const float w = kk < kn ? ivh[(size_t)(k0 + kk) * DR + d] : 0.f;
+            const float m = kk < kn ? muh[(size_t)(k0 + kk) * DR + d] : 0.f;
+            sW[e] = w;
+            sWM[e] = w * m;
         }
         __syncthreads();
-    }
-    for (int e = threadIdx.x; e < n * K; e += BT) {
-        const int j = e / K, k = e % K;
-        float a = 0.f;
-        for (int c = 0; c < dv1; ++c) a = fmaf(vrows[j * dv1 + c], D[(size_t)k * dv1 + c], a);
-        if (causal)
-            for (int i = j; i < n; ++i) a = fmaf(P[j][i], gqs[(size_t)i * K + k], a);
-        dgk[((size_t)bh * N + j0 + j) * K + k] = a;
-    }
-}
-
-// dL = Gamma * (dGamma - <Gamma, dGamma>) in place over dg, one warp per row.
-__global__ void __launch_bounds__(BT) bwd_softmax_kernel(const float *__restrict__ g, float *__restrict__ dg,
-                                                         long long rows, int K)
-{
-    chain_enter();
-    const long long r = (long long)blockIdx.x * (BT / 32) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (r >= rows) return;
-    const float *gr = g + r * K;
-    float *dr = dg + r * K;
-    float dot = 0.f;
-    for (int k = lane; k < K; k += 32) dot = fmaf(gr[k], dr[k], dot);
+#pragma unroll 2
+        for (int q = 0; q < KT; ++q) {
+            const float4 a = *reinterpret_cast<const float4 *>(dLT + q * LT + r0);
+            float w[NC], wm[NC];
+            ld_cols<DR>(w, sW + q * DR);
+            ld_cols<DR>(wm, sWM + q * DR);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    for (int k = lane; k < K; k += 32) dr[k] = gr[k] * (dr[k] - dot);
+            for (int c = 0; c < NC; ++c) {
+                acc[0][c] = fmaf(a.x, fmaf(-w[c], x[0][c], wm[c]), acc[0][c]);
+                acc[1][c] = fmaf(a.y, fmaf(-w[c], x[1][c], wm[c]), acc[1][c]);
+                acc[2][c] = fmaf(a.z, fmaf(-w[c], x[2][c], wm[c]), acc[2][c]);
+                acc[3][c] = fmaf(a.w, fmaf(-w[c], x[3][c], wm[c]), acc[3][c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+        if (r0 + r < n)
+#pragma unroll
+            for (int c = 0; c < NC; ++c) dX[(row0 + r0 + r) * DR + ocol<DR>(c)] = from_f32<Tin>(acc[r][c]);
 }
 
-// dx_d = -sum_k dL_k (x_d - mu_kd) / s_kd, one thread per row.
+// ---------------------------------------------------------------- parameter gradients
+// Partial sums of head h over a range of 64-row blocks (query rows, then key rows; block b is side
+// b / (B nseg), batch row (b / nseg) % B, segment b % nseg) for the components of one tile:
+//   pmu[h][ch][k][d] = sum dL_k (x_d - mu_kd),  ps[h][ch][k][d] = sum dL_k (x_d - mu_kd)^2,
+//   pl[h][ch][k] = sum dL_k
+// (the factors w_kd, w_kd^2 / 2 and -w_kd / 2 are applied once, in the final kernel).  Each thread
+// keeps mu of its 4 components x (d_r / 16) dimensions in registers; per row and term: one
+// subtraction, one product and two additions.
+template <int DR>
+__host__ __device__ constexpr int param_smem_floats() { return SEG * KT + SEG * DR; }
+
 template <int DR, typename Tin>
-__global__ void __launch_bounds__(BT) bwd_dx_kernel(const Tin *__restrict__ X, const float *__restrict__ dL,
-                                                    const float *__restrict__ mu, const float *__restrict__ iv,
-                                                    Tin *__restrict__ dX, int H, int N, int K, long long rows)
-{
-    chain_enter();
-    const long long r = (long long)blockIdx.x * BT + threadIdx.x;
-    if (r >= rows) return;
-    const int h = (int)((r / N) % H);
-    float x[DR], dx[DR];
-#pragma unroll
-    for (int d = 0; d < DR; ++d) {
-        x[d] = to_f32(X[r * DR + d]);
-        dx[d] = 0.f;
-    }
-    const float *muh = mu + (size_t)h * K * DR, *ivh = iv + (size_t)h * K * DR;
-    const float *dl = dL + r * K;
-    for (int k = 0; k < K; ++k) {
-        const float a = dl[k];
-#pragma unroll
-        for (int d = 0; d < DR; ++d) dx[d] = fmaf(-a * __ldg(ivh + (size_t)k * DR + d), x[d] - __ldg(muh + (size_t)k * DR + d), dx[d]);
-    }
-#pragma unroll
-    for (int d = 0; d < DR; ++d) dX[r * DR + d] = from_f32<Tin>(dx[d]);
-}
-
-// Per-chunk partial sums of the parameter gradients of head h over its rows (query rows, then
-// key rows), for 32 components (lanes) x 32 dimensions (or d_r < 32):
-//   pmu[h][c][k][d] = sum dL_k w_kd (x_d - mu_kd),
-//   ps [h][c][k][d] = sum dL_k (w_kd^2 (x_d - mu_kd)^2 - w_kd) / 2,
-//   pl [h][c][k]    = sum dL_k (from the first dimension block only).
-template <typename Tin>
 __global__ void __launch_bounds__(BT) bwd_param_partial_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
                                                                const float *__restrict__ dLq,
                                                                const float *__restrict__ dLk,
-                                                               const float *__restrict__ mu,
-                                                               const float *__restrict__ iv, float *__restrict__ pmu,
+                                                               const float *__restrict__ mu, float *__restrict__ pmu,
                                                                float *__restrict__ ps, float *__restrict__ pl, int B,
-                                                               int H, int N, int K, int d_r, int kchunks, int R)
+                                                               int H, int N, int K, int nseg, int R)
 {
     chain_enter();
-    __shared__ float red[BT / 32][32][33];
-    const int h = blockIdx.x, kc = blockIdx.y % kchunks, dc = blockIdx.y / kchunks, ch = blockIdx.z;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int k = kc * 32 + lane, d0 = dc * 32, dn = min(32, d_r - d0);
-    const bool kv = k < K;
-    const int kk = kv ? k : K - 1;
-    float m[32], w[32], amu[32], as[32];
+    extern __shared__ __align__(16) float sm[];
+    constexpr int NC = DR / 16;
+    float *sL = sm;                  // [SEG][KT] dL rows
+    float *sX = sL + SEG * KT;       // [SEG][DR] x rows
+    const int h = blockIdx.x, k0 = blockIdx.y * KT, ch = blockIdx.z;
+    const int kn = min(KT, K - k0);
+    const int t = threadIdx.x, r0 = orow();
+    float m[4][NC], a1[4][NC], a2[4][NC];
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
-        const bool ok = u < dn;
-        m[u] = ok ? mu[((size_t)h * K + kk) * d_r + d0 + u] : 0.f;
-        w[u] = ok ? iv[((size_t)h * K + kk) * d_r + d0 + u] : 0.f;
-        amu[u] = 0.f;
-        as[u] = 0.f;
-    }
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            m[r][c] = r0 + r < kn ? mu[((size_t)h * K + k0 + r0 + r) * DR + ocol<DR>(c)] : 0.f;
+            a1[r][c] = 0.f;
+            a2[r][c] = 0.f;
+        }
     float al = 0.f;
-    const long long per = (long long)B * N, rows = 2 * per;
-    const long long lo = rows * ch / R, hi = rows * (ch + 1) / R;
-    for (long long q = lo + warp; q < hi; q += BT / 32) {
-        const int side = q >= per;
-        const long long rem = side ? q - per : q;
-        const int b = (int)(rem / N), n = (int)(rem % N);
-        const long long row = ((long long)b * H + h) * N + n;
-        const Tin *X = side ? KX : QX;
-        const float a = kv ? (side ? dLk : dLq)[row * K + k] : 0.f;
-        al += a;
-        const float xl = lane < dn ? to_f32(X[row * d_r + d0 + lane]) : 0.f;
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const float xd = __shfl_sync(0xffffffffu, xl, u);
-            const float diff = xd - m[u], wd = w[u] * diff;
-            amu[u] = fmaf(a, wd, amu[u]);
-            as[u] = fmaf(a, 0.5f * (wd * wd - w[u]), as[u]);
-        }
-    }
-    for (int pass = 0; pass < 2; ++pass) {
-        const float *acc = pass == 0 ? amu : as;
-#pragma unroll
-        for (int u = 0; u < 32; ++u) red[warp][lane][u] = acc[u];
+    const int nb = 2 * B * nseg;
+    const int lo = (int)((long long)nb * ch / R), hi = (int)((long long)nb * (ch + 1) / R);
+    for (int b = lo; b < hi; ++b) {
+        const int side = b / (B * nseg), bb = (b / nseg) % B, seg = b % nseg;
+        const int n = min(SEG, N - seg * SEG);
+        const long long row0 = ((long long)bb * H + h) * N + seg * SEG;
         __syncthreads();
-        // thread t sums (component t / 32... ) in warp order
-        for (int e = threadIdx.x; e < 32 * 32; e += BT) {
-            const int l = e / 32, u = e % 32;
-            float s = 0.f;
+        stage<KT>(sL, KT, (side ? dLk : dLq) + row0 * K + k0, K, SEG, n, kn);
+        stage<DR>(sX, DR, (side ? KX : QX) + row0 * DR, DR, SEG, n, DR);
+        __syncthreads();
+#pragma unroll 2
+        for (int q = 0; q < SEG; ++q) {
+            const float4 a = *reinterpret_cast<const float4 *>(sL + q * KT + r0);
+            float xv[NC];
+            ld_cols<DR>(xv, sX + q * DR);
+            const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int wv = 0; wv < BT / 32; ++wv) s += red[wv][l][u];
-            const int kk2 = kc * 32 + l;
-            if (kk2 < K && u < dn) {
-                float *dst = pass == 0 ? pmu : ps;
-                dst[(((size_t)h * R + ch) * K + kk2) * d_r + d0 + u] = s;
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const float d = xv[c] - m[r][c];
+                    const float u = av[r] * d;
+                    a1[r][c] += u;
+                    a2[r][c] = fmaf(u, d, a2[r][c]);
+                }
+        }
+        if (t < KT)
+            for (int q = 0; q < SEG; ++q) al += sL[q * KT + t];
+    }
+    const size_t base = ((size_t)h * R + ch) * K;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int k = k0 + r0 + r;
+        if (r0 + r < kn)
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                pmu[(base + k) * DR + ocol<DR>(c)] = a1[r][c];
+                ps[(base + k) * DR + ocol<DR>(c)] = a2[r][c];
             }
-        }
-        __syncthreads();
     }
-    if (dc == 0) {
-        red[warp][lane][0] = al;
-        __syncthreads();
-        if (warp == 0) {
-            float s = 0.f;
-#pragma unroll
-            for (int wv = 0; wv < BT / 32; ++wv) s += red[wv][lane][0];
-            if (kv) pl[((size_t)h * R + ch) * K + k] = s;
-        }
-    }
+    if (t < kn) pl[base + k0 + t] = al;
 }
 
-// dmu, d(raw) = ds * sigmoid(raw), d(logits) = dlogpi - pi * sum(dlogpi): the chunks in order.
+// dmu = w sum pmu, d(raw) = (w^2 sum ps - w sum pl) / 2 * sigmoid(raw), over the chunks in order;
+// block y == 0 of each head also takes d(logits) = dlogpi - pi * sum(dlogpi).
 __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__restrict__ pmu, const float *__restrict__ ps,
-                                                             const float *__restrict__ pl, const float *__restrict__ raw,
+                                                             const float *__restrict__ pl, const float *__restrict__ iv,
+                                                             const float *__restrict__ raw,
                                                              const float *__restrict__ logits, float *__restrict__ dmu,
                                                              float *__restrict__ draw, float *__restrict__ dlogits,
                                                              int K, int d_r, int R)
@@ -427,16 +663,20 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
     __shared__ float red[BT / 32][2];
     const int h = blockIdx.x;
     const int KD = K * d_r;
-    for (int e = threadIdx.x; e < KD; e += BT) {
-        float a = 0.f, b = 0.f;
-        for (int c = 0; c < R; ++c) {
-            a += pmu[((size_t)h * R + c) * KD + e];
-            b += ps[((size_t)h * R + c) * KD + e];
+    const int e = blockIdx.y * BT + threadIdx.x;
+    if (e < KD) {
+        const int k = e / d_r;
+        float a = 0.f, b = 0.f, c = 0.f;
+        for (int ch = 0; ch < R; ++ch) {
+            a += pmu[((size_t)h * R + ch) * KD + e];
+            b += ps[((size_t)h * R + ch) * KD + e];
+            c += pl[((size_t)h * R + ch) * K + k];
         }
-        const float r = raw[(size_t)h * KD + e];
-        dmu[(size_t)h * KD + e] = a;
-        draw[(size_t)h * KD + e] = b / (1.f + expf(-r));
+        const float w = iv[(size_t)h * KD + e], r = raw[(size_t)h * KD + e];
+        dmu[(size_t)h * KD + e] = w * a;
+        draw[(size_t)h * KD + e] = 0.5f * (w * w * b - w * c) / (1.f + expf(-r));
     }
+    if (blockIdx.y != 0) return;
     // prior logits: pi = softmax(logits); dlogits = dlogpi - pi * sum_k dlogpi
     const float *lh = logits + (size_t)h * K;
     float m = -INFINITY, tl = 0.f;
@@ -451,7 +691,7 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
     for (int k = threadIdx.x; k < K; k += BT) {
         se += expf(lh[k] - m);
         float a = 0.f;
-        for (int c = 0; c < R; ++c) a += pl[((size_t)h * R + c) * K + k];
+        for (int ch = 0; ch < R; ++ch) a += pl[((size_t)h * R + ch) * K + k];
         tl += a;
     }
 #pragma unroll
@@ -473,15 +713,15 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
     }
     for (int k = threadIdx.x; k < K; k += BT) {
         float a = 0.f;
-        for (int c = 0; c < R; ++c) a += pl[((size_t)h * R + c) * K + k];
+        for (int ch = 0; ch < R; ++ch) a += pl[((size_t)h * R + ch) * K + k];
         const float pi = expf(lh[k] - m) / se;
         dlogits[(size_t)h * K + k] = a - pi * tl;
     }
 }
 
 struct BwdLayout {
-    size_t iv, cst, gq, gk, agg, dnd, dagg, dgq, dgk, pmu, ps, pl, total;
-    int nseg, R, kchunks, dchunks;
+    size_t iv, cst, gq, gk, agg, dnd, dagg, dgq, dgk, dotq, dotk, pmu, ps, pl, total;
+    int nseg, R, ktiles;
 };
 
 BwdLayout bwd_layout(const gma_shape_t &s)
@@ -491,13 +731,12 @@ BwdLayout bwd_layout(const gma_shape_t &s)
     const size_t T = (size_t)s.B * s.H * s.N;
     const int dv1 = s.d_v + 1;
     L.nseg = (s.N + SEG - 1) / SEG;
-    L.kchunks = (s.K + 31) / 32;
-    L.dchunks = (s.d_r + 31) / 32;
-    const long long rows = 2ll * s.B * s.N;
-    int R = (int)((2 * 152 + s.H * L.kchunks * L.dchunks - 1) / (s.H * L.kchunks * L.dchunks));
+    L.ktiles = (s.K + KT - 1) / KT;
+    // parameter partials: about three blocks per SM in all, at most one chunk per 64-row block
+    const int nb = 2 * s.B * L.nseg;
+    int R = (3 * 152 + s.H * L.ktiles - 1) / (s.H * L.ktiles);
+    if (R > nb) R = nb;
     if (R < 1) R = 1;
-    if (R > 64) R = 64;
-    if (R > rows / 64 + 1) R = (int)(rows / 64 + 1);
     L.R = R;
     L.iv = c.take(sizeof(float) * (size_t)s.H * s.K * s.d_r);
     L.cst = c.take(sizeof(float) * (size_t)s.H * s.K);
@@ -508,6 +747,8 @@ BwdLayout bwd_layout(const gma_shape_t &s)
     L.dagg = c.take(sizeof(float) * (size_t)s.B * s.H * L.nseg * s.K * dv1);
     L.dgq = c.take(sizeof(float) * T * s.K);
     L.dgk = c.take(sizeof(float) * T * s.K);
+    L.dotq = c.take(sizeof(float) * T);
+    L.dotk = c.take(sizeof(float) * T);
     L.pmu = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
     L.ps = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
     L.pl = c.take(sizeof(float) * (size_t)s.H * R * s.K);
@@ -515,20 +756,75 @@ BwdLayout bwd_layout(const gma_shape_t &s)
     return L;
 }
 
-template <typename Tin>
-gma_status_t launch_dx(int d_r, const Tin *X, const float *dL, const float *mu, const float *iv, Tin *dX, int H, int N,
-                       int K, long long rows, cudaStream_t st)
+template <typename... P>
+bool set_smem(void (*k)(P...), int floats)
 {
-    const unsigned blocks = (unsigned)((rows + BT - 1) / BT);
-    gma_status_t rr = GMA_OK;
-    switch (d_r) {
-    case 16: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<16, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
-    case 32: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<32, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
-    case 64: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<64, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
-    case 128: if ((rr = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<128, Tin>, dim3(blocks), dim3(BT), 0, X, dL, mu, iv, dX, H, N, K, rows)) != GMA_OK) return rr; break;
-    default: return GMA_ERR_UNSUPPORTED_SHAPE;
-    }
-    return GMA_OK;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, floats * (int)sizeof(float)) ==
+           cudaSuccess;
+}
+
+// The segment kernels for one value width.
+template <int DV, typename Tin>
+gma_status_t launch_segments(const gma_shape_t &s, const BwdLayout &L, bool causal, const Tin *V, const Tin *dO,
+                             Tin *dV, char *ws, cudaStream_t st)
+{
+    float *gq = (float *)(ws + L.gq), *gk = (float *)(ws + L.gk), *agg = (float *)(ws + L.agg);
+    float *dnd = (float *)(ws + L.dnd), *dagg = (float *)(ws + L.dagg);
+    float *dgq = (float *)(ws + L.dgq), *dgk = (float *)(ws + L.dgk);
+    float *dotq = (float *)(ws + L.dotq), *dotk = (float *)(ws + L.dotk);
+    const int BH = s.B * s.H, cz = causal ? 1 : 0;
+    const dim3 grid((unsigned)(BH * L.nseg));
+    if (!set_smem(bwd_numden_kernel<DV, Tin>, numden_smem_floats<DV>()) ||
+        !set_smem(bwd_dgq_kernel<DV, Tin>, dgq_smem_floats<DV>()) ||
+        !set_smem(bwd_dk_kernel<DV, Tin>, dk_smem_floats<DV>()))
+        return GMA_ERR_CUDA;
+    gma_status_t r = GMA_OK;
+    if ((r = launch_chained(KID_BWD_NUMDEN, st, bwd_numden_kernel<DV, Tin>, grid, dim3(BT),
+                            sizeof(float) * numden_smem_floats<DV>(), (const float *)gq, (const float *)gk, V,
+                            (const float *)agg, dO, dnd, dagg, s.N, s.K, L.nseg, s.eps, cz)) != GMA_OK)
+        return r;
+    if ((r = launch_chained(KID_BWD_DQ, st, bwd_dgq_kernel<DV, Tin>, grid, dim3(BT),
+                            sizeof(float) * dgq_smem_floats<DV>(), (const float *)gq, (const float *)gk, V,
+                            (const float *)agg, (const float *)dnd, dgq, dotq, s.N, s.K, L.nseg, cz)) != GMA_OK)
+        return r;
+    const int KD = s.K * (s.d_v + 1);
+    const long long tot = (long long)BH * KD;
+    if ((r = launch_chained(KID_BWD_SCAN, st, bwd_scan_kernel, dim3((unsigned)((tot + BT - 1) / BT)), dim3(BT), 0,
+                            dagg, tot, L.nseg, KD, cz)) != GMA_OK)
+        return r;
+    return launch_chained(KID_BWD_DK, st, bwd_dk_kernel<DV, Tin>, grid, dim3(BT), sizeof(float) * dk_smem_floats<DV>(),
+                          (const float *)gq, (const float *)gk, V, (const float *)dagg, (const float *)dnd, dgk, dotk,
+                          dV, s.N, s.K, L.nseg, cz);
+}
+
+// The kernels through the responsibilities for one routing width.
+template <int DR, typename Tin>
+gma_status_t launch_rows(const gma_shape_t &s, const BwdLayout &L, const Tin *QX, const Tin *KX, const float *mu,
+                         const float *raw, const float *logits, Tin *dQX, Tin *dKX, float *dmu, float *draw,
+                         float *dlogits, char *ws, cudaStream_t st)
+{
+    const float *iv = (const float *)(ws + L.iv);
+    const float *gq = (const float *)(ws + L.gq), *gk = (const float *)(ws + L.gk);
+    float *dgq = (float *)(ws + L.dgq), *dgk = (float *)(ws + L.dgk);
+    const float *dotq = (const float *)(ws + L.dotq), *dotk = (const float *)(ws + L.dotk);
+    float *pmu = (float *)(ws + L.pmu), *ps = (float *)(ws + L.ps), *pl = (float *)(ws + L.pl);
+    if (!set_smem(bwd_dx_kernel<DR, Tin>, dx_smem_floats<DR>()) ||
+        !set_smem(bwd_param_partial_kernel<DR, Tin>, param_smem_floats<DR>()))
+        return GMA_ERR_CUDA;
+    gma_status_t r = GMA_OK;
+    if ((r = launch_chained(KID_BWD_DX, st, bwd_dx_kernel<DR, Tin>, dim3((unsigned)(s.B * s.H * L.nseg), 2), dim3(BT),
+                            sizeof(float) * dx_smem_floats<DR>(), QX, KX, gq, gk, dgq, dgk, dotq, dotk, mu, iv, dQX,
+                            dKX, s.H, s.N, s.K, L.nseg)) != GMA_OK)
+        return r;
+    if ((r = launch_chained(KID_BWD_PARAMS, st, bwd_param_partial_kernel<DR, Tin>,
+                            dim3((unsigned)s.H, (unsigned)L.ktiles, (unsigned)L.R), dim3(BT),
+                            sizeof(float) * param_smem_floats<DR>(), QX, KX, (const float *)dgq, (const float *)dgk,
+                            mu, pmu, ps, pl, s.B, s.H, s.N, s.K, L.nseg, L.R)) != GMA_OK)
+        return r;
+    const int KD = s.K * s.d_r;
+    return launch_chained(KID_BWD_PFINAL, st, bwd_param_final_kernel, dim3((unsigned)s.H, (unsigned)((KD + BT - 1) / BT)),
+                          dim3(BT), 0, (const float *)pmu, (const float *)ps, (const float *)pl, iv, raw, logits, dmu,
+                          draw, dlogits, s.K, s.d_r, L.R);
 }
 
 template <typename Tin>
@@ -537,40 +833,24 @@ gma_status_t backward_typed(const gma_shape_t &s, bool causal, const Tin *QX, co
                             Tin *dV, float *dmu, float *draw, float *dlogits, char *ws, cudaStream_t st)
 {
     const BwdLayout L = bwd_layout(s);
-    float *iv = (float *)(ws + L.iv), *cst = (float *)(ws + L.cst);
-    float *gq = (float *)(ws + L.gq), *gk = (float *)(ws + L.gk), *agg = (float *)(ws + L.agg);
-    float *dnd = (float *)(ws + L.dnd), *dagg = (float *)(ws + L.dagg);
-    float *dgq = (float *)(ws + L.dgq), *dgk = (float *)(ws + L.dgk);
-    float *pmu = (float *)(ws + L.pmu), *ps = (float *)(ws + L.ps), *pl = (float *)(ws + L.pl);
-    gma_status_t r = simt_prepare(s, causal, QX, KX, V, mu, raw, logits, iv, cst, gq, gk, agg, st);
+    gma_status_t r = simt_prepare(s, causal, QX, KX, V, mu, raw, logits, (float *)(ws + L.iv), (float *)(ws + L.cst),
+                                  (float *)(ws + L.gq), (float *)(ws + L.gk), (float *)(ws + L.agg), st);
     if (r != GMA_OK) return r;
-    gma_status_t rr = GMA_OK;
-    const int BH = s.B * s.H, cz = causal ? 1 : 0;
-    const unsigned nblk = (unsigned)(BH * L.nseg);
-    const size_t smem = sizeof(float) * (size_t)seg_smem_floats(s.d_v);
-    if (cudaFuncSetAttribute(bwd_numden_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_dgq_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_dk_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return GMA_ERR_CUDA;
-    if ((rr = launch_chained(KID_BWD_NUMDEN, st, bwd_numden_kernel<Tin>, dim3(nblk), dim3(BT), smem, gq, gk, V, agg, dO, dnd, s.N, s.K, s.d_v, L.nseg, s.eps, cz)) != GMA_OK) return rr;
-    if ((rr = launch_chained(KID_BWD_DQ, st, bwd_dgq_kernel<Tin>, dim3(nblk), dim3(BT), smem, gk, V, agg, dnd, dgq, s.N, s.K, s.d_v, L.nseg, cz)) != GMA_OK) return rr;
-    dim3 gs(nblk, (unsigned)((s.K + KT - 1) / KT));
-    if ((rr = launch_chained(KID_BWD_SEG, st, bwd_seg_kernel, dim3(gs), dim3(BT), 0, gq, dnd, dagg, s.N, s.K, s.d_v, L.nseg)) != GMA_OK) return rr;
-    const int KD = s.K * (s.d_v + 1);
-    const long long tot = (long long)BH * KD;
-    if ((rr = launch_chained(KID_BWD_SCAN, st, bwd_scan_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, dagg, tot, L.nseg, KD, cz)) != GMA_OK) return rr;
-    if ((rr = launch_chained(KID_BWD_DK, st, bwd_dk_kernel<Tin>, dim3(nblk), dim3(BT), smem, gq, gk, V, dagg, dnd, dgk, dV, s.N, s.K, s.d_v, L.nseg, cz)) != GMA_OK) return rr;
-    const long long T = (long long)BH * s.N;
-    if ((rr = launch_chained(KID_BWD_SOFTMAX, st, bwd_softmax_kernel, dim3((unsigned)((T + 7) / 8)), dim3(BT), 0, gq, dgq, T, s.K)) != GMA_OK) return rr;
-    if ((rr = launch_chained(KID_BWD_SOFTMAX, st, bwd_softmax_kernel, dim3((unsigned)((T + 7) / 8)), dim3(BT), 0, gk, dgk, T, s.K)) != GMA_OK) return rr;
-    r = launch_dx<Tin>(s.d_r, QX, dgq, mu, iv, dQX, s.H, s.N, s.K, T, st);
+    switch (s.d_v) {
+    case 16: r = launch_segments<16, Tin>(s, L, causal, V, dO, dV, ws, st); break;
+    case 32: r = launch_segments<32, Tin>(s, L, causal, V, dO, dV, ws, st); break;
+    case 64: r = launch_segments<64, Tin>(s, L, causal, V, dO, dV, ws, st); break;
+    case 128: r = launch_segments<128, Tin>(s, L, causal, V, dO, dV, ws, st); break;
+    default: return GMA_ERR_UNSUPPORTED_SHAPE;
+    }
     if (r != GMA_OK) return r;
-    r = launch_dx<Tin>(s.d_r, KX, dgk, mu, iv, dKX, s.H, s.N, s.K, T, st);
-    if (r != GMA_OK) return r;
-    dim3 gp((unsigned)s.H, (unsigned)(L.kchunks * L.dchunks), (unsigned)L.R);
-    if ((rr = launch_chained(KID_BWD_PARAMS, st, bwd_param_partial_kernel<Tin>, dim3(gp), dim3(BT), 0, QX, KX, dgq, dgk, mu, iv, pmu, ps, pl, s.B, s.H, s.N, s.K, s.d_r, L.kchunks, L.R)) != GMA_OK) return rr;
-    if ((rr = launch_chained(KID_BWD_PFINAL, st, bwd_param_final_kernel, dim3((unsigned)s.H), dim3(BT), 0, pmu, ps, pl, raw, logits, dmu, draw, dlogits, s.K, s.d_r, L.R)) != GMA_OK) return rr;
-    return GMA_OK;
+    switch (s.d_r) {
+    case 16: return launch_rows<16, Tin>(s, L, QX, KX, mu, raw, logits, dQX, dKX, dmu, draw, dlogits, ws, st);
+    case 32: return launch_rows<32, Tin>(s, L, QX, KX, mu, raw, logits, dQX, dKX, dmu, draw, dlogits, ws, st);
+    case 64: return launch_rows<64, Tin>(s, L, QX, KX, mu, raw, logits, dQX, dKX, dmu, draw, dlogits, ws, st);
+    case 128: return launch_rows<128, Tin>(s, L, QX, KX, mu, raw, logits, dQX, dKX, dmu, draw, dlogits, ws, st);
+    default: return GMA_ERR_UNSUPPORTED_SHAPE;
+    }
 }
 
 }  // namespace

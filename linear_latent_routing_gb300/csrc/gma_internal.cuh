@@ -67,8 +67,7 @@ enum KernelId {
     KID_SIMT_PARAMS = 1, KID_SIMT_RESP, KID_SIMT_STATE, KID_SIMT_SCAN, KID_SIMT_OUT, KID_SIMT_SMALL,
     KID_TC_PARAMS = 16, KID_TC_RESP, KID_TC_BIDIR_WRITE, KID_TC_BIDIR_READ, KID_TC_CAUSAL_AGG,
     KID_TC_CAUSAL_SCAN, KID_TC_CAUSAL_OUT, KID_TC_LSE, KID_TC_DIVIDE, KID_TC_CAUSAL_FUSED, KID_DECODE = 32, KID_DECODE_PARAMS, KID_USAGE_ROWS, KID_USAGE_MASS, KID_USAGE_STATS, KID_BWD_NUMDEN,
-    KID_BWD_DQ, KID_BWD_SEG, KID_BWD_SCAN, KID_BWD_DK, KID_BWD_SOFTMAX, KID_BWD_DX, KID_BWD_PARAMS,
-    KID_BWD_PFINAL, KID_COUNT
+    KID_BWD_DQ, KID_BWD_SCAN, KID_BWD_DK, KID_BWD_DX, KID_BWD_PARAMS, KID_BWD_PFINAL, KID_COUNT
 };
 const char *kernel_name(int id);
 void timing_begin(cudaStream_t st, int kernel_id);

@@ -53,10 +53,8 @@ const char *kernel_name(int id)
     case KID_USAGE_STATS: return "usage_stats";
     case KID_BWD_NUMDEN: return "bwd_numden";
     case KID_BWD_DQ: return "bwd_dgamma_q";
-    case KID_BWD_SEG: return "bwd_segment_memory";
     case KID_BWD_SCAN: return "bwd_segment_scan";
     case KID_BWD_DK: return "bwd_dgamma_k_dv";
-    case KID_BWD_SOFTMAX: return "bwd_softmax";
     case KID_BWD_DX: return "bwd_dx";
     case KID_BWD_PARAMS: return "bwd_param_partials";
     case KID_BWD_PFINAL: return "bwd_param_final";
