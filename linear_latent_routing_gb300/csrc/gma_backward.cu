@@ -23,6 +23,7 @@
 // contracts over keys, for instance), so no result is transposed in memory.  All sums run in a
 // fixed order (no atomics): repeated calls give identical bits.
 #include "gma_internal.cuh"
+#include "simt_tile.cuh"
 #include "tc_ptx.cuh"
 
 namespace gma {
@@ -47,104 +48,7 @@ gma_status_t launch_chained(int kid, cudaStream_t st, void (*k)(P...), dim3 g, d
 
 constexpr int SEG = 64;   // tokens per segment (the forward preparation's split)
 constexpr int KT = 64;    // components per tile
-constexpr int BT = 256;   // threads per block
-constexpr int LT = 68;    // row stride of a transposed tile 64 wide (a multiple of 4 for 16-byte
-                          // loads, not of 8, which spreads its column-wise writes over the banks)
-
-// The thread's first output row and its c-th output column in an output W columns wide: groups
-// of four contiguous columns (two groups 64 apart at W = 128), narrower strips below 64.
-__device__ __forceinline__ int orow() { return (threadIdx.x >> 4) * 4; }
-template <int W>
-__device__ __forceinline__ int ocol(int c)
-{
-    const int tx = threadIdx.x & 15;
-    if constexpr (W == 128) return (c >> 2) * 64 + tx * 4 + (c & 3);
-    else return tx * (W / 16) + c;
-}
-
-// The thread's W / 16 columns of one staged row.
-template <int W>
-__device__ __forceinline__ void ld_cols(float (&b)[W / 16], const float *row)
-{
-    const int tx = threadIdx.x & 15;
-    if constexpr (W == 16) {
-        b[0] = row[tx];
-    } else if constexpr (W == 32) {
-        const float2 v = *reinterpret_cast<const float2 *>(row + 2 * tx);
-        b[0] = v.x;
-        b[1] = v.y;
-    } else {
-#pragma unroll
-        for (int g = 0; g < W / 64; ++g) {
-            const float4 v = *reinterpret_cast<const float4 *>(row + 64 * g + 4 * tx);
-            b[4 * g] = v.x;
-            b[4 * g + 1] = v.y;
-            b[4 * g + 2] = v.z;
-            b[4 * g + 3] = v.w;
-        }
-    }
-}
-
-// acc[r][c] += sum_{q < nq} At[q][orow() + r] * Bt[q][ocol<W>(c)]: both operands in shared memory
-// with the contracted index as their row (row strides lda, ldb floats, multiples of 4).
-template <int W>
-__device__ __forceinline__ void mac(float (&acc)[4][W / 16], const float *At, int lda, const float *Bt, int ldb,
-                                    int nq)
-{
-    const int r0 = orow();
-#pragma unroll 4
-    for (int q = 0; q < nq; ++q) {
-        const float4 a = *reinterpret_cast<const float4 *>(At + q * lda + r0);
-        float b[W / 16];
-        ld_cols<W>(b, Bt + q * ldb);
-#pragma unroll
-        for (int c = 0; c < W / 16; ++c) {
-            acc[0][c] = fmaf(a.x, b[c], acc[0][c]);
-            acc[1][c] = fmaf(a.y, b[c], acc[1][c]);
-            acc[2][c] = fmaf(a.z, b[c], acc[2][c]);
-            acc[3][c] = fmaf(a.w, b[c], acc[3][c]);
-        }
-    }
-}
-
-template <int W>
-__device__ __forceinline__ void zero(float (&acc)[4][W / 16])
-{
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < W / 16; ++c) acc[r][c] = 0.f;
-}
-
-// dst[r][c] = src[r * sld + c] for r < R, c < C (zero where r >= nr or c >= nc; those elements of
-// src are not read); dst has row stride ld.  Lanes run along c: coalesced reads, conflict-free
-// writes.
-template <int C, typename T>
-__device__ __forceinline__ void stage(float *dst, int ld, const T *src, long long sld, int R, int nr, int nc)
-{
-    for (int e = threadIdx.x; e < R * C; e += BT) {
-        const int r = e / C, c = e % C;
-        dst[r * ld + c] = (r < nr && c < nc) ? to_f32(src[(long long)r * sld + c]) : 0.f;
-    }
-}
-
-// The transpose: dst[c][r] = src[r * sld + c], dst with row stride ld.
-template <int C, typename T>
-__device__ __forceinline__ void stage_t(float *dst, int ld, const T *src, long long sld, int R, int nr, int nc)
-{
-    for (int e = threadIdx.x; e < R * C; e += BT) {
-        const int r = e / C, c = e % C;
-        dst[c * ld + r] = (r < nr && c < nc) ? to_f32(src[(long long)r * sld + c]) : 0.f;
-    }
-}
-
-// Sum over the 16 threads that share a row of the output grid (lanes xor 1, 2, 4, 8 of a warp).
-__device__ __forceinline__ float row_sum16(float v)
-{
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+using namespace tile;
 
 // ---------------------------------------------------------------- query side, per segment
 // num = Gamma_Q S + tril(P) V and den = Gamma_Q Z + tril(P) 1 + eps for the query rows of one
@@ -156,7 +60,7 @@ template <int DV>
 __host__ __device__ constexpr int numden_smem_floats() { return 2 * KT * LT + KT * DV + KT + 2 * SEG; }
 
 template <int DV, typename Tin>
-__global__ void __launch_bounds__(BT) bwd_numden_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
+__global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_numden_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                         const Tin *__restrict__ V, const float *__restrict__ agg,
                                                         const Tin *__restrict__ dO, float *__restrict__ dnd,
                                                         float *__restrict__ dagg, int N, int K, int nseg, float eps,
@@ -183,9 +87,9 @@ __global__ void __launch_bounds__(BT) bwd_numden_kernel(const float *__restrict_
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        stage_t<KT>(gqT, LT, gq + row0 * K + k0, K, SEG, n, kn);
-        if (causal) stage_t<KT>(gkT, LT, gk + row0 * K + k0, K, SEG, n, kn);
-        stage<DV>(sS, DV, S + (size_t)k0 * DV1, DV1, KT, kn, DV);
+        stage_t<KT>(gqT, LT, gq + row0 * K + k0, K, n, kn);
+        if (causal) stage_t<KT>(gkT, LT, gk + row0 * K + k0, K, n, kn);
+        stage<DV>(sS, DV, S + (size_t)k0 * DV1, DV1, kn, DV);
         if (t < KT) zS[t] = t < kn ? S[(size_t)(k0 + t) * DV1 + DV] : 0.f;
         __syncthreads();
         if (causal) mac<64>(accP, gkT, LT, gqT, LT, KT);   // P^T: rows j, columns i
@@ -205,9 +109,9 @@ __global__ void __launch_bounds__(BT) bwd_numden_kernel(const float *__restrict_
                 const int j = r0 + r, i = ocol<64>(c);
                 gkT[j * LT + i] = i >= j ? accP[r][c] : 0.f;
             }
-        stage<DV>(sS, DV, V + row0 * DV, DV, SEG, n, DV);
+        stage<DV>(sS, DV, V + row0 * DV, DV, n, DV);
         __syncthreads();
-        mac<DV>(accN, gkT, LT, sS, DV, SEG);
+        mac_range<DV>(accN, gkT, LT, sS, DV, 0, r0 + 4);   // (P^T[j][i] = 0 for j > i)
         if (t < SEG) {
             float a = 0.f;
             for (int j = 0; j < SEG; ++j) a += gkT[j * LT + t];
@@ -216,26 +120,32 @@ __global__ void __launch_bounds__(BT) bwd_numden_kernel(const float *__restrict_
     }
     if (t < SEG) den[t] = dpart + eps;
     __syncthreads();
-    // dnum over num, then dden: the rows' dot products are summed over the 16 threads of a row
+    // dnum over num, then dden (the rows' dot products summed over the 16 threads of each row)
+    float dot[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int i = r0 + r;
         const float dn = den[i];
-        float dot = 0.f;
+        dot[r] = 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             const float o = i < n ? to_f32(dO[(row0 + i) * DV + ocol<DV>(c)]) : 0.f;
-            dot = fmaf(o, accN[r][c], dot);
+            dot[r] = fmaf(o, accN[r][c], dot[r]);
             accN[r][c] = o / dn;
         }
-        dot = row_sum16(dot);
-        const float ddi = i < n ? -dot / (dn * dn) : 0.f;
+    }
+    row_sums(dot);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = r0 + r;
+        const float dn = den[i];
+        const float ddi = i < n ? -dot[r] / (dn * dn) : 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             if (i < n) dnd[(row0 + i) * DV1 + ocol<DV>(c)] = accN[r][c];
             sS[i * DV + ocol<DV>(c)] = accN[r][c];
         }
-        if ((t & 15) == 0) {
+        if (tile_tx() == 0) {
             if (i < n) dnd[(row0 + i) * DV1 + DV] = ddi;
             dd[i] = ddi;
         }
@@ -245,7 +155,7 @@ __global__ void __launch_bounds__(BT) bwd_numden_kernel(const float *__restrict_
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        stage<KT>(gqT, KT, gq + row0 * K + k0, K, SEG, n, kn);
+        stage<KT>(gqT, KT, gq + row0 * K + k0, K, n, kn);
         __syncthreads();
         float accG[4][NC];
         zero<DV>(accG);
@@ -272,7 +182,7 @@ template <int DV>
 __host__ __device__ constexpr int dgq_smem_floats() { return 2 * DV * LT + SEG * LT + SEG * KT + KT + SEG; }
 
 template <int DV, typename Tin>
-__global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
+__global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dgq_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                      const Tin *__restrict__ V, const float *__restrict__ agg,
                                                      const float *__restrict__ dnd, float *__restrict__ dgq,
                                                      float *__restrict__ dotq, int N, int K, int nseg, int causal)
@@ -291,10 +201,10 @@ __global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ g
     const long long row0 = (long long)bh * N + i0;
     const float *S = agg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * DV1;
     const int t = threadIdx.x, r0 = orow();
-    stage_t<DV>(dnT, LT, dnd + row0 * DV1, DV1, SEG, n, DV);
+    stage_t<DV>(dnT, LT, dnd + row0 * DV1, DV1, n, DV);
     if (t < SEG) dd[t] = t < n ? dnd[(row0 + t) * DV1 + DV] : 0.f;
     if (causal) {
-        stage_t<DV>(VT, LT, V + row0 * DV, DV, SEG, n, DV);
+        stage_t<DV>(VT, LT, V + row0 * DV, DV, n, DV);
         __syncthreads();
         float accA[4][4];
         zero<64>(accA);
@@ -307,18 +217,18 @@ __global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ g
                 AT[j * LT + i] = i >= j ? accA[r][c] + dd[i] : 0.f;
             }
     }
-    float dot[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool one = K <= KT;
+    float dot[4] = {0.f, 0.f, 0.f, 0.f}, gsv[4][4], acc[4][4];
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        stage_t<DV>(VT, LT, S + (size_t)k0 * DV1, DV1, KT, kn, DV);   // S^T: [c][k]
+        stage_t<DV>(VT, LT, S + (size_t)k0 * DV1, DV1, kn, DV);   // S^T: [c][k]
         if (t < KT) zS[t] = t < kn ? S[(size_t)(k0 + t) * DV1 + DV] : 0.f;
-        if (causal) stage<KT>(gK, KT, gk + row0 * K + k0, K, SEG, n, kn);
+        if (causal) stage<KT>(gK, KT, gk + row0 * K + k0, K, n, kn);
         __syncthreads();
-        float acc[4][4];
         zero<64>(acc);
         mac<64>(acc, dnT, LT, VT, LT, DV);                  // rows i, columns k
-        if (causal) mac<64>(acc, AT, LT, gK, KT, SEG);
+        if (causal) mac_range<64>(acc, AT, LT, gK, KT, 0, r0 + 4);   // (A^T[j][i] = 0 for j > i)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = r0 + r;
@@ -326,24 +236,35 @@ __global__ void __launch_bounds__(BT) bwd_dgq_kernel(const float *__restrict__ g
             for (int c = 0; c < 4; ++c) {
                 const int kk = ocol<64>(c), k = k0 + kk;
                 const float v = fmaf(dd[i], zS[kk], acc[r][c]);
-                if (i < n && k < K) {
-                    dgq[(row0 + i) * K + k] = v;
-                    dot[r] = fmaf(gq[(row0 + i) * K + k], v, dot[r]);
-                }
+                gsv[r][c] = i < n && k < K ? gq[(row0 + i) * K + k] : 0.f;
+                dot[r] = fmaf(gsv[r][c], v, dot[r]);
+                acc[r][c] = v;
+                if (!one && i < n && k < K) dgq[(row0 + i) * K + k] = v;
             }
         }
     }
+    row_sums(dot);
+    // one tile: the row's dGamma is all here, so dL = Gamma (dGamma - <Gamma, dGamma>) is written
+    // in its place; otherwise the kernel through the responsibilities forms it from dot
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const float s = row_sum16(dot[r]);
-        if ((t & 15) == 0 && r0 + r < n) dotq[row0 + r0 + r] = s;
+        const int i = r0 + r;
+        if (one) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int k = ocol<64>(c);
+                if (i < n && k < K) dgq[(row0 + i) * K + k] = gsv[r][c] * (acc[r][c] - dot[r]);
+            }
+        } else if (tile_tx() == 0 && i < n) {
+            dotq[row0 + i] = dot[r];
+        }
     }
 }
 
 // Causal: each segment's partial becomes the exclusive suffix over later segments (what the
 // keys of the segment see from queries after it).  Bidirectional: the total into segment 0.
-// One thread per element of the K x (d_v + 1) memory; the loads of eight segments are issued
-// before their sums, so a thread waits once per eight segments.
+// One thread per element of the K x (d_v + 1) memory; the loads of 32 segments are issued before
+// their sums, so a thread waits once per 32 segments.
 __global__ void __launch_bounds__(BT) bwd_scan_kernel(float *__restrict__ dagg, long long total, int nseg, int KD,
                                                       int causal)
 {
@@ -353,12 +274,12 @@ __global__ void __launch_bounds__(BT) bwd_scan_kernel(float *__restrict__ dagg, 
     const long long bh = idx / KD, e = idx % KD;
     float *base = dagg + bh * nseg * KD + e;
     float run = 0.f;
-    for (int s1 = nseg; s1 > 0; s1 -= 8) {
-        float a[8];
+    for (int s1 = nseg; s1 > 0; s1 -= 32) {
+        float a[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) a[u] = s1 - 1 - u >= 0 ? base[(size_t)(s1 - 1 - u) * KD] : 0.f;
+        for (int u = 0; u < 32; ++u) a[u] = s1 - 1 - u >= 0 ? base[(size_t)(s1 - 1 - u) * KD] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 32; ++u) {
             if (s1 - 1 - u < 0) break;
             if (causal) base[(size_t)(s1 - 1 - u) * KD] = run;
             run += a[u];
@@ -377,7 +298,7 @@ template <int DV>
 __host__ __device__ constexpr int dk_smem_floats() { return 2 * KT * LT + 2 * DV * LT + KT + SEG; }
 
 template <int DV, typename Tin>
-__global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
+__global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dk_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                     const Tin *__restrict__ V, const float *__restrict__ dagg,
                                                     const float *__restrict__ dnd, float *__restrict__ dgk,
                                                     float *__restrict__ dotk, Tin *__restrict__ dV, int N, int K,
@@ -405,9 +326,9 @@ __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        if (causal) stage_t<KT>(gqT, LT, gq + row0 * K + k0, K, SEG, n, kn);
-        stage_t<KT>(gkT, LT, gk + row0 * K + k0, K, SEG, n, kn);
-        stage<DV>(sD, DV, D + (size_t)k0 * DV1, DV1, KT, kn, DV);
+        if (causal) stage_t<KT>(gqT, LT, gq + row0 * K + k0, K, n, kn);
+        stage_t<KT>(gkT, LT, gk + row0 * K + k0, K, n, kn);
+        stage<DV>(sD, DV, D + (size_t)k0 * DV1, DV1, kn, DV);
         __syncthreads();
         if (causal) mac<64>(accP, gqT, LT, gkT, LT, KT);   // P: rows i, columns j
         mac<DV>(accV, gkT, LT, sD, DV, KT);                // rows j, columns c
@@ -421,9 +342,9 @@ __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq
                 const int i = r0 + r, j = ocol<64>(c);
                 gqT[i * LT + j] = i >= j ? accP[r][c] : 0.f;
             }
-        stage<DV>(sD, DV, dnd + row0 * DV1, DV1, SEG, n, DV);
+        stage<DV>(sD, DV, dnd + row0 * DV1, DV1, n, DV);
         __syncthreads();
-        mac<DV>(accV, gqT, LT, sD, DV, SEG);   // sum_i P[i][j] dnum_i
+        mac_range<DV>(accV, gqT, LT, sD, DV, r0, SEG);   // sum_{i >= j} P[i][j] dnum_i
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -434,9 +355,9 @@ __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq
     }
     // dGamma_K
     __syncthreads();
-    stage_t<DV>(VT, LT, V + row0 * DV, DV, SEG, n, DV);
+    stage_t<DV>(VT, LT, V + row0 * DV, DV, n, DV);
     if (causal) {
-        stage_t<DV>(DT, LT, dnd + row0 * DV1, DV1, SEG, n, DV);
+        stage_t<DV>(DT, LT, dnd + row0 * DV1, DV1, n, DV);
         if (t < SEG) dd[t] = t < n ? dnd[(row0 + t) * DV1 + DV] : 0.f;
         __syncthreads();
         float accA[4][4];
@@ -450,18 +371,18 @@ __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq
                 gqT[i * LT + j] = i >= j ? accA[r][c] + dd[i] : 0.f;
             }
     }
-    float dot[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool one = K <= KT;
+    float dot[4] = {0.f, 0.f, 0.f, 0.f}, gsv[4][4], acc[4][4];
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        stage_t<DV>(DT, LT, D + (size_t)k0 * DV1, DV1, KT, kn, DV);   // D^T: [c][k]
+        stage_t<DV>(DT, LT, D + (size_t)k0 * DV1, DV1, kn, DV);   // D^T: [c][k]
         if (t < KT) zD[t] = t < kn ? D[(size_t)(k0 + t) * DV1 + DV] : 0.f;
-        if (causal) stage<KT>(gkT, KT, gq + row0 * K + k0, K, SEG, n, kn);
+        if (causal) stage<KT>(gkT, KT, gq + row0 * K + k0, K, n, kn);
         __syncthreads();
-        float acc[4][4];
         zero<64>(acc);
         mac<64>(acc, VT, LT, DT, LT, DV);                 // rows j, columns k
-        if (causal) mac<64>(acc, gqT, LT, gkT, KT, SEG);
+        if (causal) mac_range<64>(acc, gqT, LT, gkT, KT, r0, SEG);   // (A[i][j] = 0 for i < j)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int j = r0 + r;
@@ -469,23 +390,33 @@ __global__ void __launch_bounds__(BT) bwd_dk_kernel(const float *__restrict__ gq
             for (int c = 0; c < 4; ++c) {
                 const int kk = ocol<64>(c), k = k0 + kk;
                 const float v = acc[r][c] + zD[kk];
-                if (j < n && k < K) {
-                    dgk[(row0 + j) * K + k] = v;
-                    dot[r] = fmaf(gk[(row0 + j) * K + k], v, dot[r]);
-                }
+                gsv[r][c] = j < n && k < K ? gk[(row0 + j) * K + k] : 0.f;
+                dot[r] = fmaf(gsv[r][c], v, dot[r]);
+                acc[r][c] = v;
+                if (!one && j < n && k < K) dgk[(row0 + j) * K + k] = v;
             }
         }
     }
+    row_sums(dot);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const float s = row_sum16(dot[r]);
-        if ((t & 15) == 0 && r0 + r < n) dotk[row0 + r0 + r] = s;
+        const int j = r0 + r;
+        if (one) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int k = ocol<64>(c);
+                if (j < n && k < K) dgk[(row0 + j) * K + k] = gsv[r][c] * (acc[r][c] - dot[r]);
+            }
+        } else if (tile_tx() == 0 && j < n) {
+            dotk[row0 + j] = dot[r];
+        }
     }
 }
 
 // ---------------------------------------------------------------- through the responsibilities
 // The rows of one segment of one side (blockIdx.y: 0 queries, 1 keys):
-//   dL = Gamma (dGamma - <Gamma, dGamma>)     (written back over dGamma for the parameters)
+//   dL = Gamma (dGamma - <Gamma, dGamma>)     (written back over dGamma for the parameters; with
+//                                             one component tile the kernels before formed it)
 //   dx_d = sum_k dL_k (w_kd mu_kd - w_kd x_d)  (w = 1 / sigma^2)
 // The contraction over k runs as the products above, with the factor w_kd mu_kd - w_kd x_d formed
 // per step from the thread's own x (two FMAs per term).
@@ -493,7 +424,7 @@ template <int DR>
 __host__ __device__ constexpr int dx_smem_floats() { return KT * LT + 2 * KT * DR + SEG; }
 
 template <int DR, typename Tin>
-__global__ void __launch_bounds__(BT) bwd_dx_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
+__global__ void __launch_bounds__(BT, 2) bwd_dx_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
                                                     const float *__restrict__ gq, const float *__restrict__ gk,
                                                     float *__restrict__ dgq, float *__restrict__ dgk,
                                                     const float *__restrict__ dotq, const float *__restrict__ dotk,
@@ -517,7 +448,8 @@ __global__ void __launch_bounds__(BT) bwd_dx_kernel(const Tin *__restrict__ QX, 
     const int i0 = seg * SEG, n = min(SEG, N - i0);
     const long long row0 = (long long)bh * N + i0;
     const int t = threadIdx.x, r0 = orow();
-    if (t < SEG) sdot[t] = t < n ? (side ? dotk : dotq)[row0 + t] : 0.f;
+    const bool one = K <= KT;   // (one component tile: dGamma already holds dL)
+    if (t < SEG) sdot[t] = t < n && !one ? (side ? dotk : dotq)[row0 + t] : 0.f;
     float x[4][NC], acc[4][NC];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -530,23 +462,29 @@ __global__ void __launch_bounds__(BT) bwd_dx_kernel(const Tin *__restrict__ QX, 
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        for (int e = t; e < SEG * KT; e += BT) {
-            const int r = e / KT, kk = e % KT;
-            float v = 0.f;
-            if (r < n && kk < kn) {
-                const long long o = (row0 + r) * K + k0 + kk;
-                v = g[o] * (dg[o] - sdot[r]);
-                dg[o] = v;
-            }
-            dLT[kk * LT + r] = v;
+        // the tile's Gamma and dGamma first (16 of each per thread in flight), then dL; a thread
+        // keeps component kk and takes rows rb, rb + 4, ...
+        constexpr int PER = SEG * KT / BT;
+        const int kk = t % KT, rb = t / KT;
+        const bool kok = kk < kn;
+        const long long o0 = (row0 + rb) * K + k0 + kk;
+        float gv[PER], dv[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const bool ok = kok && rb + 4 * u < n;
+            gv[u] = ok && !one ? g[o0 + (long long)u * 4 * K] : 0.f;
+            dv[u] = ok ? dg[o0 + (long long)u * 4 * K] : 0.f;
         }
-        for (int e = t; e < KT * DR; e += BT) {
-            const int kk = e / DR, d = e % DR;
-            const float w = kk < kn ? ivh[(size_t)(k0 + kk) * DR + d] : 0.f;
-            const float m = kk < kn ? muh[(size_t)(k0 + kk) * DR + d] : 0.f;
-            sW[e] = w;
-            sWM[e] = w * m;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const float v = one ? dv[u] : gv[u] * (dv[u] - sdot[rb + 4 * u]);
+            if (!one && kok && rb + 4 * u < n) dg[o0 + (long long)u * 4 * K] = v;
+            dLT[kk * LT + rb + 4 * u] = v;
         }
+        stage<DR>(sW, DR, ivh + (size_t)k0 * DR, DR, kn, DR);
+        stage<DR>(sWM, DR, muh + (size_t)k0 * DR, DR, kn, DR);
+        __syncthreads();
+        for (int e = t; e < KT * DR; e += BT) sWM[e] *= sW[e];   // w mu
         __syncthreads();
 #pragma unroll 2
         for (int q = 0; q < KT; ++q) {
@@ -573,21 +511,19 @@ __global__ void __launch_bounds__(BT) bwd_dx_kernel(const Tin *__restrict__ QX, 
 // ---------------------------------------------------------------- parameter gradients
 // Partial sums of head h over a range of 64-row blocks (query rows, then key rows; block b is side
 // b / (B nseg), batch row (b / nseg) % B, segment b % nseg) for the components of one tile:
-//   pmu[h][ch][k][d] = sum dL_k (x_d - mu_kd),  ps[h][ch][k][d] = sum dL_k (x_d - mu_kd)^2,
-//   pl[h][ch][k] = sum dL_k
-// (the factors w_kd, w_kd^2 / 2 and -w_kd / 2 are applied once, in the final kernel).  Each thread
-// keeps mu of its 4 components x (d_r / 16) dimensions in registers; per row and term: one
-// subtraction, one product and two additions.
+//   m1[h][ch][k][d] = sum dL_k x_d,  m2[h][ch][k][d] = sum dL_k x_d^2,  pl[h][ch][k] = sum dL_k,
+// two FMAs per term (x^2 formed once per row and column); the final kernel turns them into
+// sum dL_k (x_d - mu_kd) = m1 - mu pl and sum dL_k (x_d - mu_kd)^2 = m2 - 2 mu m1 + mu^2 pl.
 template <int DR>
 __host__ __device__ constexpr int param_smem_floats() { return SEG * KT + SEG * DR; }
 
 template <int DR, typename Tin>
-__global__ void __launch_bounds__(BT) bwd_param_partial_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
-                                                               const float *__restrict__ dLq,
-                                                               const float *__restrict__ dLk,
-                                                               const float *__restrict__ mu, float *__restrict__ pmu,
-                                                               float *__restrict__ ps, float *__restrict__ pl, int B,
-                                                               int H, int N, int K, int nseg, int R)
+__global__ void __launch_bounds__(BT, 2) bwd_param_partial_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
+                                                                  const float *__restrict__ dLq,
+                                                                  const float *__restrict__ dLk,
+                                                                  float *__restrict__ m1, float *__restrict__ m2,
+                                                                  float *__restrict__ pl, int B, int H, int N, int K,
+                                                                  int nseg, int R)
 {
     chain_enter();
     extern __shared__ __align__(16) float sm[];
@@ -597,41 +533,48 @@ __global__ void __launch_bounds__(BT) bwd_param_partial_kernel(const Tin *__rest
     const int h = blockIdx.x, k0 = blockIdx.y * KT, ch = blockIdx.z;
     const int kn = min(KT, K - k0);
     const int t = threadIdx.x, r0 = orow();
-    float m[4][NC], a1[4][NC], a2[4][NC];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            m[r][c] = r0 + r < kn ? mu[((size_t)h * K + k0 + r0 + r) * DR + ocol<DR>(c)] : 0.f;
-            a1[r][c] = 0.f;
-            a2[r][c] = 0.f;
-        }
+    float a1[4][NC], a2[4][NC];
+    zero<DR>(a1);
+    zero<DR>(a2);
     float al = 0.f;
     const int nb = 2 * B * nseg;
     const int lo = (int)((long long)nb * ch / R), hi = (int)((long long)nb * (ch + 1) / R);
-    for (int b = lo; b < hi; ++b) {
+    // block b's dL and x rows; the loads of block b + 1 are issued before block b's products
+    Staged<KT> nL;
+    Staged<DR> nX;
+    auto load = [&](int b) {
         const int side = b / (B * nseg), bb = (b / nseg) % B, seg = b % nseg;
         const int n = min(SEG, N - seg * SEG);
         const long long row0 = ((long long)bb * H + h) * N + seg * SEG;
+        stage_load<KT>(nL, (side ? dLk : dLq) + row0 * K + k0, K, n, kn);
+        stage_load<DR>(nX, (side ? KX : QX) + row0 * DR, DR, n, DR);
+    };
+    constexpr bool PREFETCH = DR <= 64;   // (at d_r = 128 the accumulators leave no registers for it)
+    if (PREFETCH && lo < hi) load(lo);
+    for (int b = lo; b < hi; ++b) {
         __syncthreads();
-        stage<KT>(sL, KT, (side ? dLk : dLq) + row0 * K + k0, K, SEG, n, kn);
-        stage<DR>(sX, DR, (side ? KX : QX) + row0 * DR, DR, SEG, n, DR);
+        if (!PREFETCH) load(b);
+        stage_store<KT>(sL, KT, nL);
+        stage_store<DR>(sX, DR, nX);
         __syncthreads();
-#pragma unroll 2
+        if (PREFETCH && b + 1 < hi) load(b + 1);
+#pragma unroll 4
         for (int q = 0; q < SEG; ++q) {
             const float4 a = *reinterpret_cast<const float4 *>(sL + q * KT + r0);
             float xv[NC];
             ld_cols<DR>(xv, sX + q * DR);
-            const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const float d = xv[c] - m[r][c];
-                    const float u = av[r] * d;
-                    a1[r][c] += u;
-                    a2[r][c] = fmaf(u, d, a2[r][c]);
-                }
+            for (int c = 0; c < NC; ++c) {
+                const float x2 = xv[c] * xv[c];
+                a1[0][c] = fmaf(a.x, xv[c], a1[0][c]);
+                a1[1][c] = fmaf(a.y, xv[c], a1[1][c]);
+                a1[2][c] = fmaf(a.z, xv[c], a1[2][c]);
+                a1[3][c] = fmaf(a.w, xv[c], a1[3][c]);
+                a2[0][c] = fmaf(a.x, x2, a2[0][c]);
+                a2[1][c] = fmaf(a.y, x2, a2[1][c]);
+                a2[2][c] = fmaf(a.z, x2, a2[2][c]);
+                a2[3][c] = fmaf(a.w, x2, a2[3][c]);
+            }
         }
         if (t < KT)
             for (int q = 0; q < SEG; ++q) al += sL[q * KT + t];
@@ -643,18 +586,20 @@ __global__ void __launch_bounds__(BT) bwd_param_partial_kernel(const Tin *__rest
         if (r0 + r < kn)
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                pmu[(base + k) * DR + ocol<DR>(c)] = a1[r][c];
-                ps[(base + k) * DR + ocol<DR>(c)] = a2[r][c];
+                m1[(base + k) * DR + ocol<DR>(c)] = a1[r][c];
+                m2[(base + k) * DR + ocol<DR>(c)] = a2[r][c];
             }
     }
     if (t < kn) pl[base + k0 + t] = al;
 }
 
-// dmu = w sum pmu, d(raw) = (w^2 sum ps - w sum pl) / 2 * sigmoid(raw), over the chunks in order;
-// block y == 0 of each head also takes d(logits) = dlogpi - pi * sum(dlogpi).
-__global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__restrict__ pmu, const float *__restrict__ ps,
+// Over the chunks in order, a1 = sum dL_k x_d, a2 = sum dL_k x_d^2, c = sum dL_k; then
+//   dmu = w (a1 - mu c),  d(raw) = (w^2 (a2 - 2 mu a1 + mu^2 c) - w c) / 2 * sigmoid(raw);
+// block y == 0 of each head also takes d(logits) = dlogpi - pi * sum(dlogpi).  Eight chunks' loads
+// are issued at a time.
+__global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__restrict__ m1, const float *__restrict__ m2,
                                                              const float *__restrict__ pl, const float *__restrict__ iv,
-                                                             const float *__restrict__ raw,
+                                                             const float *__restrict__ mu, const float *__restrict__ raw,
                                                              const float *__restrict__ logits, float *__restrict__ dmu,
                                                              float *__restrict__ draw, float *__restrict__ dlogits,
                                                              int K, int d_r, int R)
@@ -667,14 +612,28 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
     if (e < KD) {
         const int k = e / d_r;
         float a = 0.f, b = 0.f, c = 0.f;
-        for (int ch = 0; ch < R; ++ch) {
-            a += pmu[((size_t)h * R + ch) * KD + e];
-            b += ps[((size_t)h * R + ch) * KD + e];
-            c += pl[((size_t)h * R + ch) * K + k];
+        for (int c0 = 0; c0 < R; c0 += 8) {
+            float va[8], vb[8], vc[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const bool ok = c0 + u < R;
+                const size_t ch = (size_t)h * R + c0 + u;
+                va[u] = ok ? m1[ch * KD + e] : 0.f;
+                vb[u] = ok ? m2[ch * KD + e] : 0.f;
+                vc[u] = ok ? pl[ch * K + k] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                a += va[u];
+                b += vb[u];
+                c += vc[u];
+            }
         }
-        const float w = iv[(size_t)h * KD + e], r = raw[(size_t)h * KD + e];
-        dmu[(size_t)h * KD + e] = w * a;
-        draw[(size_t)h * KD + e] = 0.5f * (w * w * b - w * c) / (1.f + expf(-r));
+        const float w = iv[(size_t)h * KD + e], m = mu[(size_t)h * KD + e], r = raw[(size_t)h * KD + e];
+        const float s1 = fmaf(-m, c, a);                       // sum dL (x - mu)
+        const float s2 = fmaf(m, fmaf(m, c, -2.f * a), b);     // sum dL (x - mu)^2
+        dmu[(size_t)h * KD + e] = w * s1;
+        draw[(size_t)h * KD + e] = 0.5f * (w * w * s2 - w * c) / (1.f + expf(-r));
     }
     if (blockIdx.y != 0) return;
     // prior logits: pi = softmax(logits); dlogits = dlogpi - pi * sum_k dlogpi
@@ -720,7 +679,7 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
 }
 
 struct BwdLayout {
-    size_t iv, cst, gq, gk, agg, dnd, dagg, dgq, dgk, dotq, dotk, pmu, ps, pl, total;
+    size_t iv, cst, gq, gk, agg, dnd, dagg, dgq, dgk, dotq, dotk, m1, m2, pl, total;
     int nseg, R, ktiles;
 };
 
@@ -732,9 +691,9 @@ BwdLayout bwd_layout(const gma_shape_t &s)
     const int dv1 = s.d_v + 1;
     L.nseg = (s.N + SEG - 1) / SEG;
     L.ktiles = (s.K + KT - 1) / KT;
-    // parameter partials: about three blocks per SM in all, at most one chunk per 64-row block
+    // parameter partials: one wave of two blocks per SM, at most one chunk per 64-row block
     const int nb = 2 * s.B * L.nseg;
-    int R = (3 * 152 + s.H * L.ktiles - 1) / (s.H * L.ktiles);
+    int R = 2 * 152 / (s.H * L.ktiles);
     if (R > nb) R = nb;
     if (R < 1) R = 1;
     L.R = R;
@@ -749,8 +708,8 @@ BwdLayout bwd_layout(const gma_shape_t &s)
     L.dgk = c.take(sizeof(float) * T * s.K);
     L.dotq = c.take(sizeof(float) * T);
     L.dotk = c.take(sizeof(float) * T);
-    L.pmu = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
-    L.ps = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
+    L.m1 = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
+    L.m2 = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
     L.pl = c.take(sizeof(float) * (size_t)s.H * R * s.K);
     L.total = c.total();
     return L;
@@ -807,7 +766,7 @@ gma_status_t launch_rows(const gma_shape_t &s, const BwdLayout &L, const Tin *QX
     const float *gq = (const float *)(ws + L.gq), *gk = (const float *)(ws + L.gk);
     float *dgq = (float *)(ws + L.dgq), *dgk = (float *)(ws + L.dgk);
     const float *dotq = (const float *)(ws + L.dotq), *dotk = (const float *)(ws + L.dotk);
-    float *pmu = (float *)(ws + L.pmu), *ps = (float *)(ws + L.ps), *pl = (float *)(ws + L.pl);
+    float *m1 = (float *)(ws + L.m1), *m2 = (float *)(ws + L.m2), *pl = (float *)(ws + L.pl);
     if (!set_smem(bwd_dx_kernel<DR, Tin>, dx_smem_floats<DR>()) ||
         !set_smem(bwd_param_partial_kernel<DR, Tin>, param_smem_floats<DR>()))
         return GMA_ERR_CUDA;
@@ -819,11 +778,11 @@ gma_status_t launch_rows(const gma_shape_t &s, const BwdLayout &L, const Tin *QX
     if ((r = launch_chained(KID_BWD_PARAMS, st, bwd_param_partial_kernel<DR, Tin>,
                             dim3((unsigned)s.H, (unsigned)L.ktiles, (unsigned)L.R), dim3(BT),
                             sizeof(float) * param_smem_floats<DR>(), QX, KX, (const float *)dgq, (const float *)dgk,
-                            mu, pmu, ps, pl, s.B, s.H, s.N, s.K, L.nseg, L.R)) != GMA_OK)
+                            m1, m2, pl, s.B, s.H, s.N, s.K, L.nseg, L.R)) != GMA_OK)
         return r;
     const int KD = s.K * s.d_r;
     return launch_chained(KID_BWD_PFINAL, st, bwd_param_final_kernel, dim3((unsigned)s.H, (unsigned)((KD + BT - 1) / BT)),
-                          dim3(BT), 0, (const float *)pmu, (const float *)ps, (const float *)pl, iv, raw, logits, dmu,
+                          dim3(BT), 0, (const float *)m1, (const float *)m2, (const float *)pl, iv, mu, raw, logits, dmu,
                           draw, dlogits, s.K, s.d_r, L.R);
 }
 

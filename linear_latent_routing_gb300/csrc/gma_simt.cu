@@ -14,6 +14,7 @@
 // exclusive-prefix-scanned (causal); each query segment then reads its memory and, for the
 // causal variant, adds the masked in-segment affinity (Gamma_Q Gamma_K^T restricted to j <= i).
 #include "gma_internal.cuh"
+#include "simt_tile.cuh"
 #include "tc_ptx.cuh"
 
 namespace gma {
@@ -150,99 +151,211 @@ __device__ __forceinline__ float2 logit_direct_pair(const float (&x)[DR], const 
     return make_float2(hi, lo);
 }
 
-// One thread per routing vector: online max/sum over K, then a second pass writes
-// gamma_k = exp(L_k - max) / sum.  fp32 inputs take the logits as TwoSum pairs (above): the
-// maximum m is taken over the high parts, and exp((hi_k - m) + lo_k) is evaluated with the
-// subtraction first, which is exact for every logit within a factor of two of the maximum.
+// The routing vectors of one 64-row segment of one (b, h) slice per block of 256 threads: a 16 x 16
+// grid in which each thread forms the logits of 4 rows x 4 components of a 64-component tile, from
+// x^T, mu^T and (1 / sigma^2)^T staged in shared memory (per dimension one 16-byte load of each, 48
+// operations).  Each logit is summed over d in order, exactly as logit_direct (bf16 inputs) and
+// logit_direct_pair (fp32 inputs) do.  The softmax over K: the row's maximum and sum are reduced
+// over the 16 threads that hold it; above 64 components a first sweep keeps a running maximum and
+// sum per row, and a second recomputes the logits and writes gamma_k = exp(L_k - max) / sum.
+// fp32 inputs take the logits as TwoSum pairs: the maximum is taken over the high parts and
+// exp((hi_k - m) + lo_k) is evaluated with the subtraction first.
+constexpr int RT = 64;    // components per tile
+constexpr int RLD = 68;   // row stride of the transposed tiles (a multiple of 4, not of 8)
+
+template <int DR>
+__host__ __device__ constexpr int resp_smem_floats() { return 3 * DR * RLD + RT; }
+
+// blockIdx.y picks the side: routing vectors X0 (N0 per slice) into gamma0, or X1 (N1) into gamma1.
 template <int DR, typename Tin, typename Tout>
-__global__ void simt_resp_kernel(const Tin *__restrict__ X, const float *__restrict__ mu,
-                                 const float *__restrict__ inv_var, const float *__restrict__ cst,
-                                 Tout *__restrict__ gamma, int H, int N, int K, long long rows)
+__global__ void __launch_bounds__(THREADS, 2) simt_resp_kernel(const Tin *__restrict__ X0, const Tin *__restrict__ X1,
+                                                              const float *__restrict__ mu,
+                                                              const float *__restrict__ inv_var,
+                                                              const float *__restrict__ cst, Tout *__restrict__ gamma0,
+                                                              Tout *__restrict__ gamma1, int B, int H, int N0, int N1,
+                                                              int K)
 {
     chain_enter();
+    const int N = blockIdx.y ? N1 : N0, nseg = (N + SEG - 1) / SEG;
+    if ((int)blockIdx.x >= B * H * nseg) return;
+    const Tin *X = blockIdx.y ? X1 : X0;
+    Tout *gamma = blockIdx.y ? gamma1 : gamma0;
     constexpr bool PRECISE = sizeof(Tin) == 4;
-    const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= rows) return;
-    const int h = (int)((r / N) % H);
-    float x[DR];
+    extern __shared__ __align__(16) float smr[];
+    float *xT = smr;                 // [DR][RLD] x^T
+    float *mT = xT + DR * RLD;       // [DR][RLD] mu^T of the tile
+    float *wT = mT + DR * RLD;       // [DR][RLD] (1 / sigma^2)^T of the tile
+    float *cs = wT + DR * RLD;       // [RT]      log pi_k - 1/2 sum_d log sigma^2_kd
+    const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg, h = bh % H;
+    const int n = min(SEG, N - seg * SEG);
+    const long long row0 = (long long)bh * N + seg * SEG;
+    const int t = threadIdx.x, tx = t & 15, r0 = (t >> 4) * 4;
+    const float *muh = mu + (size_t)h * K * DR, *ivh = inv_var + (size_t)h * K * DR, *ch = cst + (size_t)h * K;
+#pragma unroll 8
+    for (int e = t; e < SEG * DR; e += THREADS) {
+        const int r = e / DR, d = e % DR;
+        xT[d * RLD + r] = r < n ? to_f32(X[(row0 + r) * DR + d]) : 0.f;
+    }
+    // logits of the tile starting at k0 into hi (and lo); -inf beyond K
+    float hi[4][4], lo[4][4];
+    auto logits = [&](int k0) {
+        const int kn = min(RT, K - k0);
+        __syncthreads();
+#pragma unroll 8
+        for (int e = t; e < RT * DR; e += THREADS) {
+            const int kk = e / DR, d = e % DR;
+            const bool ok = kk < kn;
+            mT[d * RLD + kk] = ok ? muh[(size_t)(k0 + kk) * DR + d] : 0.f;
+            wT[d * RLD + kk] = ok ? ivh[(size_t)(k0 + kk) * DR + d] : 0.f;
+        }
+        if (t < RT) cs[t] = t < kn ? ch[k0 + t] : 0.f;
+        __syncthreads();
 #pragma unroll
-    for (int d = 0; d < DR; ++d) x[d] = to_f32(X[r * DR + d]);
-    const float *muh = mu + (size_t)h * K * DR;
-    const float *ivh = inv_var + (size_t)h * K * DR;
-    const float *ch = cst + (size_t)h * K;
-    auto logit = [&](int k) -> float2 {
-        if (PRECISE) return logit_direct_pair<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k));
-        return make_float2(logit_direct<DR>(x, muh + (size_t)k * DR, ivh + (size_t)k * DR, __ldg(ch + k)), 0.f);
-    };
-    // four components' logits at a time: independent chains of loads and FMAs, each summed in
-    // its own order as before; the online maximum and sum then take them one by one
-    float m = -INFINITY, s = 0.f;
-    for (int k0 = 0; k0 < K; k0 += 4) {
-        float2 L4[4];
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) L4[u] = k0 + u < K ? logit(k0 + u) : make_float2(-INFINITY, 0.f);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (k0 + u >= K) break;
-            const float2 L = L4[u];
-            if (L.x > m) {
-                s = s * expf(m - L.x) + expf(L.y);
-                m = L.x;
-            } else {
-                s += expf((L.x - m) + L.y);
+            for (int c = 0; c < 4; ++c) {
+                hi[r][c] = PRECISE ? cs[4 * tx + c] : 0.f;
+                lo[r][c] = 0.f;
             }
+        if constexpr (PRECISE) {
+            for (int d0 = 0; d0 < DR; d0 += 4) {
+                float p[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) p[r][c] = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int d = d0 + u;
+                    const float4 a = *reinterpret_cast<const float4 *>(xT + d * RLD + r0);
+                    const float4 m = *reinterpret_cast<const float4 *>(mT + d * RLD + 4 * tx);
+                    const float4 w = *reinterpret_cast<const float4 *>(wT + d * RLD + 4 * tx);
+                    const float av[4] = {a.x, a.y, a.z, a.w}, mv[4] = {m.x, m.y, m.z, m.w}, wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float q = av[r] - mv[c];
+                            p[r][c] = fmaf(q * q, wv[c], p[r][c]);
+                        }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) two_sum_acc(hi[r][c], lo[r][c], -0.5f * p[r][c]);
+            }
+        } else {
+#pragma unroll 4
+            for (int d = 0; d < DR; ++d) {
+                const float4 a = *reinterpret_cast<const float4 *>(xT + d * RLD + r0);
+                const float4 m = *reinterpret_cast<const float4 *>(mT + d * RLD + 4 * tx);
+                const float4 w = *reinterpret_cast<const float4 *>(wT + d * RLD + 4 * tx);
+                const float av[4] = {a.x, a.y, a.z, a.w}, mv[4] = {m.x, m.y, m.z, m.w}, wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float q = av[r] - mv[c];
+                        hi[r][c] = fmaf(q * q, wv[c], hi[r][c]);
+                    }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) hi[r][c] = fmaf(-0.5f, hi[r][c], cs[4 * tx + c]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (4 * tx + c >= kn)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    hi[r][c] = -INFINITY;
+                    lo[r][c] = 0.f;
+                }
+    };
+    auto rmax16 = [](float v) {
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        return v;
+    };
+    auto rsum16 = [](float v) {
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        return v;
+    };
+    float m[4], ssum[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        m[r] = -INFINITY;
+        ssum[r] = 0.f;
+    }
+    for (int k0 = 0; k0 < K; k0 += RT) {
+        logits(k0);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float tm = rmax16(fmaxf(fmaxf(hi[r][0], hi[r][1]), fmaxf(hi[r][2], hi[r][3])));
+            const float nm = fmaxf(m[r], tm);
+            float e = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) e += expf((hi[r][c] - nm) + lo[r][c]);
+            ssum[r] = ssum[r] * expf(m[r] - nm) + rsum16(e);
+            m[r] = nm;
         }
     }
-    const float inv = 1.f / s;
-    Tout *g = gamma + r * K;
-    for (int k0 = 0; k0 < K; k0 += 4) {
-        float2 L4[4];
+    for (int k0 = 0; k0 < K; k0 += RT) {
+        if (K > RT) logits(k0);   // (one tile: its logits are still in registers)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) L4[u] = k0 + u < K ? logit(k0 + u) : make_float2(0.f, 0.f);
+        for (int r = 0; r < 4; ++r) {
+            const float inv = 1.f / ssum[r];
+            if (r0 + r < n)
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (k0 + u < K) g[k0 + u] = from_f32<Tout>(expf((L4[u].x - m) + L4[u].y) * inv);
+                for (int c = 0; c < 4; ++c) {
+                    const int k = k0 + 4 * tx + c;
+                    if (k < K) gamma[(row0 + r0 + r) * K + k] = from_f32<Tout>(expf((hi[r][c] - m[r]) + lo[r][c]) * inv);
+                }
+        }
     }
 }
 
 // ---------------------------------------------------------------- write phase, per segment
-// agg[bh][seg][k][c] = sum_{j in seg} gamma_K[j][k] * [v_j | 1][c],  c in [0, d_v].
-template <typename Tin>
-__global__ void simt_state_kernel(const float *__restrict__ gk, const Tin *__restrict__ V,
-                                  float *__restrict__ agg, int N, int K, int d_v, int nseg)
+// agg[bh][seg][k][c] = sum_{j in seg} gamma_K[j][k] * [v_j | 1][c],  c in [0, d_v], for one tile of
+// 64 components (blockIdx.y): a register-tiled product over the staged Gamma_K tile and value rows
+// (simt_tile.cuh), summed over j in order.
+template <int DV, typename Tin>
+__global__ void __launch_bounds__(THREADS, 2) simt_state_kernel(const float *__restrict__ gk, const Tin *__restrict__ V,
+                                                            float *__restrict__ agg, int N, int K, int nseg)
 {
     chain_enter();
-    const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
-    const int k0 = blockIdx.y * KT;
-    const int j0 = seg * SEG, jn = min(SEG, N - j0);
-    const int kn = min(KT, K - k0);
-    const int DV1 = d_v + 1;
-    __shared__ float sg[SEG][KT + 1];
-    __shared__ float sv[SEG][129];
-    for (int e = threadIdx.x; e < SEG * KT; e += blockDim.x) {
-        const int j = e / KT, kk = e % KT;
-        sg[j][kk] = (j < jn && kk < kn) ? gk[((size_t)bh * N + j0 + j) * K + k0 + kk] : 0.f;
-    }
-    for (int e = threadIdx.x; e < SEG * d_v; e += blockDim.x) {
-        const int j = e / d_v, c = e % d_v;
-        sv[j][c] = j < jn ? to_f32(V[((size_t)bh * N + j0 + j) * d_v + c]) : 0.f;
-    }
+    __shared__ __align__(16) float sg[SEG * 64];   // Gamma_K tile [j][k]
+    __shared__ __align__(16) float sv[SEG * DV];   // value rows [j][c]
+    const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg, k0 = blockIdx.y * 64;
+    const int j0 = seg * SEG, jn = min(SEG, N - j0), kn = min(64, K - k0);
+    const long long row0 = (long long)bh * N + j0;
+    tile::stage<64>(sg, 64, gk + row0 * K + k0, K, jn, kn);
+    tile::stage<DV>(sv, DV, V + row0 * DV, DV, jn, DV);
     __syncthreads();
-    float *out = agg + ((size_t)bh * nseg + seg) * K * DV1;
-    for (int e = threadIdx.x; e < kn * DV1; e += blockDim.x) {
-        const int kk = e / DV1, c = e % DV1;
-        float acc = 0.f;
-        if (c < d_v) {
-            for (int j = 0; j < jn; ++j) acc = fmaf(sg[j][kk], sv[j][c], acc);
-        } else {
-            for (int j = 0; j < jn; ++j) acc += sg[j][kk];
-        }
-        out[(size_t)(k0 + kk) * DV1 + c] = acc;
+    float acc[4][DV / 16];
+    tile::zero<DV>(acc);
+    tile::mac<DV>(acc, sg, 64, sv, DV, SEG);   // rows k, columns c
+    float *out = agg + ((size_t)bh * nseg + seg) * K * (DV + 1);
+    const int r0 = tile::orow();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int k = k0 + r0 + r;
+        if (k < K)
+#pragma unroll
+            for (int c = 0; c < DV / 16; ++c) out[(size_t)k * (DV + 1) + tile::ocol<DV>(c)] = acc[r][c];
+    }
+    if ((int)threadIdx.x < kn) {
+        float z = 0.f;
+        for (int jj = 0; jj < SEG; ++jj) z += sg[jj * 64 + threadIdx.x];
+        out[(size_t)(k0 + threadIdx.x) * (DV + 1) + DV] = z;
     }
 }
 
 // Causal: replace each segment's partial by the exclusive prefix over earlier segments.
-// Bidirectional: write the total over all segments into segment 0's slot.
+// Bidirectional: write the total over all segments into segment 0's slot.  One thread per element
+// of the K x (d_v + 1) memory; the loads of 32 segments are issued before their sums.
 __global__ void simt_scan_kernel(float *__restrict__ agg, long long total, int nseg, int KD,
                                  int causal)
 {
@@ -252,10 +365,16 @@ __global__ void simt_scan_kernel(float *__restrict__ agg, long long total, int n
     const long long bh = idx / KD, e = idx % KD;
     float *base = agg + bh * nseg * KD + e;
     float run = 0.f;
-    for (int s = 0; s < nseg; ++s) {
-        const float a = base[(size_t)s * KD];
-        if (causal) base[(size_t)s * KD] = run;
-        run += a;
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+        float a[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) a[u] = s0 + u < nseg ? base[(size_t)(s0 + u) * KD] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            if (s0 + u >= nseg) break;
+            if (causal) base[(size_t)(s0 + u) * KD] = run;
+            run += a[u];
+        }
     }
     if (!causal) base[0] = run;
 }
@@ -516,16 +635,33 @@ gma_status_t launch_chained(int kid, cudaStream_t st, void (*k)(P...), dim3 g, d
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
-template <typename Tin, typename Tout>
-gma_status_t launch_resp(int d_r, const Tin *X, const float *mu, const float *iv, const float *cst,
-                         Tout *g, int H, int N, int K, long long rows, cudaStream_t st)
+// Responsibilities of X0 (N0 rows per slice) into g0 and, when X1 is given, of X1 (N1) into g1, in
+// one launch.
+template <int DR, typename Tin, typename Tout>
+gma_status_t launch_resp_dr(const Tin *X0, const Tin *X1, const float *mu, const float *iv, const float *cst, Tout *g0,
+                            Tout *g1, int B, int H, int N0, int N1, int K, cudaStream_t st)
 {
-    const unsigned blocks = (unsigned)((rows + 127) / 128);
+    const int nseg = (max(N0, X1 ? N1 : 0) + SEG - 1) / SEG;
+    const int smem = (int)sizeof(float) * resp_smem_floats<DR>();
+    if (cudaFuncSetAttribute(simt_resp_kernel<DR, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return GMA_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    GMA_LAUNCH(KID_SIMT_RESP, st,
+               (e = launch_pdl(simt_resp_kernel<DR, Tin, Tout>, dim3((unsigned)(B * H * nseg), X1 ? 2u : 1u),
+                               dim3(THREADS), (size_t)smem, st, X0, X1, mu, iv, cst, g0, g1, B, H, N0, N1, K)));
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
+template <typename Tin, typename Tout>
+gma_status_t launch_resp(int d_r, const Tin *X0, const Tin *X1, const float *mu, const float *iv, const float *cst,
+                         Tout *g0, Tout *g1, int B, int H, int N0, int N1, int K, cudaStream_t st)
+{
     switch (d_r) {
-    case 16: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<16, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
-    case 32: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<32, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
-    case 64: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<64, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
-    case 128: return launch_chained(KID_SIMT_RESP, st, simt_resp_kernel<128, Tin, Tout>, dim3(blocks), dim3(128), X, mu, iv, cst, g, H, N, K, rows);
+    case 16: return launch_resp_dr<16, Tin, Tout>(X0, X1, mu, iv, cst, g0, g1, B, H, N0, N1, K, st);
+    case 32: return launch_resp_dr<32, Tin, Tout>(X0, X1, mu, iv, cst, g0, g1, B, H, N0, N1, K, st);
+    case 64: return launch_resp_dr<64, Tin, Tout>(X0, X1, mu, iv, cst, g0, g1, B, H, N0, N1, K, st);
+    case 128: return launch_resp_dr<128, Tin, Tout>(X0, X1, mu, iv, cst, g0, g1, B, H, N0, N1, K, st);
     default: return GMA_ERR_UNSUPPORTED_SHAPE;
     }
 }
@@ -538,17 +674,20 @@ gma_status_t prepare_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
                            const Tin *V, const float *mu, const float *raw, const float *logits, float *iv,
                            float *cst, float *gq, float *gk, float *agg, int nseg, cudaStream_t st)
 {
-    const long long rows = (long long)s.B * s.H * s.N, rows_k = (long long)s.B * s.H * n_k;
     gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel, dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)),
                                     dim3(PARAM_THREADS), raw, logits, iv, cst, s.K, s.d_r, s.var_floor);
     if (r != GMA_OK) return r;
-    r = launch_resp<Tin, float>(s.d_r, QX, mu, iv, cst, gq, s.H, s.N, s.K, rows, st);
-    if (r != GMA_OK) return r;
-    r = launch_resp<Tin, float>(s.d_r, KX, mu, iv, cst, gk, s.H, n_k, s.K, rows_k, st);
+    r = launch_resp<Tin, float>(s.d_r, QX, KX, mu, iv, cst, gq, gk, s.B, s.H, s.N, n_k, s.K, st);
     if (r != GMA_OK) return r;
     const int BH = s.B * s.H;
-    dim3 gs((unsigned)(BH * nseg), (unsigned)((s.K + KT - 1) / KT));
-    r = launch_chained(KID_SIMT_STATE, st, simt_state_kernel<Tin>, gs, dim3(THREADS), gk, V, agg, n_k, s.K, s.d_v, nseg);
+    dim3 gs((unsigned)(BH * nseg), (unsigned)((s.K + 63) / 64));
+    switch (s.d_v) {
+    case 16: r = launch_chained(KID_SIMT_STATE, st, simt_state_kernel<16, Tin>, gs, dim3(THREADS), gk, V, agg, n_k, s.K, nseg); break;
+    case 32: r = launch_chained(KID_SIMT_STATE, st, simt_state_kernel<32, Tin>, gs, dim3(THREADS), gk, V, agg, n_k, s.K, nseg); break;
+    case 64: r = launch_chained(KID_SIMT_STATE, st, simt_state_kernel<64, Tin>, gs, dim3(THREADS), gk, V, agg, n_k, s.K, nseg); break;
+    case 128: r = launch_chained(KID_SIMT_STATE, st, simt_state_kernel<128, Tin>, gs, dim3(THREADS), gk, V, agg, n_k, s.K, nseg); break;
+    default: return GMA_ERR_UNSUPPORTED_SHAPE;
+    }
     if (r != GMA_OK) return r;
     const int KD = s.K * (s.d_v + 1);
     const long long tot = (long long)BH * KD;
@@ -638,13 +777,12 @@ gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const fl
                                           dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), dim3(PARAM_THREADS), raw,
                                           logits, iv, cst, s.K, s.d_r, s.var_floor);
     if (r != GMA_OK) return r;
-    const long long rows = (long long)s.B * s.H * s.N;
     const bool out32 = (s.flags & GMA_FLAG_OUT_F32) || s.dtype == GMA_F32;
     if (s.dtype == GMA_F32)
-        return launch_resp<float, float>(s.d_r, (const float *)X, mu, iv, cst, (float *)gamma, s.H, s.N, s.K, rows, st);
+        return launch_resp<float, float>(s.d_r, (const float *)X, (const float *)nullptr, mu, iv, cst, (float *)gamma, (float *)nullptr, s.B, s.H, s.N, 0, s.K, st);
     if (out32)
-        return launch_resp<__nv_bfloat16, float>(s.d_r, (const __nv_bfloat16 *)X, mu, iv, cst, (float *)gamma, s.H, s.N, s.K, rows, st);
-    return launch_resp<__nv_bfloat16, __nv_bfloat16>(s.d_r, (const __nv_bfloat16 *)X, mu, iv, cst, (__nv_bfloat16 *)gamma, s.H, s.N, s.K, rows, st);
+        return launch_resp<__nv_bfloat16, float>(s.d_r, (const __nv_bfloat16 *)X, (const __nv_bfloat16 *)nullptr, mu, iv, cst, (float *)gamma, (float *)nullptr, s.B, s.H, s.N, 0, s.K, st);
+    return launch_resp<__nv_bfloat16, __nv_bfloat16>(s.d_r, (const __nv_bfloat16 *)X, (const __nv_bfloat16 *)nullptr, mu, iv, cst, (__nv_bfloat16 *)gamma, (__nv_bfloat16 *)nullptr, s.B, s.H, s.N, 0, s.K, st);
 }
 
 gma_status_t simt_forward(const gma_shape_t &s, bool causal, int n_k, const void *QX, const void *KX,
