@@ -63,8 +63,8 @@ template <int DV, typename Tin>
 __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_numden_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                         const Tin *__restrict__ V, const float *__restrict__ agg,
                                                         const Tin *__restrict__ dO, float *__restrict__ dnd,
-                                                        float *__restrict__ dagg, int N, int K, int nseg, float eps,
-                                                        int causal)
+                                                        float *__restrict__ dagg, float *__restrict__ Pg, int N, int K,
+                                                        int nseg, float eps, int causal)
 {
     chain_enter();
     extern __shared__ __align__(16) float sm[];
@@ -102,13 +102,19 @@ __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_numden_kernel(const 
     }
     __syncthreads();
     if (causal) {
+        // P^T[j][i], kept for i >= j; also stored for the key-side kernel (row j: 64 floats)
+        float *Pt = Pg + (size_t)blockIdx.x * SEG * SEG;
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int j = r0 + r, i = ocol<64>(c);
-                gkT[j * LT + i] = i >= j ? accP[r][c] : 0.f;
-            }
+        for (int r = 0; r < 4; ++r) {
+            const int j = r0 + r;
+            float4 v;
+            v.x = ocol<64>(0) >= j ? accP[r][0] : 0.f;
+            v.y = ocol<64>(1) >= j ? accP[r][1] : 0.f;
+            v.z = ocol<64>(2) >= j ? accP[r][2] : 0.f;
+            v.w = ocol<64>(3) >= j ? accP[r][3] : 0.f;
+            *reinterpret_cast<float4 *>(gkT + j * LT + ocol<64>(0)) = v;
+            *reinterpret_cast<float4 *>(Pt + j * SEG + ocol<64>(0)) = v;
+        }
         stage<DV>(sS, DV, V + row0 * DV, DV, n, DV);
         __syncthreads();
         mac_range<DV>(accN, gkT, LT, sS, DV, 0, r0 + 4);   // (P^T[j][i] = 0 for j > i)
@@ -185,7 +191,8 @@ template <int DV, typename Tin>
 __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dgq_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                      const Tin *__restrict__ V, const float *__restrict__ agg,
                                                      const float *__restrict__ dnd, float *__restrict__ dgq,
-                                                     float *__restrict__ dotq, int N, int K, int nseg, int causal)
+                                                     float *__restrict__ dotq, float *__restrict__ Ag, int N, int K,
+                                                     int nseg, int causal)
 {
     chain_enter();
     extern __shared__ __align__(16) float sm[];
@@ -209,13 +216,21 @@ __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dgq_kernel(const flo
         float accA[4][4];
         zero<64>(accA);
         mac<64>(accA, VT, LT, dnT, LT, DV);   // rows j, columns i: v_j . dnum_i
+        // also stored for the key-side kernel (row j: 64 floats)
+        float *At = Ag + (size_t)blockIdx.x * SEG * SEG;
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < 4; ++r) {
+            const int j = r0 + r;
+            float a[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int j = r0 + r, i = ocol<64>(c);
-                AT[j * LT + i] = i >= j ? accA[r][c] + dd[i] : 0.f;
+                const int i = ocol<64>(c);
+                a[c] = i >= j ? accA[r][c] + dd[i] : 0.f;
             }
+            const float4 v = make_float4(a[0], a[1], a[2], a[3]);
+            *reinterpret_cast<float4 *>(AT + j * LT + ocol<64>(0)) = v;
+            *reinterpret_cast<float4 *>(At + j * SEG + ocol<64>(0)) = v;
+        }
     }
     const bool one = K <= KT;
     float dot[4] = {0.f, 0.f, 0.f, 0.f}, gsv[4][4], acc[4][4];
@@ -292,27 +307,27 @@ __global__ void __launch_bounds__(BT) bwd_scan_kernel(float *__restrict__ dagg, 
 //   dV[j] = Gamma_K[j] D + sum_{i >= j in segment} P[i][j] dnum_i      (the first d_v columns
 //                                                                      of d[v_j | 1])
 //   dGamma_K[j][k] = [v_j | 1] . D[k] + sum_{i >= j in segment} A[i][j] Gamma_Q[i][k]
-// (P = Gamma_Q Gamma_K^T and A[i][j] = dnd_i . [v_j | 1], causal only), and the row's
-// <Gamma_K, dGamma_K>.
+// (P = Gamma_Q Gamma_K^T and A[i][j] = dnd_i . [v_j | 1], causal only: the query-side kernels'
+// tiles, stored transposed per segment and read back here), and the row's <Gamma_K, dGamma_K>.
 template <int DV>
-__host__ __device__ constexpr int dk_smem_floats() { return 2 * KT * LT + 2 * DV * LT + KT + SEG; }
+__host__ __device__ constexpr int dk_smem_floats() { return 2 * KT * LT + 2 * DV * LT + KT; }
 
 template <int DV, typename Tin>
 __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dk_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                     const Tin *__restrict__ V, const float *__restrict__ dagg,
-                                                    const float *__restrict__ dnd, float *__restrict__ dgk,
+                                                    const float *__restrict__ dnd, const float *__restrict__ Pg,
+                                                    const float *__restrict__ Ag, float *__restrict__ dgk,
                                                     float *__restrict__ dotk, Tin *__restrict__ dV, int N, int K,
                                                     int nseg, int causal)
 {
     chain_enter();
     extern __shared__ __align__(16) float sm[];
     constexpr int DV1 = DV + 1, NC = DV / 16;
-    float *gqT = sm;                 // [KT][LT] Gamma_Q^T tile; later P [SEG][LT], then A [SEG][LT]
+    float *gqT = sm;                 // [SEG][LT] P, then A
     float *gkT = gqT + KT * LT;      // [KT][LT] Gamma_K^T tile; later Gamma_Q tiles [SEG][KT]
     float *VT = gkT + KT * LT;       // [DV][LT] V^T; before it, the D tiles [KT][DV], then the dnum rows
-    float *DT = VT + DV * LT;        // [DV][LT] dnum^T; later the D^T tiles
+    float *DT = VT + DV * LT;        // [DV][LT] D^T tiles
     float *zD = DT + DV * LT;        // [KT]
-    float *dd = zD + KT;             // [SEG]
     float *sD = VT;
     const int bh = blockIdx.x / nseg, seg = blockIdx.x % nseg;
     const int j0 = seg * SEG, n = min(SEG, N - j0);
@@ -320,28 +335,20 @@ __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dk_kernel(const floa
     const float *D = dagg + ((size_t)bh * nseg + (causal ? seg : 0)) * K * DV1;
     const int t = threadIdx.x, r0 = orow();
     // dV
-    float accP[4][4], accV[4][NC];
-    zero<64>(accP);
+    float accV[4][NC];
     zero<DV>(accV);
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        if (causal) stage_t<KT>(gqT, LT, gq + row0 * K + k0, K, n, kn);
         stage_t<KT>(gkT, LT, gk + row0 * K + k0, K, n, kn);
         stage<DV>(sD, DV, D + (size_t)k0 * DV1, DV1, kn, DV);
         __syncthreads();
-        if (causal) mac<64>(accP, gqT, LT, gkT, LT, KT);   // P: rows i, columns j
         mac<DV>(accV, gkT, LT, sD, DV, KT);                // rows j, columns c
     }
     __syncthreads();
     if (causal) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = r0 + r, j = ocol<64>(c);
-                gqT[i * LT + j] = i >= j ? accP[r][c] : 0.f;
-            }
+        // P[i][j] from the query-side kernel's P^T tile
+        stage_t<SEG>(gqT, LT, Pg + (size_t)blockIdx.x * SEG * SEG, SEG, SEG, SEG);
         stage<DV>(sD, DV, dnd + row0 * DV1, DV1, n, DV);
         __syncthreads();
         mac_range<DV>(accV, gqT, LT, sD, DV, r0, SEG);   // sum_{i >= j} P[i][j] dnum_i
@@ -356,21 +363,8 @@ __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dk_kernel(const floa
     // dGamma_K
     __syncthreads();
     stage_t<DV>(VT, LT, V + row0 * DV, DV, n, DV);
-    if (causal) {
-        stage_t<DV>(DT, LT, dnd + row0 * DV1, DV1, n, DV);
-        if (t < SEG) dd[t] = t < n ? dnd[(row0 + t) * DV1 + DV] : 0.f;
-        __syncthreads();
-        float accA[4][4];
-        zero<64>(accA);
-        mac<64>(accA, DT, LT, VT, LT, DV);   // rows i, columns j: dnum_i . v_j
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = r0 + r, j = ocol<64>(c);
-                gqT[i * LT + j] = i >= j ? accA[r][c] + dd[i] : 0.f;
-            }
-    }
+    // A[i][j] from the query-side kernel's A^T tile
+    if (causal) stage_t<SEG>(gqT, LT, Ag + (size_t)blockIdx.x * SEG * SEG, SEG, SEG, SEG);
     const bool one = K <= KT;
     float dot[4] = {0.f, 0.f, 0.f, 0.f}, gsv[4][4], acc[4][4];
     for (int k0 = 0; k0 < K; k0 += KT) {
@@ -424,7 +418,7 @@ template <int DR>
 __host__ __device__ constexpr int dx_smem_floats() { return KT * LT + 2 * KT * DR + SEG; }
 
 template <int DR, typename Tin>
-__global__ void __launch_bounds__(BT, 2) bwd_dx_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
+__global__ void __launch_bounds__(BT, DR <= 64 ? 3 : 2) bwd_dx_kernel(const Tin *__restrict__ QX, const Tin *__restrict__ KX,
                                                     const float *__restrict__ gq, const float *__restrict__ gk,
                                                     float *__restrict__ dgq, float *__restrict__ dgk,
                                                     const float *__restrict__ dotq, const float *__restrict__ dotk,
@@ -462,24 +456,29 @@ __global__ void __launch_bounds__(BT, 2) bwd_dx_kernel(const Tin *__restrict__ Q
     for (int k0 = 0; k0 < K; k0 += KT) {
         const int kn = min(KT, K - k0);
         __syncthreads();
-        // the tile's Gamma and dGamma first (16 of each per thread in flight), then dL; a thread
+        // the tile's Gamma and dGamma first (8 of each per thread in flight), then dL; a thread
         // keeps component kk and takes rows rb, rb + 4, ...
         constexpr int PER = SEG * KT / BT;
         const int kk = t % KT, rb = t / KT;
         const bool kok = kk < kn;
         const long long o0 = (row0 + rb) * K + k0 + kk;
-        float gv[PER], dv[PER];
 #pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const bool ok = kok && rb + 4 * u < n;
-            gv[u] = ok && !one ? g[o0 + (long long)u * 4 * K] : 0.f;
-            dv[u] = ok ? dg[o0 + (long long)u * 4 * K] : 0.f;
-        }
+        for (int h0 = 0; h0 < PER; h0 += PER / 2) {   // (two halves: fewer registers held)
+            float gv[PER / 2], dv[PER / 2];
 #pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const float v = one ? dv[u] : gv[u] * (dv[u] - sdot[rb + 4 * u]);
-            if (!one && kok && rb + 4 * u < n) dg[o0 + (long long)u * 4 * K] = v;
-            dLT[kk * LT + rb + 4 * u] = v;
+            for (int u = 0; u < PER / 2; ++u) {
+                const int rr = rb + 4 * (h0 + u);
+                const bool ok = kok && rr < n;
+                gv[u] = ok && !one ? g[o0 + (long long)(h0 + u) * 4 * K] : 0.f;
+                dv[u] = ok ? dg[o0 + (long long)(h0 + u) * 4 * K] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < PER / 2; ++u) {
+                const int rr = rb + 4 * (h0 + u);
+                const float v = one ? dv[u] : gv[u] * (dv[u] - sdot[rr]);
+                if (!one && kok && rr < n) dg[o0 + (long long)(h0 + u) * 4 * K] = v;
+                dLT[kk * LT + rr] = v;
+            }
         }
         stage<DR>(sW, DR, ivh + (size_t)k0 * DR, DR, kn, DR);
         stage<DR>(sWM, DR, muh + (size_t)k0 * DR, DR, kn, DR);
@@ -595,8 +594,8 @@ __global__ void __launch_bounds__(BT, 2) bwd_param_partial_kernel(const Tin *__r
 
 // Over the chunks in order, a1 = sum dL_k x_d, a2 = sum dL_k x_d^2, c = sum dL_k; then
 //   dmu = w (a1 - mu c),  d(raw) = (w^2 (a2 - 2 mu a1 + mu^2 c) - w c) / 2 * sigmoid(raw);
-// block y == 0 of each head also takes d(logits) = dlogpi - pi * sum(dlogpi).  Eight chunks' loads
-// are issued at a time.
+// the last block row (blockIdx.y == gridDim.y - 1) takes d(logits) = dlogpi - pi * sum(dlogpi) per
+// head instead.  Eight chunks' loads are issued at a time.
 __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__restrict__ m1, const float *__restrict__ m2,
                                                              const float *__restrict__ pl, const float *__restrict__ iv,
                                                              const float *__restrict__ mu, const float *__restrict__ raw,
@@ -606,10 +605,12 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
 {
     chain_enter();
     __shared__ float red[BT / 32][2];
+    __shared__ float sl[1024];   // dlogpi per component (K <= 1024)
     const int h = blockIdx.x;
     const int KD = K * d_r;
-    const int e = blockIdx.y * BT + threadIdx.x;
-    if (e < KD) {
+    if (blockIdx.y + 1 < gridDim.y) {
+        const int e = blockIdx.y * BT + threadIdx.x;
+        if (e >= KD) return;
         const int k = e / d_r;
         float a = 0.f, b = 0.f, c = 0.f;
         for (int c0 = 0; c0 < R; c0 += 8) {
@@ -634,52 +635,57 @@ __global__ void __launch_bounds__(BT) bwd_param_final_kernel(const float *__rest
         const float s2 = fmaf(m, fmaf(m, c, -2.f * a), b);     // sum dL (x - mu)^2
         dmu[(size_t)h * KD + e] = w * s1;
         draw[(size_t)h * KD + e] = 0.5f * (w * w * s2 - w * c) / (1.f + expf(-r));
+        return;
     }
-    if (blockIdx.y != 0) return;
     // prior logits: pi = softmax(logits); dlogits = dlogpi - pi * sum_k dlogpi
     const float *lh = logits + (size_t)h * K;
     float m = -INFINITY, tl = 0.f;
-    for (int k = threadIdx.x; k < K; k += BT) m = fmaxf(m, lh[k]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5][0] = m;
-    __syncthreads();
-    m = red[0][0];
-    for (int wv = 1; wv < BT / 32; ++wv) m = fmaxf(m, red[wv][0]);
-    float se = 0.f;
     for (int k = threadIdx.x; k < K; k += BT) {
-        se += expf(lh[k] - m);
+        m = fmaxf(m, lh[k]);
         float a = 0.f;
-        for (int ch = 0; ch < R; ++ch) a += pl[((size_t)h * R + ch) * K + k];
+        for (int c0 = 0; c0 < R; c0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = c0 + u < R ? pl[((size_t)h * R + c0 + u) * K + k] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a += v[u];
+        }
+        sl[k] = a;
         tl += a;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        se += __shfl_xor_sync(0xffffffffu, se, o);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         tl += __shfl_xor_sync(0xffffffffu, tl, o);
     }
-    __syncthreads();
     if ((threadIdx.x & 31) == 0) {
-        red[threadIdx.x >> 5][0] = se;
+        red[threadIdx.x >> 5][0] = m;
         red[threadIdx.x >> 5][1] = tl;
     }
     __syncthreads();
-    se = 0.f;
+    m = red[0][0];
     tl = 0.f;
     for (int wv = 0; wv < BT / 32; ++wv) {
-        se += red[wv][0];
+        m = fmaxf(m, red[wv][0]);
         tl += red[wv][1];
     }
+    float se = 0.f;
+    for (int k = threadIdx.x; k < K; k += BT) se += expf(lh[k] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5][0] = se;
+    __syncthreads();
+    se = 0.f;
+    for (int wv = 0; wv < BT / 32; ++wv) se += red[wv][0];
     for (int k = threadIdx.x; k < K; k += BT) {
-        float a = 0.f;
-        for (int ch = 0; ch < R; ++ch) a += pl[((size_t)h * R + ch) * K + k];
         const float pi = expf(lh[k] - m) / se;
-        dlogits[(size_t)h * K + k] = a - pi * tl;
+        dlogits[(size_t)h * K + k] = sl[k] - pi * tl;
     }
 }
 
 struct BwdLayout {
-    size_t iv, cst, gq, gk, agg, dnd, dagg, dgq, dgk, dotq, dotk, m1, m2, pl, total;
+    size_t iv, cst, gq, gk, agg, dnd, dagg, dgq, dgk, dotq, dotk, pt, at, m1, m2, pl, total;
     int nseg, R, ktiles;
 };
 
@@ -708,6 +714,8 @@ BwdLayout bwd_layout(const gma_shape_t &s)
     L.dgk = c.take(sizeof(float) * T * s.K);
     L.dotq = c.take(sizeof(float) * T);
     L.dotk = c.take(sizeof(float) * T);
+    L.pt = c.take(sizeof(float) * (size_t)s.B * s.H * L.nseg * SEG * SEG);   // P^T per segment
+    L.at = c.take(sizeof(float) * (size_t)s.B * s.H * L.nseg * SEG * SEG);   // A^T per segment
     L.m1 = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
     L.m2 = c.take(sizeof(float) * (size_t)s.H * R * s.K * s.d_r);
     L.pl = c.take(sizeof(float) * (size_t)s.H * R * s.K);
@@ -731,6 +739,7 @@ gma_status_t launch_segments(const gma_shape_t &s, const BwdLayout &L, bool caus
     float *dnd = (float *)(ws + L.dnd), *dagg = (float *)(ws + L.dagg);
     float *dgq = (float *)(ws + L.dgq), *dgk = (float *)(ws + L.dgk);
     float *dotq = (float *)(ws + L.dotq), *dotk = (float *)(ws + L.dotk);
+    float *pt = (float *)(ws + L.pt), *at = (float *)(ws + L.at);
     const int BH = s.B * s.H, cz = causal ? 1 : 0;
     const dim3 grid((unsigned)(BH * L.nseg));
     if (!set_smem(bwd_numden_kernel<DV, Tin>, numden_smem_floats<DV>()) ||
@@ -740,11 +749,11 @@ gma_status_t launch_segments(const gma_shape_t &s, const BwdLayout &L, bool caus
     gma_status_t r = GMA_OK;
     if ((r = launch_chained(KID_BWD_NUMDEN, st, bwd_numden_kernel<DV, Tin>, grid, dim3(BT),
                             sizeof(float) * numden_smem_floats<DV>(), (const float *)gq, (const float *)gk, V,
-                            (const float *)agg, dO, dnd, dagg, s.N, s.K, L.nseg, s.eps, cz)) != GMA_OK)
+                            (const float *)agg, dO, dnd, dagg, pt, s.N, s.K, L.nseg, s.eps, cz)) != GMA_OK)
         return r;
     if ((r = launch_chained(KID_BWD_DQ, st, bwd_dgq_kernel<DV, Tin>, grid, dim3(BT),
                             sizeof(float) * dgq_smem_floats<DV>(), (const float *)gq, (const float *)gk, V,
-                            (const float *)agg, (const float *)dnd, dgq, dotq, s.N, s.K, L.nseg, cz)) != GMA_OK)
+                            (const float *)agg, (const float *)dnd, dgq, dotq, at, s.N, s.K, L.nseg, cz)) != GMA_OK)
         return r;
     const int KD = s.K * (s.d_v + 1);
     const long long tot = (long long)BH * KD;
@@ -752,8 +761,8 @@ gma_status_t launch_segments(const gma_shape_t &s, const BwdLayout &L, bool caus
                             dagg, tot, L.nseg, KD, cz)) != GMA_OK)
         return r;
     return launch_chained(KID_BWD_DK, st, bwd_dk_kernel<DV, Tin>, grid, dim3(BT), sizeof(float) * dk_smem_floats<DV>(),
-                          (const float *)gq, (const float *)gk, V, (const float *)dagg, (const float *)dnd, dgk, dotk,
-                          dV, s.N, s.K, L.nseg, cz);
+                          (const float *)gq, (const float *)gk, V, (const float *)dagg, (const float *)dnd,
+                          (const float *)pt, (const float *)at, dgk, dotk, dV, s.N, s.K, L.nseg, cz);
 }
 
 // The kernels through the responsibilities for one routing width.
@@ -781,7 +790,7 @@ gma_status_t launch_rows(const gma_shape_t &s, const BwdLayout &L, const Tin *QX
                             m1, m2, pl, s.B, s.H, s.N, s.K, L.nseg, L.R)) != GMA_OK)
         return r;
     const int KD = s.K * s.d_r;
-    return launch_chained(KID_BWD_PFINAL, st, bwd_param_final_kernel, dim3((unsigned)s.H, (unsigned)((KD + BT - 1) / BT)),
+    return launch_chained(KID_BWD_PFINAL, st, bwd_param_final_kernel, dim3((unsigned)s.H, (unsigned)((KD + BT - 1) / BT + 1)),
                           dim3(BT), 0, (const float *)m1, (const float *)m2, (const float *)pl, iv, mu, raw, logits, dmu,
                           draw, dlogits, s.K, s.d_r, L.R);
 }

@@ -35,12 +35,12 @@ __device__ __forceinline__ void chain_enter()
 constexpr int SEG = 64;        // tokens per segment
 constexpr int KT = 32;         // component tile for the staged dot products
 constexpr int THREADS = 256;
-constexpr int PARAM_THREADS = 256;
+constexpr int PARAM_THREADS = 64;   // two component rows per block: the fp64 log-determinants spread over the SMs
 
 // ---------------------------------------------------------------- reparametrisation
 // Per head h: inv_var[h][k][d] = 1 / (softplus(raw) + floor);
 //             cst[h][k]        = log pi_k - 1/2 sum_d log sigma^2_kd,  log pi = log softmax.
-// One warp per component row (grid H x ceil(K / 8)); every warp first reduces its head's
+// One warp per component row (grid H x ceil(K / 2)); every warp first reduces its head's
 // prior logits to their log-sum-exp (K <= 1024: at most 32 values per lane).
 __global__ void simt_params_kernel(const float *__restrict__ raw, const float *__restrict__ logits,
                                    float *__restrict__ inv_var, float *__restrict__ cst, int K,
@@ -168,7 +168,7 @@ __host__ __device__ constexpr int resp_smem_floats() { return 3 * DR * RLD + RT;
 
 // blockIdx.y picks the side: routing vectors X0 (N0 per slice) into gamma0, or X1 (N1) into gamma1.
 template <int DR, typename Tin, typename Tout>
-__global__ void __launch_bounds__(THREADS, 2) simt_resp_kernel(const Tin *__restrict__ X0, const Tin *__restrict__ X1,
+__global__ void __launch_bounds__(THREADS, sizeof(Tin) == 4 ? 2 : 3) simt_resp_kernel(const Tin *__restrict__ X0, const Tin *__restrict__ X1,
                                                               const float *__restrict__ mu,
                                                               const float *__restrict__ inv_var,
                                                               const float *__restrict__ cst, Tout *__restrict__ gamma0,
@@ -674,7 +674,7 @@ gma_status_t prepare_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
                            const Tin *V, const float *mu, const float *raw, const float *logits, float *iv,
                            float *cst, float *gq, float *gk, float *agg, int nseg, cudaStream_t st)
 {
-    gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel, dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)),
+    gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel, dim3((unsigned)s.H, (unsigned)((s.K + PARAM_THREADS / 32 - 1) / (PARAM_THREADS / 32))),
                                     dim3(PARAM_THREADS), raw, logits, iv, cst, s.K, s.d_r, s.var_floor);
     if (r != GMA_OK) return r;
     r = launch_resp<Tin, float>(s.d_r, QX, KX, mu, iv, cst, gq, gk, s.B, s.H, s.N, n_k, s.K, st);
@@ -774,7 +774,7 @@ gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const fl
     char *w = (char *)ws;
     float *iv = (float *)(w + L.inv_var), *cst = (float *)(w + L.cst);
     const gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel,
-                                          dim3((unsigned)s.H, (unsigned)((s.K + 7) / 8)), dim3(PARAM_THREADS), raw,
+                                          dim3((unsigned)s.H, (unsigned)((s.K + PARAM_THREADS / 32 - 1) / (PARAM_THREADS / 32))), dim3(PARAM_THREADS), raw,
                                           logits, iv, cst, s.K, s.d_r, s.var_floor);
     if (r != GMA_OK) return r;
     const bool out32 = (s.flags & GMA_FLAG_OUT_F32) || s.dtype == GMA_F32;
