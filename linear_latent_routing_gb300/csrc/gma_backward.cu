@@ -278,26 +278,30 @@ __global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_dgq_kernel(const flo
 
 // Causal: each segment's partial becomes the exclusive suffix over later segments (what the
 // keys of the segment see from queries after it).  Bidirectional: the total into segment 0.
-// One thread per element of the K x (d_v + 1) memory; the loads of 32 segments are issued before
-// their sums, so a thread waits once per 32 segments.
+// One thread per V4 consecutive elements of the K x (d_v + 1) memory (V4 = 4 with 16-byte accesses
+// when K (d_v + 1) is a multiple of 4, else 1); the loads of 16 segments are issued before their
+// sums, so a thread waits once per 16 segments.
+template <int V4>
 __global__ void __launch_bounds__(BT) bwd_scan_kernel(float *__restrict__ dagg, long long total, int nseg, int KD,
                                                       int causal)
 {
     chain_enter();
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    typedef typename std::conditional<V4 == 4, float4, float>::type vec;
+    const long long idx = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * V4;
     if (idx >= total) return;
     const long long bh = idx / KD, e = idx % KD;
-    float *base = dagg + bh * nseg * KD + e;
-    float run = 0.f;
-    for (int s1 = nseg; s1 > 0; s1 -= 32) {
-        float a[32];
+    vec *base = reinterpret_cast<vec *>(dagg + bh * nseg * KD + e);
+    const size_t step = (size_t)KD / V4;
+    vec run = vzero<vec>();
+    for (int s1 = nseg; s1 > 0; s1 -= 16) {
+        vec a[16];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) a[u] = s1 - 1 - u >= 0 ? base[(size_t)(s1 - 1 - u) * KD] : 0.f;
+        for (int u = 0; u < 16; ++u) a[u] = s1 - 1 - u >= 0 ? base[(size_t)(s1 - 1 - u) * step] : vzero<vec>();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
+        for (int u = 0; u < 16; ++u) {
             if (s1 - 1 - u < 0) break;
-            if (causal) base[(size_t)(s1 - 1 - u) * KD] = run;
-            run += a[u];
+            if (causal) base[(size_t)(s1 - 1 - u) * step] = run;
+            run = vadd(run, a[u]);
         }
     }
     if (!causal) base[0] = run;
@@ -757,9 +761,13 @@ gma_status_t launch_segments(const gma_shape_t &s, const BwdLayout &L, bool caus
         return r;
     const int KD = s.K * (s.d_v + 1);
     const long long tot = (long long)BH * KD;
-    if ((r = launch_chained(KID_BWD_SCAN, st, bwd_scan_kernel, dim3((unsigned)((tot + BT - 1) / BT)), dim3(BT), 0,
-                            dagg, tot, L.nseg, KD, cz)) != GMA_OK)
-        return r;
+    if (KD % 4 == 0)
+        r = launch_chained(KID_BWD_SCAN, st, bwd_scan_kernel<4>, dim3((unsigned)((tot / 4 + BT - 1) / BT)), dim3(BT), 0,
+                           dagg, tot, L.nseg, KD, cz);
+    else
+        r = launch_chained(KID_BWD_SCAN, st, bwd_scan_kernel<1>, dim3((unsigned)((tot + BT - 1) / BT)), dim3(BT), 0,
+                           dagg, tot, L.nseg, KD, cz);
+    if (r != GMA_OK) return r;
     return launch_chained(KID_BWD_DK, st, bwd_dk_kernel<DV, Tin>, grid, dim3(BT), sizeof(float) * dk_smem_floats<DV>(),
                           (const float *)gq, (const float *)gk, V, (const float *)dagg, (const float *)dnd,
                           (const float *)pt, (const float *)at, dgk, dotk, dV, s.N, s.K, L.nseg, cz);

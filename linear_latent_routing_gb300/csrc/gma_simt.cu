@@ -354,26 +354,30 @@ __global__ void __launch_bounds__(THREADS, 2) simt_state_kernel(const float *__r
 }
 
 // Causal: replace each segment's partial by the exclusive prefix over earlier segments.
-// Bidirectional: write the total over all segments into segment 0's slot.  One thread per element
-// of the K x (d_v + 1) memory; the loads of 32 segments are issued before their sums.
+// Bidirectional: write the total over all segments into segment 0's slot.  One thread per V4
+// consecutive elements of the K x (d_v + 1) memory (16-byte accesses when K (d_v + 1) is a multiple
+// of 4); the loads of 16 segments are issued before their sums.
+template <int V4>
 __global__ void simt_scan_kernel(float *__restrict__ agg, long long total, int nseg, int KD,
                                  int causal)
 {
     chain_enter();
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    typedef typename std::conditional<V4 == 4, float4, float>::type vec;
+    const long long idx = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * V4;
     if (idx >= total) return;
     const long long bh = idx / KD, e = idx % KD;
-    float *base = agg + bh * nseg * KD + e;
-    float run = 0.f;
-    for (int s0 = 0; s0 < nseg; s0 += 32) {
-        float a[32];
+    vec *base = reinterpret_cast<vec *>(agg + bh * nseg * KD + e);
+    const size_t step = (size_t)KD / V4;
+    vec run = tile::vzero<vec>();
+    for (int s0 = 0; s0 < nseg; s0 += 16) {
+        vec a[16];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) a[u] = s0 + u < nseg ? base[(size_t)(s0 + u) * KD] : 0.f;
+        for (int u = 0; u < 16; ++u) a[u] = s0 + u < nseg ? base[(size_t)(s0 + u) * step] : tile::vzero<vec>();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
+        for (int u = 0; u < 16; ++u) {
             if (s0 + u >= nseg) break;
-            if (causal) base[(size_t)(s0 + u) * KD] = run;
-            run += a[u];
+            if (causal) base[(size_t)(s0 + u) * step] = run;
+            run = tile::vadd(run, a[u]);
         }
     }
     if (!causal) base[0] = run;
@@ -691,8 +695,11 @@ gma_status_t prepare_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
     if (r != GMA_OK) return r;
     const int KD = s.K * (s.d_v + 1);
     const long long tot = (long long)BH * KD;
-    return launch_chained(KID_SIMT_SCAN, st, simt_scan_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), agg, tot,
-                          nseg, KD, causal ? 1 : 0);
+    if (KD % 4 == 0)
+        return launch_chained(KID_SIMT_SCAN, st, simt_scan_kernel<4>, dim3((unsigned)((tot / 4 + 255) / 256)), dim3(256),
+                              agg, tot, nseg, KD, causal ? 1 : 0);
+    return launch_chained(KID_SIMT_SCAN, st, simt_scan_kernel<1>, dim3((unsigned)((tot + 255) / 256)), dim3(256), agg,
+                          tot, nseg, KD, causal ? 1 : 0);
 }
 
 // The one-launch path for short bidirectional slices (simt_small_kernel).

@@ -7,6 +7,7 @@
 // load of four rows of A, one or two loads of B and 4 W / 16 FMAs, summed in the order of the
 // contracted index.
 #pragma once
+#include <type_traits>
 #include "gma_internal.cuh"
 
 namespace gma {
@@ -157,6 +158,16 @@ __device__ __forceinline__ void stage_t(float *dst, int ld, const T *src, long l
 #pragma unroll
     for (int u = 0; u < PER; ++u) dst[c * ld + r0 + u * STEP] = v[u];
 }
+
+// Zero and element-wise sum of a float or a float4 (the scans' vectors).
+template <typename V>
+__device__ __forceinline__ V vzero();
+template <>
+__device__ __forceinline__ float vzero<float>() { return 0.f; }
+template <>
+__device__ __forceinline__ float4 vzero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ float vadd(float a, float b) { return a + b; }
+__device__ __forceinline__ float4 vadd(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 
 // v[r] (the thread's partial for its row orow() + r) becomes the sum over the 16 threads of that row
 // (a half-warp: shuffles over lanes xor 1, 2, 4, 8).
