@@ -42,9 +42,12 @@ constexpr int PARAM_THREADS = 64;   // two component rows per block: the fp64 lo
 //             cst[h][k]        = log pi_k - 1/2 sum_d log sigma^2_kd,  log pi = log softmax.
 // One warp per component row (grid H x ceil(K / 2)); every warp first reduces its head's
 // prior logits to their log-sum-exp (K <= 1024: at most 32 values per lane).
+// The block at inv_var also receives the transposes the responsibilities stage from: mu^T and
+// (1 / sigma^2)^T, [H][d_r][K] each, after the H K d_r values of inv_var (the callers' workspace
+// holds all three).
 __global__ void simt_params_kernel(const float *__restrict__ raw, const float *__restrict__ logits,
-                                   float *__restrict__ inv_var, float *__restrict__ cst, int K,
-                                   int d_r, float floor_)
+                                   const float *__restrict__ mu, float *__restrict__ inv_var,
+                                   float *__restrict__ cst, int K, int d_r, float floor_)
 {
     chain_enter();
     const int h = blockIdx.x, lane = threadIdx.x & 31;
@@ -76,6 +79,9 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
             const float r = rv[i];
             const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
             ik[d] = 1.0f / var;
+            const size_t HKD = (size_t)gridDim.x * K * d_r, tr = ((size_t)h * d_r + d) * K + k;
+            inv_var[HKD + tr] = mu[((size_t)h * K + k) * d_r + d];
+            inv_var[2 * HKD + tr] = 1.0f / var;
             logdet += log((double)var);
         }
     }
@@ -190,7 +196,9 @@ __global__ void __launch_bounds__(THREADS, sizeof(Tin) == 4 ? 2 : 3) simt_resp_k
     const int n = min(SEG, N - seg * SEG);
     const long long row0 = (long long)bh * N + seg * SEG;
     const int t = threadIdx.x, tx = t & 15, r0 = (t >> 4) * 4;
-    const float *muh = mu + (size_t)h * K * DR, *ivh = inv_var + (size_t)h * K * DR, *ch = cst + (size_t)h * K;
+    const size_t HKD = (size_t)H * K * DR;
+    const float *muTh = inv_var + HKD + (size_t)h * DR * K, *ivTh = inv_var + 2 * HKD + (size_t)h * DR * K;
+    const float *ch = cst + (size_t)h * K;
 #pragma unroll 8
     for (int e = t; e < SEG * DR; e += THREADS) {
         const int r = e / DR, d = e % DR;
@@ -202,11 +210,11 @@ __global__ void __launch_bounds__(THREADS, sizeof(Tin) == 4 ? 2 : 3) simt_resp_k
         const int kn = min(RT, K - k0);
         __syncthreads();
 #pragma unroll 8
-        for (int e = t; e < RT * DR; e += THREADS) {
-            const int kk = e / DR, d = e % DR;
+        for (int e = t; e < RT * DR; e += THREADS) {   // rows of the transposes: coalesced, conflict-free
+            const int d = e / RT, kk = e % RT;
             const bool ok = kk < kn;
-            mT[d * RLD + kk] = ok ? muh[(size_t)(k0 + kk) * DR + d] : 0.f;
-            wT[d * RLD + kk] = ok ? ivh[(size_t)(k0 + kk) * DR + d] : 0.f;
+            mT[d * RLD + kk] = ok ? muTh[(size_t)d * K + k0 + kk] : 0.f;
+            wT[d * RLD + kk] = ok ? ivTh[(size_t)d * K + k0 + kk] : 0.f;
         }
         if (t < RT) cs[t] = t < kn ? ch[k0 + t] : 0.f;
         __syncthreads();
@@ -346,10 +354,14 @@ __global__ void __launch_bounds__(THREADS, 2) simt_state_kernel(const float *__r
 #pragma unroll
             for (int c = 0; c < DV / 16; ++c) out[(size_t)k * (DV + 1) + tile::ocol<DV>(c)] = acc[r][c];
     }
-    if ((int)threadIdx.x < kn) {
+    {   // Z: four threads per component (t / 4), rows t % 4, t % 4 + 4, ... then two shuffles
+        const int t = threadIdx.x, k = t >> 2;
         float z = 0.f;
-        for (int jj = 0; jj < SEG; ++jj) z += sg[jj * 64 + threadIdx.x];
-        out[(size_t)(k0 + threadIdx.x) * (DV + 1) + DV] = z;
+#pragma unroll 4
+        for (int jj = t & 3; jj < SEG; jj += 4) z += sg[jj * 64 + k];
+        z += __shfl_xor_sync(0xffffffffu, z, 1);
+        z += __shfl_xor_sync(0xffffffffu, z, 2);
+        if ((t & 3) == 0 && k < kn) out[(size_t)(k0 + k) * (DV + 1) + DV] = z;
     }
 }
 
@@ -616,7 +628,7 @@ SimtLayout simt_layout(const gma_shape_t &s, int variant, int n_k)
     Carve c;
     const size_t rows = (size_t)s.B * s.H * s.N;
     const size_t rows_k = (size_t)s.B * s.H * n_k;
-    L.inv_var = c.take(sizeof(float) * (size_t)s.H * s.K * s.d_r);
+    L.inv_var = c.take(3 * sizeof(float) * (size_t)s.H * s.K * s.d_r);   // 1/sigma^2, mu^T, (1/sigma^2)^T
     L.cst = c.take(sizeof(float) * (size_t)s.H * s.K);
     L.nseg = (n_k + SEG - 1) / SEG;
     if (variant != GMA_VARIANT_RESPONSIBILITIES) {
@@ -679,7 +691,7 @@ gma_status_t prepare_typed(const gma_shape_t &s, bool causal, int n_k, const Tin
                            float *cst, float *gq, float *gk, float *agg, int nseg, cudaStream_t st)
 {
     gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel, dim3((unsigned)s.H, (unsigned)((s.K + PARAM_THREADS / 32 - 1) / (PARAM_THREADS / 32))),
-                                    dim3(PARAM_THREADS), raw, logits, iv, cst, s.K, s.d_r, s.var_floor);
+                                    dim3(PARAM_THREADS), raw, logits, mu, iv, cst, s.K, s.d_r, s.var_floor);
     if (r != GMA_OK) return r;
     r = launch_resp<Tin, float>(s.d_r, QX, KX, mu, iv, cst, gq, gk, s.B, s.H, s.N, n_k, s.K, st);
     if (r != GMA_OK) return r;
@@ -782,7 +794,7 @@ gma_status_t simt_responsibilities(const gma_shape_t &s, const void *X, const fl
     float *iv = (float *)(w + L.inv_var), *cst = (float *)(w + L.cst);
     const gma_status_t r = launch_chained(KID_SIMT_PARAMS, st, simt_params_kernel,
                                           dim3((unsigned)s.H, (unsigned)((s.K + PARAM_THREADS / 32 - 1) / (PARAM_THREADS / 32))), dim3(PARAM_THREADS), raw,
-                                          logits, iv, cst, s.K, s.d_r, s.var_floor);
+                                          logits, mu, iv, cst, s.K, s.d_r, s.var_floor);
     if (r != GMA_OK) return r;
     const bool out32 = (s.flags & GMA_FLAG_OUT_F32) || s.dtype == GMA_F32;
     if (s.dtype == GMA_F32)
