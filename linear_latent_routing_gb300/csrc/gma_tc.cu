@@ -732,9 +732,12 @@ gma_status_t forward_dr(const gma_shape_t &s, bool causal, const void *QX, const
         aq.nseg = pq.nseg;
         aq.cps = pq.cps;
         aq.agg_nseg = p.nseg;
-        CUtensorMap qmap;
+        CUtensorMap qmap, omap;
         if (!make_xmap(&qmap, aq.QX, BH, n_q, DR)) return GMA_ERR_CUDA;
-        const gma_status_t r = launch_bidir_read2<DR>(aq, qmap, BH * pq.nseg, st);
+        // bf16 output rows of 64-column multiples leave through TMA stores (boxes of 64 x 128); an
+        // output the tensor map cannot describe keeps the threads' own stores
+        const bool o_tma = !aq.out_f32 && s.d_v % 64 == 0 && make_vmap128(&omap, aq.O, BH, n_q, s.d_v);
+        const gma_status_t r = launch_bidir_read2<DR>(aq, qmap, o_tma ? &omap : nullptr, BH * pq.nseg, st);
         if (r != GMA_OK) return r;
     }
     return GMA_OK;
@@ -877,7 +880,7 @@ gma_status_t tiled_bidir_dr(const gma_shape_t &sk, const void *QX, const void *K
         aq.cps = pq.cps;
         aq.agg_nseg = p.nseg;
         aq.pmode = t == 0 ? 1 : 2;
-        if ((r = launch_bidir_read2<DR>(aq, qmap, BH * pq.nseg, st)) != GMA_OK) return r;
+        if ((r = launch_bidir_read2<DR>(aq, qmap, nullptr, BH * pq.nseg, st)) != GMA_OK) return r;
     }
     const long long groups = (long long)BH * n_q * (sk.d_v / 16);
     cudaError_t e = cudaSuccess;

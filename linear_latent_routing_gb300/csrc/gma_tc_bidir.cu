@@ -23,11 +23,14 @@ namespace tck {
 namespace {
 
 constexpr int BTHREADS = 256;
-enum BBar { B_BIMG, B_X0, B_X1, B_SP, B_A0, B_A1, B_E0, B_E1, B_L0, B_L1, B_O0, B_O1, B_NBAR };
+// (B_F*: a group's output stage is free, its previous TMA store having read it; B_W*: the stage
+// holds all 128 rows of the chunk)
+enum BBar { B_BIMG, B_X0, B_X1, B_SP, B_A0, B_A1, B_E0, B_E1, B_L0, B_L1, B_O0, B_O1, B_F0, B_F1, B_W0, B_W1, B_NBAR };
 
 struct BidirSmem {
-    uint32_t bimg, ax, ab0, ab1, sp, z, bars, misc, total;
+    uint32_t bimg, ax, ab0, ab1, sp, os0, os1, z, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    // (the output stages, C rows of d_v bf16 per group, exist when d_v is a multiple of 64)
     __host__ __device__ BidirSmem(int DR, int kn16, int d_v)
     {
         const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
@@ -38,6 +41,9 @@ struct BidirSmem {
         ab0 = o; o = al(o + (uint32_t)C * DR * 4u);   // group 0's [x^2 | x]
         ab1 = o; o = al(o + (uint32_t)C * DR * 4u);   // group 1's
         sp = o; o = al(o + (uint32_t)d_v * KMAX * 2u);
+        const uint32_t ost = d_v % 64 == 0 ? (uint32_t)C * d_v * 2u : 0u;
+        os0 = o; o = al(o + ost);
+        os1 = o; o = al(o + ost);
         z = o; o += KMAX * 4u;
         bars = o; o += B_NBAR * 8u;
         misc = o; o += 16u;
@@ -133,11 +139,30 @@ __device__ __forceinline__ void store_row(uint32_t tl, int d_v, float inv, bool 
 
 }  // namespace
 
+// The same row into the output stage os (rows of d_v bf16 in 64-column blocks with the 128-byte
+// swizzle: the layout of the TMA boxes), zeros for rows past the end.
+__device__ __forceinline__ void stage_row(uint32_t tl, int d_v, float inv, bool valid, uint8_t *os, int row)
+{
+    const float s = valid ? inv : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < d_v / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4 *>(os + sw128(row, 4 * c + q, C)) =
+                make_uint4(pk2(r[8 * q], r[8 * q + 1], s), pk2(r[8 * q + 2], r[8 * q + 3], s),
+                           pk2(r[8 * q + 4], r[8 * q + 5], s), pk2(r[8 * q + 6], r[8 * q + 7], s));
+    }
+}
+
 // MINB: CTAs per SM the register allocation is sized for (two for shapes whose tensor memory
 // and shared memory let two CTAs share an SM, one otherwise).
 template <int DR, int MINB>
 __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Args a,
-                                                                     const __grid_constant__ CUtensorMap qmap)
+                                                                     const __grid_constant__ CUtensorMap qmap,
+                                                                     const __grid_constant__ CUtensorMap omap)
 {
     // (no wait here: the set-up and the first query rows, which no kernel writes, overlap the
     // kernel before; the threads that read its results wait below)
@@ -162,7 +187,8 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
     const bool leader = i == 0;
 
     if (t == 0) {
-        for (int b = 0; b < B_NBAR; ++b) mbar_init(bars + b, (b >= B_SP && b <= B_E1) ? 128u : 1u);
+        for (int b = 0; b < B_NBAR; ++b)
+            mbar_init(bars + b, ((b >= B_SP && b <= B_E1) || b == B_W0 || b == B_W1) ? 128u : 1u);
         *abort = 0;
         fence_mbar_init();
     }
@@ -267,13 +293,33 @@ __global__ void __launch_bounds__(BTHREADS, MINB) tc_bidir_read2_kernel(const Ar
         }
         if (!(ok = mbar_wait_abortable(bo, n, a.hdr, 156, abort))) break;
         tc_fence_after();
-        if (a.pmode)
+        if (a.pmode) {
             tile_partial_row(lane + R_O, d_v, sd.y + a.eps * sd.x, valid, a.part, a.pden, (long long)bh * a.N + row,
                              a.pmode);
-        else
+        } else if (a.o_tma) {
+            // the group's stage is free once the TMA store of its previous chunk has read it (the
+            // leader's own bulk group); then the rows go in, and the leader stores the box(es)
+            uint8_t *os = smem + (g ? L.os1 : L.os0);
+            if (leader && c >= 2) {
+                bulk_wait_read();
+                mbar_arrive(bars + B_F0 + g);
+            }
+            if (c >= 2 && !(ok = mbar_wait_abortable(bars + B_F0 + g, ((c >> 1) - 1) & 1, a.hdr, 159, abort))) break;
+            stage_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), valid, os, i);
+            fence_proxy_async_smem();
+            mbar_arrive(bars + B_W0 + g);
+            if (leader) {
+                if (!(ok = mbar_wait_abortable(bars + B_W0 + g, n, a.hdr, 160, abort))) break;
+                for (int hb = 0; hb < d_v / 64; ++hb) tma_store_3d(&omap, os + hb * C * 128, 64 * hb, tok0 + c * C, bh);
+                bulk_commit_group();
+            }
+        } else {
             store_row(lane + R_O, d_v, 1.0f / (sd.y + a.eps * sd.x), valid, a.O, (long long)bh * a.N + row,
                       a.out_f32);
+        }
     }
+    // the output stores have completed before the CTA (and its shared memory) is released
+    if (a.o_tma && leader) bulk_wait_all();
     // a TMA load issued but not consumed (only after a timeout) completes before shared memory
     // is released
     if (leader && !ok && last_x >= 0) mbar_wait(bx, (uint32_t)(last_x >> 1) & 1u, a.hdr, 157);
@@ -303,27 +349,34 @@ int bidir_read2_ctas_per_sm(int d_r, int kn16, int d_v)
 }
 
 template <int DR, int MINB>
-gma_status_t launch_bidir_read2_n(const Args &a, const CUtensorMap &qmap, int nblocks, uint32_t sm, cudaStream_t st)
+gma_status_t launch_bidir_read2_n(const Args &a, const CUtensorMap &qmap, const CUtensorMap &omap, int nblocks,
+                                  uint32_t sm, cudaStream_t st)
 {
     if (!set_smem(tc_bidir_read2_kernel<DR, MINB>, sm)) return GMA_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     GMA_LAUNCH(KID_TC_BIDIR_READ, st,
-               (e = launch_pdl(tc_bidir_read2_kernel<DR, MINB>, dim3(nblocks), dim3(BTHREADS), sm, st, a, qmap)));
+               (e = launch_pdl(tc_bidir_read2_kernel<DR, MINB>, dim3(nblocks), dim3(BTHREADS), sm, st, a, qmap, omap)));
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
+// omap: the output's tensor map (bf16, 64-column boxes, 128-byte swizzle), or null for stores from
+// the threads (fp32 output, d_v not a multiple of 64, or the tiles' partial sums).
 template <int DR>
-gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblocks, cudaStream_t st)
+gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, const CUtensorMap *omap, int nblocks,
+                                cudaStream_t st)
 {
     const uint32_t sm = bidir_read2_smem(DR, a.kn16, a.d_v);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
-    return bidir_read2_ctas_per_sm(DR, a.kn16, a.d_v) == 2 ? launch_bidir_read2_n<DR, 2>(a, qmap, nblocks, sm, st)
-                                                           : launch_bidir_read2_n<DR, 1>(a, qmap, nblocks, sm, st);
+    Args b = a;
+    b.o_tma = omap && !a.out_f32 && !a.pmode && a.d_v % 64 == 0 ? 1 : 0;
+    const CUtensorMap &om = b.o_tma ? *omap : qmap;   // (not read unless o_tma)
+    return bidir_read2_ctas_per_sm(DR, a.kn16, a.d_v) == 2 ? launch_bidir_read2_n<DR, 2>(b, qmap, om, nblocks, sm, st)
+                                                           : launch_bidir_read2_n<DR, 1>(b, qmap, om, nblocks, sm, st);
 }
 
-template gma_status_t launch_bidir_read2<16>(const Args &, const CUtensorMap &, int, cudaStream_t);
-template gma_status_t launch_bidir_read2<32>(const Args &, const CUtensorMap &, int, cudaStream_t);
-template gma_status_t launch_bidir_read2<64>(const Args &, const CUtensorMap &, int, cudaStream_t);
+template gma_status_t launch_bidir_read2<16>(const Args &, const CUtensorMap &, const CUtensorMap *, int, cudaStream_t);
+template gma_status_t launch_bidir_read2<32>(const Args &, const CUtensorMap &, const CUtensorMap *, int, cudaStream_t);
+template gma_status_t launch_bidir_read2<64>(const Args &, const CUtensorMap &, const CUtensorMap *, int, cudaStream_t);
 
 }  // namespace tck
 }  // namespace gma

@@ -53,6 +53,8 @@ struct Args {
     int kg;
     int test_withhold;       // GMA_FLAG_TEST_WITHHOLD: the key pass withholds one hand-off
     int v128;                // value tiles in 64-column boxes with the 128-byte swizzle (d_v >= 64)
+    int o_tma;               // bidirectional read: output rows staged in shared memory, written by
+                             // TMA stores of 64-column boxes (bf16 output, d_v a multiple of 64)
     // More than 128 components: the components are cut into tiles of 128 and each pass works on
     // one tile (components [128 tile, 128 tile + K) of the head's K_all, K being the tile's count)
     // with every routing row's log2-sum-exp over all components precomputed (lse_q for the
@@ -305,7 +307,8 @@ gma_status_t launch_segmem_pipelined(const Args &a, const CUtensorMap &vmap, con
                                      const CUtensorMap &gmap, int nblocks, cudaStream_t st);
 uint32_t bidir_read2_smem(int d_r, int kn16, int d_v);
 template <int DR>
-gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, int nblocks, cudaStream_t st);
+gma_status_t launch_bidir_read2(const Args &a, const CUtensorMap &qmap, const CUtensorMap *omap, int nblocks,
+                                cudaStream_t st);
 uint32_t causal_gamma_smem(int d_r, int kn16, int d_v);
 template <int DR>
 gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
