@@ -101,8 +101,8 @@ def kernel_work(w, name):
         return "alu", 2 * th * w.K * w.d_r * 5, "TFLOP/s"
     if name == "bwd_dx":            # one launch covers both sides: two FMAs per term, and the softmax step
         return "alu", 2 * th * w.K * (4 * w.d_r + 2), "TFLOP/s"
-    if name == "simt_responsibilities":      # one launch covers one side (queries or keys)
-        return "alu", th * 2 * w.K * w.d_r * 3, "TFLOP/s"
+    if name == "simt_responsibilities":      # one launch covers both sides (queries and keys)
+        return "alu", (th + w.key_heads) * 2 * w.K * w.d_r * 3, "TFLOP/s"
     if name == "simt_small_one_launch":   # parameters, both sides' responsibilities, memory and read
         f = th * 2 * w.K * w.d_r * 3 + w.key_heads * (2 * w.K * w.d_r * 3 + 2 * w.K * (w.d_v + 1))
         return "alu", f + th * 2 * w.K * (w.d_v + 1), "TFLOP/s"
