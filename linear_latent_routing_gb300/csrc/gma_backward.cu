@@ -707,7 +707,7 @@ BwdLayout bwd_layout(const gma_shape_t &s)
     if (R > nb) R = nb;
     if (R < 1) R = 1;
     L.R = R;
-    L.iv = c.take(3 * sizeof(float) * (size_t)s.H * s.K * s.d_r);   // 1/sigma^2, mu^T, (1/sigma^2)^T
+    L.iv = c.take(5 * sizeof(float) * (size_t)s.H * s.K * s.d_r);   // 1/sigma^2 and four transposes
     L.cst = c.take(sizeof(float) * (size_t)s.H * s.K);
     L.gq = c.take(sizeof(float) * T * s.K);
     L.gk = c.take(sizeof(float) * T * s.K);

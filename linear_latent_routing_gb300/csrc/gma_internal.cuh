@@ -104,7 +104,8 @@ gma_status_t simt_forward(const gma_shape_t &s, bool causal, int n_k, const void
                           void *O, void *ws, cudaStream_t st);
 size_t simt_workspace_size_cross(const gma_shape_t &s, int n_k);
 // The read phase's inputs (fp32 CUDA cores, direct form): per-head 1/sigma^2 [H][K][d_r] followed by
-// mu^T and (1/sigma^2)^T [H][d_r][K] (iv holds 3 H K d_r floats), and constants [H][K]; Gamma_Q, Gamma_K [B*H*N][K]; segment memories [B*H][ceil(N/64)][K][d_v+1],
+// mu^T, (1/sigma^2)^T, (1/sigma)^T and (-mu/sigma)^T [H][d_r][K] (iv holds 5 H K d_r floats), and
+// constants [H][K]; Gamma_Q, Gamma_K [B*H*N][K]; segment memories [B*H][ceil(N/64)][K][d_v+1],
 // scanned (causal: exclusive prefix per 64-token segment; bidirectional: the total in segment 0).
 gma_status_t simt_prepare(const gma_shape_t &s, bool causal, const void *QX, const void *KX, const void *V,
                           const float *mu, const float *raw, const float *logits, float *iv, float *cst, float *gq,

@@ -42,9 +42,9 @@ constexpr int PARAM_THREADS = 64;   // two component rows per block: the fp64 lo
 //             cst[h][k]        = log pi_k - 1/2 sum_d log sigma^2_kd,  log pi = log softmax.
 // One warp per component row (grid H x ceil(K / 2)); every warp first reduces its head's
 // prior logits to their log-sum-exp (K <= 1024: at most 32 values per lane).
-// The block at inv_var also receives the transposes the responsibilities stage from: mu^T and
-// (1 / sigma^2)^T, [H][d_r][K] each, after the H K d_r values of inv_var (the callers' workspace
-// holds all three).
+// The block at inv_var also receives the transposes the responsibilities stage from, [H][d_r][K]
+// each, after the H K d_r values of inv_var: mu^T, (1 / sigma^2)^T, (1 / sigma)^T and
+// (-mu / sigma)^T (the callers' workspace holds all five).
 __global__ void simt_params_kernel(const float *__restrict__ raw, const float *__restrict__ logits,
                                    const float *__restrict__ mu, float *__restrict__ inv_var,
                                    float *__restrict__ cst, int K, int d_r, float floor_)
@@ -80,8 +80,11 @@ __global__ void simt_params_kernel(const float *__restrict__ raw, const float *_
             const float var = fmaxf(r, 0.f) + log1pf(expf(-fabsf(r))) + floor_;
             ik[d] = 1.0f / var;
             const size_t HKD = (size_t)gridDim.x * K * d_r, tr = ((size_t)h * d_r + d) * K + k;
-            inv_var[HKD + tr] = mu[((size_t)h * K + k) * d_r + d];
+            const float m = mu[((size_t)h * K + k) * d_r + d], sd = 1.0f / sqrtf(var);
+            inv_var[HKD + tr] = m;
             inv_var[2 * HKD + tr] = 1.0f / var;
+            inv_var[3 * HKD + tr] = sd;
+            inv_var[4 * HKD + tr] = -sd * m;
             logdet += log((double)var);
         }
     }
@@ -159,9 +162,10 @@ __device__ __forceinline__ float2 logit_direct_pair(const float (&x)[DR], const 
 
 // The routing vectors of one 64-row segment of one (b, h) slice per block of 256 threads: a 16 x 16
 // grid in which each thread forms the logits of 4 rows x 4 components of a 64-component tile, from
-// x^T, mu^T and (1 / sigma^2)^T staged in shared memory (per dimension one 16-byte load of each, 48
-// operations).  Each logit is summed over d in order, exactly as logit_direct (bf16 inputs) and
-// logit_direct_pair (fp32 inputs) do.  The softmax over K: the row's maximum and sum are reduced
+// x^T and two parameter transposes staged in shared memory (per dimension one 16-byte load of
+// each).  Each logit is summed over d in order.  fp32 inputs: exactly as logit_direct_pair does,
+// (x - mu)^2 / sigma^2 in four-term partials into a TwoSum pair.  bf16 inputs: u^2 with
+// u = x / sigma - mu / sigma, two FMAs per term.  The softmax over K: the row's maximum and sum are reduced
 // over the 16 threads that hold it; above 64 components a first sweep keeps a running maximum and
 // sum per row, and a second recomputes the logits and writes gamma_k = exp(L_k - max) / sum.
 // fp32 inputs take the logits as TwoSum pairs: the maximum is taken over the high parts and
@@ -196,8 +200,11 @@ __global__ void __launch_bounds__(THREADS, sizeof(Tin) == 4 ? 2 : 3) simt_resp_k
     const int n = min(SEG, N - seg * SEG);
     const long long row0 = (long long)bh * N + seg * SEG;
     const int t = threadIdx.x, tx = t & 15, r0 = (t >> 4) * 4;
+    // staged pair: mu^T and (1 / sigma^2)^T for fp32 inputs; (-mu / sigma)^T and (1 / sigma)^T for
+    // bf16 inputs, whose terms are then u = x / sigma - mu / sigma (one FMA) and u^2 (one more)
     const size_t HKD = (size_t)H * K * DR;
-    const float *muTh = inv_var + HKD + (size_t)h * DR * K, *ivTh = inv_var + 2 * HKD + (size_t)h * DR * K;
+    const float *muTh = inv_var + (PRECISE ? 1 : 4) * HKD + (size_t)h * DR * K;
+    const float *ivTh = inv_var + (PRECISE ? 2 : 3) * HKD + (size_t)h * DR * K;
     const float *ch = cst + (size_t)h * K;
 #pragma unroll 8
     for (int e = t; e < SEG * DR; e += THREADS) {
@@ -263,8 +270,8 @@ __global__ void __launch_bounds__(THREADS, sizeof(Tin) == 4 ? 2 : 3) simt_resp_k
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const float q = av[r] - mv[c];
-                        hi[r][c] = fmaf(q * q, wv[c], hi[r][c]);
+                        const float u = fmaf(av[r], wv[c], mv[c]);   // (x - mu) / sigma
+                        hi[r][c] = fmaf(u, u, hi[r][c]);
                     }
             }
 #pragma unroll
@@ -628,7 +635,7 @@ SimtLayout simt_layout(const gma_shape_t &s, int variant, int n_k)
     Carve c;
     const size_t rows = (size_t)s.B * s.H * s.N;
     const size_t rows_k = (size_t)s.B * s.H * n_k;
-    L.inv_var = c.take(3 * sizeof(float) * (size_t)s.H * s.K * s.d_r);   // 1/sigma^2, mu^T, (1/sigma^2)^T
+    L.inv_var = c.take(5 * sizeof(float) * (size_t)s.H * s.K * s.d_r);   // 1/sigma^2 and four transposes
     L.cst = c.take(sizeof(float) * (size_t)s.H * s.K);
     L.nseg = (n_k + SEG - 1) / SEG;
     if (variant != GMA_VARIANT_RESPONSIBILITIES) {
