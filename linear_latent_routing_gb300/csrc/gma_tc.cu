@@ -137,13 +137,13 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t &phase, WsHeade
 
 // ================================================================== kernels
 
-// Per head h (grid.x) and group of 16 components (grid.y): the Gaussian table (main part
+// Per head h (grid.x) and group of 8 components (grid.y): the Gaussian table (main part
 // log2e * [-w/2 ; mu w] as fp16, K-major SW128, kn16 rows; const part (c_hi, c_lo) with
 // c_hi + c_lo = c_k = log2e * (log pi_k - 1/2 sum_d (mu^2 w + log sigma^2)), K-major SW32) and
 // the fp32 constants cst[h][k] = c_k.  w = 1 / (softplus(raw) + floor), log pi = log softmax.
 // Padded components (k >= K) get zero rows.  Values beyond fp16 range are reported as
-// GMA_ERR_RANGE.  Each component is handled by 8 consecutive threads, one 16-byte feature chunk
-// at a time; their partial sums meet through warp shuffles.
+// GMA_ERR_RANGE.  Each component is handled by 16 consecutive threads (grid.y: groups of 8
+// components), one 16-byte feature chunk at a time; their partial sums meet through warp shuffles.
 __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restrict__ mu,
                                                             const float *__restrict__ raw,
                                                             const float *__restrict__ logits,
@@ -175,16 +175,16 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
     if ((threadIdx.x & 31) == 0) red[1][threadIdx.x >> 5] = sum;
     __syncthreads();
     const float lse = m + logf((red[1][0] + red[1][1]) + (red[1][2] + red[1][3]));
-    const int n = blockIdx.y * 16 + (threadIdx.x >> 3);   // component
+    const int n = blockIdx.y * 8 + (threadIdx.x >> 4);    // component
     uint8_t *img = bimg + (size_t)h * ntile * bimg_bytes + (size_t)(n / kn16) * bimg_bytes;
     const int nr = n % kn16;                               // its row in its tile's image
-    const int sub = threadIdx.x & 7;
+    const int sub = threadIdx.x & 15;
     const bool in_table = n < kn16 * ntile;
     const bool real = n < K;
     float acc = 0.f;
     bool range_ok = true;
     if (in_table) {
-        for (int q = sub; q < ka / 8; q += 8) {
+        for (int q = sub; q < ka / 8; q += 16) {
             // this chunk's raw variances and means, all loaded before any is used
             float rr[8], mm[8];
 #pragma unroll
@@ -224,10 +224,11 @@ __global__ void __launch_bounds__(THREADS) tc_params_kernel(const float *__restr
             *reinterpret_cast<uint4 *>(img + sw128(nr, q, kn16)) = v;
         }
     }
-    // sum the 8 partial sums of this component (lanes 8g .. 8g+7 of the warp)
+    // sum the 16 partial sums of this component (lanes 16g .. 16g+15 of the warp)
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 8);
     if (in_table && sub == 0) {
         const float c = real ? ((lh[n] - lse) - 0.5f * acc) * LOG2E : 0.f;
         if (!(fabsf(c) < 65504.f)) range_ok = false;
@@ -645,7 +646,7 @@ gma_status_t launch_params(const gma_shape_t &s, const Plan &p, char *ws, const 
                            const float *raw, const float *logits, cudaStream_t st)
 {
     GMA_LAUNCH(KID_TC_PARAMS, st,
-               (tc_params_kernel<<<dim3(s.H, p.ntile * p.kn16 / 16), THREADS, 0, st>>>(mu, raw, logits, (uint8_t *)(ws + p.off_bimg),
+               (tc_params_kernel<<<dim3(s.H, p.ntile * p.kn16 / 8), THREADS, 0, st>>>(mu, raw, logits, (uint8_t *)(ws + p.off_bimg),
                                                           (float *)(ws + p.off_cst), s.K, p.kn16, s.d_r,
                                                           p.bimg_bytes, p.bimg_main_bytes, p.ntile, s.var_floor, (WsHeader *)ws)));
     return GMA_OK;
