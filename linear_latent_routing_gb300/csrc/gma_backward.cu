@@ -60,7 +60,7 @@ template <int DV>
 __host__ __device__ constexpr int numden_smem_floats() { return 2 * KT * LT + KT * DV + KT + 2 * SEG; }
 
 template <int DV, typename Tin>
-__global__ void __launch_bounds__(BT, DV == 64 ? 3 : 2) bwd_numden_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
+__global__ void __launch_bounds__(BT, DV == 64 ? 4 : 2) bwd_numden_kernel(const float *__restrict__ gq, const float *__restrict__ gk,
                                                         const Tin *__restrict__ V, const float *__restrict__ agg,
                                                         const Tin *__restrict__ dO, float *__restrict__ dnd,
                                                         float *__restrict__ dagg, float *__restrict__ Pg, int N, int K,
