@@ -178,7 +178,7 @@ __host__ __device__ constexpr int resp_smem_floats() { return 3 * DR * RLD + RT;
 
 // blockIdx.y picks the side: routing vectors X0 (N0 per slice) into gamma0, or X1 (N1) into gamma1.
 template <int DR, typename Tin, typename Tout>
-__global__ void __launch_bounds__(THREADS, sizeof(Tin) == 4 ? 2 : 3) simt_resp_kernel(const Tin *__restrict__ X0, const Tin *__restrict__ X1,
+__global__ void __launch_bounds__(THREADS, sizeof(Tin) == 4 ? 2 : 4) simt_resp_kernel(const Tin *__restrict__ X0, const Tin *__restrict__ X1,
                                                               const float *__restrict__ mu,
                                                               const float *__restrict__ inv_var,
                                                               const float *__restrict__ cst, Tout *__restrict__ gamma0,
