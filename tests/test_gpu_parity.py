@@ -42,6 +42,10 @@ SMALL = [
     W.scaled(W.LRA_BIDIR, B=2, H=2, N=777),
     W.scaled(W.LONG_CAUSAL, B=1, H=2, N=1500),
     W.scaled(W.LONG_CAUSAL, B=1, H=1, N=700, causal=False),
+    # bidirectional read with TMA-stored output rows of two 64-column boxes: two slices and a
+    # ragged length, so that a box clipped wrongly at the first slice's end would write into the
+    # second slice's rows
+    W.scaled(W.LONG_CAUSAL, B=2, H=1, N=700, causal=False),
     W.scaled(W.LM_CAUSAL, B=1, H=1, N=1, K=16),
     W.scaled(W.LM_CAUSAL, B=1, H=1, N=129, K=1),
     W.scaled(W.LRA_BIDIR, B=1, H=1, N=130, K=1),
