@@ -15,13 +15,11 @@
 // memories, scanned), then per 64-token segment the in-segment (causal) terms explicitly and the
 // carried memory D or S for the rest, exactly as the forward read phase splits its work.
 //
-// Every contraction is a register-tiled product over shared-memory tiles: the 256 threads of a
-// block form a 16 x 16 grid, each thread holding 4 rows x (W / 16) columns of a 64-row output W
-// columns wide, and both operands are staged with the contracted index as their row, so that a
-// step of the product is one 16-byte load of four rows of A, one or two loads of B and 4 W / 16
-// FMAs.  Each product is formed in the orientation its consumer reads (P^T where the next product
-// contracts over keys, for instance), so no result is transposed in memory.  All sums run in a
-// fixed order (no atomics): repeated calls give identical bits.
+// Every contraction is a register-tiled product over shared-memory tiles (simt_tile.cuh).  Each is
+// formed in the orientation its consumer reads (P^T where the next product contracts over keys,
+// for instance); the query side's in-segment P^T and A^T tiles are also stored, and the key side
+// stages them back (transposed into shared memory) instead of forming them again.  All sums run
+// in a fixed order (no atomics): repeated calls give identical bits.
 #include "gma_internal.cuh"
 #include "simt_tile.cuh"
 #include "tc_ptx.cuh"
