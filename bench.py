@@ -84,9 +84,10 @@ def kernel_work(w, name):
         return "hbm", w.key_heads * esz * (w.d_r + w.d_v), "GB/s"
     if name == "tc_bidir_read":
         return "hbm", th * esz * (w.d_r + w.d_v), "GB/s"
-    if name == "tc_responsibilities":   # fp32 responsibilities when they feed the diagnostics
-        osz = 4 if w.name.startswith("usage_") else esz
-        return "hbm", th * (esz * w.d_r + osz * w.K), "GB/s"
+    if name == "tc_responsibilities":
+        if w.name.startswith("usage_"):   # the diagnostics pass: the rows read, one int32 assignment written
+            return "hbm", usage_bytes(w), "GB/s"
+        return "hbm", th * (esz * w.d_r + esz * w.K), "GB/s"
     if name == "usage_rows":
         return "hbm", th * (4 * w.K + 4), "GB/s"
     # backward (fp32 CUDA cores): flops of each kernel's arithmetic, in-segment (64-token) terms included
@@ -738,7 +739,7 @@ def run_usage(args, ws, rank, local):
     sh = stream.cuda_stream
 
     def step(xp=None):
-        r = gma.gma_usage(shape, (xp or X).data_ptr(), par["mu"].data_ptr(), par["raw"].data_ptr(),
+        r = gma.gma_usage(shape, (X if xp is None else xp).data_ptr(), par["mu"].data_ptr(), par["raw"].data_ptr(),
                           par["logits"].data_ptr(), out["assign"].data_ptr(), out["counts"].data_ptr(),
                           out["mass"].data_ptr(), out["used"].data_ptr(), out["entropy"].data_ptr(),
                           workspace.data_ptr(), ws_n, sh)

@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
         const int nb = base + C;
         load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, x);
         // softmax over the row in three passes over TMEM, 32 components at a time (the maximum,
-        // the sum, then the normalised values), so no thread holds the whole row in registers;
-        // with components in tiles, one pass: gamma = exp2(L - lse)
+        // the sum with the exponentials stored back, then the normalised values), so no thread
+        // holds the whole row in registers; with components in tiles, one pass: gamma = exp2(L - lse)
         float m = tiled ? lse : NEG_BIG;
         int arg = 0;   // the first component of largest responsibility
         float inv = 1.f;
@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
                 a.assign[(long long)bh * a.N + base + t] = arg;
                 atomicAdd(&hist[arg], 1);
             }
+            // the exponentials go back into the logits' columns, so the last pass only scales them
             float s = 0.f;
 #pragma unroll 1
             for (int c = 0; c < kc; ++c) {
@@ -361,9 +362,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
                 tmem_ld32(tmem + lane_off + c * 32, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c * 32 + j < a.K) s += ex2(__uint_as_float(r[j]) + cst[c * 32 + j] - m);
+                for (int j = 0; j < 32; ++j) {
+                    const float e = c * 32 + j < a.K ? ex2(__uint_as_float(r[j]) + cst[c * 32 + j] - m) : 0.f;
+                    s += e;
+                    r[j] = __float_as_uint(e);
+                }
+                tmem_st16(tmem + lane_off + c * 32, *reinterpret_cast<const uint32_t(*)[16]>(r));
+                tmem_st16(tmem + lane_off + c * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(r + 16));
             }
+            tmem_st_wait();
             inv = 1.0f / s;
         }
         // the tile's rows leave through shared memory, 32 components at a time, so that a warp's
@@ -378,17 +385,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int k = c * 32 + j;
-                stage[t * 33 + j] = k < a.K ? ex2(__uint_as_float(r[j]) + cst[k] - m) * inv : 0.f;
+                stage[t * 33 + j] = k >= a.K ? 0.f
+                                   : tiled ? ex2(__uint_as_float(r[j]) + cst[k] - m) * inv
+                                           : __uint_as_float(r[j]) * inv;   // (the stored exponential)
             }
             __syncthreads();
             const int ncol = min(32, a.K - c * 32);
             if (usage) {
-                // column sums of the tile (rows beyond the sequence hold zeros), one warp
-                if (t < 32) {
-                    float cs = 0.f;
-                    for (int rr = 0; rr < nrows; ++rr) cs += stage[rr * 33 + t];
-                    msum[c * 32 + t] += cs;
-                }
+                // column sums of the tile's rows: four threads per column (rows q, q + 4, ...),
+                // then two shuffles
+                const int j = t >> 2, q = t & 3;
+                float cs = 0.f;
+                for (int rr = q; rr < nrows; rr += 4) cs += stage[rr * 33 + j];
+                cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+                cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+                if (q == 0) msum[c * 32 + j] += cs;
             } else {
                 for (int e = t; e < nrows * 32; e += THREADS) {
                     const int rr = e >> 5, j = e & 31;
