@@ -279,6 +279,10 @@ __global__ void __launch_bounds__(256) tc_scan_kernel(float *__restrict__ agg, l
 }
 
 
+// The responsibilities kernel stages its output rows ([C][33] floats) in the [x^2, x] buffer when
+// that buffer (ka / 64 x 128 B x C) holds them: d_r >= 64.
+__host__ __device__ constexpr bool resp_stage_in_a(int d_r) { return (d_r * 2 < 64 ? 64 : d_r * 2) / 64 * 128 * C >= C * 33 * 4; }
+
 // Responsibilities only: gamma rows (normalised) straight from registers to global memory.
 template <int DR>
 __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
@@ -298,12 +302,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t sb = smem_u32(smem);
     float *cst = reinterpret_cast<float *>(smem + L.cst);
-    float *stage = reinterpret_cast<float *>(smem + ((L.total + 127u) & ~127u));   // [C][33]
-    // usage diagnostics: histogram and column sums of this CTA's rows
+    // the staging tile [C][33]: in the [x^2, x] buffer when that is large enough (it is free between
+    // the logits MMA and the next tile's build), else after the layout
+    constexpr bool STAGE_IN_A = resp_stage_in_a(DR);
+    uint8_t *extra = smem + ((L.total + 127u) & ~127u);
+    float *stage = reinterpret_cast<float *>(STAGE_IN_A ? smem + L.abuf : extra);
+    // usage diagnostics: histogram and column sums of this CTA's rows, and the column sums' partials
     const bool usage = a.assign != nullptr;
     const bool tiled = a.lse_q != nullptr;   // more than 128 components: this launch does one tile
-    int *hist = reinterpret_cast<int *>(stage + C * 33);
+    int *hist = reinterpret_cast<int *>(STAGE_IN_A ? extra : extra + (size_t)C * 33 * 4);
     float *msum = reinterpret_cast<float *>(hist + KMAX);
+    float *cpart = msum + KMAX;   // [4][32]
     if (usage) {
         for (int k = t; k < KMAX; k += THREADS) {
             hist[k] = 0;
@@ -392,14 +401,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
             __syncthreads();
             const int ncol = min(32, a.K - c * 32);
             if (usage) {
-                // column sums of the tile's rows: four threads per column (rows q, q + 4, ...),
-                // then two shuffles
-                const int j = t >> 2, q = t & 3;
+                // column sums of the tile's rows: each warp a quarter of the rows (q, q + 4, ...),
+                // one column per lane (conflict-free), then the four partials in order
+                const int j = t & 31, q = t >> 5;
                 float cs = 0.f;
+#pragma unroll 8
                 for (int rr = q; rr < nrows; rr += 4) cs += stage[rr * 33 + j];
-                cs += __shfl_xor_sync(0xffffffffu, cs, 1);
-                cs += __shfl_xor_sync(0xffffffffu, cs, 2);
-                if (q == 0) msum[c * 32 + j] += cs;
+                cpart[q * 32 + j] = cs;
+                __syncthreads();
+                if (t < 32) msum[c * 32 + t] += (cpart[t] + cpart[32 + t]) + (cpart[64 + t] + cpart[96 + t]);
             } else {
                 for (int e = t; e < nrows * 32; e += THREADS) {
                     const int rr = e >> 5, j = e & 31;
@@ -491,6 +501,24 @@ constexpr int kSms = 152;   // GB300
 uint32_t keysmall_smem(int d_r, int K, int d_v);   // gma_tc_keysmall.cu
 
 // The bidirectional key pass runs two CTAs per SM (gma_tc_keysmall.cu) where the shape allows.
+uint32_t smem_for(uint32_t need, uint32_t tmem_cols);
+
+// Dynamic shared memory of the responsibilities kernel (layout, staging tile unless it lives in the
+// [x^2, x] buffer, histogram, column sums and their partials), and its CTAs per SM (at most four:
+// 128 TMEM columns each).
+uint32_t resp_smem(int d_r, int kn16)
+{
+    const uint32_t base = (Smem(d_r, kn16, 16, false, false, false).total + 127u) & ~127u;
+    const uint32_t extra = (resp_stage_in_a(d_r) ? 0u : (uint32_t)C * 33u * 4u) + KMAX * 8u + 4u * 32u * 4u;
+    return smem_for(base + extra + 1024u, 128);
+}
+
+int resp_ctas_per_sm(int d_r, int kn16)
+{
+    const int n = (int)(228u * 1024u / resp_smem(d_r, kn16));
+    return n < 1 ? 1 : n > 4 ? 4 : n;
+}
+
 bool key_pass_small(const gma_shape_t &s, int variant)
 {
     return variant == GMA_VARIANT_BIDIRECTIONAL && s.K <= 64 && keysmall_smem(s.d_r, s.K, s.d_v) != 0;
@@ -516,8 +544,8 @@ Plan make_plan(const gma_shape_t &s, int variant, int per_sm = 0, int n_q = -1)
     // first chunk's loads) worth about 0.6 chunk; the cheapest split wins (the larger one on a
     // tie).
     if (variant == GMA_VARIANT_RESPONSIBILITIES) {
-        // up to four CTAs per SM (128 TMEM columns each): about four per SM in one wave
-        int n = (4 * kSms + BH - 1) / BH;
+        // as many CTAs as fit on the SMs at once (128 TMEM columns each, shared memory): one wave
+        int n = resp_ctas_per_sm(s.d_r, p.kn16) * kSms / BH;
         if (n > nchunks) n = nchunks;
         if (n < 1) n = 1;
         p.cps = (nchunks + n - 1) / n;
@@ -913,8 +941,7 @@ gma_status_t resp_dr(const gma_shape_t &s, const void *X, void *gamma, char *ws,
     a.assign = assign;
     a.counts = counts;
     a.mass_part = mass_part;
-    const uint32_t stage = (uint32_t)C * 33u * 4u + KMAX * 8u;   // the staging tile; usage sums
-    const uint32_t sm = smem_for(((Smem(DR, p.kn16, 16, false, false, false).total + 127u) & ~127u) + stage + 1024, 128);
+    const uint32_t sm = resp_smem(DR, p.kn16);
     if (!set_smem(tc_resp_kernel<DR>, sm)) return GMA_ERR_CUDA;
     if (p.ntile > 1) {
         float *lse = (float *)(ws + p.off_lse_q);
