@@ -338,27 +338,32 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
         const int nb = base + C;
         load_x<DR>(a.QX, (long long)bh * a.N + nb + t, nb + t < tok_end, x);
         // softmax over the row in three passes over TMEM, 32 components at a time (the maximum,
-        // the sum with the exponentials stored back, then the normalised values), so no thread
-        // holds the whole row in registers; with components in tiles, one pass: gamma = exp2(L - lse)
+        // with the logits plus their constants stored back; the sum, with the exponentials stored
+        // back; then the normalised values), so no thread holds the whole row in registers; with
+        // components in tiles, one pass: gamma = exp2(L - lse)
         float m = tiled ? lse : NEG_BIG;
         int arg = 0;   // the first component of largest responsibility
         float inv = 1.f;
         if (!tiled) {
+            // (the logits with their constants go back into TMEM for the next pass)
 #pragma unroll 1
             for (int c = 0; c < kc; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + c * 32, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c * 32 + j < a.K) {
-                        const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
-                        if (l > m) {
-                            m = l;
-                            arg = c * 32 + j;
-                        }
+                for (int j = 0; j < 32; ++j) {
+                    const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
+                    r[j] = __float_as_uint(l);
+                    if (c * 32 + j < a.K && l > m) {
+                        m = l;
+                        arg = c * 32 + j;
                     }
+                }
+                tmem_st16(tmem + lane_off + c * 32, *reinterpret_cast<const uint32_t(*)[16]>(r));
+                tmem_st16(tmem + lane_off + c * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(r + 16));
             }
+            tmem_st_wait();
             if (usage && valid) {
                 a.assign[(long long)bh * a.N + base + t] = arg;
                 atomicAdd(&hist[arg], 1);
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float e = c * 32 + j < a.K ? ex2(__uint_as_float(r[j]) + cst[c * 32 + j] - m) : 0.f;
+                    const float e = c * 32 + j < a.K ? ex2(__uint_as_float(r[j]) - m) : 0.f;
                     s += e;
                     r[j] = __float_as_uint(e);
                 }
