@@ -351,13 +351,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + c * 32, r);
                 tmem_ld_wait();
+                if (c * 32 + 32 <= a.K) {   // (a whole group: no bound tests)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
-                    r[j] = __float_as_uint(l);
-                    if (c * 32 + j < a.K && l > m) {
-                        m = l;
-                        arg = c * 32 + j;
+                    for (int j = 0; j < 32; ++j) {
+                        const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
+                        r[j] = __float_as_uint(l);
+                        if (l > m) {
+                            m = l;
+                            arg = c * 32 + j;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float l = __uint_as_float(r[j]) + cst[c * 32 + j];
+                        r[j] = __float_as_uint(l);
+                        if (c * 32 + j < a.K && l > m) {
+                            m = l;
+                            arg = c * 32 + j;
+                        }
                     }
                 }
                 tmem_st16(tmem + lane_off + c * 32, *reinterpret_cast<const uint32_t(*)[16]>(r));
@@ -375,11 +387,20 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + c * 32, r);
                 tmem_ld_wait();
+                if (c * 32 + 32 <= a.K) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float e = c * 32 + j < a.K ? ex2(__uint_as_float(r[j]) - m) : 0.f;
-                    s += e;
-                    r[j] = __float_as_uint(e);
+                    for (int j = 0; j < 32; ++j) {
+                        const float e = ex2(__uint_as_float(r[j]) - m);
+                        s += e;
+                        r[j] = __float_as_uint(e);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float e = c * 32 + j < a.K ? ex2(__uint_as_float(r[j]) - m) : 0.f;
+                        s += e;
+                        r[j] = __float_as_uint(e);
+                    }
                 }
                 tmem_st16(tmem + lane_off + c * 32, *reinterpret_cast<const uint32_t(*)[16]>(r));
                 tmem_st16(tmem + lane_off + c * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(r + 16));
@@ -396,12 +417,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_resp_kernel(const Args a)
             uint32_t r[32];
             tmem_ld32(tmem + lane_off + c * 32, r);
             tmem_ld_wait();
+            if (!tiled && c * 32 + 32 <= a.K) {   // (the stored exponentials of a whole group)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int k = c * 32 + j;
-                stage[t * 33 + j] = k >= a.K ? 0.f
-                                   : tiled ? ex2(__uint_as_float(r[j]) + cst[k] - m) * inv
-                                           : __uint_as_float(r[j]) * inv;   // (the stored exponential)
+                for (int j = 0; j < 32; ++j) stage[t * 33 + j] = __uint_as_float(r[j]) * inv;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int k = c * 32 + j;
+                    stage[t * 33 + j] = k >= a.K ? 0.f
+                                       : tiled ? ex2(__uint_as_float(r[j]) + cst[k] - m) * inv
+                                               : __uint_as_float(r[j]) * inv;   // (the stored exponential)
+                }
             }
             __syncthreads();
             const int ncol = min(32, a.K - c * 32);
