@@ -175,8 +175,11 @@ def test_recompute_flag_shrinks_workspace_and_matches():
     assert (a - b).abs().max().item() <= 2e-2 * float(np.abs(ref).max())
 
 
-def test_fp32_output_flag():
-    w = W.scaled(W.LM_CAUSAL, B=1, H=2, N=500)
+@pytest.mark.parametrize("w", [W.scaled(W.LM_CAUSAL, B=1, H=2, N=500), W.scaled(W.LRA_BIDIR, B=2, H=1, N=700)],
+                         ids=["causal", "bidir"])
+def test_fp32_output_flag(w):
+    """fp32 output rows (GMA_FLAG_OUT_F32): the threads' own stores, which the bidirectional read
+    takes instead of its TMA-stored bf16 boxes."""
     host = W.make_inputs(w)
     dev = to_device(host)
     O = gpu_forward(w, dev, flags=_gma().GMA_FLAG_OUT_F32)
