@@ -74,6 +74,9 @@ CASES = [
     # keeps the case well conditioned while it still checks the one-token code path
     W.scaled(W.LM_CAUSAL, B=1, H=1, N=1, K=16, dtype="f32", eps=0.1),
     W.scaled(W.LONG_CAUSAL, B=1, H=1, N=129, K=300, dtype="f32"),
+    # bf16 with two component tiles (K = 128): the softmax step on its own (row dot products, dL
+    # formed by the dx kernel) rather than folded into dGamma, and d_v = 128
+    W.scaled(W.LONG_CAUSAL, B=2, H=1, N=150),
 ]
 
 
