@@ -11,8 +11,11 @@
 // One CTA works through a flat list of 128-row chunks of two row sets (the queries and the keys
 // of a causal call).  Per chunk, [x^2, x] is built once in shared memory; the head's 128-component
 // table tiles stream through two shared-memory buffers (bulk copies), each tile's logits go into
-// one of two TMEM regions (the next tile's MMA is issued before the rows read the current one),
-// and one thread per row keeps a running maximum and sum over 32-column groups.
+// one of two TMEM regions (the next tile's MMA is issued before the rows read the current one).
+// Two threads share each row, one per half of every tile's columns: each keeps a running maximum
+// and sum, updated once per tile (the tile's maximum over eight independent chains, then its
+// exponentials summed over four), and the two halves are merged at the end of the chunk.  Eight
+// warps per CTA and two CTAs per SM keep the exponential units fed.
 #include "tc_rows.cuh"
 
 namespace gma {
@@ -20,12 +23,12 @@ namespace tck {
 
 namespace {
 
-constexpr int LTHREADS = 128;
+constexpr int LTHREADS = 256;   // two threads per row of a 128-row chunk
 constexpr int LSE_CTAS = 2 * 152;   // two CTAs per GB300 SM (shared memory and 256 TMEM columns each)
 enum LBar { L_TB0, L_TB1, L_MMA0, L_MMA1, L_NBAR };
 
 struct LseSmem {
-    uint32_t tb0, tb1, abuf, ax, bars, misc, total;
+    uint32_t tb0, tb1, abuf, ax, xch, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ LseSmem(int DR, int bimg_bytes)
     {
@@ -35,11 +38,45 @@ struct LseSmem {
         tb1 = o; o = al(o + (uint32_t)bimg_bytes);
         abuf = o; o = al(o + ka / 64u * 128u * (uint32_t)C);
         ax = o; o = al(o + (uint32_t)C * 32u);
+        xch = o; o += (uint32_t)C * 16u;   // the upper half's (max, sum, best logit, argmax) per row
         bars = o; o += L_NBAR * 8u;
         misc = o; o += 16u;
         total = o;
     }
 };
+
+// One thread's share of a tile: nv valid logits in ra then rb (NV: all 64 at compile time, or 0
+// for a count known only at run time) update the running maximum m and sum s of exp2(L - m), and
+// with want_arg the first column (index col0 + q) of largest logit.
+template <int NV>
+__device__ __forceinline__ void tile_update(const uint32_t (&ra)[32], const uint32_t (&rb)[32], int nv, float &m,
+                                            float &s, float &best, int &arg, int col0, bool want_arg)
+{
+    auto val = [&](int q) { return __uint_as_float(q < 32 ? ra[q] : rb[q - 32]); };
+    auto in = [&](int q) { return NV == 64 || q < nv; };
+    float mx[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mx[u] = NEG_BIG;
+#pragma unroll
+    for (int q = 0; q < 64; ++q)
+        if (in(q)) mx[q & 7] = fmaxf(mx[q & 7], val(q));
+    const float tm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    if (want_arg) {
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+            if (in(q) && val(q) > best) {
+                best = val(q);
+                arg = col0 + q;
+            }
+    }
+    const float mn = fmaxf(m, tm);
+    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 64; ++q)
+        if (in(q)) sa[q & 3] += ex2(val(q) - mn);
+    s = s * ex2(m - mn) + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
+    m = mn;
+}
 
 }  // namespace
 
@@ -49,7 +86,7 @@ struct LseSmem {
 // assign non-null (usage diagnostics of rows0) each row's argmax over all components (the lowest
 // index on ties) is written there and counted into counts [H][K_all].
 template <int DR>
-__global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
+__global__ void __launch_bounds__(LTHREADS, 2) tc_lse_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
                                                              float *lse0, float *lse1, int K_all, int BH,
                                                              int N1, int *assign, int *counts)
 {
@@ -60,6 +97,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
     volatile int *stop = reinterpret_cast<volatile int *>(smem + L.misc + 4);
     const int t = threadIdx.x, warp = t >> 5;
+    const int rt = t & (C - 1), half = t >> 7;   // this thread's row of the chunk, and its half of the columns
     const int ntile = (K_all + KMAX - 1) / KMAX;
     const int cpn0 = (a.N + C - 1) / C, cpn1 = (N1 + C - 1) / C;   // chunks per slice of each set
     const long long side_chunks = (long long)BH * cpn0;
@@ -69,7 +107,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 256);
-    {   // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
+    if (half == 0) {   // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
         const uint32_t one2 = 0x3C003C00u;   // fp16 pair (1, 1)
         const int flip = (t >> 2) & 1;
         *reinterpret_cast<uint4 *>(smem + L.ax + t * 32 + (flip << 4)) = make_uint4(one2, 0, 0, 0);
@@ -82,7 +120,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
-    const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t tb[2] = {L.tb0, L.tb1};
     uint32_t ph_tb[2] = {0, 0}, ph_mma[2] = {0, 0};   // (ph_tb: thread 0 alone loads and waits)
     bool pending[2] = {false, false};                 // thread 0: a table load not waited for yet
@@ -106,13 +144,13 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
         out = side ? lse1 : lse0;
     };
     int resident_h = -1;   // thread 0: the head whose two table images are in the buffers
-    uint4 x[DR / 8];       // this chunk's routing row, loaded during the chunk before
-    if (c_begin < c_end) {
+    uint4 x[DR / 8];       // this chunk's routing row, loaded during the chunk before (lower half)
+    if (c_begin < c_end && half == 0) {
         int bh0, tk0, n0;
         const bf16 *X0;
         float *o0;
         chunk_at(c_begin, bh0, tk0, n0, X0, o0);
-        load_x<DR>(X0, (long long)bh0 * n0 + tk0 + t, tk0 + t < n0, x);
+        load_x<DR>(X0, (long long)bh0 * n0 + tk0 + rt, tk0 + rt < n0, x);
     }
     for (long long c = c_begin; c < c_end; ++c) {
         int bh, tok0, nrow;
@@ -120,17 +158,17 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
         float *out;
         chunk_at(c, bh, tok0, nrow, X, out);
         const int h = bh % a.H;
-        const int row = tok0 + t;
+        const int row = tok0 + rt;
         const bool valid = row < nrow;
         const uint8_t *img = a.bimg + (size_t)h * a.bimg_head;
-        build_a<DR>(smem + L.abuf, t, x);
+        if (half == 0) build_a<DR>(smem + L.abuf, rt, x);
         fence_proxy_async_smem();
-        if (c + 1 < c_end) {   // the next chunk's row, in flight while this one is computed
+        if (c + 1 < c_end && half == 0) {   // the next chunk's row, in flight while this one is computed
             int bh1, tk1, n1;
             const bf16 *X1;
             float *o1;
             chunk_at(c + 1, bh1, tk1, n1, X1, o1);
-            load_x<DR>(X1, (long long)bh1 * n1 + tk1 + t, tk1 + t < n1, x);
+            load_x<DR>(X1, (long long)bh1 * n1 + tk1 + rt, tk1 + rt < n1, x);
         }
         if (t == 0 && !(ntile <= 2 && h == resident_h)) {
             for (int j = 0; j < 2 && j < ntile; ++j) {
@@ -177,42 +215,37 @@ __global__ void __launch_bounds__(LTHREADS, 1) tc_lse_kernel(const Args a, const
                 }
                 if (j + 1 < ntile) issue(j + 1);
             }
-            // running maximum and sum over this tile's valid components, 32 at a time
-            const int kvalid = min(KMAX, K_all - KMAX * j);
-#pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-                uint32_t r[32];
-                tmem_ld32(lane + 128u * b + 32u * g, r);   // (every lane loads: warp-collective)
-                tmem_ld_wait();
-                if (32 * g >= kvalid) continue;
-                float gm = NEG_BIG;
-#pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    if (32 * g + q < kvalid) gm = fmaxf(gm, __uint_as_float(r[q]));
-                if (assign) {   // the first component of largest logit
-#pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        if (32 * g + q < kvalid && __uint_as_float(r[q]) > best) {
-                            best = __uint_as_float(r[q]);
-                            arg = KMAX * j + 32 * g + q;
-                        }
-                }
-                const float mn = fmaxf(m, gm);
-                float gs = 0.f;
-#pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    if (32 * g + q < kvalid) gs += ex2(__uint_as_float(r[q]) - mn);
-                s = s * ex2(m - mn) + gs;
-                m = mn;
+            // this half's 64 columns of the tile: their maximum, then the running maximum and sum
+            const int nv = min(64, max(0, min(KMAX, K_all - KMAX * j) - 64 * half));
+            uint32_t ra[32], rb[32];
+            tmem_ld32(lane + 128u * b + 64u * half, ra);   // (every lane loads: warp-collective)
+            tmem_ld32(lane + 128u * b + 64u * half + 32u, rb);
+            tmem_ld_wait();
+            if (nv > 0) {
+                const int col0 = KMAX * j + 64 * half;
+                if (nv == 64)
+                    tile_update<64>(ra, rb, 64, m, s, best, arg, col0, assign != nullptr);
+                else
+                    tile_update<0>(ra, rb, nv, m, s, best, arg, col0, assign != nullptr);
             }
             tc_fence_before();
             __syncthreads();   // region b read by every row before the MMA of tile j + 2 writes it
             tc_fence_after();
         }
         if (*stop) break;
-        if (valid) {
-            out[(long long)bh * nrow + row] = m + log2f(s);
-            if (assign) {
+        // the upper half hands its row's state to the lower half (read before the lower half
+        // reaches the next chunk's first barrier, so one slot per row suffices)
+        float4 *xch = reinterpret_cast<float4 *>(smem + L.xch);
+        if (half) xch[rt] = make_float4(m, s, best, __int_as_float(arg));
+        __syncthreads();
+        if (!half && valid) {
+            const float4 o = xch[rt];
+            const float mm = fmaxf(m, o.x);
+            const float ss = s * ex2(m - mm) + o.y * ex2(o.x - mm);
+            out[(long long)bh * nrow + row] = mm + log2f(ss);
+            if (assign) {   // the larger logit; on a tie the lower component index
+                const int oarg = __float_as_int(o.w);
+                if (o.z > best || (o.z == best && oarg < arg)) arg = oarg;
                 assign[(long long)bh * nrow + row] = arg;
                 atomicAdd(counts + (size_t)h * K_all + arg, 1);
             }
