@@ -8,14 +8,28 @@
 // exp2(L_k - lse), where lse = log2 sum_j exp2(L_j) over all components is computed here first
 // (the table holds log2e-scaled logits, so everything is in the log2 domain).
 //
-// One CTA works through a flat list of 128-row chunks of two row sets (the queries and the keys
-// of a causal call).  Per chunk, [x^2, x] is built once in shared memory; the head's 128-component
-// table tiles stream through two shared-memory buffers (bulk copies), each tile's logits go into
-// one of two TMEM regions (the next tile's MMA is issued before the rows read the current one).
-// Two threads share each row, one per half of every tile's columns: each keeps a running maximum
-// and sum, updated once per tile (the tile's maximum over eight independent chains, then its
-// exponentials summed over four), and the two halves are merged at the end of the chunk.  Eight
-// warps per CTA and two CTAs per SM keep the exponential units fed.
+// Both kernels work through the list of 128-row chunks of two row sets (the queries and the keys
+// of a causal call), each CTA a contiguous share of it, so that consecutive chunks mostly share a
+// head.  Two threads share each row, one per half of every tile's columns: each keeps a running
+// maximum and sum, updated once per tile (the tile's maximum over eight independent chains, then
+// its exponentials summed over four), and the two halves merge at the end of the chunk.
+//
+// Two tiles (up to 256 components): tc_lse_resident_kernel, one CTA per SM, keeps both of a
+// head's table images in shared memory and runs a pipeline over its (chunk, tile) steps:
+//   control warp:  one lane issues each step's logits MMA into one of four 128-column TMEM
+//                  regions (a ring) as soon as the region is free and the chunk's [x^2, x] tile
+//                  is built, and loads a head's table images a step before their first use;
+//   reader warps:  eight: each loads its 64 logits of a step, frees the region at once, and
+//                  updates its row's state; the lower half also builds the next chunk's [x^2, x]
+//                  tile (two buffers) from rows loaded a chunk ahead, and merges the upper half's
+//                  state at the end of each chunk.
+// More tiles: tc_lse_stream_kernel, two CTAs per SM, streams the table images through two
+// buffers, tile by tile; per chunk, [x^2, x] is built once, each tile's logits go into one of two
+// TMEM regions, and the next tile's MMA is issued before the rows read the current one.  With
+// eight tiles per chunk its two CTAs per SM keep more loads and MMAs in flight than a pipelined
+// CTA streaming its tables through four buffers (measured at 1024 components: 384 us against
+// 621 us; at 256 components the resident pipeline takes 139 us, this kernel 170 us).
+// Every wait is bounded, and a timeout stops all roles.
 #include "tc_rows.cuh"
 
 namespace gma {
@@ -23,14 +37,15 @@ namespace tck {
 
 namespace {
 
-constexpr int LTHREADS = 256;   // two threads per row of a 128-row chunk
-constexpr int LSE_CTAS = 2 * 152;   // two CTAs per GB300 SM (shared memory and 256 TMEM columns each)
-enum LBar { L_TB0, L_TB1, L_MMA0, L_MMA1, L_NBAR };
+// ------------------------------------------------------------------ streamed tables
+constexpr int STHREADS = 256;   // two threads per row of a 128-row chunk
+constexpr int STREAM_CTAS = 2 * 152;   // two CTAs per GB300 SM (shared memory and 256 TMEM columns each)
+enum SBar { S_TB0, S_TB1, S_MMA0, S_MMA1, S_NBAR };
 
-struct LseSmem {
+struct StreamSmem {
     uint32_t tb0, tb1, abuf, ax, xch, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
-    __host__ __device__ LseSmem(int DR, int bimg_bytes)
+    __host__ __device__ StreamSmem(int DR, int bimg_bytes)
     {
         const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
         uint32_t o = 0;
@@ -39,6 +54,49 @@ struct LseSmem {
         abuf = o; o = al(o + ka / 64u * 128u * (uint32_t)C);
         ax = o; o = al(o + (uint32_t)C * 32u);
         xch = o; o += (uint32_t)C * 16u;   // the upper half's (max, sum, best logit, argmax) per row
+        bars = o; o += S_NBAR * 8u;
+        misc = o; o += 16u;
+        total = o;
+    }
+};
+
+// ------------------------------------------------------------------ resident tables, pipelined
+constexpr int RTHREADS = 288;   // eight reader warps (two threads per row of a chunk), one control warp
+constexpr int RESIDENT_CTAS = 152;   // one CTA per GB300 SM: four 128-column logits regions fill the TMEM
+constexpr int NREG = 4;         // TMEM regions in the ring
+constexpr int NTB = 2;          // table image buffers: the tiles of one head
+// TB: a table buffer is loaded (transaction bytes); FULL: a region's logits are complete (MMA
+// commit); FREE: every reader warp has loaded a region (8 arrivals); A: a chunk's [x^2, x] tile is
+// built (4: the lower half's warps); XF / XE: the upper half's row states are in the exchange
+// slot of a chunk parity / the lower half has read them (4 each); FIN: every MMA issued is done
+enum LBar { L_TB0, L_FIN = L_TB0 + NTB, L_FULL0, L_FREE0 = L_FULL0 + NREG, L_A0 = L_FREE0 + NREG, L_A1, L_XF0, L_XF1,
+            L_XE0, L_XE1, L_NBAR };
+
+// The control lane's record of a table buffer (in shared memory: indexed at run time, it would
+// otherwise live in local memory, which the small L1 left by this kernel's shared memory misses)
+struct TbState {
+    int last;         // last step whose MMA read the buffer (-1: none)
+    int h, j;         // head and tile the buffer holds (-1: none)
+    uint32_t ph;      // phase of its next load's completion
+    int pend;         // a load not waited for yet
+};
+
+struct ResidentSmem {
+    uint32_t tb0, tbstep, ab0, ab1, ax, xch, ctl, bars, misc, total;   // (table buffer b at tb0 + b tbstep)
+    __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    __host__ __device__ ResidentSmem(int DR, int bimg_bytes)
+    {
+        const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
+        uint32_t o = 0;
+        tb0 = o;
+        tbstep = al((uint32_t)bimg_bytes);
+        o += NTB * tbstep;
+        ab0 = o; o = al(o + ka / 64u * 128u * (uint32_t)C);   // [x^2, x] of even chunks
+        ab1 = o; o = al(o + ka / 64u * 128u * (uint32_t)C);   // and of odd ones
+        ax = o; o = al(o + (uint32_t)C * 32u);
+        xch = o; o += 2u * (uint32_t)C * 16u;   // the upper half's (max, sum, best logit, argmax) per row, by chunk parity
+        ctl = o; o += (uint32_t)(NTB * sizeof(TbState));
+        o = (o + 7u) & ~7u;
         bars = o; o += L_NBAR * 8u;
         misc = o; o += 16u;
         total = o;
@@ -78,6 +136,26 @@ __device__ __forceinline__ void tile_update(const uint32_t (&ra)[32], const uint
     m = mn;
 }
 
+// The chunk list: every 128-row chunk of every slice of the first row set, then of the second.
+struct ChunkInfo {
+    const bf16 *X;
+    float *out;
+    int bh, tok0, n;   // slice, first row, rows per slice
+};
+struct ChunkList {
+    const bf16 *rows0, *rows1;
+    float *lse0, *lse1;
+    long long side_chunks;   // chunks of the first set
+    int cpn0, cpn1, N0, N1;  // chunks per slice and rows per slice of each set
+    __device__ __forceinline__ ChunkInfo at(long long c) const
+    {
+        const bool side = c >= side_chunks;
+        const long long cc = side ? c - side_chunks : c;
+        const int cpn = side ? cpn1 : cpn0;
+        return ChunkInfo{side ? rows1 : rows0, side ? lse1 : lse0, (int)(cc / cpn), (int)(cc % cpn) * C, side ? N1 : N0};
+    }
+};
+
 }  // namespace
 
 // rows0 / rows1: the row sets (B*H slices of a.N and N1 rows of d_r bf16 each; rows1 may be null),
@@ -86,13 +164,13 @@ __device__ __forceinline__ void tile_update(const uint32_t (&ra)[32], const uint
 // assign non-null (usage diagnostics of rows0) each row's argmax over all components (the lowest
 // index on ties) is written there and counted into counts [H][K_all].
 template <int DR>
-__global__ void __launch_bounds__(LTHREADS, 2) tc_lse_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
+__global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
                                                              float *lse0, float *lse1, int K_all, int BH,
                                                              int N1, int *assign, int *counts)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const LseSmem L(DR, a.bimg_bytes);
+    const StreamSmem L(DR, a.bimg_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
     volatile int *stop = reinterpret_cast<volatile int *>(smem + L.misc + 4);
@@ -102,7 +180,7 @@ __global__ void __launch_bounds__(LTHREADS, 2) tc_lse_kernel(const Args a, const
     const int cpn0 = (a.N + C - 1) / C, cpn1 = (N1 + C - 1) / C;   // chunks per slice of each set
     const long long side_chunks = (long long)BH * cpn0;
     if (t == 0) {
-        for (int i = 0; i < L_NBAR; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < S_NBAR; ++i) mbar_init(bars + i, 1);
         *stop = 0;
         fence_mbar_init();
     }
@@ -121,9 +199,8 @@ __global__ void __launch_bounds__(LTHREADS, 2) tc_lse_kernel(const Args a, const
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
     const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t tb[2] = {L.tb0, L.tb1};
-    uint32_t ph_tb[2] = {0, 0}, ph_mma[2] = {0, 0};   // (ph_tb: thread 0 alone loads and waits)
-    bool pending[2] = {false, false};                 // thread 0: a table load not waited for yet
+    // phases and pending loads of the two buffers, one bit each (ph_tb, pending: thread 0 alone)
+    uint32_t ph_tb = 0, ph_mma = 0, pending = 0;
     const int main_bytes = a.bimg_main_bytes;
 
     // each CTA takes a contiguous range of the chunk list, so that consecutive chunks mostly share
@@ -172,9 +249,10 @@ __global__ void __launch_bounds__(LTHREADS, 2) tc_lse_kernel(const Args a, const
         }
         if (t == 0 && !(ntile <= 2 && h == resident_h)) {
             for (int j = 0; j < 2 && j < ntile; ++j) {
-                mbar_arrive_expect_tx(bars + L_TB0 + j, (uint32_t)a.bimg_bytes);
-                bulk_g2s(smem + tb[j], img + (size_t)j * a.bimg_bytes, (uint32_t)a.bimg_bytes, bars + L_TB0 + j);
-                pending[j] = true;
+                mbar_arrive_expect_tx(bars + S_TB0 + j, (uint32_t)a.bimg_bytes);
+                bulk_g2s(smem + (j ? L.tb1 : L.tb0), img + (size_t)j * a.bimg_bytes, (uint32_t)a.bimg_bytes,
+                         bars + S_TB0 + j);
+                pending |= 1u << j;
             }
             resident_h = ntile <= 2 ? h : -1;
         }
@@ -184,34 +262,34 @@ __global__ void __launch_bounds__(LTHREADS, 2) tc_lse_kernel(const Args a, const
         // thread 0: the logits of tile j, once its table is in
         auto issue = [&](int j) {
             const int b = j & 1;
-            if (pending[b]) {   // (with two tiles and the same head as before, nothing was loaded)
-                if (!mbar_wait(bars + L_TB0 + b, ph_tb[b], a.hdr, 60)) {
+            if ((pending >> b) & 1u) {   // (with two tiles and the same head as before, nothing was loaded)
+                if (!mbar_wait(bars + S_TB0 + b, (ph_tb >> b) & 1u, a.hdr, 60)) {
                     *stop = 1;
                     return;
                 }
-                ph_tb[b] ^= 1u;
-                pending[b] = false;
+                ph_tb ^= 1u << b;
+                pending &= ~(1u << b);
             }
             tc_fence_after();
-            issue_logits_c<DR>(tmem + 128u * b, sb + L.abuf, sb + tb[b], sb + tb[b] + (uint32_t)main_bytes, sb + L.ax,
-                               KMAX);
-            mma_commit(bars + L_MMA0 + b);
+            const uint32_t tbuf = sb + (b ? L.tb1 : L.tb0);
+            issue_logits_c<DR>(tmem + 128u * b, sb + L.abuf, tbuf, tbuf + (uint32_t)main_bytes, sb + L.ax, KMAX);
+            mma_commit(bars + S_MMA0 + b);
         };
         if (t == 0) issue(0);
         float m = NEG_BIG, s = 0.f, best = NEG_BIG;
         int arg = 0;
         for (int j = 0; j < ntile; ++j) {
             const int b = j & 1;
-            const bool ok = !*stop && mbar_wait(bars + L_MMA0 + b, ph_mma[b], a.hdr, 61);
-            ph_mma[b] ^= 1u;
+            const bool ok = !*stop && mbar_wait(bars + S_MMA0 + b, (ph_mma >> b) & 1u, a.hdr, 61);
+            ph_mma ^= 1u << b;
             if (__syncthreads_or(!ok)) break;
             tc_fence_after();
             if (t == 0) {
                 if (j + 2 < ntile) {   // this buffer's table has been read by the MMA just completed
-                    mbar_arrive_expect_tx(bars + L_TB0 + b, (uint32_t)a.bimg_bytes);
-                    bulk_g2s(smem + tb[b], img + (size_t)(j + 2) * a.bimg_bytes, (uint32_t)a.bimg_bytes,
-                             bars + L_TB0 + b);
-                    pending[b] = true;
+                    mbar_arrive_expect_tx(bars + S_TB0 + b, (uint32_t)a.bimg_bytes);
+                    bulk_g2s(smem + (b ? L.tb1 : L.tb0), img + (size_t)(j + 2) * a.bimg_bytes, (uint32_t)a.bimg_bytes,
+                             bars + S_TB0 + b);
+                    pending |= 1u << b;
                 }
                 if (j + 1 < ntile) issue(j + 1);
             }
@@ -255,33 +333,256 @@ __global__ void __launch_bounds__(LTHREADS, 2) tc_lse_kernel(const Args a, const
     // an MMA that was issued has completed or been waited for by every thread
     if (t == 0)
         for (int b = 0; b < 2; ++b)
-            if (pending[b]) mbar_wait(bars + L_TB0 + b, ph_tb[b], a.hdr, 62);
+            if ((pending >> b) & 1u) mbar_wait(bars + S_TB0 + b, (ph_tb >> b) & 1u, a.hdr, 62);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-uint32_t lse_smem(int d_r, int bimg_bytes)
+template <int DR>
+__global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
+                                                             float *lse0, float *lse1, int K_all, int BH,
+                                                             int N1, int *assign, int *counts)
 {
-    const uint32_t need = LseSmem(d_r, bimg_bytes).total + 1024;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const ResidentSmem L(DR, a.bimg_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
+    volatile int *stop = reinterpret_cast<volatile int *>(smem + L.misc + 4);
+    const int t = threadIdx.x, warp = t >> 5, lid = t & 31;
+    const int rt = t & (C - 1), half = (t >> 7) & 1;   // a reader's row of the chunk, and its half of the columns
+    const int ntile = (K_all + KMAX - 1) / KMAX;
+    const int cpn0 = (a.N + C - 1) / C, cpn1 = (N1 + C - 1) / C;   // chunks per slice of each set
+    const long long side_chunks = (long long)BH * cpn0;
+    if (t == 0) {
+        for (int i = 0; i < L_NBAR; ++i) {
+            const uint32_t n = (i >= L_FREE0 && i < L_FREE0 + NREG) ? 8u : (i >= L_A0) ? 4u : 1u;
+            mbar_init(bars + i, n);
+        }
+        *stop = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    if (t < C) {   // constant A operand of the logits: (1, 1, 0, ...) in every row, K-major SW32
+        const uint32_t one2 = 0x3C003C00u;   // fp16 pair (1, 1)
+        const int flip = (t >> 2) & 1;
+        *reinterpret_cast<uint4 *>(smem + L.ax + t * 32 + (flip << 4)) = make_uint4(one2, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(smem + L.ax + t * 32 + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
+    }
+    // each CTA takes a contiguous range of the chunk list, so that consecutive chunks mostly share
+    // a head: with two tiles, both table images then stay in shared memory from chunk to chunk
+    const int nsets = rows1 ? 2 : 1;
+    const long long total = side_chunks + (nsets > 1 ? (long long)BH * cpn1 : 0ll);
+    const long long per = (total + gridDim.x - 1) / gridDim.x;
+    const long long c_begin = (long long)blockIdx.x * per, c_end = min(total, c_begin + per);
+    const int nloc = c_end > c_begin ? (int)(c_end - c_begin) : 0;
+    const ChunkList cl{rows0, rows1, lse0, lse1, side_chunks, cpn0, cpn1, a.N, N1};
+    uint4 x[DR / 8];   // lower half: the row of the chunk whose [x^2, x] tile is built next
+#define LSE_FETCH_ROW(lc)                                                                                        \
+    do {                                                                                                         \
+        const ChunkInfo ci_ = cl.at(c_begin + (lc));                                                            \
+        load_x<DR>(ci_.X, (long long)ci_.bh * ci_.n + ci_.tok0 + rt, ci_.tok0 + rt < ci_.n, x);                  \
+    } while (0)
+    if (warp < 4 && nloc > 0) LSE_FETCH_ROW(0);   // (the rows are inputs: no kernel before writes them)
+    grid_dependency_wait();   // the tables come from the parameter kernel
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t sb = smem_u32(smem);
+    const int nf = nloc * ntile;   // steps: (chunk, tile) pairs
+
+    if (warp == 8) {
+        // ============================================================ control warp: MMAs, tables
+        if (lid == 0) {
+            TbState *tbs = reinterpret_cast<TbState *>(smem + L.ctl);
+            for (int b = 0; b < NTB; ++b) tbs[b] = TbState{-1, -1, -1, 0u, 0};
+            // table buffer of step f: its tile's own, f % ntile (both of a head's images resident);
+            // a head's images are loaded a step ahead of their first use
+            const int nbuf = ntile;
+            const int ahead = 1;
+            // One pass over the steps, `ahead` ahead of the MMAs: at g, the MMA of step g - ahead, then
+            // the table image of step g into its buffer unless it is there already.  (The load waits
+            // for the MMA that last read the buffer: the step before g - ahead + 1 at most, so its
+            // region's next MMA is not issued yet.)
+            bool ok = true, issued = false;
+            for (int g = 0; ok && g < nf + ahead; ++g) {
+                const int f = g - ahead;
+                if (f >= 0) {
+                    const int lc = f / ntile, j = f % ntile, r = f % NREG, b = f % nbuf;
+                    TbState &st = tbs[b];
+                    if (st.pend) {
+                        if (!(ok = mbar_wait_abortable(bars + L_TB0 + b, st.ph, a.hdr, 60, stop))) break;
+                        st.ph ^= 1u;
+                        st.pend = 0;
+                    }
+                    if (j == 0 &&
+                        !(ok = mbar_wait_abortable(bars + L_A0 + (lc & 1), (uint32_t)((lc >> 1) & 1), a.hdr, 64, stop)))
+                        break;
+                    if (f >= NREG &&
+                        !(ok = mbar_wait_abortable(bars + L_FREE0 + r, (uint32_t)((f / NREG - 1) & 1), a.hdr, 65, stop)))
+                        break;
+                    tc_fence_after();
+                    issue_logits_c<DR>(tmem + 128u * r, sb + ((lc & 1) ? L.ab1 : L.ab0), sb + (L.tb0 + (uint32_t)b * L.tbstep),
+                                       sb + (L.tb0 + (uint32_t)b * L.tbstep) + (uint32_t)a.bimg_main_bytes, sb + L.ax, KMAX);
+                    mma_commit(bars + L_FULL0 + r);
+                    issued = true;
+                    st.last = f;
+                }
+                if (g < nf) {
+                    const int b = g % nbuf, j = g % ntile;
+                    const int h = cl.at(c_begin + g / ntile).bh % a.H;
+                    TbState &st = tbs[b];
+                    if (st.h != h || st.j != j) {
+                        if (st.last >= 0 && !(ok = mbar_wait_abortable(bars + L_FULL0 + st.last % NREG,
+                                                                       (uint32_t)((st.last / NREG) & 1), a.hdr, 63, stop)))
+                            break;
+                        mbar_arrive_expect_tx(bars + L_TB0 + b, (uint32_t)a.bimg_bytes);
+                        bulk_g2s(smem + (L.tb0 + (uint32_t)b * L.tbstep), a.bimg + (size_t)h * a.bimg_head + (size_t)j * a.bimg_bytes,
+                                 (uint32_t)a.bimg_bytes, bars + L_TB0 + b);
+                        st.pend = 1;
+                        st.h = h;
+                        st.j = j;
+                    }
+                }
+            }
+            // table loads still in flight (only after a stop) complete before shared memory is released,
+            // and every MMA issued before the tensor memory is (one more commit, on a barrier of its own)
+            for (int b = 0; b < NTB; ++b)
+                if (tbs[b].pend) mbar_wait(bars + L_TB0 + b, tbs[b].ph, a.hdr, 62);
+            if (issued) {
+                mma_commit(bars + L_FIN);
+                mbar_wait(bars + L_FIN, 0, a.hdr, 68);
+            }
+        }
+    } else {
+        // ============================================================ readers
+        const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        float4 *xch = reinterpret_cast<float4 *>(smem + L.xch);
+        bool ok = true;
+        if (half == 0 && nloc > 0) {   // the first chunk's [x^2, x] tile, and the next chunk's rows in flight
+            build_a<DR>(smem + L.ab0, rt, x);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lid == 0) mbar_arrive(bars + L_A0);
+            if (nloc > 1) LSE_FETCH_ROW(1);
+        }
+        for (int lc = 0; ok && lc < nloc; ++lc) {
+            const ChunkInfo ci = cl.at(c_begin + lc);
+            const int bh = ci.bh, tok0 = ci.tok0, nrow = ci.n;
+            float *out = ci.out;
+            const int h = bh % a.H;
+            const int row = tok0 + rt;
+            const bool valid = row < nrow;
+            if (half == 0 && lc + 1 < nloc) {
+                // the next chunk's tile: its buffer was last read by the MMAs of chunk lc - 1, all of
+                // which this thread has seen complete
+                build_a<DR>(smem + (((lc + 1) & 1) ? L.ab1 : L.ab0), rt, x);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lid == 0) mbar_arrive(bars + L_A0 + ((lc + 1) & 1));
+                if (lc + 2 < nloc) LSE_FETCH_ROW(lc + 2);
+            }
+            float m = NEG_BIG, s = 0.f, best = NEG_BIG;
+            int arg = 0;
+            for (int j = 0; j < ntile; ++j) {
+                const int f = lc * ntile + j;
+                const int r = f % NREG;
+                if (!(ok = mbar_wait_abortable(bars + L_FULL0 + r, (uint32_t)((f / NREG) & 1), a.hdr, 61, stop))) break;
+                tc_fence_after();
+                uint32_t ra[32], rb[32];
+                tmem_ld32(lane + 128u * r + 64u * half, ra);
+                tmem_ld32(lane + 128u * r + 64u * half + 32u, rb);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lid == 0) mbar_arrive(bars + L_FREE0 + r);   // the region is free for the step four on
+                const int nv = min(64, max(0, min(KMAX, K_all - KMAX * j) - 64 * half));
+                if (nv > 0) {
+                    const int col0 = KMAX * j + 64 * half;
+                    if (nv == 64)
+                        tile_update<64>(ra, rb, 64, m, s, best, arg, col0, assign != nullptr);
+                    else
+                        tile_update<0>(ra, rb, nv, m, s, best, arg, col0, assign != nullptr);
+                }
+            }
+            if (!ok) break;
+            // the upper half hands its row's state to the lower half through the slot of this
+            // chunk's parity (free once the lower half has read it two chunks ago)
+            const int p = lc & 1;
+            if (half) {
+                if (lc >= 2 && !(ok = mbar_wait_abortable(bars + L_XE0 + p, (uint32_t)(((lc >> 1) - 1) & 1), a.hdr, 66, stop)))
+                    break;
+                xch[p * C + rt] = make_float4(m, s, best, __int_as_float(arg));
+                __syncwarp();
+                if (lid == 0) mbar_arrive(bars + L_XF0 + p);
+            } else {
+                if (!(ok = mbar_wait_abortable(bars + L_XF0 + p, (uint32_t)((lc >> 1) & 1), a.hdr, 67, stop))) break;
+                const float4 o = xch[p * C + rt];
+                __syncwarp();
+                if (lid == 0) mbar_arrive(bars + L_XE0 + p);
+                if (valid) {
+                    const float mm = fmaxf(m, o.x);
+                    const float ss = s * ex2(m - mm) + o.y * ex2(o.x - mm);
+                    out[(long long)bh * nrow + row] = mm + log2f(ss);
+                    if (assign) {   // the larger logit; on a tie the lower component index
+                        const int oarg = __float_as_int(o.w);
+                        if (o.z > best || (o.z == best && oarg < arg)) arg = oarg;
+                        assign[(long long)bh * nrow + row] = arg;
+                        atomicAdd(counts + (size_t)h * K_all + arg, 1);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+#undef LSE_FETCH_ROW
+}
+
+
+// Dynamic shared memory of each kernel (0 if it does not fit); the resident kernel's forces one
+// CTA per SM (it allocates all 512 TMEM columns).
+uint32_t lse_stream_smem(int d_r, int bimg_bytes)
+{
+    const uint32_t need = StreamSmem(d_r, bimg_bytes).total + 1024;
     return need <= 227u * 1024u ? smem_for(need, 256) : 0;
+}
+
+uint32_t lse_resident_smem(int d_r, int bimg_bytes)
+{
+    const uint32_t need = ResidentSmem(d_r, bimg_bytes).total + 1024;
+    return need <= 227u * 1024u ? smem_for(need, 512) : 0;
 }
 
 template <int DR>
 gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, float *lse0, float *lse1, int K_all,
                         int BH, cudaStream_t st, int *assign, int *counts, int N1)
 {
-    const uint32_t sm = lse_smem(DR, a.bimg_bytes);
-    if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
-    if (!set_smem(tc_lse_kernel<DR>, sm)) return GMA_ERR_CUDA;
     if (N1 < 0) N1 = a.N;
     const long long chunks = (long long)BH * ((a.N + C - 1) / C) + (rows1 ? (long long)BH * ((N1 + C - 1) / C) : 0ll);
-    const int grid = (int)(chunks < LSE_CTAS ? chunks : LSE_CTAS);
+    const bool resident = (K_all + KMAX - 1) / KMAX <= 2;
+    const uint32_t sm = resident ? lse_resident_smem(DR, a.bimg_bytes) : lse_stream_smem(DR, a.bimg_bytes);
+    if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     cudaError_t e = cudaSuccess;
-    GMA_LAUNCH(KID_TC_LSE, st,
-               (e = launch_pdl(tc_lse_kernel<DR>, dim3(grid), dim3(LTHREADS), sm, st, a, rows0, rows1, lse0, lse1,
-                               K_all, BH, N1, assign, counts)));
+    if (resident) {
+        if (!set_smem(tc_lse_resident_kernel<DR>, sm)) return GMA_ERR_CUDA;
+        const int grid = (int)(chunks < RESIDENT_CTAS ? chunks : RESIDENT_CTAS);
+        GMA_LAUNCH(KID_TC_LSE, st,
+                   (e = launch_pdl(tc_lse_resident_kernel<DR>, dim3(grid), dim3(RTHREADS), sm, st, a, rows0, rows1, lse0,
+                                   lse1, K_all, BH, N1, assign, counts)));
+    } else {
+        if (!set_smem(tc_lse_stream_kernel<DR>, sm)) return GMA_ERR_CUDA;
+        const int grid = (int)(chunks < STREAM_CTAS ? chunks : STREAM_CTAS);
+        GMA_LAUNCH(KID_TC_LSE, st,
+                   (e = launch_pdl(tc_lse_stream_kernel<DR>, dim3(grid), dim3(STHREADS), sm, st, a, rows0, rows1, lse0,
+                                   lse1, K_all, BH, N1, assign, counts)));
+    }
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
