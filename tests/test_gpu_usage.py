@@ -78,6 +78,10 @@ CASES = [
     W.scaled(W.K_SWEEP[3], B=1, H=1, N=300),
     W.scaled(W.LM_CAUSAL, B=1, H=2, N=257, d_r=128, K=48),
     W.scaled(W.LM_CAUSAL, B=2, H=2, N=500, d_r=32, K=300),   # tensor cores, components in tiles
+    # two tiles: the pre-pass keeps both tables resident and pipelines its steps (argmax and counts
+    # merged from the two halves of each row); a partial second tile, then exactly two full ones
+    W.scaled(W.LM_CAUSAL, B=2, H=2, N=777, K=200),
+    W.scaled(W.LM_CAUSAL, B=1, H=2, N=300, K=256),
 ]
 
 
