@@ -14,21 +14,21 @@
 // maximum and sum, updated once per tile (the tile's maximum over eight independent chains, then
 // its exponentials summed over four), and the two halves merge at the end of the chunk.
 //
-// Two tiles (up to 256 components): tc_lse_resident_kernel, one CTA per SM, keeps both of a
-// head's table images in shared memory and runs a pipeline over its (chunk, tile) steps:
-//   control warp:  one lane issues each step's logits MMA into one of four 128-column TMEM
-//                  regions (a ring) as soon as the region is free and the chunk's [x^2, x] tile
-//                  is built, and loads a head's table images a step before their first use;
-//   reader warps:  eight: each loads its 64 logits of a step, frees the region at once, and
-//                  updates its row's state; the lower half also builds the next chunk's [x^2, x]
-//                  tile (two buffers) from rows loaded a chunk ahead, and merges the upper half's
-//                  state at the end of each chunk.
+// Two tiles (129 to 256 components): tc_lse_resident_kernel, one CTA per SM, keeps a head's table
+// in shared memory as one N = 256 operand and runs a pipeline over its chunks:
+//   control warp:  one lane issues each chunk's logits (one MMA chain for both tiles) into one of
+//                  two 256-column TMEM regions, as soon as the region is free and the chunk's
+//                  [x^2, x] tile is built, and loads the table when the head changes;
+//   reader warps:  eight: each loads its tile's 128 logits of a chunk, 64 at a time, frees the
+//                  region, and updates its row's state; the lower half also builds the next
+//                  chunk's [x^2, x] tile (two buffers) from rows loaded a chunk ahead, and merges
+//                  the upper half's state at the end of each chunk.
 // More tiles: tc_lse_stream_kernel, two CTAs per SM, streams the table images through two
 // buffers, tile by tile; per chunk, [x^2, x] is built once, each tile's logits go into one of two
 // TMEM regions, and the next tile's MMA is issued before the rows read the current one.  With
 // eight tiles per chunk its two CTAs per SM keep more loads and MMAs in flight than a pipelined
 // CTA streaming its tables through four buffers (measured at 1024 components: 384 us against
-// 621 us; at 256 components the resident pipeline takes 139 us, this kernel 170 us).
+// 621 us; at 256 components the resident pipeline takes 103 us, this kernel 170 us).
 // Every wait is bounded, and a timeout stops all roles.
 #include "tc_rows.cuh"
 
@@ -62,41 +62,30 @@ struct StreamSmem {
 
 // ------------------------------------------------------------------ resident tables, pipelined
 constexpr int RTHREADS = 288;   // eight reader warps (two threads per row of a chunk), one control warp
-constexpr int RESIDENT_CTAS = 152;   // one CTA per GB300 SM: four 128-column logits regions fill the TMEM
-constexpr int NREG = 4;         // TMEM regions in the ring
-constexpr int NTB = 2;          // table image buffers: the tiles of one head
-// TB: a table buffer is loaded (transaction bytes); FULL: a region's logits are complete (MMA
-// commit); FREE: every reader warp has loaded a region (8 arrivals); A: a chunk's [x^2, x] tile is
-// built (4: the lower half's warps); XF / XE: the upper half's row states are in the exchange
-// slot of a chunk parity / the lower half has read them (4 each); FIN: every MMA issued is done
-enum LBar { L_TB0, L_FIN = L_TB0 + NTB, L_FULL0, L_FREE0 = L_FULL0 + NREG, L_A0 = L_FREE0 + NREG, L_A1, L_XF0, L_XF1,
-            L_XE0, L_XE1, L_NBAR };
+constexpr int RESIDENT_CTAS = 152;   // one CTA per GB300 SM: two 256-column logits regions fill the TMEM
+constexpr int NREG = 2;         // TMEM regions in the ring (one chunk's 256 logits each)
+// TB: the table is loaded (transaction bytes); FULL: a region's logits are complete (MMA commit);
+// FREE: every reader warp has loaded a region (8 arrivals); A: a chunk's [x^2, x] tile is built
+// (4: the lower half's warps); XF / XE: the upper half's row states are in the exchange slot of a
+// chunk parity / the lower half has read them (4 each); FIN: every MMA issued is done
+enum LBar { L_TB, L_FIN, L_FULL0, L_FREE0 = L_FULL0 + NREG, L_A0 = L_FREE0 + NREG, L_A1, L_XF0, L_XF1, L_XE0, L_XE1,
+            L_NBAR };
 
-// The control lane's record of a table buffer (in shared memory: indexed at run time, it would
-// otherwise live in local memory, which the small L1 left by this kernel's shared memory misses)
-struct TbState {
-    int last;         // last step whose MMA read the buffer (-1: none)
-    int h, j;         // head and tile the buffer holds (-1: none)
-    uint32_t ph;      // phase of its next load's completion
-    int pend;         // a load not waited for yet
-};
-
+// The two tiles of a head's table as one N = 256 operand: each 64-column block of the [x^2, x]
+// part holds tile 0's 128 rows, then tile 1's (so that one MMA chain covers both), and the constant
+// part holds both tiles' rows in order.
 struct ResidentSmem {
-    uint32_t tb0, tbstep, ab0, ab1, ax, xch, ctl, bars, misc, total;   // (table buffer b at tb0 + b tbstep)
+    uint32_t tab, ab0, ab1, ax, xch, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ ResidentSmem(int DR, int bimg_bytes)
     {
         const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
         uint32_t o = 0;
-        tb0 = o;
-        tbstep = al((uint32_t)bimg_bytes);
-        o += NTB * tbstep;
+        tab = o; o = al(o + 2u * (uint32_t)bimg_bytes);
         ab0 = o; o = al(o + ka / 64u * 128u * (uint32_t)C);   // [x^2, x] of even chunks
         ab1 = o; o = al(o + ka / 64u * 128u * (uint32_t)C);   // and of odd ones
         ax = o; o = al(o + (uint32_t)C * 32u);
         xch = o; o += 2u * (uint32_t)C * 16u;   // the upper half's (max, sum, best logit, argmax) per row, by chunk parity
-        ctl = o; o += (uint32_t)(NTB * sizeof(TbState));
-        o = (o + 7u) & ~7u;
         bars = o; o += L_NBAR * 8u;
         misc = o; o += 16u;
         total = o;
@@ -353,7 +342,6 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
     volatile int *stop = reinterpret_cast<volatile int *>(smem + L.misc + 4);
     const int t = threadIdx.x, warp = t >> 5, lid = t & 31;
     const int rt = t & (C - 1), half = (t >> 7) & 1;   // a reader's row of the chunk, and its half of the columns
-    const int ntile = (K_all + KMAX - 1) / KMAX;
     const int cpn0 = (a.N + C - 1) / C, cpn1 = (N1 + C - 1) / C;   // chunks per slice of each set
     const long long side_chunks = (long long)BH * cpn0;
     if (t == 0) {
@@ -393,66 +381,58 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
-    const int nf = nloc * ntile;   // steps: (chunk, tile) pairs
+    const int main_bytes = a.bimg_main_bytes, blk = 128 * 128;   // (one tile's 64-column block: 16 KB)
 
     if (warp == 8) {
-        // ============================================================ control warp: MMAs, tables
+        // ============================================================ control warp: MMAs, table
         if (lid == 0) {
-            TbState *tbs = reinterpret_cast<TbState *>(smem + L.ctl);
-            for (int b = 0; b < NTB; ++b) tbs[b] = TbState{-1, -1, -1, 0u, 0};
-            // table buffer of step f: its tile's own, f % ntile (both of a head's images resident);
-            // a head's images are loaded a step ahead of their first use
-            const int nbuf = ntile;
-            const int ahead = 1;
-            // One pass over the steps, `ahead` ahead of the MMAs: at g, the MMA of step g - ahead, then
-            // the table image of step g into its buffer unless it is there already.  (The load waits
-            // for the MMA that last read the buffer: the step before g - ahead + 1 at most, so its
-            // region's next MMA is not issued yet.)
+            int res_h = -1;               // head whose table is in shared memory
+            bool pend = false;            // its load not waited for yet
+            uint32_t ph_tb = 0;
             bool ok = true, issued = false;
-            for (int g = 0; ok && g < nf + ahead; ++g) {
-                const int f = g - ahead;
-                if (f >= 0) {
-                    const int lc = f / ntile, j = f % ntile, r = f % NREG, b = f % nbuf;
-                    TbState &st = tbs[b];
-                    if (st.pend) {
-                        if (!(ok = mbar_wait_abortable(bars + L_TB0 + b, st.ph, a.hdr, 60, stop))) break;
-                        st.ph ^= 1u;
-                        st.pend = 0;
-                    }
-                    if (j == 0 &&
-                        !(ok = mbar_wait_abortable(bars + L_A0 + (lc & 1), (uint32_t)((lc >> 1) & 1), a.hdr, 64, stop)))
-                        break;
-                    if (f >= NREG &&
-                        !(ok = mbar_wait_abortable(bars + L_FREE0 + r, (uint32_t)((f / NREG - 1) & 1), a.hdr, 65, stop)))
-                        break;
-                    tc_fence_after();
-                    issue_logits_c<DR>(tmem + 128u * r, sb + ((lc & 1) ? L.ab1 : L.ab0), sb + (L.tb0 + (uint32_t)b * L.tbstep),
-                                       sb + (L.tb0 + (uint32_t)b * L.tbstep) + (uint32_t)a.bimg_main_bytes, sb + L.ax, KMAX);
-                    mma_commit(bars + L_FULL0 + r);
-                    issued = true;
-                    st.last = f;
+            // the table of chunk lc's head, unless it is there already (after the MMA of the chunk
+            // before, the last to read the old one)
+            auto load_table = [&](int lc) -> bool {
+                const int h = cl.at(c_begin + lc).bh % a.H;
+                if (h == res_h) return true;
+                if (lc > 0 && !mbar_wait_abortable(bars + L_FULL0 + ((lc - 1) & 1), (uint32_t)(((lc - 1) >> 1) & 1),
+                                                   a.hdr, 63, stop))
+                    return false;
+                const uint8_t *img = a.bimg + (size_t)h * a.bimg_head;
+                mbar_arrive_expect_tx(bars + L_TB, 2u * (uint32_t)a.bimg_bytes);
+                for (int t2 = 0; t2 < 2; ++t2) {
+                    const uint8_t *src = img + (size_t)t2 * a.bimg_bytes;
+                    for (int q = 0; q < main_bytes / blk; ++q)
+                        bulk_g2s(smem + L.tab + (uint32_t)(q * 2 * blk + t2 * blk), src + (size_t)q * blk, (uint32_t)blk,
+                                 bars + L_TB);
+                    bulk_g2s(smem + L.tab + (uint32_t)(2 * main_bytes + t2 * 128 * 32), src + main_bytes, 128u * 32u,
+                             bars + L_TB);
                 }
-                if (g < nf) {
-                    const int b = g % nbuf, j = g % ntile;
-                    const int h = cl.at(c_begin + g / ntile).bh % a.H;
-                    TbState &st = tbs[b];
-                    if (st.h != h || st.j != j) {
-                        if (st.last >= 0 && !(ok = mbar_wait_abortable(bars + L_FULL0 + st.last % NREG,
-                                                                       (uint32_t)((st.last / NREG) & 1), a.hdr, 63, stop)))
-                            break;
-                        mbar_arrive_expect_tx(bars + L_TB0 + b, (uint32_t)a.bimg_bytes);
-                        bulk_g2s(smem + (L.tb0 + (uint32_t)b * L.tbstep), a.bimg + (size_t)h * a.bimg_head + (size_t)j * a.bimg_bytes,
-                                 (uint32_t)a.bimg_bytes, bars + L_TB0 + b);
-                        st.pend = 1;
-                        st.h = h;
-                        st.j = j;
-                    }
+                pend = true;
+                res_h = h;
+                return true;
+            };
+            for (int lc = 0; ok && lc < nloc; ++lc) {
+                const int r = lc & 1;
+                if (!(ok = load_table(lc))) break;
+                if (pend) {
+                    if (!(ok = mbar_wait_abortable(bars + L_TB, ph_tb, a.hdr, 60, stop))) break;
+                    ph_tb ^= 1u;
+                    pend = false;
                 }
+                if (!(ok = mbar_wait_abortable(bars + L_A0 + r, (uint32_t)((lc >> 1) & 1), a.hdr, 64, stop))) break;
+                if (lc >= NREG &&
+                    !(ok = mbar_wait_abortable(bars + L_FREE0 + r, (uint32_t)(((lc >> 1) - 1) & 1), a.hdr, 65, stop)))
+                    break;
+                tc_fence_after();
+                issue_logits_c<DR>(tmem + 256u * r, sb + (r ? L.ab1 : L.ab0), sb + L.tab, sb + L.tab + 2u * (uint32_t)main_bytes,
+                                   sb + L.ax, 2 * KMAX);
+                mma_commit(bars + L_FULL0 + r);
+                issued = true;
             }
-            // table loads still in flight (only after a stop) complete before shared memory is released,
-            // and every MMA issued before the tensor memory is (one more commit, on a barrier of its own)
-            for (int b = 0; b < NTB; ++b)
-                if (tbs[b].pend) mbar_wait(bars + L_TB0 + b, tbs[b].ph, a.hdr, 62);
+            // the table load still in flight (only after a stop) completes before shared memory is
+            // released, and every MMA issued before the tensor memory is
+            if (pend) mbar_wait(bars + L_TB, ph_tb, a.hdr, 62);
             if (issued) {
                 mma_commit(bars + L_FIN);
                 mbar_wait(bars + L_FIN, 0, a.hdr, 68);
@@ -477,9 +457,10 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
             const int h = bh % a.H;
             const int row = tok0 + rt;
             const bool valid = row < nrow;
+            const int r = lc & 1;
             if (half == 0 && lc + 1 < nloc) {
-                // the next chunk's tile: its buffer was last read by the MMAs of chunk lc - 1, all of
-                // which this thread has seen complete
+                // the next chunk's tile: its buffer was last read by the MMAs of chunk lc - 1, which
+                // this thread has seen complete
                 build_a<DR>(smem + (((lc + 1) & 1) ? L.ab1 : L.ab0), rt, x);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -488,28 +469,31 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
             }
             float m = NEG_BIG, s = 0.f, best = NEG_BIG;
             int arg = 0;
-            for (int j = 0; j < ntile; ++j) {
-                const int f = lc * ntile + j;
-                const int r = f % NREG;
-                if (!(ok = mbar_wait_abortable(bars + L_FULL0 + r, (uint32_t)((f / NREG) & 1), a.hdr, 61, stop))) break;
-                tc_fence_after();
+            if (!(ok = mbar_wait_abortable(bars + L_FULL0 + r, (uint32_t)((lc >> 1) & 1), a.hdr, 61, stop))) break;
+            tc_fence_after();
+            // this half's tile (128 columns of the region), 64 at a time; the region is freed once
+            // both loads are in registers
+            const int kv = min(KMAX, K_all - KMAX * half);   // valid components of the tile
+            for (int sub = 0; sub < 2; ++sub) {
                 uint32_t ra[32], rb[32];
-                tmem_ld32(lane + 128u * r + 64u * half, ra);
-                tmem_ld32(lane + 128u * r + 64u * half + 32u, rb);
+                const uint32_t col = 256u * r + 128u * half + 64u * sub;
+                tmem_ld32(lane + col, ra);
+                tmem_ld32(lane + col + 32u, rb);
                 tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lid == 0) mbar_arrive(bars + L_FREE0 + r);   // the region is free for the step four on
-                const int nv = min(64, max(0, min(KMAX, K_all - KMAX * j) - 64 * half));
+                if (sub == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lid == 0) mbar_arrive(bars + L_FREE0 + r);
+                }
+                const int nv = min(64, max(0, kv - 64 * sub));
                 if (nv > 0) {
-                    const int col0 = KMAX * j + 64 * half;
+                    const int col0 = KMAX * half + 64 * sub;
                     if (nv == 64)
                         tile_update<64>(ra, rb, 64, m, s, best, arg, col0, assign != nullptr);
                     else
                         tile_update<0>(ra, rb, nv, m, s, best, arg, col0, assign != nullptr);
                 }
             }
-            if (!ok) break;
             // the upper half hands its row's state to the lower half through the slot of this
             // chunk's parity (free once the lower half has read it two chunks ago)
             const int p = lc & 1;
@@ -566,7 +550,7 @@ gma_status_t launch_lse(const Args &a, const bf16 *rows0, const bf16 *rows1, flo
 {
     if (N1 < 0) N1 = a.N;
     const long long chunks = (long long)BH * ((a.N + C - 1) / C) + (rows1 ? (long long)BH * ((N1 + C - 1) / C) : 0ll);
-    const bool resident = (K_all + KMAX - 1) / KMAX <= 2;
+    const bool resident = (K_all + KMAX - 1) / KMAX == 2;
     const uint32_t sm = resident ? lse_resident_smem(DR, a.bimg_bytes) : lse_stream_smem(DR, a.bimg_bytes);
     if (sm == 0) return GMA_ERR_UNSUPPORTED_SHAPE;
     cudaError_t e = cudaSuccess;
