@@ -10,9 +10,9 @@
 //
 // Both kernels work through the list of 128-row chunks of two row sets (the queries and the keys
 // of a causal call), each CTA a contiguous share of it, so that consecutive chunks mostly share a
-// head.  Two threads share each row, one per half of every tile's columns: each keeps a running
-// maximum and sum, updated once per tile (the tile's maximum over eight independent chains, then
-// its exponentials summed over four), and the two halves merge at the end of the chunk.
+// head.  Two threads share each row, each with a share of the row's columns: each keeps a running
+// maximum and sum, updated once per 64 of its columns (their maximum over eight independent
+// chains, then their exponentials summed over four), and the two merge at the end of the chunk.
 //
 // Two tiles (129 to 256 components): tc_lse_resident_kernel, one CTA per SM, keeps a head's table
 // in shared memory as one N = 256 operand and runs a pipeline over its chunks:
