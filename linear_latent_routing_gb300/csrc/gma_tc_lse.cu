@@ -23,12 +23,12 @@
 //                  region, and updates its row's state; the lower half also builds the next
 //                  chunk's [x^2, x] tile (two buffers) from rows loaded a chunk ahead, and merges
 //                  the upper half's state at the end of each chunk.
-// More tiles: tc_lse_stream_kernel, two CTAs per SM, streams the table images through two
-// buffers, tile by tile; per chunk, [x^2, x] is built once, each tile's logits go into one of two
-// TMEM regions, and the next tile's MMA is issued before the rows read the current one.  With
-// eight tiles per chunk its two CTAs per SM keep more loads and MMAs in flight than a pipelined
-// CTA streaming its tables through four buffers (measured at 1024 components: 384 us against
-// 621 us; at 256 components the resident pipeline takes 103 us, this kernel 170 us).
+// More tiles: tc_lse_stream_kernel, two CTAs per SM, streams the table images a pair of tiles at a
+// time through one buffer, in the same N = 256 layout: per chunk, [x^2, x] is built once; per
+// pair, one MMA chain fills the CTA's 256 TMEM columns, and the next pair's images load while the
+// rows read them.  Two CTAs per SM overlap one another's waits (measured at 1024 components:
+// 347 us, against 384 us streaming single tiles through two buffers, and 621 us for a pipelined
+// CTA per SM streaming single tiles through four).
 // Every wait is bounded, and a timeout stops all roles.
 #include "tc_rows.cuh"
 
@@ -37,20 +37,19 @@ namespace tck {
 
 namespace {
 
-// ------------------------------------------------------------------ streamed tables
+// ------------------------------------------------------------------ streamed tables, in pairs
 constexpr int STHREADS = 256;   // two threads per row of a 128-row chunk
 constexpr int STREAM_CTAS = 2 * 152;   // two CTAs per GB300 SM (shared memory and 256 TMEM columns each)
-enum SBar { S_TB0, S_TB1, S_MMA0, S_MMA1, S_NBAR };
+enum SBar { S_TB, S_MMA, S_NBAR };
 
 struct StreamSmem {
-    uint32_t tb0, tb1, abuf, ax, xch, bars, misc, total;
+    uint32_t tab, abuf, ax, xch, bars, misc, total;
     __host__ __device__ static uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
     __host__ __device__ StreamSmem(int DR, int bimg_bytes)
     {
         const uint32_t ka = DR * 2 < 64 ? 64u : (uint32_t)DR * 2u;
         uint32_t o = 0;
-        tb0 = o; o = al(o + (uint32_t)bimg_bytes);
-        tb1 = o; o = al(o + (uint32_t)bimg_bytes);
+        tab = o; o = al(o + 2u * (uint32_t)bimg_bytes);   // a pair of tiles as one N = 256 operand
         abuf = o; o = al(o + ka / 64u * 128u * (uint32_t)C);
         ax = o; o = al(o + (uint32_t)C * 32u);
         xch = o; o += (uint32_t)C * 16u;   // the upper half's (max, sum, best logit, argmax) per row
@@ -145,6 +144,24 @@ struct ChunkList {
     }
 };
 
+// Tiles 2 j and 2 j + 1 (the second if there is one) of a head's table images (img) into tab as one
+// N = 256 operand: each 64-column block of the [x^2, x] part holds the first tile's 128 rows, then
+// the second's; the constant part holds both tiles' rows in order.  One thread; the bytes complete
+// on bar.
+__device__ __forceinline__ void load_table_pair(uint8_t *tab, const uint8_t *img, int bimg_bytes, int main_bytes,
+                                                int ntile, int j, uint64_t *bar)
+{
+    constexpr int BLK = 128 * 128;   // one tile's 64-column block: 128 rows of 128 bytes
+    const int nt = ntile - 2 * j < 2 ? ntile - 2 * j : 2;
+    mbar_arrive_expect_tx(bar, (uint32_t)(nt * bimg_bytes));
+    for (int t2 = 0; t2 < nt; ++t2) {
+        const uint8_t *src = img + (size_t)(2 * j + t2) * bimg_bytes;
+        for (int q = 0; q < main_bytes / BLK; ++q)
+            bulk_g2s(tab + q * 2 * BLK + t2 * BLK, src + (size_t)q * BLK, (uint32_t)BLK, bar);
+        bulk_g2s(tab + 2 * main_bytes + t2 * 128 * 32, src + main_bytes, 128u * 32u, bar);
+    }
+}
+
 }  // namespace
 
 // rows0 / rows1: the row sets (B*H slices of a.N and N1 rows of d_r bf16 each; rows1 may be null),
@@ -154,8 +171,8 @@ struct ChunkList {
 // index on ties) is written there and counted into counts [H][K_all].
 template <int DR>
 __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a, const bf16 *rows0, const bf16 *rows1,
-                                                             float *lse0, float *lse1, int K_all, int BH,
-                                                             int N1, int *assign, int *counts)
+                                                                    float *lse0, float *lse1, int K_all, int BH,
+                                                                    int N1, int *assign, int *counts)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -164,8 +181,8 @@ __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L.misc);
     volatile int *stop = reinterpret_cast<volatile int *>(smem + L.misc + 4);
     const int t = threadIdx.x, warp = t >> 5;
-    const int rt = t & (C - 1), half = t >> 7;   // this thread's row of the chunk, and its half of the columns
-    const int ntile = (K_all + KMAX - 1) / KMAX;
+    const int rt = t & (C - 1), half = t >> 7;   // this thread's row of the chunk, and its tile of each pair
+    const int ntile = (K_all + KMAX - 1) / KMAX, npair = (ntile + 1) / 2;
     const int cpn0 = (a.N + C - 1) / C, cpn1 = (N1 + C - 1) / C;   // chunks per slice of each set
     const long long side_chunks = (long long)BH * cpn0;
     if (t == 0) {
@@ -180,6 +197,18 @@ __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a
         *reinterpret_cast<uint4 *>(smem + L.ax + t * 32 + (flip << 4)) = make_uint4(one2, 0, 0, 0);
         *reinterpret_cast<uint4 *>(smem + L.ax + t * 32 + ((flip ^ 1) << 4)) = make_uint4(0, 0, 0, 0);
     }
+    // each CTA takes a contiguous range of the chunk list
+    const int nsets = rows1 ? 2 : 1;
+    const long long total = side_chunks + (nsets > 1 ? (long long)BH * cpn1 : 0ll);
+    const long long per = (total + gridDim.x - 1) / gridDim.x;
+    const long long c_begin = (long long)blockIdx.x * per, c_end = min(total, c_begin + per);
+    const int nloc = c_end > c_begin ? (int)(c_end - c_begin) : 0;
+    const ChunkList cl{rows0, rows1, lse0, lse1, side_chunks, cpn0, cpn1, a.N, N1};
+    uint4 x[DR / 8];   // lower half: this chunk's routing row, loaded during the chunk before
+    if (half == 0 && nloc > 0) {
+        const ChunkInfo ci = cl.at(c_begin);
+        load_x<DR>(ci.X, (long long)ci.bh * ci.n + ci.tok0 + rt, ci.tok0 + rt < ci.n, x);
+    }
     grid_dependency_wait();   // the tables come from the parameter kernel
     fence_proxy_async_smem();
     tc_fence_before();
@@ -188,118 +217,92 @@ __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
     const uint32_t lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    // phases and pending loads of the two buffers, one bit each (ph_tb, pending: thread 0 alone)
-    uint32_t ph_tb = 0, ph_mma = 0, pending = 0;
     const int main_bytes = a.bimg_main_bytes;
-
-    // each CTA takes a contiguous range of the chunk list, so that consecutive chunks mostly share
-    // a head: with two tiles, both table images then stay in shared memory from chunk to chunk
-    const int nsets = rows1 ? 2 : 1;
-    const long long total = side_chunks + (nsets > 1 ? (long long)BH * cpn1 : 0ll);
-    const long long per = (total + gridDim.x - 1) / gridDim.x;
-    const long long c_begin = (long long)blockIdx.x * per, c_end = min(total, c_begin + per);
-    // the chunk list: chunk c's slice, first token, rows per slice, rows and output
-    auto chunk_at = [&](long long c, int &bh, int &tok0, int &n, const bf16 *&X, float *&out) {
-        const int side = c >= side_chunks;
-        const long long cc = side ? c - side_chunks : c;
-        const int cpn = side ? cpn1 : cpn0;
-        bh = (int)(cc / cpn);
-        tok0 = (int)(cc % cpn) * C;
-        n = side ? N1 : a.N;
-        X = side ? rows1 : rows0;
-        out = side ? lse1 : lse0;
-    };
-    int resident_h = -1;   // thread 0: the head whose two table images are in the buffers
-    uint4 x[DR / 8];       // this chunk's routing row, loaded during the chunk before (lower half)
-    if (c_begin < c_end && half == 0) {
-        int bh0, tk0, n0;
-        const bf16 *X0;
-        float *o0;
-        chunk_at(c_begin, bh0, tk0, n0, X0, o0);
-        load_x<DR>(X0, (long long)bh0 * n0 + tk0 + rt, tk0 + rt < n0, x);
+    // thread 0: the pair in the table buffer, and its load
+    int res_h = -1, res_j = -1;
+    bool pend = false;
+    uint32_t ph_tb = 0;
+    if (t == 0 && nloc > 0) {
+        res_h = cl.at(c_begin).bh % a.H;
+        res_j = 0;
+        load_table_pair(smem + L.tab, a.bimg + (size_t)res_h * a.bimg_head, a.bimg_bytes, main_bytes, ntile, 0,
+                        bars + S_TB);
+        pend = true;
     }
-    for (long long c = c_begin; c < c_end; ++c) {
-        int bh, tok0, nrow;
-        const bf16 *X;
-        float *out;
-        chunk_at(c, bh, tok0, nrow, X, out);
-        const int h = bh % a.H;
-        const int row = tok0 + rt;
+    uint32_t ph_mma = 0;
+    for (int lc = 0; lc < nloc; ++lc) {
+        const ChunkInfo ci = cl.at(c_begin + lc);
+        const int bh = ci.bh, nrow = ci.n, h = bh % a.H;
+        const int row = ci.tok0 + rt;
         const bool valid = row < nrow;
-        const uint8_t *img = a.bimg + (size_t)h * a.bimg_head;
-        if (half == 0) build_a<DR>(smem + L.abuf, rt, x);
+        if (half == 0) build_a<DR>(smem + L.abuf, rt, x);   // (the MMAs of the chunk before are done)
         fence_proxy_async_smem();
-        if (c + 1 < c_end && half == 0) {   // the next chunk's row, in flight while this one is computed
-            int bh1, tk1, n1;
-            const bf16 *X1;
-            float *o1;
-            chunk_at(c + 1, bh1, tk1, n1, X1, o1);
-            load_x<DR>(X1, (long long)bh1 * n1 + tk1 + rt, tk1 + rt < n1, x);
-        }
-        if (t == 0 && !(ntile <= 2 && h == resident_h)) {
-            for (int j = 0; j < 2 && j < ntile; ++j) {
-                mbar_arrive_expect_tx(bars + S_TB0 + j, (uint32_t)a.bimg_bytes);
-                bulk_g2s(smem + (j ? L.tb1 : L.tb0), img + (size_t)j * a.bimg_bytes, (uint32_t)a.bimg_bytes,
-                         bars + S_TB0 + j);
-                pending |= 1u << j;
-            }
-            resident_h = ntile <= 2 ? h : -1;
+        if (half == 0 && lc + 1 < nloc) {   // the next chunk's row, in flight while this one is computed
+            const ChunkInfo cn = cl.at(c_begin + lc + 1);
+            load_x<DR>(cn.X, (long long)cn.bh * cn.n + cn.tok0 + rt, cn.tok0 + rt < cn.n, x);
         }
         tc_fence_before();
-        __syncthreads();
+        __syncthreads();   // [x^2, x] built; the logits region read by every row
         tc_fence_after();
-        // thread 0: the logits of tile j, once its table is in
-        auto issue = [&](int j) {
-            const int b = j & 1;
-            if ((pending >> b) & 1u) {   // (with two tiles and the same head as before, nothing was loaded)
-                if (!mbar_wait(bars + S_TB0 + b, (ph_tb >> b) & 1u, a.hdr, 60)) {
-                    *stop = 1;
-                    return;
-                }
-                ph_tb ^= 1u << b;
-                pending &= ~(1u << b);
-            }
-            tc_fence_after();
-            const uint32_t tbuf = sb + (b ? L.tb1 : L.tb0);
-            issue_logits_c<DR>(tmem + 128u * b, sb + L.abuf, tbuf, tbuf + (uint32_t)main_bytes, sb + L.ax, KMAX);
-            mma_commit(bars + S_MMA0 + b);
-        };
-        if (t == 0) issue(0);
         float m = NEG_BIG, s = 0.f, best = NEG_BIG;
         int arg = 0;
-        for (int j = 0; j < ntile; ++j) {
-            const int b = j & 1;
-            const bool ok = !*stop && mbar_wait(bars + S_MMA0 + b, (ph_mma >> b) & 1u, a.hdr, 61);
-            ph_mma ^= 1u << b;
+        bool ok = true;
+        for (int j = 0; j < npair; ++j) {
+            if (t == 0) {   // this pair's logits, once its table is in
+                if (pend) {
+                    if (!mbar_wait(bars + S_TB, ph_tb, a.hdr, 60)) *stop = 1;
+                    ph_tb ^= 1u;
+                    pend = false;
+                }
+                if (!*stop) {
+                    tc_fence_after();
+                    issue_logits_c<DR>(tmem, sb + L.abuf, sb + L.tab, sb + L.tab + 2u * (uint32_t)main_bytes, sb + L.ax,
+                                       2 * KMAX);
+                    mma_commit(bars + S_MMA);
+                }
+            }
+            __syncthreads();   // (thread 0's stop is seen by every thread)
+            ok = !*stop && mbar_wait(bars + S_MMA, ph_mma, a.hdr, 61);
+            ph_mma ^= 1u;
             if (__syncthreads_or(!ok)) break;
             tc_fence_after();
-            if (t == 0) {
-                if (j + 2 < ntile) {   // this buffer's table has been read by the MMA just completed
-                    mbar_arrive_expect_tx(bars + S_TB0 + b, (uint32_t)a.bimg_bytes);
-                    bulk_g2s(smem + (b ? L.tb1 : L.tb0), img + (size_t)(j + 2) * a.bimg_bytes, (uint32_t)a.bimg_bytes,
-                             bars + S_TB0 + b);
-                    pending |= 1u << b;
+            if (t == 0) {   // the next step's pair, while the rows read this one (its MMA is done)
+                const bool last = j + 1 == npair;
+                if (!last || lc + 1 < nloc) {
+                    const int hn = last ? cl.at(c_begin + lc + 1).bh % a.H : h, jn = last ? 0 : j + 1;
+                    if (hn != res_h || jn != res_j) {
+                        load_table_pair(smem + L.tab, a.bimg + (size_t)hn * a.bimg_head, a.bimg_bytes, main_bytes, ntile,
+                                        jn, bars + S_TB);
+                        pend = true;
+                        res_h = hn;
+                        res_j = jn;
+                    }
                 }
-                if (j + 1 < ntile) issue(j + 1);
             }
-            // this half's 64 columns of the tile: their maximum, then the running maximum and sum
-            const int nv = min(64, max(0, min(KMAX, K_all - KMAX * j) - 64 * half));
-            uint32_t ra[32], rb[32];
-            tmem_ld32(lane + 128u * b + 64u * half, ra);   // (every lane loads: warp-collective)
-            tmem_ld32(lane + 128u * b + 64u * half + 32u, rb);
-            tmem_ld_wait();
-            if (nv > 0) {
-                const int col0 = KMAX * j + 64 * half;
-                if (nv == 64)
-                    tile_update<64>(ra, rb, 64, m, s, best, arg, col0, assign != nullptr);
-                else
-                    tile_update<0>(ra, rb, nv, m, s, best, arg, col0, assign != nullptr);
+            // this thread's tile of the pair (128 columns), 64 at a time
+            const int kv = min(KMAX, K_all - KMAX * (2 * j + half));
+            if (kv > 0) {
+                for (int sub = 0; sub < 2; ++sub) {
+                    uint32_t ra[32], rb[32];
+                    const uint32_t col = 128u * half + 64u * sub;
+                    tmem_ld32(lane + col, ra);   // (warp-uniform: every lane loads)
+                    tmem_ld32(lane + col + 32u, rb);
+                    tmem_ld_wait();
+                    const int nv = min(64, max(0, kv - 64 * sub));
+                    if (nv > 0) {
+                        const int col0 = KMAX * (2 * j + half) + 64 * sub;
+                        if (nv == 64)
+                            tile_update<64>(ra, rb, 64, m, s, best, arg, col0, assign != nullptr);
+                        else
+                            tile_update<0>(ra, rb, nv, m, s, best, arg, col0, assign != nullptr);
+                    }
+                }
             }
             tc_fence_before();
-            __syncthreads();   // region b read by every row before the MMA of tile j + 2 writes it
+            __syncthreads();   // the region read by every row before the next MMA writes it
             tc_fence_after();
         }
-        if (*stop) break;
+        if (!ok) break;
         // the upper half hands its row's state to the lower half (read before the lower half
         // reaches the next chunk's first barrier, so one slot per row suffices)
         float4 *xch = reinterpret_cast<float4 *>(smem + L.xch);
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a
             const float4 o = xch[rt];
             const float mm = fmaxf(m, o.x);
             const float ss = s * ex2(m - mm) + o.y * ex2(o.x - mm);
-            out[(long long)bh * nrow + row] = mm + log2f(ss);
+            ci.out[(long long)bh * nrow + row] = mm + log2f(ss);
             if (assign) {   // the larger logit; on a tie the lower component index
                 const int oarg = __float_as_int(o.w);
                 if (o.z > best || (o.z == best && oarg < arg)) arg = oarg;
@@ -318,11 +321,9 @@ __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a
             }
         }
     }
-    // table loads still in flight (only after a stop) complete before shared memory is released;
-    // an MMA that was issued has completed or been waited for by every thread
-    if (t == 0)
-        for (int b = 0; b < 2; ++b)
-            if ((pending >> b) & 1u) mbar_wait(bars + S_TB0 + b, (ph_tb >> b) & 1u, a.hdr, 62);
+    // a table load still in flight (only after a stop, or prefetched past the last chunk: never)
+    // completes before shared memory is released; every MMA issued has been waited for
+    if (t == 0 && pend) mbar_wait(bars + S_TB, ph_tb, a.hdr, 62);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = smem_u32(smem);
-    const int main_bytes = a.bimg_main_bytes, blk = 128 * 128;   // (one tile's 64-column block: 16 KB)
+    const int main_bytes = a.bimg_main_bytes;
 
     if (warp == 8) {
         // ============================================================ control warp: MMAs, table
@@ -398,16 +399,8 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
                 if (lc > 0 && !mbar_wait_abortable(bars + L_FULL0 + ((lc - 1) & 1), (uint32_t)(((lc - 1) >> 1) & 1),
                                                    a.hdr, 63, stop))
                     return false;
-                const uint8_t *img = a.bimg + (size_t)h * a.bimg_head;
-                mbar_arrive_expect_tx(bars + L_TB, 2u * (uint32_t)a.bimg_bytes);
-                for (int t2 = 0; t2 < 2; ++t2) {
-                    const uint8_t *src = img + (size_t)t2 * a.bimg_bytes;
-                    for (int q = 0; q < main_bytes / blk; ++q)
-                        bulk_g2s(smem + L.tab + (uint32_t)(q * 2 * blk + t2 * blk), src + (size_t)q * blk, (uint32_t)blk,
-                                 bars + L_TB);
-                    bulk_g2s(smem + L.tab + (uint32_t)(2 * main_bytes + t2 * 128 * 32), src + main_bytes, 128u * 32u,
-                             bars + L_TB);
-                }
+                load_table_pair(smem + L.tab, a.bimg + (size_t)h * a.bimg_head, a.bimg_bytes, main_bytes, 2, 0,
+                                bars + L_TB);
                 pend = true;
                 res_h = h;
                 return true;
