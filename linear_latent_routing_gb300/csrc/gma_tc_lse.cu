@@ -144,6 +144,14 @@ struct ChunkList {
     }
 };
 
+// Row rt of chunk c's routing rows into x (zeros past the end of its slice).
+template <int DR>
+__device__ __forceinline__ void fetch_row(const ChunkList &cl, long long c, int rt, uint4 (&x)[DR / 8])
+{
+    const ChunkInfo ci = cl.at(c);
+    load_x<DR>(ci.X, (long long)ci.bh * ci.n + ci.tok0 + rt, ci.tok0 + rt < ci.n, x);
+}
+
 // Tiles 2 j and 2 j + 1 (the second if there is one) of a head's table images (img) into tab as one
 // N = 256 operand: each 64-column block of the [x^2, x] part holds the first tile's 128 rows, then
 // the second's; the constant part holds both tiles' rows in order.  One thread; the bytes complete
@@ -205,10 +213,7 @@ __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a
     const int nloc = c_end > c_begin ? (int)(c_end - c_begin) : 0;
     const ChunkList cl{rows0, rows1, lse0, lse1, side_chunks, cpn0, cpn1, a.N, N1};
     uint4 x[DR / 8];   // lower half: this chunk's routing row, loaded during the chunk before
-    if (half == 0 && nloc > 0) {
-        const ChunkInfo ci = cl.at(c_begin);
-        load_x<DR>(ci.X, (long long)ci.bh * ci.n + ci.tok0 + rt, ci.tok0 + rt < ci.n, x);
-    }
+    if (half == 0 && nloc > 0) fetch_row<DR>(cl, c_begin, rt, x);
     grid_dependency_wait();   // the tables come from the parameter kernel
     fence_proxy_async_smem();
     tc_fence_before();
@@ -237,10 +242,8 @@ __global__ void __launch_bounds__(STHREADS, 2) tc_lse_stream_kernel(const Args a
         const bool valid = row < nrow;
         if (half == 0) build_a<DR>(smem + L.abuf, rt, x);   // (the MMAs of the chunk before are done)
         fence_proxy_async_smem();
-        if (half == 0 && lc + 1 < nloc) {   // the next chunk's row, in flight while this one is computed
-            const ChunkInfo cn = cl.at(c_begin + lc + 1);
-            load_x<DR>(cn.X, (long long)cn.bh * cn.n + cn.tok0 + rt, cn.tok0 + rt < cn.n, x);
-        }
+        if (half == 0 && lc + 1 < nloc)   // the next chunk's row, in flight while this one is computed
+            fetch_row<DR>(cl, c_begin + lc + 1, rt, x);
         tc_fence_before();
         __syncthreads();   // [x^2, x] built; the logits region read by every row
         tc_fence_after();
@@ -369,12 +372,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
     const int nloc = c_end > c_begin ? (int)(c_end - c_begin) : 0;
     const ChunkList cl{rows0, rows1, lse0, lse1, side_chunks, cpn0, cpn1, a.N, N1};
     uint4 x[DR / 8];   // lower half: the row of the chunk whose [x^2, x] tile is built next
-#define LSE_FETCH_ROW(lc)                                                                                        \
-    do {                                                                                                         \
-        const ChunkInfo ci_ = cl.at(c_begin + (lc));                                                            \
-        load_x<DR>(ci_.X, (long long)ci_.bh * ci_.n + ci_.tok0 + rt, ci_.tok0 + rt < ci_.n, x);                  \
-    } while (0)
-    if (warp < 4 && nloc > 0) LSE_FETCH_ROW(0);   // (the rows are inputs: no kernel before writes them)
+    if (warp < 4 && nloc > 0) fetch_row<DR>(cl, c_begin, rt, x);   // (the rows are inputs: no kernel before writes them)
     grid_dependency_wait();   // the tables come from the parameter kernel
     fence_proxy_async_smem();
     tc_fence_before();
@@ -441,7 +439,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
             fence_proxy_async_smem();
             __syncwarp();
             if (lid == 0) mbar_arrive(bars + L_A0);
-            if (nloc > 1) LSE_FETCH_ROW(1);
+            if (nloc > 1) fetch_row<DR>(cl, c_begin + 1, rt, x);
         }
         for (int lc = 0; ok && lc < nloc; ++lc) {
             const ChunkInfo ci = cl.at(c_begin + lc);
@@ -458,7 +456,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lid == 0) mbar_arrive(bars + L_A0 + ((lc + 1) & 1));
-                if (lc + 2 < nloc) LSE_FETCH_ROW(lc + 2);
+                if (lc + 2 < nloc) fetch_row<DR>(cl, c_begin + lc + 2, rt, x);
             }
             float m = NEG_BIG, s = 0.f, best = NEG_BIG;
             int arg = 0;
@@ -519,7 +517,6 @@ __global__ void __launch_bounds__(RTHREADS, 1) tc_lse_resident_kernel(const Args
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
-#undef LSE_FETCH_ROW
 }
 
 
